@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""KDA on GB300: prefill tokens/s (chunked, BF16, B=1 H=8 T=4096 d=128) and
+decode tokens/s (256 sequences x 56 heads, 64 single-token steps), with the
+roofline fraction of the dominant kernel.
+
+One step = one whole prefill of the workload through the library's three
+stages (transfer pass over segments 0..S-2, the segment scan, the output pass
+over all segments; a single output pass when the library picks S = 1), each
+bracketed by CUDA events on the launching stream.  Inputs are resident in HBM;
+the 50 MB working set is smaller than L2, so a 512 MB buffer is rewritten
+between timed steps (outside the events).  ``e2e`` times the one-call C entry
+point with pinned host buffers, including the copies in and out.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PREFILL = "kda_prefill_bf16_h8_t4096_d128"
+DECODE = "kda_decode_b256_h56_d128_x64"
+METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of roofline"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (weak scaling: each rank owns a full batch)
+# ---------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value, dist, device=None):
+    """Max of a float over ranks (the slowest rank sets the job's time)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [s for s in vis.split(",") if s.strip()]
+        self.index = ids[local_rank] if local_rank < len(ids) and ids[local_rank].isdigit() \
+            else str(local_rank)
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.index, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax.append(float(f[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, f[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if sm:
+            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                   "reasons": sorted(reasons), "samples": len(sm)}
+        return out
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the method must move, per launch)
+# ---------------------------------------------------------------------------
+def prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes, seg_tokens):
+    """Bytes each stage must read and write at minimum.
+
+    output pass : q, k, v, out (activation dtype) + g (fp32) + beta (fp32) per
+                  head-token, plus the start states read and final states written.
+    transfer    : k, v, g, beta for segments 0..S-2, plus A and B written.
+    scan        : A, B read for S-1 segments, start states written.
+    """
+    per_ht = (2 * dk + 2 * dv) * act_bytes + 4 * dk + 4
+    out_pass = T * H * per_ht + N * H * Sg * dk * dv * 4 + N * H * dk * dv * 4
+    if Sg == 1:
+        return {"output_pass": out_pass}
+    tr_tokens = seg_tokens
+    transfer = tr_tokens * H * ((dk + dv) * act_bytes + 4 * dk + 4) + \
+        N * H * (Sg - 1) * (dk * dk + dk * dv) * 4
+    scan = N * H * (Sg - 1) * (dk * dk + dk * dv) * 4 + N * H * Sg * dk * dv * 4
+    return {"transfer_pass": transfer, "segment_scan": scan, "output_pass": out_pass}
+
+
+def transfer_tokens(lengths, Sg, chunk=16):
+    """Tokens in segments 0..S-2 (the ones the transfer pass reads), with the
+    library's split: segment s of a sequence of c chunks takes chunks
+    [floor(s c / S), floor((s+1) c / S))."""
+    if Sg <= 1:
+        return 0
+    total = 0
+    for L in lengths:
+        c = -(-L // chunk)
+        total += min(L, ((Sg - 1) * c // Sg) * chunk)
+    return total
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import kimi_delta_attention_18_gb300 as kda
+    from kimi_delta_attention_18_gb300.inputs import WORKLOADS, make_decode_inputs, \
+        make_prefill_inputs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    kda.lib()  # fail loudly now if the library is missing
+
+    w = WORKLOADS[PREFILL]
+    x = make_prefill_inputs(w["lengths"], w["H"], w["dk"], w["dv"], w["act"], seed=rank,
+                            device=dev)
+    T, H, dk = x["q"].shape
+    dv = x["v"].shape[2]
+    N = len(w["lengths"])
+    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"])
+    Sg = kda.prefill_num_segments(desc)
+    act_bytes = x["q"].element_size()
+    out = torch.empty_like(x["v"])
+    S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    A = torch.empty((N, H, Sg, dk, dk), dtype=torch.float32, device=dev)
+    B = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
+    starts = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev):
+        # exactly the launches kda_prefill_chunked makes, with events between them
+        ev[0].record(stream)
+        if Sg > 1:
+            kda.state_transfer(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], Sg,
+                               seg_begin=0, seg_end=Sg - 1, transfer=A, zero_init_state=B)
+        ev[1].record(stream)
+        if Sg > 1:
+            kda.state_compose(A.view(N * H, Sg, dk, dk), B.view(N * H, Sg, dk, dv), None,
+                              seg_init_states=starts.view(N * H, Sg, dk, dv),
+                              want_final_state=False)
+        ev[2].record(stream)
+        kda.prefill_segments(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                             starts if Sg > 1 else None, x["cu_seqlens"], Sg, out=out,
+                             S_final=S_final)
+        ev[3].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step(mk())
+    torch.cuda.synchronize()
+    events = [mk() for _ in range(args.steps)]
+    clocks = Clocks(local)
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        step(events[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(dist)
+    clk = clocks.stop()
+
+    stage_ms = {"transfer_pass": [], "segment_scan": [], "output_pass": []}
+    total_ms = []
+    for ev in events:
+        stage_ms["transfer_pass"].append(ev[0].elapsed_time(ev[1]))
+        stage_ms["segment_scan"].append(ev[1].elapsed_time(ev[2]))
+        stage_ms["output_pass"].append(ev[2].elapsed_time(ev[3]))
+        total_ms.append(ev[0].elapsed_time(ev[3]))
+    dev_ms = sum(total_ms)
+    dev_ms_max = max_over_ranks(dev_ms, dist, dev)
+    tokens = T * args.steps * world
+    value = tokens / (dev_ms_max / 1e3)
+
+    # roofline of the dominant kernel (HBM-bound: see the design notes)
+    peaks = measured_peaks()
+    seg_tokens = transfer_tokens(w["lengths"], Sg)
+    sbytes = prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes, seg_tokens)
+    means = {k_: statistics.mean(v_) for k_, v_ in stage_ms.items() if k_ in sbytes}
+    dom = max(means, key=means.get)
+    achieved = sbytes[dom] / (means[dom] / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": None, "peak_source": peaks["source"] + " (burst copy)",
+                "stage_ms": {k_: round(v_, 4) for k_, v_ in means.items()},
+                "stage_bytes": sbytes}
+    launches_per_step = 3 if Sg > 1 else 1
+
+    result = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+              "ms_per_step": round(dev_ms_max / args.steps, 5), "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+              "config": {"workload": PREFILL, "batch": N, "seq_len": T, "heads": H, "dk": dk,
+                         "dv": dv, "chunk": 16, "segments": Sg, "state": "fp32",
+                         "l2": "512 MB buffer rewritten between timed steps (working set 50 MB)",
+                         "parallelism": "dp%d (one batch per GPU)" % world},
+              "wall_s_timed_loop": round(wall, 4), "clocks": clk, "roofline": roofline,
+              "gpu_launches": launches_per_step * args.steps}
+
+    # e2e: one-call C entry point with pinned host buffers, copies included
+    result["e2e"] = run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world)
+    if not args.no_decode:
+        result["decode"] = run_decode(args, kda, make_decode_inputs, WORKLOADS[DECODE], dev,
+                                      dist, world, peaks, rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(x, N, H)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world):
+    import torch
+    host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    dbuf = {n: torch.empty_like(x[n]) for n in host}
+    out_h = torch.empty((T, H, dv), dtype=x["q"].dtype).pin_memory()
+    sf_h = torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(x["v"])
+    sf_d = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"])
+    ws = torch.empty(max(1, kda.prefill_workspace_size(desc)), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + sf_h.numel() * sf_h.element_size()
+
+    def one():
+        for n in host:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        kda.prefill_chunked(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], None,
+                            x["cu_seqlens"], out=out_d, S_final=sf_d, workspace=ws)
+        out_h.copy_(out_d, non_blocking=True)
+        sf_h.copy_(sf_d, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.e2e_steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    return {"value": round(T * args.e2e_steps * world / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / args.e2e_steps, 4)}
+
+
+def run_decode(args, kda, make_decode_inputs, w, dev, dist, world, peaks, rank):
+    import torch
+    steps = w["steps"]
+    x = make_decode_inputs(w["batch"], w["H"], w["dk"], w["dv"], steps, w["act"],
+                           s0_std=w["s0_std"], seed=rank, device=dev)
+    S = x["S0"].clone()
+    out = torch.empty((w["batch"], w["H"], w["dv"]), dtype=x["q"].dtype, device=dev)
+    for t in range(3):
+        kda.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], S, out=out)
+    S.copy_(x["S0"])
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    barrier(dist)
+    clocks = Clocks(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    ev[0].record()
+    for t in range(steps):
+        kda.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], S, out=out)
+        ev[t + 1].record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    per = [ev[t].elapsed_time(ev[t + 1]) for t in range(steps)]
+    total = max_over_ranks(sum(per), dist, dev)
+    units = w["batch"] * w["H"]
+    act_b = x["q"].element_size()
+    bytes_per_launch = units * (2 * w["dk"] * w["dv"] * 4 + (2 * w["dk"] + 2 * w["dv"]) * act_b +
+                                4 * w["dk"] + 4)
+    achieved = bytes_per_launch / (statistics.mean(per) / 1e3) / 1e9
+    return {"value": round(w["batch"] * steps * world / (total / 1e3), 1), "unit": "tokens/s",
+            "workload": "kda_decode_b256_h56_d128_x64", "steps": steps,
+            "ms_per_step": round(total / steps, 5), "gpu_launches": steps,
+            "clocks": clk,
+            "roofline": {"bound": "hbm", "kernel": "decode_step", "achieved": round(achieved, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "bytes_per_launch": bytes_per_launch, "traffic": None,
+                         "peak_source": peaks["source"] + " (burst copy)"}}
+
+
+def cpu_baseline(x, N, H, target_s=8.0):
+    """The fp64 oracle as it stands, on the host cores, over a bounded sample of the
+    same workload (the first heads of the batch, whole sequence)."""
+    import oracle
+    f = lambda t: t.detach().float().cpu().double().numpy()
+    q, k, v, g, b = (f(x[n]) for n in ("q", "k", "v", "g", "beta"))
+    cu = x["cu_seqlens"].cpu().numpy()
+    threads = oracle.host_threads()
+    t0 = time.perf_counter()
+    oracle.kda_forward(q[:, :1], k[:, :1], v[:, :1], g[:, :1], b[:, :1], None, cu,
+                       threads=threads)
+    one = time.perf_counter() - t0
+    heads = max(1, min(H, int(target_s / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    oracle.kda_forward(q[:, :heads], k[:, :heads], v[:, :heads], g[:, :heads], b[:, :heads],
+                       None, cu, threads=threads)
+    dt = time.perf_counter() - t0
+    T = q.shape[0]
+    return {"value": round(T * heads / H / dt, 2), "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d of %d heads x %d tokens (fp64 token-by-token C oracle, %.2f s)" %
+                      (heads, H, T, dt)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores, same workload and metric
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from kimi_delta_attention_18_gb300.inputs import WORKLOADS, make_prefill_inputs
+    w = WORKLOADS[PREFILL]
+    x = make_prefill_inputs(w["lengths"], w["H"], w["dk"], w["dv"], w["act"], seed=0)
+    f = lambda t: t.detach().float().double().numpy()
+    q, k, v, g, b = (f(x[n]) for n in ("q", "k", "v", "g", "beta"))
+    T, H = q.shape[:2]
+    threads = oracle.host_threads()
+    # size each step (a token prefix of one head) so the whole run stays within ~2 min
+    t0 = time.perf_counter()
+    oracle.kda_forward(q[:512, :1], k[:512, :1], v[:512, :1], g[:512, :1], b[:512, :1],
+                       threads=threads)
+    per_tok = (time.perf_counter() - t0) / 512
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    Ts = int(max(64, min(T, budget / max(per_tok, 1e-9))))
+    sl = lambda a: np.ascontiguousarray(a[:Ts, :1])
+    qs, ks, vs, gs, bs = map(sl, (q, k, v, g, b))
+    for _ in range(args.warmup):
+        oracle.kda_forward(qs, ks, vs, gs, bs, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.kda_forward(qs, ks, vs, gs, bs, threads=threads)
+    dt = time.perf_counter() - t0
+    value = Ts * args.steps / H / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL, "batch": 1, "seq_len": T, "heads": H, "dk": 128,
+                   "dv": 128, "chunk": 16},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "1 of %d heads x %d tokens per step (fp64 C oracle)" % (H, Ts)},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

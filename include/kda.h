@@ -1,0 +1,193 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library, libkda.so.
+ *
+ * The operation.  Per (sequence, head) the library keeps a fixed-size state
+ * S in R^{dk x dv} (fp32) and applies, for every token t, in this order
+ * ("Kimi K3 Architecture Explained", section 3 "Kimi Delta Attention": decay
+ * stale context first, then erase conflicting memory, then write):
+ *
+ *     S <- Diag(exp(g_t)) S               decay, per key channel
+ *     S <- S - beta_t k_t (k_t^T S)        erase
+ *     S <- S + beta_t k_t v_t^T            write
+ *     o_t = S^T q_t                        read, after the update
+ *
+ * g is the caller's log-decay, normally g = -5 sigmoid(x) so that g lies in
+ * (-5, 0) (Kimi K3 technical-report digest, section 2.1 (1): bounded scaled
+ * sigmoid, g_min = -5).  There is no positional input and no 1/sqrt(d) scale.
+ *
+ * Layouts (all row-major, innermost index last, no padding):
+ *   q, k : [T_tot, H, dk]   activation dtype (fp32 or bf16)
+ *   v    : [T_tot, H, dv]   activation dtype
+ *   out  : [T_tot, H, dv]   activation dtype
+ *   g    : [T_tot, H, dk]   fp32
+ *   beta : [T_tot, H]       fp32
+ *   states (S0, S_final, S_inout, zero-initial states) : [.., dk, dv] fp32
+ *   transfer matrices : [.., dk, dk] fp32
+ * Sequences are packed along T_tot and delimited by cu_seqlens (device int32
+ * [N+1], cu[0] = 0, non-decreasing, cu[N] = T_tot).
+ *
+ * Ownership and execution.  Every pointer except the descriptor is a DEVICE
+ * pointer owned by the caller.  The library allocates no memory, never
+ * synchronises the host, and launches only on the given stream (a
+ * cudaStream_t passed as void*, NULL = the legacy default stream).  Results
+ * are ready when that stream reaches them.  Outputs must not alias inputs,
+ * except that S_final may equal S0.
+ *
+ * Errors.  Argument checks that the host can make return a status at once and
+ * launch nothing.  Problems only the device can see (a malformed cu_seqlens, a
+ * bounded wait that ran out) are written to *dev_status (device int32, may be
+ * NULL; the first error sticks, 0 means no error) and the affected work is
+ * skipped.  A failed launch returns KDA_ERR_CUDA.  Nothing aborts or throws.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, bad cu_seqlens */
+    KDA_ERR_UNSUPPORTED = 2, /* shape or dtype outside what the kernels cover      */
+    KDA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required         */
+    KDA_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed               */
+    KDA_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (dev_status)    */
+} kda_status_t;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype_t;
+
+/* Problem description for the chunked prefill and the transfer pass. */
+typedef struct {
+    int32_t num_seqs;     /* N >= 0                                               */
+    int32_t total_tokens; /* T_tot >= 0, equal to cu_seqlens[N]                   */
+    int32_t num_heads;    /* H >= 1                                               */
+    int32_t dk;           /* key / query width, 1..128                            */
+    int32_t dv;           /* value width, 1..128                                  */
+    int32_t act_dtype;    /* kda_dtype_t of q, k, v and out                       */
+    int32_t chunk;        /* must be 16: the 16-token block of the digest, 2.1 (1) */
+    int32_t num_segments; /* 0 = choose, 1 = one pass per (seq, head), S > 1 =     */
+                          /* split every sequence into S chunk-aligned segments    */
+                          /* joined by the transfer-matrix scan (digest 2.4 (1))   */
+} kda_prefill_desc_t;
+
+/*
+ * Number of segments kda_prefill_chunked will use for desc (resolves
+ * num_segments = 0 from the problem size and the current device's SM count).
+ * Returns 0 for an invalid descriptor.
+ */
+int32_t kda_prefill_num_segments(const kda_prefill_desc_t *desc);
+
+/*
+ * Device workspace, in bytes, that kda_prefill_chunked needs for desc: zero
+ * when it runs one pass, else room for N*H*S transfer matrices, zero-initial
+ * states and segment start states (fp32).  Call with the same desc, on the
+ * same device, as the prefill itself.
+ */
+size_t kda_prefill_workspace_size(const kda_prefill_desc_t *desc);
+
+/*
+ * Chunked prefill (the hot path): for every packed sequence and head, run the
+ * recurrence above over its tokens starting from S0 (NULL = zeros), write o_t
+ * for every token to out and, if S_final != NULL, the state after the last
+ * token.  Chunked form: 16-token blocks, each turned into a WY/UT-transform
+ * representation of its product of (I - beta k k^T) Diag(alpha) factors
+ * ("intra-chunk parallel work"), then a sequential fp32 state step per block
+ * ("cross-chunk state propagation"), overlapped as in the digest, section
+ * 2.4 (1), FlashKDA.  With S > 1 segments every sequence is also split for
+ * parallelism: per segment a transfer matrix and a zero-initial state are
+ * computed, scanned, and the segments then run from their true start states
+ * (digest 2.4 (1), KCP).  A zero-length sequence gives S_final = S0.
+ *
+ *   desc            problem description (host pointer).
+ *   q, k, v, g, beta, out   device arrays in the layouts above; 16-byte aligned.
+ *   S0              [N, H, dk, dv] fp32 or NULL.
+ *   cu_seqlens      [N+1] int32 (device).
+ *   S_final         [N, H, dk, dv] fp32 or NULL; may equal S0.
+ *   workspace       device buffer of workspace_bytes >= kda_prefill_workspace_size
+ *                   (may be NULL when that is 0).  Contents on entry don't matter.
+ *   dev_status      device int32 or NULL (see Errors).
+ *   stream          cudaStream_t.
+ */
+kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, const void *k,
+                                 const void *v, const float *g, const float *beta,
+                                 const float *S0, const int32_t *cu_seqlens, void *out,
+                                 float *S_final, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream);
+
+/*
+ * One decode step for `batch` independent sequences (one new token each): the
+ * recurrence above applied once, in place on S_inout [batch, H, dk, dv] fp32,
+ * with q, k [batch, H, dk], v, out [batch, H, dv] in act_dtype, g [batch, H,
+ * dk] and beta [batch, H] fp32.  Streams each state through once.  dv must be
+ * a multiple of 4 and every pointer 16-byte aligned.
+ */
+kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv,
+                             int32_t act_dtype, const void *q, const void *k, const void *v,
+                             const float *g, const float *beta, float *S_inout, void *out,
+                             void *stream);
+
+/*
+ * Transfer pass of the context-parallel split (digest, section 2.4 (1)): with
+ * S = desc->num_segments >= 1, split every sequence into S chunk-aligned
+ * segments (sequence n has c = ceil(len_n / 16) chunks; segment s takes chunks
+ * [floor(s c / S), floor((s+1) c / S))) and compute for each (n, h, s)
+ *     transfer        [N, H, S, dk, dk]  the matrix A with S_end = A S_start + B
+ *     zero_init_state [N, H, S, dk, dv]  B, the state the segment reaches from 0.
+ * Only segments s in [seg_begin, seg_end) are computed (0 <= seg_begin <=
+ * seg_end <= S); the other slots are left untouched, so ranks or passes can
+ * split the segments between them.  An empty segment gives A = I, B = 0.
+ * q is not needed.
+ */
+kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begin,
+                                int32_t seg_end, const void *k, const void *v, const float *g,
+                                const float *beta, const int32_t *cu_seqlens, float *transfer,
+                                float *zero_init_state, int32_t *dev_status, void *stream);
+
+/*
+ * Prefix scan that joins the segments (digest, section 2.4 (1)): for each of
+ * `units` independent chains of `segments` (A_s, B_s) pairs,
+ *     start_0 = S0 (NULL = zeros),  start_s = A_{s-1} start_{s-1} + B_{s-1},
+ * written to seg_init_states [units, segments, dk, dv] (may be NULL), and
+ * S_final [units, dk, dv] = A_{S-1} start_{S-1} + B_{S-1} (may be NULL; when it
+ * is NULL the last pair is never read, so it need not have been computed).
+ * transfer is [units, segments, dk, dk], zero_init_state [units, segments, dk,
+ * dv]; all fp32, 16-byte aligned.  The scan is sequential over segments and
+ * parallel over units and column blocks, in fp32.
+ */
+kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int32_t dv,
+                               const float *transfer, const float *zero_init_state,
+                               const float *S0, float *seg_init_states, float *S_final,
+                               void *stream);
+
+/*
+ * Output pass of the context-parallel split: with S = desc->num_segments >= 1
+ * (segments as in kda_state_transfer), run segments [seg_begin, seg_end) of
+ * every (sequence, head) from their given start states seg_init_states [N, H,
+ * S, dk, dv] (as written by kda_state_compose; NULL = zeros), write o_t for
+ * those segments' tokens to out and, if S_final != NULL and seg_end == S, the
+ * state after the last segment.  kda_prefill_chunked with S > 1 is exactly
+ * kda_state_transfer on segments [0, S-1), kda_state_compose with S_final =
+ * NULL, then this call on [0, S); with S = 1 and seg_init_states = S0 it is the
+ * one-pass prefill.  Arguments otherwise as for kda_prefill_chunked.
+ */
+kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_begin,
+                                  int32_t seg_end, const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta,
+                                  const float *seg_init_states, const int32_t *cu_seqlens,
+                                  void *out, float *S_final, int32_t *dev_status, void *stream);
+
+/* Human-readable name of a status. Never NULL. */
+const char *kda_status_string(kda_status_t status);
+
+/* Build description (target architecture, library version). Never NULL. */
+const char *kda_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

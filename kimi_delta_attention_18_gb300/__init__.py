@@ -1,0 +1,25 @@
+"""Kimi Delta Attention (KDA) on GB300 (sm_103a).
+
+The compute lives in ``libkda.so`` (hand-written CUDA kernels behind the C ABI
+declared in ``include/kda.h``); this package is its thin Python binding.  The
+library is built in-tree by ``kimi_delta_attention_18_gb300.build`` and loaded
+on first use; if it cannot be built or loaded, every call raises.
+"""
+from ._native import (  # noqa: F401
+    KDAError,
+    PrefillDesc,
+    decode_step,
+    lib,
+    library_path,
+    prefill_chunked,
+    prefill_desc,
+    prefill_num_segments,
+    prefill_segments,
+    prefill_workspace_size,
+    state_compose,
+    state_transfer,
+)
+
+__all__ = ["KDAError", "PrefillDesc", "decode_step", "lib", "library_path", "prefill_chunked",
+           "prefill_desc", "prefill_num_segments", "prefill_segments", "prefill_workspace_size", "state_compose",
+           "state_transfer"]

@@ -1,0 +1,289 @@
+"""ctypes binding to libkda.so: argument marshalling only.
+
+Every function takes torch CUDA tensors, checks their dtype / shape / layout,
+allocates the outputs the caller did not pass (with torch, on the tensors'
+device), and calls the C entry point of the same name on the current CUDA
+stream.  All arithmetic runs in the library's kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import build as _build
+
+_lib = None
+_lock = threading.Lock()
+
+
+class KDAError(RuntimeError):
+    """A libkda entry point returned a non-zero kda_status_t."""
+
+    def __init__(self, fn, status, msg):
+        super().__init__("%s failed: %s (status %d)" % (fn, msg, status))
+        self.status = status
+
+
+class PrefillDesc(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("act_dtype", ctypes.c_int32), ("chunk", ctypes.c_int32),
+                ("num_segments", ctypes.c_int32)]
+
+
+F32, BF16 = 0, 1
+_ACT = {torch.float32: F32, torch.bfloat16: BF16}
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+
+
+def lib():
+    """Load (building first if needed) the in-tree libkda.so.  Raises if it cannot."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            L.kda_prefill_num_segments.restype = _I
+            L.kda_prefill_num_segments.argtypes = [ctypes.POINTER(PrefillDesc)]
+            L.kda_prefill_workspace_size.restype = ctypes.c_size_t
+            L.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillDesc)]
+            L.kda_prefill_chunked.restype = ctypes.c_int
+            L.kda_prefill_chunked.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 10 + \
+                [ctypes.c_size_t, _P, _P]
+            L.kda_prefill_segments.restype = ctypes.c_int
+            L.kda_prefill_segments.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 11
+            L.kda_decode_step.restype = ctypes.c_int
+            L.kda_decode_step.argtypes = [_I] * 5 + [_P] * 8
+            L.kda_state_transfer.restype = ctypes.c_int
+            L.kda_state_transfer.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 9
+            L.kda_state_compose.restype = ctypes.c_int
+            L.kda_state_compose.argtypes = [_I] * 4 + [_P] * 6
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_status_string.argtypes = [ctypes.c_int]
+            L.kda_build_info.restype = ctypes.c_char_p
+            L.kda_build_info.argtypes = []
+            _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise KDAError(fn, rc, lib().kda_status_string(rc).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype=None, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t
+
+
+def _desc(N, T, H, dk, dv, act, num_segments):
+    return PrefillDesc(N, T, H, dk, dv, act, 16, int(num_segments))
+
+
+def prefill_desc(q_or_k, v, cu_seqlens, num_segments=0):
+    T, H, dk = q_or_k.shape
+    return _desc(cu_seqlens.numel() - 1, T, H, dk, v.shape[2], _ACT[q_or_k.dtype], num_segments)
+
+
+def prefill_num_segments(desc) -> int:
+    return int(lib().kda_prefill_num_segments(ctypes.byref(desc)))
+
+
+def prefill_workspace_size(desc) -> int:
+    return int(lib().kda_prefill_workspace_size(ctypes.byref(desc)))
+
+
+def prefill_chunked(q, k, v, g, beta, S0=None, cu_seqlens=None, *, num_segments=0, out=None,
+                    S_final=None, want_final_state=True, workspace=None, dev_status=None,
+                    stream=None):
+    """Chunked KDA prefill over packed sequences (see kda_prefill_chunked in kda.h).
+
+    q, k ``[T, H, dk]`` and v ``[T, H, dv]`` (fp32 or bf16, same dtype); g ``[T, H,
+    dk]`` and beta ``[T, H]`` fp32; S0 ``[N, H, dk, dv]`` fp32 or None;
+    cu_seqlens int32 ``[N+1]`` (None = one sequence).  Returns ``(out, S_final)``.
+    """
+    dev = q.device
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    act = _ACT.get(q.dtype)
+    if act is None:
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, "q", q.dtype, (T, H, dk))
+    _need(k, "k", q.dtype, (T, H, dk), dev)
+    _need(v, "v", q.dtype, (T, H, dv), dev)
+    _need(g, "g", torch.float32, (T, H, dk), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+    N = cu_seqlens.numel() - 1
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _need(out, "out", q.dtype, (T, H, dv), dev)
+    if S_final is None and want_final_state:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if S_final is not None:
+        _need(S_final, "S_final", torch.float32, (N, H, dk, dv), dev)
+    desc = _desc(N, T, H, dk, dv, act, num_segments)
+    ws_bytes = prefill_workspace_size(desc)
+    if ws_bytes > 0 and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, None, dev)
+    rc = lib().kda_prefill_chunked(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(out),
+                                   _ptr(S_final), _ptr(workspace), ws_len, _ptr(dev_status),
+                                   _stream(stream, dev))
+    _check("kda_prefill_chunked", rc)
+    return out, S_final
+
+
+def prefill_segments(q, k, v, g, beta, seg_init_states, cu_seqlens, num_segments, *, seg_begin=0,
+                     seg_end=None, out=None, S_final=None, want_final_state=True,
+                     dev_status=None, stream=None):
+    """Run segments [seg_begin, seg_end) from their given start states (see
+    kda_prefill_segments in kda.h).  seg_init_states ``[N, H, S, dk, dv]`` fp32
+    (None = zeros for every segment).  Returns ``(out, S_final)``."""
+    dev = q.device
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    act = _ACT.get(q.dtype)
+    if act is None:
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, "q", q.dtype, (T, H, dk))
+    _need(k, "k", q.dtype, (T, H, dk), dev)
+    _need(v, "v", q.dtype, (T, H, dv), dev)
+    _need(g, "g", torch.float32, (T, H, dk), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+    N = cu_seqlens.numel() - 1
+    Sg = int(num_segments)
+    if seg_init_states is not None:
+        _need(seg_init_states, "seg_init_states", torch.float32, (N, H, Sg, dk, dv), dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _need(out, "out", q.dtype, (T, H, dv), dev)
+    if S_final is None and want_final_state:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if S_final is not None:
+        _need(S_final, "S_final", torch.float32, (N, H, dk, dv), dev)
+    desc = _desc(N, T, H, dk, dv, act, Sg)
+    seg_end = Sg if seg_end is None else int(seg_end)
+    rc = lib().kda_prefill_segments(ctypes.byref(desc), int(seg_begin), seg_end, _ptr(q), _ptr(k),
+                                    _ptr(v), _ptr(g),
+                                    _ptr(beta), _ptr(seg_init_states), _ptr(cu_seqlens),
+                                    _ptr(out), _ptr(S_final), _ptr(dev_status),
+                                    _stream(stream, dev))
+    _check("kda_prefill_segments", rc)
+    return out, S_final
+
+
+def decode_step(q, k, v, g, beta, S, *, out=None, stream=None):
+    """One decode token per sequence; updates S ``[B, H, dk, dv]`` in place and
+    returns out ``[B, H, dv]`` (see kda_decode_step in kda.h)."""
+    dev = S.device
+    B, H, dk, dv = S.shape
+    act = _ACT.get(q.dtype)
+    if act is None:
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, "q", q.dtype, (B, H, dk), dev)
+    _need(k, "k", q.dtype, (B, H, dk), dev)
+    _need(v, "v", q.dtype, (B, H, dv), dev)
+    _need(g, "g", torch.float32, (B, H, dk), dev)
+    _need(beta, "beta", torch.float32, (B, H), dev)
+    _need(S, "S", torch.float32, (B, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
+    _need(out, "out", q.dtype, (B, H, dv), dev)
+    rc = lib().kda_decode_step(B, H, dk, dv, act, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               _ptr(S), _ptr(out), _stream(stream, dev))
+    _check("kda_decode_step", rc)
+    return out
+
+
+def state_transfer(k, v, g, beta, cu_seqlens, num_segments, *, seg_begin=0, seg_end=None,
+                   transfer=None, zero_init_state=None, dev_status=None, stream=None):
+    """Per (sequence, head, segment) transfer matrix and zero-initial state for
+    segments [seg_begin, seg_end) (see kda_state_transfer in kda.h).  Returns
+    ``(A [N,H,S,dk,dk], B [N,H,S,dk,dv])``; other segments' slots are untouched."""
+    dev = k.device
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    act = _ACT.get(k.dtype)
+    if act is None:
+        raise ValueError("k must be float32 or bfloat16")
+    _need(k, "k", k.dtype, (T, H, dk))
+    _need(v, "v", k.dtype, (T, H, dv), dev)
+    _need(g, "g", torch.float32, (T, H, dk), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+    N = cu_seqlens.numel() - 1
+    Sg = int(num_segments)
+    if transfer is None:
+        transfer = torch.empty((N, H, Sg, dk, dk), dtype=torch.float32, device=dev)
+    if zero_init_state is None:
+        zero_init_state = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
+    _need(transfer, "transfer", torch.float32, (N, H, Sg, dk, dk), dev)
+    _need(zero_init_state, "zero_init_state", torch.float32, (N, H, Sg, dk, dv), dev)
+    desc = _desc(N, T, H, dk, dv, act, Sg)
+    seg_end = Sg if seg_end is None else int(seg_end)
+    rc = lib().kda_state_transfer(ctypes.byref(desc), int(seg_begin), seg_end, _ptr(k), _ptr(v),
+                                  _ptr(g), _ptr(beta),
+                                  _ptr(cu_seqlens), _ptr(transfer), _ptr(zero_init_state),
+                                  _ptr(dev_status), _stream(stream, dev))
+    _check("kda_state_transfer", rc)
+    return transfer, zero_init_state
+
+
+def state_compose(transfer, zero_init_state, S0=None, *, seg_init_states=None, S_final=None,
+                  want_starts=True, want_final_state=True, stream=None):
+    """Prefix scan over segments (see kda_state_compose in kda.h): transfer ``[U, S,
+    dk, dk]``, zero_init_state ``[U, S, dk, dv]``, S0 ``[U, dk, dv]`` or None.
+    Returns ``(seg_init_states [U,S,dk,dv] or None, S_final [U,dk,dv] or None)``;
+    without a final state the last pair is never read."""
+    dev = transfer.device
+    U, Sg, dk, _ = transfer.shape
+    dv = zero_init_state.shape[-1]
+    _need(transfer, "transfer", torch.float32, (U, Sg, dk, dk))
+    _need(zero_init_state, "zero_init_state", torch.float32, (U, Sg, dk, dv), dev)
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, (U, dk, dv), dev)
+    if seg_init_states is None and want_starts:
+        seg_init_states = torch.empty((U, Sg, dk, dv), dtype=torch.float32, device=dev)
+    if S_final is None and want_final_state:
+        S_final = torch.empty((U, dk, dv), dtype=torch.float32, device=dev)
+    rc = lib().kda_state_compose(U, Sg, dk, dv, _ptr(transfer), _ptr(zero_init_state), _ptr(S0),
+                                 _ptr(seg_init_states), _ptr(S_final), _stream(stream, dev))
+    _check("kda_state_compose", rc)
+    return seg_init_states, S_final

@@ -1,0 +1,259 @@
+// C ABI of libkda: host-side argument checks, segment planning and dispatch.
+// Nothing here allocates device memory or synchronises the host.
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+using namespace kda;
+
+constexpr int kMaxDim = 128;
+constexpr int kMaxSegments = 4096;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+kda_status_t check_desc(const kda_prefill_desc_t *d) {
+    if (!d) return KDA_ERR_INVALID_ARG;
+    if (d->num_seqs < 0 || d->total_tokens < 0 || d->num_heads < 1) return KDA_ERR_INVALID_ARG;
+    if (d->dk < 1 || d->dv < 1 || d->num_segments < 0) return KDA_ERR_INVALID_ARG;
+    if (d->chunk != 16) return KDA_ERR_UNSUPPORTED;
+    if (d->act_dtype != KDA_DTYPE_F32 && d->act_dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
+    if (d->dk > kMaxDim || d->dv > kMaxDim) return KDA_ERR_UNSUPPORTED;
+    if (d->num_segments > kMaxSegments) return KDA_ERR_UNSUPPORTED;
+    // Every index the kernels form must fit the int/size_t arithmetic they use.
+    if ((long long)d->total_tokens * d->num_heads * (d->dk > d->dv ? d->dk : d->dv) >
+        (1ll << 40))
+        return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
+PrefillArgs base_args(const kda_prefill_desc_t *d) {
+    PrefillArgs a;
+    memset(&a, 0, sizeof(a));
+    a.N = d->num_seqs;
+    a.T_tot = d->total_tokens;
+    a.H = d->num_heads;
+    a.dk = d->dk;
+    a.dv = d->dv;
+    a.act = d->act_dtype;
+    return a;
+}
+
+// Segments per sequence when the caller leaves the choice to the library.
+// One pass per (sequence, head) is used when those chains already cover the
+// GPU twice over; otherwise every sequence is split so that the chains fill it,
+// keeping at least 8 blocks (128 tokens) per segment.
+int choose_segments(const kda_prefill_desc_t *d) {
+    if (d->num_segments > 0) return d->num_segments;
+    const long long chains = (long long)d->num_seqs * d->num_heads;
+    if (chains == 0) return 1;
+    const long long want = 2ll * sm_count();
+    if (chains >= want) return 1;
+    const long long avg_chunks = ((long long)d->total_tokens / d->num_seqs + 15) / 16;
+    long long sg = (want + chains - 1) / chains;
+    const long long cap = avg_chunks / 8;
+    if (sg > cap) sg = cap;
+    if (sg > 64) sg = 64;
+    if (sg < 1) sg = 1;
+    return (int)sg;
+}
+
+size_t workspace_bytes_for(const kda_prefill_desc_t *d, int Sg) {
+    if (Sg <= 1) return 0;
+    const size_t units = (size_t)d->num_seqs * d->num_heads * Sg;
+    const size_t per = (size_t)d->dk * d->dk + 2 * (size_t)d->dk * d->dv;
+    return units * per * sizeof(float);
+}
+
+cudaError_t run_prefill_pass(const PrefillArgs &a, cudaStream_t st) {
+    if (prefill_tc_supported(a)) return launch_prefill_tc(a, st);
+    return launch_prefill_simt(a, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kda_prefill_num_segments(const kda_prefill_desc_t *desc) {
+    if (check_desc(desc) != KDA_OK) return 0;
+    return choose_segments(desc);
+}
+
+size_t kda_prefill_workspace_size(const kda_prefill_desc_t *desc) {
+    if (check_desc(desc) != KDA_OK) return 0;
+    return workspace_bytes_for(desc, choose_segments(desc));
+}
+
+kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, const void *k,
+                                 const void *v, const float *g, const float *beta,
+                                 const float *S0, const int32_t *cu_seqlens, void *out,
+                                 float *S_final, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream) {
+    kda_status_t rc = check_desc(desc);
+    if (rc != KDA_OK) return rc;
+    if (desc->num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (desc->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out))
+        return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, S0, out, S_final, cu_seqlens};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const int Sg = choose_segments(desc);
+    const size_t need = workspace_bytes_for(desc, Sg);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return KDA_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    PrefillArgs a = base_args(desc);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens;
+    a.out = out; a.S_final = S_final; a.dev_status = dev_status;
+    a.Sg = Sg;
+
+    if (Sg == 1) {
+        a.S0 = S0;
+        a.seg_count = 1;
+        a.mode = MODE_OUTPUT;
+        return from_cuda(run_prefill_pass(a, st));
+    }
+
+    // Context-parallel split: transfer pass on segments 0..Sg-2, scan, then
+    // every segment from its true start state.
+    const size_t units = (size_t)desc->num_seqs * desc->num_heads;
+    float *A = (float *)workspace;
+    float *B = A + units * Sg * desc->dk * desc->dk;
+    float *starts = B + units * Sg * desc->dk * desc->dv;
+
+    PrefillArgs t = a;
+    t.mode = MODE_TRANSFER;
+    t.seg_begin = 0;
+    t.seg_count = Sg - 1;
+    t.transfer = A;
+    t.zero_state = B;
+    t.out = nullptr;
+    t.S_final = nullptr;
+    cudaError_t e = run_prefill_pass(t, st);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    e = launch_compose((int)units, Sg, desc->dk, desc->dv, A, B, S0, starts, nullptr, st);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    a.mode = MODE_OUTPUT;
+    a.seg_count = Sg;
+    a.seg_init = starts;
+    return from_cuda(run_prefill_pass(a, st));
+}
+
+kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_begin,
+                                  int32_t seg_end, const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta,
+                                  const float *seg_init_states, const int32_t *cu_seqlens,
+                                  void *out, float *S_final, int32_t *dev_status, void *stream) {
+    kda_status_t rc = check_desc(desc);
+    if (rc != KDA_OK) return rc;
+    if (desc->num_segments < 1) return KDA_ERR_INVALID_ARG;
+    if (seg_begin < 0 || seg_end < seg_begin || seg_end > desc->num_segments)
+        return KDA_ERR_INVALID_ARG;
+    if (seg_end == seg_begin) return KDA_OK;
+    if (desc->num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (desc->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out))
+        return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, seg_init_states, out, S_final, cu_seqlens};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    PrefillArgs a = base_args(desc);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens;
+    a.out = out; a.S_final = S_final; a.dev_status = dev_status;
+    a.Sg = desc->num_segments;
+    a.seg_begin = seg_begin;
+    a.seg_count = seg_end - seg_begin;
+    a.mode = MODE_OUTPUT;
+    a.seg_init = seg_init_states;
+    return from_cuda(run_prefill_pass(a, (cudaStream_t)stream));
+}
+
+kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv,
+                             int32_t act_dtype, const void *q, const void *k, const void *v,
+                             const float *g, const float *beta, float *S_inout, void *out,
+                             void *stream) {
+    if (batch < 0 || num_heads < 1 || dk < 1 || dv < 1) return KDA_ERR_INVALID_ARG;
+    if (act_dtype != KDA_DTYPE_F32 && act_dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
+    if (dk > kMaxDim || dv > kMaxDim || (dv & 3) != 0) return KDA_ERR_UNSUPPORTED;
+    if ((long long)batch * num_heads > 0x7fffffffll) return KDA_ERR_UNSUPPORTED;
+    if (batch == 0) return KDA_OK;
+    const void *ptrs[] = {q, k, v, g, beta, S_inout, out};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    return from_cuda(launch_decode(batch, num_heads, dk, dv, act_dtype, q, k, v, g, beta,
+                                   S_inout, out, (cudaStream_t)stream));
+}
+
+kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begin,
+                                int32_t seg_end, const void *k, const void *v, const float *g,
+                                const float *beta, const int32_t *cu_seqlens, float *transfer,
+                                float *zero_init_state, int32_t *dev_status, void *stream) {
+    kda_status_t rc = check_desc(desc);
+    if (rc != KDA_OK) return rc;
+    if (desc->num_segments < 1) return KDA_ERR_INVALID_ARG;
+    if (seg_begin < 0 || seg_end < seg_begin || seg_end > desc->num_segments)
+        return KDA_ERR_INVALID_ARG;
+    if (seg_end == seg_begin) return KDA_OK;
+    if (desc->num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens || !transfer || !zero_init_state) return KDA_ERR_INVALID_ARG;
+    if (desc->total_tokens > 0 && (!k || !v || !g || !beta)) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {k, v, g, beta, cu_seqlens, transfer, zero_init_state};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    PrefillArgs t = base_args(desc);
+    t.k = k; t.v = v; t.g = g; t.beta = beta; t.cu = cu_seqlens; t.dev_status = dev_status;
+    t.Sg = desc->num_segments;
+    t.seg_begin = seg_begin;
+    t.seg_count = seg_end - seg_begin;
+    t.mode = MODE_TRANSFER;
+    t.transfer = transfer;
+    t.zero_state = zero_init_state;
+    return from_cuda(run_prefill_pass(t, (cudaStream_t)stream));
+}
+
+kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int32_t dv,
+                               const float *transfer, const float *zero_init_state,
+                               const float *S0, float *seg_init_states, float *S_final,
+                               void *stream) {
+    if (units < 0 || segments < 1 || dk < 1 || dv < 1) return KDA_ERR_INVALID_ARG;
+    if (dk > kMaxDim || dv > kMaxDim) return KDA_ERR_UNSUPPORTED;
+    if (units == 0) return KDA_OK;
+    if (!transfer || !zero_init_state) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {transfer, zero_init_state, S0, seg_init_states, S_final};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    return from_cuda(launch_compose(units, segments, dk, dv, transfer, zero_init_state, S0,
+                                    seg_init_states, S_final, (cudaStream_t)stream));
+}
+
+const char *kda_status_string(kda_status_t s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDA_ERR_CUDA: return "CUDA launch or runtime error";
+        case KDA_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *kda_build_info(void) {
+    return "libkda 0.1 sm_103a tc:0";
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Internal declarations shared by the libkda translation units (not installed).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// ---------------------------------------------------------------------------
+// Activation load / store in fp32 registers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float act_ld(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float act_ld(const __nv_bfloat16 *p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void act_st(float *p, size_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void act_st(__nv_bfloat16 *p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+// First error wins; 0 means "no error yet".
+__device__ __forceinline__ void dev_fail(int32_t *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// Token range [t_begin, t_end) of segment s (of Sg) of sequence n.  The
+// sequence's chunks are split evenly: segment s takes chunks
+// [floor(s c / Sg), floor((s+1) c / Sg)) with c = ceil(len / 16).
+// Returns false (and records KDA_ERR_INVALID_ARG) if cu_seqlens is malformed.
+__device__ __forceinline__ bool segment_range(const int32_t *cu, int n, int N, int T_tot,
+                                              int s, int Sg, int32_t *status, int &t_begin,
+                                              int &t_end) {
+    const int a = cu[n], b = cu[n + 1];
+    if (a < 0 || b < a || b > T_tot || cu[0] != 0 || cu[N] != T_tot) {
+        dev_fail(status, KDA_ERR_INVALID_ARG);
+        return false;
+    }
+    const long long len = b - a;
+    const long long c = (len + 15) / 16;
+    const long long c0 = (long long)s * c / Sg, c1 = (long long)(s + 1) * c / Sg;
+    t_begin = a + (int)min(len, c0 * 16);
+    t_end = a + (int)min(len, c1 * 16);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Chunked prefill launch description (shared by the SIMT and tensor-core paths).
+// ---------------------------------------------------------------------------
+enum PrefillMode { MODE_OUTPUT = 0, MODE_TRANSFER = 1 };
+
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *g, *beta;
+    const float *S0;        // [N,H,dk,dv] or null                (MODE_OUTPUT)
+    const float *seg_init;  // [N,H,Sg,dk,dv] start states or null (MODE_OUTPUT, Sg > 1)
+    const int32_t *cu;
+    void *out;
+    float *S_final;         // [N,H,dk,dv] or null; written by segment Sg-1
+    float *transfer;        // [N,H,Sg,dk,dk]                       (MODE_TRANSFER)
+    float *zero_state;      // [N,H,Sg,dk,dv]                       (MODE_TRANSFER)
+    int32_t *dev_status;
+    int N, T_tot, H, dk, dv;
+    int Sg;                 // segments per sequence (layout and bounds)
+    int seg_begin;          // segments seg_begin .. seg_begin+seg_count-1 are
+    int seg_count;          // processed by this launch
+    int mode;
+    int act;                // kda_dtype_t
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t st);
+bool prefill_tc_supported(const PrefillArgs &a);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st);
+cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, const float *B,
+                           const float *S0, float *seg_init, float *S_final, cudaStream_t st);
+cudaError_t launch_decode(int batch, int H, int dk, int dv, int act, const void *q,
+                          const void *k, const void *v, const float *g, const float *beta,
+                          float *S, void *out, cudaStream_t st);
+
+}  // namespace kda

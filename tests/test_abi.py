@@ -1,0 +1,131 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads, exports
+every entry point declared in include/kda.h, and rejects bad arguments on the
+host (before any launch) with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import kimi_delta_attention_18_gb300 as kda
+from kimi_delta_attention_18_gb300._native import PrefillDesc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA, TIMEOUT = range(6)
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kda_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported():
+    L = kda.lib()
+    names = _declared_functions()
+    assert len(names) >= 8
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_build_info():
+    L = kda.lib()
+    for s in range(6):
+        assert L.kda_status_string(s)
+    assert L.kda_status_string(99) == b"unknown status"
+    assert b"sm_103a" in L.kda_build_info()
+
+
+def _desc(**kw):
+    base = dict(num_seqs=1, total_tokens=64, num_heads=2, dk=16, dv=16, act_dtype=0, chunk=16,
+                num_segments=1)
+    base.update(kw)
+    return PrefillDesc(*[base[f] for f, _ in PrefillDesc._fields_])
+
+
+def _prefill(desc, ptr=0x10000, ws=None, ws_len=0, cu=0x20000):
+    L = kda.lib()
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return L.kda_prefill_chunked(ctypes.byref(desc) if desc is not None else None, p, p, p, p, p,
+                                 None, ctypes.c_void_p(cu) if cu else None, p, None,
+                                 ctypes.c_void_p(ws) if ws else None, ws_len, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk=8), UNSUPPORTED),
+    (dict(dk=129), UNSUPPORTED),
+    (dict(dv=0), INVALID),
+    (dict(act_dtype=5), UNSUPPORTED),
+    (dict(num_seqs=-1), INVALID),
+    (dict(num_heads=0), INVALID),
+    (dict(num_segments=-2), INVALID),
+    (dict(num_segments=5000), UNSUPPORTED),
+])
+def test_prefill_rejects_bad_descriptor(kw, code):
+    assert _prefill(_desc(**kw)) == code
+
+
+def test_prefill_rejects_null_and_misaligned_pointers():
+    L = kda.lib()
+    assert L.kda_prefill_chunked(None, *([None] * 9), None, 0, None, None) == INVALID
+    assert _prefill(_desc(), ptr=0) == INVALID          # q, k, ... missing
+    assert _prefill(_desc(), ptr=0x10004) == INVALID    # not 16-byte aligned
+    assert _prefill(_desc(), cu=0) == INVALID           # cu_seqlens missing
+    assert _prefill(_desc(num_seqs=0)) == OK            # nothing to do, nothing launched
+
+
+def test_prefill_split_requires_workspace():
+    d = _desc(num_segments=4)
+    need = kda.prefill_workspace_size(d)
+    assert need == 1 * 2 * 4 * (16 * 16 + 2 * 16 * 16) * 4
+    assert _prefill(d) == WORKSPACE
+    assert _prefill(d, ws=0x40000, ws_len=need - 1) == WORKSPACE
+    assert _prefill(d, ws=0x40008, ws_len=need) == WORKSPACE  # misaligned workspace
+
+
+def test_segment_choice():
+    assert kda.prefill_num_segments(_desc(num_segments=7)) == 7
+    # many chains: one pass each
+    assert kda.prefill_num_segments(_desc(num_seqs=4, num_heads=128, total_tokens=4096,
+                                          num_segments=0)) == 1
+    # few long chains: split, at least 8 blocks per segment, at most 64 segments
+    s = kda.prefill_num_segments(_desc(num_seqs=1, num_heads=8, total_tokens=4096, dk=128,
+                                       dv=128, num_segments=0))
+    assert 2 <= s <= 32
+    s = kda.prefill_num_segments(_desc(num_seqs=1, num_heads=1, total_tokens=1 << 20,
+                                       num_segments=0))
+    assert s == 64
+    assert kda.prefill_num_segments(_desc(chunk=4)) == 0
+    assert kda.prefill_workspace_size(_desc(num_segments=1)) == 0
+
+
+def test_decode_and_compose_host_checks():
+    L = kda.lib()
+    p = ctypes.c_void_p(0x10000)
+    assert L.kda_decode_step(4, 2, 16, 18, 1, p, p, p, p, p, p, p, None) == UNSUPPORTED  # dv % 4
+    assert L.kda_decode_step(4, 2, 256, 16, 1, p, p, p, p, p, p, p, None) == UNSUPPORTED
+    assert L.kda_decode_step(4, 2, 16, 16, 3, p, p, p, p, p, p, p, None) == UNSUPPORTED
+    assert L.kda_decode_step(4, 0, 16, 16, 1, p, p, p, p, p, p, p, None) == INVALID
+    assert L.kda_decode_step(4, 2, 16, 16, 1, p, p, p, p, None, p, p, None) == INVALID
+    assert L.kda_decode_step(4, 2, 16, 16, 1, p, p, p, p, ctypes.c_void_p(0x10002), p, p,
+                             None) == INVALID
+    assert L.kda_decode_step(0, 2, 16, 16, 1, p, p, p, p, p, p, p, None) == OK
+    assert L.kda_state_compose(2, 0, 16, 16, p, p, None, None, None, None) == INVALID
+    assert L.kda_state_compose(2, 3, 16, 200, p, p, None, None, None, None) == UNSUPPORTED
+    assert L.kda_state_compose(2, 3, 16, 16, None, p, None, None, None, None) == INVALID
+    assert L.kda_state_compose(0, 3, 16, 16, None, None, None, None, None, None) == OK
+    d = _desc(num_segments=0)
+    assert L.kda_state_transfer(ctypes.byref(d), 0, 1, p, p, p, p, p, p, p, None, None) == INVALID
+    assert L.kda_prefill_segments(ctypes.byref(d), 0, 1, p, p, p, p, p, None, p, p, None, None,
+                                  None) == INVALID
+    d = _desc(num_segments=4)
+    for a, b in ((-1, 2), (3, 2), (0, 5)):
+        assert L.kda_state_transfer(ctypes.byref(d), a, b, p, p, p, p, p, p, p, None,
+                                    None) == INVALID
+        assert L.kda_prefill_segments(ctypes.byref(d), a, b, p, p, p, p, p, None, p, p, None,
+                                      None, None) == INVALID
+    assert L.kda_state_transfer(ctypes.byref(d), 2, 2, p, p, p, p, p, p, p, None, None) == OK
