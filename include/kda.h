@@ -103,7 +103,8 @@ size_t kda_prefill_workspace_size(const kda_prefill_desc_t *desc);
  * (digest 2.4 (1), KCP).  A zero-length sequence gives S_final = S0.
  *
  *   desc            problem description (host pointer).
- *   q, k, v, g, beta, out   device arrays in the layouts above; 16-byte aligned.
+ *   q, k, v, g, beta, out   device arrays in the layouts above; q, k, v, g and
+ *                   out 16-byte aligned, the rest 4-byte aligned.
  *   S0              [N, H, dk, dv] fp32 or NULL.
  *   cu_seqlens      [N+1] int32 (device).
  *   S_final         [N, H, dk, dv] fp32 or NULL; may equal S0.
@@ -123,7 +124,7 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
  * recurrence above applied once, in place on S_inout [batch, H, dk, dv] fp32,
  * with q, k [batch, H, dk], v, out [batch, H, dv] in act_dtype, g [batch, H,
  * dk] and beta [batch, H] fp32.  Streams each state through once.  dv must be
- * a multiple of 4 and every pointer 16-byte aligned.
+ * a multiple of 4 and S_inout 16-byte aligned (the others 4-byte aligned).
  */
 kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv,
                              int32_t act_dtype, const void *q, const void *k, const void *v,

@@ -13,6 +13,7 @@ constexpr int kMaxDim = 128;
 constexpr int kMaxSegments = 4096;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
 
 kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
@@ -107,9 +108,14 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
     if (desc->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out))
         return KDA_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, g, beta, S0, out, S_final, cu_seqlens};
-    for (const void *p : ptrs)
+    // Row-wise bulk copies and vector stores need 16-byte bases; the rest is read
+    // element by element.
+    const void *rows[] = {q, k, v, g, out};
+    for (const void *p : rows)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const void *elems[] = {beta, S0, S_final, cu_seqlens};
+    for (const void *p : elems)
+        if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
     const int Sg = choose_segments(desc);
     const size_t need = workspace_bytes_for(desc, Sg);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
@@ -168,9 +174,12 @@ kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_be
     if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
     if (desc->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out))
         return KDA_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, g, beta, seg_init_states, out, S_final, cu_seqlens};
-    for (const void *p : ptrs)
+    const void *rows[] = {q, k, v, g, out};
+    for (const void *p : rows)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const void *elems[] = {beta, seg_init_states, S_final, cu_seqlens};
+    for (const void *p : elems)
+        if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
     PrefillArgs a = base_args(desc);
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens;
     a.out = out; a.S_final = S_final; a.dev_status = dev_status;
@@ -191,9 +200,13 @@ kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32
     if (dk > kMaxDim || dv > kMaxDim || (dv & 3) != 0) return KDA_ERR_UNSUPPORTED;
     if ((long long)batch * num_heads > 0x7fffffffll) return KDA_ERR_UNSUPPORTED;
     if (batch == 0) return KDA_OK;
-    const void *ptrs[] = {q, k, v, g, beta, S_inout, out};
-    for (const void *p : ptrs)
-        if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    // The state is streamed as float4; everything else is read element by element.
+    const uintptr_t act_align = act_dtype == KDA_DTYPE_BF16 ? 2u : 4u;
+    const void *acts[] = {q, k, v, out};
+    for (const void *p : acts)
+        if (!p || ((uintptr_t)p & (act_align - 1u)) != 0) return KDA_ERR_INVALID_ARG;
+    if (!g || !beta || !aligned4(g) || !aligned4(beta)) return KDA_ERR_INVALID_ARG;
+    if (!S_inout || !aligned16(S_inout)) return KDA_ERR_INVALID_ARG;
     return from_cuda(launch_decode(batch, num_heads, dk, dv, act_dtype, q, k, v, g, beta,
                                    S_inout, out, (cudaStream_t)stream));
 }
@@ -211,9 +224,12 @@ kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begi
     if (desc->num_seqs == 0) return KDA_OK;
     if (!cu_seqlens || !transfer || !zero_init_state) return KDA_ERR_INVALID_ARG;
     if (desc->total_tokens > 0 && (!k || !v || !g || !beta)) return KDA_ERR_INVALID_ARG;
-    const void *ptrs[] = {k, v, g, beta, cu_seqlens, transfer, zero_init_state};
-    for (const void *p : ptrs)
+    const void *rows[] = {k, v, g};
+    for (const void *p : rows)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const void *elems[] = {beta, cu_seqlens, transfer, zero_init_state};
+    for (const void *p : elems)
+        if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
     PrefillArgs t = base_args(desc);
     t.k = k; t.v = v; t.g = g; t.beta = beta; t.cu = cu_seqlens; t.dev_status = dev_status;
     t.Sg = desc->num_segments;
