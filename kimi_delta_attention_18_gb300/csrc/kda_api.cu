@@ -207,6 +207,12 @@ kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32
         if (!p || ((uintptr_t)p & (act_align - 1u)) != 0) return KDA_ERR_INVALID_ARG;
     if (!g || !beta || !aligned4(g) || !aligned4(beta)) return KDA_ERR_INVALID_ARG;
     if (!S_inout || !aligned16(S_inout)) return KDA_ERR_INVALID_ARG;
+    // dk = dv = 128 with 16-byte aligned rows: the TMA-streamed kernel; otherwise the
+    // register-streamed one.
+    if (decode_tma_supported(dk, dv) && aligned16(q) && aligned16(k) && aligned16(v) &&
+        aligned16(g))
+        return from_cuda(launch_decode_tma(batch, num_heads, act_dtype, q, k, v, g, beta,
+                                           S_inout, out, (cudaStream_t)stream));
     return from_cuda(launch_decode(batch, num_heads, dk, dv, act_dtype, q, k, v, g, beta,
                                    S_inout, out, (cudaStream_t)stream));
 }
@@ -269,7 +275,7 @@ const char *kda_status_string(kda_status_t s) {
 }
 
 const char *kda_build_info(void) {
-    return "libkda 0.1 sm_103a tc:0";
+    return "libkda 0.1 sm_103a tc:1";
 }
 
 }  // extern "C"

@@ -1,10 +1,571 @@
-// Tensor-core (tcgen05) chunked prefill for BF16 activations at dk = dv = 128.
+// Tensor-core chunked KDA prefill for BF16 activations at dk = dv = 128 (sm_103a).
+//
+// What it computes: the chunked form of the KDA recurrence (decay, then erase,
+// then write, then read: "Kimi K3 Architecture Explained", section 3), with the
+// bounded log-decay g > -5 keeping every in-block factor exp(+-Gamma), |Gamma| <
+// 80, inside BF16 range so that both the intra-block ("diagonal") and the
+// state ("off-diagonal") products run on tensor cores (Kimi K3 technical-report
+// digest, section 2.1 (1)).  Per 16-token block, from state S (128 x 128, fp32):
+//   prep (state-free):  Gamma = cumsum g;  Kh = K e^{Gamma};  Kt = K e^{-Gamma};
+//                       Qh = Q e^{Gamma};  Kb = K e^{Gamma_C - Gamma};
+//                       L = Diag(beta) strict_lower(Kh Kt^T);  Mq = lower(Qh Kt^T);
+//                       T = (I + L)^{-1} Diag(beta);  W = T Kh;  Ut = T V
+//   chain (sequential): U = Ut - W S;  O = Qh S + Mq U;  S <- e^{Gamma_C} S + Kb^T U
+// The digest's FlashKDA overlaps the intra-block work with the cross-block state
+// propagation (section 2.4 (1)); here that is warp specialisation inside one CTA:
+//
+//   warp 0      producer: bulk copies (TMA engine) of each block's q/k/v/g rows
+//   warp 1      issues tcgen05.mma (one thread); owns the TMEM allocation
+//   warps 2-5   prep of block c+1 (CUDA cores + mma.sync for the 16x16 products)
+//   warps 6-13  state: fp32 master state S in registers (lane = dv column j,
+//               64 dk channels per warp), U, the decayed update, the output read
+//
+// Transposed so the MMA M dimension is the 128 state columns (TMEM lanes):
+//   D1[j][r]      = (S^T [W; Qh]^T)          M=128 N=32 K=128  (8 x K16)
+//   D1[j][16+r]  += (U^T Mq^T)               M=128 N=16 K=16
+//   D3[j][i]      = (U^T Kb)                 M=128 N=128 K=16
+// with S^T, U^T as bf16 A operands in shared memory and fp32 accumulators in
+// TMEM.  The master state never leaves fp32 registers; only its bf16 copy feeds
+// the MMA.  One CTA per (sequence, head, segment); in the transfer pass two
+// CTAs per unit run the same recurrence on the identity (values 0) and on zeros
+// (the unit's values) to give the transfer matrix and the zero-initial state.
+//
+// Every wait is bounded: a stalled barrier sets an abort flag, records
+// KDA_ERR_TIMEOUT in dev_status, and all roles leave their loops, free TMEM and
+// return.
 #include "kda_internal.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
+namespace {
 
-bool prefill_tc_supported(const PrefillArgs &) { return false; }
+using namespace sm100;
 
-cudaError_t launch_prefill_tc(const PrefillArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int C = 16;   // tokens per block
+constexpr int D = 128;  // dk = dv
+constexpr int NS = 3;   // input stages in flight
+constexpr int NP = 2;   // prepared-operand stages
+constexpr int W_PROD = 0, W_MMA = 1, W_PREP0 = 2, N_PREP = 4, W_STATE0 = 6, N_STATE = 8;
+constexpr int NWARPS = W_STATE0 + N_STATE;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr long long kWaitLimit = 4000000000ll;  // ~2 s of SM clocks
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t D3_COL = 0;    // 128 columns: U^T Kb
+constexpr uint32_t D1_COL = 128;  // 2 x 32 columns: [W S | Qh S + Mq U]^T, double-buffered
+
+// ---- shared memory map (bytes from a 1024-aligned base) ----
+constexpr int ROWB = 272;  // one 128-element bf16 row padded to 136 elements
+// UMMA operands (canonical K-major, no swizzle: 8x16-byte core matrices,
+// LBO = 128 bytes between core matrices along K, SBO between 8-row groups).
+constexpr int SA_OFF = 0;                    // S^T  [j 128][i 128]  SBO 2048   32 KB
+constexpr int UA_OFF = SA_OFF + 32768;       // U^T  [j 128][r 16]   SBO 256     4 KB
+constexpr int PP_OFF = UA_OFF + 4096;        // prepared stages
+constexpr int PP_B1 = 0;                     // [W; Qh] [r 32][i 128] SBO 2048   8 KB
+constexpr int PP_B2 = 8192;                  // Mq   [r 16][i 16]   SBO 256    512 B
+constexpr int PP_B3 = PP_B2 + 512;           // Kb^T [i 128][r 16]  SBO 256     4 KB
+constexpr int UT_LD = 132;                   // Ut fp32 row stride (floats)
+constexpr int PP_UT = PP_B3 + 4096;          // Ut   fp32 [16][132]
+constexpr int PP_DECAY = PP_UT + C * UT_LD * 4;  // exp(Gamma_C) fp32 [128]
+constexpr int PP_SIZE = PP_DECAY + 512;
+constexpr int IN_OFF = PP_OFF + NP * PP_SIZE;  // input stages
+constexpr int IN_Q = 0;                        // bf16 rows, 272-byte stride
+constexpr int IN_K = IN_Q + C * ROWB;
+constexpr int IN_V = IN_K + C * ROWB;
+constexpr int IN_G = IN_V + C * ROWB;          // fp32 [16][128]
+constexpr int IN_B = IN_G + C * 512;           // beta fp32 [16]
+constexpr int IN_SIZE = IN_B + 64;
+constexpr int SC_OFF = IN_OFF + NS * IN_SIZE;  // prep scratch
+constexpr int SC_KH = 0;                       // Kh bf16 [16][136]
+constexpr int SC_KT = SC_KH + C * ROWB;        // Kt bf16 [16][136]
+constexpr int SC_QH = SC_KT + C * ROWB;        // Qh bf16 [16][136]
+constexpr int SC_L = SC_QH + C * ROWB;         // Diag(beta) L fp32 [16][17]
+constexpr int SC_T = SC_L + C * 17 * 4;        // T bf16 [16][24]
+constexpr int SC_SIZE = SC_T + C * 48;
+constexpr int BAR_OFF = (SC_OFF + SC_SIZE + 7) & ~7;
+enum {
+    B_IN_FULL = 0,
+    B_IN_EMPTY = B_IN_FULL + NS,
+    B_PP_FULL = B_IN_EMPTY + NS,
+    B_PP_EMPTY = B_PP_FULL + NP,
+    B_MMA1 = B_PP_EMPTY + NP,
+    B_UREADY,
+    B_MMA3,
+    B_SREADY,
+    NBARS
+};
+constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // [0] TMEM base, [1] abort, [2] prep flag
+constexpr int SMEM_USED = MISC_OFF + 16;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
+
+static_assert(PP_SIZE % 128 == 0 && IN_SIZE % 16 == 0, "stage alignment");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+// Byte offset of element (row, k) in a canonical no-swizzle K-major operand.
+__device__ __forceinline__ uint32_t kmaj_off(int row, int k, int sbo) {
+    return (uint32_t)((row >> 3) * sbo + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
+
+struct Ctx {
+    const PrefillArgs *p;
+    uint8_t *smem;
+    uint32_t sbase;
+    uint32_t tmem;
+    volatile int *abort;
+    volatile int *prep_ok;
+    int n, h, s;
+    int t_begin, t_end, nchunks;
+    bool transfer, partA, want_q, want_v;
+    __device__ uint32_t bar(int i) const { return sbase + BAR_OFF + 8 * i; }
+};
+
+__device__ __forceinline__ bool warp_wait(const Ctx &x, int b, uint32_t parity) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(x.bar(b), parity, x.abort, kWaitLimit);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void report_abort(const Ctx &x) {
+    if (*x.abort) dev_fail(x.p->dev_status, KDA_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ producer
+__device__ void producer_role(const Ctx &x) {
+    const PrefillArgs &p = *x.p;
+    const int lane = threadIdx.x & 31;
+    const __nv_bfloat16 *q = (const __nv_bfloat16 *)p.q;
+    const __nv_bfloat16 *k = (const __nv_bfloat16 *)p.k;
+    const __nv_bfloat16 *v = (const __nv_bfloat16 *)p.v;
+    int issued = 0;
+    for (int c = 0; c < x.nchunks; ++c) {
+        const int st = c % NS;
+        if (!warp_wait(x, B_IN_EMPTY + st, ((c / NS) & 1) ^ 1)) break;
+        const int t0 = x.t_begin + C * c;
+        const int nt = min(C, x.t_end - t0);
+        const uint32_t row_bytes = (x.want_q ? 256u : 0u) + 256u + (x.want_v ? 256u : 0u) + 512u;
+        const uint32_t full = x.bar(B_IN_FULL + st);
+        const uint32_t base = x.sbase + IN_OFF + st * IN_SIZE;
+        if (lane == 0) mbar_arrive_expect_tx(full, row_bytes * nt);
+        __syncwarp();
+        if (lane < nt) {
+            const size_t row = (size_t)(t0 + lane) * p.H + x.h;
+            if (x.want_q) bulk_g2s(base + IN_Q + lane * ROWB, q + row * D, 256, full);
+            bulk_g2s(base + IN_K + lane * ROWB, k + row * D, 256, full);
+            if (x.want_v) bulk_g2s(base + IN_V + lane * ROWB, v + row * D, 256, full);
+            bulk_g2s(base + IN_G + lane * 512, p.g + row * D, 512, full);
+        }
+        if (lane < C) {
+            float b = 0.f;
+            if (lane < nt) b = p.beta[(size_t)(t0 + lane) * p.H + x.h];
+            ((float *)(x.smem + IN_OFF + st * IN_SIZE + IN_B))[lane] = b;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full);  // second arrival: beta is in place
+        issued = c + 1;
+    }
+    // On an abort, let copies already in flight land before the CTA can exit.
+    if (*x.abort && lane == 0) {
+        volatile int never = 0;
+        for (int c = max(0, issued - NS); c < issued; ++c)
+            mbar_wait(x.bar(B_IN_FULL + c % NS), (c / NS) & 1, &never, kWaitLimit);
+    }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+__device__ void mma_role(const Ctx &x) {
+    const uint32_t id32 = umma_idesc_bf16(128, 32), id16 = umma_idesc_bf16(128, 16),
+                   id128 = umma_idesc_bf16(128, 128);
+    const uint32_t n1 = x.want_q ? id32 : id16;
+    const uint64_t ua = umma_desc(x.sbase + UA_OFF, 128, 256);
+    for (int c = 0; c < x.nchunks; ++c) {
+        const int pp = c % NP;
+        if (!mbar_wait(x.bar(B_PP_FULL + pp), (c / NP) & 1, x.abort, kWaitLimit)) break;
+        if (!mbar_wait(x.bar(B_SREADY), c & 1, x.abort, kWaitLimit)) break;
+        tc_fence_after();
+        const uint32_t d1 = x.tmem + D1_COL + (c & 1) * 32;
+        const uint32_t pbase = x.sbase + PP_OFF + pp * PP_SIZE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(d1, umma_desc(x.sbase + SA_OFF + kk * 256, 128, 2048),
+                      umma_desc(pbase + PP_B1 + kk * 256, 128, 2048), n1, kk > 0);
+        umma_commit(x.bar(B_MMA1));
+        if (!mbar_wait(x.bar(B_UREADY), c & 1, x.abort, kWaitLimit)) break;
+        tc_fence_after();
+        if (x.want_q) umma_bf16(d1 + 16, ua, umma_desc(pbase + PP_B2, 128, 256), id16, 1);
+        umma_bf16(x.tmem + D3_COL, ua, umma_desc(pbase + PP_B3, 128, 256), id128, 0);
+        umma_commit(x.bar(B_MMA3));
+        umma_commit(x.bar(B_PP_EMPTY + pp));
+    }
+}
+
+// ------------------------------------------------------------------ prep
+__device__ void prep_role(const Ctx &x) {
+    const int pt = threadIdx.x - W_PREP0 * 32;  // 0..127: the key channel in elementwise work
+    const int pw = pt >> 5, lane = pt & 31;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    uint8_t *sc = x.smem + SC_OFF;
+    const uint32_t sc_s = x.sbase + SC_OFF;
+    __nv_bfloat16 *Kh = (__nv_bfloat16 *)(sc + SC_KH);
+    __nv_bfloat16 *Kt = (__nv_bfloat16 *)(sc + SC_KT);
+    __nv_bfloat16 *Qh = (__nv_bfloat16 *)(sc + SC_QH);
+    float *Lf = (float *)(sc + SC_L);
+    __nv_bfloat16 *Tb = (__nv_bfloat16 *)(sc + SC_T);
+
+    for (int c = 0; c < x.nchunks; ++c) {
+        const int st = c % NS, pp = c % NP;
+        if (pt == 0) {
+            bool ok = mbar_wait(x.bar(B_IN_FULL + st), (c / NS) & 1, x.abort, kWaitLimit) &&
+                      mbar_wait(x.bar(B_PP_EMPTY + pp), ((c / NP) & 1) ^ 1, x.abort, kWaitLimit);
+            *x.prep_ok = ok ? 1 : 0;
+        }
+        named_bar_sync(1, N_PREP * 32);
+        if (!*x.prep_ok) break;
+
+        uint8_t *in = x.smem + IN_OFF + st * IN_SIZE;
+        uint8_t *pp_s = x.smem + PP_OFF + pp * PP_SIZE;
+        const float *gin = (const float *)(in + IN_G);
+        const float *bin = (const float *)(in + IN_B);
+        const int t0 = x.t_begin + C * c;
+        const int nt = min(C, x.t_end - t0);
+
+        // ---- elementwise: one key channel per thread
+        {
+            const int ch = pt;
+            float alpha[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) alpha[r] = r < nt ? expf(gin[r * D + ch]) : 1.f;
+            float fwd[C], rev[C];  // e^{Gamma_r}, e^{Gamma_C - Gamma_r}
+            float a = 1.f;
+#pragma unroll
+            for (int r = 0; r < C; ++r) { a *= alpha[r]; fwd[r] = a; }
+            float b = 1.f;
+#pragma unroll
+            for (int r = C - 1; r >= 0; --r) { rev[r] = b; b *= alpha[r]; }
+            const float eGC = fwd[C - 1];
+            const float einv = 1.f / eGC;
+            float kv[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                kv[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_K + r * ROWB))[ch])
+                               : 0.f;
+                Kh[r * 136 + ch] = __float2bfloat16_rn(kv[r] * fwd[r]);
+                Kt[r * 136 + ch] = __float2bfloat16_rn(kv[r] * (einv * rev[r]));
+                if (x.want_q) {
+                    const float qr =
+                        r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_Q + r * ROWB))[ch])
+                               : 0.f;
+                    const __nv_bfloat16 qh = __float2bfloat16_rn(qr * fwd[r]);
+                    Qh[r * 136 + ch] = qh;
+                    *(__nv_bfloat16 *)(pp_s + PP_B1 + kmaj_off(16 + r, ch, 2048)) = qh;
+                }
+            }
+            // Kb^T row ch (its 16 positions) as two 16-byte core-matrix rows.
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r0 = h8 * 8 + 2 * e;
+                    w[e] = pack_bf16x2(kv[r0] * rev[r0], kv[r0 + 1] * rev[r0 + 1]);
+                }
+                *(uint4 *)(pp_s + PP_B3 + kmaj_off(ch, h8 * 8, 256)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            ((float *)(pp_s + PP_DECAY))[ch] = eGC;
+        }
+        named_bar_sync(1, N_PREP * 32);
+
+        // ---- intra-block products on tensor cores (mma.sync): L (warp 0), Mq (warp 1)
+        if (pw == 0 || (pw == 1 && x.want_q)) {
+            const uint32_t a_base = sc_s + (pw == 0 ? SC_KH : SC_QH);
+            float acc[2][4] = {};
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t af[4], bf[4];
+                ldsm_x4(a_base + (lane & 15) * ROWB + (kk * 16 + (lane >> 4) * 8) * 2, af);
+                const int brow = (lane & 7) + ((lane >> 4) << 3);
+                const int bcol = kk * 16 + ((lane >> 3) & 1) * 8;
+                ldsm_x4(sc_s + SC_KT + brow * ROWB + bcol * 2, bf);
+                mma_bf16_16816(acc[0], af, bf[0], bf[1]);
+                mma_bf16_16816(acc[1], af, bf[2], bf[3]);
+            }
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = g8 + 8 * hh;
+                    const int i0 = nb * 8 + 2 * t4;
+                    const float v0 = acc[nb][2 * hh], v1 = acc[nb][2 * hh + 1];
+                    if (pw == 0) {
+                        const float br = bin[r];
+                        Lf[r * 17 + i0] = i0 < r ? br * v0 : 0.f;
+                        Lf[r * 17 + i0 + 1] = i0 + 1 < r ? br * v1 : 0.f;
+                    } else {
+                        const uint32_t w = pack_bf16x2(i0 <= r ? v0 : 0.f, i0 + 1 <= r ? v1 : 0.f);
+                        *(uint32_t *)(pp_s + PP_B2 + kmaj_off(r, i0, 256)) = w;
+                    }
+                }
+        }
+        named_bar_sync(1, N_PREP * 32);
+
+        // ---- T = (I + Diag(beta) L)^{-1} Diag(beta): forward substitution, lane = column
+        if (pw == 0 && lane < C) {
+            const int j = lane;
+            float xv[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) xv[r] = (r == j) ? 1.f : 0.f;
+#pragma unroll
+            for (int r = 1; r < C; ++r) {
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) {
+                    if (m & 1) s1 += Lf[r * 17 + m] * xv[m];
+                    else s0 += Lf[r * 17 + m] * xv[m];
+                }
+                if (r > j) xv[r] = -(s0 + s1);
+            }
+            const float bj = bin[j];
+#pragma unroll
+            for (int r = 0; r < C; ++r) Tb[r * 24 + j] = __float2bfloat16_rn(xv[r] * bj);
+        }
+        named_bar_sync(1, N_PREP * 32);
+
+        // ---- W = T Kh and Ut = T V: warp pw owns channels [32 pw, 32 pw + 32)
+        {
+            uint32_t af[4];
+            ldsm_x4(sc_s + SC_T + (lane & 15) * 48 + (lane >> 4) * 16, af);
+            float *Ut = (float *)(pp_s + PP_UT);
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                const int n0 = 32 * pw + 16 * np;
+                uint32_t bf[4];
+                ldsm_x4_t(sc_s + SC_KH + (lane & 15) * ROWB + (n0 + (lane >> 4) * 8) * 2, bf);
+                float w0[4] = {}, w1[4] = {};
+                mma_bf16_16816(w0, af, bf[0], bf[1]);
+                mma_bf16_16816(w1, af, bf[2], bf[3]);
+                float u0[4] = {}, u1[4] = {};
+                if (x.want_v) {
+                    uint32_t vf[4];
+                    ldsm_x4_t(x.sbase + IN_OFF + st * IN_SIZE + IN_V + (lane & 15) * ROWB +
+                                  (n0 + (lane >> 4) * 8) * 2,
+                              vf);
+                    mma_bf16_16816(u0, af, vf[0], vf[1]);
+                    mma_bf16_16816(u1, af, vf[2], vf[3]);
+                }
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    const float *wv = hb ? w1 : w0;
+                    const float *uv = hb ? u1 : u0;
+                    const int col = n0 + 8 * hb + 2 * t4;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int r = g8 + 8 * hh;
+                        *(uint32_t *)(pp_s + PP_B1 + kmaj_off(r, col, 2048)) =
+                            pack_bf16x2(wv[2 * hh], wv[2 * hh + 1]);
+                        *(float2 *)(Ut + r * UT_LD + col) = make_float2(uv[2 * hh], uv[2 * hh + 1]);
+                    }
+                }
+            }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(x.bar(B_PP_FULL + pp));
+            mbar_arrive(x.bar(B_IN_EMPTY + st));
+        }
+    }
+}
+
+// ------------------------------------------------------------------ state
+__device__ __forceinline__ void write_state_operand(const Ctx &x, const float (&S)[64], int j,
+                                                    int cbase) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        uint4 w;
+        w.x = pack_bf16x2(S[8 * g + 0], S[8 * g + 1]);
+        w.y = pack_bf16x2(S[8 * g + 2], S[8 * g + 3]);
+        w.z = pack_bf16x2(S[8 * g + 4], S[8 * g + 5]);
+        w.w = pack_bf16x2(S[8 * g + 6], S[8 * g + 7]);
+        *(uint4 *)(x.smem + SA_OFF + kmaj_off(j, cbase + 8 * g, 2048)) = w;
+    }
+}
+
+__device__ void state_role(const Ctx &x) {
+    const PrefillArgs &p = *x.p;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sw = warp - W_STATE0;
+    const int quarter = warp & 3;
+    const int half = sw >> 2;       // 0: dk channels 0..63 and U; 1: channels 64..127 and O
+    const int j = 32 * quarter + lane;  // state column (dv index) = TMEM lane
+    const int cbase = 64 * half;
+    const uint32_t lane_addr = x.tmem + ((uint32_t)(32 * quarter) << 16);
+    const size_t unit = (size_t)x.n * p.H + x.h;
+
+    float S[64];
+    {
+        const float *src = nullptr;
+        if (!x.transfer)
+            src = p.seg_init ? p.seg_init + (unit * p.Sg + x.s) * (size_t)D * D
+                             : (p.S0 ? p.S0 + unit * (size_t)D * D : nullptr);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+            const int i = cbase + e;
+            S[e] = x.partA ? (i == j ? 1.f : 0.f) : (src ? src[(size_t)i * D + j] : 0.f);
+        }
+    }
+    write_state_operand(x, S, j, cbase);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(x.bar(B_SREADY));
+
+    __nv_bfloat16 *out = (__nv_bfloat16 *)p.out;
+    for (int c = 0; c < x.nchunks; ++c) {
+        const int pp = c % NP;
+        const uint8_t *pp_s = x.smem + PP_OFF + pp * PP_SIZE;
+        if (!warp_wait(x, B_PP_FULL + pp, (c / NP) & 1)) break;
+        if (half == 0) {
+            if (!warp_wait(x, B_MMA1, c & 1)) break;
+            tc_fence_after();
+            float X[16];
+            tmem_ld16(lane_addr + D1_COL + (c & 1) * 32, X);
+            const float *Ut = (const float *)(pp_s + PP_UT);
+            uint32_t w[8];
+#pragma unroll
+            for (int r = 0; r < C; r += 2)
+                w[r >> 1] = pack_bf16x2(Ut[r * UT_LD + j] - X[r], Ut[(r + 1) * UT_LD + j] - X[r + 1]);
+            *(uint4 *)(x.smem + UA_OFF + kmaj_off(j, 0, 256)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *(uint4 *)(x.smem + UA_OFF + kmaj_off(j, 8, 256)) = make_uint4(w[4], w[5], w[6], w[7]);
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x.bar(B_UREADY));
+        }
+        if (!warp_wait(x, B_MMA3, c & 1)) break;
+        tc_fence_after();
+        const float *decay = (const float *)(pp_s + PP_DECAY) + cbase;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            float Dv[32];
+            tmem_ld32(lane_addr + D3_COL + cbase + 32 * blk, Dv);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                S[32 * blk + e] = fmaf(decay[32 * blk + e], S[32 * blk + e], Dv[e]);
+        }
+        write_state_operand(x, S, j, cbase);
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(x.bar(B_SREADY));
+            mbar_arrive(x.bar(B_PP_EMPTY + pp));
+        }
+        if (half == 1 && x.want_q) {
+            float O[16];
+            tmem_ld16(lane_addr + D1_COL + (c & 1) * 32 + 16, O);
+            tc_fence_before();
+            const int t0 = x.t_begin + C * c;
+            const int nt = min(C, x.t_end - t0);
+#pragma unroll
+            for (int r = 0; r < C; ++r)
+                if (r < nt) out[((size_t)(t0 + r) * p.H + x.h) * D + j] = __float2bfloat16_rn(O[r]);
+        }
+    }
+    if (*x.abort) return;
+
+    float *dst = nullptr;
+    if (!x.transfer) {
+        if (x.s == p.Sg - 1 && p.S_final) dst = p.S_final + unit * (size_t)D * D;
+    } else {
+        dst = (x.partA ? p.transfer : p.zero_state) + (unit * p.Sg + x.s) * (size_t)D * D;
+    }
+    if (dst) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) dst[(size_t)(cbase + e) * D + j] = S[e];
+    }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const PrefillArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    Ctx x;
+    x.p = &p;
+    x.smem = smem;
+    x.sbase = smem_addr(smem);
+    x.abort = (volatile int *)(smem + MISC_OFF + 4);
+    x.prep_ok = (volatile int *)(smem + MISC_OFF + 8);
+    const int u = blockIdx.x;
+    x.n = u / (p.H * p.seg_count);
+    x.h = (u / p.seg_count) % p.H;
+    x.s = p.seg_begin + u % p.seg_count;
+    x.transfer = p.mode == MODE_TRANSFER;
+    x.partA = x.transfer && blockIdx.y == 0;
+    x.want_q = !x.transfer;
+    x.want_v = !x.partA;
+    if (!segment_range(p.cu, x.n, p.N, p.T_tot, x.s, p.Sg, p.dev_status, x.t_begin, x.t_end))
+        return;
+    x.nchunks = (x.t_end - x.t_begin + C - 1) / C;
+
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(x.bar(B_IN_FULL + i), 2);
+            mbar_init(x.bar(B_IN_EMPTY + i), N_PREP);
+        }
+        for (int i = 0; i < NP; ++i) {
+            mbar_init(x.bar(B_PP_FULL + i), N_PREP);
+            mbar_init(x.bar(B_PP_EMPTY + i), 1 + N_STATE);
+        }
+        mbar_init(x.bar(B_MMA1), 1);
+        mbar_init(x.bar(B_UREADY), N_STATE / 2);
+        mbar_init(x.bar(B_MMA3), 1);
+        mbar_init(x.bar(B_SREADY), N_STATE);
+        *x.abort = 0;
+        *x.prep_ok = 0;
+        mbar_fence_init();
+    }
+    if (warp == W_MMA) {
+        tmem_alloc(x.sbase + MISC_OFF, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    x.tmem = *(volatile uint32_t *)(smem + MISC_OFF);
+
+    if (warp == W_PROD) {
+        producer_role(x);
+    } else if (warp == W_MMA) {
+        if ((threadIdx.x & 31) == 0) mma_role(x);
+        __syncwarp();
+    } else if (warp < W_STATE0) {
+        prep_role(x);
+    } else {
+        state_role(x);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) report_abort(x);
+    if (warp == W_MMA) {
+        tc_fence_after();
+        tmem_dealloc(x.tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillArgs &a) {
+    return a.act == KDA_DTYPE_BF16 && a.dk == D && a.dv == D;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
+    const int units = a.N * a.H * a.seg_count;
+    if (units == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(units, a.mode == MODE_TRANSFER ? 2 : 1);
+    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(a);
+    return cudaGetLastError();
+}
 
 }  // namespace kda

@@ -1,0 +1,60 @@
+"""Host-side logic of the multi-GPU benchmark path, on CPU with gloo (world size 2):
+each rank owns a full batch (weak scaling, no data-path collective); the job's
+time is the max over ranks; the segment token count used by the byte model
+matches the oracle's split."""
+import os
+import socket
+
+import numpy as np
+import torch.multiprocessing as mp
+
+import bench
+import oracle
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    r, w, local = bench.dist_env()
+    d = bench.dist_init(w, "gloo")
+    times = {0: 12.5, 1: 17.25}
+    worst = bench.max_over_ranks(times[r], d)
+    bench.barrier(d)
+    q.put((r, w, local, worst))
+    d.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [g[0] for g in got] == [0, 1]
+    assert all(g[1] == 2 and g[3] == 17.25 for g in got)
+    assert [g[2] for g in got] == [0, 1]
+
+
+def test_single_process_needs_no_group():
+    assert bench.max_over_ranks(3.0, None) == 3.0
+    bench.barrier(None)
+
+
+def test_transfer_token_count_matches_oracle_split():
+    for lengths, S in (([4096], 32), ([8192, 16384, 24576, 32768], 2), ([100, 0, 33], 5), ([7], 1)):
+        cu = np.concatenate([[0], np.cumsum(lengths)])
+        b = oracle.segment_bounds(cu, S)
+        expect = int(sum(b[n, s, 1] - b[n, s, 0] for n in range(len(lengths)) for s in range(S - 1)))
+        assert bench.transfer_tokens(lengths, S) == expect
