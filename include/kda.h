@@ -181,6 +181,34 @@ kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_be
                                   const float *seg_init_states, const int32_t *cu_seqlens,
                                   void *out, float *S_final, int32_t *dev_status, void *stream);
 
+/* Size of the device scratch compiled into the library for
+ * kda_prefill_chunked_noalloc: 64 MiB, held on every GPU that loads it. */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * kda_prefill_chunked for callers that cannot allocate device memory (for
+ * example an inference-engine plugin that may not call cudaMalloc while it
+ * enqueues work, or a host whose device memory is all owned by another
+ * framework's pool).  The source pages have no counterpart to this: it is a
+ * convenience of this library.
+ *
+ * Same arguments and results as kda_prefill_chunked, minus the workspace: the
+ * segment split's workspace comes from a fixed KDA_NOALLOC_SCRATCH_BYTES array
+ * inside the library, and nothing is allocated.  A problem whose workspace
+ * (kda_prefill_workspace_size) exceeds that returns KDA_ERR_WORKSPACE without
+ * launching anything; pass desc->num_segments = 1 (no workspace) or a smaller
+ * split instead.  The first call that needs the scratch on a device looks up
+ * its address there (make that first call before any stream capture).  All
+ * calls on a device share the one array and leave their data in it; nothing
+ * has to be cleared between calls, but calls whose GPU work overlaps (e.g. on
+ * two unordered streams) race on it and give wrong results.
+ */
+kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_desc_t *desc, const void *q,
+                                         const void *k, const void *v, const float *g,
+                                         const float *beta, const float *S0,
+                                         const int32_t *cu_seqlens, void *out, float *S_final,
+                                         int32_t *dev_status, void *stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char *kda_status_string(kda_status_t status);
 

@@ -55,6 +55,8 @@ def lib():
                 [ctypes.c_size_t, _P, _P]
             L.kda_prefill_segments.restype = ctypes.c_int
             L.kda_prefill_segments.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 11
+            L.kda_prefill_chunked_noalloc.restype = ctypes.c_int
+            L.kda_prefill_chunked_noalloc.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 11
             L.kda_decode_step.restype = ctypes.c_int
             L.kda_decode_step.argtypes = [_I] * 5 + [_P] * 8
             L.kda_state_transfer.restype = ctypes.c_int
