@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 PREFILL = "kda_prefill_bf16_h8_t4096_d128"
 DECODE = "kda_decode_b256_h56_d128_x64"
 METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of roofline"
+PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096")
 
 
 def parse():
@@ -43,6 +44,8 @@ def parse():
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--profile", choices=sorted(PROFILE_CASES), default=None,
+                   help="run one small case twice for an ncu capture (no timing, no JSON)")
     return p.parse_args()
 
 
@@ -451,8 +454,37 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0}}), flush=True)
 
 
+def run_profile_case(name):
+    """Workloads sized for ncu: larger than L2 (so DRAM counters mean something)
+    but a few GB on the device at most.  Each runs twice; capture with -s 1 -c 1."""
+    import torch
+    import kimi_delta_attention_18_gb300 as kda
+    from kimi_delta_attention_18_gb300.inputs import make_decode_inputs, make_prefill_inputs
+    dev = torch.device("cuda", 0)
+    if name == "decode":
+        y = make_decode_inputs(256, 56, 128, 128, 1, "bf16", device=dev)
+        S = y["S0"].clone()
+        for _ in range(2):
+            kda.decode_step(y["q"][0], y["k"][0], y["v"][0], y["g"][0], y["beta"][0], S)
+    elif name == "prefill_output_pass":
+        x = make_prefill_inputs([8192], 56, 128, 128, "bf16", device=dev)
+        for _ in range(2):
+            kda.prefill_segments(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                 x["cu_seqlens"], 1)
+    elif name == "prefill_h8_t4096":
+        x = make_prefill_inputs([4096], 8, 128, 128, "bf16", device=dev)
+        for _ in range(2):
+            kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                x["cu_seqlens"])
+    torch.cuda.synchronize()
+    print("profile case done:", name)
+
+
 def main():
     args = parse()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

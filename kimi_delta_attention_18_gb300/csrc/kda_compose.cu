@@ -72,11 +72,87 @@ __global__ void __launch_bounds__(NT) compose_kernel(int Sg, int dk, int dv, con
         }
 }
 
+// dk = 128, dv a multiple of 8, 16-byte aligned arrays: register-tiled form.
+// One CTA per (unit, 8-column block), two threads per state row, each owning a
+// row x 4-column tile of the running state; A_{s+1} is fetched into registers
+// (16 float4 per thread, coalesced) while step s computes, then staged in shared
+// memory with a padded row (conflict-free column walks).
+constexpr int FD = 128, FT = 256, FCB = 8, LAP = FD + 1;
+
+__global__ void __launch_bounds__(FT) compose_fast_kernel(int Sg, int dv, const float *A,
+                                                          const float *B, const float *S0,
+                                                          float *seg_init, float *S_final) {
+    extern __shared__ float smem[];
+    float *As = smem;              // [128][129]
+    float *X = As + FD * LAP;      // [128][8]
+    const int t = threadIdx.x, i = t >> 1, cg = t & 1;
+    const size_t u = blockIdx.x;
+    const int col = blockIdx.y * FCB + 4 * cg;
+    const size_t row_off = (size_t)i * dv + col;
+    const int nsteps = S_final ? Sg : Sg - 1;  // without S_final the last pair is never read
+
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (S0) x = *(const float4 *)(S0 + u * (size_t)FD * dv + row_off);
+    *(float4 *)(X + i * FCB + 4 * cg) = x;
+
+    float4 ar[16];
+    auto fetch = [&](int s) {
+        const float4 *src = (const float4 *)(A + (u * Sg + s) * (size_t)FD * FD);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) ar[m] = src[t + FT * m];
+    };
+    auto stage = [&]() {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int e = t + FT * m, r = e >> 5, c = (e & 31) * 4;
+            float *d = As + r * LAP + c;
+            d[0] = ar[m].x; d[1] = ar[m].y; d[2] = ar[m].z; d[3] = ar[m].w;
+        }
+    };
+    if (nsteps > 0) {
+        fetch(0);
+        stage();
+    }
+    __syncthreads();
+    for (int s = 0; s < Sg; ++s) {
+        if (seg_init) *(float4 *)(seg_init + (u * Sg + s) * (size_t)FD * dv + row_off) = x;
+        if (s >= nsteps) break;
+        if (s + 1 < nsteps) fetch(s + 1);
+        float4 acc = *(const float4 *)(B + (u * Sg + s) * (size_t)FD * dv + row_off);
+        const float *arow = As + i * LAP;
+#pragma unroll 8
+        for (int k = 0; k < FD; ++k) {
+            const float a = arow[k];
+            const float4 xk = *(const float4 *)(X + k * FCB + 4 * cg);
+            acc.x = fmaf(a, xk.x, acc.x); acc.y = fmaf(a, xk.y, acc.y);
+            acc.z = fmaf(a, xk.z, acc.z); acc.w = fmaf(a, xk.w, acc.w);
+        }
+        __syncthreads();  // every read of X and of A_s is done
+        x = acc;
+        *(float4 *)(X + i * FCB + 4 * cg) = x;
+        if (s + 1 < nsteps) stage();
+        __syncthreads();
+    }
+    if (S_final) *(float4 *)(S_final + u * (size_t)FD * dv + row_off) = x;
+}
+
 }  // namespace
 
 cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, const float *B,
                            const float *S0, float *seg_init, float *S_final, cudaStream_t st) {
     if (units == 0 || Sg == 0) return cudaSuccess;
+    auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
+    if (dk == FD && dv % FCB == 0 && al16(A) && al16(B) && al16(S0) && al16(seg_init) &&
+        al16(S_final)) {
+        const size_t fsmem = ((size_t)FD * LAP + (size_t)FD * FCB) * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(compose_fast_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)fsmem);
+        if (e != cudaSuccess) return e;
+        compose_fast_kernel<<<dim3(units, dv / FCB), FT, fsmem, st>>>(Sg, dv, A, B, S0, seg_init,
+                                                                       S_final);
+        return cudaGetLastError();
+    }
     const size_t smem = ((size_t)dk * (dk + 1) + 2 * (size_t)dk * CB) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(compose_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -158,6 +158,17 @@ __device__ void producer_role(const Ctx &x) {
             if (lane < nt) b = p.beta[(size_t)(t0 + lane) * p.H + x.h];
             ((float *)(x.smem + IN_OFF + st * IN_SIZE + IN_B))[lane] = b;
         }
+        if (lane >= nt && lane < C) {
+            // Rows past the end are multiplied by zero weights on the tensor cores, so
+            // they must hold finite numbers: clear them (0 * NaN would be NaN).
+            uint8_t *in = x.smem + IN_OFF + st * IN_SIZE;
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+                ((uint4 *)(in + IN_Q + lane * ROWB))[w] = make_uint4(0, 0, 0, 0);
+                ((uint4 *)(in + IN_K + lane * ROWB))[w] = make_uint4(0, 0, 0, 0);
+                ((uint4 *)(in + IN_V + lane * ROWB))[w] = make_uint4(0, 0, 0, 0);
+            }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(full);  // second arrival: beta is in place
         issued = c + 1;

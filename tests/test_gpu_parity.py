@@ -255,3 +255,23 @@ def test_config4_kcp_matches_sequential_and_oracle_head():
     o_ref, S_ref = _oracle_prefill(x, heads=[h])
     assert rel_err(_np(S_k[:, [h]]), S_ref) <= 2e-2
     assert rel_err(_np(out_k[::step, [h]]), o_ref[::step]) <= 2e-2
+
+
+@pytest.mark.parametrize("nseg", [1, 4, 8])
+def test_partial_last_blocks_on_fresh_stages(nseg):
+    """Segments of one to three blocks whose last block is partial: the rows past
+    the end are weighted by zero on the tensor cores, so they must never carry
+    stale shared-memory contents (0 * NaN = NaN).  Outputs start as NaN so a row
+    left unwritten cannot hide behind a reused buffer."""
+    lengths = [333, 45, 29, 7, 100]
+    x = _gpu_inputs(lengths, 4, 128, 128, "bf16", s0_std=0.5, seed=13, slow_decay=True)
+    o_ref, S_ref = _oracle_prefill(x)
+    for _ in range(2):
+        out = torch.full_like(x["v"], float("nan"))
+        SF = torch.full((len(lengths), 4, 128, 128), float("nan"), device="cuda")
+        kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["cu_seqlens"],
+                            num_segments=nseg, out=out, S_final=SF)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out.float()).all() and torch.isfinite(SF).all()
+        assert rel_err(_np(out), o_ref) <= 2e-2
+        assert rel_err(_np(SF), S_ref) <= 2e-2
