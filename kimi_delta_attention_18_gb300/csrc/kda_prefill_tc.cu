@@ -75,10 +75,11 @@ constexpr int IN_G = IN_V + C * ROWB;          // fp32 [16][128]
 constexpr int IN_B = IN_G + C * 512;           // beta fp32 [16]
 constexpr int IN_SIZE = IN_B + 64;
 constexpr int SC_OFF = IN_OFF + NS * IN_SIZE;  // prep scratch
-constexpr int SC_KH = 0;                       // Kh bf16 [16][136]
-constexpr int SC_KT = SC_KH + C * ROWB;        // Kt bf16 [16][136]
-constexpr int SC_QH = SC_KT + C * ROWB;        // Qh bf16 [16][136]
-constexpr int SC_L = SC_QH + C * ROWB;         // Diag(beta) L fp32 [16][17]
+constexpr int TROW = 48;                       // one channel's 16 positions, bf16, padded
+constexpr int SC_KH = 0;                       // Kh^T bf16 [128 ch][24]
+constexpr int SC_KT = SC_KH + D * TROW;        // Kt^T bf16 [128 ch][24]
+constexpr int SC_QH = SC_KT + D * TROW;        // Qh^T bf16 [128 ch][24]
+constexpr int SC_L = SC_QH + D * TROW;         // Diag(beta) L fp32 [16][17]
 constexpr int SC_T = SC_L + C * 17 * 4;        // T bf16 [16][24]
 constexpr int SC_SIZE = SC_T + C * 48;
 constexpr int BAR_OFF = (SC_OFF + SC_SIZE + 7) & ~7;
@@ -215,9 +216,6 @@ __device__ void prep_role(const Ctx &x) {
     const int g8 = lane >> 2, t4 = lane & 3;
     uint8_t *sc = x.smem + SC_OFF;
     const uint32_t sc_s = x.sbase + SC_OFF;
-    __nv_bfloat16 *Kh = (__nv_bfloat16 *)(sc + SC_KH);
-    __nv_bfloat16 *Kt = (__nv_bfloat16 *)(sc + SC_KT);
-    __nv_bfloat16 *Qh = (__nv_bfloat16 *)(sc + SC_QH);
     float *Lf = (float *)(sc + SC_L);
     __nv_bfloat16 *Tb = (__nv_bfloat16 *)(sc + SC_T);
 
@@ -255,19 +253,31 @@ __device__ void prep_role(const Ctx &x) {
             const float einv = 1.f / eGC;
             float kv[C];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
+            for (int r = 0; r < C; ++r)
                 kv[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_K + r * ROWB))[ch])
                                : 0.f;
-                Kh[r * 136 + ch] = __float2bfloat16_rn(kv[r] * fwd[r]);
-                Kt[r * 136 + ch] = __float2bfloat16_rn(kv[r] * (einv * rev[r]));
-                if (x.want_q) {
-                    const float qr =
-                        r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_Q + r * ROWB))[ch])
-                               : 0.f;
-                    const __nv_bfloat16 qh = __float2bfloat16_rn(qr * fwd[r]);
-                    Qh[r * 136 + ch] = qh;
-                    *(__nv_bfloat16 *)(pp_s + PP_B1 + kmaj_off(16 + r, ch, 2048)) = qh;
-                }
+            // Each operand's 16 positions for this channel, as one 48-byte row.
+            auto put_row = [&](int off, const float (&val)[C]) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(val[2 * e], val[2 * e + 1]);
+                *(uint4 *)(sc + off + ch * TROW) = make_uint4(w[0], w[1], w[2], w[3]);
+                *(uint4 *)(sc + off + ch * TROW + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+            };
+            float tmp[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) tmp[r] = kv[r] * fwd[r];
+            put_row(SC_KH, tmp);
+#pragma unroll
+            for (int r = 0; r < C; ++r) tmp[r] = kv[r] * (einv * rev[r]);
+            put_row(SC_KT, tmp);
+            if (x.want_q) {
+#pragma unroll
+                for (int r = 0; r < C; ++r)
+                    tmp[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_Q + r * ROWB))[ch]) *
+                                          fwd[r]
+                                    : 0.f;
+                put_row(SC_QH, tmp);
             }
             // Kb^T row ch (its 16 positions) as two 16-byte core-matrix rows.
 #pragma unroll
@@ -285,17 +295,22 @@ __device__ void prep_role(const Ctx &x) {
         }
         named_bar_sync(1, N_PREP * 32);
 
-        // ---- intra-block products on tensor cores (mma.sync): L (warp 0), Mq (warp 1)
+        // ---- intra-block products on tensor cores (mma.sync): L (warp 0), Mq (warp 1);
+        //      warps 2-3 meanwhile copy Qh into the [W; Qh] operand's rows 16..31.
         if (pw == 0 || (pw == 1 && x.want_q)) {
             const uint32_t a_base = sc_s + (pw == 0 ? SC_KH : SC_QH);
             float acc[2][4] = {};
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 uint32_t af[4], bf[4];
-                ldsm_x4(a_base + (lane & 15) * ROWB + (kk * 16 + (lane >> 4) * 8) * 2, af);
-                const int brow = (lane & 7) + ((lane >> 4) << 3);
-                const int bcol = kk * 16 + ((lane >> 3) & 1) * 8;
-                ldsm_x4(sc_s + SC_KT + brow * ROWB + bcol * 2, bf);
+                // A (positions x channels) from the channel-major rows, transposed
+                ldsm_x4_t(a_base + (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * TROW +
+                              ((lane >> 3) & 1) * 16,
+                          af);
+                // B (channels x positions) from Kt^T rows, transposed
+                ldsm_x4_t(sc_s + SC_KT + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * TROW +
+                              (lane >> 4) * 16,
+                          bf);
                 mma_bf16_16816(acc[0], af, bf[0], bf[1]);
                 mma_bf16_16816(acc[1], af, bf[2], bf[3]);
             }
@@ -315,6 +330,23 @@ __device__ void prep_role(const Ctx &x) {
                         *(uint32_t *)(pp_s + PP_B2 + kmaj_off(r, i0, 256)) = w;
                     }
                 }
+        } else if (pw >= 2 && x.want_q) {
+            // 256 core-matrix rows: (position r, channel group cg) <- 8 channels of Qh^T
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                const int chunk = (pt - 64) + 64 * q2;
+                const int r = chunk & 15, cg = chunk >> 4;
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat16 *row0 = (const __nv_bfloat16 *)(sc + SC_QH + (8 * cg + 2 * e) * TROW);
+                    const __nv_bfloat16 *row1 = (const __nv_bfloat16 *)(sc + SC_QH + (8 * cg + 2 * e + 1) * TROW);
+                    w[e] = (uint32_t)__bfloat16_as_ushort(row0[r]) |
+                           ((uint32_t)__bfloat16_as_ushort(row1[r]) << 16);
+                }
+                *(uint4 *)(pp_s + PP_B1 + kmaj_off(16 + r, 8 * cg, 2048)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
         named_bar_sync(1, N_PREP * 32);
 
@@ -349,7 +381,10 @@ __device__ void prep_role(const Ctx &x) {
             for (int np = 0; np < 2; ++np) {
                 const int n0 = 32 * pw + 16 * np;
                 uint32_t bf[4];
-                ldsm_x4_t(sc_s + SC_KH + (lane & 15) * ROWB + (n0 + (lane >> 4) * 8) * 2, bf);
+                // B (positions x channels) = Kh, stored channel-major: plain ldmatrix
+                ldsm_x4(sc_s + SC_KH + (n0 + (lane & 7) + ((lane >> 4) << 3)) * TROW +
+                            ((lane >> 3) & 1) * 16,
+                        bf);
                 float w0[4] = {}, w1[4] = {};
                 mma_bf16_16816(w0, af, bf[0], bf[1]);
                 mma_bf16_16816(w1, af, bf[2], bf[3]);
