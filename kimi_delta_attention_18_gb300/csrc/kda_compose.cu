@@ -96,10 +96,12 @@ __global__ void __launch_bounds__(FT) compose_fast_kernel(int Sg, int dv, const 
     *(float4 *)(X + i * FCB + 4 * cg) = x;
 
     float4 ar[16];
-    auto fetch = [&](int s) {
+    float4 bnext = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto fetch = [&](int s) {  // A_s (whole, coalesced) and this thread's tile of B_s
         const float4 *src = (const float4 *)(A + (u * Sg + s) * (size_t)FD * FD);
 #pragma unroll
         for (int m = 0; m < 16; ++m) ar[m] = src[t + FT * m];
+        bnext = *(const float4 *)(B + (u * Sg + s) * (size_t)FD * dv + row_off);
     };
     auto stage = [&]() {
 #pragma unroll
@@ -109,16 +111,18 @@ __global__ void __launch_bounds__(FT) compose_fast_kernel(int Sg, int dv, const 
             d[0] = ar[m].x; d[1] = ar[m].y; d[2] = ar[m].z; d[3] = ar[m].w;
         }
     };
+    float4 bcur = make_float4(0.f, 0.f, 0.f, 0.f);
     if (nsteps > 0) {
         fetch(0);
         stage();
+        bcur = bnext;
     }
     __syncthreads();
     for (int s = 0; s < Sg; ++s) {
         if (seg_init) *(float4 *)(seg_init + (u * Sg + s) * (size_t)FD * dv + row_off) = x;
         if (s >= nsteps) break;
-        if (s + 1 < nsteps) fetch(s + 1);
-        float4 acc = *(const float4 *)(B + (u * Sg + s) * (size_t)FD * dv + row_off);
+        if (s + 1 < nsteps) fetch(s + 1);  // in flight during the product below
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         const float *arow = As + i * LAP;
 #pragma unroll 8
         for (int k = 0; k < FD; ++k) {
@@ -127,10 +131,14 @@ __global__ void __launch_bounds__(FT) compose_fast_kernel(int Sg, int dv, const 
             acc.x = fmaf(a, xk.x, acc.x); acc.y = fmaf(a, xk.y, acc.y);
             acc.z = fmaf(a, xk.z, acc.z); acc.w = fmaf(a, xk.w, acc.w);
         }
+        acc.x += bcur.x; acc.y += bcur.y; acc.z += bcur.z; acc.w += bcur.w;
         __syncthreads();  // every read of X and of A_s is done
         x = acc;
         *(float4 *)(X + i * FCB + 4 * cg) = x;
-        if (s + 1 < nsteps) stage();
+        if (s + 1 < nsteps) {
+            stage();
+            bcur = bnext;
+        }
         __syncthreads();
     }
     if (S_final) *(float4 *)(S_final + u * (size_t)FD * dv + row_off) = x;

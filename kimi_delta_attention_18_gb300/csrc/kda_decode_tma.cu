@@ -80,8 +80,13 @@ __global__ void __launch_bounds__(NT, 1) decode_tma_kernel(int units, const TA *
         // ---------------- producer
         int i = 0;
         int issued = 0;
+        // beta is one scalar per state: load the next one a step ahead so its
+        // latency overlaps the wait for a free stage.
+        float beta_next = (lane == 0 && (int)blockIdx.x < units) ? beta[blockIdx.x] : 0.f;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
             const int st = i % NSTG;
+            const float beta_cur = beta_next;
+            if (lane == 0 && u + (int)gridDim.x < units) beta_next = beta[u + gridDim.x];
             int ok = 1;
             if (lane == 0) ok = mbar_wait(empty(st), ((i / NSTG) & 1) ^ 1, abort, kWaitLimit);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -93,7 +98,7 @@ __global__ void __launch_bounds__(NT, 1) decode_tma_kernel(int units, const TA *
                 bulk_g2s(base + L::K, k + (size_t)u * D, L::VEC, full(st));
                 bulk_g2s(base + L::V, v + (size_t)u * D, L::VEC, full(st));
                 bulk_g2s(base + L::G, g + (size_t)u * D, 512, full(st));
-                *(float *)(sm + st * L::STAGE + L::BETA) = beta[u];
+                *(float *)(sm + st * L::STAGE + L::BETA) = beta_cur;
                 mbar_arrive(full(st));
             }
             __syncwarp();

@@ -14,7 +14,8 @@
 // The digest's FlashKDA overlaps the intra-block work with the cross-block state
 // propagation (section 2.4 (1)); here that is warp specialisation inside one CTA:
 //
-//   warp 0      producer: bulk copies (TMA engine) of each block's q/k/v/g rows
+//   warp 0      producer: one 2D tensor-map TMA copy per array per block (q, k, v:
+//               16 x 128 BF16 boxes; g: 16 x 128 fp32), beta by prefetched loads
 //   warp 1      issues tcgen05.mma (one thread); owns the TMEM allocation
 //   warps 2-5   prep of block c+1 (CUDA cores + mma.sync for the 16x16 products)
 //   warps 6-13  state: fp32 master state S in registers (lane = dv column j,
@@ -33,6 +34,10 @@
 // Every wait is bounded: a stalled barrier sets an abort flag, records
 // KDA_ERR_TIMEOUT in dev_status, and all roles leave their loops, free TMEM and
 // return.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -54,7 +59,6 @@ constexpr uint32_t D3_COL = 0;    // 128 columns: U^T Kb
 constexpr uint32_t D1_COL = 128;  // 2 x 32 columns: [W S | Qh S + Mq U]^T, double-buffered
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-constexpr int ROWB = 272;  // one 128-element bf16 row padded to 136 elements
 // UMMA operands (canonical K-major, no swizzle: 8x16-byte core matrices,
 // LBO = 128 bytes between core matrices along K, SBO between 8-row groups).
 constexpr int SA_OFF = 0;                    // S^T  [j 128][i 128]  SBO 2048   32 KB
@@ -67,13 +71,14 @@ constexpr int UT_LD = 132;                   // Ut fp32 row stride (floats)
 constexpr int PP_UT = PP_B3 + 4096;          // Ut   fp32 [16][132]
 constexpr int PP_DECAY = PP_UT + C * UT_LD * 4;  // exp(Gamma_C) fp32 [128]
 constexpr int PP_SIZE = PP_DECAY + 512;
-constexpr int IN_OFF = PP_OFF + NP * PP_SIZE;  // input stages
-constexpr int IN_Q = 0;                        // bf16 rows, 272-byte stride
-constexpr int IN_K = IN_Q + C * ROWB;
-constexpr int IN_V = IN_K + C * ROWB;
-constexpr int IN_G = IN_V + C * ROWB;          // fp32 [16][128]
+constexpr int IN_OFF = PP_OFF + NP * PP_SIZE;  // input stages (TMA boxes, dense rows)
+constexpr int IN_ROWB = 256;                   // one 128-element bf16 row
+constexpr int IN_Q = 0;                        // bf16 [16][128]
+constexpr int IN_K = IN_Q + C * IN_ROWB;
+constexpr int IN_V = IN_K + C * IN_ROWB;
+constexpr int IN_G = IN_V + C * IN_ROWB;       // fp32 [16][128]
 constexpr int IN_B = IN_G + C * 512;           // beta fp32 [16]
-constexpr int IN_SIZE = IN_B + 64;
+constexpr int IN_SIZE = (IN_B + 64 + 127) & ~127;
 constexpr int SC_OFF = IN_OFF + NS * IN_SIZE;  // prep scratch
 constexpr int TROW = 48;                       // one channel's 16 positions, bf16, padded
 constexpr int SC_KH = 0;                       // Kh^T bf16 [128 ch][24]
@@ -98,7 +103,7 @@ constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // [0] TMEM base, [1] abort, [2] 
 constexpr int SMEM_USED = MISC_OFF + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 
-static_assert(PP_SIZE % 128 == 0 && IN_SIZE % 16 == 0, "stage alignment");
+static_assert(PP_SIZE % 128 == 0 && IN_SIZE % 128 == 0 && PP_OFF % 128 == 0, "stage alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 // Byte offset of element (row, k) in a canonical no-swizzle K-major operand.
@@ -108,6 +113,7 @@ __device__ __forceinline__ uint32_t kmaj_off(int row, int k, int sbo) {
 
 struct Ctx {
     const PrefillArgs *p;
+    uint64_t tm_q, tm_k, tm_v, tm_g;  // generic addresses of the tensor maps
     uint8_t *smem;
     uint32_t sbase;
     uint32_t tmem;
@@ -133,43 +139,38 @@ __device__ __forceinline__ void report_abort(const Ctx &x) {
 __device__ void producer_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int lane = threadIdx.x & 31;
-    const __nv_bfloat16 *q = (const __nv_bfloat16 *)p.q;
-    const __nv_bfloat16 *k = (const __nv_bfloat16 *)p.k;
-    const __nv_bfloat16 *v = (const __nv_bfloat16 *)p.v;
     int issued = 0;
+    // beta is strided (one value per token at stride H): lane r loads the next
+    // block's value one iteration ahead, so the load's latency overlaps the wait
+    // for a free stage instead of stalling the producer.
+    auto load_beta = [&](int c) {
+        const int t0 = x.t_begin + C * c;
+        return (c < x.nchunks && lane < C && lane < x.t_end - t0)
+                   ? p.beta[(size_t)(t0 + lane) * p.H + x.h]
+                   : 0.f;
+    };
+    float beta_next = load_beta(0);
     for (int c = 0; c < x.nchunks; ++c) {
         const int st = c % NS;
+        const float beta_cur = beta_next;
+        beta_next = load_beta(c + 1);
         if (!warp_wait(x, B_IN_EMPTY + st, ((c / NS) & 1) ^ 1)) break;
         const int t0 = x.t_begin + C * c;
-        const int nt = min(C, x.t_end - t0);
-        const uint32_t row_bytes = (x.want_q ? 256u : 0u) + 256u + (x.want_v ? 256u : 0u) + 512u;
         const uint32_t full = x.bar(B_IN_FULL + st);
         const uint32_t base = x.sbase + IN_OFF + st * IN_SIZE;
-        if (lane == 0) mbar_arrive_expect_tx(full, row_bytes * nt);
-        __syncwarp();
-        if (lane < nt) {
-            const size_t row = (size_t)(t0 + lane) * p.H + x.h;
-            if (x.want_q) bulk_g2s(base + IN_Q + lane * ROWB, q + row * D, 256, full);
-            bulk_g2s(base + IN_K + lane * ROWB, k + row * D, 256, full);
-            if (x.want_v) bulk_g2s(base + IN_V + lane * ROWB, v + row * D, 256, full);
-            bulk_g2s(base + IN_G + lane * 512, p.g + row * D, 512, full);
+        if (lane == 0) {
+            // Whole 16-row boxes: rows past the block's end hold the next sequence's
+            // tokens (masked by the prep warps) or, past the array, zero fill.
+            const uint32_t bytes =
+                (x.want_q ? 4096u : 0u) + 4096u + (x.want_v ? 4096u : 0u) + 8192u;
+            mbar_arrive_expect_tx(full, bytes);
+            const int xc = x.h * D;
+            if (x.want_q) tma_load_2d(base + IN_Q, x.tm_q, xc, t0, full);
+            tma_load_2d(base + IN_K, x.tm_k, xc, t0, full);
+            if (x.want_v) tma_load_2d(base + IN_V, x.tm_v, xc, t0, full);
+            tma_load_2d(base + IN_G, x.tm_g, xc, t0, full);
         }
-        if (lane < C) {
-            float b = 0.f;
-            if (lane < nt) b = p.beta[(size_t)(t0 + lane) * p.H + x.h];
-            ((float *)(x.smem + IN_OFF + st * IN_SIZE + IN_B))[lane] = b;
-        }
-        if (lane >= nt && lane < C) {
-            // Rows past the end are multiplied by zero weights on the tensor cores, so
-            // they must hold finite numbers: clear them (0 * NaN would be NaN).
-            uint8_t *in = x.smem + IN_OFF + st * IN_SIZE;
-#pragma unroll
-            for (int w = 0; w < 16; ++w) {
-                ((uint4 *)(in + IN_Q + lane * ROWB))[w] = make_uint4(0, 0, 0, 0);
-                ((uint4 *)(in + IN_K + lane * ROWB))[w] = make_uint4(0, 0, 0, 0);
-                ((uint4 *)(in + IN_V + lane * ROWB))[w] = make_uint4(0, 0, 0, 0);
-            }
-        }
+        if (lane < C) ((float *)(x.smem + IN_OFF + st * IN_SIZE + IN_B))[lane] = beta_cur;
         __syncwarp();
         if (lane == 0) mbar_arrive(full);  // second arrival: beta is in place
         issued = c + 1;
@@ -188,6 +189,9 @@ __device__ void mma_role(const Ctx &x) {
                    id128 = umma_idesc_bf16(128, 128);
     const uint32_t n1 = x.want_q ? id32 : id16;
     const uint64_t ua = umma_desc(x.sbase + UA_OFF, 128, 256);
+    uint64_t sa_desc[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) sa_desc[kk] = umma_desc(x.sbase + SA_OFF + kk * 256, 128, 2048);
     for (int c = 0; c < x.nchunks; ++c) {
         const int pp = c % NP;
         if (!mbar_wait(x.bar(B_PP_FULL + pp), (c / NP) & 1, x.abort, kWaitLimit)) break;
@@ -197,8 +201,7 @@ __device__ void mma_role(const Ctx &x) {
         const uint32_t pbase = x.sbase + PP_OFF + pp * PP_SIZE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            umma_bf16(d1, umma_desc(x.sbase + SA_OFF + kk * 256, 128, 2048),
-                      umma_desc(pbase + PP_B1 + kk * 256, 128, 2048), n1, kk > 0);
+            umma_bf16(d1, sa_desc[kk], umma_desc(pbase + PP_B1 + kk * 256, 128, 2048), n1, kk > 0);
         umma_commit(x.bar(B_MMA1));
         if (!mbar_wait(x.bar(B_UREADY), c & 1, x.abort, kWaitLimit)) break;
         tc_fence_after();
@@ -254,7 +257,7 @@ __device__ void prep_role(const Ctx &x) {
             float kv[C];
 #pragma unroll
             for (int r = 0; r < C; ++r)
-                kv[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_K + r * ROWB))[ch])
+                kv[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_K + r * IN_ROWB))[ch])
                                : 0.f;
             // Each operand's 16 positions for this channel, as one 48-byte row.
             auto put_row = [&](int off, const float (&val)[C]) {
@@ -274,7 +277,7 @@ __device__ void prep_role(const Ctx &x) {
             if (x.want_q) {
 #pragma unroll
                 for (int r = 0; r < C; ++r)
-                    tmp[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_Q + r * ROWB))[ch]) *
+                    tmp[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_Q + r * IN_ROWB))[ch]) *
                                           fwd[r]
                                     : 0.f;
                 put_row(SC_QH, tmp);
@@ -292,6 +295,12 @@ __device__ void prep_role(const Ctx &x) {
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
             ((float *)(pp_s + PP_DECAY))[ch] = eGC;
+            // V rows past the block's end are weighted by zero on the tensor cores:
+            // make them zero too (the next sequence's values, or anything non-finite
+            // in them, must not leak in through 0 * x).
+            if (x.want_v)
+                for (int r = nt; r < C; ++r)
+                    ((__nv_bfloat16 *)(in + IN_V + r * IN_ROWB))[ch] = __float2bfloat16_rn(0.f);
         }
         named_bar_sync(1, N_PREP * 32);
 
@@ -391,7 +400,7 @@ __device__ void prep_role(const Ctx &x) {
                 float u0[4] = {}, u1[4] = {};
                 if (x.want_v) {
                     uint32_t vf[4];
-                    ldsm_x4_t(x.sbase + IN_OFF + st * IN_SIZE + IN_V + (lane & 15) * ROWB +
+                    ldsm_x4_t(x.sbase + IN_OFF + st * IN_SIZE + IN_V + (lane & 15) * IN_ROWB +
                                   (n0 + (lane >> 4) * 8) * 2,
                               vf);
                     mma_bf16_16816(u0, af, vf[0], vf[1]);
@@ -529,11 +538,19 @@ __device__ void state_role(const Ctx &x) {
     }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const PrefillArgs p) {
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillArgs p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Ctx x;
     x.p = &p;
+    x.tm_q = reinterpret_cast<uint64_t>(&tm_q);
+    x.tm_k = reinterpret_cast<uint64_t>(&tm_k);
+    x.tm_v = reinterpret_cast<uint64_t>(&tm_v);
+    x.tm_g = reinterpret_cast<uint64_t>(&tm_g);
     x.smem = smem;
     x.sbase = smem_addr(smem);
     x.abort = (volatile int *)(smem + MISC_OFF + 4);
@@ -603,14 +620,59 @@ bool prefill_tc_supported(const PrefillArgs &a) {
     return a.act == KDA_DTYPE_BF16 && a.dk == D && a.dv == D;
 }
 
+namespace {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    }
+    return fn;
+}
+
+// [T_tot, H * 128] row-major view of a token-major array, 16 x 128 boxes.
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *ptr, int T,
+                 int H, bool fp32) {
+    const cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * D * (fp32 ? 4 : 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)C};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     const int units = a.N * a.H * a.seg_count;
     if (units == 0) return cudaSuccess;
+    CUtensorMap tq, tk, tv, tg;
+    memset(&tq, 0, sizeof(tq)); memset(&tk, 0, sizeof(tk));
+    memset(&tv, 0, sizeof(tv)); memset(&tg, 0, sizeof(tg));
+    if (a.T_tot > 0) {  // with no tokens no CTA loads anything (and the pointers may be null)
+        PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+        if (!enc) return cudaErrorNotSupported;
+        const void *qp = a.q ? a.q : a.k;  // the transfer pass has no q
+        if (!encode_rows(enc, &tq, qp, a.T_tot, a.H, false) ||
+            !encode_rows(enc, &tk, a.k, a.T_tot, a.H, false) ||
+            !encode_rows(enc, &tv, a.v, a.T_tot, a.H, false) ||
+            !encode_rows(enc, &tg, a.g, a.T_tot, a.H, true))
+            return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(units, a.mode == MODE_TRANSFER ? 2 : 1);
-    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(a);
+    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(a, tq, tk, tv, tg);
     return cudaGetLastError();
 }
 
