@@ -4,8 +4,8 @@ decode tokens/s (256 sequences x 56 heads, 64 single-token steps), with the
 roofline fraction of the dominant kernel.
 
 One step = one whole prefill of the workload through the library's three
-stages (transfer pass over segments 0..S-2, the segment scan, the output pass
-over all segments; a single output pass when the library picks S = 1), each
+stages (transfer pass over all S segments with outputs, the segment scan, the
+output combine; a single output pass when the library picks S = 1), each
 bracketed by CUDA events on the launching stream.  Inputs are resident in HBM;
 the 50 MB working set is smaller than L2, so a 512 MB buffer is rewritten
 between timed steps (outside the events).  ``e2e`` times the one-call C entry
@@ -155,36 +155,27 @@ def measured_peaks():
 # ---------------------------------------------------------------------------
 # algorithmic bytes (what the method must move, per launch)
 # ---------------------------------------------------------------------------
-def prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes, seg_tokens):
+def prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes):
     """Bytes each stage must read and write at minimum.
 
-    output pass : q, k, v, out (activation dtype) + g (fp32) + beta (fp32) per
-                  head-token, plus the start states read and final states written.
-    transfer    : k, v, g, beta for segments 0..S-2, plus A and B written.
-    scan        : A, B read for S-1 segments, start states written.
+    one pass (S = 1): q, k, v, out (activation dtype) + g, beta (fp32) per
+                      head-token, plus the final states.
+    transfer pass   : q, k, v, g, beta read once per head-token; the zero-start
+                      outputs and A_t^T q_t written (activation dtype); A and B
+                      written per (sequence, head, segment).
+    scan            : A, B read, start states and final states written.
+    combine         : A_t^T q_t and the zero-start outputs read, outputs written,
+                      start states read.
     """
-    per_ht = (2 * dk + 2 * dv) * act_bytes + 4 * dk + 4
-    out_pass = T * H * per_ht + N * H * Sg * dk * dv * 4 + N * H * dk * dv * 4
     if Sg == 1:
-        return {"output_pass": out_pass}
-    tr_tokens = seg_tokens
-    transfer = tr_tokens * H * ((dk + dv) * act_bytes + 4 * dk + 4) + \
-        N * H * (Sg - 1) * (dk * dk + dk * dv) * 4
-    scan = N * H * (Sg - 1) * (dk * dk + dk * dv) * 4 + N * H * Sg * dk * dv * 4
-    return {"transfer_pass": transfer, "segment_scan": scan, "output_pass": out_pass}
-
-
-def transfer_tokens(lengths, Sg, chunk=16):
-    """Tokens in segments 0..S-2 (the ones the transfer pass reads), with the
-    library's split: segment s of a sequence of c chunks takes chunks
-    [floor(s c / S), floor((s+1) c / S))."""
-    if Sg <= 1:
-        return 0
-    total = 0
-    for L in lengths:
-        c = -(-L // chunk)
-        total += min(L, ((Sg - 1) * c // Sg) * chunk)
-    return total
+        return {"output_pass": T * H * ((2 * dk + 2 * dv) * act_bytes + 4 * dk + 4) +
+                N * H * dk * dv * 4}
+    states = N * H * Sg * (dk * dk + dk * dv) * 4
+    transfer = T * H * ((2 * dk + dv) * act_bytes + 4 * dk + 4) + \
+        T * H * (dv + dk) * act_bytes + states
+    scan = states + N * H * Sg * dk * dv * 4 + N * H * dk * dv * 4
+    combine = T * H * (dk + 2 * dv) * act_bytes + N * H * Sg * dk * dv * 4
+    return {"transfer_pass": transfer, "segment_scan": scan, "combine": combine}
 
 
 # ---------------------------------------------------------------------------
@@ -219,21 +210,26 @@ def run_ours(args):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    aux = torch.empty((T, H, dk), dtype=x["q"].dtype, device=dev)
+
     def step(ev):
         # exactly the launches kda_prefill_chunked makes, with events between them
         ev[0].record(stream)
         if Sg > 1:
             kda.state_transfer(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], Sg,
-                               seg_begin=0, seg_end=Sg - 1, transfer=A, zero_init_state=B)
+                               transfer=A, zero_init_state=B, q=x["q"], out_zero=out,
+                               out_transfer=aux)
         ev[1].record(stream)
         if Sg > 1:
             kda.state_compose(A.view(N * H, Sg, dk, dk), B.view(N * H, Sg, dk, dv), None,
                               seg_init_states=starts.view(N * H, Sg, dk, dv),
-                              want_final_state=False)
+                              S_final=S_final.view(N * H, dk, dv))
         ev[2].record(stream)
-        kda.prefill_segments(x["q"], x["k"], x["v"], x["g"], x["beta"],
-                             starts if Sg > 1 else None, x["cu_seqlens"], Sg, out=out,
-                             S_final=S_final)
+        if Sg > 1:
+            kda.prefill_combine(out, aux, starts, x["cu_seqlens"], first_segment=1)
+        else:
+            kda.prefill_segments(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                 x["cu_seqlens"], 1, out=out, S_final=S_final)
         ev[3].record(stream)
 
     mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -256,12 +252,12 @@ def run_ours(args):
     barrier(dist)
     clk = clocks.stop()
 
-    stage_ms = {"transfer_pass": [], "segment_scan": [], "output_pass": []}
+    stage_ms = {"transfer_pass": [], "segment_scan": [], "combine": [], "output_pass": []}
     total_ms = []
     for ev in events:
         stage_ms["transfer_pass"].append(ev[0].elapsed_time(ev[1]))
         stage_ms["segment_scan"].append(ev[1].elapsed_time(ev[2]))
-        stage_ms["output_pass"].append(ev[2].elapsed_time(ev[3]))
+        stage_ms["combine" if Sg > 1 else "output_pass"].append(ev[2].elapsed_time(ev[3]))
         total_ms.append(ev[0].elapsed_time(ev[3]))
     dev_ms = sum(total_ms)
     dev_ms_max = max_over_ranks(dev_ms, dist, dev)
@@ -270,8 +266,7 @@ def run_ours(args):
 
     # roofline of the dominant kernel (HBM-bound: see the design notes)
     peaks = measured_peaks()
-    seg_tokens = transfer_tokens(w["lengths"], Sg)
-    sbytes = prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes, seg_tokens)
+    sbytes = prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes)
     means = {k_: statistics.mean(v_) for k_, v_ in stage_ms.items() if k_ in sbytes}
     dom = max(means, key=means.get)
     achieved = sbytes[dom] / (means[dom] / 1e3) / 1e9

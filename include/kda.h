@@ -84,7 +84,8 @@ int32_t kda_prefill_num_segments(const kda_prefill_desc_t *desc);
 /*
  * Device workspace, in bytes, that kda_prefill_chunked needs for desc: zero
  * when it runs one pass, else room for N*H*S transfer matrices, zero-initial
- * states and segment start states (fp32).  Call with the same desc, on the
+ * states and segment start states (fp32) and one dk-vector per token and head
+ * in the activation dtype.  Call with the same desc, on the
  * same device, as the prefill itself.
  */
 size_t kda_prefill_workspace_size(const kda_prefill_desc_t *desc);
@@ -98,9 +99,10 @@ size_t kda_prefill_workspace_size(const kda_prefill_desc_t *desc);
  * ("intra-chunk parallel work"), then a sequential fp32 state step per block
  * ("cross-chunk state propagation"), overlapped as in the digest, section
  * 2.4 (1), FlashKDA.  With S > 1 segments every sequence is also split for
- * parallelism: per segment a transfer matrix and a zero-initial state are
- * computed, scanned, and the segments then run from their true start states
- * (digest 2.4 (1), KCP).  A zero-length sequence gives S_final = S0.
+ * parallelism (digest 2.4 (1), KCP): kda_state_transfer on all S segments with
+ * outputs (the zero-start outputs go straight to out), kda_state_compose (start
+ * states and S_final), then kda_prefill_combine.  A zero-length sequence gives
+ * S_final = S0.
  *
  *   desc            problem description (host pointer).
  *   q, k, v, g, beta, out   device arrays in the layouts above; q, k, v, g and
@@ -141,12 +143,20 @@ kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32
  * Only segments s in [seg_begin, seg_end) are computed (0 <= seg_begin <=
  * seg_end <= S); the other slots are left untouched, so ranks or passes can
  * split the segments between them.  An empty segment gives A = I, B = 0.
- * q is not needed.
+ *
+ * Outputs (optional: q, out_zero and out_transfer all NULL, or all given):
+ * since S_t = A_t start + B_t inside a segment, o_t = B_t^T q_t + start^T (A_t^T
+ * q_t).  The pass then also writes, for every token of those segments,
+ *     out_zero     [T_tot, H, dv]  B_t^T q_t   (the output from a zero start)
+ *     out_transfer [T_tot, H, dk]  A_t^T q_t
+ * in the activation dtype; kda_prefill_combine adds the second term once the
+ * start states are known.
  */
 kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begin,
-                                int32_t seg_end, const void *k, const void *v, const float *g,
-                                const float *beta, const int32_t *cu_seqlens, float *transfer,
-                                float *zero_init_state, int32_t *dev_status, void *stream);
+                                int32_t seg_end, const void *q, const void *k, const void *v,
+                                const float *g, const float *beta, const int32_t *cu_seqlens,
+                                float *transfer, float *zero_init_state, void *out_zero,
+                                void *out_transfer, int32_t *dev_status, void *stream);
 
 /*
  * Prefix scan that joins the segments (digest, section 2.4 (1)): for each of
@@ -165,15 +175,30 @@ kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int3
                                void *stream);
 
 /*
+ * Output correction of the context-parallel split: for every token t of the
+ * segments s in [first_segment, S) (S = desc->num_segments),
+ *     out[t, h, :] += seg_init_states[n, h, s]^T out_transfer[t, h, :]
+ * with seg_init_states [N, H, S, dk, dv] fp32 (from kda_state_compose) and
+ * out_transfer [T_tot, H, dk] (from kda_state_transfer) in the activation
+ * dtype.  out holds the zero-start outputs on entry and the outputs on exit.
+ * first_segment = 1 skips the first segments' correction when they start from
+ * zeros.  A dense product per segment (tensor cores for BF16 at d = 128).
+ */
+kda_status_t kda_prefill_combine(const kda_prefill_desc_t *desc, int32_t first_segment,
+                                 const float *seg_init_states, const void *out_transfer,
+                                 const int32_t *cu_seqlens, void *out, int32_t *dev_status,
+                                 void *stream);
+
+/*
  * Output pass of the context-parallel split: with S = desc->num_segments >= 1
  * (segments as in kda_state_transfer), run segments [seg_begin, seg_end) of
  * every (sequence, head) from their given start states seg_init_states [N, H,
  * S, dk, dv] (as written by kda_state_compose; NULL = zeros), write o_t for
  * those segments' tokens to out and, if S_final != NULL and seg_end == S, the
- * state after the last segment.  kda_prefill_chunked with S > 1 is exactly
- * kda_state_transfer on segments [0, S-1), kda_state_compose with S_final =
- * NULL, then this call on [0, S); with S = 1 and seg_init_states = S0 it is the
- * one-pass prefill.  Arguments otherwise as for kda_prefill_chunked.
+ * state after the last segment.  With S = 1 and seg_init_states = S0 it is the
+ * one-pass prefill; with S > 1 it is the alternative to kda_prefill_combine
+ * (re-running every segment from its start state instead of correcting the
+ * zero-start outputs).  Arguments otherwise as for kda_prefill_chunked.
  */
 kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_begin,
                                   int32_t seg_end, const void *q, const void *k, const void *v,

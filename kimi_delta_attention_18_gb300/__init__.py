@@ -10,6 +10,7 @@ from ._native import (  # noqa: F401
     PrefillDesc,
     decode_step,
     lib,
+    prefill_combine,
     library_path,
     prefill_chunked,
     prefill_desc,
@@ -20,6 +21,6 @@ from ._native import (  # noqa: F401
     state_transfer,
 )
 
-__all__ = ["KDAError", "PrefillDesc", "decode_step", "lib", "library_path", "prefill_chunked",
+__all__ = ["KDAError", "PrefillDesc", "decode_step", "lib", "library_path", "prefill_chunked", "prefill_combine",
            "prefill_desc", "prefill_num_segments", "prefill_segments", "prefill_workspace_size", "state_compose",
            "state_transfer"]

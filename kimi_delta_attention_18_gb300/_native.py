@@ -60,7 +60,9 @@ def lib():
             L.kda_decode_step.restype = ctypes.c_int
             L.kda_decode_step.argtypes = [_I] * 5 + [_P] * 8
             L.kda_state_transfer.restype = ctypes.c_int
-            L.kda_state_transfer.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 9
+            L.kda_state_transfer.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 12
+            L.kda_prefill_combine.restype = ctypes.c_int
+            L.kda_prefill_combine.argtypes = [ctypes.POINTER(PrefillDesc), _I] + [_P] * 6
             L.kda_state_compose.restype = ctypes.c_int
             L.kda_state_compose.argtypes = [_I] * 4 + [_P] * 6
             L.kda_status_string.restype = ctypes.c_char_p
@@ -235,10 +237,13 @@ def decode_step(q, k, v, g, beta, S, *, out=None, stream=None):
 
 
 def state_transfer(k, v, g, beta, cu_seqlens, num_segments, *, seg_begin=0, seg_end=None,
-                   transfer=None, zero_init_state=None, dev_status=None, stream=None):
+                   transfer=None, zero_init_state=None, q=None, out_zero=None,
+                   out_transfer=None, dev_status=None, stream=None):
     """Per (sequence, head, segment) transfer matrix and zero-initial state for
-    segments [seg_begin, seg_end) (see kda_state_transfer in kda.h).  Returns
-    ``(A [N,H,S,dk,dk], B [N,H,S,dk,dv])``; other segments' slots are untouched."""
+    segments [seg_begin, seg_end) (see kda_state_transfer in kda.h).  With q given
+    it also writes the zero-start outputs and A_t^T q_t (allocated if not passed).
+    Returns ``(A [N,H,S,dk,dk], B [N,H,S,dk,dv])``, plus ``(out_zero [T,H,dv],
+    out_transfer [T,H,dk])`` when q is given."""
     dev = k.device
     T, H, dk = k.shape
     dv = v.shape[2]
@@ -258,14 +263,48 @@ def state_transfer(k, v, g, beta, cu_seqlens, num_segments, *, seg_begin=0, seg_
         zero_init_state = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
     _need(transfer, "transfer", torch.float32, (N, H, Sg, dk, dk), dev)
     _need(zero_init_state, "zero_init_state", torch.float32, (N, H, Sg, dk, dv), dev)
+    if q is not None:
+        _need(q, "q", k.dtype, (T, H, dk), dev)
+        if out_zero is None:
+            out_zero = torch.empty((T, H, dv), dtype=k.dtype, device=dev)
+        if out_transfer is None:
+            out_transfer = torch.empty((T, H, dk), dtype=k.dtype, device=dev)
+        _need(out_zero, "out_zero", k.dtype, (T, H, dv), dev)
+        _need(out_transfer, "out_transfer", k.dtype, (T, H, dk), dev)
     desc = _desc(N, T, H, dk, dv, act, Sg)
     seg_end = Sg if seg_end is None else int(seg_end)
-    rc = lib().kda_state_transfer(ctypes.byref(desc), int(seg_begin), seg_end, _ptr(k), _ptr(v),
-                                  _ptr(g), _ptr(beta),
-                                  _ptr(cu_seqlens), _ptr(transfer), _ptr(zero_init_state),
+    rc = lib().kda_state_transfer(ctypes.byref(desc), int(seg_begin), seg_end, _ptr(q), _ptr(k),
+                                  _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), _ptr(transfer),
+                                  _ptr(zero_init_state), _ptr(out_zero), _ptr(out_transfer),
                                   _ptr(dev_status), _stream(stream, dev))
     _check("kda_state_transfer", rc)
+    if q is not None:
+        return transfer, zero_init_state, out_zero, out_transfer
     return transfer, zero_init_state
+
+
+def prefill_combine(out, out_transfer, seg_init_states, cu_seqlens, *, first_segment=0,
+                    dev_status=None, stream=None):
+    """Add start_s^T (A_t^T q_t) to the zero-start outputs in ``out`` (in place),
+    see kda_prefill_combine in kda.h.  Returns ``out``."""
+    dev = out.device
+    T, H, dv = out.shape
+    dk = out_transfer.shape[2]
+    act = _ACT.get(out.dtype)
+    if act is None:
+        raise ValueError("out must be float32 or bfloat16")
+    _need(out, "out", out.dtype, (T, H, dv))
+    _need(out_transfer, "out_transfer", out.dtype, (T, H, dk), dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+    N = cu_seqlens.numel() - 1
+    Sg = seg_init_states.shape[2]
+    _need(seg_init_states, "seg_init_states", torch.float32, (N, H, Sg, dk, dv), dev)
+    desc = _desc(N, T, H, dk, dv, act, Sg)
+    rc = lib().kda_prefill_combine(ctypes.byref(desc), int(first_segment), _ptr(seg_init_states),
+                                   _ptr(out_transfer), _ptr(cu_seqlens), _ptr(out),
+                                   _ptr(dev_status), _stream(stream, dev))
+    _check("kda_prefill_combine", rc)
+    return out
 
 
 def state_compose(transfer, zero_init_state, S0=None, *, seg_init_states=None, S_final=None,

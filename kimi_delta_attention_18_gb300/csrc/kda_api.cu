@@ -53,29 +53,48 @@ PrefillArgs base_args(const kda_prefill_desc_t *d) {
 }
 
 // Segments per sequence when the caller leaves the choice to the library.
-// One pass per (sequence, head) is used when those chains already cover the
-// GPU twice over; otherwise every sequence is split so that the chains fill it,
-// keeping at least 8 blocks (128 tokens) per segment.
+// Every (sequence, head) chain is sequential over its 16-token blocks, so with
+// fewer chains than SMs the sequences are split.  The choice minimises a cost
+// model in units of one block step of one CTA (one CTA per SM):
+//   transfer pass : ceil(2 chains x S / SMs) waves x ceil(blocks / S)
+//   scan          : S steps, each ~1.8 block steps
+//   combine       : a dense correction, ~2 block steps
+//   + ~4 block steps per extra launch;   S = 1: blocks (the longest chain)
+// using the mean sequence length (the lengths live on the device).
 int choose_segments(const kda_prefill_desc_t *d) {
     if (d->num_segments > 0) return d->num_segments;
     const long long chains = (long long)d->num_seqs * d->num_heads;
     if (chains == 0) return 1;
-    const long long want = 2ll * sm_count();
-    if (chains >= want) return 1;
-    const long long avg_chunks = ((long long)d->total_tokens / d->num_seqs + 15) / 16;
-    long long sg = (want + chains - 1) / chains;
-    const long long cap = avg_chunks / 8;
-    if (sg > cap) sg = cap;
-    if (sg > 64) sg = 64;
-    if (sg < 1) sg = 1;
-    return (int)sg;
+    const long long sms = sm_count();
+    if (chains >= sms) return 1;
+    const long long blocks = ((long long)d->total_tokens / d->num_seqs + 15) / 16;
+    double best = (double)blocks;
+    int best_s = 1;
+    for (int S = 2; S <= 64 && S <= blocks; ++S) {
+        const long long per = (blocks + S - 1) / S;
+        const double cost =
+            (double)((2 * chains * S + sms - 1) / sms) * per + 1.8 * S + 2.0 + 8.0;
+        if (cost < best) {
+            best = cost;
+            best_s = S;
+        }
+    }
+    return best_s;
 }
 
+size_t act_bytes(const kda_prefill_desc_t *d) { return d->act_dtype == KDA_DTYPE_BF16 ? 2 : 4; }
+
+// Split workspace: transfer matrices, zero-initial states and start states for
+// every (sequence, head, segment) in fp32, then A_t^T q_t for every token
+// (activation dtype), each piece starting on a 256-byte boundary.
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t workspace_bytes_for(const kda_prefill_desc_t *d, int Sg) {
     if (Sg <= 1) return 0;
     const size_t units = (size_t)d->num_seqs * d->num_heads * Sg;
-    const size_t per = (size_t)d->dk * d->dk + 2 * (size_t)d->dk * d->dv;
-    return units * per * sizeof(float);
+    const size_t states = round256(units * ((size_t)d->dk * d->dk + 2 * (size_t)d->dk * d->dv) *
+                                   sizeof(float));
+    const size_t aux = round256((size_t)d->total_tokens * d->num_heads * d->dk * act_bytes(d));
+    return states + aux;
 }
 
 cudaError_t run_prefill_pass(const PrefillArgs &a, cudaStream_t st) {
@@ -134,29 +153,34 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
         return from_cuda(run_prefill_pass(a, st));
     }
 
-    // Context-parallel split: transfer pass on segments 0..Sg-2, scan, then
-    // every segment from its true start state.
+    // Context-parallel split: the transfer pass runs every segment twice (from
+    // the identity and from zeros), writing the zero-start outputs into out and
+    // A_t^T q_t into the workspace; the scan joins the segments (and gives the
+    // final state); the combine adds start_s^T (A_t^T q_t) to every output.
     const size_t units = (size_t)desc->num_seqs * desc->num_heads;
     float *A = (float *)workspace;
     float *B = A + units * Sg * desc->dk * desc->dk;
     float *starts = B + units * Sg * desc->dk * desc->dv;
+    void *aux = (uint8_t *)workspace +
+                round256(units * Sg * ((size_t)desc->dk * desc->dk + 2 * (size_t)desc->dk * desc->dv) *
+                         sizeof(float));
 
     PrefillArgs t = a;
     t.mode = MODE_TRANSFER;
     t.seg_begin = 0;
-    t.seg_count = Sg - 1;
+    t.seg_count = Sg;
     t.transfer = A;
     t.zero_state = B;
-    t.out = nullptr;
+    t.emit_out = 1;
+    t.aux_out = aux;
     t.S_final = nullptr;
     cudaError_t e = run_prefill_pass(t, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = launch_compose((int)units, Sg, desc->dk, desc->dv, A, B, S0, starts, nullptr, st);
+    e = launch_compose((int)units, Sg, desc->dk, desc->dv, A, B, S0, starts, S_final, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    a.mode = MODE_OUTPUT;
-    a.seg_count = Sg;
-    a.seg_init = starts;
-    return from_cuda(run_prefill_pass(a, st));
+    PrefillArgs c = a;
+    c.seg_begin = S0 ? 0 : 1;  // from zeros the first segment needs no correction
+    return from_cuda(launch_combine(c, starts, aux, st));
 }
 
 kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_begin,
@@ -191,6 +215,28 @@ kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_be
     return from_cuda(run_prefill_pass(a, (cudaStream_t)stream));
 }
 
+kda_status_t kda_prefill_combine(const kda_prefill_desc_t *desc, int32_t first_segment,
+                                 const float *seg_init_states, const void *out_transfer,
+                                 const int32_t *cu_seqlens, void *out, int32_t *dev_status,
+                                 void *stream) {
+    kda_status_t rc = check_desc(desc);
+    if (rc != KDA_OK) return rc;
+    if (desc->num_segments < 1 || first_segment < 0) return KDA_ERR_INVALID_ARG;
+    if (desc->num_seqs == 0 || desc->total_tokens == 0 || first_segment >= desc->num_segments)
+        return KDA_OK;
+    if (!seg_init_states || !out_transfer || !cu_seqlens || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(seg_init_states) || !aligned16(out_transfer) || !aligned16(out) ||
+        !aligned4(cu_seqlens))
+        return KDA_ERR_INVALID_ARG;
+    PrefillArgs c = base_args(desc);
+    c.cu = cu_seqlens;
+    c.out = out;
+    c.dev_status = dev_status;
+    c.Sg = desc->num_segments;
+    c.seg_begin = first_segment;
+    return from_cuda(launch_combine(c, seg_init_states, out_transfer, (cudaStream_t)stream));
+}
+
 kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv,
                              int32_t act_dtype, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, float *S_inout, void *out,
@@ -218,9 +264,10 @@ kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32
 }
 
 kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begin,
-                                int32_t seg_end, const void *k, const void *v, const float *g,
-                                const float *beta, const int32_t *cu_seqlens, float *transfer,
-                                float *zero_init_state, int32_t *dev_status, void *stream) {
+                                int32_t seg_end, const void *q, const void *k, const void *v,
+                                const float *g, const float *beta, const int32_t *cu_seqlens,
+                                float *transfer, float *zero_init_state, void *out_zero,
+                                void *out_transfer, int32_t *dev_status, void *stream) {
     kda_status_t rc = check_desc(desc);
     if (rc != KDA_OK) return rc;
     if (desc->num_segments < 1) return KDA_ERR_INVALID_ARG;
@@ -230,13 +277,19 @@ kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begi
     if (desc->num_seqs == 0) return KDA_OK;
     if (!cu_seqlens || !transfer || !zero_init_state) return KDA_ERR_INVALID_ARG;
     if (desc->total_tokens > 0 && (!k || !v || !g || !beta)) return KDA_ERR_INVALID_ARG;
-    const void *rows[] = {k, v, g};
+    const bool outputs = q || out_zero || out_transfer;
+    if (outputs && (!q || !out_zero || !out_transfer)) return KDA_ERR_INVALID_ARG;
+    const void *rows[] = {q, k, v, g, out_zero, out_transfer};
     for (const void *p : rows)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
     const void *elems[] = {beta, cu_seqlens, transfer, zero_init_state};
     for (const void *p : elems)
         if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
     PrefillArgs t = base_args(desc);
+    t.q = q;
+    t.out = out_zero;
+    t.aux_out = out_transfer;
+    t.emit_out = outputs ? 1 : 0;
     t.k = k; t.v = v; t.g = g; t.beta = beta; t.cu = cu_seqlens; t.dev_status = dev_status;
     t.Sg = desc->num_segments;
     t.seg_begin = seg_begin;

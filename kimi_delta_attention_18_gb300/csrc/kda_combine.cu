@@ -1,0 +1,176 @@
+// Output correction of the context-parallel split.
+//
+// Within segment s of a sequence the state after token t is S_t = A_t start_s +
+// B_t (transfer matrix and zero-initial state so far: Kimi K3 technical-report
+// digest, section 2.4 (1)), so the output is linear in the segment's start state:
+//     o_t = S_t^T q_t = B_t^T q_t + start_s^T (A_t^T q_t).
+// The transfer pass writes the first term into out and A_t^T q_t into aux_out;
+// once the scan has produced start_s, this kernel adds the second term:
+//     out[t, h, :] += start_s^T aux_out[t, h, :]
+// a dense (tokens x dk) x (dk x dv) product per segment, fully parallel.
+//   BF16, dk = dv = 128: mma.sync m16n8k16 (start_s rounded to BF16, fp32
+//       accumulation); one CTA per (sequence, head, segment, 64-token tile).
+//   fp32 (any dk, dv <= 128): CUDA cores, fp32 throughout.
+#include "kda_internal.cuh"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+constexpr int TILE = 64;
+
+// Token range of this CTA's tile within its segment; false if nothing to do.
+__device__ __forceinline__ bool tile_range(const PrefillArgs &p, int u, int tile, int &h,
+                                           int &s, int &t0, int &t1) {
+    const int n = u / (p.H * p.Sg);
+    h = (u / p.Sg) % p.H;
+    s = u % p.Sg;
+    if (s < p.seg_begin) return false;  // segments before seg_begin start from zeros
+    int a, b;
+    if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b)) return false;
+    t0 = a + tile * TILE;
+    t1 = min(b, t0 + TILE);
+    return t0 < t1;
+}
+
+constexpr int SB_LD = 136;  // padded bf16 row (272 bytes)
+
+constexpr int BF16_SMEM = (128 + TILE) * SB_LD * 2;
+
+__global__ void __launch_bounds__(128) combine_bf16_kernel(const __grid_constant__ PrefillArgs p,
+                                                           const float *starts,
+                                                           const __nv_bfloat16 *aux, int tile) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __nv_bfloat16 *Sb = (__nv_bfloat16 *)smem_raw;    // start_s, [i][j]
+    __nv_bfloat16 *Ab = Sb + 128 * SB_LD;              // aux tile, [t][i]
+    int h, s, t0, t1;
+    if (!tile_range(p, blockIdx.x, tile + blockIdx.y, h, s, t0, t1)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t unit = (size_t)(blockIdx.x / p.Sg);  // (n, h)
+    const float *st = starts + (unit * p.Sg + s) * 128 * 128;
+    for (int e = tid; e < 128 * 32; e += 128) {  // 128 rows x 32 float4
+        const int i = e >> 5, c4 = e & 31;
+        const float4 v = *(const float4 *)(st + i * 128 + 4 * c4);
+        uint2 w;
+        w.x = pack_bf16x2(v.x, v.y);
+        w.y = pack_bf16x2(v.z, v.w);
+        *(uint2 *)(Sb + i * SB_LD + 4 * c4) = w;
+    }
+    const int nt = t1 - t0;
+    for (int e = tid; e < TILE * 16; e += 128) {  // 64 rows x 16 x 16 bytes
+        const int r = e >> 4, c8 = e & 15;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (r < nt) w = *(const uint4 *)(aux + ((size_t)(t0 + r) * p.H + h) * 128 + 8 * c8);
+        *(uint4 *)(Ab + r * SB_LD + 8 * c8) = w;
+    }
+    __syncthreads();
+    if (warp * 16 >= nt) return;
+
+    float acc[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    const uint32_t ab = smem_addr(Ab), sbb = smem_addr(Sb);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t af[4];
+        ldsm_x4(ab + ((warp * 16 + (lane & 15)) * SB_LD + kk * 16 + (lane >> 4) * 8) * 2, af);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t bf[4];
+            ldsm_x4_t(sbb + ((kk * 16 + (lane & 15)) * SB_LD + np * 16 + (lane >> 4) * 8) * 2, bf);
+            mma_bf16_16816(acc[2 * np], af, bf[0], bf[1]);
+            mma_bf16_16816(acc[2 * np + 1], af, bf[2], bf[3]);
+        }
+    }
+    __nv_bfloat16 *out = (__nv_bfloat16 *)p.out;
+    const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int r = warp * 16 + g8 + 8 * hh;
+            if (r >= nt) continue;
+            __nv_bfloat162 *o =
+                (__nv_bfloat162 *)(out + ((size_t)(t0 + r) * p.H + h) * 128 + n * 8 + 2 * t4);
+            const float2 cur = __bfloat1622float2(*o);
+            *o = __floats2bfloat162_rn(cur.x + acc[n][2 * hh], cur.y + acc[n][2 * hh + 1]);
+        }
+}
+
+template <typename TA>
+__global__ void __launch_bounds__(256) combine_simt_kernel(const __grid_constant__ PrefillArgs p,
+                                                           const float *starts, const TA *aux,
+                                                           int tile) {
+    extern __shared__ float sm[];
+    const int dk = p.dk, dv = p.dv;
+    float *Ss = sm;             // [dk][dv]
+    float *As = sm + dk * dv;   // [TILE][dk]
+    int h, s, t0, t1;
+    if (!tile_range(p, blockIdx.x, tile + blockIdx.y, h, s, t0, t1)) return;
+    const size_t unit = (size_t)(blockIdx.x / p.Sg);
+    const float *st = starts + (unit * p.Sg + s) * (size_t)dk * dv;
+    for (int e = threadIdx.x; e < dk * dv; e += 256) Ss[e] = st[e];
+    const int nt = t1 - t0;
+    for (int e = threadIdx.x; e < nt * dk; e += 256) {
+        const int r = e / dk, i = e % dk;
+        As[e] = act_ld(aux, ((size_t)(t0 + r) * p.H + h) * dk + i);
+    }
+    __syncthreads();
+    TA *out = (TA *)p.out;
+    for (int e = threadIdx.x; e < nt * dv; e += 256) {
+        const int r = e / dv, j = e % dv;
+        float acc = 0.f;
+        for (int i = 0; i < dk; ++i) acc = fmaf(As[r * dk + i], Ss[i * dv + j], acc);
+        const size_t o = ((size_t)(t0 + r) * p.H + h) * dv + j;
+        act_st(out, o, act_ld(out, o) + acc);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void *aux_out,
+                           cudaStream_t st) {
+    const long long units = (long long)a.N * a.H * a.Sg;
+    if (units == 0 || a.T_tot == 0) return cudaSuccess;
+    // tokens of one segment: at most ceil(ceil(T_tot / 16) / Sg) blocks of 16
+    const long long blocks = ((long long)a.T_tot + 15) / 16;
+    const long long seg_tokens = 16 * ((blocks + a.Sg - 1) / a.Sg);
+    const long long tiles = (seg_tokens + TILE - 1) / TILE;
+    // grid.y is limited to 65535: launch tile ranges one after another
+    for (long long base = 0; base < tiles; base += 65535) {
+        const unsigned ny = (unsigned)(tiles - base < 65535 ? tiles - base : 65535);
+        dim3 grid((unsigned)units, ny);
+        if (a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128) {
+            cudaError_t e = cudaFuncSetAttribute(combine_bf16_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 BF16_SMEM);
+            if (e != cudaSuccess) return e;
+            combine_bf16_kernel<<<grid, 128, BF16_SMEM, st>>>(
+                a, starts, (const __nv_bfloat16 *)aux_out, (int)base);
+        } else {
+            const size_t smem = ((size_t)a.dk * a.dv + (size_t)TILE * a.dk) * sizeof(float);
+            cudaError_t e;
+            if (a.act == KDA_DTYPE_F32) {
+                e = cudaFuncSetAttribute(combine_simt_kernel<float>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                if (e != cudaSuccess) return e;
+                combine_simt_kernel<float><<<grid, 256, smem, st>>>(a, starts,
+                                                                    (const float *)aux_out,
+                                                                    (int)base);
+            } else {
+                e = cudaFuncSetAttribute(combine_simt_kernel<__nv_bfloat16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                if (e != cudaSuccess) return e;
+                combine_simt_kernel<__nv_bfloat16><<<grid, 256, smem, st>>>(
+                    a, starts, (const __nv_bfloat16 *)aux_out, (int)base);
+            }
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -122,16 +122,22 @@ __global__ void __launch_bounds__(FT) compose_fast_kernel(int Sg, int dv, const 
         if (seg_init) *(float4 *)(seg_init + (u * Sg + s) * (size_t)FD * dv + row_off) = x;
         if (s >= nsteps) break;
         if (s + 1 < nsteps) fetch(s + 1);  // in flight during the product below
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // two independent accumulation chains (even / odd k) halve the FMA latency chain
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
         const float *arow = As + i * LAP;
 #pragma unroll 8
-        for (int k = 0; k < FD; ++k) {
-            const float a = arow[k];
-            const float4 xk = *(const float4 *)(X + k * FCB + 4 * cg);
-            acc.x = fmaf(a, xk.x, acc.x); acc.y = fmaf(a, xk.y, acc.y);
-            acc.z = fmaf(a, xk.z, acc.z); acc.w = fmaf(a, xk.w, acc.w);
+        for (int k = 0; k < FD; k += 2) {
+            const float ae = arow[k], ao = arow[k + 1];
+            const float4 xe = *(const float4 *)(X + k * FCB + 4 * cg);
+            const float4 xo = *(const float4 *)(X + (k + 1) * FCB + 4 * cg);
+            a0.x = fmaf(ae, xe.x, a0.x); a0.y = fmaf(ae, xe.y, a0.y);
+            a0.z = fmaf(ae, xe.z, a0.z); a0.w = fmaf(ae, xe.w, a0.w);
+            a1.x = fmaf(ao, xo.x, a1.x); a1.y = fmaf(ao, xo.y, a1.y);
+            a1.z = fmaf(ao, xo.z, a1.z); a1.w = fmaf(ao, xo.w, a1.w);
         }
-        acc.x += bcur.x; acc.y += bcur.y; acc.z += bcur.z; acc.w += bcur.w;
+        float4 acc;
+        acc.x = a0.x + a1.x + bcur.x; acc.y = a0.y + a1.y + bcur.y;
+        acc.z = a0.z + a1.z + bcur.z; acc.w = a0.w + a1.w + bcur.w;
         __syncthreads();  // every read of X and of A_s is done
         x = acc;
         *(float4 *)(X + i * FCB + 4 * cg) = x;

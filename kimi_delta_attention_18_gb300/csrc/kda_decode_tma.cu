@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(NT, 1) decode_tma_kernel(int units, const TA *
         for (int m = 0; m < 16; ++m) {
             const int row = rg + 8 * m;
             x[m] = *(const float4 *)(Ss + row * D + 4 * c4);
-            const float a = expf(gs[row]), kr = act_ld(ks, row), qr = act_ld(qs, row);
+            const float a = __expf(gs[row]), kr = act_ld(ks, row), qr = act_ld(qs, row);
             x[m].x *= a; x[m].y *= a; x[m].z *= a; x[m].w *= a;
             r.x += kr * x[m].x; r.y += kr * x[m].y; r.z += kr * x[m].z; r.w += kr * x[m].w;
             p.x += qr * x[m].x; p.y += qr * x[m].y; p.z += qr * x[m].z; p.w += qr * x[m].w;

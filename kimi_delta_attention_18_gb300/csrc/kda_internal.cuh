@@ -61,6 +61,11 @@ struct PrefillArgs {
     float *S_final;         // [N,H,dk,dv] or null; written by segment Sg-1
     float *transfer;        // [N,H,Sg,dk,dk]                       (MODE_TRANSFER)
     float *zero_state;      // [N,H,Sg,dk,dv]                       (MODE_TRANSFER)
+    // MODE_TRANSFER with emit_out: the zero-start chain writes its outputs to
+    // `out` [T,H,dv], the identity-start chain writes A_t^T q_t to `aux_out`
+    // [T,H,dk] (both in the activation dtype); q is then required.
+    void *aux_out;
+    int emit_out;
     int32_t *dev_status;
     int N, T_tot, H, dk, dv;
     int Sg;                 // segments per sequence (layout and bounds)
@@ -80,6 +85,8 @@ bool decode_tma_supported(int dk, int dv);
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,
                               const void *v, const float *g, const float *beta, float *S,
                               void *out, cudaStream_t st);
+cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void *aux_out,
+                           cudaStream_t st);
 cudaError_t launch_decode(int batch, int H, int dk, int dv, int act, const void *q,
                           const void *k, const void *v, const float *g, const float *beta,
                           float *S, void *out, cudaStream_t st);

@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs p, int cb,
     const int h = (u / p.seg_count) % H;
     const int s = p.seg_begin + u % p.seg_count;
     const bool transfer = p.mode == MODE_TRANSFER;
+    const bool want_out = !transfer || p.emit_out;
     const bool partA = transfer && (int)blockIdx.y < ncb_a;
     const int b = partA ? (int)blockIdx.y : (int)blockIdx.y - ncb_a;
     const int c0 = b * cb;
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs p, int cb,
                 const size_t ix = ((size_t)(t0 + r) * H + h) * dk + i;
                 G += ok ? p.g[ix] : 0.f;
                 const float kr = ok ? act_ld(k, ix) : 0.f;
-                const float qr = (ok && !transfer) ? act_ld(q, ix) : 0.f;
+                const float qr = (ok && want_out) ? act_ld(q, ix) : 0.f;
                 const float eG = expf(G), eN = expf(-G);
                 sm.Kh[r * LD + i] = kr * eG;
                 sm.Kt[r * LD + i] = kr * eN;
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs p, int cb,
                 for (int c = 0; c < dk; ++c) l += sm.Kh[r * LD + c] * sm.Kt[i * LD + c];
                 l *= sm.bs[r];
             }
-            if (!transfer && r >= i)
+            if (want_out && r >= i)
                 for (int c = 0; c < dk; ++c) m += sm.Qh[r * LD + c] * sm.Kt[i * LD + c];
             sm.L[r * (C + 1) + i] = l;
             sm.Mq[r * (C + 1) + i] = m;
@@ -177,16 +178,17 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs p, int cb,
         }
         __syncthreads();
 
-        // 6. O = Qh S + Mq U
-        if (!transfer) {
-            TA *out = (TA *)p.out;
+        // 6. O = Qh S + Mq U (the identity-start chain's columns are dk wide)
+        if (want_out) {
+            TA *out = (TA *)(partA ? p.aux_out : p.out);
+            const int ow = partA ? dk : dv;
             for (int e = tid; e < nt * cb; e += NT) {
                 const int r = e / cb, c = e % cb;
                 if (c >= nc) continue;
                 float acc = 0.f;
                 for (int i = 0; i < dk; ++i) acc += sm.Qh[r * LD + i] * sm.S[i * cb + c];
                 for (int m = 0; m <= r; ++m) acc += sm.Mq[r * (C + 1) + m] * sm.U[m * cb + c];
-                act_st(out, ((size_t)(t0 + r) * H + h) * dv + c0 + c, acc);
+                act_st(out, ((size_t)(t0 + r) * H + h) * ow + c0 + c, acc);
             }
             __syncthreads();
         }

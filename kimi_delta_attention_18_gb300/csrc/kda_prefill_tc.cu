@@ -49,7 +49,7 @@ using namespace sm100;
 constexpr int C = 16;   // tokens per block
 constexpr int D = 128;  // dk = dv
 constexpr int NS = 3;   // input stages in flight
-constexpr int NP = 2;   // prepared-operand stages
+constexpr int NP = 3;   // prepared-operand stages
 constexpr int W_PROD = 0, W_MMA = 1, W_PREP0 = 2, N_PREP = 4, W_STATE0 = 6, N_STATE = 8;
 constexpr int NWARPS = W_STATE0 + N_STATE;
 constexpr int NTHREADS = NWARPS * 32;
@@ -244,7 +244,7 @@ __device__ void prep_role(const Ctx &x) {
             const int ch = pt;
             float alpha[C];
 #pragma unroll
-            for (int r = 0; r < C; ++r) alpha[r] = r < nt ? expf(gin[r * D + ch]) : 1.f;
+            for (int r = 0; r < C; ++r) alpha[r] = r < nt ? __expf(gin[r * D + ch]) : 1.f;
             float fwd[C], rev[C];  // e^{Gamma_r}, e^{Gamma_C - Gamma_r}
             float a = 1.f;
 #pragma unroll
@@ -472,7 +472,9 @@ __device__ void state_role(const Ctx &x) {
     __syncwarp();
     if (lane == 0) mbar_arrive(x.bar(B_SREADY));
 
-    __nv_bfloat16 *out = (__nv_bfloat16 *)p.out;
+    // output destination: the prefill's out, or in the transfer pass the zero-start
+    // chain's outputs (out) and the identity-start chain's A_t^T q_t (aux_out)
+    __nv_bfloat16 *out = (__nv_bfloat16 *)(x.partA ? p.aux_out : p.out);
     for (int c = 0; c < x.nchunks; ++c) {
         const int pp = c % NP;
         const uint8_t *pp_s = x.smem + PP_OFF + pp * PP_SIZE;
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     x.s = p.seg_begin + u % p.seg_count;
     x.transfer = p.mode == MODE_TRANSFER;
     x.partA = x.transfer && blockIdx.y == 0;
-    x.want_q = !x.transfer;
+    x.want_q = !x.transfer || p.emit_out;
     x.want_v = !x.partA;
     if (!segment_range(p.cu, x.n, p.N, p.T_tot, x.s, p.Sg, p.dev_status, x.t_begin, x.t_end))
         return;

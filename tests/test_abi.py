@@ -81,7 +81,9 @@ def test_prefill_rejects_null_and_misaligned_pointers():
 def test_prefill_split_requires_workspace():
     d = _desc(num_segments=4)
     need = kda.prefill_workspace_size(d)
-    assert need == 1 * 2 * 4 * (16 * 16 + 2 * 16 * 16) * 4
+    r256 = lambda b: (b + 255) // 256 * 256
+    # (A, B, start) per (seq, head, segment) in fp32 + one dk-vector per token and head
+    assert need == r256(1 * 2 * 4 * (16 * 16 + 2 * 16 * 16) * 4) + r256(64 * 2 * 16 * 4)
     assert _prefill(d) == WORKSPACE
     assert _prefill(d, ws=0x40000, ws_len=need - 1) == WORKSPACE
     assert _prefill(d, ws=0x40008, ws_len=need) == WORKSPACE  # misaligned workspace
@@ -119,13 +121,21 @@ def test_decode_and_compose_host_checks():
     assert L.kda_state_compose(2, 3, 16, 16, None, p, None, None, None, None) == INVALID
     assert L.kda_state_compose(0, 3, 16, 16, None, None, None, None, None, None) == OK
     d = _desc(num_segments=0)
-    assert L.kda_state_transfer(ctypes.byref(d), 0, 1, p, p, p, p, p, p, p, None, None) == INVALID
+    assert L.kda_state_transfer(ctypes.byref(d), 0, 1, None, p, p, p, p, p, p, p, None, None, None,
+                                None) == INVALID
     assert L.kda_prefill_segments(ctypes.byref(d), 0, 1, p, p, p, p, p, None, p, p, None, None,
                                   None) == INVALID
     d = _desc(num_segments=4)
     for a, b in ((-1, 2), (3, 2), (0, 5)):
-        assert L.kda_state_transfer(ctypes.byref(d), a, b, p, p, p, p, p, p, p, None,
-                                    None) == INVALID
+        assert L.kda_state_transfer(ctypes.byref(d), a, b, None, p, p, p, p, p, p, p, None, None,
+                                    None, None) == INVALID
         assert L.kda_prefill_segments(ctypes.byref(d), a, b, p, p, p, p, p, None, p, p, None,
                                       None, None) == INVALID
-    assert L.kda_state_transfer(ctypes.byref(d), 2, 2, p, p, p, p, p, p, p, None, None) == OK
+    assert L.kda_state_transfer(ctypes.byref(d), 2, 2, None, p, p, p, p, p, p, p, None, None, None,
+                                None) == OK
+    # outputs need q, out_zero and out_transfer together
+    assert L.kda_state_transfer(ctypes.byref(d), 0, 4, p, p, p, p, p, p, p, p, p, None, None,
+                                None) == INVALID
+    assert L.kda_prefill_combine(ctypes.byref(d), -1, p, p, p, p, None, None) == INVALID
+    assert L.kda_prefill_combine(ctypes.byref(d), 0, None, p, p, p, None, None) == INVALID
+    assert L.kda_prefill_combine(ctypes.byref(d), 4, None, None, None, None, None, None) == OK

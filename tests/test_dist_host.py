@@ -1,15 +1,12 @@
 """Host-side logic of the multi-GPU benchmark path, on CPU with gloo (world size 2):
 each rank owns a full batch (weak scaling, no data-path collective); the job's
-time is the max over ranks; the segment token count used by the byte model
-matches the oracle's split."""
+time is the max over ranks."""
 import os
 import socket
 
-import numpy as np
 import torch.multiprocessing as mp
 
 import bench
-import oracle
 
 
 def _free_port():
@@ -50,11 +47,3 @@ def test_two_rank_max_over_ranks_gloo():
 def test_single_process_needs_no_group():
     assert bench.max_over_ranks(3.0, None) == 3.0
     bench.barrier(None)
-
-
-def test_transfer_token_count_matches_oracle_split():
-    for lengths, S in (([4096], 32), ([8192, 16384, 24576, 32768], 2), ([100, 0, 33], 5), ([7], 1)):
-        cu = np.concatenate([[0], np.cumsum(lengths)])
-        b = oracle.segment_bounds(cu, S)
-        expect = int(sum(b[n, s, 1] - b[n, s, 0] for n in range(len(lengths)) for s in range(S - 1)))
-        assert bench.transfer_tokens(lengths, S) == expect

@@ -275,3 +275,26 @@ def test_partial_last_blocks_on_fresh_stages(nseg):
         assert torch.isfinite(out.float()).all() and torch.isfinite(SF).all()
         assert rel_err(_np(out), o_ref) <= 2e-2
         assert rel_err(_np(SF), S_ref) <= 2e-2
+
+
+@pytest.mark.parametrize("act,d,first", [("f32", 32, 0), ("bf16", 128, 0), ("bf16", 128, 1)])
+def test_split_stages_with_output_correction(act, d, first):
+    """The split's three stages through their entry points: transfer pass with
+    outputs (zero-start outputs and A_t^T q_t), scan, combine; against the
+    oracle.  first = 1 runs from S0 = 0, so the first segment needs no correction."""
+    lengths = [300, 45, 130]
+    nseg = 5
+    x = _gpu_inputs(lengths, 2, d, d, act, s0_std=None if first else 1.0, seed=15,
+                    slow_decay=True)
+    N, H = len(lengths), 2
+    A, B, out, aux = kda.state_transfer(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], nseg,
+                                        q=x["q"])
+    S0 = None if x["S0"] is None else x["S0"].reshape(N * H, d, d)
+    starts, SF = kda.state_compose(A.reshape(N * H, nseg, d, d), B.reshape(N * H, nseg, d, d), S0)
+    kda.prefill_combine(out, aux, starts.reshape(N, H, nseg, d, d), x["cu_seqlens"],
+                        first_segment=first)
+    torch.cuda.synchronize()
+    o_ref, S_ref = _oracle_prefill(x)
+    tol = TOL[act]
+    assert rel_err(_np(out), o_ref) <= tol
+    assert rel_err(_np(SF).reshape(N, H, d, d), S_ref) <= tol
