@@ -467,6 +467,7 @@ def run_profile_case(name):
             kda.prefill_segments(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                  x["cu_seqlens"], 1)
     elif name == "prefill_h8_t4096":
+        # the benchmark's own workload: transfer pass, scan and combine per call
         x = make_prefill_inputs([4096], 8, 128, 128, "bf16", device=dev)
         for _ in range(2):
             kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None,

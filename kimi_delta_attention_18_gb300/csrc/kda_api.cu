@@ -176,7 +176,8 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     t.S_final = nullptr;
     cudaError_t e = run_prefill_pass(t, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = launch_compose((int)units, Sg, desc->dk, desc->dv, A, B, S0, starts, S_final, st);
+    e = launch_compose((int)units, Sg, desc->dk, desc->dv, A, B, S0, starts, S_final, dev_status,
+                       st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     PrefillArgs c = a;
     c.seg_begin = S0 ? 0 : 1;  // from zeros the first segment needs no correction
@@ -312,7 +313,7 @@ kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int3
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
     return from_cuda(launch_compose(units, segments, dk, dv, transfer, zero_init_state, S0,
-                                    seg_init_states, S_final, (cudaStream_t)stream));
+                                    seg_init_states, S_final, nullptr, (cudaStream_t)stream));
 }
 
 const char *kda_status_string(kda_status_t s) {

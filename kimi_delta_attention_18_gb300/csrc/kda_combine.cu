@@ -50,20 +50,38 @@ __global__ void __launch_bounds__(128) combine_bf16_kernel(const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t unit = (size_t)(blockIdx.x / p.Sg);  // (n, h)
     const float *st = starts + (unit * p.Sg + s) * 128 * 128;
-    for (int e = tid; e < 128 * 32; e += 128) {  // 128 rows x 32 float4
-        const int i = e >> 5, c4 = e & 31;
-        const float4 v = *(const float4 *)(st + i * 128 + 4 * c4);
-        uint2 w;
-        w.x = pack_bf16x2(v.x, v.y);
-        w.y = pack_bf16x2(v.z, v.w);
-        *(uint2 *)(Sb + i * SB_LD + 4 * c4) = w;
+    // Loads are issued in batches (all in flight at once), then converted and stored.
+#pragma unroll 1
+    for (int base = 0; base < 128 * 32; base += 128 * 8) {  // 128 rows x 32 float4
+        float4 v[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int e = base + tid + 128 * b;
+            v[b] = *(const float4 *)(st + (e >> 5) * 128 + 4 * (e & 31));
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int e = base + tid + 128 * b;
+            uint2 w;
+            w.x = pack_bf16x2(v[b].x, v[b].y);
+            w.y = pack_bf16x2(v[b].z, v[b].w);
+            *(uint2 *)(Sb + (e >> 5) * SB_LD + 4 * (e & 31)) = w;
+        }
     }
     const int nt = t1 - t0;
-    for (int e = tid; e < TILE * 16; e += 128) {  // 64 rows x 16 x 16 bytes
-        const int r = e >> 4, c8 = e & 15;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (r < nt) w = *(const uint4 *)(aux + ((size_t)(t0 + r) * p.H + h) * 128 + 8 * c8);
-        *(uint4 *)(Ab + r * SB_LD + 8 * c8) = w;
+    {
+        uint4 w[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {  // 64 rows x 16 chunks of 16 bytes
+            const int e = tid + 128 * b, r = e >> 4, c8 = e & 15;
+            w[b] = r < nt ? *(const uint4 *)(aux + ((size_t)(t0 + r) * p.H + h) * 128 + 8 * c8)
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int e = tid + 128 * b, r = e >> 4, c8 = e & 15;
+            *(uint4 *)(Ab + r * SB_LD + 8 * c8) = w[b];
+        }
     }
     __syncthreads();
     if (warp * 16 >= nt) return;
@@ -87,16 +105,19 @@ __global__ void __launch_bounds__(128) combine_bf16_kernel(const __grid_constant
     __nv_bfloat16 *out = (__nv_bfloat16 *)p.out;
     const int g8 = lane >> 2, t4 = lane & 3;
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
+    for (int hh = 0; hh < 2; ++hh) {
+        const int r = warp * 16 + g8 + 8 * hh;
+        if (r >= nt) continue;
+        __nv_bfloat162 *orow = (__nv_bfloat162 *)(out + ((size_t)(t0 + r) * p.H + h) * 128 + 2 * t4);
+        __nv_bfloat162 cur[16];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = warp * 16 + g8 + 8 * hh;
-            if (r >= nt) continue;
-            __nv_bfloat162 *o =
-                (__nv_bfloat162 *)(out + ((size_t)(t0 + r) * p.H + h) * 128 + n * 8 + 2 * t4);
-            const float2 cur = __bfloat1622float2(*o);
-            *o = __floats2bfloat162_rn(cur.x + acc[n][2 * hh], cur.y + acc[n][2 * hh + 1]);
+        for (int n = 0; n < 16; ++n) cur[n] = orow[4 * n];  // all 16 reads in flight
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            const float2 c = __bfloat1622float2(cur[n]);
+            orow[4 * n] = __floats2bfloat162_rn(c.x + acc[n][2 * hh], c.y + acc[n][2 * hh + 1]);
         }
+    }
 }
 
 template <typename TA>

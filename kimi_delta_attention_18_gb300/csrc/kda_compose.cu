@@ -8,9 +8,12 @@
 // and column blocks run on different SMs with no cross-CTA waiting.  Each step
 // stages A_s (dk x dk) in shared memory with coalesced float4 loads.
 #include "kda_internal.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
+
+using namespace sm100;
 
 constexpr int NT = 256;
 constexpr int CB = 16;  // state columns per CTA
@@ -72,80 +75,110 @@ __global__ void __launch_bounds__(NT) compose_kernel(int Sg, int dk, int dv, con
         }
 }
 
-// dk = 128, dv a multiple of 8, 16-byte aligned arrays: register-tiled form.
-// One CTA per (unit, 8-column block), two threads per state row, each owning a
-// row x 4-column tile of the running state; A_{s+1} is fetched into registers
-// (16 float4 per thread, coalesced) while step s computes, then staged in shared
-// memory with a padded row (conflict-free column walks).
-constexpr int FD = 128, FT = 256, FCB = 8, LAP = FD + 1;
+// dk = 128, dv a multiple of 8, 16-byte aligned arrays.  One CTA per (unit,
+// 8-column block), two threads per state row, each owning a row x 4-column
+// tile of the running state.  A_s arrives by TMA two steps ahead into a
+// double-buffered stage (four 128-row x 32-column fp32 boxes with 128-byte
+// swizzle: the 16-byte chunk c of row i sits at chunk c ^ (i mod 8), so the
+// rows a warp walks in step hit different banks); B_{s+1} is prefetched into
+// registers.  The FMA loop therefore never waits on memory.
+constexpr int FD = 128, FT = 256, FCB = 8;
+constexpr int ABOX = FD * 32 * 4;    // one 128 x 32 fp32 box, 16 KB
+constexpr int ASTAGE = 4 * ABOX;     // A_s, 64 KB
+constexpr int FAST_SMEM = 2 * ASTAGE + FD * FCB * 4 + 64 + 1024;
+constexpr long long kWaitLimit = 4000000000ll;
 
-__global__ void __launch_bounds__(FT) compose_fast_kernel(int Sg, int dv, const float *A,
-                                                          const float *B, const float *S0,
-                                                          float *seg_init, float *S_final) {
-    extern __shared__ float smem[];
-    float *As = smem;              // [128][129]
-    float *X = As + FD * LAP;      // [128][8]
+__global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                         int Sg, int dv, const float *B,
+                                                         const float *S0, float *seg_init,
+                                                         float *S_final, int32_t *dev_status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    float *X = (float *)(sm + 2 * ASTAGE);  // [128][8]
+    uint64_t *bars = (uint64_t *)(sm + 2 * ASTAGE + FD * FCB * 4);
+    volatile int *abort = (volatile int *)(bars + 2);
+    const uint32_t sb = smem_addr(sm), bar0 = smem_addr(&bars[0]), bar1 = smem_addr(&bars[1]);
+    const uint64_t tmap = reinterpret_cast<uint64_t>(&tmA);
     const int t = threadIdx.x, i = t >> 1, cg = t & 1;
     const size_t u = blockIdx.x;
     const int col = blockIdx.y * FCB + 4 * cg;
     const size_t row_off = (size_t)i * dv + col;
     const int nsteps = S_final ? Sg : Sg - 1;  // without S_final the last pair is never read
 
+    auto issue = [&](int s) {  // one thread: A_s into stage s % 2
+        const uint32_t bar = (s & 1) ? bar1 : bar0;
+        mbar_arrive_expect_tx(bar, ASTAGE);
+        const int y = (int)((u * Sg + s) * FD);
+#pragma unroll
+        for (int b4 = 0; b4 < 4; ++b4)
+            tma_load_2d(sb + (s & 1) * ASTAGE + b4 * ABOX, tmap, 32 * b4, y, bar);
+    };
+    int issued = 0;
+    if (t == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar1, 1);
+        *abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (t == 0) {
+        for (; issued < 2 && issued < nsteps; ++issued) issue(issued);
+    }
+
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (S0) x = *(const float4 *)(S0 + u * (size_t)FD * dv + row_off);
     *(float4 *)(X + i * FCB + 4 * cg) = x;
-
-    float4 ar[16];
-    float4 bnext = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto fetch = [&](int s) {  // A_s (whole, coalesced) and this thread's tile of B_s
-        const float4 *src = (const float4 *)(A + (u * Sg + s) * (size_t)FD * FD);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) ar[m] = src[t + FT * m];
-        bnext = *(const float4 *)(B + (u * Sg + s) * (size_t)FD * dv + row_off);
-    };
-    auto stage = [&]() {
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int e = t + FT * m, r = e >> 5, c = (e & 31) * 4;
-            float *d = As + r * LAP + c;
-            d[0] = ar[m].x; d[1] = ar[m].y; d[2] = ar[m].z; d[3] = ar[m].w;
-        }
-    };
     float4 bcur = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (nsteps > 0) {
-        fetch(0);
-        stage();
-        bcur = bnext;
-    }
+    if (nsteps > 0) bcur = *(const float4 *)(B + (u * Sg) * (size_t)FD * dv + row_off);
     __syncthreads();
-    for (int s = 0; s < Sg; ++s) {
+
+    const int xi = i & 7;
+    int s = 0;
+    for (; s < Sg; ++s) {
         if (seg_init) *(float4 *)(seg_init + (u * Sg + s) * (size_t)FD * dv + row_off) = x;
         if (s >= nsteps) break;
-        if (s + 1 < nsteps) fetch(s + 1);  // in flight during the product below
-        // two independent accumulation chains (even / odd k) halve the FMA latency chain
+        float4 bnext = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s + 1 < nsteps) bnext = *(const float4 *)(B + (u * Sg + s + 1) * (size_t)FD * dv + row_off);
+        mbar_wait((s & 1) ? bar1 : bar0, (s >> 1) & 1, abort, kWaitLimit);
+        const uint8_t *stage = sm + (s & 1) * ASTAGE + i * 128;
         float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-        const float *arow = As + i * LAP;
-#pragma unroll 8
-        for (int k = 0; k < FD; k += 2) {
-            const float ae = arow[k], ao = arow[k + 1];
-            const float4 xe = *(const float4 *)(X + k * FCB + 4 * cg);
-            const float4 xo = *(const float4 *)(X + (k + 1) * FCB + 4 * cg);
-            a0.x = fmaf(ae, xe.x, a0.x); a0.y = fmaf(ae, xe.y, a0.y);
-            a0.z = fmaf(ae, xe.z, a0.z); a0.w = fmaf(ae, xe.w, a0.w);
-            a1.x = fmaf(ao, xo.x, a1.x); a1.y = fmaf(ao, xo.y, a1.y);
-            a1.z = fmaf(ao, xo.z, a1.z); a1.w = fmaf(ao, xo.w, a1.w);
+#pragma unroll
+        for (int k4 = 0; k4 < 32; ++k4) {
+            const float4 a = *(const float4 *)(stage + (k4 >> 3) * ABOX + (((k4 & 7) ^ xi) << 4));
+            const float4 x0 = *(const float4 *)(X + (4 * k4 + 0) * FCB + 4 * cg);
+            const float4 x1 = *(const float4 *)(X + (4 * k4 + 1) * FCB + 4 * cg);
+            const float4 x2 = *(const float4 *)(X + (4 * k4 + 2) * FCB + 4 * cg);
+            const float4 x3 = *(const float4 *)(X + (4 * k4 + 3) * FCB + 4 * cg);
+            a0.x = fmaf(a.x, x0.x, a0.x); a0.y = fmaf(a.x, x0.y, a0.y);
+            a0.z = fmaf(a.x, x0.z, a0.z); a0.w = fmaf(a.x, x0.w, a0.w);
+            a1.x = fmaf(a.y, x1.x, a1.x); a1.y = fmaf(a.y, x1.y, a1.y);
+            a1.z = fmaf(a.y, x1.z, a1.z); a1.w = fmaf(a.y, x1.w, a1.w);
+            a0.x = fmaf(a.z, x2.x, a0.x); a0.y = fmaf(a.z, x2.y, a0.y);
+            a0.z = fmaf(a.z, x2.z, a0.z); a0.w = fmaf(a.z, x2.w, a0.w);
+            a1.x = fmaf(a.w, x3.x, a1.x); a1.y = fmaf(a.w, x3.y, a1.y);
+            a1.z = fmaf(a.w, x3.z, a1.z); a1.w = fmaf(a.w, x3.w, a1.w);
         }
-        float4 acc;
-        acc.x = a0.x + a1.x + bcur.x; acc.y = a0.y + a1.y + bcur.y;
-        acc.z = a0.z + a1.z + bcur.z; acc.w = a0.w + a1.w + bcur.w;
-        __syncthreads();  // every read of X and of A_s is done
-        x = acc;
+        __syncthreads();  // every read of X and of stage s % 2 is done
+        if (*abort) break;
+        x.x = a0.x + a1.x + bcur.x; x.y = a0.y + a1.y + bcur.y;
+        x.z = a0.z + a1.z + bcur.z; x.w = a0.w + a1.w + bcur.w;
         *(float4 *)(X + i * FCB + 4 * cg) = x;
-        if (s + 1 < nsteps) {
-            stage();
-            bcur = bnext;
+        bcur = bnext;
+        if (t == 0 && s + 2 < nsteps) {
+            fence_async_smem();
+            issue(s + 2);
+            ++issued;
         }
         __syncthreads();
+    }
+    if (*abort) {
+        if (t == 0) {
+            dev_fail(dev_status, KDA_ERR_TIMEOUT);
+            volatile int never = 0;  // let copies already in flight land before exiting
+            for (int c = s; c < issued; ++c)
+                mbar_wait((c & 1) ? bar1 : bar0, (c >> 1) & 1, &never, kWaitLimit);
+        }
+        return;
     }
     if (S_final) *(float4 *)(S_final + u * (size_t)FD * dv + row_off) = x;
 }
@@ -153,19 +186,31 @@ __global__ void __launch_bounds__(FT) compose_fast_kernel(int Sg, int dv, const 
 }  // namespace
 
 cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, const float *B,
-                           const float *S0, float *seg_init, float *S_final, cudaStream_t st) {
+                           const float *S0, float *seg_init, float *S_final, int32_t *dev_status,
+                           cudaStream_t st) {
     if (units == 0 || Sg == 0) return cudaSuccess;
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
+    PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
     if (dk == FD && dv % FCB == 0 && al16(A) && al16(B) && al16(S0) && al16(seg_init) &&
-        al16(S_final)) {
-        const size_t fsmem = ((size_t)FD * LAP + (size_t)FD * FCB) * sizeof(float);
-        cudaError_t e = cudaFuncSetAttribute(compose_fast_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)fsmem);
-        if (e != cudaSuccess) return e;
-        compose_fast_kernel<<<dim3(units, dv / FCB), FT, fsmem, st>>>(Sg, dv, A, B, S0, seg_init,
-                                                                       S_final);
-        return cudaGetLastError();
+        al16(S_final) && enc) {
+        // A viewed as [units * Sg * 128 rows, 128 fp32 columns], 128 x 32 boxes
+        CUtensorMap tm;
+        const cuuint64_t dims[2] = {(cuuint64_t)FD, (cuuint64_t)units * Sg * FD};
+        const cuuint64_t strides[1] = {(cuuint64_t)FD * 4};
+        const cuuint32_t box[2] = {32, (cuuint32_t)FD};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(A), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+            CUDA_SUCCESS) {
+            cudaError_t e = cudaFuncSetAttribute(compose_tma_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 FAST_SMEM);
+            if (e != cudaSuccess) return e;
+            compose_tma_kernel<<<dim3(units, dv / FCB), FT, FAST_SMEM, st>>>(
+                tm, Sg, dv, B, S0, seg_init, S_final, dev_status);
+            return cudaGetLastError();
+        }
     }
     const size_t smem = ((size_t)dk * (dk + 1) + 2 * (size_t)dk * CB) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(compose_kernel,

@@ -34,8 +34,6 @@
 // Every wait is bounded: a stalled barrier sets an abort flag, records
 // KDA_ERR_TIMEOUT in dev_status, and all roles leave their loops, free TMEM and
 // return.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <string.h>
 
 #include "kda_internal.cuh"
@@ -624,21 +622,6 @@ bool prefill_tc_supported(const PrefillArgs &a) {
 
 namespace {
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// dependency on the driver library).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
-    }
-    return fn;
-}
-
 // [T_tot, H * 128] row-major view of a token-major array, 16 x 128 boxes.
 bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *ptr, int T,
                  int H, bool fp32) {
@@ -661,7 +644,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     memset(&tq, 0, sizeof(tq)); memset(&tk, 0, sizeof(tk));
     memset(&tv, 0, sizeof(tv)); memset(&tg, 0, sizeof(tg));
     if (a.T_tot > 0) {  // with no tokens no CTA loads anything (and the pointers may be null)
-        PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+        PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
         if (!enc) return cudaErrorNotSupported;
         const void *qp = a.q ? a.q : a.k;  // the transfer pass has no q
         if (!encode_rows(enc, &tq, qp, a.T_tot, a.H, false) ||
