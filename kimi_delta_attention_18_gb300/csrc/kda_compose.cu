@@ -93,7 +93,9 @@ __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__
                                                          const float *S0, float *seg_init,
                                                          float *S_final, int32_t *dev_status) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // Align by pointer arithmetic on the __shared__ array (not through an integer),
+    // so accesses keep the shared address space instead of becoming generic.
+    uint8_t *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
     float *X = (float *)(sm + 2 * ASTAGE);  // [128][8]
     uint64_t *bars = (uint64_t *)(sm + 2 * ASTAGE + FD * FCB * 4);
     volatile int *abort = (volatile int *)(bars + 2);

@@ -59,7 +59,9 @@ __global__ void __launch_bounds__(NT, 1) decode_tma_kernel(int units, const TA *
                                                            const float *beta, float *S, TA *out) {
     using L = Layout<TA>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // Align by pointer arithmetic on the __shared__ array (not through an integer),
+    // so accesses keep the shared address space instead of becoming generic.
+    uint8_t *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(sm);
     volatile int *abort = (volatile int *)(sm + L::ABORT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -544,7 +544,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_g) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // Align by pointer arithmetic on the __shared__ array (not through an integer),
+    // so accesses keep the shared address space instead of becoming generic.
+    uint8_t *smem = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
     Ctx x;
     x.p = &p;
     x.tm_q = reinterpret_cast<uint64_t>(&tm_q);
