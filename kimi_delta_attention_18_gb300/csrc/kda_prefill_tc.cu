@@ -4,36 +4,49 @@
 // then write, then read: "Kimi K3 Architecture Explained", section 3), with the
 // bounded log-decay g > -5 keeping every in-block factor exp(+-Gamma), |Gamma| <
 // 80, inside BF16 range so that both the intra-block ("diagonal") and the
-// state ("off-diagonal") products run on tensor cores (Kimi K3 technical-report
-// digest, section 2.1 (1)).  Per 16-token block, from state S (128 x 128, fp32):
+// state ("off-diagonal") products run on tensor cores with BF16 operands and
+// fp32 accumulation (Kimi K3 technical-report digest, section 2.1 (1)).  Per
+// 16-token block, from state S (128 x 128, fp32):
 //   prep (state-free):  Gamma = cumsum g;  Kh = K e^{Gamma};  Kt = K e^{-Gamma};
 //                       Qh = Q e^{Gamma};  Kb = K e^{Gamma_C - Gamma};
 //                       L = Diag(beta) strict_lower(Kh Kt^T);  Mq = lower(Qh Kt^T);
-//                       T = (I + L)^{-1} Diag(beta);  W = T Kh;  Ut = T V
-//   chain (sequential): U = Ut - W S;  O = Qh S + Mq U;  S <- e^{Gamma_C} S + Kb^T U
+//                       T = (I + L)^{-1} Diag(beta);  W = T Kh
+//   chain (sequential): U = T V - W S;  O = Qh S + Mq U;  S <- e^{Gamma_C} S + Kb^T U
 // The digest's FlashKDA overlaps the intra-block work with the cross-block state
-// propagation (section 2.4 (1)); here that is warp specialisation inside one CTA:
+// propagation (section 2.4 (1)); here that is warp specialisation in one CTA per
+// (sequence, head, segment):
 //
 //   warp 0      producer: one 2D tensor-map TMA copy per array per block (q, k, v:
-//               16 x 128 BF16 boxes; g: 16 x 128 fp32), beta by prefetched loads
-//   warp 1      issues tcgen05.mma (one thread); owns the TMEM allocation
-//   warps 2-5   prep of block c+1 (CUDA cores + mma.sync for the 16x16 products)
-//   warps 6-13  state: fp32 master state S in registers (lane = dv column j,
-//               64 dk channels per warp), U, the decayed update, the output read
+//               16 x 128 BF16 boxes; g: 16 x 128 fp32) into a 4-stage input ring,
+//               beta by prefetched loads
+//   warps 1-4   prep: warp p prepares blocks p, p+4, p+8, ... on its own (no
+//               barrier between prep warps), so four blocks are in preparation at
+//               once.  It frees its input stage as soon as it has read it and
+//               writes the block's chain operands, V included, into its record
+//               slot.
+//   warps 5-12  chain: warp w owns the state columns j in [16w, 16w+16): rows j of
+//               S^T, all 128 key channels, held as fp32 mma.sync accumulators.
+//               Columns of S never mix, so each warp runs the recurrence of its 16
+//               columns entirely in its own registers; per block it reads only the
+//               record and signals when it is done with it.
 //
-// Transposed so the MMA M dimension is the 128 state columns (TMEM lanes):
-//   D1[j][r]      = (S^T [W; Qh]^T)          M=128 N=32 K=128  (8 x K16)
-//   D1[j][16+r]  += (U^T Mq^T)               M=128 N=16 K=16
-//   D3[j][i]      = (U^T Kb)                 M=128 N=128 K=16
-// with S^T, U^T as bf16 A operands in shared memory and fp32 accumulators in
-// TMEM.  The master state never leaves fp32 registers; only its bf16 copy feeds
-// the MMA.  One CTA per (sequence, head, segment); in the transfer pass two
-// CTAs per unit run the same recurrence on the identity (values 0) and on zeros
-// (the unit's values) to give the transfer matrix and the zero-initial state.
+// The chain is a strict sequence of small products (16 x 128 x 128 per block).
+// Kept in registers, one step costs a handful of dependent mma.sync issues and
+// no round trip through shared or tensor memory, no commit and no cross-warp
+// barrier; the fp32 master state never leaves registers and only its BF16
+// rounding feeds the products, so the decay term e^{Gamma_C} S stays exact in
+// fp32.  In the transfer pass two CTAs per unit run the same recurrence from the
+// identity with zero values (transfer matrix) and from zeros (zero-initial state).
+//
+// mma.sync m16n8k16 fragments (g8 = lane / 4, t4 = lane % 4):
+//   A (16x16): a0 = A[g8][2t4..+1], a1 = A[g8+8][2t4..+1], a2 = A[g8][2t4+8..+9],
+//              a3 = A[g8+8][2t4+8..+9];  B (16x8): b0 = B[2t4..+1][g8], b1 = B[2t4+8..+9][g8];
+//   C (16x8):  c0,c1 = C[g8][2t4..+1], c2,c3 = C[g8+8][2t4..+1].
+// A chain warp's S^T accumulator n (n = 0..15) covers key channels [8n, 8n+8); two
+// adjacent accumulators are exactly the A fragment of one 16-channel k-step.
 //
 // Every wait is bounded: a stalled barrier sets an abort flag, records
-// KDA_ERR_TIMEOUT in dev_status, and all roles leave their loops, free TMEM and
-// return.
+// KDA_ERR_TIMEOUT in dev_status, and all roles leave their loops and return.
 #include <string.h>
 
 #include "kda_internal.cuh"
@@ -44,79 +57,74 @@ namespace {
 
 using namespace sm100;
 
-constexpr int C = 16;   // tokens per block
-constexpr int D = 128;  // dk = dv
-constexpr int NS = 3;   // input stages in flight
-constexpr int NP = 3;   // prepared-operand stages
-constexpr int W_PROD = 0, W_MMA = 1, W_PREP0 = 2, N_PREP = 4, W_STATE0 = 6, N_STATE = 8;
-constexpr int NWARPS = W_STATE0 + N_STATE;
+constexpr int C = 16;    // tokens per block
+constexpr int D = 128;   // dk = dv
+// Input stage and record slot i belong to prep warp i (blocks i, i + 4, ...), so
+// every wait on their barriers is at most one phase ahead of the barrier: a
+// stage shared between prep warps could be waited on two phases early, where
+// the parity test cannot tell the phases apart.
+constexpr int N_PREP = 4;
+constexpr int NS = N_PREP;  // input stages (TMA ring)
+constexpr int NR = N_PREP;  // record slots (prepared blocks waiting for the chain)
+constexpr int W_PROD = 0, W_PREP0 = 1, W_CHAIN0 = W_PREP0 + N_PREP, N_CHAIN = 8;
+constexpr int NWARPS = W_CHAIN0 + N_CHAIN;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr long long kWaitLimit = 4000000000ll;  // ~2 s of SM clocks
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t D3_COL = 0;    // 128 columns: U^T Kb
-constexpr uint32_t D1_COL = 128;  // 2 x 32 columns: [W S | Qh S + Mq U]^T, double-buffered
 
-// ---- shared memory map (bytes from a 1024-aligned base) ----
-// UMMA operands (canonical K-major, no swizzle: 8x16-byte core matrices,
-// LBO = 128 bytes between core matrices along K, SBO between 8-row groups).
-constexpr int SA_OFF = 0;                    // S^T  [j 128][i 128]  SBO 2048   32 KB
-constexpr int UA_OFF = SA_OFF + 32768;       // U^T  [j 128][r 16]   SBO 256     4 KB
-constexpr int PP_OFF = UA_OFF + 4096;        // prepared stages
-constexpr int PP_B1 = 0;                     // [W; Qh] [r 32][i 128] SBO 2048   8 KB
-constexpr int PP_B2 = 8192;                  // Mq   [r 16][i 16]   SBO 256    512 B
-constexpr int PP_B3 = PP_B2 + 512;           // Kb^T [i 128][r 16]  SBO 256     4 KB
-constexpr int UT_LD = 132;                   // Ut fp32 row stride (floats)
-constexpr int PP_UT = PP_B3 + 4096;          // Ut   fp32 [16][132]
-constexpr int PP_DECAY = PP_UT + C * UT_LD * 4;  // exp(Gamma_C) fp32 [128]
-constexpr int PP_SIZE = PP_DECAY + 512;
-constexpr int IN_OFF = PP_OFF + NP * PP_SIZE;  // input stages (TMA boxes, dense rows)
-constexpr int IN_ROWB = 256;                   // one 128-element bf16 row
-constexpr int IN_Q = 0;                        // bf16 [16][128]
+// ---- shared memory: [NS input stages | NR records | N_PREP prep scratches | O staging]
+// input stage (TMA boxes, dense rows); released by the prep warp once read
+constexpr int IN_ROWB = 256;                    // one 128-element BF16 row
+constexpr int IN_Q = 0;                         // BF16 [16][128]
 constexpr int IN_K = IN_Q + C * IN_ROWB;
 constexpr int IN_V = IN_K + C * IN_ROWB;
-constexpr int IN_G = IN_V + C * IN_ROWB;       // fp32 [16][128]
-constexpr int IN_B = IN_G + C * 512;           // beta fp32 [16]
-constexpr int IN_SIZE = (IN_B + 64 + 127) & ~127;
-constexpr int SC_OFF = IN_OFF + NS * IN_SIZE;  // prep scratch
-constexpr int TROW = 48;                       // one channel's 16 positions, bf16, padded
-constexpr int SC_KH = 0;                       // Kh^T bf16 [128 ch][24]
-constexpr int SC_KT = SC_KH + D * TROW;        // Kt^T bf16 [128 ch][24]
-constexpr int SC_QH = SC_KT + D * TROW;        // Qh^T bf16 [128 ch][24]
-constexpr int SC_L = SC_QH + D * TROW;         // Diag(beta) L fp32 [16][17]
-constexpr int SC_T = SC_L + C * 17 * 4;        // T bf16 [16][24]
-constexpr int SC_SIZE = SC_T + C * 48;
-constexpr int BAR_OFF = (SC_OFF + SC_SIZE + 7) & ~7;
+constexpr int IN_G = IN_V + C * IN_ROWB;        // fp32 [16][128]
+constexpr int IN_B = IN_G + C * 512;            // beta fp32 [16]
+constexpr int IN_SIZE = IN_B + 128;
+// record: the chain's operands for one block; released by the chain warps
+constexpr int RL = 56;                          // BF16 elements per channel row (112 B):
+constexpr int RLB = RL * 2;                     //   [-W^T (16) | Qh^T (16) | Kb^T (16) | pad]
+constexpr int RC_W = 0, RC_Q = 16, RC_K = 32;
+constexpr int TL = 24;                          // T and Mq rows: 16 BF16 + pad (48 B)
+constexpr int VROWB = 272;                      // V rows: 128 BF16 + pad
+constexpr int R_T = D * RLB;                    // T  [r][r'] BF16
+constexpr int R_MQ = R_T + C * TL * 2;          // Mq [r][r'] BF16
+constexpr int R_DECAY = R_MQ + C * TL * 2;      // e^{Gamma_C} fp32 [128]
+constexpr int R_V = R_DECAY + D * 4;            // V  [r][j] BF16 (rows past the block: 0)
+constexpr int R_SIZE = R_V + C * VROWB;
+// prep scratch (private to one prep warp)
+constexpr int TROW = 48;                        // one channel's 16 positions, BF16, padded
+constexpr int X_KH = 0;                         // Kh^T [128 ch][24]
+constexpr int X_KT = X_KH + D * TROW;           // Kt^T [128 ch][24]
+constexpr int X_L = X_KT + D * TROW;            // Diag(beta) L fp32 [16][17]
+constexpr int X_SIZE = (X_L + C * 17 * 4 + 127) & ~127;
+constexpr int IN_OFF = 0;
+constexpr int REC_OFF = IN_OFF + NS * IN_SIZE;
+constexpr int X_OFF = REC_OFF + NR * R_SIZE;
+constexpr int OST_OFF = X_OFF + N_PREP * X_SIZE;  // per chain warp: O^T staging [16 r][16 j]
+constexpr int OST_SIZE = C * 16 * 2;
+constexpr int BAR_OFF = OST_OFF + N_CHAIN * OST_SIZE;
 enum {
     B_IN_FULL = 0,
     B_IN_EMPTY = B_IN_FULL + NS,
-    B_PP_FULL = B_IN_EMPTY + NS,
-    B_PP_EMPTY = B_PP_FULL + NP,
-    B_MMA1 = B_PP_EMPTY + NP,
-    B_UREADY,
-    B_MMA3,
-    B_SREADY,
-    NBARS
+    B_REC_FULL = B_IN_EMPTY + NS,
+    B_REC_EMPTY = B_REC_FULL + NR,
+    NBARS = B_REC_EMPTY + NR
 };
-constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // [0] TMEM base, [1] abort, [2] prep flag
+constexpr int MISC_OFF = BAR_OFF + NBARS * 8;   // [0] abort flag
 constexpr int SMEM_USED = MISC_OFF + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
+constexpr int SMEM_BYTES = SMEM_USED + 128;     // slack for aligning the base
 
-static_assert(PP_SIZE % 128 == 0 && IN_SIZE % 128 == 0 && PP_OFF % 128 == 0, "stage alignment");
+static_assert(IN_SIZE % 128 == 0 && R_SIZE % 128 == 0 && X_SIZE % 128 == 0, "stage alignment");
+static_assert(RLB % 16 == 0 && (RLB / 16) % 2 == 1, "record rows: 16-byte aligned, odd stride");
+static_assert(VROWB % 16 == 0 && (VROWB / 16) % 2 == 1, "V rows: 16-byte aligned, odd stride");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-
-// Byte offset of element (row, k) in a canonical no-swizzle K-major operand.
-__device__ __forceinline__ uint32_t kmaj_off(int row, int k, int sbo) {
-    return (uint32_t)((row >> 3) * sbo + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
-}
 
 struct Ctx {
     const PrefillArgs *p;
     uint64_t tm_q, tm_k, tm_v, tm_g;  // generic addresses of the tensor maps
     uint8_t *smem;
     uint32_t sbase;
-    uint32_t tmem;
     volatile int *abort;
-    volatile int *prep_ok;
     int n, h, s;
     int t_begin, t_end, nchunks;
     bool transfer, partA, want_q, want_v;
@@ -129,12 +137,8 @@ __device__ __forceinline__ bool warp_wait(const Ctx &x, int b, uint32_t parity) 
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-__device__ __forceinline__ void report_abort(const Ctx &x) {
-    if (*x.abort) dev_fail(x.p->dev_status, KDA_ERR_TIMEOUT);
-}
-
 // ------------------------------------------------------------------ producer
-__device__ void producer_role(const Ctx &x) {
+__device__ __forceinline__ void producer_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int lane = threadIdx.x & 31;
     int issued = 0;
@@ -158,7 +162,7 @@ __device__ void producer_role(const Ctx &x) {
         const uint32_t base = x.sbase + IN_OFF + st * IN_SIZE;
         if (lane == 0) {
             // Whole 16-row boxes: rows past the block's end hold the next sequence's
-            // tokens (masked by the prep warps) or, past the array, zero fill.
+            // tokens (masked by the prep warp) or, past the array, zero fill.
             const uint32_t bytes =
                 (x.want_q ? 4096u : 0u) + 4096u + (x.want_v ? 4096u : 0u) + 8192u;
             mbar_arrive_expect_tx(full, bytes);
@@ -181,145 +185,142 @@ __device__ void producer_role(const Ctx &x) {
     }
 }
 
-// ------------------------------------------------------------------ MMA issuer
-__device__ void mma_role(const Ctx &x) {
-    const uint32_t id32 = umma_idesc_bf16(128, 32), id16 = umma_idesc_bf16(128, 16),
-                   id128 = umma_idesc_bf16(128, 128);
-    const uint32_t n1 = x.want_q ? id32 : id16;
-    const uint64_t ua = umma_desc(x.sbase + UA_OFF, 128, 256);
-    uint64_t sa_desc[8];
+// ------------------------------------------------------------------ prep
+// Elementwise factors of one block for the key channels lane + 32 m (m = 0..3):
+// Kh^T and Kt^T rows into the prep scratch, Qh^T and Kb^T rows and e^{Gamma_C}
+// into the record.  Every row of the boxes is in shared memory, so the loads are
+// unconditional; with MASK (the sequence's last, partial block) rows past its
+// end get no decay, no key and no query.  Full blocks take the unmasked form,
+// whose dependency chains are about half as long.
+template <bool WANT_Q, bool MASK>
+__device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uint8_t *rec, int nt,
+                                            int lane) {
+    const float *gin = (const float *)(in + IN_G);
+    const __nv_bfloat16 *kin = (const __nv_bfloat16 *)(in + IN_K);
+    const __nv_bfloat16 *qin = (const __nv_bfloat16 *)(in + IN_Q);
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        float al[C], kv[C];
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) sa_desc[kk] = umma_desc(x.sbase + SA_OFF + kk * 256, 128, 2048);
-    for (int c = 0; c < x.nchunks; ++c) {
-        const int pp = c % NP;
-        if (!mbar_wait(x.bar(B_PP_FULL + pp), (c / NP) & 1, x.abort, kWaitLimit)) break;
-        if (!mbar_wait(x.bar(B_SREADY), c & 1, x.abort, kWaitLimit)) break;
-        tc_fence_after();
-        const uint32_t d1 = x.tmem + D1_COL + (c & 1) * 32;
-        const uint32_t pbase = x.sbase + PP_OFF + pp * PP_SIZE;
+        for (int r = 0; r < C; ++r) {
+            al[r] = gin[r * D + ch];
+            kv[r] = __bfloat162float(kin[r * D + ch]);
+        }
+        if (MASK) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            umma_bf16(d1, sa_desc[kk], umma_desc(pbase + PP_B1 + kk * 256, 128, 2048), n1, kk > 0);
-        umma_commit(x.bar(B_MMA1));
-        if (!mbar_wait(x.bar(B_UREADY), c & 1, x.abort, kWaitLimit)) break;
-        tc_fence_after();
-        if (x.want_q) umma_bf16(d1 + 16, ua, umma_desc(pbase + PP_B2, 128, 256), id16, 1);
-        umma_bf16(x.tmem + D3_COL, ua, umma_desc(pbase + PP_B3, 128, 256), id128, 0);
-        umma_commit(x.bar(B_MMA3));
-        umma_commit(x.bar(B_PP_EMPTY + pp));
+            for (int r = 0; r < C; ++r) {
+                al[r] = r < nt ? al[r] : 0.f;
+                kv[r] = r < nt ? kv[r] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < C; ++r) al[r] = __expf(al[r]);  // alpha = e^g
+        float fwd[C], rev[C];  // e^{Gamma_r}, e^{Gamma_C - Gamma_r}
+        float a = 1.f;
+#pragma unroll
+        for (int r = 0; r < C; ++r) { a *= al[r]; fwd[r] = a; }
+        float b = 1.f;
+#pragma unroll
+        for (int r = C - 1; r >= 0; --r) { rev[r] = b; b *= al[r]; }
+        const float eGC = fwd[C - 1];
+        const float einv = 1.f / eGC;
+        // One operand's 16 positions for this channel as one 32-byte row.
+        auto put_row = [&](uint8_t *dst, const float (&val)[C]) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(val[2 * e], val[2 * e + 1]);
+            *(uint4 *)dst = make_uint4(w[0], w[1], w[2], w[3]);
+            *(uint4 *)(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        };
+        float tmp[C];
+#pragma unroll
+        for (int r = 0; r < C; ++r) tmp[r] = kv[r] * fwd[r];
+        put_row(scr + X_KH + ch * TROW, tmp);
+#pragma unroll
+        for (int r = 0; r < C; ++r) tmp[r] = kv[r] * (einv * rev[r]);
+        put_row(scr + X_KT + ch * TROW, tmp);
+#pragma unroll
+        for (int r = 0; r < C; ++r) tmp[r] = kv[r] * rev[r];
+        put_row(rec + ch * RLB + RC_K * 2, tmp);
+        if (WANT_Q) {
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                const float qv = __bfloat162float(qin[r * D + ch]);
+                tmp[r] = (MASK && r >= nt ? 0.f : qv) * fwd[r];
+            }
+            put_row(rec + ch * RLB + RC_Q * 2, tmp);
+        }
+        ((float *)(rec + R_DECAY))[ch] = eGC;
     }
 }
 
-// ------------------------------------------------------------------ prep
-__device__ void prep_role(const Ctx &x) {
-    const int pt = threadIdx.x - W_PREP0 * 32;  // 0..127: the key channel in elementwise work
-    const int pw = pt >> 5, lane = pt & 31;
-    const int g8 = lane >> 2, t4 = lane & 3;
-    uint8_t *sc = x.smem + SC_OFF;
-    const uint32_t sc_s = x.sbase + SC_OFF;
-    float *Lf = (float *)(sc + SC_L);
-    __nv_bfloat16 *Tb = (__nv_bfloat16 *)(sc + SC_T);
+// One warp prepares one whole block: elementwise factors, L and Mq, the solve
+// for T, and W = T Kh, written with V into a record slot.  Prep warp p takes
+// blocks p, p + 4, p + 8, ...; it frees the input stage as soon as it has read it.
+template <bool WANT_Q, bool WANT_V>
+__device__ __forceinline__ void prep_role(const Ctx &x) {
+    const int pw = (threadIdx.x >> 5) - W_PREP0;
+    const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
+    uint8_t *scr = x.smem + X_OFF + pw * X_SIZE;
+    const uint32_t scr_s = x.sbase + X_OFF + pw * X_SIZE;
+    float *Lf = (float *)(scr + X_L);
 
-    for (int c = 0; c < x.nchunks; ++c) {
-        const int st = c % NS, pp = c % NP;
-        if (pt == 0) {
-            bool ok = mbar_wait(x.bar(B_IN_FULL + st), (c / NS) & 1, x.abort, kWaitLimit) &&
-                      mbar_wait(x.bar(B_PP_EMPTY + pp), ((c / NP) & 1) ^ 1, x.abort, kWaitLimit);
-            *x.prep_ok = ok ? 1 : 0;
-        }
-        named_bar_sync(1, N_PREP * 32);
-        if (!*x.prep_ok) break;
-
-        uint8_t *in = x.smem + IN_OFF + st * IN_SIZE;
-        uint8_t *pp_s = x.smem + PP_OFF + pp * PP_SIZE;
-        const float *gin = (const float *)(in + IN_G);
+    for (int c = pw; c < x.nchunks; c += N_PREP) {
+        const int st = c % NS, slot = c % NR;
+        if (!warp_wait(x, B_REC_EMPTY + slot, ((c / NR) & 1) ^ 1)) break;
+        if (!warp_wait(x, B_IN_FULL + st, (c / NS) & 1)) break;
+        const uint8_t *in = x.smem + IN_OFF + st * IN_SIZE;
+        uint8_t *rec = x.smem + REC_OFF + slot * R_SIZE;
+        const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
         const float *bin = (const float *)(in + IN_B);
-        const int t0 = x.t_begin + C * c;
-        const int nt = min(C, x.t_end - t0);
+        const int nt = min(C, x.t_end - (x.t_begin + C * c));
+        // beta of rows g8 and g8 + 8 (for L) and of column lane (for T), kept in
+        // registers: the input stage is released before they are needed
+        const float beta_lo = bin[g8], beta_hi = bin[g8 + 8], beta_col = bin[lane & 15];
 
-        // ---- elementwise: one key channel per thread
-        {
-            const int ch = pt;
-            float alpha[C];
+        // ---- elementwise: lane handles key channels lane + 32 m
+        if (nt == C) elementwise<WANT_Q, false>(in, scr, rec, nt, lane);
+        else elementwise<WANT_Q, true>(in, scr, rec, nt, lane);
+        // V into the record (padded rows).  Rows past the block's end become zero:
+        // they are weighted by zero in the chain's products, and the next
+        // sequence's values (or anything non-finite in them) must not leak in.
+        if (WANT_V) {
 #pragma unroll
-            for (int r = 0; r < C; ++r) alpha[r] = r < nt ? __expf(gin[r * D + ch]) : 1.f;
-            float fwd[C], rev[C];  // e^{Gamma_r}, e^{Gamma_C - Gamma_r}
-            float a = 1.f;
-#pragma unroll
-            for (int r = 0; r < C; ++r) { a *= alpha[r]; fwd[r] = a; }
-            float b = 1.f;
-#pragma unroll
-            for (int r = C - 1; r >= 0; --r) { rev[r] = b; b *= alpha[r]; }
-            const float eGC = fwd[C - 1];
-            const float einv = 1.f / eGC;
-            float kv[C];
-#pragma unroll
-            for (int r = 0; r < C; ++r)
-                kv[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_K + r * IN_ROWB))[ch])
-                               : 0.f;
-            // Each operand's 16 positions for this channel, as one 48-byte row.
-            auto put_row = [&](int off, const float (&val)[C]) {
-                uint32_t w[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(val[2 * e], val[2 * e + 1]);
-                *(uint4 *)(sc + off + ch * TROW) = make_uint4(w[0], w[1], w[2], w[3]);
-                *(uint4 *)(sc + off + ch * TROW + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-            };
-            float tmp[C];
-#pragma unroll
-            for (int r = 0; r < C; ++r) tmp[r] = kv[r] * fwd[r];
-            put_row(SC_KH, tmp);
-#pragma unroll
-            for (int r = 0; r < C; ++r) tmp[r] = kv[r] * (einv * rev[r]);
-            put_row(SC_KT, tmp);
-            if (x.want_q) {
-#pragma unroll
-                for (int r = 0; r < C; ++r)
-                    tmp[r] = r < nt ? __bfloat162float(((const __nv_bfloat16 *)(in + IN_Q + r * IN_ROWB))[ch]) *
-                                          fwd[r]
-                                    : 0.f;
-                put_row(SC_QH, tmp);
+            for (int i = 0; i < 8; ++i) {
+                const int idx = lane + 32 * i, r = idx >> 4, q16 = idx & 15;
+                uint4 v = *(const uint4 *)(in + IN_V + r * IN_ROWB + q16 * 16);
+                if (r >= nt) v = make_uint4(0u, 0u, 0u, 0u);
+                *(uint4 *)(rec + R_V + r * VROWB + q16 * 16) = v;
             }
-            // Kb^T row ch (its 16 positions) as two 16-byte core-matrix rows.
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r0 = h8 * 8 + 2 * e;
-                    w[e] = pack_bf16x2(kv[r0] * rev[r0], kv[r0 + 1] * rev[r0 + 1]);
-                }
-                *(uint4 *)(pp_s + PP_B3 + kmaj_off(ch, h8 * 8, 256)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            ((float *)(pp_s + PP_DECAY))[ch] = eGC;
-            // V rows past the block's end are weighted by zero on the tensor cores:
-            // make them zero too (the next sequence's values, or anything non-finite
-            // in them, must not leak in through 0 * x).
-            if (x.want_v)
-                for (int r = nt; r < C; ++r)
-                    ((__nv_bfloat16 *)(in + IN_V + r * IN_ROWB))[ch] = __float2bfloat16_rn(0.f);
         }
-        named_bar_sync(1, N_PREP * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x.bar(B_IN_EMPTY + st));  // input stage fully read
 
-        // ---- intra-block products on tensor cores (mma.sync): L (warp 0), Mq (warp 1);
-        //      warps 2-3 meanwhile copy Qh into the [W; Qh] operand's rows 16..31.
-        if (pw == 0 || (pw == 1 && x.want_q)) {
-            const uint32_t a_base = sc_s + (pw == 0 ? SC_KH : SC_QH);
-            float acc[2][4] = {};
+        // ---- L = Diag(beta) strict_lower(Kh Kt^T) and Mq = lower(Qh Kt^T), 16 x 16 x 128
+        {
+            float accL[2][4] = {}, accM[2][4] = {};
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                uint32_t af[4], bf[4];
-                // A (positions x channels) from the channel-major rows, transposed
-                ldsm_x4_t(a_base + (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * TROW +
-                              ((lane >> 3) & 1) * 16,
-                          af);
+                uint32_t bf[4], af[4];
                 // B (channels x positions) from Kt^T rows, transposed
-                ldsm_x4_t(sc_s + SC_KT + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * TROW +
+                ldsm_x4_t(scr_s + X_KT + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * TROW +
                               (lane >> 4) * 16,
                           bf);
-                mma_bf16_16816(acc[0], af, bf[0], bf[1]);
-                mma_bf16_16816(acc[1], af, bf[2], bf[3]);
+                // A (positions x channels) from Kh^T rows, transposed
+                ldsm_x4_t(scr_s + X_KH + (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * TROW +
+                              ((lane >> 3) & 1) * 16,
+                          af);
+                mma_bf16_16816(accL[0], af, bf[0], bf[1]);
+                mma_bf16_16816(accL[1], af, bf[2], bf[3]);
+                if (WANT_Q) {
+                    uint32_t aq[4];
+                    ldsm_x4_t(rec_s + (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * RLB + RC_Q * 2 +
+                                  ((lane >> 3) & 1) * 16,
+                              aq);
+                    mma_bf16_16816(accM[0], aq, bf[0], bf[1]);
+                    mma_bf16_16816(accM[1], aq, bf[2], bf[3]);
+                }
             }
 #pragma unroll
             for (int nb = 0; nb < 2; ++nb)
@@ -327,38 +328,19 @@ __device__ void prep_role(const Ctx &x) {
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = g8 + 8 * hh;
                     const int i0 = nb * 8 + 2 * t4;
-                    const float v0 = acc[nb][2 * hh], v1 = acc[nb][2 * hh + 1];
-                    if (pw == 0) {
-                        const float br = bin[r];
-                        Lf[r * 17 + i0] = i0 < r ? br * v0 : 0.f;
-                        Lf[r * 17 + i0 + 1] = i0 + 1 < r ? br * v1 : 0.f;
-                    } else {
-                        const uint32_t w = pack_bf16x2(i0 <= r ? v0 : 0.f, i0 + 1 <= r ? v1 : 0.f);
-                        *(uint32_t *)(pp_s + PP_B2 + kmaj_off(r, i0, 256)) = w;
-                    }
+                    const float br = hh ? beta_hi : beta_lo;
+                    Lf[r * 17 + i0] = i0 < r ? br * accL[nb][2 * hh] : 0.f;
+                    Lf[r * 17 + i0 + 1] = i0 + 1 < r ? br * accL[nb][2 * hh + 1] : 0.f;
+                    if (WANT_Q)
+                        *(uint32_t *)(rec + R_MQ + (r * TL + i0) * 2) =
+                            pack_bf16x2(i0 <= r ? accM[nb][2 * hh] : 0.f,
+                                        i0 + 1 <= r ? accM[nb][2 * hh + 1] : 0.f);
                 }
-        } else if (pw >= 2 && x.want_q) {
-            // 256 core-matrix rows: (position r, channel group cg) <- 8 channels of Qh^T
-#pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) {
-                const int chunk = (pt - 64) + 64 * q2;
-                const int r = chunk & 15, cg = chunk >> 4;
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const __nv_bfloat16 *row0 = (const __nv_bfloat16 *)(sc + SC_QH + (8 * cg + 2 * e) * TROW);
-                    const __nv_bfloat16 *row1 = (const __nv_bfloat16 *)(sc + SC_QH + (8 * cg + 2 * e + 1) * TROW);
-                    w[e] = (uint32_t)__bfloat16_as_ushort(row0[r]) |
-                           ((uint32_t)__bfloat16_as_ushort(row1[r]) << 16);
-                }
-                *(uint4 *)(pp_s + PP_B1 + kmaj_off(16 + r, 8 * cg, 2048)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-            }
         }
-        named_bar_sync(1, N_PREP * 32);
+        __syncwarp();
 
         // ---- T = (I + Diag(beta) L)^{-1} Diag(beta): forward substitution, lane = column
-        if (pw == 0 && lane < C) {
+        if (lane < C) {
             const int j = lane;
             float xv[C];
 #pragma unroll
@@ -371,158 +353,175 @@ __device__ void prep_role(const Ctx &x) {
                     if (m & 1) s1 += Lf[r * 17 + m] * xv[m];
                     else s0 += Lf[r * 17 + m] * xv[m];
                 }
-                if (r > j) xv[r] = -(s0 + s1);
+                xv[r] = r > j ? -(s0 + s1) : xv[r];
             }
-            const float bj = bin[j];
+            __nv_bfloat16 *Tb = (__nv_bfloat16 *)(rec + R_T);
 #pragma unroll
-            for (int r = 0; r < C; ++r) Tb[r * 24 + j] = __float2bfloat16_rn(xv[r] * bj);
+            for (int r = 0; r < C; ++r) Tb[r * TL + j] = __float2bfloat16_rn(xv[r] * beta_col);
         }
-        named_bar_sync(1, N_PREP * 32);
+        __syncwarp();
 
-        // ---- W = T Kh and Ut = T V: warp pw owns channels [32 pw, 32 pw + 32)
+        // ---- W = T Kh (16 x 128, K = 16); -W^T into the record rows, transposed stores
         {
             uint32_t af[4];
-            ldsm_x4(sc_s + SC_T + (lane & 15) * 48 + (lane >> 4) * 16, af);
-            float *Ut = (float *)(pp_s + PP_UT);
-#pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                const int n0 = 32 * pw + 16 * np;
-                uint32_t bf[4];
-                // B (positions x channels) = Kh, stored channel-major: plain ldmatrix
-                ldsm_x4(sc_s + SC_KH + (n0 + (lane & 7) + ((lane >> 4) << 3)) * TROW +
+            ldsm_x4(rec_s + R_T + (lane & 15) * (TL * 2) + (lane >> 4) * 16, af);
+            uint32_t bf[2][4];
+            // B (positions x channels) = Kh, stored channel-major: plain ldmatrix
+            auto load_kh = [&](int np, uint32_t (&f)[4]) {
+                ldsm_x4(scr_s + X_KH + (16 * np + (lane & 7) + ((lane >> 4) << 3)) * TROW +
                             ((lane >> 3) & 1) * 16,
-                        bf);
+                        f);
+            };
+            load_kh(0, bf[0]);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                if (np + 1 < 8) load_kh(np + 1, bf[(np + 1) & 1]);
+                const uint32_t(&b)[4] = bf[np & 1];
                 float w0[4] = {}, w1[4] = {};
-                mma_bf16_16816(w0, af, bf[0], bf[1]);
-                mma_bf16_16816(w1, af, bf[2], bf[3]);
-                float u0[4] = {}, u1[4] = {};
-                if (x.want_v) {
-                    uint32_t vf[4];
-                    ldsm_x4_t(x.sbase + IN_OFF + st * IN_SIZE + IN_V + (lane & 15) * IN_ROWB +
-                                  (n0 + (lane >> 4) * 8) * 2,
-                              vf);
-                    mma_bf16_16816(u0, af, vf[0], vf[1]);
-                    mma_bf16_16816(u1, af, vf[2], vf[3]);
-                }
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    const float *wv = hb ? w1 : w0;
-                    const float *uv = hb ? u1 : u0;
-                    const int col = n0 + 8 * hb + 2 * t4;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int r = g8 + 8 * hh;
-                        *(uint32_t *)(pp_s + PP_B1 + kmaj_off(r, col, 2048)) =
-                            pack_bf16x2(wv[2 * hh], wv[2 * hh + 1]);
-                        *(float2 *)(Ut + r * UT_LD + col) = make_float2(uv[2 * hh], uv[2 * hh + 1]);
-                    }
-                }
+                mma_bf16_16816(w0, af, b[0], b[1]);
+                mma_bf16_16816(w1, af, b[2], b[3]);
+                // matrices: (channels 16np.., rows 0-7), (16np.., rows 8-15),
+                //           (16np+8.., rows 0-7), (16np+8.., rows 8-15)
+                stsm_x4_t(rec_s + (16 * np + (lane & 7) + 8 * (lane >> 4)) * RLB + RC_W * 2 +
+                              16 * ((lane >> 3) & 1),
+                          pack_bf16x2(-w0[0], -w0[1]), pack_bf16x2(-w0[2], -w0[3]),
+                          pack_bf16x2(-w1[0], -w1[1]), pack_bf16x2(-w1[2], -w1[3]));
             }
         }
-        fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(x.bar(B_PP_FULL + pp));
-            mbar_arrive(x.bar(B_IN_EMPTY + st));
-        }
+        if (lane == 0) mbar_arrive(x.bar(B_REC_FULL + slot));
     }
 }
 
-// ------------------------------------------------------------------ state
-__device__ __forceinline__ void write_state_operand(const Ctx &x, const float (&S)[64], int j,
-                                                    int cbase) {
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-        uint4 w;
-        w.x = pack_bf16x2(S[8 * g + 0], S[8 * g + 1]);
-        w.y = pack_bf16x2(S[8 * g + 2], S[8 * g + 3]);
-        w.z = pack_bf16x2(S[8 * g + 4], S[8 * g + 5]);
-        w.w = pack_bf16x2(S[8 * g + 6], S[8 * g + 7]);
-        *(uint4 *)(x.smem + SA_OFF + kmaj_off(j, cbase + 8 * g, 2048)) = w;
-    }
-}
-
-__device__ void state_role(const Ctx &x) {
+// ------------------------------------------------------------------ chain
+template <bool WANT_Q, bool WANT_V>
+__device__ __forceinline__ void chain_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sw = warp - W_STATE0;
-    const int quarter = warp & 3;
-    const int half = sw >> 2;       // 0: dk channels 0..63 and U; 1: channels 64..127 and O
-    const int j = 32 * quarter + lane;  // state column (dv index) = TMEM lane
-    const int cbase = 64 * half;
-    const uint32_t lane_addr = x.tmem + ((uint32_t)(32 * quarter) << 16);
+    const int cw = (threadIdx.x >> 5) - W_CHAIN0;
+    const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
+    const int j0 = 16 * cw;
     const size_t unit = (size_t)x.n * p.H + x.h;
 
-    float S[64];
+    // S^T[j][i] for j = j0 + g8 (+8), i = 8n + 2t4 (+1)
+    float S[16][4];
     {
         const float *src = nullptr;
         if (!x.transfer)
             src = p.seg_init ? p.seg_init + (unit * p.Sg + x.s) * (size_t)D * D
                              : (p.S0 ? p.S0 + unit * (size_t)D * D : nullptr);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-            const int i = cbase + e;
-            S[e] = x.partA ? (i == j ? 1.f : 0.f) : (src ? src[(size_t)i * D + j] : 0.f);
-        }
+        for (int n = 0; n < 16; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 8 * n + 2 * t4 + (e & 1), j = j0 + g8 + 8 * (e >> 1);
+                S[n][e] = x.partA ? (i == j ? 1.f : 0.f) : (src ? src[(size_t)i * D + j] : 0.f);
+            }
     }
-    write_state_operand(x, S, j, cbase);
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(x.bar(B_SREADY));
 
     // output destination: the prefill's out, or in the transfer pass the zero-start
     // chain's outputs (out) and the identity-start chain's A_t^T q_t (aux_out)
     __nv_bfloat16 *out = (__nv_bfloat16 *)(x.partA ? p.aux_out : p.out);
+    const uint32_t ost_s = x.sbase + OST_OFF + cw * OST_SIZE;
+    const uint8_t *ost = x.smem + OST_OFF + cw * OST_SIZE;
     for (int c = 0; c < x.nchunks; ++c) {
-        const int pp = c % NP;
-        const uint8_t *pp_s = x.smem + PP_OFF + pp * PP_SIZE;
-        if (!warp_wait(x, B_PP_FULL + pp, (c / NP) & 1)) break;
-        if (half == 0) {
-            if (!warp_wait(x, B_MMA1, c & 1)) break;
-            tc_fence_after();
-            float X[16];
-            tmem_ld16(lane_addr + D1_COL + (c & 1) * 32, X);
-            const float *Ut = (const float *)(pp_s + PP_UT);
-            uint32_t w[8];
+        const int slot = c % NR;
+        if (!warp_wait(x, B_REC_FULL + slot, (c / NR) & 1)) break;
+        const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
+        const float *decay = (const float *)(x.smem + REC_OFF + slot * R_SIZE + R_DECAY);
+
+        // U^T = V^T T^T - S^T W^T (j x r) in fp32, as two partial sums over the
+        // 16-channel k-steps (even / odd) to halve the dependent accumulation
+        float U0[2][4] = {}, U1[2][4] = {};
+        if (WANT_V) {
+            uint32_t va[4], tb[4];
+            ldsm_x4_t(rec_s + R_V + (8 * (lane >> 4) + (lane & 7)) * VROWB +
+                          (j0 + 8 * ((lane >> 3) & 1)) * 2,
+                      va);
+            ldsm_x4(rec_s + R_T + (8 * (lane >> 4) + (lane & 7)) * (TL * 2) + 16 * ((lane >> 3) & 1),
+                    tb);
+            mma_bf16_16816(U1[0], va, tb[0], tb[1]);
+            mma_bf16_16816(U1[1], va, tb[2], tb[3]);
+        }
+        float O[2][4] = {};  // (Qh S)^T, then + (Mq U)^T
+        {
+            uint32_t bw[2][4], bq[2][4];
+            auto load_b = [&](int kk, uint32_t (&w)[4], uint32_t (&q)[4]) {
+                const uint32_t brow =
+                    rec_s + (16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1)) * RLB + 16 * (lane >> 4);
+                ldsm_x4_t(brow + RC_W * 2, w);
+                if (WANT_Q) ldsm_x4_t(brow + RC_Q * 2, q);
+            };
+            load_b(0, bw[0], bq[0]);
 #pragma unroll
-            for (int r = 0; r < C; r += 2)
-                w[r >> 1] = pack_bf16x2(Ut[r * UT_LD + j] - X[r], Ut[(r + 1) * UT_LD + j] - X[r + 1]);
-            *(uint4 *)(x.smem + UA_OFF + kmaj_off(j, 0, 256)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *(uint4 *)(x.smem + UA_OFF + kmaj_off(j, 8, 256)) = make_uint4(w[4], w[5], w[6], w[7]);
-            fence_async_smem();
-            tc_fence_before();
+            for (int kk = 0; kk < 8; ++kk) {
+                if (kk + 1 < 8) load_b(kk + 1, bw[(kk + 1) & 1], bq[(kk + 1) & 1]);
+                const uint32_t a[4] = {pack_bf16x2(S[2 * kk][0], S[2 * kk][1]),
+                                       pack_bf16x2(S[2 * kk][2], S[2 * kk][3]),
+                                       pack_bf16x2(S[2 * kk + 1][0], S[2 * kk + 1][1]),
+                                       pack_bf16x2(S[2 * kk + 1][2], S[2 * kk + 1][3])};
+                const uint32_t(&w)[4] = bw[kk & 1];
+                if (kk & 1) {
+                    mma_bf16_16816(U1[0], a, w[0], w[1]);
+                    mma_bf16_16816(U1[1], a, w[2], w[3]);
+                } else {
+                    mma_bf16_16816(U0[0], a, w[0], w[1]);
+                    mma_bf16_16816(U0[1], a, w[2], w[3]);
+                }
+                if (WANT_Q) {
+                    const uint32_t(&q)[4] = bq[kk & 1];
+                    mma_bf16_16816(O[0], a, q[0], q[1]);
+                    mma_bf16_16816(O[1], a, q[2], q[3]);
+                }
+            }
+        }
+        const uint32_t ua[4] = {pack_bf16x2(U0[0][0] + U1[0][0], U0[0][1] + U1[0][1]),
+                                pack_bf16x2(U0[0][2] + U1[0][2], U0[0][3] + U1[0][3]),
+                                pack_bf16x2(U0[1][0] + U1[1][0], U0[1][1] + U1[1][1]),
+                                pack_bf16x2(U0[1][2] + U1[1][2], U0[1][3] + U1[1][3])};
+
+        // S^T <- S^T Diag(e^{Gamma_C}) + U^T Kb
+        {
+            uint32_t kb[2][4];
+            auto load_kb = [&](int np, uint32_t (&f)[4]) {
+                ldsm_x4(rec_s + (16 * np + (lane & 7) + 8 * (lane >> 4)) * RLB + RC_K * 2 +
+                            16 * ((lane >> 3) & 1),
+                        f);
+            };
+            load_kb(0, kb[0]);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                if (np + 1 < 8) load_kb(np + 1, kb[(np + 1) & 1]);
+                const float2 d0 = *(const float2 *)(decay + 16 * np + 2 * t4);
+                const float2 d1 = *(const float2 *)(decay + 16 * np + 8 + 2 * t4);
+                S[2 * np][0] *= d0.x; S[2 * np][1] *= d0.y;
+                S[2 * np][2] *= d0.x; S[2 * np][3] *= d0.y;
+                S[2 * np + 1][0] *= d1.x; S[2 * np + 1][1] *= d1.y;
+                S[2 * np + 1][2] *= d1.x; S[2 * np + 1][3] *= d1.y;
+                const uint32_t(&f)[4] = kb[np & 1];
+                mma_bf16_16816(S[2 * np], ua, f[0], f[1]);
+                mma_bf16_16816(S[2 * np + 1], ua, f[2], f[3]);
+            }
+        }
+
+        if (WANT_Q) {
+            uint32_t mq[4];
+            ldsm_x4(rec_s + R_MQ + (8 * (lane >> 4) + (lane & 7)) * (TL * 2) + 16 * ((lane >> 3) & 1),
+                    mq);
+            mma_bf16_16816(O[0], ua, mq[0], mq[1]);
+            mma_bf16_16816(O[1], ua, mq[2], mq[3]);
+            // O^T (j x r) -> staging [r][j], then one 16-byte store per (token, half)
+            stsm_x4_t(ost_s + ((lane & 7) + 8 * (lane >> 4)) * 32 + 16 * ((lane >> 3) & 1),
+                      pack_bf16x2(O[0][0], O[0][1]), pack_bf16x2(O[0][2], O[0][3]),
+                      pack_bf16x2(O[1][0], O[1][1]), pack_bf16x2(O[1][2], O[1][3]));
             __syncwarp();
-            if (lane == 0) mbar_arrive(x.bar(B_UREADY));
-        }
-        if (!warp_wait(x, B_MMA3, c & 1)) break;
-        tc_fence_after();
-        const float *decay = (const float *)(pp_s + PP_DECAY) + cbase;
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-            float Dv[32];
-            tmem_ld32(lane_addr + D3_COL + cbase + 32 * blk, Dv);
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                S[32 * blk + e] = fmaf(decay[32 * blk + e], S[32 * blk + e], Dv[e]);
-        }
-        write_state_operand(x, S, j, cbase);
-        fence_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(x.bar(B_SREADY));
-            mbar_arrive(x.bar(B_PP_EMPTY + pp));
-        }
-        if (half == 1 && x.want_q) {
-            float O[16];
-            tmem_ld16(lane_addr + D1_COL + (c & 1) * 32 + 16, O);
-            tc_fence_before();
             const int t0 = x.t_begin + C * c;
-            const int nt = min(C, x.t_end - t0);
-#pragma unroll
-            for (int r = 0; r < C; ++r)
-                if (r < nt) out[((size_t)(t0 + r) * p.H + x.h) * D + j] = __float2bfloat16_rn(O[r]);
+            const int r = lane >> 1, half = lane & 1;
+            if (r < x.t_end - t0)
+                *(uint4 *)(out + ((size_t)(t0 + r) * p.H + x.h) * D + j0 + 8 * half) =
+                    *(const uint4 *)(ost + r * 32 + half * 16);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x.bar(B_REC_EMPTY + slot));
     }
     if (*x.abort) return;
 
@@ -534,8 +533,18 @@ __device__ void state_role(const Ctx &x) {
     }
     if (dst) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) dst[(size_t)(cbase + e) * D + j] = S[e];
+        for (int n = 0; n < 16; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[(size_t)(8 * n + 2 * t4 + (e & 1)) * D + j0 + g8 + 8 * (e >> 1)] = S[n][e];
     }
+}
+
+template <bool WANT_Q, bool WANT_V>
+__device__ __forceinline__ void run_role(const Ctx &x, int warp) {
+    if (warp == W_PROD) producer_role(x);
+    else if (warp < W_CHAIN0) prep_role<WANT_Q, WANT_V>(x);
+    else chain_role<WANT_Q, WANT_V>(x);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -546,7 +555,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     // Align by pointer arithmetic on the __shared__ array (not through an integer),
     // so accesses keep the shared address space instead of becoming generic.
-    uint8_t *smem = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t *smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
     Ctx x;
     x.p = &p;
     x.tm_q = reinterpret_cast<uint64_t>(&tm_q);
@@ -555,8 +564,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     x.tm_g = reinterpret_cast<uint64_t>(&tm_g);
     x.smem = smem;
     x.sbase = smem_addr(smem);
-    x.abort = (volatile int *)(smem + MISC_OFF + 4);
-    x.prep_ok = (volatile int *)(smem + MISC_OFF + 8);
+    x.abort = (volatile int *)(smem + MISC_OFF);
     const int u = blockIdx.x;
     x.n = u / (p.H * p.seg_count);
     x.h = (u / p.seg_count) % p.H;
@@ -573,47 +581,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(x.bar(B_IN_FULL + i), 2);
-            mbar_init(x.bar(B_IN_EMPTY + i), N_PREP);
+            mbar_init(x.bar(B_IN_EMPTY + i), 1);
         }
-        for (int i = 0; i < NP; ++i) {
-            mbar_init(x.bar(B_PP_FULL + i), N_PREP);
-            mbar_init(x.bar(B_PP_EMPTY + i), 1 + N_STATE);
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(x.bar(B_REC_FULL + i), 1);
+            mbar_init(x.bar(B_REC_EMPTY + i), N_CHAIN);
         }
-        mbar_init(x.bar(B_MMA1), 1);
-        mbar_init(x.bar(B_UREADY), N_STATE / 2);
-        mbar_init(x.bar(B_MMA3), 1);
-        mbar_init(x.bar(B_SREADY), N_STATE);
         *x.abort = 0;
-        *x.prep_ok = 0;
         mbar_fence_init();
     }
-    if (warp == W_MMA) {
-        tmem_alloc(x.sbase + MISC_OFF, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    x.tmem = *(volatile uint32_t *)(smem + MISC_OFF);
 
-    if (warp == W_PROD) {
-        producer_role(x);
-    } else if (warp == W_MMA) {
-        if ((threadIdx.x & 31) == 0) mma_role(x);
-        __syncwarp();
-    } else if (warp < W_STATE0) {
-        prep_role(x);
+    if (x.want_q) {
+        if (x.want_v) run_role<true, true>(x, warp);
+        else run_role<true, false>(x, warp);
     } else {
-        state_role(x);
+        if (x.want_v) run_role<false, true>(x, warp);
+        else run_role<false, false>(x, warp);
     }
 
-    tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) report_abort(x);
-    if (warp == W_MMA) {
-        tc_fence_after();
-        tmem_dealloc(x.tmem, TMEM_COLS);
-    }
+    if (threadIdx.x == 0 && *x.abort) dev_fail(p.dev_status, KDA_ERR_TIMEOUT);
 }
 
 }  // namespace
