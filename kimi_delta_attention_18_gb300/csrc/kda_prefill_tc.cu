@@ -10,8 +10,8 @@
 //   prep (state-free):  Gamma = cumsum g;  Kh = K e^{Gamma};  Kt = K e^{-Gamma};
 //                       Qh = Q e^{Gamma};  Kb = K e^{Gamma_C - Gamma};
 //                       L = Diag(beta) strict_lower(Kh Kt^T);  Mq = lower(Qh Kt^T);
-//                       T = (I + L)^{-1} Diag(beta);  W = T Kh
-//   chain (sequential): U = T V - W S;  O = Qh S + Mq U;  S <- e^{Gamma_C} S + Kb^T U
+//                       T = (I + L)^{-1} Diag(beta)
+//   chain (sequential): U = T (V - Kh S);  O = Qh S + Mq U;  S <- e^{Gamma_C} S + Kb^T U
 // The digest's FlashKDA overlaps the intra-block work with the cross-block state
 // propagation (section 2.4 (1)); here that is warp specialisation in one CTA per
 // (sequence, head, segment):
@@ -59,13 +59,16 @@ using namespace sm100;
 
 constexpr int C = 16;    // tokens per block
 constexpr int D = 128;   // dk = dv
-// Input stage and record slot i belong to prep warp i (blocks i, i + 4, ...), so
-// every wait on their barriers is at most one phase ahead of the barrier: a
-// stage shared between prep warps could be waited on two phases early, where
-// the parity test cannot tell the phases apart.
+// Input stage i belongs to prep warp i (blocks i, i + 4, ...): a waiter must
+// know that the barrier's previous phase has completed, or the parity test
+// cannot tell that phase from the one it waits for.  A prep warp consumed its
+// stage's previous phase itself; a stage shared between prep warps could still
+// be one phase behind.  Record slots need no such ownership: with at least
+// N_PREP of them, the release a prep warp waits for is always the barrier's
+// next phase.
 constexpr int N_PREP = 4;
 constexpr int NS = N_PREP;  // input stages (TMA ring)
-constexpr int NR = N_PREP;  // record slots (prepared blocks waiting for the chain)
+constexpr int NR = N_PREP + 1;  // record slots (prepared blocks waiting for the chain)
 constexpr int W_PROD = 0, W_PREP0 = 1, W_CHAIN0 = W_PREP0 + N_PREP, N_CHAIN = 8;
 constexpr int NWARPS = W_CHAIN0 + N_CHAIN;
 constexpr int NTHREADS = NWARPS * 32;
@@ -82,8 +85,8 @@ constexpr int IN_B = IN_G + C * 512;            // beta fp32 [16]
 constexpr int IN_SIZE = IN_B + 128;
 // record: the chain's operands for one block; released by the chain warps
 constexpr int RL = 56;                          // BF16 elements per channel row (112 B):
-constexpr int RLB = RL * 2;                     //   [-W^T (16) | Qh^T (16) | Kb^T (16) | pad]
-constexpr int RC_W = 0, RC_Q = 16, RC_K = 32;
+constexpr int RLB = RL * 2;                     //   [Kh^T (16) | Qh^T (16) | Kb^T (16) | pad]
+constexpr int RC_KH = 0, RC_Q = 16, RC_K = 32;
 constexpr int TL = 24;                          // T and Mq rows: 16 BF16 + pad (48 B)
 constexpr int VROWB = 272;                      // V rows: 128 BF16 + pad
 constexpr int R_T = D * RLB;                    // T  [r][r'] BF16
@@ -93,8 +96,7 @@ constexpr int R_V = R_DECAY + D * 4;            // V  [r][j] BF16 (rows past the
 constexpr int R_SIZE = R_V + C * VROWB;
 // prep scratch (private to one prep warp)
 constexpr int TROW = 48;                        // one channel's 16 positions, BF16, padded
-constexpr int X_KH = 0;                         // Kh^T [128 ch][24]
-constexpr int X_KT = X_KH + D * TROW;           // Kt^T [128 ch][24]
+constexpr int X_KT = 0;                         // Kt^T [128 ch][24]
 constexpr int X_L = X_KT + D * TROW;            // Diag(beta) L fp32 [16][17]
 constexpr int X_SIZE = (X_L + C * 17 * 4 + 127) & ~127;
 constexpr int IN_OFF = 0;
@@ -187,7 +189,7 @@ __device__ __forceinline__ void producer_role(const Ctx &x) {
 
 // ------------------------------------------------------------------ prep
 // Elementwise factors of one block for the key channels lane + 32 m (m = 0..3):
-// Kh^T and Kt^T rows into the prep scratch, Qh^T and Kb^T rows and e^{Gamma_C}
+// Kt^T rows into the prep scratch, Kh^T, Qh^T and Kb^T rows and e^{Gamma_C}
 // into the record.  Every row of the boxes is in shared memory, so the loads are
 // unconditional; with MASK (the sequence's last, partial block) rows past its
 // end get no decay, no key and no query.  Full blocks take the unmasked form,
@@ -236,7 +238,7 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
         float tmp[C];
 #pragma unroll
         for (int r = 0; r < C; ++r) tmp[r] = kv[r] * fwd[r];
-        put_row(scr + X_KH + ch * TROW, tmp);
+        put_row(rec + ch * RLB + RC_KH * 2, tmp);
 #pragma unroll
         for (int r = 0; r < C; ++r) tmp[r] = kv[r] * (einv * rev[r]);
         put_row(scr + X_KT + ch * TROW, tmp);
@@ -255,8 +257,8 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
     }
 }
 
-// One warp prepares one whole block: elementwise factors, L and Mq, the solve
-// for T, and W = T Kh, written with V into a record slot.  Prep warp p takes
+// One warp prepares one whole block: elementwise factors, L and Mq and the
+// solve for T, written with V into a record slot.  Prep warp p takes
 // blocks p, p + 4, p + 8, ...; it frees the input stage as soon as it has read it.
 template <bool WANT_Q, bool WANT_V>
 __device__ __forceinline__ void prep_role(const Ctx &x) {
@@ -307,8 +309,8 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
                 ldsm_x4_t(scr_s + X_KT + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * TROW +
                               (lane >> 4) * 16,
                           bf);
-                // A (positions x channels) from Kh^T rows, transposed
-                ldsm_x4_t(scr_s + X_KH + (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * TROW +
+                // A (positions x channels) from the record's Kh^T rows, transposed
+                ldsm_x4_t(rec_s + (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * RLB + RC_KH * 2 +
                               ((lane >> 3) & 1) * 16,
                           af);
                 mma_bf16_16816(accL[0], af, bf[0], bf[1]);
@@ -361,34 +363,6 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
         }
         __syncwarp();
 
-        // ---- W = T Kh (16 x 128, K = 16); -W^T into the record rows, transposed stores
-        {
-            uint32_t af[4];
-            ldsm_x4(rec_s + R_T + (lane & 15) * (TL * 2) + (lane >> 4) * 16, af);
-            uint32_t bf[2][4];
-            // B (positions x channels) = Kh, stored channel-major: plain ldmatrix
-            auto load_kh = [&](int np, uint32_t (&f)[4]) {
-                ldsm_x4(scr_s + X_KH + (16 * np + (lane & 7) + ((lane >> 4) << 3)) * TROW +
-                            ((lane >> 3) & 1) * 16,
-                        f);
-            };
-            load_kh(0, bf[0]);
-#pragma unroll
-            for (int np = 0; np < 8; ++np) {
-                if (np + 1 < 8) load_kh(np + 1, bf[(np + 1) & 1]);
-                const uint32_t(&b)[4] = bf[np & 1];
-                float w0[4] = {}, w1[4] = {};
-                mma_bf16_16816(w0, af, b[0], b[1]);
-                mma_bf16_16816(w1, af, b[2], b[3]);
-                // matrices: (channels 16np.., rows 0-7), (16np.., rows 8-15),
-                //           (16np+8.., rows 0-7), (16np+8.., rows 8-15)
-                stsm_x4_t(rec_s + (16 * np + (lane & 7) + 8 * (lane >> 4)) * RLB + RC_W * 2 +
-                              16 * ((lane >> 3) & 1),
-                          pack_bf16x2(-w0[0], -w0[1]), pack_bf16x2(-w0[2], -w0[3]),
-                          pack_bf16x2(-w1[0], -w1[1]), pack_bf16x2(-w1[2], -w1[3]));
-            }
-        }
-        __syncwarp();
         if (lane == 0) mbar_arrive(x.bar(B_REC_FULL + slot));
     }
 }
@@ -429,43 +403,47 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
         const float *decay = (const float *)(x.smem + REC_OFF + slot * R_SIZE + R_DECAY);
 
-        // U^T = V^T T^T - S^T W^T (j x r) in fp32, as two partial sums over the
-        // 16-channel k-steps (even / odd) to halve the dependent accumulation
-        float U0[2][4] = {}, U1[2][4] = {};
+        // E^T = S^T Kh^T - V^T (j x r) = -(V - Kh S)^T in fp32, as two partial sums
+        // over the 16-channel k-steps (even / odd) to halve the dependent chain.
+        // V^T is loaded as an A fragment, whose element positions are those of
+        // the 16 x 16 accumulator pair, so it seeds E directly.
+        float E0[2][4] = {}, E1[2][4] = {};
         if (WANT_V) {
-            uint32_t va[4], tb[4];
+            uint32_t va[4];
             ldsm_x4_t(rec_s + R_V + (8 * (lane >> 4) + (lane & 7)) * VROWB +
                           (j0 + 8 * ((lane >> 3) & 1)) * 2,
                       va);
-            ldsm_x4(rec_s + R_T + (8 * (lane >> 4) + (lane & 7)) * (TL * 2) + 16 * ((lane >> 3) & 1),
-                    tb);
-            mma_bf16_16816(U1[0], va, tb[0], tb[1]);
-            mma_bf16_16816(U1[1], va, tb[2], tb[3]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 v2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&va[q]));
+                E1[q >> 1][2 * (q & 1)] = -v2.x;
+                E1[q >> 1][2 * (q & 1) + 1] = -v2.y;
+            }
         }
         float O[2][4] = {};  // (Qh S)^T, then + (Mq U)^T
         {
-            uint32_t bw[2][4], bq[2][4];
+            uint32_t bk[2][4], bq[2][4];
             auto load_b = [&](int kk, uint32_t (&w)[4], uint32_t (&q)[4]) {
                 const uint32_t brow =
                     rec_s + (16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1)) * RLB + 16 * (lane >> 4);
-                ldsm_x4_t(brow + RC_W * 2, w);
+                ldsm_x4_t(brow + RC_KH * 2, w);
                 if (WANT_Q) ldsm_x4_t(brow + RC_Q * 2, q);
             };
-            load_b(0, bw[0], bq[0]);
+            load_b(0, bk[0], bq[0]);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                if (kk + 1 < 8) load_b(kk + 1, bw[(kk + 1) & 1], bq[(kk + 1) & 1]);
+                if (kk + 1 < 8) load_b(kk + 1, bk[(kk + 1) & 1], bq[(kk + 1) & 1]);
                 const uint32_t a[4] = {pack_bf16x2(S[2 * kk][0], S[2 * kk][1]),
                                        pack_bf16x2(S[2 * kk][2], S[2 * kk][3]),
                                        pack_bf16x2(S[2 * kk + 1][0], S[2 * kk + 1][1]),
                                        pack_bf16x2(S[2 * kk + 1][2], S[2 * kk + 1][3])};
-                const uint32_t(&w)[4] = bw[kk & 1];
+                const uint32_t(&w)[4] = bk[kk & 1];
                 if (kk & 1) {
-                    mma_bf16_16816(U1[0], a, w[0], w[1]);
-                    mma_bf16_16816(U1[1], a, w[2], w[3]);
+                    mma_bf16_16816(E1[0], a, w[0], w[1]);
+                    mma_bf16_16816(E1[1], a, w[2], w[3]);
                 } else {
-                    mma_bf16_16816(U0[0], a, w[0], w[1]);
-                    mma_bf16_16816(U0[1], a, w[2], w[3]);
+                    mma_bf16_16816(E0[0], a, w[0], w[1]);
+                    mma_bf16_16816(E0[1], a, w[2], w[3]);
                 }
                 if (WANT_Q) {
                     const uint32_t(&q)[4] = bq[kk & 1];
@@ -474,10 +452,21 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
                 }
             }
         }
-        const uint32_t ua[4] = {pack_bf16x2(U0[0][0] + U1[0][0], U0[0][1] + U1[0][1]),
-                                pack_bf16x2(U0[0][2] + U1[0][2], U0[0][3] + U1[0][3]),
-                                pack_bf16x2(U0[1][0] + U1[1][0], U0[1][1] + U1[1][1]),
-                                pack_bf16x2(U0[1][2] + U1[1][2], U0[1][3] + U1[1][3])};
+        // U^T = (V - Kh S)^T T^T = -E^T T^T
+        float U[2][4] = {};
+        {
+            const uint32_t ea[4] = {pack_bf16x2(-(E0[0][0] + E1[0][0]), -(E0[0][1] + E1[0][1])),
+                                    pack_bf16x2(-(E0[0][2] + E1[0][2]), -(E0[0][3] + E1[0][3])),
+                                    pack_bf16x2(-(E0[1][0] + E1[1][0]), -(E0[1][1] + E1[1][1])),
+                                    pack_bf16x2(-(E0[1][2] + E1[1][2]), -(E0[1][3] + E1[1][3]))};
+            uint32_t tb[4];
+            ldsm_x4(rec_s + R_T + (8 * (lane >> 4) + (lane & 7)) * (TL * 2) + 16 * ((lane >> 3) & 1),
+                    tb);
+            mma_bf16_16816(U[0], ea, tb[0], tb[1]);
+            mma_bf16_16816(U[1], ea, tb[2], tb[3]);
+        }
+        const uint32_t ua[4] = {pack_bf16x2(U[0][0], U[0][1]), pack_bf16x2(U[0][2], U[0][3]),
+                                pack_bf16x2(U[1][0], U[1][1]), pack_bf16x2(U[1][2], U[1][3])};
 
         // S^T <- S^T Diag(e^{Gamma_C}) + U^T Kb
         {
