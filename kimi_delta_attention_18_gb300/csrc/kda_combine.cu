@@ -9,7 +9,8 @@
 //     out[t, h, :] += start_s^T aux_out[t, h, :]
 // a dense (tokens x dk) x (dk x dv) product per segment, fully parallel.
 //   BF16, dk = dv = 128: mma.sync m16n8k16 (start_s rounded to BF16, fp32
-//       accumulation); one CTA per (sequence, head, segment, 64-token tile).
+//       accumulation); one CTA per (sequence, head, segment, group of 64-token
+//       tiles), so each start state is converted once per group.
 //   fp32 (any dk, dv <= 128): CUDA cores, fp32 throughout.
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
@@ -35,88 +36,103 @@ __device__ __forceinline__ bool tile_range(const PrefillArgs &p, int u, int tile
     return t0 < t1;
 }
 
-constexpr int SB_LD = 136;  // padded bf16 row (272 bytes)
+constexpr int SB_LD = 136;  // padded bf16 row (272 bytes): ldmatrix rows hit distinct banks
+constexpr int BF_WARPS = 8;
+constexpr int BF16_SMEM = (128 + BF_WARPS * 16) * SB_LD * 2;
 
-constexpr int BF16_SMEM = (128 + TILE) * SB_LD * 2;
-
-__global__ void __launch_bounds__(128) combine_bf16_kernel(const __grid_constant__ PrefillArgs p,
-                                                           const float *starts,
-                                                           const __nv_bfloat16 *aux, int tile) {
+// One CTA per (sequence, head, segment, group of `gtiles` 64-token tiles): start_s
+// is converted to BF16 in shared memory once, then each warp takes 16-token slabs
+// of the group on its own (aux rows staged in its private shared rows, the
+// product on mma.sync, out read, corrected in fp32 and rewritten).
+__global__ void __launch_bounds__(BF_WARPS * 32) combine_bf16_kernel(
+    const __grid_constant__ PrefillArgs p, const float *starts, const __nv_bfloat16 *aux,
+    int group_base, int gtiles) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    __nv_bfloat16 *Sb = (__nv_bfloat16 *)smem_raw;    // start_s, [i][j]
-    __nv_bfloat16 *Ab = Sb + 128 * SB_LD;              // aux tile, [t][i]
-    int h, s, t0, t1;
-    if (!tile_range(p, blockIdx.x, tile + blockIdx.y, h, s, t0, t1)) return;
+    __nv_bfloat16 *Sb = (__nv_bfloat16 *)smem_raw;  // start_s, [i][j]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const size_t unit = (size_t)(blockIdx.x / p.Sg);  // (n, h)
+    __nv_bfloat16 *Ab = Sb + 128 * SB_LD + warp * 16 * SB_LD;  // this warp's aux rows [t][i]
+    const int u = blockIdx.x;
+    const int n = u / (p.H * p.Sg), h = (u / p.Sg) % p.H, s = u % p.Sg;
+    if (s < p.seg_begin) return;  // segments before seg_begin start from zeros
+    int a, b;
+    if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b)) return;
+    const int t0 = a + (group_base + blockIdx.y) * gtiles * TILE;
+    const int t1 = min(b, t0 + gtiles * TILE);
+    if (t0 >= t1) return;
+    const size_t unit = (size_t)(u / p.Sg);  // (n, h)
     const float *st = starts + (unit * p.Sg + s) * 128 * 128;
     // Loads are issued in batches (all in flight at once), then converted and stored.
 #pragma unroll 1
-    for (int base = 0; base < 128 * 32; base += 128 * 8) {  // 128 rows x 32 float4
+    for (int base = 0; base < 128 * 32; base += BF_WARPS * 32 * 8) {  // 128 rows x 32 float4
         float4 v[8];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int e = base + tid + 128 * b;
-            v[b] = *(const float4 *)(st + (e >> 5) * 128 + 4 * (e & 31));
+        for (int q = 0; q < 8; ++q) {
+            const int e = base + tid + BF_WARPS * 32 * q;
+            v[q] = *(const float4 *)(st + (e >> 5) * 128 + 4 * (e & 31));
         }
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int e = base + tid + 128 * b;
+        for (int q = 0; q < 8; ++q) {
+            const int e = base + tid + BF_WARPS * 32 * q;
             uint2 w;
-            w.x = pack_bf16x2(v[b].x, v[b].y);
-            w.y = pack_bf16x2(v[b].z, v[b].w);
+            w.x = pack_bf16x2(v[q].x, v[q].y);
+            w.y = pack_bf16x2(v[q].z, v[q].w);
             *(uint2 *)(Sb + (e >> 5) * SB_LD + 4 * (e & 31)) = w;
         }
     }
-    const int nt = t1 - t0;
-    {
-        uint4 w[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {  // 64 rows x 16 chunks of 16 bytes
-            const int e = tid + 128 * b, r = e >> 4, c8 = e & 15;
-            w[b] = r < nt ? *(const uint4 *)(aux + ((size_t)(t0 + r) * p.H + h) * 128 + 8 * c8)
-                          : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int e = tid + 128 * b, r = e >> 4, c8 = e & 15;
-            *(uint4 *)(Ab + r * SB_LD + 8 * c8) = w[b];
-        }
-    }
     __syncthreads();
-    if (warp * 16 >= nt) return;
 
-    float acc[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
     const uint32_t ab = smem_addr(Ab), sbb = smem_addr(Sb);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        uint32_t af[4];
-        ldsm_x4(ab + ((warp * 16 + (lane & 15)) * SB_LD + kk * 16 + (lane >> 4) * 8) * 2, af);
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-            uint32_t bf[4];
-            ldsm_x4_t(sbb + ((kk * 16 + (lane & 15)) * SB_LD + np * 16 + (lane >> 4) * 8) * 2, bf);
-            mma_bf16_16816(acc[2 * np], af, bf[0], bf[1]);
-            mma_bf16_16816(acc[2 * np + 1], af, bf[2], bf[3]);
-        }
-    }
     __nv_bfloat16 *out = (__nv_bfloat16 *)p.out;
     const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll 1
+    for (int r0 = t0 + 16 * warp; r0 < t1; r0 += 16 * BF_WARPS) {
+        const int nt = min(16, t1 - r0);
+        {
+            uint4 w[8];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const int r = warp * 16 + g8 + 8 * hh;
-        if (r >= nt) continue;
-        __nv_bfloat162 *orow = (__nv_bfloat162 *)(out + ((size_t)(t0 + r) * p.H + h) * 128 + 2 * t4);
-        __nv_bfloat162 cur[16];
+            for (int q = 0; q < 8; ++q) {  // 16 rows x 16 chunks of 16 bytes
+                const int e = lane + 32 * q, r = e >> 4, c8 = e & 15;
+                w[q] = r < nt ? *(const uint4 *)(aux + ((size_t)(r0 + r) * p.H + h) * 128 + 8 * c8)
+                              : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-        for (int n = 0; n < 16; ++n) cur[n] = orow[4 * n];  // all 16 reads in flight
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            const float2 c = __bfloat1622float2(cur[n]);
-            orow[4 * n] = __floats2bfloat162_rn(c.x + acc[n][2 * hh], c.y + acc[n][2 * hh + 1]);
+            for (int q = 0; q < 8; ++q) {
+                const int e = lane + 32 * q, r = e >> 4, c8 = e & 15;
+                *(uint4 *)(Ab + r * SB_LD + 8 * c8) = w[q];
+            }
         }
+        __syncwarp();
+        float acc[16][4];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t af[4];
+            ldsm_x4(ab + ((lane & 15) * SB_LD + kk * 16 + (lane >> 4) * 8) * 2, af);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                uint32_t bf[4];
+                ldsm_x4_t(sbb + ((kk * 16 + (lane & 15)) * SB_LD + np * 16 + (lane >> 4) * 8) * 2, bf);
+                mma_bf16_16816(acc[2 * np], af, bf[0], bf[1]);
+                mma_bf16_16816(acc[2 * np + 1], af, bf[2], bf[3]);
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int r = g8 + 8 * hh;
+            if (r >= nt) continue;
+            __nv_bfloat162 *orow =
+                (__nv_bfloat162 *)(out + ((size_t)(r0 + r) * p.H + h) * 128 + 2 * t4);
+            __nv_bfloat162 cur[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) cur[q] = orow[4 * q];  // all 16 reads in flight
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float2 c = __bfloat1622float2(cur[q]);
+                orow[4 * q] = __floats2bfloat162_rn(c.x + acc[q][2 * hh], c.y + acc[q][2 * hh + 1]);
+            }
+        }
+        __syncwarp();  // the staging rows are rewritten for the next slab
     }
 }
 
@@ -159,39 +175,54 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
     const long long blocks = ((long long)a.T_tot + 15) / 16;
     const long long seg_tokens = 16 * ((blocks + a.Sg - 1) / a.Sg);
     const long long tiles = (seg_tokens + TILE - 1) / TILE;
-    // grid.y is limited to 65535: launch tile ranges one after another
+    if (a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128) {
+        // Tiles per CTA: about one CTA per SM, each reusing its converted start
+        // state for as many tiles as that allows (at least two: the eight warps
+        // take 128 tokens per pass).
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess)
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const long long active = units - (long long)a.N * a.H * a.seg_begin;
+        long long gtiles = active > 0 ? (active * tiles) / sms : 2;
+        gtiles = gtiles < 2 ? 2 : gtiles;
+        gtiles = gtiles > tiles ? tiles : gtiles;
+        const long long groups = (tiles + gtiles - 1) / gtiles;
+        cudaError_t e = cudaFuncSetAttribute(combine_bf16_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             BF16_SMEM);
+        if (e != cudaSuccess) return e;
+        // grid.y is limited to 65535: launch group ranges one after another
+        for (long long base = 0; base < groups; base += 65535) {
+            const unsigned ny = (unsigned)(groups - base < 65535 ? groups - base : 65535);
+            combine_bf16_kernel<<<dim3((unsigned)units, ny), BF_WARPS * 32, BF16_SMEM, st>>>(
+                a, starts, (const __nv_bfloat16 *)aux_out, (int)base, (int)gtiles);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     for (long long base = 0; base < tiles; base += 65535) {
         const unsigned ny = (unsigned)(tiles - base < 65535 ? tiles - base : 65535);
         dim3 grid((unsigned)units, ny);
-        if (a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128) {
-            cudaError_t e = cudaFuncSetAttribute(combine_bf16_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 BF16_SMEM);
+        const size_t smem = ((size_t)a.dk * a.dv + (size_t)TILE * a.dk) * sizeof(float);
+        cudaError_t e;
+        if (a.act == KDA_DTYPE_F32) {
+            e = cudaFuncSetAttribute(combine_simt_kernel<float>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            combine_bf16_kernel<<<grid, 128, BF16_SMEM, st>>>(
-                a, starts, (const __nv_bfloat16 *)aux_out, (int)base);
+            combine_simt_kernel<float><<<grid, 256, smem, st>>>(a, starts, (const float *)aux_out,
+                                                                (int)base);
         } else {
-            const size_t smem = ((size_t)a.dk * a.dv + (size_t)TILE * a.dk) * sizeof(float);
-            cudaError_t e;
-            if (a.act == KDA_DTYPE_F32) {
-                e = cudaFuncSetAttribute(combine_simt_kernel<float>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                if (e != cudaSuccess) return e;
-                combine_simt_kernel<float><<<grid, 256, smem, st>>>(a, starts,
-                                                                    (const float *)aux_out,
-                                                                    (int)base);
-            } else {
-                e = cudaFuncSetAttribute(combine_simt_kernel<__nv_bfloat16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                if (e != cudaSuccess) return e;
-                combine_simt_kernel<__nv_bfloat16><<<grid, 256, smem, st>>>(
-                    a, starts, (const __nv_bfloat16 *)aux_out, (int)base);
-            }
+            e = cudaFuncSetAttribute(combine_simt_kernel<__nv_bfloat16>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            combine_simt_kernel<__nv_bfloat16><<<grid, 256, smem, st>>>(
+                a, starts, (const __nv_bfloat16 *)aux_out, (int)base);
         }
-        cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace kda

@@ -16,19 +16,20 @@
 // propagation (section 2.4 (1)); here that is warp specialisation in one CTA per
 // (sequence, head, segment):
 //
-//   warp 0      producer: one 2D tensor-map TMA copy per array per block (q, k, v:
-//               16 x 128 BF16 boxes; g: 16 x 128 fp32) into a 4-stage input ring,
-//               beta by prefetched loads
-//   warps 1-4   prep: warp p prepares blocks p, p+4, p+8, ... on its own (no
-//               barrier between prep warps), so four blocks are in preparation at
-//               once.  It frees its input stage as soon as it has read it and
-//               writes the block's chain operands, V included, into its record
-//               slot.
-//   warps 5-12  chain: warp w owns the state columns j in [16w, 16w+16): rows j of
-//               S^T, all 128 key channels, held as fp32 mma.sync accumulators.
-//               Columns of S never mix, so each warp runs the recurrence of its 16
-//               columns entirely in its own registers; per block it reads only the
-//               record and signals when it is done with it.
+//   warps 0-3   prep: warp p owns input stage p and prepares blocks p, p+4, p+8,
+//               ... on its own (no barrier between prep warps), so four blocks are
+//               in preparation at once.  It loads its own blocks (one 2D
+//               tensor-map TMA copy per array: q, k, v as 16 x 128 BF16 boxes, g
+//               as a 16 x 128 fp32 box; beta by loads one block ahead), issuing
+//               the next block's copy into its stage as soon as it has read the
+//               current one, and writes each block's chain operands, V included,
+//               into one of five record slots.
+//   warps 4-7   chain: warp w owns the state columns j in [32w, 32w+32): rows j of
+//               S^T, all 128 key channels, held as fp32 mma.sync accumulators in
+//               two 16-row m-tiles that share every operand fragment.  Columns of
+//               S never mix, so each warp runs the recurrence of its columns
+//               entirely in its own registers; per block it reads only the record
+//               and signals when it is done with it.
 //
 // The chain is a strict sequence of small products (16 x 128 x 128 per block).
 // Kept in registers, one step costs a handful of dependent mma.sync issues and
@@ -42,8 +43,9 @@
 //   A (16x16): a0 = A[g8][2t4..+1], a1 = A[g8+8][2t4..+1], a2 = A[g8][2t4+8..+9],
 //              a3 = A[g8+8][2t4+8..+9];  B (16x8): b0 = B[2t4..+1][g8], b1 = B[2t4+8..+9][g8];
 //   C (16x8):  c0,c1 = C[g8][2t4..+1], c2,c3 = C[g8+8][2t4..+1].
-// A chain warp's S^T accumulator n (n = 0..15) covers key channels [8n, 8n+8); two
-// adjacent accumulators are exactly the A fragment of one 16-channel k-step.
+// A chain warp's S^T accumulator n (n = 0..15) of an m-tile covers key channels
+// [8n, 8n+8); two adjacent accumulators are exactly the A fragment of one
+// 16-channel k-step.
 //
 // Every wait is bounded: a stalled barrier sets an abort flag, records
 // KDA_ERR_TIMEOUT in dev_status, and all roles leave their loops and return.
@@ -69,7 +71,7 @@ constexpr int D = 128;   // dk = dv
 constexpr int N_PREP = 4;
 constexpr int NS = N_PREP;  // input stages (TMA ring)
 constexpr int NR = N_PREP + 1;  // record slots (prepared blocks waiting for the chain)
-constexpr int W_PROD = 0, W_PREP0 = 1, W_CHAIN0 = W_PREP0 + N_PREP, N_CHAIN = 8;
+constexpr int W_PREP0 = 0, W_CHAIN0 = W_PREP0 + N_PREP, N_CHAIN = 4;
 constexpr int NWARPS = W_CHAIN0 + N_CHAIN;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr long long kWaitLimit = 4000000000ll;  // ~2 s of SM clocks
@@ -81,8 +83,7 @@ constexpr int IN_Q = 0;                         // BF16 [16][128]
 constexpr int IN_K = IN_Q + C * IN_ROWB;
 constexpr int IN_V = IN_K + C * IN_ROWB;
 constexpr int IN_G = IN_V + C * IN_ROWB;        // fp32 [16][128]
-constexpr int IN_B = IN_G + C * 512;            // beta fp32 [16]
-constexpr int IN_SIZE = IN_B + 128;
+constexpr int IN_SIZE = IN_G + C * 512;
 // record: the chain's operands for one block; released by the chain warps
 constexpr int RL = 56;                          // BF16 elements per channel row (112 B):
 constexpr int RLB = RL * 2;                     //   [Kh^T (16) | Qh^T (16) | Kb^T (16) | pad]
@@ -103,12 +104,11 @@ constexpr int IN_OFF = 0;
 constexpr int REC_OFF = IN_OFF + NS * IN_SIZE;
 constexpr int X_OFF = REC_OFF + NR * R_SIZE;
 constexpr int OST_OFF = X_OFF + N_PREP * X_SIZE;  // per chain warp: O^T staging [16 r][16 j]
-constexpr int OST_SIZE = C * 16 * 2;
+constexpr int OST_SIZE = 2 * C * 16 * 2;  // two m-tiles
 constexpr int BAR_OFF = OST_OFF + N_CHAIN * OST_SIZE;
 enum {
     B_IN_FULL = 0,
-    B_IN_EMPTY = B_IN_FULL + NS,
-    B_REC_FULL = B_IN_EMPTY + NS,
+    B_REC_FULL = B_IN_FULL + NS,
     B_REC_EMPTY = B_REC_FULL + NR,
     NBARS = B_REC_EMPTY + NR
 };
@@ -137,54 +137,6 @@ __device__ __forceinline__ bool warp_wait(const Ctx &x, int b, uint32_t parity) 
     int ok = 0;
     if ((threadIdx.x & 31) == 0) ok = mbar_wait(x.bar(b), parity, x.abort, kWaitLimit);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// ------------------------------------------------------------------ producer
-__device__ __forceinline__ void producer_role(const Ctx &x) {
-    const PrefillArgs &p = *x.p;
-    const int lane = threadIdx.x & 31;
-    int issued = 0;
-    // beta is strided (one value per token at stride H): lane r loads the next
-    // block's value one iteration ahead, so the load's latency overlaps the wait
-    // for a free stage instead of stalling the producer.
-    auto load_beta = [&](int c) {
-        const int t0 = x.t_begin + C * c;
-        return (c < x.nchunks && lane < C && lane < x.t_end - t0)
-                   ? p.beta[(size_t)(t0 + lane) * p.H + x.h]
-                   : 0.f;
-    };
-    float beta_next = load_beta(0);
-    for (int c = 0; c < x.nchunks; ++c) {
-        const int st = c % NS;
-        const float beta_cur = beta_next;
-        beta_next = load_beta(c + 1);
-        if (!warp_wait(x, B_IN_EMPTY + st, ((c / NS) & 1) ^ 1)) break;
-        const int t0 = x.t_begin + C * c;
-        const uint32_t full = x.bar(B_IN_FULL + st);
-        const uint32_t base = x.sbase + IN_OFF + st * IN_SIZE;
-        if (lane == 0) {
-            // Whole 16-row boxes: rows past the block's end hold the next sequence's
-            // tokens (masked by the prep warp) or, past the array, zero fill.
-            const uint32_t bytes =
-                (x.want_q ? 4096u : 0u) + 4096u + (x.want_v ? 4096u : 0u) + 8192u;
-            mbar_arrive_expect_tx(full, bytes);
-            const int xc = x.h * D;
-            if (x.want_q) tma_load_2d(base + IN_Q, x.tm_q, xc, t0, full);
-            tma_load_2d(base + IN_K, x.tm_k, xc, t0, full);
-            if (x.want_v) tma_load_2d(base + IN_V, x.tm_v, xc, t0, full);
-            tma_load_2d(base + IN_G, x.tm_g, xc, t0, full);
-        }
-        if (lane < C) ((float *)(x.smem + IN_OFF + st * IN_SIZE + IN_B))[lane] = beta_cur;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full);  // second arrival: beta is in place
-        issued = c + 1;
-    }
-    // On an abort, let copies already in flight land before the CTA can exit.
-    if (*x.abort && lane == 0) {
-        volatile int never = 0;
-        for (int c = max(0, issued - NS); c < issued; ++c)
-            mbar_wait(x.bar(B_IN_FULL + c % NS), (c / NS) & 1, &never, kWaitLimit);
-    }
 }
 
 // ------------------------------------------------------------------ prep
@@ -262,24 +214,59 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
 // blocks p, p + 4, p + 8, ...; it frees the input stage as soon as it has read it.
 template <bool WANT_Q, bool WANT_V>
 __device__ __forceinline__ void prep_role(const Ctx &x) {
+    const PrefillArgs &p = *x.p;
     const int pw = (threadIdx.x >> 5) - W_PREP0;
     const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
     uint8_t *scr = x.smem + X_OFF + pw * X_SIZE;
     const uint32_t scr_s = x.sbase + X_OFF + pw * X_SIZE;
     float *Lf = (float *)(scr + X_L);
+    const int st = pw;  // this warp's input stage
+    const uint32_t full = x.bar(B_IN_FULL + st);
+    const uint32_t in_s = x.sbase + IN_OFF + st * IN_SIZE;
+    const uint8_t *in = x.smem + IN_OFF + st * IN_SIZE;
 
-    for (int c = pw; c < x.nchunks; c += N_PREP) {
-        const int st = c % NS, slot = c % NR;
+    // The warp loads its own blocks: one 2D tensor-map TMA copy per array (whole
+    // 16-row boxes; rows past the block's end hold the next sequence's tokens,
+    // masked below, or past the array zero fill).
+    auto issue = [&](int c) {
+        if (lane == 0) {
+            const uint32_t bytes =
+                (WANT_Q ? 4096u : 0u) + 4096u + (WANT_V ? 4096u : 0u) + 8192u;
+            mbar_arrive_expect_tx(full, bytes);
+            const int xc = x.h * D, t0 = x.t_begin + C * c;
+            if (WANT_Q) tma_load_2d(in_s + IN_Q, x.tm_q, xc, t0, full);
+            tma_load_2d(in_s + IN_K, x.tm_k, xc, t0, full);
+            if (WANT_V) tma_load_2d(in_s + IN_V, x.tm_v, xc, t0, full);
+            tma_load_2d(in_s + IN_G, x.tm_g, xc, t0, full);
+        }
+    };
+    // beta of rows g8 and g8 + 8 (for L) and of column lane (for T), zero past the
+    // block's end; loaded one block ahead
+    auto load_beta = [&](int c, float &lo, float &hi, float &col) {
+        const int t0 = x.t_begin + C * c, nt = min(C, x.t_end - t0);
+        const float *bp = p.beta + (size_t)t0 * p.H + x.h;
+        lo = g8 < nt ? bp[(size_t)g8 * p.H] : 0.f;
+        hi = g8 + 8 < nt ? bp[(size_t)(g8 + 8) * p.H] : 0.f;
+        col = (lane & 15) < nt ? bp[(size_t)(lane & 15) * p.H] : 0.f;
+    };
+    int issued = 0;  // blocks whose copies were issued (for an orderly abort)
+    float b_lo = 0.f, b_hi = 0.f, b_col = 0.f;
+    if (pw < x.nchunks) {
+        issue(pw);
+        issued = 1;
+        load_beta(pw, b_lo, b_hi, b_col);
+    }
+
+    int uses = 0;  // completed uses of the input stage
+    for (int c = pw; c < x.nchunks; c += N_PREP, ++uses) {
+        const int slot = c % NR;
+        const float beta_lo = b_lo, beta_hi = b_hi, beta_col = b_col;
+        if (c + N_PREP < x.nchunks) load_beta(c + N_PREP, b_lo, b_hi, b_col);
         if (!warp_wait(x, B_REC_EMPTY + slot, ((c / NR) & 1) ^ 1)) break;
-        if (!warp_wait(x, B_IN_FULL + st, (c / NS) & 1)) break;
-        const uint8_t *in = x.smem + IN_OFF + st * IN_SIZE;
+        if (!warp_wait(x, B_IN_FULL + st, uses & 1)) break;
         uint8_t *rec = x.smem + REC_OFF + slot * R_SIZE;
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
-        const float *bin = (const float *)(in + IN_B);
         const int nt = min(C, x.t_end - (x.t_begin + C * c));
-        // beta of rows g8 and g8 + 8 (for L) and of column lane (for T), kept in
-        // registers: the input stage is released before they are needed
-        const float beta_lo = bin[g8], beta_hi = bin[g8 + 8], beta_col = bin[lane & 15];
 
         // ---- elementwise: lane handles key channels lane + 32 m
         if (nt == C) elementwise<WANT_Q, false>(in, scr, rec, nt, lane);
@@ -297,7 +284,13 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(x.bar(B_IN_EMPTY + st));  // input stage fully read
+        // Input stage read: load this warp's next block into it (the generic reads
+        // above are ordered before the copy's writes by the proxy fence).
+        if (c + N_PREP < x.nchunks) {
+            if (lane == 0) fence_async_smem();
+            issue(c + N_PREP);
+            ++issued;
+        }
 
         // ---- L = Diag(beta) strict_lower(Kh Kt^T) and Mq = lower(Qh Kt^T), 16 x 16 x 128
         {
@@ -365,31 +358,43 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
 
         if (lane == 0) mbar_arrive(x.bar(B_REC_FULL + slot));
     }
+    // On an abort, let this warp's copies in flight land before the CTA can exit.
+    if (*x.abort && lane == 0 && issued > uses) {
+        volatile int never = 0;
+        mbar_wait(full, uses & 1, &never, kWaitLimit);
+    }
 }
 
 // ------------------------------------------------------------------ chain
+// Chain warp w owns state columns [32w, 32w+32) as two 16-column m-tiles, which
+// share every B fragment the warp loads from the record.
+constexpr int MT = 2;  // m-tiles per chain warp
+
 template <bool WANT_Q, bool WANT_V>
 __device__ __forceinline__ void chain_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int cw = (threadIdx.x >> 5) - W_CHAIN0;
     const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
-    const int j0 = 16 * cw;
+    const int j0 = 16 * MT * cw;
     const size_t unit = (size_t)x.n * p.H + x.h;
 
-    // S^T[j][i] for j = j0 + g8 (+8), i = 8n + 2t4 (+1)
-    float S[16][4];
+    // S^T[j][i] for j = j0 + 16 m + g8 (+8), i = 8n + 2t4 (+1)
+    float S[MT][16][4];
     {
         const float *src = nullptr;
         if (!x.transfer)
             src = p.seg_init ? p.seg_init + (unit * p.Sg + x.s) * (size_t)D * D
                              : (p.S0 ? p.S0 + unit * (size_t)D * D : nullptr);
 #pragma unroll
-        for (int n = 0; n < 16; ++n)
+        for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = 8 * n + 2 * t4 + (e & 1), j = j0 + g8 + 8 * (e >> 1);
-                S[n][e] = x.partA ? (i == j ? 1.f : 0.f) : (src ? src[(size_t)i * D + j] : 0.f);
-            }
+            for (int n = 0; n < 16; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 8 * n + 2 * t4 + (e & 1), j = j0 + 16 * m + g8 + 8 * (e >> 1);
+                    S[m][n][e] = x.partA ? (i == j ? 1.f : 0.f)
+                                         : (src ? src[(size_t)i * D + j] : 0.f);
+                }
     }
 
     // output destination: the prefill's out, or in the transfer pass the zero-start
@@ -403,24 +408,27 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
         const float *decay = (const float *)(x.smem + REC_OFF + slot * R_SIZE + R_DECAY);
 
-        // E^T = S^T Kh^T - V^T (j x r) = -(V - Kh S)^T in fp32, as two partial sums
-        // over the 16-channel k-steps (even / odd) to halve the dependent chain.
-        // V^T is loaded as an A fragment, whose element positions are those of
-        // the 16 x 16 accumulator pair, so it seeds E directly.
-        float E0[2][4] = {}, E1[2][4] = {};
+        // E^T = S^T Kh^T - V^T (j x r) = -(V - Kh S)^T in fp32.  V^T is loaded as
+        // an A fragment, whose element positions are those of the 16 x 16
+        // accumulator pair, so it seeds E directly.
+        float E[MT][2][4] = {};
         if (WANT_V) {
-            uint32_t va[4];
-            ldsm_x4_t(rec_s + R_V + (8 * (lane >> 4) + (lane & 7)) * VROWB +
-                          (j0 + 8 * ((lane >> 3) & 1)) * 2,
-                      va);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 v2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&va[q]));
-                E1[q >> 1][2 * (q & 1)] = -v2.x;
-                E1[q >> 1][2 * (q & 1) + 1] = -v2.y;
+            for (int m = 0; m < MT; ++m) {
+                uint32_t va[4];
+                ldsm_x4_t(rec_s + R_V + (8 * (lane >> 4) + (lane & 7)) * VROWB +
+                              (j0 + 16 * m + 8 * ((lane >> 3) & 1)) * 2,
+                          va);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 v2 =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&va[q]));
+                    E[m][q >> 1][2 * (q & 1)] = -v2.x;
+                    E[m][q >> 1][2 * (q & 1) + 1] = -v2.y;
+                }
             }
         }
-        float O[2][4] = {};  // (Qh S)^T, then + (Mq U)^T
+        float O[MT][2][4] = {};  // (Qh S)^T, then + (Mq U)^T
         {
             uint32_t bk[2][4], bq[2][4];
             auto load_b = [&](int kk, uint32_t (&w)[4], uint32_t (&q)[4]) {
@@ -433,40 +441,44 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 if (kk + 1 < 8) load_b(kk + 1, bk[(kk + 1) & 1], bq[(kk + 1) & 1]);
-                const uint32_t a[4] = {pack_bf16x2(S[2 * kk][0], S[2 * kk][1]),
-                                       pack_bf16x2(S[2 * kk][2], S[2 * kk][3]),
-                                       pack_bf16x2(S[2 * kk + 1][0], S[2 * kk + 1][1]),
-                                       pack_bf16x2(S[2 * kk + 1][2], S[2 * kk + 1][3])};
                 const uint32_t(&w)[4] = bk[kk & 1];
-                if (kk & 1) {
-                    mma_bf16_16816(E1[0], a, w[0], w[1]);
-                    mma_bf16_16816(E1[1], a, w[2], w[3]);
-                } else {
-                    mma_bf16_16816(E0[0], a, w[0], w[1]);
-                    mma_bf16_16816(E0[1], a, w[2], w[3]);
-                }
-                if (WANT_Q) {
-                    const uint32_t(&q)[4] = bq[kk & 1];
-                    mma_bf16_16816(O[0], a, q[0], q[1]);
-                    mma_bf16_16816(O[1], a, q[2], q[3]);
+                const uint32_t(&q)[4] = bq[kk & 1];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t a[4] = {pack_bf16x2(S[m][2 * kk][0], S[m][2 * kk][1]),
+                                           pack_bf16x2(S[m][2 * kk][2], S[m][2 * kk][3]),
+                                           pack_bf16x2(S[m][2 * kk + 1][0], S[m][2 * kk + 1][1]),
+                                           pack_bf16x2(S[m][2 * kk + 1][2], S[m][2 * kk + 1][3])};
+                    mma_bf16_16816(E[m][0], a, w[0], w[1]);
+                    mma_bf16_16816(E[m][1], a, w[2], w[3]);
+                    if (WANT_Q) {
+                        mma_bf16_16816(O[m][0], a, q[0], q[1]);
+                        mma_bf16_16816(O[m][1], a, q[2], q[3]);
+                    }
                 }
             }
         }
         // U^T = (V - Kh S)^T T^T = -E^T T^T
-        float U[2][4] = {};
+        uint32_t ua[MT][4];
         {
-            const uint32_t ea[4] = {pack_bf16x2(-(E0[0][0] + E1[0][0]), -(E0[0][1] + E1[0][1])),
-                                    pack_bf16x2(-(E0[0][2] + E1[0][2]), -(E0[0][3] + E1[0][3])),
-                                    pack_bf16x2(-(E0[1][0] + E1[1][0]), -(E0[1][1] + E1[1][1])),
-                                    pack_bf16x2(-(E0[1][2] + E1[1][2]), -(E0[1][3] + E1[1][3]))};
             uint32_t tb[4];
             ldsm_x4(rec_s + R_T + (8 * (lane >> 4) + (lane & 7)) * (TL * 2) + 16 * ((lane >> 3) & 1),
                     tb);
-            mma_bf16_16816(U[0], ea, tb[0], tb[1]);
-            mma_bf16_16816(U[1], ea, tb[2], tb[3]);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const uint32_t ea[4] = {pack_bf16x2(-E[m][0][0], -E[m][0][1]),
+                                        pack_bf16x2(-E[m][0][2], -E[m][0][3]),
+                                        pack_bf16x2(-E[m][1][0], -E[m][1][1]),
+                                        pack_bf16x2(-E[m][1][2], -E[m][1][3])};
+                float U[2][4] = {};
+                mma_bf16_16816(U[0], ea, tb[0], tb[1]);
+                mma_bf16_16816(U[1], ea, tb[2], tb[3]);
+                ua[m][0] = pack_bf16x2(U[0][0], U[0][1]);
+                ua[m][1] = pack_bf16x2(U[0][2], U[0][3]);
+                ua[m][2] = pack_bf16x2(U[1][0], U[1][1]);
+                ua[m][3] = pack_bf16x2(U[1][2], U[1][3]);
+            }
         }
-        const uint32_t ua[4] = {pack_bf16x2(U[0][0], U[0][1]), pack_bf16x2(U[0][2], U[0][3]),
-                                pack_bf16x2(U[1][0], U[1][1]), pack_bf16x2(U[1][2], U[1][3])};
 
         // S^T <- S^T Diag(e^{Gamma_C}) + U^T Kb
         {
@@ -482,13 +494,16 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
                 if (np + 1 < 8) load_kb(np + 1, kb[(np + 1) & 1]);
                 const float2 d0 = *(const float2 *)(decay + 16 * np + 2 * t4);
                 const float2 d1 = *(const float2 *)(decay + 16 * np + 8 + 2 * t4);
-                S[2 * np][0] *= d0.x; S[2 * np][1] *= d0.y;
-                S[2 * np][2] *= d0.x; S[2 * np][3] *= d0.y;
-                S[2 * np + 1][0] *= d1.x; S[2 * np + 1][1] *= d1.y;
-                S[2 * np + 1][2] *= d1.x; S[2 * np + 1][3] *= d1.y;
                 const uint32_t(&f)[4] = kb[np & 1];
-                mma_bf16_16816(S[2 * np], ua, f[0], f[1]);
-                mma_bf16_16816(S[2 * np + 1], ua, f[2], f[3]);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    S[m][2 * np][0] *= d0.x; S[m][2 * np][1] *= d0.y;
+                    S[m][2 * np][2] *= d0.x; S[m][2 * np][3] *= d0.y;
+                    S[m][2 * np + 1][0] *= d1.x; S[m][2 * np + 1][1] *= d1.y;
+                    S[m][2 * np + 1][2] *= d1.x; S[m][2 * np + 1][3] *= d1.y;
+                    mma_bf16_16816(S[m][2 * np], ua[m], f[0], f[1]);
+                    mma_bf16_16816(S[m][2 * np + 1], ua[m], f[2], f[3]);
+                }
             }
         }
 
@@ -496,18 +511,25 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
             uint32_t mq[4];
             ldsm_x4(rec_s + R_MQ + (8 * (lane >> 4) + (lane & 7)) * (TL * 2) + 16 * ((lane >> 3) & 1),
                     mq);
-            mma_bf16_16816(O[0], ua, mq[0], mq[1]);
-            mma_bf16_16816(O[1], ua, mq[2], mq[3]);
-            // O^T (j x r) -> staging [r][j], then one 16-byte store per (token, half)
-            stsm_x4_t(ost_s + ((lane & 7) + 8 * (lane >> 4)) * 32 + 16 * ((lane >> 3) & 1),
-                      pack_bf16x2(O[0][0], O[0][1]), pack_bf16x2(O[0][2], O[0][3]),
-                      pack_bf16x2(O[1][0], O[1][1]), pack_bf16x2(O[1][2], O[1][3]));
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                mma_bf16_16816(O[m][0], ua[m], mq[0], mq[1]);
+                mma_bf16_16816(O[m][1], ua[m], mq[2], mq[3]);
+                // O^T (j x r) -> staging [r][j], then one 16-byte store per (token, half)
+                stsm_x4_t(ost_s + m * 512 + ((lane & 7) + 8 * (lane >> 4)) * 32 +
+                              16 * ((lane >> 3) & 1),
+                          pack_bf16x2(O[m][0][0], O[m][0][1]), pack_bf16x2(O[m][0][2], O[m][0][3]),
+                          pack_bf16x2(O[m][1][0], O[m][1][1]), pack_bf16x2(O[m][1][2], O[m][1][3]));
+            }
             __syncwarp();
             const int t0 = x.t_begin + C * c;
             const int r = lane >> 1, half = lane & 1;
-            if (r < x.t_end - t0)
-                *(uint4 *)(out + ((size_t)(t0 + r) * p.H + x.h) * D + j0 + 8 * half) =
-                    *(const uint4 *)(ost + r * 32 + half * 16);
+            if (r < x.t_end - t0) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    *(uint4 *)(out + ((size_t)(t0 + r) * p.H + x.h) * D + j0 + 16 * m + 8 * half) =
+                        *(const uint4 *)(ost + m * 512 + r * 32 + half * 16);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(x.bar(B_REC_EMPTY + slot));
@@ -522,17 +544,19 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
     }
     if (dst) {
 #pragma unroll
-        for (int n = 0; n < 16; ++n)
+        for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                dst[(size_t)(8 * n + 2 * t4 + (e & 1)) * D + j0 + g8 + 8 * (e >> 1)] = S[n][e];
+            for (int n = 0; n < 16; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[(size_t)(8 * n + 2 * t4 + (e & 1)) * D + j0 + 16 * m + g8 + 8 * (e >> 1)] =
+                        S[m][n][e];
     }
 }
 
 template <bool WANT_Q, bool WANT_V>
 __device__ __forceinline__ void run_role(const Ctx &x, int warp) {
-    if (warp == W_PROD) producer_role(x);
-    else if (warp < W_CHAIN0) prep_role<WANT_Q, WANT_V>(x);
+    if (warp < W_CHAIN0) prep_role<WANT_Q, WANT_V>(x);
     else chain_role<WANT_Q, WANT_V>(x);
 }
 
@@ -568,10 +592,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(x.bar(B_IN_FULL + i), 2);
-            mbar_init(x.bar(B_IN_EMPTY + i), 1);
-        }
+        for (int i = 0; i < NS; ++i) mbar_init(x.bar(B_IN_FULL + i), 1);
         for (int i = 0; i < NR; ++i) {
             mbar_init(x.bar(B_REC_FULL + i), 1);
             mbar_init(x.bar(B_REC_EMPTY + i), N_CHAIN);
