@@ -133,10 +133,12 @@ struct Ctx {
     __device__ uint32_t bar(int i) const { return sbase + BAR_OFF + 8 * i; }
 };
 
+// Every lane polls the barrier (each with acquire semantics), so the warp does
+// not split around the wait: a lane-0 wait with the other lanes parked at a
+// shuffle cost thousands of cycles of reconvergence per wait on sm_103a.
 __device__ __forceinline__ bool warp_wait(const Ctx &x, int b, uint32_t parity) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(x.bar(b), parity, x.abort, kWaitLimit);
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    const bool ok = mbar_wait(x.bar(b), parity, x.abort, kWaitLimit);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // ------------------------------------------------------------------ prep
