@@ -3,13 +3,15 @@
 decode tokens/s (256 sequences x 56 heads, 64 single-token steps), with the
 roofline fraction of the dominant kernel.
 
-One step = one whole prefill of the workload through the library's three
-stages (transfer pass over all S segments with outputs, the segment scan, the
-output combine; a single output pass when the library picks S = 1), each
-bracketed by CUDA events on the launching stream.  Inputs are resident in HBM;
-the 50 MB working set is smaller than L2, so a 512 MB buffer is rewritten
-between timed steps (outside the events).  ``e2e`` times the one-call C entry
-point with pinned host buffers, including the copies in and out.
+One step = one whole prefill of the workload through the one-call entry point
+kda_prefill_chunked, bracketed by CUDA events on the launching stream: the
+transfer pass over all S segments with outputs, the segment scan and the output
+combine launched back to back (a single output pass when the library picks
+S = 1).  A separate pass through the three stage entry points, with events
+between them, gives the per-stage times behind the roofline.  Inputs are
+resident in HBM; the 50 MB working set is smaller than L2, so a 512 MB buffer is
+rewritten between timed steps (outside the events).  ``e2e`` times the same
+call with pinned host buffers, including the copies in and out.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own batch (weak scaling, no collective on
@@ -212,7 +214,19 @@ def run_ours(args):
 
     aux = torch.empty((T, H, dk), dtype=x["q"].dtype, device=dev)
 
+    ws_bytes = kda.prefill_workspace_size(desc)
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
     def step(ev):
+        # the call a user makes: kda_prefill_chunked launches the transfer pass,
+        # the segment scan and the output combine back to back (or one output
+        # pass when the split is a single segment)
+        ev[0].record(stream)
+        kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["cu_seqlens"],
+                            out=out, S_final=S_final, workspace=workspace)
+        ev[1].record(stream)
+
+    def staged(ev):
         # exactly the launches kda_prefill_chunked makes, with events between them
         ev[0].record(stream)
         if Sg > 1:
@@ -232,12 +246,12 @@ def run_ours(args):
                                  x["cu_seqlens"], 1, out=out, S_final=S_final)
         ev[3].record(stream)
 
-    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     for _ in range(args.warmup):
         flush.fill_(1)
-        step(mk())
+        step(mk(2))
     torch.cuda.synchronize()
-    events = [mk() for _ in range(args.steps)]
+    events = [mk(2) for _ in range(args.steps)]
     clocks = Clocks(local)
     barrier(dist)
     torch.cuda.synchronize()
@@ -251,18 +265,23 @@ def run_ours(args):
     wall = time.perf_counter() - wall0
     barrier(dist)
     clk = clocks.stop()
-
-    stage_ms = {"transfer_pass": [], "segment_scan": [], "combine": [], "output_pass": []}
-    total_ms = []
-    for ev in events:
-        stage_ms["transfer_pass"].append(ev[0].elapsed_time(ev[1]))
-        stage_ms["segment_scan"].append(ev[1].elapsed_time(ev[2]))
-        stage_ms["combine" if Sg > 1 else "output_pass"].append(ev[2].elapsed_time(ev[3]))
-        total_ms.append(ev[0].elapsed_time(ev[3]))
+    total_ms = [ev[0].elapsed_time(ev[1]) for ev in events]
     dev_ms = sum(total_ms)
     dev_ms_max = max_over_ranks(dev_ms, dist, dev)
     tokens = T * args.steps * world
     value = tokens / (dev_ms_max / 1e3)
+
+    # per-stage device times (a separate pass through the stage entry points; the
+    # host has time to queue each step's launches behind the L2 flush)
+    stage_ms = {"transfer_pass": [], "segment_scan": [], "combine": [], "output_pass": []}
+    for _ in range(max(3, min(args.steps, 10))):
+        ev = mk(4)
+        flush.fill_(1)
+        staged(ev)
+        torch.cuda.synchronize()
+        stage_ms["transfer_pass"].append(ev[0].elapsed_time(ev[1]))
+        stage_ms["segment_scan"].append(ev[1].elapsed_time(ev[2]))
+        stage_ms["combine" if Sg > 1 else "output_pass"].append(ev[2].elapsed_time(ev[3]))
 
     # roofline of the dominant kernel (HBM-bound: see the design notes)
     peaks = measured_peaks()

@@ -76,16 +76,21 @@ __global__ void __launch_bounds__(NT) compose_kernel(int Sg, int dk, int dv, con
 }
 
 // dk = 128, dv a multiple of 8, 16-byte aligned arrays.  One CTA per (unit,
-// 8-column block), two threads per state row, each owning a row x 4-column
-// tile of the running state.  A_s arrives by TMA two steps ahead into a
+// 8-column block), 256 threads.  A_s arrives by TMA two steps ahead into a
 // double-buffered stage (four 128-row x 32-column fp32 boxes with 128-byte
-// swizzle: the 16-byte chunk c of row i sits at chunk c ^ (i mod 8), so the
-// rows a warp walks in step hit different banks); B_{s+1} is prefetched into
-// registers.  The FMA loop therefore never waits on memory.
+// swizzle: the 16-byte chunk c of row i sits at chunk c ^ (i mod 8)); B_{s+1} is
+// prefetched into registers.  The product A_s X is register-blocked: a thread
+// takes rows r, r+32, r+64, r+96 (one swizzle phase, so the 16 rows a warp reads
+// at once hit different banks) and 4 columns over one quarter of the 128 key
+// channels; the four quarters' partial sums meet in shared memory, where each
+// thread then adds up one row x 4 columns of the next state.  The running state
+// is double-buffered, so each step needs two barriers.
 constexpr int FD = 128, FT = 256, FCB = 8;
 constexpr int ABOX = FD * 32 * 4;    // one 128 x 32 fp32 box, 16 KB
 constexpr int ASTAGE = 4 * ABOX;     // A_s, 64 KB
-constexpr int FAST_SMEM = 2 * ASTAGE + FD * FCB * 4 + 64 + 1024;
+constexpr int FX = 2 * FD * FCB;     // running state, two buffers [2][128][8]
+constexpr int FP = 4 * FD * FCB;     // partial sums [4 quarters][128][8]
+constexpr int FAST_SMEM = 2 * ASTAGE + (FX + FP) * 4 + 64 + 1024;
 constexpr long long kWaitLimit = 4000000000ll;
 
 __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -96,15 +101,17 @@ __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__
     // Align by pointer arithmetic on the __shared__ array (not through an integer),
     // so accesses keep the shared address space instead of becoming generic.
     uint8_t *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
-    float *X = (float *)(sm + 2 * ASTAGE);  // [128][8]
-    uint64_t *bars = (uint64_t *)(sm + 2 * ASTAGE + FD * FCB * 4);
+    float *X = (float *)(sm + 2 * ASTAGE);
+    float *P = X + FX;
+    uint64_t *bars = (uint64_t *)(P + FP);
     volatile int *abort = (volatile int *)(bars + 2);
     const uint32_t sb = smem_addr(sm), bar0 = smem_addr(&bars[0]), bar1 = smem_addr(&bars[1]);
     const uint64_t tmap = reinterpret_cast<uint64_t>(&tmA);
-    const int t = threadIdx.x, i = t >> 1, cg = t & 1;
+    const int t = threadIdx.x;
+    const int kq = t >> 6, r = (t >> 1) & 31, cg = t & 1;  // product: quarter, rows r + 32 m
+    const int oi = t >> 1, ocg = t & 1;                     // output: row oi, columns 4 ocg..
     const size_t u = blockIdx.x;
-    const int col = blockIdx.y * FCB + 4 * cg;
-    const size_t row_off = (size_t)i * dv + col;
+    const size_t row_off = (size_t)oi * dv + blockIdx.y * FCB + 4 * ocg;
     const int nsteps = S_final ? Sg : Sg - 1;  // without S_final the last pair is never read
 
     auto issue = [&](int s) {  // one thread: A_s into stage s % 2
@@ -129,12 +136,12 @@ __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__
 
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (S0) x = *(const float4 *)(S0 + u * (size_t)FD * dv + row_off);
-    *(float4 *)(X + i * FCB + 4 * cg) = x;
+    *(float4 *)(X + oi * FCB + 4 * ocg) = x;
     float4 bcur = make_float4(0.f, 0.f, 0.f, 0.f);
     if (nsteps > 0) bcur = *(const float4 *)(B + (u * Sg) * (size_t)FD * dv + row_off);
     __syncthreads();
 
-    const int xi = i & 7;
+    const int xi = r & 7;  // swizzle phase shared by rows r + 32 m
     int s = 0;
     for (; s < Sg; ++s) {
         if (seg_init) *(float4 *)(seg_init + (u * Sg + s) * (size_t)FD * dv + row_off) = x;
@@ -142,36 +149,49 @@ __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__
         float4 bnext = make_float4(0.f, 0.f, 0.f, 0.f);
         if (s + 1 < nsteps) bnext = *(const float4 *)(B + (u * Sg + s + 1) * (size_t)FD * dv + row_off);
         mbar_wait((s & 1) ? bar1 : bar0, (s >> 1) & 1, abort, kWaitLimit);
-        const uint8_t *stage = sm + (s & 1) * ASTAGE + i * 128;
-        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+        const uint8_t *stage = sm + (s & 1) * ASTAGE;
+        const float *Xc = X + (s & 1) * FD * FCB;
+        float acc[4][4] = {};
 #pragma unroll
-        for (int k4 = 0; k4 < 32; ++k4) {
-            const float4 a = *(const float4 *)(stage + (k4 >> 3) * ABOX + (((k4 & 7) ^ xi) << 4));
-            const float4 x0 = *(const float4 *)(X + (4 * k4 + 0) * FCB + 4 * cg);
-            const float4 x1 = *(const float4 *)(X + (4 * k4 + 1) * FCB + 4 * cg);
-            const float4 x2 = *(const float4 *)(X + (4 * k4 + 2) * FCB + 4 * cg);
-            const float4 x3 = *(const float4 *)(X + (4 * k4 + 3) * FCB + 4 * cg);
-            a0.x = fmaf(a.x, x0.x, a0.x); a0.y = fmaf(a.x, x0.y, a0.y);
-            a0.z = fmaf(a.x, x0.z, a0.z); a0.w = fmaf(a.x, x0.w, a0.w);
-            a1.x = fmaf(a.y, x1.x, a1.x); a1.y = fmaf(a.y, x1.y, a1.y);
-            a1.z = fmaf(a.y, x1.z, a1.z); a1.w = fmaf(a.y, x1.w, a1.w);
-            a0.x = fmaf(a.z, x2.x, a0.x); a0.y = fmaf(a.z, x2.y, a0.y);
-            a0.z = fmaf(a.z, x2.z, a0.z); a0.w = fmaf(a.z, x2.w, a0.w);
-            a1.x = fmaf(a.w, x3.x, a1.x); a1.y = fmaf(a.w, x3.y, a1.y);
-            a1.z = fmaf(a.w, x3.z, a1.z); a1.w = fmaf(a.w, x3.w, a1.w);
+        for (int k4h = 0; k4h < 8; ++k4h) {
+            const int k4 = 8 * kq + k4h;
+            const uint8_t *box = stage + (k4 >> 3) * ABOX + (((k4 & 7) ^ xi) << 4);
+            float4 xr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) xr[e] = *(const float4 *)(Xc + (4 * k4 + e) * FCB + 4 * cg);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float4 a = *(const float4 *)(box + (r + 32 * m) * 128);
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[m][0] = fmaf(av[e], xr[e].x, acc[m][0]);
+                    acc[m][1] = fmaf(av[e], xr[e].y, acc[m][1]);
+                    acc[m][2] = fmaf(av[e], xr[e].z, acc[m][2]);
+                    acc[m][3] = fmaf(av[e], xr[e].w, acc[m][3]);
+                }
+            }
         }
-        __syncthreads();  // every read of X and of stage s % 2 is done
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            *(float4 *)(P + (kq * FD + r + 32 * m) * FCB + 4 * cg) =
+                make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+        __syncthreads();  // partials written; every read of X and of stage s % 2 is done
         if (*abort) break;
-        x.x = a0.x + a1.x + bcur.x; x.y = a0.y + a1.y + bcur.y;
-        x.z = a0.z + a1.z + bcur.z; x.w = a0.w + a1.w + bcur.w;
-        *(float4 *)(X + i * FCB + 4 * cg) = x;
-        bcur = bnext;
         if (t == 0 && s + 2 < nsteps) {
-            fence_async_smem();
             issue(s + 2);
             ++issued;
         }
-        __syncthreads();
+        float4 sum = bcur;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 pp = *(const float4 *)(P + (q * FD + oi) * FCB + 4 * ocg);
+            sum.x += pp.x; sum.y += pp.y; sum.z += pp.z; sum.w += pp.w;
+        }
+        x = sum;
+        *(float4 *)(X + ((s + 1) & 1) * FD * FCB + oi * FCB + 4 * ocg) = x;
+        bcur = bnext;
+        __syncthreads();  // next state complete, partials free
     }
     if (*abort) {
         if (t == 0) {
