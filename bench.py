@@ -165,18 +165,22 @@ def prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes):
     transfer pass   : q, k, v, g, beta read once per head-token; the zero-start
                       outputs and A_t^T q_t written (activation dtype); A and B
                       written per (sequence, head, segment).
-    scan            : A, B read, start states and final states written.
+    scan            : A, B read, start states and final states written (and, for
+                      BF16 at d = 128, each start state's BF16 operand image).
     combine         : A_t^T q_t and the zero-start outputs read, outputs written,
-                      start states read.
+                      start states read (their BF16 images for BF16 at d = 128).
     """
     if Sg == 1:
         return {"output_pass": T * H * ((2 * dk + 2 * dv) * act_bytes + 4 * dk + 4) +
                 N * H * dk * dv * 4}
     states = N * H * Sg * (dk * dk + dk * dv) * 4
+    start_bytes = 2 if (act_bytes == 2 and dk == 128 and dv == 128) else 4
     transfer = T * H * ((2 * dk + dv) * act_bytes + 4 * dk + 4) + \
         T * H * (dv + dk) * act_bytes + states
     scan = states + N * H * Sg * dk * dv * 4 + N * H * dk * dv * 4
-    combine = T * H * (dk + 2 * dv) * act_bytes + N * H * Sg * dk * dv * 4
+    if start_bytes == 2:
+        scan += N * H * Sg * dk * dv * 2
+    combine = T * H * (dk + 2 * dv) * act_bytes + N * H * Sg * dk * dv * start_bytes
     return {"transfer_pass": transfer, "segment_scan": scan, "combine": combine}
 
 
@@ -213,6 +217,9 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     aux = torch.empty((T, H, dk), dtype=x["q"].dtype, device=dev)
+    # the start states' BF16 operand images (BF16 at d = 128), as the one-call path uses
+    imgs = (torch.empty((N * H, Sg, dk * dv), dtype=torch.bfloat16, device=dev)
+            if x["q"].dtype == torch.bfloat16 and dk == 128 and dv == 128 else None)
 
     ws_bytes = kda.prefill_workspace_size(desc)
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -237,10 +244,11 @@ def run_ours(args):
         if Sg > 1:
             kda.state_compose(A.view(N * H, Sg, dk, dk), B.view(N * H, Sg, dk, dv), None,
                               seg_init_states=starts.view(N * H, Sg, dk, dv),
-                              S_final=S_final.view(N * H, dk, dv))
+                              S_final=S_final.view(N * H, dk, dv), start_images=imgs)
         ev[2].record(stream)
         if Sg > 1:
-            kda.prefill_combine(out, aux, starts, x["cu_seqlens"], first_segment=1)
+            kda.prefill_combine(out, aux, starts, x["cu_seqlens"], first_segment=1,
+                                start_images=imgs)
         else:
             kda.prefill_segments(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                  x["cu_seqlens"], 1, out=out, S_final=S_final)

@@ -84,9 +84,11 @@ int32_t kda_prefill_num_segments(const kda_prefill_desc_t *desc);
 /*
  * Device workspace, in bytes, that kda_prefill_chunked needs for desc: zero
  * when it runs one pass, else room for N*H*S transfer matrices, zero-initial
- * states and segment start states (fp32) and one dk-vector per token and head
- * in the activation dtype.  Call with the same desc, on the
- * same device, as the prefill itself.
+ * states and segment start states (fp32), for BF16 at dk = dv = 128 also a BF16
+ * copy of each start state laid out as a tensor-core operand (N*H*S x 128 x 128
+ * x 2 bytes), and one dk-vector per token and head in the activation dtype;
+ * each piece rounded up to 256 bytes.  Call with the same desc, on the same
+ * device, as the prefill itself.
  */
 size_t kda_prefill_workspace_size(const kda_prefill_desc_t *desc);
 
@@ -168,11 +170,16 @@ kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begi
  * transfer is [units, segments, dk, dk], zero_init_state [units, segments, dk,
  * dv]; all fp32, 16-byte aligned.  The scan is sequential over segments and
  * parallel over units and column blocks, in fp32.
+ *
+ * start_images (may be NULL; dk = dv = 128 only, else it must be NULL):
+ * [units, segments, 128 * 128] BF16, 16-byte aligned, each start state rounded
+ * to BF16 and laid out as the B operand of kda_prefill_combine's tensor-core
+ * product (an internal layout: only kda_prefill_combine reads it).
  */
 kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int32_t dv,
                                const float *transfer, const float *zero_init_state,
                                const float *S0, float *seg_init_states, float *S_final,
-                               void *stream);
+                               void *start_images, void *stream);
 
 /*
  * Output correction of the context-parallel split: for every token t of the
@@ -182,12 +189,16 @@ kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int3
  * out_transfer [T_tot, H, dk] (from kda_state_transfer) in the activation
  * dtype.  out holds the zero-start outputs on entry and the outputs on exit.
  * first_segment = 1 skips the first segments' correction when they start from
- * zeros.  A dense product per segment (tensor cores for BF16 at d = 128).
+ * zeros.  A dense product per segment on tensor cores for BF16 at d = 128: with
+ * start_images (the BF16 images kda_state_compose wrote for the same states,
+ * 16-byte aligned) through tcgen05, and seg_init_states may then be NULL;
+ * without them from the fp32 states through mma.sync.  Other shapes: fp32 on
+ * CUDA cores from seg_init_states.
  */
 kda_status_t kda_prefill_combine(const kda_prefill_desc_t *desc, int32_t first_segment,
-                                 const float *seg_init_states, const void *out_transfer,
-                                 const int32_t *cu_seqlens, void *out, int32_t *dev_status,
-                                 void *stream);
+                                 const float *seg_init_states, const void *start_images,
+                                 const void *out_transfer, const int32_t *cu_seqlens, void *out,
+                                 int32_t *dev_status, void *stream);
 
 /*
  * Output pass of the context-parallel split: with S = desc->num_segments >= 1

@@ -62,9 +62,9 @@ def lib():
             L.kda_state_transfer.restype = ctypes.c_int
             L.kda_state_transfer.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 12
             L.kda_prefill_combine.restype = ctypes.c_int
-            L.kda_prefill_combine.argtypes = [ctypes.POINTER(PrefillDesc), _I] + [_P] * 6
+            L.kda_prefill_combine.argtypes = [ctypes.POINTER(PrefillDesc), _I] + [_P] * 7
             L.kda_state_compose.restype = ctypes.c_int
-            L.kda_state_compose.argtypes = [_I] * 4 + [_P] * 6
+            L.kda_state_compose.argtypes = [_I] * 4 + [_P] * 7
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_status_string.argtypes = [ctypes.c_int]
             L.kda_build_info.restype = ctypes.c_char_p
@@ -284,9 +284,11 @@ def state_transfer(k, v, g, beta, cu_seqlens, num_segments, *, seg_begin=0, seg_
 
 
 def prefill_combine(out, out_transfer, seg_init_states, cu_seqlens, *, first_segment=0,
-                    dev_status=None, stream=None):
+                    start_images=None, num_segments=None, dev_status=None, stream=None):
     """Add start_s^T (A_t^T q_t) to the zero-start outputs in ``out`` (in place),
-    see kda_prefill_combine in kda.h.  Returns ``out``."""
+    see kda_prefill_combine in kda.h.  ``start_images`` (from state_compose) selects
+    the tcgen05 path; ``seg_init_states`` may then be None, with ``num_segments``
+    given.  Returns ``out``."""
     dev = out.device
     T, H, dv = out.shape
     dk = out_transfer.shape[2]
@@ -297,22 +299,31 @@ def prefill_combine(out, out_transfer, seg_init_states, cu_seqlens, *, first_seg
     _need(out_transfer, "out_transfer", out.dtype, (T, H, dk), dev)
     _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
     N = cu_seqlens.numel() - 1
-    Sg = seg_init_states.shape[2]
-    _need(seg_init_states, "seg_init_states", torch.float32, (N, H, Sg, dk, dv), dev)
+    if seg_init_states is not None:
+        Sg = seg_init_states.shape[2]
+        _need(seg_init_states, "seg_init_states", torch.float32, (N, H, Sg, dk, dv), dev)
+    else:
+        if start_images is None or num_segments is None:
+            raise ValueError("seg_init_states, or start_images with num_segments, is required")
+        Sg = int(num_segments)
+    if start_images is not None:
+        _need(start_images, "start_images", torch.bfloat16, (N * H, Sg, dk * dv), dev)
     desc = _desc(N, T, H, dk, dv, act, Sg)
     rc = lib().kda_prefill_combine(ctypes.byref(desc), int(first_segment), _ptr(seg_init_states),
-                                   _ptr(out_transfer), _ptr(cu_seqlens), _ptr(out),
-                                   _ptr(dev_status), _stream(stream, dev))
+                                   _ptr(start_images), _ptr(out_transfer), _ptr(cu_seqlens),
+                                   _ptr(out), _ptr(dev_status), _stream(stream, dev))
     _check("kda_prefill_combine", rc)
     return out
 
 
 def state_compose(transfer, zero_init_state, S0=None, *, seg_init_states=None, S_final=None,
-                  want_starts=True, want_final_state=True, stream=None):
+                  want_starts=True, want_final_state=True, start_images=None, stream=None):
     """Prefix scan over segments (see kda_state_compose in kda.h): transfer ``[U, S,
     dk, dk]``, zero_init_state ``[U, S, dk, dv]``, S0 ``[U, dk, dv]`` or None.
     Returns ``(seg_init_states [U,S,dk,dv] or None, S_final [U,dk,dv] or None)``;
-    without a final state the last pair is never read."""
+    without a final state the last pair is never read.  ``start_images`` (BF16
+    ``[U, S, 128 * 128]``, dk = dv = 128) also receives each start state as the
+    operand image prefill_combine's tcgen05 path reads."""
     dev = transfer.device
     U, Sg, dk, _ = transfer.shape
     dv = zero_init_state.shape[-1]
@@ -324,7 +335,10 @@ def state_compose(transfer, zero_init_state, S0=None, *, seg_init_states=None, S
         seg_init_states = torch.empty((U, Sg, dk, dv), dtype=torch.float32, device=dev)
     if S_final is None and want_final_state:
         S_final = torch.empty((U, dk, dv), dtype=torch.float32, device=dev)
+    if start_images is not None:
+        _need(start_images, "start_images", torch.bfloat16, (U, Sg, dk * dv), dev)
     rc = lib().kda_state_compose(U, Sg, dk, dv, _ptr(transfer), _ptr(zero_init_state), _ptr(S0),
-                                 _ptr(seg_init_states), _ptr(S_final), _stream(stream, dev))
+                                 _ptr(seg_init_states), _ptr(S_final), _ptr(start_images),
+                                 _stream(stream, dev))
     _check("kda_state_compose", rc)
     return seg_init_states, S_final

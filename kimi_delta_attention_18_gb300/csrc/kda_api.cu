@@ -85,16 +85,26 @@ int choose_segments(const kda_prefill_desc_t *d) {
 size_t act_bytes(const kda_prefill_desc_t *d) { return d->act_dtype == KDA_DTYPE_BF16 ? 2 : 4; }
 
 // Split workspace: transfer matrices, zero-initial states and start states for
-// every (sequence, head, segment) in fp32, then A_t^T q_t for every token
-// (activation dtype), each piece starting on a 256-byte boundary.
+// every (sequence, head, segment) in fp32; for BF16 at dk = dv = 128 also each
+// start state's BF16 operand image (kStartImgElems elements) for the tensor-core
+// combine; then A_t^T q_t for every token (activation dtype).  Each piece
+// starts on a 256-byte boundary.
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+bool wants_start_img(const kda_prefill_desc_t *d) {
+    return d->act_dtype == KDA_DTYPE_BF16 && d->dk == 128 && d->dv == 128;
+}
+size_t states_bytes_for(const kda_prefill_desc_t *d, int Sg) {
+    const size_t units = (size_t)d->num_seqs * d->num_heads * Sg;
+    return round256(units * ((size_t)d->dk * d->dk + 2 * (size_t)d->dk * d->dv) * sizeof(float));
+}
+size_t img_bytes_for(const kda_prefill_desc_t *d, int Sg) {
+    if (!wants_start_img(d)) return 0;
+    return round256((size_t)d->num_seqs * d->num_heads * Sg * kStartImgElems * 2);
+}
 size_t workspace_bytes_for(const kda_prefill_desc_t *d, int Sg) {
     if (Sg <= 1) return 0;
-    const size_t units = (size_t)d->num_seqs * d->num_heads * Sg;
-    const size_t states = round256(units * ((size_t)d->dk * d->dk + 2 * (size_t)d->dk * d->dv) *
-                                   sizeof(float));
     const size_t aux = round256((size_t)d->total_tokens * d->num_heads * d->dk * act_bytes(d));
-    return states + aux;
+    return states_bytes_for(d, Sg) + img_bytes_for(d, Sg) + aux;
 }
 
 cudaError_t run_prefill_pass(const PrefillArgs &a, cudaStream_t st) {
@@ -161,9 +171,10 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     float *A = (float *)workspace;
     float *B = A + units * Sg * desc->dk * desc->dk;
     float *starts = B + units * Sg * desc->dk * desc->dv;
-    void *aux = (uint8_t *)workspace +
-                round256(units * Sg * ((size_t)desc->dk * desc->dk + 2 * (size_t)desc->dk * desc->dv) *
-                         sizeof(float));
+    __nv_bfloat16 *img = wants_start_img(desc)
+                             ? (__nv_bfloat16 *)((uint8_t *)workspace + states_bytes_for(desc, Sg))
+                             : nullptr;
+    void *aux = (uint8_t *)workspace + states_bytes_for(desc, Sg) + img_bytes_for(desc, Sg);
 
     PrefillArgs t = a;
     t.mode = MODE_TRANSFER;
@@ -176,12 +187,12 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     t.S_final = nullptr;
     cudaError_t e = run_prefill_pass(t, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = launch_compose((int)units, Sg, desc->dk, desc->dv, A, B, S0, starts, S_final, dev_status,
-                       st);
+    e = launch_compose((int)units, Sg, desc->dk, desc->dv, A, B, S0, starts, S_final, img,
+                       dev_status, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     PrefillArgs c = a;
     c.seg_begin = S0 ? 0 : 1;  // from zeros the first segment needs no correction
-    return from_cuda(launch_combine(c, starts, aux, st));
+    return from_cuda(launch_combine(c, starts, aux, img, st));
 }
 
 kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_begin,
@@ -217,17 +228,20 @@ kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_be
 }
 
 kda_status_t kda_prefill_combine(const kda_prefill_desc_t *desc, int32_t first_segment,
-                                 const float *seg_init_states, const void *out_transfer,
-                                 const int32_t *cu_seqlens, void *out, int32_t *dev_status,
-                                 void *stream) {
+                                 const float *seg_init_states, const void *start_images,
+                                 const void *out_transfer, const int32_t *cu_seqlens, void *out,
+                                 int32_t *dev_status, void *stream) {
     kda_status_t rc = check_desc(desc);
     if (rc != KDA_OK) return rc;
     if (desc->num_segments < 1 || first_segment < 0) return KDA_ERR_INVALID_ARG;
+    if (start_images && !wants_start_img(desc)) return KDA_ERR_INVALID_ARG;
     if (desc->num_seqs == 0 || desc->total_tokens == 0 || first_segment >= desc->num_segments)
         return KDA_OK;
-    if (!seg_init_states || !out_transfer || !cu_seqlens || !out) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(seg_init_states) || !aligned16(out_transfer) || !aligned16(out) ||
-        !aligned4(cu_seqlens))
+    if ((!seg_init_states && !start_images) || !out_transfer || !cu_seqlens || !out)
+        return KDA_ERR_INVALID_ARG;
+    if ((seg_init_states && !aligned16(seg_init_states)) ||
+        (start_images && !aligned16(start_images)) || !aligned16(out_transfer) ||
+        !aligned16(out) || !aligned4(cu_seqlens))
         return KDA_ERR_INVALID_ARG;
     PrefillArgs c = base_args(desc);
     c.cu = cu_seqlens;
@@ -235,7 +249,8 @@ kda_status_t kda_prefill_combine(const kda_prefill_desc_t *desc, int32_t first_s
     c.dev_status = dev_status;
     c.Sg = desc->num_segments;
     c.seg_begin = first_segment;
-    return from_cuda(launch_combine(c, seg_init_states, out_transfer, (cudaStream_t)stream));
+    return from_cuda(launch_combine(c, seg_init_states, out_transfer,
+                                    (const __nv_bfloat16 *)start_images, (cudaStream_t)stream));
 }
 
 kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv,
@@ -304,16 +319,18 @@ kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begi
 kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int32_t dv,
                                const float *transfer, const float *zero_init_state,
                                const float *S0, float *seg_init_states, float *S_final,
-                               void *stream) {
+                               void *start_images, void *stream) {
     if (units < 0 || segments < 1 || dk < 1 || dv < 1) return KDA_ERR_INVALID_ARG;
     if (dk > kMaxDim || dv > kMaxDim) return KDA_ERR_UNSUPPORTED;
+    if (start_images && (dk != 128 || dv != 128)) return KDA_ERR_INVALID_ARG;
     if (units == 0) return KDA_OK;
     if (!transfer || !zero_init_state) return KDA_ERR_INVALID_ARG;
-    const void *ptrs[] = {transfer, zero_init_state, S0, seg_init_states, S_final};
+    const void *ptrs[] = {transfer, zero_init_state, S0, seg_init_states, S_final, start_images};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
     return from_cuda(launch_compose(units, segments, dk, dv, transfer, zero_init_state, S0,
-                                    seg_init_states, S_final, nullptr, (cudaStream_t)stream));
+                                    seg_init_states, S_final, (__nv_bfloat16 *)start_images,
+                                    nullptr, (cudaStream_t)stream));
 }
 
 const char *kda_status_string(kda_status_t s) {

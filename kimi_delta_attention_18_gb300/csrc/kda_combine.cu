@@ -8,9 +8,14 @@
 // once the scan has produced start_s, this kernel adds the second term:
 //     out[t, h, :] += start_s^T aux_out[t, h, :]
 // a dense (tokens x dk) x (dk x dv) product per segment, fully parallel.
-//   BF16, dk = dv = 128: mma.sync m16n8k16 (start_s rounded to BF16, fp32
-//       accumulation); one CTA per (sequence, head, segment, group of 64-token
-//       tiles), so each start state is converted once per group.
+//   BF16, dk = dv = 128, with the scan's BF16 start images: tcgen05 (one CTA per
+//       (sequence, head, segment, 128-token tile): A_t^T q_t rows by TMA and the
+//       start image by one bulk copy into shared memory, eight MMAs into 128
+//       TMEM columns, fp32 read-back and correction of out).
+//   BF16, dk = dv = 128, from fp32 start states: mma.sync m16n8k16 (start_s
+//       rounded to BF16, fp32 accumulation); one CTA per (sequence, head,
+//       segment, group of 64-token tiles), so each start state is converted once
+//       per group.
 //   fp32 (any dk, dv <= 128): CUDA cores, fp32 throughout.
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
@@ -136,6 +141,122 @@ __global__ void __launch_bounds__(BF_WARPS * 32) combine_bf16_kernel(
     }
 }
 
+// ---- tcgen05 path: D[t][j] = sum_i aux[t][i] start_s[i][j] over a 128-token tile
+constexpr int TC_TILE = 128;
+constexpr int TC_A = 0;         // aux tile: 16 TMA boxes of 8 channels x 128 rows (2 KB each)
+constexpr int TC_B = 32768;     // start image, the same core-matrix layout (rows j)
+constexpr int TC_BAR = 65536;   // [0] operands landed, [8] products done, [16] abort, [24] TMEM base
+constexpr int TC_SMEM = TC_BAR + 32 + 128;  // + slack for aligning the base
+constexpr uint32_t TC_COLS = 128;
+constexpr long long kTcWaitLimit = 4000000000ll;  // ~2 s of SM clocks
+
+// Both operands are K-major without swizzle: core matrices (8 rows x 16 bytes)
+// adjacent along K 2048 bytes apart (one TMA box each for A), 8-row groups 128
+// bytes apart.  The accumulator row m is TMEM lane m, so warp w reads the
+// products of tokens 32w..32w+31 and corrects their out rows in fp32.  All waits
+// are bounded; a CTA that gives up records KDA_ERR_TIMEOUT, lets its copies land
+// and frees its TMEM.
+__global__ void __launch_bounds__(128) combine_tc_kernel(const __grid_constant__ PrefillArgs p,
+                                                         const __grid_constant__ CUtensorMap tm_aux,
+                                                         const __nv_bfloat16 *img, int tile_base) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+    const uint32_t sb = smem_addr(sm);
+    const uint32_t full = sb + TC_BAR, mmad = sb + TC_BAR + 8;
+    volatile int *abort = (volatile int *)(sm + TC_BAR + 16);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int u = blockIdx.x;
+    const int n = u / (p.H * p.Sg), h = (u / p.Sg) % p.H, s = u % p.Sg;
+    if (s < p.seg_begin) return;  // segments before seg_begin start from zeros
+    int a, b;
+    if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b)) return;
+    const int t0 = a + (tile_base + blockIdx.y) * TC_TILE;
+    if (t0 >= b) return;
+    const int nt = min(TC_TILE, b - t0);
+    const size_t unit = (size_t)(u / p.Sg);  // (n, h)
+
+    // this thread's out row, loaded now so the loads overlap the copies and products
+    const int row = 32 * warp + lane;
+    const bool live = row < nt;
+    uint4 *orow = (uint4 *)((__nv_bfloat16 *)p.out + ((size_t)(t0 + row) * p.H + h) * 128);
+    uint4 ov[16];
+    if (live) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) ov[q] = orow[q];
+    }
+
+    if (tid == 0) {
+        mbar_init(full, 1);
+        mbar_init(mmad, 1);
+        *abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(sb + TC_BAR + 24, TC_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *(volatile uint32_t *)(sm + TC_BAR + 24);
+
+    bool landed = false;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(full, 2 * 32768);
+        const uint64_t tmap = reinterpret_cast<uint64_t>(&tm_aux);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) tma_load_2d(sb + TC_A + c * 2048, tmap, h * 128 + 8 * c, t0, full);
+        bulk_g2s(sb + TC_B, img + (unit * p.Sg + s) * (size_t)kStartImgElems, 32768, full);
+        landed = mbar_wait(full, 0, abort, kTcWaitLimit);
+        if (landed) {
+            tc_fence_after();
+            const uint32_t idesc = umma_idesc_bf16(128, 128);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                umma_bf16(tmem, umma_desc(sb + TC_A + kk * 4096, 2048, 128),
+                          umma_desc(sb + TC_B + kk * 4096, 2048, 128), idesc, kk > 0);
+            umma_commit(mmad);
+        }
+    }
+    const bool done = mbar_wait(mmad, 0, abort, kTcWaitLimit);
+    if (__all_sync(0xffffffffu, done)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // 32 columns j at a time
+            float d[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * c, d);
+            if (live) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const __nv_bfloat162 *o2 = (const __nv_bfloat162 *)&ov[4 * c + q4];
+                    const float *dd = d + 8 * q4;
+                    uint4 w;
+                    const float2 f0 = __bfloat1622float2(o2[0]), f1 = __bfloat1622float2(o2[1]);
+                    const float2 f2 = __bfloat1622float2(o2[2]), f3 = __bfloat1622float2(o2[3]);
+                    w.x = pack_bf16x2(f0.x + dd[0], f0.y + dd[1]);
+                    w.y = pack_bf16x2(f1.x + dd[2], f1.y + dd[3]);
+                    w.z = pack_bf16x2(f2.x + dd[4], f2.y + dd[5]);
+                    w.w = pack_bf16x2(f3.x + dd[6], f3.y + dd[7]);
+                    orow[4 * c + q4] = w;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && *abort) {
+        dev_fail(p.dev_status, KDA_ERR_TIMEOUT);
+        if (!landed) {  // let the copies in flight land before the CTA exits
+            volatile int never = 0;
+            mbar_wait(full, 0, &never, kTcWaitLimit);
+        }
+    }
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TC_COLS);
+    }
+}
+
 template <typename TA>
 __global__ void __launch_bounds__(256) combine_simt_kernel(const __grid_constant__ PrefillArgs p,
                                                            const float *starts, const TA *aux,
@@ -168,13 +289,40 @@ __global__ void __launch_bounds__(256) combine_simt_kernel(const __grid_constant
 }  // namespace
 
 cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void *aux_out,
-                           cudaStream_t st) {
+                           const __nv_bfloat16 *start_img, cudaStream_t st) {
     const long long units = (long long)a.N * a.H * a.Sg;
     if (units == 0 || a.T_tot == 0) return cudaSuccess;
     // tokens of one segment: at most ceil(ceil(T_tot / 16) / Sg) blocks of 16
     const long long blocks = ((long long)a.T_tot + 15) / 16;
     const long long seg_tokens = 16 * ((blocks + a.Sg - 1) / a.Sg);
     const long long tiles = (seg_tokens + TILE - 1) / TILE;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
+    if (a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128 && start_img && enc &&
+        ((uintptr_t)start_img & 15u) == 0 && ((uintptr_t)aux_out & 15u) == 0) {
+        // aux viewed as [T_tot, H * 128] BF16, boxes of 8 channels x 128 tokens
+        CUtensorMap tm;
+        const cuuint64_t dims[2] = {(cuuint64_t)a.H * 128, (cuuint64_t)a.T_tot};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.H * 128 * 2};
+        const cuuint32_t box[2] = {8, (cuuint32_t)TC_TILE};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(aux_out), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        cudaError_t e = cudaFuncSetAttribute(combine_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        if (e != cudaSuccess) return e;
+        const long long tc_tiles = (seg_tokens + TC_TILE - 1) / TC_TILE;
+        for (long long base = 0; base < tc_tiles; base += 65535) {
+            const unsigned ny = (unsigned)(tc_tiles - base < 65535 ? tc_tiles - base : 65535);
+            combine_tc_kernel<<<dim3((unsigned)units, ny), 128, TC_SMEM, st>>>(a, tm, start_img,
+                                                                             (int)base);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     if (a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128) {
         // Tiles per CTA: about one CTA per SM, each reusing its converted start
         // state for as many tiles as that allows (at least two: the eight warps

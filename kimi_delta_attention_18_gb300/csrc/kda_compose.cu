@@ -20,7 +20,8 @@ constexpr int CB = 16;  // state columns per CTA
 
 __global__ void __launch_bounds__(NT) compose_kernel(int Sg, int dk, int dv, const float *A,
                                                      const float *B, const float *S0,
-                                                     float *seg_init, float *S_final) {
+                                                     float *seg_init, float *S_final,
+                                                     __nv_bfloat16 *img) {
     extern __shared__ float smem[];
     const int LA = dk + 1;
     float *As = smem;              // [dk][dk+1]
@@ -44,6 +45,13 @@ __global__ void __launch_bounds__(NT) compose_kernel(int Sg, int dk, int dv, con
             for (int e = tid; e < dk * CB; e += NT) {
                 const int i = e / CB, c = e % CB;
                 if (c < nc) dst[(size_t)i * dv + c0 + c] = X[e];
+            }
+        }
+        if (img) {  // dk = dv = 128 only
+            __nv_bfloat16 *im = img + (u * Sg + s) * (size_t)kStartImgElems;
+            for (int e = tid; e < dk * CB; e += NT) {
+                const int i = e / CB, c = e % CB;
+                if (c < nc) im[start_img_index(c0 + c, i)] = __float2bfloat16_rn(X[e]);
             }
         }
         if (s == Sg - 1 && !S_final) break;  // only the start states are wanted
@@ -96,7 +104,8 @@ constexpr long long kWaitLimit = 4000000000ll;
 __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                                                          int Sg, int dv, const float *B,
                                                          const float *S0, float *seg_init,
-                                                         float *S_final, int32_t *dev_status) {
+                                                         float *S_final, __nv_bfloat16 *img,
+                                                         int32_t *dev_status) {
     extern __shared__ uint8_t smem_raw[];
     // Align by pointer arithmetic on the __shared__ array (not through an integer),
     // so accesses keep the shared address space instead of becoming generic.
@@ -145,6 +154,14 @@ __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__
     int s = 0;
     for (; s < Sg; ++s) {
         if (seg_init) *(float4 *)(seg_init + (u * Sg + s) * (size_t)FD * dv + row_off) = x;
+        if (img) {  // dv = 128 only: columns jb..jb+3 of row oi
+            __nv_bfloat16 *im = img + (u * Sg + s) * (size_t)kStartImgElems;
+            const int jb = blockIdx.y * FCB + 4 * ocg;
+            im[start_img_index(jb + 0, oi)] = __float2bfloat16_rn(x.x);
+            im[start_img_index(jb + 1, oi)] = __float2bfloat16_rn(x.y);
+            im[start_img_index(jb + 2, oi)] = __float2bfloat16_rn(x.z);
+            im[start_img_index(jb + 3, oi)] = __float2bfloat16_rn(x.w);
+        }
         if (s >= nsteps) break;
         float4 bnext = make_float4(0.f, 0.f, 0.f, 0.f);
         if (s + 1 < nsteps) bnext = *(const float4 *)(B + (u * Sg + s + 1) * (size_t)FD * dv + row_off);
@@ -208,8 +225,9 @@ __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__
 }  // namespace
 
 cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, const float *B,
-                           const float *S0, float *seg_init, float *S_final, int32_t *dev_status,
-                           cudaStream_t st) {
+                           const float *S0, float *seg_init, float *S_final,
+                           __nv_bfloat16 *start_img, int32_t *dev_status, cudaStream_t st) {
+    if (dk != 128 || dv != 128) start_img = nullptr;
     if (units == 0 || Sg == 0) return cudaSuccess;
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
     PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
@@ -230,7 +248,7 @@ cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, co
                                                  FAST_SMEM);
             if (e != cudaSuccess) return e;
             compose_tma_kernel<<<dim3(units, dv / FCB), FT, FAST_SMEM, st>>>(
-                tm, Sg, dv, B, S0, seg_init, S_final, dev_status);
+                tm, Sg, dv, B, S0, seg_init, S_final, start_img, dev_status);
             return cudaGetLastError();
         }
     }
@@ -239,7 +257,7 @@ cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, co
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(units, (dv + CB - 1) / CB);
-    compose_kernel<<<grid, NT, smem, st>>>(Sg, dk, dv, A, B, S0, seg_init, S_final);
+    compose_kernel<<<grid, NT, smem, st>>>(Sg, dk, dv, A, B, S0, seg_init, S_final, start_img);
     return cudaGetLastError();
 }
 

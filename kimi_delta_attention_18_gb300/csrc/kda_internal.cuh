@@ -80,14 +80,25 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t st);
 bool prefill_tc_supported(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st);
 cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, const float *B,
-                           const float *S0, float *seg_init, float *S_final, int32_t *dev_status,
-                           cudaStream_t st);
+                           const float *S0, float *seg_init, float *S_final,
+                           __nv_bfloat16 *start_img, int32_t *dev_status, cudaStream_t st);
 bool decode_tma_supported(int dk, int dv);
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,
                               const void *v, const float *g, const float *beta, float *S,
                               void *out, cudaStream_t st);
 cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void *aux_out,
-                           cudaStream_t st);
+                           const __nv_bfloat16 *start_img, cudaStream_t st);
+
+// BF16 image of a 128 x 128 start state as the B operand of a tensor-core
+// product over its 128 key channels i (N = 128 columns j, K = 128 rows i),
+// in the canonical K-major layout without swizzle: 8 x 8 core matrices of 128
+// contiguous bytes (8 rows j of 16 bytes, 8 consecutive i each), core matrices
+// adjacent along K (i) 2048 bytes apart, adjacent along N (j) 128 bytes apart.
+// Element index of (j, i) within one image of 16384 elements:
+__host__ __device__ constexpr int start_img_index(int j, int i) {
+    return (i >> 3) * 1024 + (j >> 3) * 64 + (j & 7) * 8 + (i & 7);
+}
+constexpr int kStartImgElems = 128 * 128;
 cudaError_t launch_decode(int batch, int H, int dk, int dv, int act, const void *q,
                           const void *k, const void *v, const float *g, const float *beta,
                           float *S, void *out, cudaStream_t st);

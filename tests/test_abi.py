@@ -84,6 +84,12 @@ def test_prefill_split_requires_workspace():
     r256 = lambda b: (b + 255) // 256 * 256
     # (A, B, start) per (seq, head, segment) in fp32 + one dk-vector per token and head
     assert need == r256(1 * 2 * 4 * (16 * 16 + 2 * 16 * 16) * 4) + r256(64 * 2 * 16 * 4)
+    # BF16 at dk = dv = 128 adds each start state's BF16 operand image (128 x 128)
+    d2 = _desc(num_seqs=1, num_heads=8, total_tokens=4096, dk=128, dv=128, act_dtype=1,
+               num_segments=9)
+    need2 = kda.prefill_workspace_size(d2)
+    assert need2 == (r256(1 * 8 * 9 * (128 * 128 + 2 * 128 * 128) * 4) +
+                     r256(1 * 8 * 9 * 128 * 128 * 2) + r256(4096 * 8 * 128 * 2))
     assert _prefill(d) == WORKSPACE
     assert _prefill(d, ws=0x40000, ws_len=need - 1) == WORKSPACE
     assert _prefill(d, ws=0x40008, ws_len=need) == WORKSPACE  # misaligned workspace
@@ -116,10 +122,14 @@ def test_decode_and_compose_host_checks():
     assert L.kda_decode_step(4, 2, 16, 16, 1, p, p, p, p, ctypes.c_void_p(0x10002), p, p,
                              None) == INVALID
     assert L.kda_decode_step(0, 2, 16, 16, 1, p, p, p, p, p, p, p, None) == OK
-    assert L.kda_state_compose(2, 0, 16, 16, p, p, None, None, None, None) == INVALID
-    assert L.kda_state_compose(2, 3, 16, 200, p, p, None, None, None, None) == UNSUPPORTED
-    assert L.kda_state_compose(2, 3, 16, 16, None, p, None, None, None, None) == INVALID
-    assert L.kda_state_compose(0, 3, 16, 16, None, None, None, None, None, None) == OK
+    assert L.kda_state_compose(2, 0, 16, 16, p, p, None, None, None, None, None) == INVALID
+    assert L.kda_state_compose(2, 3, 16, 200, p, p, None, None, None, None, None) == UNSUPPORTED
+    assert L.kda_state_compose(2, 3, 16, 16, None, p, None, None, None, None, None) == INVALID
+    assert L.kda_state_compose(0, 3, 16, 16, None, None, None, None, None, None, None) == OK
+    # start images exist only for dk = dv = 128 and must be 16-byte aligned
+    assert L.kda_state_compose(2, 3, 16, 16, p, p, None, None, None, p, None) == INVALID
+    assert L.kda_state_compose(2, 3, 128, 128, p, p, None, None, None,
+                               ctypes.c_void_p(0x10008), None) == INVALID
     d = _desc(num_segments=0)
     assert L.kda_state_transfer(ctypes.byref(d), 0, 1, None, p, p, p, p, p, p, p, None, None, None,
                                 None) == INVALID
@@ -136,6 +146,9 @@ def test_decode_and_compose_host_checks():
     # outputs need q, out_zero and out_transfer together
     assert L.kda_state_transfer(ctypes.byref(d), 0, 4, p, p, p, p, p, p, p, p, p, None, None,
                                 None) == INVALID
-    assert L.kda_prefill_combine(ctypes.byref(d), -1, p, p, p, p, None, None) == INVALID
-    assert L.kda_prefill_combine(ctypes.byref(d), 0, None, p, p, p, None, None) == INVALID
-    assert L.kda_prefill_combine(ctypes.byref(d), 4, None, None, None, None, None, None) == OK
+    assert L.kda_prefill_combine(ctypes.byref(d), -1, p, None, p, p, p, None, None) == INVALID
+    assert L.kda_prefill_combine(ctypes.byref(d), 0, None, None, p, p, p, None, None) == INVALID
+    assert L.kda_prefill_combine(ctypes.byref(d), 4, None, None, None, None, None, None,
+                                 None) == OK
+    # start images only for BF16 at dk = dv = 128
+    assert L.kda_prefill_combine(ctypes.byref(d), 0, p, p, p, p, p, None, None) == INVALID

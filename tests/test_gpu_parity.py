@@ -290,11 +290,25 @@ def test_split_stages_with_output_correction(act, d, first):
     A, B, out, aux = kda.state_transfer(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], nseg,
                                         q=x["q"])
     S0 = None if x["S0"] is None else x["S0"].reshape(N * H, d, d)
-    starts, SF = kda.state_compose(A.reshape(N * H, nseg, d, d), B.reshape(N * H, nseg, d, d), S0)
-    kda.prefill_combine(out, aux, starts.reshape(N, H, nseg, d, d), x["cu_seqlens"],
-                        first_segment=first)
+    # BF16 at d = 128: the scan also writes the start states' BF16 operand images and
+    # the combine reads only those (its tcgen05 path); otherwise the fp32 states
+    imgs = (torch.empty((N * H, nseg, d * d), dtype=torch.bfloat16, device="cuda")
+            if act == "bf16" and d == 128 else None)
+    starts, SF = kda.state_compose(A.reshape(N * H, nseg, d, d), B.reshape(N * H, nseg, d, d), S0,
+                                   start_images=imgs)
+    if imgs is None:
+        kda.prefill_combine(out, aux, starts.reshape(N, H, nseg, d, d), x["cu_seqlens"],
+                            first_segment=first)
+    else:
+        out2 = out.clone()
+        kda.prefill_combine(out, aux, None, x["cu_seqlens"], first_segment=first,
+                            start_images=imgs, num_segments=nseg)
+        kda.prefill_combine(out2, aux, starts.reshape(N, H, nseg, d, d), x["cu_seqlens"],
+                            first_segment=first)
     torch.cuda.synchronize()
     o_ref, S_ref = _oracle_prefill(x)
     tol = TOL[act]
     assert rel_err(_np(out), o_ref) <= tol
     assert rel_err(_np(SF).reshape(N, H, d, d), S_ref) <= tol
+    if imgs is not None:  # the mma.sync path from the fp32 states agrees too
+        assert rel_err(_np(out2), o_ref) <= tol
