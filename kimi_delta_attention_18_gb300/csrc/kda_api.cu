@@ -180,15 +180,18 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     t.mode = MODE_TRANSFER;
     t.seg_begin = 0;
     t.seg_count = Sg;
-    t.transfer = A;
+    // BF16 at d = 128: A goes to the scan as hi/lo BF16 images (the same bytes)
+    __nv_bfloat16 *a_img = wants_start_img(desc) ? (__nv_bfloat16 *)A : nullptr;
+    t.transfer = a_img ? nullptr : A;
+    t.transfer_img = a_img;
     t.zero_state = B;
     t.emit_out = 1;
     t.aux_out = aux;
     t.S_final = nullptr;
     cudaError_t e = run_prefill_pass(t, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = launch_compose((int)units, Sg, desc->dk, desc->dv, A, B, S0, starts, S_final, img,
-                       dev_status, st);
+    e = launch_compose((int)units, Sg, desc->dk, desc->dv, a_img ? nullptr : A, a_img, B, S0,
+                       starts, S_final, img, dev_status, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     PrefillArgs c = a;
     c.seg_begin = S0 ? 0 : 1;  // from zeros the first segment needs no correction
@@ -328,8 +331,8 @@ kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int3
     const void *ptrs[] = {transfer, zero_init_state, S0, seg_init_states, S_final, start_images};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
-    return from_cuda(launch_compose(units, segments, dk, dv, transfer, zero_init_state, S0,
-                                    seg_init_states, S_final, (__nv_bfloat16 *)start_images,
+    return from_cuda(launch_compose(units, segments, dk, dv, transfer, nullptr, zero_init_state,
+                                    S0, seg_init_states, S_final, (__nv_bfloat16 *)start_images,
                                     nullptr, (cudaStream_t)stream));
 }
 

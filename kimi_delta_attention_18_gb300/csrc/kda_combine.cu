@@ -160,6 +160,8 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tm_aux,
                                                          const __nv_bfloat16 *img, int tile_base) {
     extern __shared__ uint8_t smem_raw[];
+    griddep_wait();  // out, A_t^T q_t and the start images come from earlier kernels
+    griddep_launch_dependents();
     uint8_t *sm = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
     const uint32_t sb = smem_addr(sm);
     const uint32_t full = sb + TC_BAR, mmad = sb + TC_BAR + 8;
@@ -316,9 +318,8 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
         const long long tc_tiles = (seg_tokens + TC_TILE - 1) / TC_TILE;
         for (long long base = 0; base < tc_tiles; base += 65535) {
             const unsigned ny = (unsigned)(tc_tiles - base < 65535 ? tc_tiles - base : 65535);
-            combine_tc_kernel<<<dim3((unsigned)units, ny), 128, TC_SMEM, st>>>(a, tm, start_img,
-                                                                             (int)base);
-            e = cudaGetLastError();
+            e = launch_dependent(combine_tc_kernel, dim3((unsigned)units, ny), dim3(128), TC_SMEM, st,
+                                 a, tm, start_img, (int)base);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;

@@ -222,13 +222,218 @@ __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__
     if (S_final) *(float4 *)(S_final + u * (size_t)FD * dv + row_off) = x;
 }
 
+// BF16 workloads at dk = dv = 128, from the transfer pass's hi/lo BF16 images of
+// A_s (A^T stored row-major, i.e. [j][i]).  One CTA per (unit, 8-column block):
+// 8 compute warps and one producer warp.  Compute warp w owns rows [16w, 16w+16)
+// of the next state over all 128 key channels, so no partial sums cross warps
+// and a step needs one barrier among the compute warps.  The product runs on
+// mma.sync with a three-term BF16 split,
+//     A X ~ A_hi X_hi + A_hi X_lo + A_lo X_hi     (fp32 accumulation),
+// whose dropped term and own rounding are ~2^-16 of |A| |X| per step.  The
+// producer warp streams, two steps ahead, A_s hi and lo (64-channel x 128-row
+// boxes, 128-byte swizzle: chunk q of row j sits at q ^ (j mod 8), so transposed
+// ldmatrix rows hit different banks) and this CTA's 8 columns of B_s (one
+// 8 x 128 fp32 box) into a stage; compute warps free a stage through an
+// mbarrier, so neither the copy issue nor a global load sits on the step's
+// critical path.  The running state is kept transposed in fp32 ([column][j],
+// rows padded to 136 floats) and double-buffered.
+constexpr int MB_T = 288;               // 8 compute warps + 1 producer warp
+constexpr int MB_ABOX = 128 * 128;      // one 64-channel x 128-row BF16 box, 16 KB
+constexpr int MB_BBOX = FD * FCB * 4;   // 8 columns x 128 rows of B_s, fp32, 4 KB
+constexpr int MB_STAGE = 4 * MB_ABOX + MB_BBOX;  // hi (2 boxes), lo (2 boxes), B
+constexpr int MB_XLD = 136;             // padded row of the transposed state
+constexpr int MB_X = 2 * MB_STAGE;
+constexpr int MB_XSZ = FCB * MB_XLD * 4;
+constexpr int MB_BAR = MB_X + 2 * MB_XSZ;
+constexpr int MB_SMEM = MB_BAR + 64 + 1024;
+static_assert(MB_STAGE % 1024 == 0, "stages keep the 128-byte swizzle's 1024-byte alignment");
+
+__global__ void __launch_bounds__(MB_T) compose_mma_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                           const __grid_constant__ CUtensorMap tmB,
+                                                           int Sg, const float *S0,
+                                                           float *seg_init, float *S_final,
+                                                           __nv_bfloat16 *img, int32_t *dev_status) {
+    extern __shared__ uint8_t smem_raw[];
+    griddep_wait();  // A_s, B_s come from the transfer pass just before
+    griddep_launch_dependents();
+    uint8_t *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
+    float *Xt = (float *)(sm + MB_X);
+    uint64_t *bars = (uint64_t *)(sm + MB_BAR);  // full[2], empty[2]
+    volatile int *abort = (volatile int *)(bars + 4);
+    const uint32_t sb = smem_addr(sm);
+    auto full = [&](int s) { return smem_addr(&bars[s & 1]); };
+    auto empty = [&](int s) { return smem_addr(&bars[2 + (s & 1)]); };
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31, g8 = lane >> 2, t4 = lane & 3;
+    const size_t u = blockIdx.x;
+    const int c0 = blockIdx.y * FCB;
+    const int nsteps = S_final ? Sg : Sg - 1;  // without S_final the last pair is never read
+    constexpr int dv = 128;
+    constexpr int NCW = 8;  // compute warps
+
+    if (t == 0) {
+        mbar_init(full(0), 1);
+        mbar_init(full(1), 1);
+        mbar_init(empty(0), NCW);
+        mbar_init(empty(1), NCW);
+        *abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (w == NCW) {  // ---- producer: A_s hi / lo and B_s columns into stage s % 2
+        if (lane != 0) return;
+        const uint64_t ta = reinterpret_cast<uint64_t>(&tmA);
+        const uint64_t tb = reinterpret_cast<uint64_t>(&tmB);
+        int issued = 0;
+        for (; issued < nsteps; ++issued) {
+            const int s = issued;
+            if (s >= 2 && !mbar_wait(empty(s), ((s >> 1) - 1) & 1, abort, kWaitLimit)) break;
+            const uint32_t bar = full(s), dst = sb + (s & 1) * MB_STAGE;
+            mbar_arrive_expect_tx(bar, MB_STAGE);
+            const int y = (int)((u * Sg + s) * 2 * FD);
+            tma_load_2d(dst, ta, 0, y, bar);
+            tma_load_2d(dst + MB_ABOX, ta, 64, y, bar);
+            tma_load_2d(dst + 2 * MB_ABOX, ta, 0, y + FD, bar);
+            tma_load_2d(dst + 3 * MB_ABOX, ta, 64, y + FD, bar);
+            tma_load_2d(dst + 4 * MB_ABOX, tb, c0, (int)((u * Sg + s) * FD), bar);
+        }
+        if (*abort) {
+            dev_fail(dev_status, KDA_ERR_TIMEOUT);
+            volatile int never = 0;  // let copies still in flight land before exiting
+            for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c)
+                mbar_wait(full(c), (c >> 1) & 1, &never, kWaitLimit);
+        }
+        return;
+    }
+
+    // ---- compute warps.  Running state: transposed copy for the products, this
+    // thread's outputs (rows i0, i1; columns c0+cc, +1) in fp32.
+    const int i0 = 16 * w + g8, i1 = i0 + 8, cc = 2 * t4;
+    const float *s0 = S0 ? S0 + u * (size_t)FD * dv : nullptr;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int idx = t + 256 * e, c = idx >> 7, j = idx & 127;
+        Xt[c * MB_XLD + j] = s0 ? s0[(size_t)j * dv + c0 + c] : 0.f;
+    }
+    float2 xo0 = make_float2(0.f, 0.f), xo1 = xo0;
+    if (s0) {  // S0 and S_final come from the caller, 4-byte aligned only: scalar accesses
+        xo0 = make_float2(s0[(size_t)i0 * dv + c0 + cc], s0[(size_t)i0 * dv + c0 + cc + 1]);
+        xo1 = make_float2(s0[(size_t)i1 * dv + c0 + cc], s0[(size_t)i1 * dv + c0 + cc + 1]);
+    }
+    named_bar_sync(1, NCW * 32);
+
+    // A fragment rows: box (w >> 2) of hi / lo, channel chunks q0 = 2 (w & 3) (+1)
+    const int abox = (w >> 2) * MB_ABOX, q0 = 2 * (w & 3);
+    const int mi = lane >> 3, lr = lane & 7;
+    bool aborted = false;
+    for (int s = 0; s < Sg; ++s) {
+        const size_t us = u * Sg + s;
+        if (seg_init) {
+            float *d = seg_init + us * (size_t)FD * dv + c0 + cc;
+            *(float2 *)(d + (size_t)i0 * dv) = xo0;
+            *(float2 *)(d + (size_t)i1 * dv) = xo1;
+        }
+        if (img) {
+            __nv_bfloat16 *im = img + us * (size_t)kStartImgElems;
+            im[start_img_index(c0 + cc, i0)] = __float2bfloat16_rn(xo0.x);
+            im[start_img_index(c0 + cc + 1, i0)] = __float2bfloat16_rn(xo0.y);
+            im[start_img_index(c0 + cc, i1)] = __float2bfloat16_rn(xo1.x);
+            im[start_img_index(c0 + cc + 1, i1)] = __float2bfloat16_rn(xo1.y);
+        }
+        if (s >= nsteps) break;
+        // a failed wait still runs the step (on whatever the stage holds) up to the
+        // barrier below, which makes the decision to stop the same for every warp
+        const bool ok = mbar_wait(full(s), (s >> 1) & 1, abort, kWaitLimit);
+        const uint32_t st_s = sb + (s & 1) * MB_STAGE;
+        const float *Bs = (const float *)(sm + (s & 1) * MB_STAGE + 4 * MB_ABOX);
+        const float *Xc = Xt + (s & 1) * FCB * MB_XLD;
+        float hh[4] = {}, hl[4] = {}, lh[4] = {};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int j = 16 * kk + lr + 8 * (mi >> 1), q = q0 + (mi & 1);
+            const uint32_t off = abox + j * 128 + ((q ^ (j & 7)) << 4);
+            uint32_t ahi[4], alo[4];
+            ldsm_x4_t(st_s + off, ahi);
+            ldsm_x4_t(st_s + 2 * MB_ABOX + off, alo);
+            const float2 x0 = *(const float2 *)(Xc + g8 * MB_XLD + 16 * kk + cc);
+            const float2 x1 = *(const float2 *)(Xc + g8 * MB_XLD + 16 * kk + 8 + cc);
+            const __nv_bfloat162 h0 = __floats2bfloat162_rn(x0.x, x0.y);
+            const __nv_bfloat162 h1 = __floats2bfloat162_rn(x1.x, x1.y);
+            const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+            const uint32_t bh0 = *(const uint32_t *)&h0, bh1 = *(const uint32_t *)&h1;
+            const uint32_t bl0 = pack_bf16x2(x0.x - f0.x, x0.y - f0.y);
+            const uint32_t bl1 = pack_bf16x2(x1.x - f1.x, x1.y - f1.y);
+            mma_bf16_16816(hh, ahi, bh0, bh1);
+            mma_bf16_16816(hl, ahi, bl0, bl1);
+            mma_bf16_16816(lh, alo, bh0, bh1);
+        }
+        const float2 b0 = *(const float2 *)(Bs + i0 * FCB + cc);
+        const float2 b1 = *(const float2 *)(Bs + i1 * FCB + cc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));  // this warp's reads of the stage are done
+        xo0 = make_float2(hh[0] + hl[0] + lh[0] + b0.x, hh[1] + hl[1] + lh[1] + b0.y);
+        xo1 = make_float2(hh[2] + hl[2] + lh[2] + b1.x, hh[3] + hl[3] + lh[3] + b1.y);
+        float *Xn = Xt + ((s + 1) & 1) * FCB * MB_XLD;
+        Xn[cc * MB_XLD + i0] = xo0.x;
+        Xn[(cc + 1) * MB_XLD + i0] = xo0.y;
+        Xn[cc * MB_XLD + i1] = xo1.x;
+        Xn[(cc + 1) * MB_XLD + i1] = xo1.y;
+        // next state complete; stop together if any wait (or the producer) gave up
+        aborted = named_bar_or(1, NCW * 32, !ok || *abort);
+        if (aborted) break;
+    }
+    if (aborted) {
+        if (t == 0) dev_fail(dev_status, KDA_ERR_TIMEOUT);
+        return;
+    }
+    if (S_final) {
+        float *d = S_final + u * (size_t)FD * dv + c0 + cc;
+        d[(size_t)i0 * dv] = xo0.x;
+        d[(size_t)i0 * dv + 1] = xo0.y;
+        d[(size_t)i1 * dv] = xo1.x;
+        d[(size_t)i1 * dv + 1] = xo1.y;
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, const float *B,
-                           const float *S0, float *seg_init, float *S_final,
-                           __nv_bfloat16 *start_img, int32_t *dev_status, cudaStream_t st) {
+cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A,
+                           const __nv_bfloat16 *a_img, const float *B, const float *S0,
+                           float *seg_init, float *S_final, __nv_bfloat16 *start_img,
+                           int32_t *dev_status, cudaStream_t st) {
     if (dk != 128 || dv != 128) start_img = nullptr;
     if (units == 0 || Sg == 0) return cudaSuccess;
+    if (a_img) {
+        // BF16 images of A_s: [units * Sg * 2 * 128 rows j, 128 channels i], boxes of
+        // 64 channels x 128 rows with 128-byte swizzle
+        auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
+        PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
+        if (dk != 128 || dv != 128 || !enc || !al16(a_img) || !al16(B)) return cudaErrorInvalidValue;
+        CUtensorMap tm, tmb;
+        const cuuint64_t dims[2] = {(cuuint64_t)FD, (cuuint64_t)units * Sg * 2 * FD};
+        const cuuint64_t strides[1] = {(cuuint64_t)FD * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)FD};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(a_img), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        // B viewed as [units * Sg * 128 rows, 128 fp32 columns], 8-column x 128-row boxes
+        const cuuint64_t bdims[2] = {(cuuint64_t)dv, (cuuint64_t)units * Sg * FD};
+        const cuuint64_t bstrides[1] = {(cuuint64_t)dv * 4};
+        const cuuint32_t bbox[2] = {(cuuint32_t)FCB, (cuuint32_t)FD};
+        if (enc(&tmb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(B), bdims, bstrides,
+                bbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        cudaError_t e = cudaFuncSetAttribute(compose_mma_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, MB_SMEM);
+        if (e != cudaSuccess) return e;
+        return launch_dependent(compose_mma_kernel, dim3(units, dv / FCB), dim3(MB_T), MB_SMEM, st,
+                                tm, tmb, Sg, S0, seg_init, S_final, start_img, dev_status);
+    }
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
     PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
     if (dk == FD && dv % FCB == 0 && al16(A) && al16(B) && al16(S0) && al16(seg_init) &&

@@ -59,7 +59,11 @@ struct PrefillArgs {
     const int32_t *cu;
     void *out;
     float *S_final;         // [N,H,dk,dv] or null; written by segment Sg-1
-    float *transfer;        // [N,H,Sg,dk,dk]                       (MODE_TRANSFER)
+    float *transfer;        // [N,H,Sg,dk,dk] or null               (MODE_TRANSFER)
+    // MODE_TRANSFER, dk = dv = 128: if set, the identity-start chain also writes
+    // its transfer matrix A as two BF16 images hi = bf16(A), lo = bf16(A - hi),
+    // each stored transposed ([j][i], i contiguous): [N,H,Sg][2][128][128].
+    __nv_bfloat16 *transfer_img;
     float *zero_state;      // [N,H,Sg,dk,dv]                       (MODE_TRANSFER)
     // MODE_TRANSFER with emit_out: the zero-start chain writes its outputs to
     // `out` [T,H,dv], the identity-start chain writes A_t^T q_t to `aux_out`
@@ -75,13 +79,36 @@ struct PrefillArgs {
     int act;                // kda_dtype_t
 };
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream drains, so it must call
+// sm100::griddep_wait() before its first global memory access.  Used for the
+// kernels of the split prefill, which run back to back.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t st);
 bool prefill_tc_supported(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st);
-cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A, const float *B,
-                           const float *S0, float *seg_init, float *S_final,
-                           __nv_bfloat16 *start_img, int32_t *dev_status, cudaStream_t st);
+// A (fp32) or, for BF16 at dk = dv = 128, a_img (the transfer pass's hi/lo
+// images) gives the transfer matrices; exactly one of them is non-null.
+cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A,
+                           const __nv_bfloat16 *a_img, const float *B, const float *S0,
+                           float *seg_init, float *S_final, __nv_bfloat16 *start_img,
+                           int32_t *dev_status, cudaStream_t st);
 bool decode_tma_supported(int dk, int dv);
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,
                               const void *v, const float *g, const float *beta, float *S,

@@ -542,7 +542,50 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
     if (!x.transfer) {
         if (x.s == p.Sg - 1 && p.S_final) dst = p.S_final + unit * (size_t)D * D;
     } else {
-        dst = (x.partA ? p.transfer : p.zero_state) + (unit * p.Sg + x.s) * (size_t)D * D;
+        float *base = x.partA ? p.transfer : p.zero_state;
+        if (base) dst = base + (unit * p.Sg + x.s) * (size_t)D * D;
+    }
+    if (x.partA && p.transfer_img) {
+        // A[i][j] as hi/lo BF16 images, transposed ([j][i]).  A lane holds channel
+        // pairs (2 t4, 2 t4 + 1) of each 8-channel tile; a 4 x 4 word transpose
+        // within the quad gives lane t4 all 8 channels of tile 4q + t4, so every
+        // store is 16 bytes and a quad writes 64 contiguous bytes of a row.
+        __nv_bfloat16 *hi = p.transfer_img + (unit * p.Sg + x.s) * (size_t)2 * D * D;
+        const bool l1 = (t4 >> 1) & 1, l0 = t4 & 1;
+        auto quad_transpose = [&](uint32_t (&v)[4]) {
+            const uint32_t r0 = __shfl_xor_sync(0xffffffffu, l1 ? v[0] : v[2], 2);
+            const uint32_t r1 = __shfl_xor_sync(0xffffffffu, l1 ? v[1] : v[3], 2);
+            const uint32_t a0 = l1 ? r0 : v[0], a1 = l1 ? r1 : v[1];
+            const uint32_t a2 = l1 ? v[2] : r0, a3 = l1 ? v[3] : r1;
+            const uint32_t w0 = __shfl_xor_sync(0xffffffffu, l0 ? a0 : a1, 1);
+            const uint32_t w1 = __shfl_xor_sync(0xffffffffu, l0 ? a2 : a3, 1);
+            v[0] = l0 ? w0 : a0;
+            v[1] = l0 ? a1 : w0;
+            v[2] = l0 ? w1 : a2;
+            v[3] = l0 ? a3 : w1;
+        };
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t vh[4], vl[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float v0 = S[m][4 * q + k][2 * hh], v1 = S[m][4 * q + k][2 * hh + 1];
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
+                        const float2 hf = __bfloat1622float2(h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+                        vh[k] = *(const uint32_t *)&h2;
+                        vl[k] = *(const uint32_t *)&l2;
+                    }
+                    quad_transpose(vh);
+                    quad_transpose(vl);
+                    const size_t o = (size_t)(j0 + 16 * m + g8 + 8 * hh) * D + 32 * q + 8 * t4;
+                    *(uint4 *)(hi + o) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+                    *(uint4 *)(hi + (size_t)D * D + o) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+                }
     }
     if (dst) {
 #pragma unroll
@@ -568,6 +611,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_g) {
     extern __shared__ uint8_t smem_raw[];
+    griddep_wait();  // inputs may come from the previous kernel in the stream
+    griddep_launch_dependents();
     // Align by pointer arithmetic on the __shared__ array (not through an integer),
     // so accesses keep the shared address space instead of becoming generic.
     uint8_t *smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
@@ -659,8 +704,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(units, a.mode == MODE_TRANSFER ? 2 : 1);
-    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(a, tq, tk, tv, tg);
-    return cudaGetLastError();
+    return launch_dependent(prefill_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, a, tq, tk, tv,
+                            tg);
 }
 
 }  // namespace kda
