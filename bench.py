@@ -213,6 +213,11 @@ def run_ours(args):
     A = torch.empty((N, H, Sg, dk, dk), dtype=torch.float32, device=dev)
     B = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
     starts = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
+    # L2 flush between timed steps: zero_() is a cudaMemsetAsync, which evicts the
+    # 129 MB L2 without a kernel of its own code; a fill kernel with a larger code
+    # footprint would also leave each step's kernels to start with cold
+    # instruction caches (about 7 us per step on this workload), i.e. it would
+    # time the flush's side effects rather than the prefill
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -256,7 +261,7 @@ def run_ours(args):
 
     mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush.zero_()
         step(mk(2))
     torch.cuda.synchronize()
     events = [mk(2) for _ in range(args.steps)]
@@ -267,7 +272,7 @@ def run_ours(args):
     time.sleep(0.3)
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
+        flush.zero_()
         step(events[i])
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -284,7 +289,7 @@ def run_ours(args):
     stage_ms = {"transfer_pass": [], "segment_scan": [], "combine": [], "output_pass": []}
     for _ in range(max(3, min(args.steps, 10))):
         ev = mk(4)
-        flush.fill_(1)
+        flush.zero_()
         staged(ev)
         torch.cuda.synchronize()
         stage_ms["transfer_pass"].append(ev[0].elapsed_time(ev[1]))
@@ -311,7 +316,7 @@ def run_ours(args):
               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
               "config": {"workload": PREFILL, "batch": N, "seq_len": T, "heads": H, "dk": dk,
                          "dv": dv, "chunk": 16, "segments": Sg, "state": "fp32",
-                         "l2": "512 MB buffer rewritten between timed steps (working set 50 MB)",
+                         "l2": "512 MB buffer zeroed (cudaMemsetAsync) between timed steps (working set 50 MB)",
                          "parallelism": "dp%d (one batch per GPU)" % world},
               "wall_s_timed_loop": round(wall, 4), "clocks": clk, "roofline": roofline,
               "gpu_launches": launches_per_step * args.steps}

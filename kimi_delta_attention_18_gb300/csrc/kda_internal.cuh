@@ -60,9 +60,10 @@ struct PrefillArgs {
     void *out;
     float *S_final;         // [N,H,dk,dv] or null; written by segment Sg-1
     float *transfer;        // [N,H,Sg,dk,dk] or null               (MODE_TRANSFER)
-    // MODE_TRANSFER, dk = dv = 128: if set, the identity-start chain also writes
-    // its transfer matrix A as two BF16 images hi = bf16(A), lo = bf16(A - hi),
-    // each stored transposed ([j][i], i contiguous): [N,H,Sg][2][128][128].
+    // MODE_TRANSFER, dk = dv = 128: if set, the identity-start chain writes its
+    // transfer matrix A as two BF16 images hi = bf16(A), lo = bf16(A - hi), each
+    // stored transposed ([j][i], i contiguous): [N,H,Sg][2][128][128], instead of
+    // the fp32 matrix (transfer is then ignored).
     __nv_bfloat16 *transfer_img;
     float *zero_state;      // [N,H,Sg,dk,dv]                       (MODE_TRANSFER)
     // MODE_TRANSFER with emit_out: the zero-start chain writes its outputs to

@@ -117,6 +117,15 @@ constexpr int SMEM_USED = MISC_OFF + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 128;     // slack for aligning the base
 
 static_assert(IN_SIZE % 128 == 0 && R_SIZE % 128 == 0 && X_SIZE % 128 == 0, "stage alignment");
+// Final-write staging per chain warp, in the input stages once they are idle: the
+// BF16 hi/lo images of its 32 columns ([32 j][FW_IROW bytes] each; 272-byte rows
+// keep stmatrix rows on distinct banks) or its fp32 state columns ([128 i][FW_JROW]
+// floats; 36-float rows make the transposing scalar stores conflict-free).
+constexpr int FW_IROW = 272;
+constexpr int FW_JROW = 36;
+constexpr int FW_SIZE = 128 * FW_JROW * 4;
+static_assert(2 * 32 * FW_IROW <= FW_SIZE && N_CHAIN * FW_SIZE <= NS * IN_SIZE,
+              "final-write staging fits in the input stages");
 static_assert(RLB % 16 == 0 && (RLB / 16) % 2 == 1, "record rows: 16-byte aligned, odd stride");
 static_assert(VROWB % 16 == 0 && (VROWB / 16) % 2 == 1, "V rows: 16-byte aligned, odd stride");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -545,57 +554,74 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         float *base = x.partA ? p.transfer : p.zero_state;
         if (base) dst = base + (unit * p.Sg + x.s) * (size_t)D * D;
     }
+    // Final writes go through shared memory so that every global store is a fully
+    // used 16-byte piece of a contiguous run.  Every record has been consumed, so
+    // the prep warps are done with the input stages; each chain warp stages its
+    // 32 columns j in a private FW_SIZE slice of them.
+    uint8_t *fw = x.smem + IN_OFF + cw * FW_SIZE;
+    const uint32_t fw_s = x.sbase + IN_OFF + cw * FW_SIZE;
     if (x.partA && p.transfer_img) {
-        // A[i][j] as hi/lo BF16 images, transposed ([j][i]).  A lane holds channel
-        // pairs (2 t4, 2 t4 + 1) of each 8-channel tile; a 4 x 4 word transpose
-        // within the quad gives lane t4 all 8 channels of tile 4q + t4, so every
-        // store is 16 bytes and a quad writes 64 contiguous bytes of a row.
-        __nv_bfloat16 *hi = p.transfer_img + (unit * p.Sg + x.s) * (size_t)2 * D * D;
-        const bool l1 = (t4 >> 1) & 1, l0 = t4 & 1;
-        auto quad_transpose = [&](uint32_t (&v)[4]) {
-            const uint32_t r0 = __shfl_xor_sync(0xffffffffu, l1 ? v[0] : v[2], 2);
-            const uint32_t r1 = __shfl_xor_sync(0xffffffffu, l1 ? v[1] : v[3], 2);
-            const uint32_t a0 = l1 ? r0 : v[0], a1 = l1 ? r1 : v[1];
-            const uint32_t a2 = l1 ? v[2] : r0, a3 = l1 ? v[3] : r1;
-            const uint32_t w0 = __shfl_xor_sync(0xffffffffu, l0 ? a0 : a1, 1);
-            const uint32_t w1 = __shfl_xor_sync(0xffffffffu, l0 ? a2 : a3, 1);
-            v[0] = l0 ? w0 : a0;
-            v[1] = l0 ? a1 : w0;
-            v[2] = l0 ? w1 : a2;
-            v[3] = l0 ? a3 : w1;
-        };
+        // A[i][j] as hi/lo BF16 images, transposed ([j][i], i contiguous): the
+        // accumulator fragments are already j-row / i-column, so stmatrix writes
+        // 16 x 16 blocks of each image into [32 j][FW_IROW bytes] rows.
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int pb = 0; pb < 8; ++pb) {  // one 16 x 16 block of both images
+                uint32_t rh[4], rl[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t vh[4], vl[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float v0 = S[m][4 * q + k][2 * hh], v1 = S[m][4 * q + k][2 * hh + 1];
-                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
-                        const float2 hf = __bfloat1622float2(h2);
-                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
-                        vh[k] = *(const uint32_t *)&h2;
-                        vl[k] = *(const uint32_t *)&l2;
-                    }
-                    quad_transpose(vh);
-                    quad_transpose(vl);
-                    const size_t o = (size_t)(j0 + 16 * m + g8 + 8 * hh) * D + 32 * q + 8 * t4;
-                    *(uint4 *)(hi + o) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
-                    *(uint4 *)(hi + (size_t)D * D + o) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+                for (int k = 0; k < 4; ++k) {  // matrix k: rows +8 (k & 1), cols +8 (k >> 1)
+                    const float v0 = S[m][2 * pb + (k >> 1)][2 * (k & 1)];
+                    const float v1 = S[m][2 * pb + (k >> 1)][2 * (k & 1) + 1];
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
+                    const float2 hf = __bfloat1622float2(h2);
+                    rh[k] = *(const uint32_t *)&h2;
+                    rl[k] = pack_bf16x2(v0 - hf.x, v1 - hf.y);
                 }
-    }
-    if (dst) {
+                const int mk = lane >> 3, row = 16 * m + (lane & 7) + 8 * (mk & 1);
+                const uint32_t o = row * FW_IROW + (16 * pb + 8 * (mk >> 1)) * 2;
+                stsm_x4(fw_s + o, rh[0], rh[1], rh[2], rh[3]);
+                stsm_x4(fw_s + 32 * FW_IROW + o, rl[0], rl[1], rl[2], rl[3]);
+            }
+        __syncwarp();
+        // rows j0 .. j0+31 of each image are 8 KB contiguous in global memory
+        __nv_bfloat16 *hi = p.transfer_img + (unit * p.Sg + x.s) * (size_t)2 * D * D;
+#pragma unroll
+        for (int img = 0; img < 2; ++img)
+#pragma unroll 4
+            for (int it = 0; it < 16; ++it) {
+                const int idx = 32 * it + lane, row = idx >> 4, c16 = idx & 15;
+                *(uint4 *)(hi + (size_t)img * D * D + (size_t)(j0 + row) * D + 8 * c16) =
+                    *(const uint4 *)(fw + img * 32 * FW_IROW + row * FW_IROW + 16 * c16);
+            }
+    } else if (dst) {
+        // S[i][j] (j contiguous) is the transpose of the accumulator layout: stage
+        // this warp's columns as [128 i][FW_JROW floats] (conflict-free scalar
+        // stores), then write 128-byte row segments.
+        float *f = (float *)fw;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int n = 0; n < 16; ++n)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    dst[(size_t)(8 * n + 2 * t4 + (e & 1)) * D + j0 + 16 * m + g8 + 8 * (e >> 1)] =
-                        S[m][n][e];
+                    f[(8 * n + 2 * t4 + (e & 1)) * FW_JROW + 16 * m + g8 + 8 * (e >> 1)] = S[m][n][e];
+        __syncwarp();
+        const bool v16 = ((uintptr_t)dst & 15u) == 0;  // S_final is only 4-byte aligned
+#pragma unroll 4
+        for (int it = 0; it < 32; ++it) {
+            const int idx = 32 * it + lane, i = idx >> 3, c = idx & 7;
+            const float4 v = *(const float4 *)(f + i * FW_JROW + 4 * c);
+            float *d = dst + (size_t)i * D + j0 + 4 * c;
+            if (v16) {
+                *(float4 *)d = v;
+            } else {
+                d[0] = v.x;
+                d[1] = v.y;
+                d[2] = v.z;
+                d[3] = v.w;
+            }
+        }
     }
 }
 
