@@ -213,11 +213,8 @@ def run_ours(args):
     A = torch.empty((N, H, Sg, dk, dk), dtype=torch.float32, device=dev)
     B = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
     starts = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
-    # L2 flush between timed steps: zero_() is a cudaMemsetAsync, which evicts the
-    # 129 MB L2 without a kernel of its own code; a fill kernel with a larger code
-    # footprint would also leave each step's kernels to start with cold
-    # instruction caches (about 7 us per step on this workload), i.e. it would
-    # time the flush's side effects rather than the prefill
+    # L2 flush between timed steps: a 512 MB fill (torch's fill kernel) evicts the
+    # 129 MB L2 before every step
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -316,7 +313,7 @@ def run_ours(args):
               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
               "config": {"workload": PREFILL, "batch": N, "seq_len": T, "heads": H, "dk": dk,
                          "dv": dv, "chunk": 16, "segments": Sg, "state": "fp32",
-                         "l2": "512 MB buffer zeroed (cudaMemsetAsync) between timed steps (working set 50 MB)",
+                         "l2": "512 MB buffer zero-filled between timed steps (working set 50 MB)",
                          "parallelism": "dp%d (one batch per GPU)" % world},
               "wall_s_timed_loop": round(wall, 4), "clocks": clk, "roofline": roofline,
               "gpu_launches": launches_per_step * args.steps}
