@@ -235,15 +235,17 @@ __global__ void __launch_bounds__(FT) compose_tma_kernel(const __grid_constant__
 // ldmatrix rows hit different banks) and this CTA's 8 columns of B_s (one
 // 8 x 128 fp32 box) into a stage; compute warps free a stage through an
 // mbarrier, so neither the copy issue nor a global load sits on the step's
-// critical path.  The running state is kept transposed in fp32 ([column][j],
-// rows padded to 136 floats) and double-buffered.
+// critical path.  Each warp keeps its rows of the running state in fp32
+// registers and publishes them, already split, as BF16 hi/lo images of X^T
+// ([column j][key channel i], 272-byte rows so ldmatrix rows hit different
+// banks), double-buffered: a k-step then needs one ldmatrix for both X splits.
 constexpr int MB_T = 288;               // 8 compute warps + 1 producer warp
 constexpr int MB_ABOX = 128 * 128;      // one 64-channel x 128-row BF16 box, 16 KB
 constexpr int MB_BBOX = FD * FCB * 4;   // 8 columns x 128 rows of B_s, fp32, 4 KB
 constexpr int MB_STAGE = 4 * MB_ABOX + MB_BBOX;  // hi (2 boxes), lo (2 boxes), B
-constexpr int MB_XLD = 136;             // padded row of the transposed state
+constexpr int MB_XROW = 272;            // bytes per row of an X^T image (128 BF16 + pad)
 constexpr int MB_X = 2 * MB_STAGE;
-constexpr int MB_XSZ = FCB * MB_XLD * 4;
+constexpr int MB_XSZ = 2 * FCB * MB_XROW;  // hi and lo images of one state
 constexpr int MB_BAR = MB_X + 2 * MB_XSZ;
 constexpr int MB_SMEM = MB_BAR + 64 + 1024;
 static_assert(MB_STAGE % 1024 == 0, "stages keep the 128-byte swizzle's 1024-byte alignment");
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(MB_T) compose_mma_kernel(const __grid_constant
     griddep_wait();  // A_s, B_s come from the transfer pass just before
     griddep_launch_dependents();
     uint8_t *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
-    float *Xt = (float *)(sm + MB_X);
+    uint8_t *Xb = sm + MB_X;
     uint64_t *bars = (uint64_t *)(sm + MB_BAR);  // full[2], empty[2]
     volatile int *abort = (volatile int *)(bars + 4);
     const uint32_t sb = smem_addr(sm);
@@ -310,10 +312,19 @@ __global__ void __launch_bounds__(MB_T) compose_mma_kernel(const __grid_constant
     // thread's outputs (rows i0, i1; columns c0+cc, +1) in fp32.
     const int i0 = 16 * w + g8, i1 = i0 + 8, cc = 2 * t4;
     const float *s0 = S0 ? S0 + u * (size_t)FD * dv : nullptr;
+    // X^T image element (column c, channel i) of buffer b, split img (0 hi, 1 lo)
+    auto xb_at = [&](int b, int img, int c, int i) {
+        return (__nv_bfloat16 *)(Xb + b * MB_XSZ + img * FCB * MB_XROW + c * MB_XROW) + i;
+    };
+    auto put_x = [&](int b, int c, int i, float v) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        *xb_at(b, 0, c, i) = h;
+        *xb_at(b, 1, c, i) = __float2bfloat16_rn(v - __bfloat162float(h));
+    };
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const int idx = t + 256 * e, c = idx >> 7, j = idx & 127;
-        Xt[c * MB_XLD + j] = s0 ? s0[(size_t)j * dv + c0 + c] : 0.f;
+        const int idx = t + 256 * e, c = idx >> 7, i = idx & 127;
+        put_x(0, c, i, s0 ? s0[(size_t)i * dv + c0 + c] : 0.f);
     }
     float2 xo0 = make_float2(0.f, 0.f), xo1 = xo0;
     if (s0) {  // S0 and S_final come from the caller, 4-byte aligned only: scalar accesses
@@ -326,7 +337,8 @@ __global__ void __launch_bounds__(MB_T) compose_mma_kernel(const __grid_constant
     const int abox = (w >> 2) * MB_ABOX, q0 = 2 * (w & 3);
     const int mi = lane >> 3, lr = lane & 7;
     bool aborted = false;
-    for (int s = 0; s < Sg; ++s) {
+    // start state of segment s (this thread's four values)
+    auto put_start = [&](int s) {
         const size_t us = u * Sg + s;
         if (seg_init) {
             float *d = seg_init + us * (size_t)FD * dv + c0 + cc;
@@ -340,32 +352,38 @@ __global__ void __launch_bounds__(MB_T) compose_mma_kernel(const __grid_constant
             im[start_img_index(c0 + cc, i1)] = __float2bfloat16_rn(xo1.x);
             im[start_img_index(c0 + cc + 1, i1)] = __float2bfloat16_rn(xo1.y);
         }
+    };
+    for (int s = 0; s < Sg; ++s) {
+        put_start(s);
         if (s >= nsteps) break;
         // a failed wait still runs the step (on whatever the stage holds) up to the
         // barrier below, which makes the decision to stop the same for every warp
         const bool ok = mbar_wait(full(s), (s >> 1) & 1, abort, kWaitLimit);
         const uint32_t st_s = sb + (s & 1) * MB_STAGE;
         const float *Bs = (const float *)(sm + (s & 1) * MB_STAGE + 4 * MB_ABOX);
-        const float *Xc = Xt + (s & 1) * FCB * MB_XLD;
-        float hh[4] = {}, hl[4] = {}, lh[4] = {};
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        // B fragments of X (hi: matrices 0, 1; lo: 2, 3) for k-step kk
+        const uint32_t xb_s = sb + MB_X + (s & 1) * MB_XSZ + (mi >> 1) * FCB * MB_XROW +
+                              lr * MB_XROW + 16 * (mi & 1);
+        auto load_a = [&](int kk, uint32_t (&ahi)[4], uint32_t (&alo)[4]) {
             const int j = 16 * kk + lr + 8 * (mi >> 1), q = q0 + (mi & 1);
             const uint32_t off = abox + j * 128 + ((q ^ (j & 7)) << 4);
-            uint32_t ahi[4], alo[4];
             ldsm_x4_t(st_s + off, ahi);
             ldsm_x4_t(st_s + 2 * MB_ABOX + off, alo);
-            const float2 x0 = *(const float2 *)(Xc + g8 * MB_XLD + 16 * kk + cc);
-            const float2 x1 = *(const float2 *)(Xc + g8 * MB_XLD + 16 * kk + 8 + cc);
-            const __nv_bfloat162 h0 = __floats2bfloat162_rn(x0.x, x0.y);
-            const __nv_bfloat162 h1 = __floats2bfloat162_rn(x1.x, x1.y);
-            const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-            const uint32_t bh0 = *(const uint32_t *)&h0, bh1 = *(const uint32_t *)&h1;
-            const uint32_t bl0 = pack_bf16x2(x0.x - f0.x, x0.y - f0.y);
-            const uint32_t bl1 = pack_bf16x2(x1.x - f1.x, x1.y - f1.y);
-            mma_bf16_16816(hh, ahi, bh0, bh1);
-            mma_bf16_16816(hl, ahi, bl0, bl1);
-            mma_bf16_16816(lh, alo, bh0, bh1);
+        };
+        float hh[4] = {}, hl[4] = {}, lh[4] = {};
+        uint32_t ahi[2][4], alo[2][4], bx[2][4];
+        load_a(0, ahi[0], alo[0]);
+        ldsm_x4(xb_s, bx[0]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            if (kk + 1 < 8) {
+                load_a(kk + 1, ahi[(kk + 1) & 1], alo[(kk + 1) & 1]);
+                ldsm_x4(xb_s + 32 * (kk + 1), bx[(kk + 1) & 1]);
+            }
+            const uint32_t(&b)[4] = bx[kk & 1];
+            mma_bf16_16816(hh, ahi[kk & 1], b[0], b[1]);
+            mma_bf16_16816(hl, ahi[kk & 1], b[2], b[3]);
+            mma_bf16_16816(lh, alo[kk & 1], b[0], b[1]);
         }
         const float2 b0 = *(const float2 *)(Bs + i0 * FCB + cc);
         const float2 b1 = *(const float2 *)(Bs + i1 * FCB + cc);
@@ -373,11 +391,11 @@ __global__ void __launch_bounds__(MB_T) compose_mma_kernel(const __grid_constant
         if (lane == 0) mbar_arrive(empty(s));  // this warp's reads of the stage are done
         xo0 = make_float2(hh[0] + hl[0] + lh[0] + b0.x, hh[1] + hl[1] + lh[1] + b0.y);
         xo1 = make_float2(hh[2] + hl[2] + lh[2] + b1.x, hh[3] + hl[3] + lh[3] + b1.y);
-        float *Xn = Xt + ((s + 1) & 1) * FCB * MB_XLD;
-        Xn[cc * MB_XLD + i0] = xo0.x;
-        Xn[(cc + 1) * MB_XLD + i0] = xo0.y;
-        Xn[cc * MB_XLD + i1] = xo1.x;
-        Xn[(cc + 1) * MB_XLD + i1] = xo1.y;
+        const int nb = (s + 1) & 1;
+        put_x(nb, cc, i0, xo0.x);
+        put_x(nb, cc + 1, i0, xo0.y);
+        put_x(nb, cc, i1, xo1.x);
+        put_x(nb, cc + 1, i1, xo1.y);
         // next state complete; stop together if any wait (or the producer) gave up
         aborted = named_bar_or(1, NCW * 32, !ok || *abort);
         if (aborted) break;
