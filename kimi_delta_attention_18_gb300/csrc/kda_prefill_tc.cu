@@ -223,7 +223,7 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
 // One warp prepares one whole block: elementwise factors, L and Mq and the
 // solve for T, written with V into a record slot.  Prep warp p takes
 // blocks p, p + 4, p + 8, ...; it frees the input stage as soon as it has read it.
-template <bool WANT_Q, bool WANT_V>
+template <bool WANT_Q>
 __device__ __forceinline__ void prep_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int pw = (threadIdx.x >> 5) - W_PREP0;
@@ -242,12 +242,12 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
     auto issue = [&](int c) {
         if (lane == 0) {
             const uint32_t bytes =
-                (WANT_Q ? 4096u : 0u) + 4096u + (WANT_V ? 4096u : 0u) + 8192u;
+                (WANT_Q ? 4096u : 0u) + 4096u + (x.want_v ? 4096u : 0u) + 8192u;
             mbar_arrive_expect_tx(full, bytes);
             const int xc = x.h * D, t0 = x.t_begin + C * c;
             if (WANT_Q) tma_load_2d(in_s + IN_Q, x.tm_q, xc, t0, full);
             tma_load_2d(in_s + IN_K, x.tm_k, xc, t0, full);
-            if (WANT_V) tma_load_2d(in_s + IN_V, x.tm_v, xc, t0, full);
+            if (x.want_v) tma_load_2d(in_s + IN_V, x.tm_v, xc, t0, full);
             tma_load_2d(in_s + IN_G, x.tm_g, xc, t0, full);
         }
     };
@@ -285,7 +285,7 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
         // V into the record (padded rows).  Rows past the block's end become zero:
         // they are weighted by zero in the chain's products, and the next
         // sequence's values (or anything non-finite in them) must not leak in.
-        if (WANT_V) {
+        if (x.want_v) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int idx = lane + 32 * i, r = idx >> 4, q16 = idx & 15;
@@ -381,7 +381,7 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
 // share every B fragment the warp loads from the record.
 constexpr int MT = 2;  // m-tiles per chain warp
 
-template <bool WANT_Q, bool WANT_V>
+template <bool WANT_Q>
 __device__ __forceinline__ void chain_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int cw = (threadIdx.x >> 5) - W_CHAIN0;
@@ -423,7 +423,7 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         // an A fragment, whose element positions are those of the 16 x 16
         // accumulator pair, so it seeds E directly.
         float E[MT][2][4] = {};
-        if (WANT_V) {
+        if (x.want_v) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 uint32_t va[4];
@@ -625,10 +625,14 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
     }
 }
 
-template <bool WANT_Q, bool WANT_V>
+// With or without V is a runtime switch (uniform per CTA), not a template
+// parameter: the identity-start and zero-start CTAs of the transfer pass then
+// run the same instructions, so the code that the first of them fetches into the
+// instruction caches serves the other, and the kernel's code footprint halves.
+template <bool WANT_Q>
 __device__ __forceinline__ void run_role(const Ctx &x, int warp) {
-    if (warp < W_CHAIN0) prep_role<WANT_Q, WANT_V>(x);
-    else chain_role<WANT_Q, WANT_V>(x);
+    if (warp < W_CHAIN0) prep_role<WANT_Q>(x);
+    else chain_role<WANT_Q>(x);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -675,13 +679,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncthreads();
 
-    if (x.want_q) {
-        if (x.want_v) run_role<true, true>(x, warp);
-        else run_role<true, false>(x, warp);
-    } else {
-        if (x.want_v) run_role<false, true>(x, warp);
-        else run_role<false, false>(x, warp);
-    }
+    if (x.want_q) run_role<true>(x, warp);
+    else run_role<false>(x, warp);
 
     __syncthreads();
     if (threadIdx.x == 0 && *x.abort) dev_fail(p.dev_status, KDA_ERR_TIMEOUT);
