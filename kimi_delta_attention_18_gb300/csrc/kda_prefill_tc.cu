@@ -198,22 +198,37 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
             *(uint4 *)dst = make_uint4(w[0], w[1], w[2], w[3]);
             *(uint4 *)(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
         };
+        // products over adjacent token pairs as packed f32x2 multiplies
+        auto vmul = [&](float (&o)[C], const float (&x)[C], const float (&y)[C]) {
+#pragma unroll
+            for (int e = 0; e < C / 2; ++e) {
+                o[2 * e] = x[2 * e];
+                o[2 * e + 1] = x[2 * e + 1];
+                mul2_inplace(o[2 * e], o[2 * e + 1], make_float2(y[2 * e], y[2 * e + 1]));
+            }
+        };
         float tmp[C];
-#pragma unroll
-        for (int r = 0; r < C; ++r) tmp[r] = kv[r] * fwd[r];
+        vmul(tmp, kv, fwd);
         put_row(rec + ch * RLB + RC_KH * 2, tmp);
+        float inv[C];  // e^{-Gamma_r} = e^{Gamma_C - Gamma_r} / e^{Gamma_C}
 #pragma unroll
-        for (int r = 0; r < C; ++r) tmp[r] = kv[r] * (einv * rev[r]);
+        for (int e = 0; e < C / 2; ++e) {
+            inv[2 * e] = rev[2 * e];
+            inv[2 * e + 1] = rev[2 * e + 1];
+            mul2_inplace(inv[2 * e], inv[2 * e + 1], make_float2(einv, einv));
+        }
+        vmul(tmp, kv, inv);
         put_row(scr + X_KT + ch * TROW, tmp);
-#pragma unroll
-        for (int r = 0; r < C; ++r) tmp[r] = kv[r] * rev[r];
+        vmul(tmp, kv, rev);
         put_row(rec + ch * RLB + RC_K * 2, tmp);
         if (WANT_Q) {
+            float qv[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float qv = __bfloat162float(qin[r * D + ch]);
-                tmp[r] = (MASK && r >= nt ? 0.f : qv) * fwd[r];
+                const float q1 = __bfloat162float(qin[r * D + ch]);
+                qv[r] = MASK && r >= nt ? 0.f : q1;
             }
+            vmul(tmp, qv, fwd);
             put_row(rec + ch * RLB + RC_Q * 2, tmp);
         }
         ((float *)(rec + R_DECAY))[ch] = eGC;
@@ -491,27 +506,31 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
             }
         }
 
-        // S^T <- S^T Diag(e^{Gamma_C}) + U^T Kb
+        // S^T <- S^T Diag(e^{Gamma_C}) + U^T Kb.  Kb fragments and the decay pairs are
+        // loaded one tile pair ahead; the decay runs as packed f32x2 multiplies
+        // (the two channels a lane holds per row are adjacent).
         {
             uint32_t kb[2][4];
-            auto load_kb = [&](int np, uint32_t (&f)[4]) {
+            float2 dd[2][2];
+            auto load_kb = [&](int np, uint32_t (&f)[4], float2 (&d)[2]) {
                 ldsm_x4(rec_s + (16 * np + (lane & 7) + 8 * (lane >> 4)) * RLB + RC_K * 2 +
                             16 * ((lane >> 3) & 1),
                         f);
+                d[0] = *(const float2 *)(decay + 16 * np + 2 * t4);
+                d[1] = *(const float2 *)(decay + 16 * np + 8 + 2 * t4);
             };
-            load_kb(0, kb[0]);
+            load_kb(0, kb[0], dd[0]);
 #pragma unroll
             for (int np = 0; np < 8; ++np) {
-                if (np + 1 < 8) load_kb(np + 1, kb[(np + 1) & 1]);
-                const float2 d0 = *(const float2 *)(decay + 16 * np + 2 * t4);
-                const float2 d1 = *(const float2 *)(decay + 16 * np + 8 + 2 * t4);
+                if (np + 1 < 8) load_kb(np + 1, kb[(np + 1) & 1], dd[(np + 1) & 1]);
+                const float2 d0 = dd[np & 1][0], d1 = dd[np & 1][1];
                 const uint32_t(&f)[4] = kb[np & 1];
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    S[m][2 * np][0] *= d0.x; S[m][2 * np][1] *= d0.y;
-                    S[m][2 * np][2] *= d0.x; S[m][2 * np][3] *= d0.y;
-                    S[m][2 * np + 1][0] *= d1.x; S[m][2 * np + 1][1] *= d1.y;
-                    S[m][2 * np + 1][2] *= d1.x; S[m][2 * np + 1][3] *= d1.y;
+                    mul2_inplace(S[m][2 * np][0], S[m][2 * np][1], d0);
+                    mul2_inplace(S[m][2 * np][2], S[m][2 * np][3], d0);
+                    mul2_inplace(S[m][2 * np + 1][0], S[m][2 * np + 1][1], d1);
+                    mul2_inplace(S[m][2 * np + 1][2], S[m][2 * np + 1][3], d1);
                     mma_bf16_16816(S[m][2 * np], ua[m], f[0], f[1]);
                     mma_bf16_16816(S[m][2 * np + 1], ua[m], f[2], f[3]);
                 }

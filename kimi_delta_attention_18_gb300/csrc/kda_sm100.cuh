@@ -262,6 +262,14 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r
                  "r"(r0), "r"(r1), "r"(r2), "r"(r3)
                  : "memory");
 }
+// (x, y) *= (d.x, d.y) as one packed fp32x2 multiply (round to nearest, the same
+// result as two scalar multiplies).
+__device__ __forceinline__ void mul2_inplace(float &x, float &y, float2 d) {
+    asm("{\n\t.reg .b64 a, b;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\t"
+        "mul.rn.f32x2 a, a, b;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "f"(d.x), "f"(d.y));
+}
 // C(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                                uint32_t b1) {
