@@ -98,8 +98,9 @@ constexpr int R_SIZE = R_V + C * VROWB;
 // prep scratch (private to one prep warp)
 constexpr int TROW = 48;                        // one channel's 16 positions, BF16, padded
 constexpr int X_KT = 0;                         // Kt^T [128 ch][24]
-constexpr int X_L = X_KT + D * TROW;            // Diag(beta) L fp32 [16][17]
-constexpr int X_SIZE = (X_L + C * 17 * 4 + 127) & ~127;
+constexpr int LS = 20;                          // row stride of L: 16-byte aligned rows
+constexpr int X_L = X_KT + D * TROW;            // Diag(beta) L fp32 [16][LS]
+constexpr int X_SIZE = (X_L + C * LS * 4 + 127) & ~127;
 constexpr int IN_OFF = 0;
 constexpr int REC_OFF = IN_OFF + NS * IN_SIZE;
 constexpr int X_OFF = REC_OFF + NR * R_SIZE;
@@ -350,8 +351,9 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
                     const int r = g8 + 8 * hh;
                     const int i0 = nb * 8 + 2 * t4;
                     const float br = hh ? beta_hi : beta_lo;
-                    Lf[r * 17 + i0] = i0 < r ? br * accL[nb][2 * hh] : 0.f;
-                    Lf[r * 17 + i0 + 1] = i0 + 1 < r ? br * accL[nb][2 * hh + 1] : 0.f;
+                    *(float2 *)(Lf + r * LS + i0) =
+                        make_float2(i0 < r ? br * accL[nb][2 * hh] : 0.f,
+                                    i0 + 1 < r ? br * accL[nb][2 * hh + 1] : 0.f);
                     if (WANT_Q)
                         *(uint32_t *)(rec + R_MQ + (r * TL + i0) * 2) =
                             pack_bf16x2(i0 <= r ? accM[nb][2 * hh] : 0.f,
@@ -369,10 +371,19 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
 #pragma unroll
             for (int r = 1; r < C; ++r) {
                 float s0 = 0.f, s1 = 0.f;
+                // row r of L in 16-byte pieces (one broadcast load per four entries)
 #pragma unroll
-                for (int m = 0; m < r; ++m) {
-                    if (m & 1) s1 += Lf[r * 17 + m] * xv[m];
-                    else s0 += Lf[r * 17 + m] * xv[m];
+                for (int c4 = 0; 4 * c4 < r; ++c4) {
+                    const float4 lv = *(const float4 *)(Lf + r * LS + 4 * c4);
+                    const float l4[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int m = 4 * c4 + q;
+                        if (m < r) {
+                            if (m & 1) s1 += l4[q] * xv[m];
+                            else s0 += l4[q] * xv[m];
+                        }
+                    }
                 }
                 xv[r] = r > j ? -(s0 + s1) : xv[r];
             }
