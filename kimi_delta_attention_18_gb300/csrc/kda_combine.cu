@@ -143,26 +143,30 @@ __global__ void __launch_bounds__(BF_WARPS * 32) combine_bf16_kernel(
 
 // ---- tcgen05 path: D[t][j] = sum_i aux[t][i] start_s[i][j] over a 128-token tile
 constexpr int TC_TILE = 128;
-constexpr int TC_A = 0;         // aux tile: 16 TMA boxes of 8 channels x 128 rows (2 KB each)
-constexpr int TC_B = 32768;     // start image, the same core-matrix layout (rows j)
-constexpr int TC_BAR = 65536;   // [0] operands landed, [8] products done, [16] abort, [24] TMEM base
-constexpr int TC_SMEM = TC_BAR + 32 + 128;  // + slack for aligning the base
+constexpr int TC_A = 0;         // aux tile: 2 TMA boxes of 64 channels x 128 rows, 128-byte swizzle
+constexpr int TC_B = 32768;     // start image: K-major core matrices without swizzle (rows j)
+constexpr int TC_O = 65536;     // out tile: 2 TMA boxes of 64 columns x 128 rows, 128-byte swizzle
+constexpr int TC_BAR = 98304;   // [0] operands landed, [8] products done, [16] abort, [24] TMEM base
+constexpr int TC_SMEM = TC_BAR + 32 + 1024;  // + slack for the 1024-byte alignment of the base
 constexpr uint32_t TC_COLS = 128;
 constexpr long long kTcWaitLimit = 4000000000ll;  // ~2 s of SM clocks
 
-// Both operands are K-major without swizzle: core matrices (8 rows x 16 bytes)
-// adjacent along K 2048 bytes apart (one TMA box each for A), 8-row groups 128
-// bytes apart.  The accumulator row m is TMEM lane m, so warp w reads the
-// products of tokens 32w..32w+31 and corrects their out rows in fp32.  All waits
-// are bounded; a CTA that gives up records KDA_ERR_TIMEOUT, lets its copies land
-// and frees its TMEM.
+// A (the tile's A_t^T q_t rows) and the tile's out rows arrive as two 64-column
+// TMA boxes each with 128-byte swizzle, so every copy moves whole 128-byte row
+// pieces; B, the start image, is K-major without swizzle (core matrices 8 rows x
+// 16 bytes, adjacent along K 2048 bytes apart, 8-row groups 128 bytes apart).
+// The accumulator row m is TMEM lane m, so warp w reads the products of tokens
+// 32w..32w+31 and corrects their out rows in fp32 (each thread reads its row's
+// swizzled chunks: conflict-free).  All waits are bounded; a CTA that gives up
+// records KDA_ERR_TIMEOUT, lets its copies land and frees its TMEM.
 __global__ void __launch_bounds__(128) combine_tc_kernel(const __grid_constant__ PrefillArgs p,
                                                          const __grid_constant__ CUtensorMap tm_aux,
+                                                         const __grid_constant__ CUtensorMap tm_out,
                                                          const __nv_bfloat16 *img, int tile_base) {
     extern __shared__ uint8_t smem_raw[];
     griddep_wait();  // out, A_t^T q_t and the start images come from earlier kernels
     griddep_launch_dependents();
-    uint8_t *sm = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+    uint8_t *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(sm);
     const uint32_t full = sb + TC_BAR, mmad = sb + TC_BAR + 8;
     volatile int *abort = (volatile int *)(sm + TC_BAR + 16);
@@ -177,15 +181,9 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const __grid_constant__
     const int nt = min(TC_TILE, b - t0);
     const size_t unit = (size_t)(u / p.Sg);  // (n, h)
 
-    // this thread's out row, loaded now so the loads overlap the copies and products
-    const int row = 32 * warp + lane;
+    const int row = 32 * warp + lane;  // this thread's token in the tile
     const bool live = row < nt;
     uint4 *orow = (uint4 *)((__nv_bfloat16 *)p.out + ((size_t)(t0 + row) * p.H + h) * 128);
-    uint4 ov[16];
-    if (live) {
-#pragma unroll
-        for (int q = 0; q < 16; ++q) ov[q] = orow[q];
-    }
 
     if (tid == 0) {
         mbar_init(full, 1);
@@ -204,10 +202,16 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const __grid_constant__
 
     bool landed = false;
     if (tid == 0) {
-        mbar_arrive_expect_tx(full, 2 * 32768);
-        const uint64_t tmap = reinterpret_cast<uint64_t>(&tm_aux);
+        mbar_arrive_expect_tx(full, 3 * 32768);
+        const uint64_t ta = reinterpret_cast<uint64_t>(&tm_aux);
+        const uint64_t to = reinterpret_cast<uint64_t>(&tm_out);
+        // rows past the segment's end come along (the next segment's, or zero fill
+        // past the array); they are never used
 #pragma unroll
-        for (int c = 0; c < 16; ++c) tma_load_2d(sb + TC_A + c * 2048, tmap, h * 128 + 8 * c, t0, full);
+        for (int bx = 0; bx < 2; ++bx) {
+            tma_load_2d(sb + TC_A + bx * 16384, ta, h * 128 + 64 * bx, t0, full);
+            tma_load_2d(sb + TC_O + bx * 16384, to, h * 128 + 64 * bx, t0, full);
+        }
         bulk_g2s(sb + TC_B, img + (unit * p.Sg + s) * (size_t)kStartImgElems, 32768, full);
         landed = mbar_wait(full, 0, abort, kTcWaitLimit);
         if (landed) {
@@ -215,14 +219,21 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const __grid_constant__
             const uint32_t idesc = umma_idesc_bf16(128, 128);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                umma_bf16(tmem, umma_desc(sb + TC_A + kk * 4096, 2048, 128),
+                umma_bf16(tmem, umma_desc_sw128(sb + TC_A + (kk >> 2) * 16384 + (kk & 3) * 32, 1024),
                           umma_desc(sb + TC_B + kk * 4096, 2048, 128), idesc, kk > 0);
             umma_commit(mmad);
         }
     }
-    const bool done = mbar_wait(mmad, 0, abort, kTcWaitLimit);
+    // products done; the operand barrier (long complete) orders the out tile's
+    // landing before this thread's reads of it
+    const bool done = mbar_wait(mmad, 0, abort, kTcWaitLimit) && mbar_wait(full, 0, abort, kTcWaitLimit);
     if (__all_sync(0xffffffffu, done)) {
         tc_fence_after();
+        uint4 ov[16];  // this thread's out row from the swizzled tile
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            ov[q] = *(const uint4 *)(sm + TC_O + (q >> 3) * 16384 + row * 128 +
+                                     (((q & 7) ^ (row & 7)) << 4));
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // 32 columns j at a time
             float d[32];
@@ -301,16 +312,22 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
     PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
     if (a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128 && start_img && enc &&
         ((uintptr_t)start_img & 15u) == 0 && ((uintptr_t)aux_out & 15u) == 0) {
-        // aux viewed as [T_tot, H * 128] BF16, boxes of 8 channels x 128 tokens
-        CUtensorMap tm;
+        // aux and out viewed as [T_tot, H * 128] BF16, boxes of 64 columns x 128
+        // tokens with 128-byte swizzle
+        CUtensorMap tm, tmo;
         const cuuint64_t dims[2] = {(cuuint64_t)a.H * 128, (cuuint64_t)a.T_tot};
         const cuuint64_t strides[1] = {(cuuint64_t)a.H * 128 * 2};
-        const cuuint32_t box[2] = {8, (cuuint32_t)TC_TILE};
+        const cuuint32_t box[2] = {64, (cuuint32_t)TC_TILE};
         const cuuint32_t estr[2] = {1, 1};
+        if (((uintptr_t)a.out & 15u) != 0) return cudaErrorInvalidValue;
         if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(aux_out), dims,
-                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-            CUDA_SUCCESS)
+                CUDA_SUCCESS ||
+            enc(&tmo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+                CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         cudaError_t e = cudaFuncSetAttribute(combine_tc_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
@@ -319,7 +336,7 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
         for (long long base = 0; base < tc_tiles; base += 65535) {
             const unsigned ny = (unsigned)(tc_tiles - base < 65535 ? tc_tiles - base : 65535);
             e = launch_dependent(combine_tc_kernel, dim3((unsigned)units, ny), dim3(128), TC_SMEM, st,
-                                 a, tm, start_img, (int)base);
+                                 a, tm, tmo, start_img, (int)base);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;

@@ -204,6 +204,21 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// K-major operand with 128-byte swizzle, as a SWIZZLE_128B TMA box of 64 BF16
+// columns lays it down: 8-row x 128-byte atoms (rows 128 bytes apart, 16-byte
+// chunk c of row r at c ^ (r mod 8)), 8-row groups `sbo` bytes apart, atoms
+// 1024-byte aligned.  A K-step of 16 elements starts `saddr` 32 bytes further
+// into the atom; the leading-dimension offset is unused for this layout.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;  // LBO (unused with swizzling)
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;  // descriptor version for the sm_100 family
+    d |= (uint64_t)2u << 61;  // layout type: 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor for kind::f16 with BF16 A and B, FP32 accumulator,
 // both operands K-major, dense, shape M x N.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
