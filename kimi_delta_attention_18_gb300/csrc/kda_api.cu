@@ -190,11 +190,14 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     t.S_final = nullptr;
     cudaError_t e = run_prefill_pass(t, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = launch_compose((int)units, Sg, desc->dk, desc->dv, a_img ? nullptr : A, a_img, B, S0,
-                       starts, S_final, img, dev_status, st);
-    if (e != cudaSuccess) return KDA_ERR_CUDA;
     PrefillArgs c = a;
     c.seg_begin = S0 ? 0 : 1;  // from zeros the first segment needs no correction
+    // the tcgen05 combine reads the start states' BF16 images only: the scan then
+    // skips the fp32 copies
+    float *starts_f32 = combine_uses_images(c, aux, img) ? nullptr : starts;
+    e = launch_compose((int)units, Sg, desc->dk, desc->dv, a_img ? nullptr : A, a_img, B, S0,
+                       starts_f32, S_final, img, dev_status, st);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
     return from_cuda(launch_combine(c, starts, aux, img, st));
 }
 

@@ -301,6 +301,13 @@ __global__ void __launch_bounds__(256) combine_simt_kernel(const __grid_constant
 
 }  // namespace
 
+bool combine_uses_images(const PrefillArgs &a, const void *aux_out,
+                         const __nv_bfloat16 *start_img) {
+    return a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128 && start_img &&
+           sm100::tensor_map_encoder() && ((uintptr_t)start_img & 15u) == 0 &&
+           ((uintptr_t)aux_out & 15u) == 0 && ((uintptr_t)a.out & 15u) == 0;
+}
+
 cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void *aux_out,
                            const __nv_bfloat16 *start_img, cudaStream_t st) {
     const long long units = (long long)a.N * a.H * a.Sg;
@@ -310,8 +317,7 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
     const long long seg_tokens = 16 * ((blocks + a.Sg - 1) / a.Sg);
     const long long tiles = (seg_tokens + TILE - 1) / TILE;
     PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
-    if (a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128 && start_img && enc &&
-        ((uintptr_t)start_img & 15u) == 0 && ((uintptr_t)aux_out & 15u) == 0) {
+    if (combine_uses_images(a, aux_out, start_img)) {
         // aux and out viewed as [T_tot, H * 128] BF16, boxes of 64 columns x 128
         // tokens with 128-byte swizzle
         CUtensorMap tm, tmo;
@@ -319,7 +325,6 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
         const cuuint64_t strides[1] = {(cuuint64_t)a.H * 128 * 2};
         const cuuint32_t box[2] = {64, (cuuint32_t)TC_TILE};
         const cuuint32_t estr[2] = {1, 1};
-        if (((uintptr_t)a.out & 15u) != 0) return cudaErrorInvalidValue;
         if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(aux_out), dims,
                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=

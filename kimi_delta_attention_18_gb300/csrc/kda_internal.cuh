@@ -116,6 +116,10 @@ cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const vo
                               void *out, cudaStream_t st);
 cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void *aux_out,
                            const __nv_bfloat16 *start_img, cudaStream_t st);
+// True when launch_combine with these arguments reads only the start images (its
+// tcgen05 path), so the fp32 start states need not be written.
+bool combine_uses_images(const PrefillArgs &a, const void *aux_out,
+                         const __nv_bfloat16 *start_img);
 
 // BF16 image of a 128 x 128 start state as the B operand of a tensor-core
 // product over its 128 key channels i (N = 128 columns j, K = 128 rows i),
