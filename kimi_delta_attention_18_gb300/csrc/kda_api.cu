@@ -3,6 +3,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+#include <vector>
+
 #include "kda_internal.cuh"
 
 namespace {
@@ -106,6 +109,28 @@ size_t workspace_bytes_for(const kda_prefill_desc_t *d, int Sg) {
     const size_t aux = round256((size_t)d->total_tokens * d->num_heads * d->dk * act_bytes(d));
     return states_bytes_for(d, Sg) + img_bytes_for(d, Sg) + aux;
 }
+
+}  // namespace
+
+cudaError_t kda::set_max_dynamic_smem(const void *kernel, int bytes) {
+    struct Entry {
+        const void *kernel;
+        int device, bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &x : done)
+        if (x.kernel == kernel && x.device == dev && x.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.push_back({kernel, dev, bytes});
+    return e;
+}
+
+namespace {
 
 cudaError_t run_prefill_pass(const PrefillArgs &a, cudaStream_t st) {
     if (prefill_tc_supported(a)) return launch_prefill_tc(a, st);

@@ -334,8 +334,7 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
                 CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(combine_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        cudaError_t e = set_max_dynamic_smem((const void *)combine_tc_kernel, TC_SMEM);
         if (e != cudaSuccess) return e;
         const long long tc_tiles = (seg_tokens + TC_TILE - 1) / TC_TILE;
         for (long long base = 0; base < tc_tiles; base += 65535) {
@@ -358,9 +357,7 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
         gtiles = gtiles < 2 ? 2 : gtiles;
         gtiles = gtiles > tiles ? tiles : gtiles;
         const long long groups = (tiles + gtiles - 1) / gtiles;
-        cudaError_t e = cudaFuncSetAttribute(combine_bf16_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             BF16_SMEM);
+        cudaError_t e = set_max_dynamic_smem((const void *)combine_bf16_kernel, BF16_SMEM);
         if (e != cudaSuccess) return e;
         // grid.y is limited to 65535: launch group ranges one after another
         for (long long base = 0; base < groups; base += 65535) {
@@ -378,14 +375,12 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
         const size_t smem = ((size_t)a.dk * a.dv + (size_t)TILE * a.dk) * sizeof(float);
         cudaError_t e;
         if (a.act == KDA_DTYPE_F32) {
-            e = cudaFuncSetAttribute(combine_simt_kernel<float>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            e = set_max_dynamic_smem((const void *)combine_simt_kernel<float>, (int)smem);
             if (e != cudaSuccess) return e;
             combine_simt_kernel<float><<<grid, 256, smem, st>>>(a, starts, (const float *)aux_out,
                                                                 (int)base);
         } else {
-            e = cudaFuncSetAttribute(combine_simt_kernel<__nv_bfloat16>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            e = set_max_dynamic_smem((const void *)combine_simt_kernel<__nv_bfloat16>, (int)smem);
             if (e != cudaSuccess) return e;
             combine_simt_kernel<__nv_bfloat16><<<grid, 256, smem, st>>>(
                 a, starts, (const __nv_bfloat16 *)aux_out, (int)base);

@@ -446,8 +446,7 @@ cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
             CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(compose_mma_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, MB_SMEM);
+        cudaError_t e = set_max_dynamic_smem((const void *)compose_mma_kernel, MB_SMEM);
         if (e != cudaSuccess) return e;
         return launch_dependent(compose_mma_kernel, dim3(units, dv / FCB), dim3(MB_T), MB_SMEM, st,
                                 tm, tmb, Sg, S0, seg_init, S_final, start_img, dev_status);
@@ -466,9 +465,7 @@ cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A,
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
             CUDA_SUCCESS) {
-            cudaError_t e = cudaFuncSetAttribute(compose_tma_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 FAST_SMEM);
+            cudaError_t e = set_max_dynamic_smem((const void *)compose_tma_kernel, FAST_SMEM);
             if (e != cudaSuccess) return e;
             compose_tma_kernel<<<dim3(units, dv / FCB), FT, FAST_SMEM, st>>>(
                 tm, Sg, dv, B, S0, seg_init, S_final, start_img, dev_status);
@@ -476,8 +473,7 @@ cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A,
         }
     }
     const size_t smem = ((size_t)dk * (dk + 1) + 2 * (size_t)dk * CB) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(compose_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_dynamic_smem((const void *)compose_kernel, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(units, (dv + CB - 1) / CB);
     compose_kernel<<<grid, NT, smem, st>>>(Sg, dk, dv, A, B, S0, seg_init, S_final, start_img);

@@ -204,16 +204,14 @@ cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const vo
     const int grid = units < sms ? units : sms;
     if (act == KDA_DTYPE_F32) {
         const int bytes = Layout<float>::BYTES;
-        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<float>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaError_t e = set_max_dynamic_smem((const void *)decode_tma_kernel<float>, bytes);
         if (e != cudaSuccess) return e;
         decode_tma_kernel<float><<<grid, NT, bytes, st>>>(units, (const float *)q, (const float *)k,
                                                           (const float *)v, g, beta, S,
                                                           (float *)out);
     } else {
         const int bytes = Layout<__nv_bfloat16>::BYTES;
-        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<__nv_bfloat16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaError_t e = set_max_dynamic_smem((const void *)decode_tma_kernel<__nv_bfloat16>, bytes);
         if (e != cudaSuccess) return e;
         decode_tma_kernel<__nv_bfloat16><<<grid, NT, bytes, st>>>(
             units, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g,

@@ -100,6 +100,11 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device
+// once: the attribute stays set in the context, so later launches skip the
+// runtime call.  Thread-safe.
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t st);
 bool prefill_tc_supported(const PrefillArgs &a);

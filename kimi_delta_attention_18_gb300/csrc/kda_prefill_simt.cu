@@ -233,13 +233,11 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t st) {
     dim3 grid(units, ncb_v + ncb_a);
     cudaError_t e;
     if (a.act == KDA_DTYPE_F32) {
-        e = cudaFuncSetAttribute(prefill_simt_kernel<float>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = set_max_dynamic_smem((const void *)prefill_simt_kernel<float>, (int)smem);
         if (e != cudaSuccess) return e;
         prefill_simt_kernel<float><<<grid, NT, smem, st>>>(a, cb, ncb_a);
     } else {
-        e = cudaFuncSetAttribute(prefill_simt_kernel<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = set_max_dynamic_smem((const void *)prefill_simt_kernel<__nv_bfloat16>, (int)smem);
         if (e != cudaSuccess) return e;
         prefill_simt_kernel<__nv_bfloat16><<<grid, NT, smem, st>>>(a, cb, ncb_a);
     }

@@ -755,8 +755,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
             !encode_rows(enc, &tg, a.g, a.T_tot, a.H, true))
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = set_max_dynamic_smem((const void *)prefill_tc_kernel, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(units, a.mode == MODE_TRANSFER ? 2 : 1);
     return launch_dependent(prefill_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, a, tq, tk, tv,
