@@ -186,6 +186,25 @@ def prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes):
     return {"transfer_pass": transfer, "segment_scan": scan, "combine": combine}
 
 
+def method_roofline(head_tokens, ms, dk, dv, act_bytes, peaks):
+    """The whole step against the method's own algorithmic counts per head-token:
+    flops = 6 dk dv + C (3 dk + 2 dv) (C = 16, triangle-aware) and bytes = q, k, v,
+    out in the activation dtype + g fp32 + beta fp32; the attainable ceiling is
+    min(P_bf16, I * BW) with I = flops / bytes (I * BW is below P here: HBM-bound)."""
+    C = 16
+    flops = 6 * dk * dv + C * (3 * dk + 2 * dv)
+    nbytes = (2 * dk + 2 * dv) * act_bytes + 4 * dk + 4
+    sec = ms / 1e3
+    tflops = head_tokens * flops / sec / 1e12
+    gbs = head_tokens * nbytes / sec / 1e9
+    attain = min(peaks["bf16_tflops"], flops / nbytes * peaks["hbm_gbs"] / 1e3)
+    return {"flops_per_head_token": flops, "bytes_per_head_token": nbytes,
+            "tflops": round(tflops, 2), "tflops_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
+            "attainable_tflops": round(attain, 1), "attainable_frac": round(tflops / attain, 4),
+            "gbs": round(gbs, 1), "gbs_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "peak_source": peaks["source"]}
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -318,6 +337,8 @@ def run_ours(args):
                          "l2": "512 MB buffer zero-filled between timed steps (working set 50 MB)",
                          "parallelism": "dp%d (one batch per GPU)" % world},
               "wall_s_timed_loop": round(wall, 4), "clocks": clk, "roofline": roofline,
+              "method": method_roofline(T * H * world, dev_ms_max / args.steps, dk, dv,
+                                        act_bytes, peaks),
               "gpu_launches": launches_per_step * args.steps}
 
     # e2e: one-call C entry point with pinned host buffers, copies included
