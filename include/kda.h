@@ -124,6 +124,32 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
                                  int32_t *dev_status, void *stream);
 
 /*
+ * Sparse state checkpoints during prefill (the fixed-size state is the unit of
+ * the prefix cache: digest, section 2.4 (4)).  Everything kda_prefill_chunked
+ * does, and in addition, for every sequence n and k = 0, 1, ... with
+ * (k+1) * ckpt_interval <= len_n, the state after its first (k+1) * ckpt_interval
+ * tokens is written to
+ *     ckpt_states[(base_n + k) * H * dk * dv ...]   ([K, H, dk, dv] fp32),
+ * base_n = sum over m < n of floor(len_m / ckpt_interval), K = that sum over all
+ * sequences (the caller sizes ckpt_states for it; a checkpoint at a sequence's
+ * last token equals its S_final).  ckpt_interval must be a positive multiple of
+ * 16 (the block size), ckpt_states 4-byte aligned and not aliasing any other
+ * argument.  With S > 1 segments the transfer pass also keeps the transfer matrix
+ * so far at each checkpoint (floor(T_tot / ckpt_interval) * H * dk * dk fp32 of
+ * extra workspace) and a last kernel adds its product with the segment's start
+ * state once the scan has it.  Workspace: kda_prefill_ckpt_workspace_size(desc,
+ * ckpt_interval) (0 on invalid arguments).  Errors as for kda_prefill_chunked;
+ * a non-positive or unaligned interval returns KDA_ERR_INVALID_ARG.
+ */
+size_t kda_prefill_ckpt_workspace_size(const kda_prefill_desc_t *desc, int32_t ckpt_interval);
+kda_status_t kda_prefill_chunked_ckpt(const kda_prefill_desc_t *desc, const void *q,
+                                      const void *k, const void *v, const float *g,
+                                      const float *beta, const float *S0,
+                                      const int32_t *cu_seqlens, void *out, float *S_final,
+                                      int32_t ckpt_interval, float *ckpt_states, void *workspace,
+                                      size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * One decode step for `batch` independent sequences (one new token each): the
  * recurrence above applied once, in place on S_inout [batch, H, dk, dv] fp32,
  * with q, k [batch, H, dk], v, out [batch, H, dv] in act_dtype, g [batch, H,

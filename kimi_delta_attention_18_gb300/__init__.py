@@ -13,6 +13,8 @@ from ._native import (  # noqa: F401
     prefill_combine,
     library_path,
     prefill_chunked,
+    prefill_chunked_ckpt,
+    num_checkpoints,
     prefill_desc,
     prefill_num_segments,
     prefill_segments,
@@ -21,6 +23,7 @@ from ._native import (  # noqa: F401
     state_transfer,
 )
 
-__all__ = ["KDAError", "PrefillDesc", "decode_step", "lib", "library_path", "prefill_chunked", "prefill_combine",
-           "prefill_desc", "prefill_num_segments", "prefill_segments", "prefill_workspace_size", "state_compose",
+__all__ = ["KDAError", "PrefillDesc", "decode_step", "lib", "library_path", "num_checkpoints",
+           "prefill_chunked", "prefill_chunked_ckpt", "prefill_combine", "prefill_desc",
+           "prefill_num_segments", "prefill_segments", "prefill_workspace_size", "state_compose",
            "state_transfer"]

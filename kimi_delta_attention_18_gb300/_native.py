@@ -53,6 +53,11 @@ def lib():
             L.kda_prefill_chunked.restype = ctypes.c_int
             L.kda_prefill_chunked.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 10 + \
                 [ctypes.c_size_t, _P, _P]
+            L.kda_prefill_ckpt_workspace_size.restype = ctypes.c_size_t
+            L.kda_prefill_ckpt_workspace_size.argtypes = [ctypes.POINTER(PrefillDesc), _I]
+            L.kda_prefill_chunked_ckpt.restype = ctypes.c_int
+            L.kda_prefill_chunked_ckpt.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 9 + \
+                [_I, _P, _P, ctypes.c_size_t, _P, _P]
             L.kda_prefill_segments.restype = ctypes.c_int
             L.kda_prefill_segments.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 11
             L.kda_prefill_chunked_noalloc.restype = ctypes.c_int
@@ -171,6 +176,70 @@ def prefill_chunked(q, k, v, g, beta, S0=None, cu_seqlens=None, *, num_segments=
                                    _stream(stream, dev))
     _check("kda_prefill_chunked", rc)
     return out, S_final
+
+
+def num_checkpoints(cu_seqlens, ckpt_interval) -> int:
+    """Number of state checkpoints kda_prefill_chunked_ckpt writes: sum over the
+    sequences of floor(len / ckpt_interval) (reads cu_seqlens on the host)."""
+    cu = cu_seqlens.detach().cpu().tolist()
+    return sum((cu[i + 1] - cu[i]) // ckpt_interval for i in range(len(cu) - 1))
+
+
+def prefill_chunked_ckpt(q, k, v, g, beta, S0=None, cu_seqlens=None, *, ckpt_interval,
+                         ckpt_states=None, num_segments=0, out=None, S_final=None,
+                         want_final_state=True, workspace=None, dev_status=None, stream=None):
+    """prefill_chunked that also writes the state after every ckpt_interval tokens
+    of each sequence (see kda_prefill_chunked_ckpt in kda.h).  ckpt_states
+    ``[K, H, dk, dv]`` fp32 with K >= num_checkpoints(cu_seqlens, ckpt_interval)
+    (allocated when None).  Returns ``(out, S_final, ckpt_states)``."""
+    dev = q.device
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    act = _ACT.get(q.dtype)
+    if act is None:
+        raise ValueError("q must be float32 or bfloat16")
+    if int(ckpt_interval) <= 0 or int(ckpt_interval) % 16:
+        raise ValueError("ckpt_interval must be a positive multiple of 16")
+    _need(q, "q", q.dtype, (T, H, dk))
+    _need(k, "k", q.dtype, (T, H, dk), dev)
+    _need(v, "v", q.dtype, (T, H, dv), dev)
+    _need(g, "g", torch.float32, (T, H, dk), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+    N = cu_seqlens.numel() - 1
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _need(out, "out", q.dtype, (T, H, dv), dev)
+    if S_final is None and want_final_state:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if S_final is not None:
+        _need(S_final, "S_final", torch.float32, (N, H, dk, dv), dev)
+    ckpt_buf = ckpt_states
+    if ckpt_states is None:  # at least one slot: the library takes a valid pointer
+        K = num_checkpoints(cu_seqlens, int(ckpt_interval))
+        ckpt_buf = torch.empty((max(K, 1), H, dk, dv), dtype=torch.float32, device=dev)
+        ckpt_states = ckpt_buf[:K]
+    _need(ckpt_buf, "ckpt_states", torch.float32, None, dev)
+    if tuple(ckpt_buf.shape[1:]) != (H, dk, dv) or ckpt_buf.numel() == 0:
+        raise ValueError("ckpt_states must have shape [K, %d, %d, %d], K >= 1" % (H, dk, dv))
+    desc = _desc(N, T, H, dk, dv, act, num_segments)
+    ws_bytes = int(lib().kda_prefill_ckpt_workspace_size(ctypes.byref(desc), int(ckpt_interval)))
+    if ws_bytes > 0 and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, None, dev)
+    rc = lib().kda_prefill_chunked_ckpt(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(out),
+                                        _ptr(S_final), int(ckpt_interval), _ptr(ckpt_buf),
+                                        _ptr(workspace), ws_len, _ptr(dev_status),
+                                        _stream(stream, dev))
+    _check("kda_prefill_chunked_ckpt", rc)
+    return out, S_final, ckpt_states
 
 
 def prefill_segments(q, k, v, g, beta, seg_init_states, cu_seqlens, num_segments, *, seg_begin=0,

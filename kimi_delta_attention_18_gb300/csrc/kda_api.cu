@@ -109,6 +109,16 @@ size_t workspace_bytes_for(const kda_prefill_desc_t *d, int Sg) {
     const size_t aux = round256((size_t)d->total_tokens * d->num_heads * d->dk * act_bytes(d));
     return states_bytes_for(d, Sg) + img_bytes_for(d, Sg) + aux;
 }
+// Checkpoints on the split path: at most floor(T_tot / interval) of them; each
+// holds the identity-start chain's transfer matrix so far (dk x dk fp32 per head).
+int max_checkpoints(const kda_prefill_desc_t *d, int interval) {
+    return interval > 0 ? d->total_tokens / interval : 0;
+}
+size_t ckpt_scratch_bytes(const kda_prefill_desc_t *d, int Sg, int interval) {
+    if (Sg <= 1 || interval <= 0) return 0;
+    return round256((size_t)max_checkpoints(d, interval) * d->num_heads * d->dk * d->dk *
+                    sizeof(float));
+}
 
 }  // namespace
 
@@ -151,11 +161,17 @@ size_t kda_prefill_workspace_size(const kda_prefill_desc_t *desc) {
     return workspace_bytes_for(desc, choose_segments(desc));
 }
 
-kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, const void *k,
-                                 const void *v, const float *g, const float *beta,
-                                 const float *S0, const int32_t *cu_seqlens, void *out,
-                                 float *S_final, void *workspace, size_t workspace_bytes,
-                                 int32_t *dev_status, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// The one-call prefill, optionally with sparse state checkpoints (interval 0:
+// none).
+kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, const void *k,
+                              const void *v, const float *g, const float *beta, const float *S0,
+                              const int32_t *cu_seqlens, void *out, float *S_final,
+                              int32_t ckpt_interval, float *ckpt, void *workspace,
+                              size_t workspace_bytes, int32_t *dev_status, void *stream) {
     kda_status_t rc = check_desc(desc);
     if (rc != KDA_OK) return rc;
     if (desc->num_seqs == 0) return KDA_OK;
@@ -170,8 +186,10 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     const void *elems[] = {beta, S0, S_final, cu_seqlens};
     for (const void *p : elems)
         if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
+    if (ckpt_interval < 0 || ckpt_interval % 16 != 0) return KDA_ERR_INVALID_ARG;
+    if (ckpt_interval > 0 && (!ckpt || !aligned4(ckpt))) return KDA_ERR_INVALID_ARG;
     const int Sg = choose_segments(desc);
-    const size_t need = workspace_bytes_for(desc, Sg);
+    const size_t need = workspace_bytes_for(desc, Sg) + ckpt_scratch_bytes(desc, Sg, ckpt_interval);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
         return KDA_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
@@ -180,6 +198,8 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens;
     a.out = out; a.S_final = S_final; a.dev_status = dev_status;
     a.Sg = Sg;
+    a.ckpt_interval = ckpt_interval;
+    a.ckpt = ckpt_interval > 0 ? ckpt : nullptr;
 
     if (Sg == 1) {
         a.S0 = S0;
@@ -213,17 +233,53 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
     t.emit_out = 1;
     t.aux_out = aux;
     t.S_final = nullptr;
+    if (ckpt_interval > 0)  // partial transfer matrices at the checkpoints
+        t.ckpt_a = (float *)((uint8_t *)workspace + workspace_bytes_for(desc, Sg));
     cudaError_t e = run_prefill_pass(t, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     PrefillArgs c = a;
     c.seg_begin = S0 ? 0 : 1;  // from zeros the first segment needs no correction
+    c.ckpt_interval = 0;
     // the tcgen05 combine reads the start states' BF16 images only: the scan then
-    // skips the fp32 copies
-    float *starts_f32 = combine_uses_images(c, aux, img) ? nullptr : starts;
+    // skips the fp32 copies (unless checkpoints need them)
+    float *starts_f32 =
+        combine_uses_images(c, aux, img) && ckpt_interval == 0 ? nullptr : starts;
     e = launch_compose((int)units, Sg, desc->dk, desc->dv, a_img ? nullptr : A, a_img, B, S0,
                        starts_f32, S_final, img, dev_status, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    return from_cuda(launch_combine(c, starts, aux, img, st));
+    e = launch_combine(c, starts, aux, img, st);
+    if (e != cudaSuccess || ckpt_interval == 0) return from_cuda(e);
+    return from_cuda(launch_ckpt_fixup(t, S0, starts, max_checkpoints(desc, ckpt_interval), st));
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, const void *k,
+                                 const void *v, const float *g, const float *beta,
+                                 const float *S0, const int32_t *cu_seqlens, void *out,
+                                 float *S_final, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream) {
+    return prefill_one_call(desc, q, k, v, g, beta, S0, cu_seqlens, out, S_final, 0, nullptr,
+                            workspace, workspace_bytes, dev_status, stream);
+}
+
+size_t kda_prefill_ckpt_workspace_size(const kda_prefill_desc_t *desc, int32_t ckpt_interval) {
+    if (check_desc(desc) != KDA_OK || ckpt_interval < 0 || ckpt_interval % 16 != 0) return 0;
+    const int Sg = choose_segments(desc);
+    return workspace_bytes_for(desc, Sg) + ckpt_scratch_bytes(desc, Sg, ckpt_interval);
+}
+
+kda_status_t kda_prefill_chunked_ckpt(const kda_prefill_desc_t *desc, const void *q,
+                                      const void *k, const void *v, const float *g,
+                                      const float *beta, const float *S0,
+                                      const int32_t *cu_seqlens, void *out, float *S_final,
+                                      int32_t ckpt_interval, float *ckpt_states, void *workspace,
+                                      size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    if (ckpt_interval <= 0) return KDA_ERR_INVALID_ARG;
+    return prefill_one_call(desc, q, k, v, g, beta, S0, cu_seqlens, out, S_final, ckpt_interval,
+                            ckpt_states, workspace, workspace_bytes, dev_status, stream);
 }
 
 kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_begin,

@@ -72,6 +72,16 @@ struct PrefillArgs {
     void *aux_out;
     int emit_out;
     int32_t *dev_status;
+    // Sparse state checkpoints (ckpt_interval = 0: none).  After every
+    // ckpt_interval tokens of a sequence (a positive multiple of 16) the state goes
+    // to ckpt [K][H][dk][dv] fp32, slot ckpt_base(n) + k for the (k+1)-th
+    // checkpoint of sequence n.  MODE_OUTPUT writes the true state; in
+    // MODE_TRANSFER the zero-start chain writes its state to ckpt and the
+    // identity-start chain its transfer matrix so far to ckpt_a [K][H][dk][dk] (if
+    // set), and launch_ckpt_fixup adds ckpt_a x start_s after the scan.
+    int ckpt_interval;
+    float *ckpt;
+    float *ckpt_a;
     int N, T_tot, H, dk, dv;
     int Sg;                 // segments per sequence (layout and bounds)
     int seg_begin;          // segments seg_begin .. seg_begin+seg_count-1 are
@@ -105,6 +115,14 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 // runtime call.  Thread-safe.
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
 
+// Slot of sequence n's first checkpoint: checkpoints of earlier sequences come
+// first, floor(len / interval) of them per sequence.
+__device__ __forceinline__ int ckpt_base(const int32_t *cu, int n, int interval) {
+    int b = 0;
+    for (int m = 0; m < n; ++m) b += (cu[m + 1] - cu[m]) / interval;
+    return b;
+}
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t st);
 bool prefill_tc_supported(const PrefillArgs &a);
@@ -115,6 +133,12 @@ cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A,
                            const __nv_bfloat16 *a_img, const float *B, const float *S0,
                            float *seg_init, float *S_final, __nv_bfloat16 *start_img,
                            int32_t *dev_status, cudaStream_t st);
+// Split path with checkpoints: ckpt[k] += ckpt_a[k] x start_s for every checkpoint
+// k of every segment s with a nonzero start state (start_0 = S0, start_s for s >= 1
+// from `starts` [N,H,Sg,dk,dv] written by the scan); max_ckpt bounds the number of
+// checkpoints (floor(T_tot / ckpt_interval)).
+cudaError_t launch_ckpt_fixup(const PrefillArgs &a, const float *S0, const float *starts,
+                              int max_ckpt, cudaStream_t st);
 bool decode_tma_supported(int dk, int dv);
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,
                               const void *v, const float *g, const float *beta, float *S,

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs p, int cb,
     int t_begin, t_end;
     if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, t_begin, t_end)) return;
 
+    const int seq0 = p.cu[n];
+    const int cbase = p.ckpt_interval > 0 ? ckpt_base(p.cu, n, p.ckpt_interval) : 0;
     const TA *q = (const TA *)p.q;
     const TA *k = (const TA *)p.k;
     const TA *v = (const TA *)p.v;
@@ -201,6 +203,19 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs p, int cb,
             sm.S[e] = acc;
         }
         __syncthreads();
+
+        if (p.ckpt_interval > 0) {  // state checkpoint after this block
+            const int done = t0 + nt - seq0;
+            float *d = partA ? p.ckpt_a : p.ckpt;
+            const int ldd = partA ? dk : dv;
+            if (done % p.ckpt_interval == 0 && d) {
+                d += ((size_t)(cbase + done / p.ckpt_interval - 1) * H + h) * (size_t)dk * ldd;
+                for (int e = tid; e < dk * cb; e += NT) {
+                    const int i = e / cb, c = e % cb;
+                    if (c < nc) d[(size_t)i * ldd + c0 + c] = sm.S[e];
+                }
+            }
+        }
     }
 
     // Write the state block out.

@@ -138,6 +138,7 @@ struct Ctx {
     uint32_t sbase;
     volatile int *abort;
     int n, h, s;
+    int seq0, ckpt_base;  // the sequence's first token; its first checkpoint slot
     int t_begin, t_end, nchunks;
     bool transfer, partA, want_q, want_v;
     __device__ uint32_t bar(int i) const { return sbase + BAR_OFF + 8 * i; }
@@ -574,6 +575,21 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(x.bar(B_REC_EMPTY + slot));
+        if (p.ckpt_interval > 0) {  // state checkpoint after this block
+            const int done = min(x.t_begin + C * (c + 1), x.t_end) - x.seq0;
+            float *d = x.partA ? p.ckpt_a : p.ckpt;
+            if (done % p.ckpt_interval == 0 && d) {
+                d += ((size_t)(x.ckpt_base + done / p.ckpt_interval - 1) * p.H + x.h) * D * D;
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int n = 0; n < 16; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            d[(size_t)(8 * n + 2 * t4 + (e & 1)) * D + j0 + 16 * m + g8 + 8 * (e >> 1)] =
+                                S[m][n][e];
+            }
+        }
     }
     if (*x.abort) return;
 
@@ -696,6 +712,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (!segment_range(p.cu, x.n, p.N, p.T_tot, x.s, p.Sg, p.dev_status, x.t_begin, x.t_end))
         return;
     x.nchunks = (x.t_end - x.t_begin + C - 1) / C;
+    x.seq0 = p.cu[x.n];
+    x.ckpt_base = p.ckpt_interval > 0 ? ckpt_base(p.cu, x.n, p.ckpt_interval) : 0;
 
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {

@@ -152,3 +152,29 @@ def test_decode_and_compose_host_checks():
                                  None) == OK
     # start images only for BF16 at dk = dv = 128
     assert L.kda_prefill_combine(ctypes.byref(d), 0, p, p, p, p, p, None, None) == INVALID
+
+
+def _prefill_ckpt(desc, interval, ckpt=0x50000, ws=None, ws_len=0):
+    L = kda.lib()
+    p = ctypes.c_void_p(0x10000)
+    return L.kda_prefill_chunked_ckpt(ctypes.byref(desc), p, p, p, p, p, None,
+                                      ctypes.c_void_p(0x20000), p, None, interval,
+                                      ctypes.c_void_p(ckpt) if ckpt else None,
+                                      ctypes.c_void_p(ws) if ws else None, ws_len, None, None)
+
+
+def test_checkpoint_arguments_and_workspace():
+    assert _prefill_ckpt(_desc(), 0) == INVALID         # interval required
+    assert _prefill_ckpt(_desc(), 24) == INVALID        # not a multiple of 16
+    assert _prefill_ckpt(_desc(), -16) == INVALID
+    assert _prefill_ckpt(_desc(), 32, ckpt=0) == INVALID       # buffer missing
+    assert _prefill_ckpt(_desc(), 32, ckpt=0x50002) == INVALID  # misaligned buffer
+    L = kda.lib()
+    d1 = _desc()  # one pass: no extra workspace
+    assert L.kda_prefill_ckpt_workspace_size(ctypes.byref(d1), 32) == 0
+    assert L.kda_prefill_ckpt_workspace_size(ctypes.byref(d1), 24) == 0   # invalid interval
+    d = _desc(num_segments=4)  # split: + floor(T / interval) transfer matrices per head
+    need = L.kda_prefill_ckpt_workspace_size(ctypes.byref(d), 32)
+    r256 = lambda b: (b + 255) // 256 * 256
+    assert need == kda.prefill_workspace_size(d) + r256((64 // 32) * 2 * 16 * 16 * 4)
+    assert _prefill_ckpt(d, 32, ws=0x40000, ws_len=kda.prefill_workspace_size(d)) == WORKSPACE
