@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 PREFILL = "kda_prefill_bf16_h8_t4096_d128"
 DECODE = "kda_decode_b256_h56_d128_x64"
 METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of roofline"
-PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096")
+PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_ckpt_h8_t4096")
 
 
 def parse():
@@ -341,6 +341,9 @@ def run_ours(args):
                                         act_bytes, peaks),
               "gpu_launches": launches_per_step * args.steps}
 
+    # the same step with a state checkpoint every 512 tokens of each sequence
+    result["checkpoints"] = run_ckpt(args, kda, x, flush, stream, dev, dist,
+                                     dev_ms_max / args.steps)
     # e2e: one-call C entry point with pinned host buffers, copies included
     result["e2e"] = run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world)
     if not args.no_decode:
@@ -352,6 +355,45 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_ckpt(args, kda, x, flush, stream, dev, dist, plain_ms, interval=512):
+    """kda_prefill_chunked_ckpt on the timed workload: the step with a state
+    checkpoint after every `interval` tokens, timed like the plain step (L2
+    flushed before each call, CUDA events around it)."""
+    import torch
+    T, H, dk = x["q"].shape
+    dv = x["v"].shape[2]
+    K = kda.num_checkpoints(x["cu_seqlens"], interval)
+    ck = torch.empty((max(K, 1), H, dk, dv), dtype=torch.float32, device=dev)
+    out = torch.empty_like(x["v"])
+    SF = torch.empty((len(x["lengths"]), H, dk, dv), dtype=torch.float32, device=dev)
+    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"])
+    ws_bytes = kda.prefill_ckpt_workspace_size(desc, interval)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def call():
+        kda.prefill_chunked_ckpt(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                 x["cu_seqlens"], ckpt_interval=interval, ckpt_states=ck,
+                                 out=out, S_final=SF, workspace=ws)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    steps = max(5, min(args.steps, 20))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dist, dev) / steps
+    return {"interval": interval, "checkpoints_per_step": K * H,
+            "bytes_per_step": K * H * dk * dv * 4, "ms_per_step": round(ms, 5),
+            "overhead_vs_plain": round(ms / plain_ms - 1.0, 4)}
 
 
 def run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world):
@@ -547,6 +589,12 @@ def run_profile_case(name):
         for _ in range(2):
             kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                 x["cu_seqlens"])
+    elif name == "prefill_ckpt_h8_t4096":
+        # the benchmark's workload with a state checkpoint every 512 tokens
+        x = make_prefill_inputs([4096], 8, 128, 128, "bf16", device=dev)
+        for _ in range(2):
+            kda.prefill_chunked_ckpt(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                     x["cu_seqlens"], ckpt_interval=512)
     torch.cuda.synchronize()
     print("profile case done:", name)
 

@@ -178,6 +178,10 @@ def prefill_chunked(q, k, v, g, beta, S0=None, cu_seqlens=None, *, num_segments=
     return out, S_final
 
 
+def prefill_ckpt_workspace_size(desc, ckpt_interval) -> int:
+    return int(lib().kda_prefill_ckpt_workspace_size(ctypes.byref(desc), int(ckpt_interval)))
+
+
 def num_checkpoints(cu_seqlens, ckpt_interval) -> int:
     """Number of state checkpoints kda_prefill_chunked_ckpt writes: sum over the
     sequences of floor(len / ckpt_interval) (reads cu_seqlens on the host)."""
@@ -227,7 +231,7 @@ def prefill_chunked_ckpt(q, k, v, g, beta, S0=None, cu_seqlens=None, *, ckpt_int
     if tuple(ckpt_buf.shape[1:]) != (H, dk, dv) or ckpt_buf.numel() == 0:
         raise ValueError("ckpt_states must have shape [K, %d, %d, %d], K >= 1" % (H, dk, dv))
     desc = _desc(N, T, H, dk, dv, act, num_segments)
-    ws_bytes = int(lib().kda_prefill_ckpt_workspace_size(ctypes.byref(desc), int(ckpt_interval)))
+    ws_bytes = prefill_ckpt_workspace_size(desc, ckpt_interval)
     if ws_bytes > 0 and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()

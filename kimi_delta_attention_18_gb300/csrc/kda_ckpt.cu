@@ -15,12 +15,16 @@
 namespace kda {
 namespace {
 
-constexpr int FX_ROWS = 16;   // rows i of one checkpoint per CTA
-constexpr int FX_T = 256;
+constexpr int FX_ROWS = 32;   // rows i of one checkpoint per CTA
+constexpr int FX_T = 256;     // 8 warps: warp w takes rows 4w..4w+3, lane l columns 4l..4l+3
+constexpr int FX_ALD = FX_ROWS + 4;  // transposed A rows: 16-byte aligned, 4-way store conflicts
 
 // grid (max_ckpt, H, ceil(dk / FX_ROWS)); CTA (k, h, r) updates rows
-// [16 r, 16 r + 16) of checkpoint k of head h, if that checkpoint exists and its
-// segment has a nonzero start state.
+// [32 r, 32 r + 32) of checkpoint k of head h, if that checkpoint exists and its
+// segment has a nonzero start state.  dv = 4 x 32 lanes = 128 at most: each
+// thread keeps a 4 x 4 block of the product in registers; per key channel q one
+// float4 of A^T (the warp's four rows, a broadcast) and one float4 of the start
+// state row feed 16 fused multiply-adds.
 __global__ void __launch_bounds__(FX_T) ckpt_fixup_kernel(const PrefillArgs p, const float *S0,
                                                           const float *starts) {
     extern __shared__ float sm[];
@@ -53,16 +57,66 @@ __global__ void __launch_bounds__(FX_T) ckpt_fixup_kernel(const PrefillArgs p, c
     const float *A = p.ckpt_a + ((size_t)kg * H + h) * dk * dk;
     float *out = p.ckpt + ((size_t)kg * H + h) * dk * dv;
 
-    float *As = sm;                       // [FX_ROWS][dk]
-    float *Xs = sm + FX_ROWS * dk;        // [dk][dv]
-    for (int e = threadIdx.x; e < rows * dk; e += FX_T) As[e] = A[(size_t)(i0 + e / dk) * dk + e % dk];
-    for (int e = threadIdx.x; e < dk * dv; e += FX_T) Xs[e] = start[e];
+    float *At = sm;                     // [dk][FX_ALD]: A^T of this CTA's rows (0 past `rows`)
+    float *Xs = sm + dk * FX_ALD;       // [dk][dv]
+    // fills with 16-byte loads where the rows allow (A_part lives in the
+    // workspace; S0 is the caller's and only 4-byte aligned)
+    if ((dk & 3) == 0) {
+        for (int e = threadIdx.x; e < FX_ROWS * dk / 4; e += FX_T) {
+            const int r = e / (dk / 4), q = 4 * (e % (dk / 4));
+            const float4 v = r < rows ? *(const float4 *)(A + (size_t)(i0 + r) * dk + q)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            At[q * FX_ALD + r] = v.x;
+            At[(q + 1) * FX_ALD + r] = v.y;
+            At[(q + 2) * FX_ALD + r] = v.z;
+            At[(q + 3) * FX_ALD + r] = v.w;
+        }
+    } else {
+        for (int e = threadIdx.x; e < FX_ROWS * dk; e += FX_T) {
+            const int r = e / dk, q = e % dk;
+            At[q * FX_ALD + r] = r < rows ? A[(size_t)(i0 + r) * dk + q] : 0.f;
+        }
+    }
+    if (((uintptr_t)start & 15u) == 0 && ((dk * dv) & 3) == 0) {
+        for (int e = threadIdx.x; e < dk * dv / 4; e += FX_T)
+            ((float4 *)Xs)[e] = ((const float4 *)start)[e];
+    } else {
+        for (int e = threadIdx.x; e < dk * dv; e += FX_T) Xs[e] = start[e];
+    }
     __syncthreads();
-    for (int e = threadIdx.x; e < rows * dv; e += FX_T) {
-        const int r = e / dv, j = e % dv;
-        float acc = 0.f;
-        for (int q = 0; q < dk; ++q) acc += As[r * dk + q] * Xs[q * dv + j];
-        out[(size_t)(i0 + r) * dv + j] += acc;
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int r0 = 4 * w, j0 = 4 * l;
+    if (j0 >= dv) return;
+    float acc[4][4] = {};
+    auto fma_row = [&](int q, const float (&xr)[4]) {
+        const float4 a = *(const float4 *)(At + q * FX_ALD + r0);
+        const float ar[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) acc[r][t] += ar[r] * xr[t];
+    };
+    if ((dv & 3) == 0 && j0 + 4 <= dv) {  // 16-byte aligned rows of the start state
+#pragma unroll 4
+        for (int q = 0; q < dk; ++q) {
+            const float4 x = *(const float4 *)(Xs + q * dv + j0);
+            const float xr[4] = {x.x, x.y, x.z, x.w};
+            fma_row(q, xr);
+        }
+    } else {
+        for (int q = 0; q < dk; ++q) {
+            float xr[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) xr[t] = j0 + t < dv ? Xs[q * dv + j0 + t] : 0.f;
+            fma_row(q, xr);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        if (r0 + r >= rows) break;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (j0 + t < dv) out[(size_t)(i0 + r0 + r) * dv + j0 + t] += acc[r][t];
     }
 }
 
@@ -71,7 +125,7 @@ __global__ void __launch_bounds__(FX_T) ckpt_fixup_kernel(const PrefillArgs p, c
 cudaError_t launch_ckpt_fixup(const PrefillArgs &a, const float *S0, const float *starts,
                               int max_ckpt, cudaStream_t st) {
     if (a.ckpt_interval <= 0 || !a.ckpt || !a.ckpt_a || max_ckpt <= 0 || a.H == 0) return cudaSuccess;
-    const size_t smem = (size_t)(FX_ROWS * a.dk + a.dk * a.dv) * sizeof(float);
+    const size_t smem = (size_t)(a.dk * FX_ALD + a.dk * a.dv) * sizeof(float);
     cudaError_t e = set_max_dynamic_smem((const void *)ckpt_fixup_kernel, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)max_ckpt, (unsigned)a.H, (unsigned)((a.dk + FX_ROWS - 1) / FX_ROWS));
