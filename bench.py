@@ -341,6 +341,8 @@ def run_ours(args):
                                         act_bytes, peaks),
               "gpu_launches": launches_per_step * args.steps}
 
+    # the same step from the pre-activations (fused gate prologue)
+    result["gated"] = run_gated(args, kda, x, flush, stream, dev, dist, dev_ms_max / args.steps)
     # the same step with a state checkpoint every 512 tokens of each sequence
     result["checkpoints"] = run_ckpt(args, kda, x, flush, stream, dev, dist,
                                      dev_ms_max / args.steps)
@@ -355,6 +357,44 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_gated(args, kda, x, flush, stream, dev, dist, plain_ms):
+    """kda_prefill_chunked_gated on the timed workload (raw q, k; x_g in BF16 and
+    x_beta fp32; the kernels form g, beta and the normalised q, k), timed like the
+    plain step."""
+    import torch
+    T, H, dk = x["q"].shape
+    dv = x["v"].shape[2]
+    if x["q"].dtype != torch.bfloat16 or dk != 128 or dv != 128:
+        return None
+    out = torch.empty_like(x["v"])
+    SF = torch.empty((len(x["lengths"]), H, dk, dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(kda.prefill_workspace_size(kda.prefill_desc(x["q"], x["v"],
+                                                                     x["cu_seqlens"])), 1),
+                     dtype=torch.uint8, device=dev)
+
+    def call():
+        kda.prefill_chunked_gated(x["q_raw"], x["k_raw"], x["v"], x["x_g"], x["x_beta"], None,
+                                  x["cu_seqlens"], out=out, S_final=SF, workspace=ws)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    steps = max(5, min(args.steps, 20))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dist, dev) / steps
+    nbytes = T * H * ((2 * dk + 2 * dv) * 2 + 2 * dk + 4)  # q, k, v, out, x_g BF16, x_beta
+    return {"ms_per_step": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
+            "bytes_per_head_token": nbytes // (T * H), "vs_plain": round(ms / plain_ms - 1.0, 4)}
 
 
 def run_ckpt(args, kda, x, flush, stream, dev, dist, plain_ms, interval=512):

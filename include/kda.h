@@ -124,6 +124,26 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
                                  int32_t *dev_status, void *stream);
 
 /*
+ * Fused gate prologue (digest, section 2.1 (1): g = -5 sigmoid(x), so g in
+ * (-5, 0)): kda_prefill_chunked from the pre-activations, so the gates and the
+ * normalised q, k are never written to memory.  The kernels take
+ *     g = -5 sigmoid(x_g),  beta = sigmoid(x_beta),
+ *     q <- q / ||q||,  k <- k / ||k||  per (token, head) over the key channels
+ * (a zero row stays zero), in fp32, then run exactly as kda_prefill_chunked.
+ * q, k [T_tot, H, dk] and v [T_tot, H, dv] as there (q, k not normalised); x_g
+ * [T_tot, H, dk] in the activation dtype, 16-byte aligned; x_beta [T_tot, H]
+ * fp32.  BF16 activations with dk = dv = 128 only (else KDA_ERR_UNSUPPORTED);
+ * workspace as kda_prefill_workspace_size(desc).  HBM traffic per head-token
+ * falls from 1540 to 1284 bytes at d = 128 (x_g in BF16 instead of fp32 g).
+ */
+kda_status_t kda_prefill_chunked_gated(const kda_prefill_desc_t *desc, const void *q,
+                                       const void *k, const void *v, const void *x_g,
+                                       const float *x_beta, const float *S0,
+                                       const int32_t *cu_seqlens, void *out, float *S_final,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *stream);
+
+/*
  * Sparse state checkpoints during prefill (the fixed-size state is the unit of
  * the prefix cache: digest, section 2.4 (4)).  Everything kda_prefill_chunked
  * does, and in addition, for every sequence n and k = 0, 1, ... with

@@ -14,6 +14,7 @@ from ._native import (  # noqa: F401
     library_path,
     prefill_chunked,
     prefill_chunked_ckpt,
+    prefill_chunked_gated,
     prefill_ckpt_workspace_size,
     num_checkpoints,
     prefill_desc,
@@ -25,7 +26,7 @@ from ._native import (  # noqa: F401
 )
 
 __all__ = ["KDAError", "PrefillDesc", "decode_step", "lib", "library_path", "num_checkpoints",
-           "prefill_chunked", "prefill_chunked_ckpt",
+           "prefill_chunked", "prefill_chunked_ckpt", "prefill_chunked_gated",
            "prefill_ckpt_workspace_size", "prefill_combine", "prefill_desc",
            "prefill_num_segments", "prefill_segments", "prefill_workspace_size", "state_compose",
            "state_transfer"]

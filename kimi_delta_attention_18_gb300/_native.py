@@ -53,6 +53,9 @@ def lib():
             L.kda_prefill_chunked.restype = ctypes.c_int
             L.kda_prefill_chunked.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 10 + \
                 [ctypes.c_size_t, _P, _P]
+            L.kda_prefill_chunked_gated.restype = ctypes.c_int
+            L.kda_prefill_chunked_gated.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 10 + \
+                [ctypes.c_size_t, _P, _P]
             L.kda_prefill_ckpt_workspace_size.restype = ctypes.c_size_t
             L.kda_prefill_ckpt_workspace_size.argtypes = [ctypes.POINTER(PrefillDesc), _I]
             L.kda_prefill_chunked_ckpt.restype = ctypes.c_int
@@ -175,6 +178,52 @@ def prefill_chunked(q, k, v, g, beta, S0=None, cu_seqlens=None, *, num_segments=
                                    _ptr(S_final), _ptr(workspace), ws_len, _ptr(dev_status),
                                    _stream(stream, dev))
     _check("kda_prefill_chunked", rc)
+    return out, S_final
+
+
+def prefill_chunked_gated(q, k, v, x_g, x_beta, S0=None, cu_seqlens=None, *, num_segments=0,
+                          out=None, S_final=None, want_final_state=True, workspace=None,
+                          dev_status=None, stream=None):
+    """Prefill from the pre-activations (see kda_prefill_chunked_gated in kda.h):
+    q, k ``[T, H, 128]`` BF16 not normalised, v ``[T, H, 128]`` BF16, x_g ``[T, H,
+    128]`` BF16, x_beta ``[T, H]`` fp32; the kernels form g = -5 sigmoid(x_g), beta =
+    sigmoid(x_beta) and the normalised q, k.  Returns ``(out, S_final)``."""
+    dev = q.device
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    act = _ACT.get(q.dtype)
+    if act is None:
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, "q", q.dtype, (T, H, dk))
+    _need(k, "k", q.dtype, (T, H, dk), dev)
+    _need(v, "v", q.dtype, (T, H, dv), dev)
+    _need(x_g, "x_g", q.dtype, (T, H, dk), dev)
+    _need(x_beta, "x_beta", torch.float32, (T, H), dev)
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+    N = cu_seqlens.numel() - 1
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _need(out, "out", q.dtype, (T, H, dv), dev)
+    if S_final is None and want_final_state:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if S_final is not None:
+        _need(S_final, "S_final", torch.float32, (N, H, dk, dv), dev)
+    desc = _desc(N, T, H, dk, dv, act, num_segments)
+    ws_bytes = prefill_workspace_size(desc)
+    if ws_bytes > 0 and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, None, dev)
+    rc = lib().kda_prefill_chunked_gated(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(x_g), _ptr(x_beta), _ptr(S0), _ptr(cu_seqlens),
+                                         _ptr(out), _ptr(S_final), _ptr(workspace), ws_len,
+                                         _ptr(dev_status), _stream(stream, dev))
+    _check("kda_prefill_chunked_gated", rc)
     return out, S_final
 
 

@@ -171,8 +171,13 @@ kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, con
                               const void *v, const float *g, const float *beta, const float *S0,
                               const int32_t *cu_seqlens, void *out, float *S_final,
                               int32_t ckpt_interval, float *ckpt, void *workspace,
-                              size_t workspace_bytes, int32_t *dev_status, void *stream) {
+                              size_t workspace_bytes, int32_t *dev_status, void *stream,
+                              int gate = 0) {
     kda_status_t rc = check_desc(desc);
+    if (rc != KDA_OK) return rc;
+    // the fused gate prologue runs in the tensor-core kernels only
+    if (gate && !(desc->act_dtype == KDA_DTYPE_BF16 && desc->dk == 128 && desc->dv == 128))
+        return KDA_ERR_UNSUPPORTED;
     if (rc != KDA_OK) return rc;
     if (desc->num_seqs == 0) return KDA_OK;
     if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
@@ -200,6 +205,7 @@ kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, con
     a.Sg = Sg;
     a.ckpt_interval = ckpt_interval;
     a.ckpt = ckpt_interval > 0 ? ckpt : nullptr;
+    a.gate = gate;
 
     if (Sg == 1) {
         a.S0 = S0;
@@ -263,6 +269,17 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
                                  int32_t *dev_status, void *stream) {
     return prefill_one_call(desc, q, k, v, g, beta, S0, cu_seqlens, out, S_final, 0, nullptr,
                             workspace, workspace_bytes, dev_status, stream);
+}
+
+kda_status_t kda_prefill_chunked_gated(const kda_prefill_desc_t *desc, const void *q,
+                                       const void *k, const void *v, const void *x_g,
+                                       const float *x_beta, const float *S0,
+                                       const int32_t *cu_seqlens, void *out, float *S_final,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *stream) {
+    return prefill_one_call(desc, q, k, v, (const float *)x_g, x_beta, S0, cu_seqlens, out,
+                            S_final, 0, nullptr, workspace, workspace_bytes, dev_status, stream,
+                            1);
 }
 
 size_t kda_prefill_ckpt_workspace_size(const kda_prefill_desc_t *desc, int32_t ckpt_interval) {

@@ -82,6 +82,11 @@ struct PrefillArgs {
     int ckpt_interval;
     float *ckpt;
     float *ckpt_a;
+    // Fused gate prologue (BF16, dk = dv = 128): g points to x_g [T_tot, H, dk] in
+    // the activation dtype and beta to x_beta [T_tot, H] fp32; the kernels take
+    // g = -5 sigmoid(x_g), beta = sigmoid(x_beta) and q, k divided by their L2 norm
+    // per (token, head) (a zero row stays zero).
+    int gate;
     int N, T_tot, H, dk, dv;
     int Sg;                 // segments per sequence (layout and bounds)
     int seg_begin;          // segments seg_begin .. seg_begin+seg_count-1 are

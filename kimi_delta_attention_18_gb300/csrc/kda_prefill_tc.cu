@@ -159,10 +159,13 @@ __device__ __forceinline__ bool warp_wait(const Ctx &x, int b, uint32_t parity) 
 // unconditional; with MASK (the sequence's last, partial block) rows past its
 // end get no decay, no key and no query.  Full blocks take the unmasked form,
 // whose dependency chains are about half as long.
-template <bool WANT_Q, bool MASK>
+// With GATE the box at IN_G holds x_g in BF16, g = -5 sigmoid(x_g) is formed
+// here, and k, q are scaled by their rows' inverse L2 norms rk, rq.
+template <bool WANT_Q, bool MASK, bool GATE>
 __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uint8_t *rec, int nt,
-                                            int lane) {
+                                            int lane, const float (&rk)[C], const float (&rq)[C]) {
     const float *gin = (const float *)(in + IN_G);
+    const __nv_bfloat16 *xin = (const __nv_bfloat16 *)(in + IN_G);
     const __nv_bfloat16 *kin = (const __nv_bfloat16 *)(in + IN_K);
     const __nv_bfloat16 *qin = (const __nv_bfloat16 *)(in + IN_Q);
 #pragma unroll 1
@@ -171,8 +174,16 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
         float al[C], kv[C];
 #pragma unroll
         for (int r = 0; r < C; ++r) {
-            al[r] = gin[r * D + ch];
-            kv[r] = __bfloat162float(kin[r * D + ch]);
+            if (GATE) {
+                const float xg = __bfloat162float(xin[r * D + ch]);
+                // g = -5 sigmoid(x_g); the fast divide (reciprocal and multiply, ~2 ulp)
+                // is far below the BF16 rounding of the operands g feeds
+                al[r] = __fdividef(-5.f, 1.f + __expf(-xg));
+                kv[r] = __bfloat162float(kin[r * D + ch]) * rk[r];
+            } else {
+                al[r] = gin[r * D + ch];
+                kv[r] = __bfloat162float(kin[r * D + ch]);
+            }
         }
         if (MASK) {
 #pragma unroll
@@ -227,7 +238,7 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
             float qv[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float q1 = __bfloat162float(qin[r * D + ch]);
+                const float q1 = __bfloat162float(qin[r * D + ch]) * (GATE ? rq[r] : 1.f);
                 qv[r] = MASK && r >= nt ? 0.f : q1;
             }
             vmul(tmp, qv, fwd);
@@ -240,7 +251,7 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
 // One warp prepares one whole block: elementwise factors, L and Mq and the
 // solve for T, written with V into a record slot.  Prep warp p takes
 // blocks p, p + 4, p + 8, ...; it frees the input stage as soon as it has read it.
-template <bool WANT_Q>
+template <bool WANT_Q, bool GATE>
 __device__ __forceinline__ void prep_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int pw = (threadIdx.x >> 5) - W_PREP0;
@@ -259,7 +270,7 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
     auto issue = [&](int c) {
         if (lane == 0) {
             const uint32_t bytes =
-                (WANT_Q ? 4096u : 0u) + 4096u + (x.want_v ? 4096u : 0u) + 8192u;
+                (WANT_Q ? 4096u : 0u) + 4096u + (x.want_v ? 4096u : 0u) + (GATE ? 4096u : 8192u);
             mbar_arrive_expect_tx(full, bytes);
             const int xc = x.h * D, t0 = x.t_begin + C * c;
             if (WANT_Q) tma_load_2d(in_s + IN_Q, x.tm_q, xc, t0, full);
@@ -273,9 +284,13 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
     auto load_beta = [&](int c, float &lo, float &hi, float &col) {
         const int t0 = x.t_begin + C * c, nt = min(C, x.t_end - t0);
         const float *bp = p.beta + (size_t)t0 * p.H + x.h;
-        lo = g8 < nt ? bp[(size_t)g8 * p.H] : 0.f;
-        hi = g8 + 8 < nt ? bp[(size_t)(g8 + 8) * p.H] : 0.f;
-        col = (lane & 15) < nt ? bp[(size_t)(lane & 15) * p.H] : 0.f;
+        auto b = [&](int r) {  // beta, or sigmoid(x_beta) with the fused prologue
+            const float v = bp[(size_t)r * p.H];
+            return GATE ? __fdividef(1.f, 1.f + __expf(-v)) : v;
+        };
+        lo = g8 < nt ? b(g8) : 0.f;
+        hi = g8 + 8 < nt ? b(g8 + 8) : 0.f;
+        col = (lane & 15) < nt ? b(lane & 15) : 0.f;
     };
     int issued = 0;  // blocks whose copies were issued (for an orderly abort)
     float b_lo = 0.f, b_hi = 0.f, b_col = 0.f;
@@ -296,9 +311,37 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
         const int nt = min(C, x.t_end - (x.t_begin + C * c));
 
+        // ---- fused prologue: inverse L2 norms of this block's k and q rows (a zero
+        // row keeps scale 0), over the 128 channels = 4 per lane, then the warp
+        float rk[C], rq[C];
+        if (GATE) {
+            const __nv_bfloat16 *kin = (const __nv_bfloat16 *)(in + IN_K);
+            const __nv_bfloat16 *qin = (const __nv_bfloat16 *)(in + IN_Q);
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                float sk = 0.f, sq = 0.f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float kv = __bfloat162float(kin[r * D + lane + 32 * m]);
+                    sk += kv * kv;
+                    if (WANT_Q) {
+                        const float qv = __bfloat162float(qin[r * D + lane + 32 * m]);
+                        sq += qv * qv;
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                    if (WANT_Q) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                }
+                rk[r] = sk > 0.f ? rsqrtf(sk) : 0.f;
+                rq[r] = sq > 0.f ? rsqrtf(sq) : 0.f;
+            }
+        }
+
         // ---- elementwise: lane handles key channels lane + 32 m
-        if (nt == C) elementwise<WANT_Q, false>(in, scr, rec, nt, lane);
-        else elementwise<WANT_Q, true>(in, scr, rec, nt, lane);
+        if (nt == C) elementwise<WANT_Q, false, GATE>(in, scr, rec, nt, lane, rk, rq);
+        else elementwise<WANT_Q, true, GATE>(in, scr, rec, nt, lane, rk, rq);
         // V into the record (padded rows).  Rows past the block's end become zero:
         // they are weighted by zero in the chain's products, and the next
         // sequence's values (or anything non-finite in them) must not leak in.
@@ -675,12 +718,16 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
 // parameter: the identity-start and zero-start CTAs of the transfer pass then
 // run the same instructions, so the code that the first of them fetches into the
 // instruction caches serves the other, and the kernel's code footprint halves.
-template <bool WANT_Q>
+template <bool WANT_Q, bool GATE>
 __device__ __forceinline__ void run_role(const Ctx &x, int warp) {
-    if (warp < W_CHAIN0) prep_role<WANT_Q>(x);
+    if (warp < W_CHAIN0) prep_role<WANT_Q, GATE>(x);
     else chain_role<WANT_Q>(x);
 }
 
+// GATE (the fused prologue) is a separate kernel: the plain kernel's code is then
+// only its own, which matters because the kernel starts with cold instruction
+// caches after the scan and the combine of the previous call.
+template <bool GATE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -727,8 +774,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncthreads();
 
-    if (x.want_q) run_role<true>(x, warp);
-    else run_role<false>(x, warp);
+    if (GATE) run_role<true, true>(x, warp);  // (the fused prologue always has q)
+    else if (x.want_q) run_role<true, false>(x, warp);
+    else run_role<false, false>(x, warp);
 
     __syncthreads();
     if (threadIdx.x == 0 && *x.abort) dev_fail(p.dev_status, KDA_ERR_TIMEOUT);
@@ -737,6 +785,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs &a) {
+    if (a.gate && !(a.q && (a.mode == MODE_OUTPUT || a.emit_out))) return false;
     return a.act == KDA_DTYPE_BF16 && a.dk == D && a.dv == D;
 }
 
@@ -770,14 +819,20 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
         if (!encode_rows(enc, &tq, qp, a.T_tot, a.H, false) ||
             !encode_rows(enc, &tk, a.k, a.T_tot, a.H, false) ||
             !encode_rows(enc, &tv, a.v, a.T_tot, a.H, false) ||
-            !encode_rows(enc, &tg, a.g, a.T_tot, a.H, true))
+            !encode_rows(enc, &tg, a.g, a.T_tot, a.H, !a.gate))
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = set_max_dynamic_smem((const void *)prefill_tc_kernel, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
     dim3 grid(units, a.mode == MODE_TRANSFER ? 2 : 1);
-    return launch_dependent(prefill_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, a, tq, tk, tv,
-                            tg);
+    if (a.gate) {
+        cudaError_t e = set_max_dynamic_smem((const void *)prefill_tc_kernel<true>, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        return launch_dependent(prefill_tc_kernel<true>, grid, dim3(NTHREADS), SMEM_BYTES, st, a,
+                                tq, tk, tv, tg);
+    }
+    cudaError_t e = set_max_dynamic_smem((const void *)prefill_tc_kernel<false>, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(prefill_tc_kernel<false>, grid, dim3(NTHREADS), SMEM_BYTES, st, a, tq,
+                            tk, tv, tg);
 }
 
 }  // namespace kda

@@ -42,15 +42,19 @@ def make_prefill_inputs(lengths, H, dk, dv, act="bf16", *, seed=0, s0_std=None,
 
     Returns a dict: q, k ``[T, H, dk]`` and v ``[T, H, dv]`` in the activation
     dtype; g ``[T, H, dk]`` and beta ``[T, H]`` fp32; S0 ``[N, H, dk, dv]`` fp32 or
-    None; cu_seqlens int32 ``[N+1]`` (on ``device``) and ``lengths``.
+    None; cu_seqlens int32 ``[N+1]`` (on ``device``) and ``lengths``.  The same
+    draws before their preparation, for the fused-prologue entry point: q_raw,
+    k_raw (not normalised) and x_g in the activation dtype, x_beta fp32.
     """
     lengths = [int(x) for x in lengths]
     T = sum(lengths)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     dt = DTYPES[act]
-    q = _unit_rows(_normal((T, H, dk), gen, device)).to(dt)
-    k = _unit_rows(_normal((T, H, dk), gen, device)).to(dt)
+    q_raw = _normal((T, H, dk), gen, device)
+    k_raw = _normal((T, H, dk), gen, device)
+    q = _unit_rows(q_raw).to(dt)
+    k = _unit_rows(k_raw).to(dt)
     v = _normal((T, H, dv), gen, device).to(dt)
     xg = _normal((T, H, dk), gen, device, mean=-10.0 if slow_decay else 0.0)
     xb = _normal((T, H), gen, device, mean=-6.0 if slow_decay else 0.0)
@@ -64,7 +68,9 @@ def make_prefill_inputs(lengths, H, dk, dv, act="bf16", *, seed=0, s0_std=None,
         cu.append(cu[-1] + L)
     cu_seqlens = torch.tensor(cu, dtype=torch.int32, device=device)
     return {"q": q, "k": k, "v": v, "g": g.contiguous(), "beta": beta.contiguous(),
-            "S0": S0, "cu_seqlens": cu_seqlens, "lengths": lengths}
+            "S0": S0, "cu_seqlens": cu_seqlens, "lengths": lengths,
+            "q_raw": q_raw.to(dt), "k_raw": k_raw.to(dt), "x_g": xg.to(dt).contiguous(),
+            "x_beta": xb.contiguous()}
 
 
 def make_decode_inputs(batch, H, dk, dv, steps, act="bf16", *, seed=0, s0_std=0.02,

@@ -20,6 +20,10 @@ Contents
                         zero-initial state B (the recurrence run from zeros):
                         S_end = A S_start + B (digest section 2.4 (1)).
 ``kda_state_compose``   the prefix scan S_s = A_{s-1} S_{s-1} + B_{s-1}.
+``gate_prologue``       the inputs from their pre-activations: g = -5 sigmoid(x_g)
+                        (digest section 2.1 (1)), beta = sigmoid(x_beta), and q, k
+                        divided by their L2 norm per (token, head), as the input
+                        recipe prepares them (a zero row stays zero).
 
 Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
 closed forms, brute-force matrix products, special cases and invariants; none is
@@ -202,3 +206,18 @@ def kda_state_compose(A, B, S0=None):
         starts[:, s] = cur
         cur = np.matmul(A[:, s], cur) + B[:, s]
     return starts, cur
+
+
+def gate_prologue(q, k, x_g, x_beta):
+    """Fused-prologue reference, in fp64: returns (q / |q|, k / |k|, g, beta) with
+    g = -5 sigmoid(x_g) (the bounded gate of the digest, section 2.1 (1): g in
+    (-5, 0)) and beta = sigmoid(x_beta); norms over the last (key-channel) axis
+    per (token, head); a row of zeros stays zero."""
+    q, k, x_g, x_beta = _f64(q), _f64(k), _f64(x_g), _f64(x_beta)
+
+    def unit(x):
+        n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+        return np.where(n > 0, x / np.where(n > 0, n, 1.0), 0.0)
+
+    sig = lambda z: 1.0 / (1.0 + np.exp(-z))
+    return unit(q), unit(k), -5.0 * sig(x_g), sig(x_beta)

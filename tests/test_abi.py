@@ -178,3 +178,17 @@ def test_checkpoint_arguments_and_workspace():
     r256 = lambda b: (b + 255) // 256 * 256
     assert need == kda.prefill_workspace_size(d) + r256((64 // 32) * 2 * 16 * 16 * 4)
     assert _prefill_ckpt(d, 32, ws=0x40000, ws_len=kda.prefill_workspace_size(d)) == WORKSPACE
+
+
+def test_gated_prefill_host_checks():
+    L = kda.lib()
+    p = ctypes.c_void_p(0x10000)
+    call = lambda d: L.kda_prefill_chunked_gated(ctypes.byref(d), p, p, p, p, p, None,
+                                                 ctypes.c_void_p(0x20000), p, None, None, 0,
+                                                 None, None)
+    # the fused prologue runs in the BF16 d = 128 kernels only
+    assert call(_desc()) == UNSUPPORTED
+    assert call(_desc(act_dtype=1, dk=64, dv=64)) == UNSUPPORTED
+    assert call(_desc(act_dtype=1, dk=128, dv=128, num_seqs=0)) == OK  # nothing to do
+    d = _desc(act_dtype=1, dk=128, dv=128, num_segments=4)
+    assert call(d) == WORKSPACE  # split needs the workspace of kda_prefill_workspace_size

@@ -344,3 +344,25 @@ def test_segment_bounds_cover_each_sequence_once():
             assert b[n, 0, 0] == cu[n] and b[n, -1, 1] == cu[n + 1]
             assert np.all(b[n, 1:, 0] == b[n, :-1, 1])
             assert np.all((b[n, :, 0] - cu[n]) % 16 == 0)
+
+
+def test_gate_prologue_closed_forms():
+    """g = -5 sigmoid(x) and beta = sigmoid(x) at points with exact values, the
+    reflection sigmoid(x) + sigmoid(-x) = 1 (catches a sign slip in the
+    exponent), and the per-row L2 normalisation of q and k (3-4-5 rows, a zero
+    row, scale invariance, over the last axis only)."""
+    x = np.array([0.0, np.log(3.0), -np.log(3.0), 40.0, -40.0])
+    q = np.array([[[3.0, 4.0]], [[0.0, 0.0]], [[-6.0, 8.0]]])  # [T=3, H=1, d=2]
+    k = 2.5 * q
+    qn, kn, g, beta = oracle.gate_prologue(q, k, x, x)
+    assert g[0] == -2.5 and beta[0] == 0.5
+    assert abs(beta[1] - 0.75) < 1e-15 and abs(beta[2] - 0.25) < 1e-15
+    assert abs(g[1] + 3.75) < 1e-14 and abs(g[2] + 1.25) < 1e-14
+    assert abs(g[3] + 5.0) < 1e-15 and -1e-15 < g[4] < 0.0
+    assert np.allclose(g[[1, 3]] + g[[2, 4]], -5.0, atol=1e-14, rtol=0)
+    assert np.allclose(qn[0, 0], [0.6, 0.8], atol=1e-15) and np.all(qn[1] == 0.0)
+    assert np.allclose(qn[2, 0], [-0.6, 0.8], atol=1e-15)
+    assert np.allclose(kn, qn, atol=1e-15)  # scale invariance
+    rows = oracle.gate_prologue(np.random.default_rng(1).normal(size=(5, 3, 16)),
+                                np.zeros((5, 3, 16)), np.zeros(1), np.zeros(1))[0]
+    assert np.allclose(np.linalg.norm(rows, axis=-1), 1.0, atol=1e-14)
