@@ -297,6 +297,15 @@ const char *kda_status_string(kda_status_t status);
 /* Build description (target architecture, library version). Never NULL. */
 const char *kda_build_info(void);
 
+/*
+ * Self-test of the bounded device-side waits: one CTA waits, with a limit of
+ * about limit_us microseconds of SM clocks, on an mbarrier that nothing arrives
+ * on, then records KDA_ERR_TIMEOUT in dev_status (device int32, first error
+ * wins) and returns, the same path every kernel takes when a wait gives up.
+ * Nothing faults and the context stays usable.  limit_us in (0, 1e7].
+ */
+kda_status_t kda_selftest_wait_timeout(int32_t limit_us, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -73,6 +73,8 @@ def lib():
             L.kda_prefill_combine.argtypes = [ctypes.POINTER(PrefillDesc), _I] + [_P] * 7
             L.kda_state_compose.restype = ctypes.c_int
             L.kda_state_compose.argtypes = [_I] * 4 + [_P] * 7
+            L.kda_selftest_wait_timeout.restype = ctypes.c_int
+            L.kda_selftest_wait_timeout.argtypes = [_I, _P, _P]
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_status_string.argtypes = [ctypes.c_int]
             L.kda_build_info.restype = ctypes.c_char_p
@@ -464,3 +466,13 @@ def state_compose(transfer, zero_init_state, S0=None, *, seg_init_states=None, S
                                  _stream(stream, dev))
     _check("kda_state_compose", rc)
     return seg_init_states, S_final
+
+
+def selftest_wait_timeout(limit_us, dev_status, stream=None):
+    """Run the bounded-wait self-test (see kda_selftest_wait_timeout in kda.h): a
+    wait that nothing completes gives up after ~limit_us and writes status 5
+    (KDA_ERR_TIMEOUT) to dev_status (a device int32 tensor)."""
+    _need(dev_status, "dev_status", torch.int32, None)
+    rc = lib().kda_selftest_wait_timeout(int(limit_us), _ptr(dev_status),
+                                         _stream(stream, dev_status.device))
+    _check("kda_selftest_wait_timeout", rc)

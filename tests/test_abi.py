@@ -192,3 +192,9 @@ def test_gated_prefill_host_checks():
     assert call(_desc(act_dtype=1, dk=128, dv=128, num_seqs=0)) == OK  # nothing to do
     d = _desc(act_dtype=1, dk=128, dv=128, num_segments=4)
     assert call(d) == WORKSPACE  # split needs the workspace of kda_prefill_workspace_size
+
+
+def test_selftest_host_checks():
+    L = kda.lib()
+    assert L.kda_selftest_wait_timeout(0, ctypes.c_void_p(0x10000), None) == INVALID
+    assert L.kda_selftest_wait_timeout(1000, None, None) == INVALID

@@ -312,3 +312,17 @@ def test_split_stages_with_output_correction(act, d, first):
     assert rel_err(_np(SF).reshape(N, H, d, d), S_ref) <= tol
     if imgs is not None:  # the mma.sync path from the fp32 states agrees too
         assert rel_err(_np(out2), o_ref) <= tol
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """A device-side wait that nothing completes gives up after its limit, writes
+    KDA_ERR_TIMEOUT (5) to dev_status and leaves the context usable: the next
+    prefill runs and matches the oracle."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda._native.selftest_wait_timeout(2000, st)  # ~2 ms
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5
+    x = _gpu_inputs([100, 37], 2, 128, 128, "bf16", seed=41)
+    o_ref, S_ref = _oracle_prefill(x)
+    out, SF = _run(x, 1)
+    assert rel_err(_np(out), o_ref) <= 2e-2 and rel_err(_np(SF), S_ref) <= 2e-2
