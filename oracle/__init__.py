@@ -20,6 +20,9 @@ Contents
                         zero-initial state B (the recurrence run from zeros):
                         S_end = A S_start + B (digest section 2.4 (1)).
 ``kda_state_compose``   the prefix scan S_s = A_{s-1} S_{s-1} + B_{s-1}.
+``kda_backward``        gradients of the recurrence for <d_out, o> + <d_S_final,
+                        S_final> with respect to q, k, v, g, beta and S0 (fp64
+                        PyTorch autograd over the token loop; small problems).
 ``gate_prologue``       the inputs from their pre-activations: g = -5 sigmoid(x_g)
                         (digest section 2.1 (1)), beta = sigmoid(x_beta), and q, k
                         divided by their L2 norm per (token, head), as the input
@@ -221,3 +224,48 @@ def gate_prologue(q, k, x_g, x_beta):
 
     sig = lambda z: 1.0 / (1.0 + np.exp(-z))
     return unit(q), unit(k), -5.0 * sig(x_g), sig(x_beta)
+
+
+def kda_backward(q, k, v, g, beta, S0, cu_seqlens, d_out, d_S_final=None):
+    """Gradients of the recurrence (the same token loop as ``kda_forward``: decay,
+    erase, write, then read o_t = S_t^T q_t; "Kimi K3 Architecture Explained",
+    section 3) with respect to q, k, v, g, beta and S0, for the loss
+    <d_out, o> + <d_S_final, S_final>.  Plain fp64 PyTorch on the CPU: the forward
+    written out token by token and differentiated by autograd (a library
+    primitive); small problems only.  Returns (dq, dk, dv, dg, dbeta, dS0) as numpy
+    arrays (dS0 zero-shaped like S0, or None when S0 is None)."""
+    import torch
+
+    t = lambda a: torch.tensor(_f64(a), dtype=torch.float64, requires_grad=True)
+    Q, K, V, G, B = t(q), t(k), t(v), t(g), t(beta)
+    T, H, dk = Q.shape
+    dv = V.shape[2]
+    cu = [int(c) for c in np.asarray(cu_seqlens)]
+    N = len(cu) - 1
+    S0t = t(S0) if S0 is not None else None
+    outs, finals = [], []
+    for n in range(N):
+        rows = []
+        fin = []
+        for h in range(H):
+            S = S0t[n, h] if S0t is not None else torch.zeros(dk, dv, dtype=torch.float64)
+            o_h = []
+            for i in range(cu[n], cu[n + 1]):
+                S = torch.exp(G[i, h])[:, None] * S                      # decay
+                kk = K[i, h]
+                S = S - B[i, h] * torch.outer(kk, kk @ S)                # erase
+                S = S + B[i, h] * torch.outer(kk, V[i, h])               # write
+                o_h.append(S.T @ Q[i, h])                                # read
+            rows.append(torch.stack(o_h) if o_h else torch.zeros(0, dv, dtype=torch.float64))
+            fin.append(S)
+        outs.append(torch.stack(rows, dim=1))
+        finals.append(torch.stack(fin))
+    O = torch.cat(outs, dim=0)
+    SF = torch.stack(finals)
+    loss = (O * torch.tensor(_f64(d_out))).sum()
+    if d_S_final is not None:
+        loss = loss + (SF * torch.tensor(_f64(d_S_final))).sum()
+    loss.backward()
+    g_or_zero = lambda x: (x.grad if x.grad is not None else torch.zeros_like(x)).numpy()
+    dS0 = g_or_zero(S0t) if S0t is not None else None
+    return g_or_zero(Q), g_or_zero(K), g_or_zero(V), g_or_zero(G), g_or_zero(B), dS0

@@ -366,3 +366,41 @@ def test_gate_prologue_closed_forms():
     rows = oracle.gate_prologue(np.random.default_rng(1).normal(size=(5, 3, 16)),
                                 np.zeros((5, 3, 16)), np.zeros(1), np.zeros(1))[0]
     assert np.allclose(np.linalg.norm(rows, axis=-1), 1.0, atol=1e-14)
+
+
+def test_backward_forward_matches_and_finite_differences():
+    """The backward's own forward equals the C oracle, and every gradient equals
+    central finite differences of the C oracle's loss on a tiny problem (two
+    sequences, S0, non-uniform gates), so a dropped term or a wrong sign in the
+    differentiated loop fails here and not only on the GPU."""
+    rng = np.random.default_rng(7)
+    lengths, H, d = [4, 3], 2, 3
+    T = sum(lengths)
+    cu = np.array([0, 4, 7], dtype=np.int32)
+    q, k, v = (rng.normal(size=(T, H, d)) for _ in range(3))
+    g = -5.0 / (1.0 + np.exp(-rng.normal(size=(T, H, d))))
+    beta = 1.0 / (1.0 + np.exp(-rng.normal(size=(T, H))))
+    S0 = rng.normal(size=(2, H, d, d))
+    dO = rng.normal(size=(T, H, d))
+    dSF = rng.normal(size=(2, H, d, d))
+    grads = oracle.kda_backward(q, k, v, g, beta, S0, cu, dO, dSF)
+
+    def loss(q_, k_, v_, g_, b_, s_):
+        o, sf = oracle.kda_forward(q_, k_, v_, g_, b_, s_, cu)
+        return float(np.sum(o * dO) + np.sum(sf * dSF))
+
+    args = [q, k, v, g, beta, S0]
+    eps = 1e-6
+    for which, grad in enumerate(grads):
+        x = args[which]
+        flat = x.reshape(-1)
+        fd = np.zeros_like(flat)
+        for i in range(flat.size):
+            keep = flat[i]
+            flat[i] = keep + eps
+            up = loss(*args)
+            flat[i] = keep - eps
+            dn = loss(*args)
+            flat[i] = keep
+            fd[i] = (up - dn) / (2 * eps)
+        assert np.allclose(grad.reshape(-1), fd, rtol=1e-6, atol=1e-7), which
