@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 PREFILL = "kda_prefill_bf16_h8_t4096_d128"
 DECODE = "kda_decode_b256_h56_d128_x64"
 METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of roofline"
-PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_ckpt_h8_t4096")
+PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_ckpt_h8_t4096",
+                 "backward_h8_t1024")
 
 
 def parse():
@@ -346,6 +347,7 @@ def run_ours(args):
     # the same step with a state checkpoint every 512 tokens of each sequence
     result["checkpoints"] = run_ckpt(args, kda, x, flush, stream, dev, dist,
                                      dev_ms_max / args.steps)
+    result["backward"] = run_backward(args, kda, x, flush, stream, dev, dist)
     # e2e: one-call C entry point with pinned host buffers, copies included
     result["e2e"] = run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world)
     if not args.no_decode:
@@ -434,6 +436,44 @@ def run_ckpt(args, kda, x, flush, stream, dev, dist, plain_ms, interval=512):
     return {"interval": interval, "checkpoints_per_step": K * H,
             "bytes_per_step": K * H * dk * dv * 4, "ms_per_step": round(ms, 5),
             "overhead_vs_plain": round(ms / plain_ms - 1.0, 4)}
+
+
+def run_backward(args, kda, x, flush, stream, dev, dist):
+    """kda_prefill_backward on the timed workload (d_out ~ N(0, 1), d_S_final ~
+    N(0, 1)): dq, dk, dv, dg, dbeta, dS0 in fp32; L2 flushed before each call,
+    CUDA events around it."""
+    import torch
+    from kimi_delta_attention_18_gb300.inputs import make_backward_adjoints
+    T, H, dk = x["q"].shape
+    dv = x["v"].shape[2]
+    N = len(x["lengths"])
+    act = "bf16" if x["q"].dtype == torch.bfloat16 else "f32"
+    d_out, d_sf = make_backward_adjoints(T, N, H, dk, dv, act, seed=7, device=dev)
+    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"])
+    ws = torch.empty(max(kda.prefill_backward_workspace_size(desc), 16), dtype=torch.uint8,
+                     device=dev)
+
+    def call():
+        kda.prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["cu_seqlens"],
+                             d_out, d_sf, workspace=ws)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    steps = 5
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dist, dev) / steps
+    return {"what": "dq, dk, dv, dg, dbeta, dS0 (fp32), token-level SIMT kernel",
+            "ms_per_step": round(ms, 4), "tokens_per_s": round(N and T / (ms * 1e-3), 1),
+            "ctas": N * H * ((dv + 31) // 32)}
 
 
 def run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world):
@@ -635,6 +675,14 @@ def run_profile_case(name):
         for _ in range(2):
             kda.prefill_chunked_ckpt(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                      x["cu_seqlens"], ckpt_interval=512)
+    elif name == "backward_h8_t1024":
+        # the backward kernel on the benchmark's shape at a quarter of its length
+        from kimi_delta_attention_18_gb300.inputs import make_backward_adjoints
+        x = make_prefill_inputs([1024], 8, 128, 128, "bf16", device=dev)
+        d_out, d_sf = make_backward_adjoints(1024, 1, 8, 128, 128, "bf16", seed=7, device=dev)
+        for _ in range(2):
+            kda.prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                 x["cu_seqlens"], d_out, d_sf)
     torch.cuda.synchronize()
     print("profile case done:", name)
 

@@ -291,6 +291,33 @@ kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_desc_t *desc, const v
                                          const int32_t *cu_seqlens, void *out, float *S_final,
                                          int32_t *dev_status, void *stream);
 
+/*
+ * Backward pass of the prefill ("Kimi K3 Architecture Explained", section 3: the
+ * per-token recurrence, differentiated).  For the same inputs as
+ * kda_prefill_chunked (q, k, v, g, beta, S0, cu_seqlens; q and k as the recurrence
+ * uses them, i.e. already normalised) and the adjoints d_out [T_tot, H, dv] (the
+ * activation dtype) and d_S_final [N, H, dk, dv] fp32 (NULL: zero), writes the
+ * gradients of <d_out, o> + <d_S_final, S_final>:
+ *     dq, dk, dg  [T_tot, H, dk] fp32,   dv [T_tot, H, dv] fp32,
+ *     dbeta [T_tot, H] fp32,             dS0 [N, H, dk, dv] fp32 (NULL: skipped).
+ * dg is the gradient with respect to the log-decay g (alpha = e^g).  All outputs
+ * are overwritten (dq, dk, dg, dbeta are zeroed on the stream, then accumulated);
+ * none may alias an input.  Computed in fp32 at token granularity: one CTA per
+ * (sequence, head, 32 value columns) recomputes the states from a checkpoint at
+ * every 16-token block start kept in the workspace
+ * (kda_prefill_backward_workspace_size(desc), 0 on invalid arguments; 16-byte
+ * aligned).  desc->num_segments is ignored.  Pointers 4-byte aligned;
+ * KDA_ERR_INVALID_ARG on a missing or misaligned pointer, KDA_ERR_WORKSPACE on a
+ * short workspace, KDA_ERR_UNSUPPORTED as kda_prefill_chunked.
+ */
+size_t kda_prefill_backward_workspace_size(const kda_prefill_desc_t *desc);
+kda_status_t kda_prefill_backward(const kda_prefill_desc_t *desc, const void *q, const void *k,
+                                  const void *v, const float *g, const float *beta,
+                                  const float *S0, const int32_t *cu_seqlens, const void *d_out,
+                                  const float *d_S_final, float *dq, float *dk, float *dv,
+                                  float *dg, float *dbeta, float *dS0, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, void *stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char *kda_status_string(kda_status_t status);
 

@@ -12,6 +12,8 @@ from ._native import (  # noqa: F401
     lib,
     prefill_combine,
     library_path,
+    prefill_backward,
+    prefill_backward_workspace_size,
     prefill_chunked,
     prefill_chunked_ckpt,
     prefill_chunked_gated,
@@ -26,7 +28,8 @@ from ._native import (  # noqa: F401
 )
 
 __all__ = ["KDAError", "PrefillDesc", "decode_step", "lib", "library_path", "num_checkpoints",
-           "prefill_chunked", "prefill_chunked_ckpt", "prefill_chunked_gated",
+           "prefill_backward",
+           "prefill_backward_workspace_size", "prefill_chunked", "prefill_chunked_ckpt", "prefill_chunked_gated",
            "prefill_ckpt_workspace_size", "prefill_combine", "prefill_desc",
            "prefill_num_segments", "prefill_segments", "prefill_workspace_size", "state_compose",
            "state_transfer"]

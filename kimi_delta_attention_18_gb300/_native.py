@@ -61,6 +61,11 @@ def lib():
             L.kda_prefill_chunked_ckpt.restype = ctypes.c_int
             L.kda_prefill_chunked_ckpt.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 9 + \
                 [_I, _P, _P, ctypes.c_size_t, _P, _P]
+            L.kda_prefill_backward_workspace_size.restype = ctypes.c_size_t
+            L.kda_prefill_backward_workspace_size.argtypes = [ctypes.POINTER(PrefillDesc)]
+            L.kda_prefill_backward.restype = ctypes.c_int
+            L.kda_prefill_backward.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 16 + \
+                [ctypes.c_size_t, _P, _P]
             L.kda_prefill_segments.restype = ctypes.c_int
             L.kda_prefill_segments.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 11
             L.kda_prefill_chunked_noalloc.restype = ctypes.c_int
@@ -295,6 +300,60 @@ def prefill_chunked_ckpt(q, k, v, g, beta, S0=None, cu_seqlens=None, *, ckpt_int
                                         _stream(stream, dev))
     _check("kda_prefill_chunked_ckpt", rc)
     return out, S_final, ckpt_states
+
+
+def prefill_backward_workspace_size(desc) -> int:
+    """Workspace bytes kda_prefill_backward needs for ``desc`` (0 on invalid input)."""
+    return int(lib().kda_prefill_backward_workspace_size(ctypes.byref(desc)))
+
+
+def prefill_backward(q, k, v, g, beta, S0, cu_seqlens, d_out, d_S_final=None, *,
+                     want_dS0=True, workspace=None, dev_status=None, stream=None):
+    """Gradients of <d_out, o> + <d_S_final, S_final> for the prefill of the same
+    inputs (see kda_prefill_backward in kda.h).  d_out ``[T, H, dv]`` in the
+    activation dtype, d_S_final ``[N, H, dk, dv]`` fp32 or None.  Returns fp32
+    ``(dq, dk, dv, dg, dbeta, dS0)`` (dS0 None unless want_dS0)."""
+    dev = q.device
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    act = _ACT.get(q.dtype)
+    if act is None:
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, "q", q.dtype, (T, H, dk))
+    _need(k, "k", q.dtype, (T, H, dk), dev)
+    _need(v, "v", q.dtype, (T, H, dv), dev)
+    _need(g, "g", torch.float32, (T, H, dk), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    _need(d_out, "d_out", q.dtype, (T, H, dv), dev)
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+    N = cu_seqlens.numel() - 1
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, (N, H, dk, dv), dev)
+    if d_S_final is not None:
+        _need(d_S_final, "d_S_final", torch.float32, (N, H, dk, dv), dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq = torch.empty((T, H, dk), **f32)
+    dk_ = torch.empty((T, H, dk), **f32)
+    dv_ = torch.empty((T, H, dv), **f32)
+    dg = torch.empty((T, H, dk), **f32)
+    dbeta = torch.empty((T, H), **f32)
+    dS0 = torch.empty((N, H, dk, dv), **f32) if want_dS0 else None
+    desc = _desc(N, T, H, dk, dv, act, 0)
+    ws_bytes = prefill_backward_workspace_size(desc)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    ws_len = workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, None, dev)
+    rc = lib().kda_prefill_backward(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                    _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(d_out),
+                                    _ptr(d_S_final), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg),
+                                    _ptr(dbeta), _ptr(dS0), _ptr(workspace), ws_len,
+                                    _ptr(dev_status), _stream(stream, dev))
+    _check("kda_prefill_backward", rc)
+    return dq, dk_, dv_, dg, dbeta, dS0
 
 
 def prefill_segments(q, k, v, g, beta, seg_init_states, cu_seqlens, num_segments, *, seg_begin=0,

@@ -299,6 +299,39 @@ kda_status_t kda_prefill_chunked_ckpt(const kda_prefill_desc_t *desc, const void
                             ckpt_states, workspace, workspace_bytes, dev_status, stream);
 }
 
+size_t kda_prefill_backward_workspace_size(const kda_prefill_desc_t *desc) {
+    if (check_desc(desc) != KDA_OK) return 0;
+    return backward_workspace_bytes(desc->num_seqs, desc->total_tokens, desc->num_heads, desc->dk,
+                                    desc->dv);
+}
+
+kda_status_t kda_prefill_backward(const kda_prefill_desc_t *desc, const void *q, const void *k,
+                                  const void *v, const float *g, const float *beta,
+                                  const float *S0, const int32_t *cu_seqlens, const void *d_out,
+                                  const float *d_S_final, float *dq, float *dk, float *dv,
+                                  float *dg, float *dbeta, float *dS0, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    kda_status_t rc = check_desc(desc);
+    if (rc != KDA_OK) return rc;
+    if (desc->num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (desc->total_tokens > 0 &&
+        (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg || !dbeta))
+        return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, S0, cu_seqlens, d_out, d_S_final,
+                          dq, dk, dv, dg, dbeta, dS0};
+    for (const void *p : ptrs)
+        if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
+    const size_t need = backward_workspace_bytes(desc->num_seqs, desc->total_tokens,
+                                                 desc->num_heads, desc->dk, desc->dv);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+    PrefillArgs a = base_args(desc);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0; a.cu = cu_seqlens;
+    a.dev_status = dev_status;
+    return from_cuda(launch_backward(a, d_out, d_S_final, dq, dk, dv, dg, dbeta, dS0, workspace,
+                                     (cudaStream_t)stream));
+}
+
 kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_begin,
                                   int32_t seg_end, const void *q, const void *k, const void *v,
                                   const float *g, const float *beta,

@@ -144,6 +144,13 @@ cudaError_t launch_compose(int units, int Sg, int dk, int dv, const float *A,
 // checkpoints (floor(T_tot / ckpt_interval)).
 cudaError_t launch_ckpt_fixup(const PrefillArgs &a, const float *S0, const float *starts,
                               int max_ckpt, cudaStream_t st);
+
+// Backward pass (kda_backward.cu): workspace bytes, and the launch (zeroes the
+// accumulated outputs on st first).
+size_t backward_workspace_bytes(int N, int T_tot, int H, int dk, int dv);
+cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float *dSF, float *dq,
+                            float *dk, float *dv, float *dg, float *dbeta, float *dS0,
+                            void *workspace, cudaStream_t st);
 bool decode_tma_supported(int dk, int dv);
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,
                               const void *v, const float *g, const float *beta, float *S,

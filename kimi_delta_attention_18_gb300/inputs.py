@@ -73,6 +73,18 @@ def make_prefill_inputs(lengths, H, dk, dv, act="bf16", *, seed=0, s0_std=None,
             "x_beta": xb.contiguous()}
 
 
+def make_backward_adjoints(T, N, H, dk, dv, act="bf16", *, seed=0, device="cpu",
+                           final=True):
+    """Adjoints for the backward pass: d_out ``[T, H, dv]`` ~ N(0, 1) in the
+    activation dtype and, if ``final``, d_S_final ``[N, H, dk, dv]`` ~ N(0, 1) fp32
+    (else None), drawn in that order from one generator seeded with ``seed``."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    d_out = _normal((T, H, dv), gen, device).to(DTYPES[act])
+    d_sf = _normal((N, H, dk, dv), gen, device) if final else None
+    return d_out, d_sf
+
+
 def make_decode_inputs(batch, H, dk, dv, steps, act="bf16", *, seed=0, s0_std=0.02,
                        device="cpu", slow_decay=False):
     """``steps`` successive single-token inputs for ``batch`` sequences.

@@ -198,3 +198,33 @@ def test_selftest_host_checks():
     L = kda.lib()
     assert L.kda_selftest_wait_timeout(0, ctypes.c_void_p(0x10000), None) == INVALID
     assert L.kda_selftest_wait_timeout(1000, None, None) == INVALID
+
+
+def test_backward_host_checks():
+    L = kda.lib()
+    p = ctypes.c_void_p(0x10000)
+
+    def call(d, ws=None, ws_len=0, g=p, cu=ctypes.c_void_p(0x20000), dq=p):
+        return L.kda_prefill_backward(ctypes.byref(d), p, p, p, g, p, None, cu, p, None, dq, p,
+                                      p, p, p, None, ctypes.c_void_p(ws) if ws else None,
+                                      ws_len, None, None)
+
+    d = _desc()
+    need = L.kda_prefill_backward_workspace_size(ctypes.byref(d))
+    # block-start states [T/16 + N blocks][H][dk][dv] (256-rounded) + one block of
+    # token states [16][dk][32 columns] per (sequence, head, column block)
+    r256 = lambda b: (b + 255) // 256 * 256
+    blocks = d.total_tokens // 16 + d.num_seqs
+    ncb = (d.dv + 31) // 32
+    assert need == r256(blocks * d.num_heads * d.dk * d.dv * 4) + \
+        d.num_seqs * d.num_heads * ncb * 16 * d.dk * 32 * 4
+    assert L.kda_prefill_backward_workspace_size(ctypes.byref(_desc(chunk=32))) == 0
+    assert call(d) == WORKSPACE
+    assert call(d, ws=0x40000, ws_len=need - 1) == WORKSPACE
+    assert call(d, ws=0x40008, ws_len=need) == WORKSPACE       # not 16-byte aligned
+    assert call(d, ws=0x40000, ws_len=need, g=None) == INVALID  # input missing
+    assert call(d, ws=0x40000, ws_len=need, dq=None) == INVALID  # output missing
+    assert call(d, ws=0x40000, ws_len=need, dq=ctypes.c_void_p(0x10002)) == INVALID
+    assert call(d, ws=0x40000, ws_len=need, cu=None) == INVALID
+    assert call(_desc(num_seqs=0)) == OK  # nothing to do
+    assert call(_desc(dk=256)) == UNSUPPORTED

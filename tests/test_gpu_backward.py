@@ -1,0 +1,108 @@
+"""GPU parity of the backward pass (kda_prefill_backward) against the oracle's
+fp64 autograd of the token recurrence: every gradient element by element on
+ragged multi-sequence batches (several 16-token blocks and a ragged tail per
+sequence, a ragged last column block, empty sequences), with a material initial
+state and final-state adjoint; at the bench size, two sampled heads against the
+oracle and linearity in the adjoints over the whole output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import kimi_delta_attention_18_gb300 as kda
+from kimi_delta_attention_18_gb300.inputs import make_backward_adjoints, make_prefill_inputs
+from tests.conftest import rel_err
+
+pytestmark = pytest.mark.gpu
+
+# fp32 arithmetic on both activation dtypes: the oracle sees the same (BF16-exact)
+# inputs, so the fp32 bound applies to both.
+TOL = 1e-4
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dS0")
+
+
+def _np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def _run(x, d_out, d_sf, **kw):
+    x = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    got = kda.prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"],
+                               x["cu_seqlens"], d_out.cuda(),
+                               None if d_sf is None else d_sf.cuda(), **kw)
+    torch.cuda.synchronize()
+    return got
+
+
+def _oracle(x, d_out, d_sf, heads=None):
+    sel = (lambda a: a) if heads is None else (lambda a: a[:, heads])
+    q, k, v, g, b = (sel(_np(x[n])) for n in ("q", "k", "v", "g", "beta"))
+    N = len(x["lengths"])
+    S0 = _np(x["S0"]) if x["S0"] is not None else np.zeros(
+        (N, x["q"].shape[1], x["q"].shape[2], x["v"].shape[2]))
+    if heads is not None:
+        S0 = S0[:, heads]
+    dsf = None if d_sf is None else _np(d_sf)
+    if dsf is not None and heads is not None:
+        dsf = dsf[:, heads]
+    return oracle.kda_backward(q, k, v, g, b, S0, x["cu_seqlens"].cpu().numpy(),
+                               sel(_np(d_out)), dsf)
+
+
+@pytest.mark.parametrize("act,dk,dv,lengths,slow", [
+    ("f32", 32, 32, [100, 37], True),
+    ("f32", 48, 40, [53, 0, 81, 16], True),   # ragged column block (40 = 32 + 8)
+    ("f32", 16, 16, [64], False),
+    ("bf16", 128, 128, [70, 33], True),
+    ("bf16", 128, 96, [47, 90], False),
+])
+def test_backward_matches_oracle(act, dk, dv, lengths, slow):
+    H = 2
+    x = make_prefill_inputs(lengths, H, dk, dv, act, s0_std=1.0, seed=31, slow_decay=slow)
+    d_out, d_sf = make_backward_adjoints(sum(lengths), len(lengths), H, dk, dv, act, seed=32)
+    got = _run(x, d_out, d_sf)
+    ref = _oracle(x, d_out, d_sf)
+    for name, a, b in zip(NAMES, got, ref):
+        assert rel_err(_np(a), b) <= TOL, (name, rel_err(_np(a), b))
+
+
+def test_backward_without_initial_or_final_state():
+    lengths = [29, 0, 50]
+    x = make_prefill_inputs(lengths, 2, 32, 32, "f32", seed=33)
+    d_out, _ = make_backward_adjoints(sum(lengths), 3, 2, 32, 32, "f32", seed=34, final=False)
+    got = _run(x, d_out, None)
+    ref = _oracle(x, d_out, None)  # zero S0: its gradient is still defined
+    for name, a, b in zip(NAMES, got, ref):
+        assert rel_err(_np(a), b) <= TOL, name
+    # an empty sequence's dS0 is its (zero) final-state adjoint
+    assert torch.count_nonzero(got[5][1]) == 0
+
+
+def test_backward_skips_dS0_and_overwrites_outputs():
+    lengths = [40, 24]
+    x = make_prefill_inputs(lengths, 2, 32, 32, "f32", s0_std=1.0, seed=35)
+    d_out, d_sf = make_backward_adjoints(64, 2, 2, 32, 32, "f32", seed=36)
+    a = _run(x, d_out, d_sf)
+    b = _run(x, d_out, d_sf, want_dS0=False)
+    assert b[5] is None
+    for u, w in zip(a[:5], b[:5]):  # the accumulated outputs start from zero every call
+        assert torch.allclose(u, w, rtol=0, atol=1e-6 * float(u.abs().max()))
+
+
+def test_backward_bench_size_sampled_heads_and_linearity():
+    """B=1, H=8, T=4096, d=128 BF16 (the bench workload): heads 0 and 5 against the
+    oracle; all heads: the gradients are linear in (d_out, d_S_final)."""
+    T, H, d = 4096, 8, 128
+    x = make_prefill_inputs([T], H, d, d, "bf16", seed=37)
+    d1, s1 = make_backward_adjoints(T, 1, H, d, d, "bf16", seed=38)
+    got = _run(x, d1, s1)
+    for h in (0, 5):
+        ref = _oracle(x, d1, s1, heads=[h])
+        for name, a, b in zip(NAMES, got, ref):
+            a = _np(a)[:, [h]]
+            assert rel_err(a, b) <= TOL, (h, name)
+    # linearity: backward(2 d_out, 2 d_S_final) = 2 backward(d_out, d_S_final),
+    # exact in binary floating point up to the atomics' summation order
+    g2 = _run(x, (d1.float() * 2).to(d1.dtype), s1 * 2)
+    for name, a, b in zip(NAMES, got, g2):
+        assert rel_err(_np(b), 2 * _np(a)) <= 1e-5, name
