@@ -15,69 +15,111 @@
 //     dS_prev = Diag(alpha) dM
 // and at the sequence start dS0 = dS.
 //
-// Columns of S and dS evolve independently (every step mixes rows only), so one
-// CTA takes (sequence, head, 32-column block): thread i holds row i of both
-// blocks in registers.  A forward pass stores the state at every 16-token block
-// start (workspace); the reverse pass recomputes each block's 16 token states
-// from its start and walks them backwards.  Column sums (u, w) go through
-// shared memory; row sums (dq, dk, dg) and dbeta, which every column block
-// contributes to, are accumulated with atomics into zeroed fp32 outputs.
-// fp32 throughout: a first, token-level implementation of the row (the chunked
-// tensor-core form of the backward is not built).
+// Columns of S and dS evolve independently (every step mixes rows only).  One
+// CTA takes (sequence, head, 32 value columns): four consumer warps own 8
+// columns each and all dk <= 128 rows (4 rows per lane), so the column sums u and
+// w of a token stay inside a warp (shuffles, no block barrier).  A producer warp
+// stages every 8-token block's inputs (g, k, q, v, d_out, beta) into a
+// double-buffered shared-memory ring ahead of use, by bulk copies where the rows
+// allow.  A forward pass keeps the state at every block start in the workspace;
+// the reverse pass recomputes the block's token states into shared memory and
+// walks them backwards.  dv and dS0 are column-local and written directly; the
+// row sums dq, dk, dg and dbeta are summed over the consumer warps in shared
+// memory once per block and added to zeroed fp32 outputs with global atomics
+// (one per column block).  fp32 throughout: a token-level
+// implementation (the chunked tensor-core form of the backward is not built).
 #include "kda_internal.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int BC = 16;   // tokens per stored block
-constexpr int CB = 32;   // state columns per CTA
-constexpr int BT = 128;  // threads: one state row each (dk <= 128)
+using namespace sm100;
+
+constexpr int BB = 8;             // tokens per stored block
+constexpr int WC = 8;             // state columns per consumer warp
+constexpr int NWC = 4;            // consumer warps (one per SM sub-partition)
+constexpr int CTC = WC * NWC;     // columns per CTA
+constexpr int RPL = 4;            // rows per lane: dk <= 128
+constexpr int BT = 32 * (NWC + 1);
+constexpr long long kWaitLimit = 4000000000ll;  // ~2 s of SM clocks
+
+// shared memory (floats): ring [2] of {alpha = e^g [BB][128] fp32; k, q [BB][128] and v,
+// d_out [BB][CTC] in the activation dtype (regions sized for fp32); beta [BB]};
+// token states [NWC][BB][WC/4][128] float4; each consumer warp's row sums
+// [NWC][BB][3][128] and dbeta [NWC][BB] of the block; then the mbarriers and
+// the abort flag.
+constexpr int R_G = 0, R_K = BB * 128, R_Q = 2 * BB * 128, R_V = 3 * BB * 128,
+              R_D = R_V + BB * CTC, R_B = R_D + BB * CTC, R_SIZE = 3600;
+constexpr int SM_TOK = 2 * R_SIZE;
+constexpr int TOK_W = BB * 128 * WC;
+constexpr int SM_PART = SM_TOK + NWC * TOK_W;
+constexpr int SM_PB = SM_PART + NWC * BB * 3 * 128;
+constexpr int SM_BAR = SM_PB + NWC * BB;  // 6 mbarriers (12 floats), then the flag
+constexpr size_t BWD_SMEM = (size_t)(SM_BAR + 12 + 4) * sizeof(float);
+static_assert(R_B + BB <= R_SIZE && (R_SIZE % 4) == 0 && (R_D % 4) == 0, "ring layout");
+static_assert((SM_BAR % 2) == 0 && (SM_TOK % 4) == 0, "alignment");
+static_assert(WC % 4 == 0 && 32 % WC == 0, "columns per warp");
 
 struct BwdArgs {
     const void *q, *k, *v, *dout;
     const float *g, *beta, *S0, *dSF;
     const int32_t *cu;
     float *gq, *gk, *gv, *gg, *gbeta, *gS0;  // dq, dk, dv, dg, dbeta, dS0
-    float *blk_states;   // [sum_n ceil(len_n / 16)][H][dk][dv]: state at each block start
-    float *tok_states;   // [N*H*ncb][16][dk][CB]: one block's pre-token states
+    float *blk_states;  // [blocks][H][ncw][dk][8]: the state at each 8-token block start
     int32_t *dev_status;
-    int N, T_tot, H, dk, dv, ncb, act;
+    int N, T_tot, H, dk, dv, ncw, act;
+    int bulk;  // rows and column slices meet the bulk-copy rules (16-byte aligned)
 };
 
-// Column sums of a 32 x 32 block held one row per lane: x[j] of lane l is entry
-// (l, j); lane l returns the sum of column l.  Each halving step trades half of
-// the remaining columns with the partner lane (16 + 8 + 4 + 2 + 1 shuffles).
-__device__ __forceinline__ float warp_colsum(float (&x)[CB]) {
+// Column sums of a WC-column block spread over the warp's lanes (p[j] of lane
+// l: lane l's part of column j); lane l returns the total of column l % WC.
+// log2(WC) halving steps trade half of the remaining columns with the partner
+// lane, then log2(32 / WC) more add the lane groups.
+__device__ __forceinline__ float colsum(float (&p)[WC]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
+    for (int off = WC / 2; off >= 1; off >>= 1) {
         const bool up = lane & off;
 #pragma unroll
         for (int j = 0; j < off; ++j) {
-            const float send = up ? x[j] : x[j + off];
-            const float keep = up ? x[j + off] : x[j];
-            x[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            const float send = up ? p[j] : p[j + off];
+            const float keep = up ? p[j + off] : p[j];
+            p[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
-    return x[0];
+    float s = p[0];
+#pragma unroll
+    for (int off = WC; off < 32; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    return s;
 }
 
-// One token's inputs as a thread needs them (row i of q, k, g; column i of v and
-// d_out), loaded a token ahead of their use.
-struct TokIn {
-    float g, kv, qv, b, vj, dj;
-};
+// WC consecutive activations (aligned to their size) as fp32
+__device__ __forceinline__ void loadW(const float *p, float (&o)[WC]) {
+#pragma unroll
+    for (int i = 0; i < WC / 4; ++i) {
+        const float4 a = ((const float4 *)p)[i];
+        o[4 * i] = a.x; o[4 * i + 1] = a.y; o[4 * i + 2] = a.z; o[4 * i + 3] = a.w;
+    }
+}
+__device__ __forceinline__ void loadW(const __nv_bfloat16 *p, float (&o)[WC]) {
+#pragma unroll
+    for (int i = 0; i < WC / 4; ++i) {
+        const uint2 a = ((const uint2 *)p)[i];
+        o[4 * i] = __uint_as_float(a.x << 16);
+        o[4 * i + 1] = __uint_as_float(a.x & 0xffff0000u);
+        o[4 * i + 2] = __uint_as_float(a.y << 16);
+        o[4 * i + 3] = __uint_as_float(a.y & 0xffff0000u);
+    }
+}
 
 template <typename TA>
-__global__ void __launch_bounds__(BT) backward_kernel(const BwdArgs a) {
-    __shared__ float part[2][BT / 32][CB];  // per-warp column sums
-    __shared__ float col[2][CB];            // u, w after the cross-warp sum
-    __shared__ float vs[CB], dos[CB];       // this token's v and d_out columns
-    const int unit = blockIdx.x, cbk = blockIdx.y;
+__global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const int unit = blockIdx.x, cb = blockIdx.y;
     const int n = unit / a.H, h = unit % a.H;
-    const int c0 = cbk * CB, nc = min(CB, a.dv - c0);
-    const int i = threadIdx.x, wp = i >> 5, lane = i & 31;
-    const bool row = i < a.dk;
+    const int c0 = cb * CTC;
+    const int wp = threadIdx.x >> 5, l = threadIdx.x & 31;
     const int dk = a.dk, dv = a.dv, H = a.H;
     int t_begin, t_end;
     if (!segment_range(a.cu, n, a.N, a.T_tot, 0, 1, a.dev_status, t_begin, t_end)) return;
@@ -88,194 +130,384 @@ __global__ void __launch_bounds__(BT) backward_kernel(const BwdArgs a) {
             dev_fail(a.dev_status, KDA_ERR_INVALID_ARG);
             return;
         }
-        blk_base += (lm + BC - 1) / BC;
+        blk_base += (lm + BB - 1) / BB;
     }
-    const int nblk = (t_end - t_begin + BC - 1) / BC;
-    const TA *q = (const TA *)a.q, *k = (const TA *)a.k, *v = (const TA *)a.v;
-    const TA *dout = (const TA *)a.dout;
-    // this CTA's token states [16][dk][CB] (256-byte aligned: whole float4 rows)
-    float4 *tok = (float4 *)(a.tok_states + ((size_t)unit * a.ncb + cbk) * BC * dk * CB);
-    auto blk_row = [&](int c) {
-        return a.blk_states + (((size_t)(blk_base + c) * H + h) * dk + i) * dv + c0;
-    };
-    auto load = [&](int t, bool back) {
-        TokIn r;
-        const size_t ix = ((size_t)t * H + h) * dk + i;
-        const size_t iv = ((size_t)t * H + h) * dv + c0 + i;
-        r.g = row ? a.g[ix] : 0.f;
-        r.kv = row ? act_ld(k, ix) : 0.f;
-        r.qv = back && row ? act_ld(q, ix) : 0.f;
-        r.b = a.beta[(size_t)t * H + h];
-        r.vj = i < nc ? act_ld(v, iv) : 0.f;  // zero past the last column: those
-        r.dj = back && i < nc ? act_ld(dout, iv) : 0.f;  // columns of S, dS stay 0
-        return r;
-    };
-
-    float S[CB];
-#pragma unroll
-    for (int j = 0; j < CB; ++j)
-        S[j] = (row && j < nc && a.S0) ? a.S0[((size_t)unit * dk + i) * dv + c0 + j] : 0.f;
-
-    // one forward token step on this column block: S <- M + beta k u^T with
-    // M = Diag(alpha) S, u = v - M^T k
-    auto step = [&](const TokIn &x) {
-        const float alpha = row ? expf(x.g) : 0.f;
-        if (i < CB) vs[i] = x.vj;
-        float y[CB];
-#pragma unroll
-        for (int j = 0; j < CB; ++j) {
-            S[j] *= alpha;
-            y[j] = S[j] * x.kv;
+    const int nblk = (t_end - t_begin + BB - 1) / BB;
+    // full[2] (ring slot ready), empty[2] (slot consumed), landed[2] (bulk copies in)
+    const uint32_t bar0 = smem_addr(sm + SM_BAR);
+    volatile int *abort = (volatile int *)(sm + SM_BAR + 12);
+    // padded rows (past dk) and columns (past dv) of the ring stay zero: the
+    // producer writes only the real ones
+    for (int e = threadIdx.x; e < 2 * R_SIZE; e += BT) sm[e] = 0.f;
+    fence_async_smem();  // before the bulk copies overwrite these bytes
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar0 + 8 * b, 32);                // producer lanes
+            mbar_init(bar0 + 16 + 8 * b, 32 * NWC);     // consumer threads
+            mbar_init(bar0 + 32 + 8 * b, 1);            // bulk bytes
         }
-        part[0][wp][lane] = warp_colsum(y);
-        __syncthreads();
-        if (i < CB) {
-            float s = 0.f;
-#pragma unroll
-            for (int w = 0; w < BT / 32; ++w) s += part[0][w][i];
-            col[0][i] = vs[i] - s;
-        }
-        __syncthreads();
-        const float bk = x.b * x.kv;
-#pragma unroll
-        for (int j = 0; j < CB; ++j) S[j] += bk * col[0][j];
-        __syncthreads();  // part, col and vs are rewritten by the next step
-    };
-
-    // forward: the state at every block start
-    {
-        TokIn cur = t_begin < t_end ? load(t_begin, false) : TokIn{};
-        for (int t = t_begin; t < t_end; ++t) {
-            if (((t - t_begin) & (BC - 1)) == 0 && row) {
-                float *d = blk_row((t - t_begin) / BC);
-#pragma unroll
-                for (int j = 0; j < CB; ++j)
-                    if (j < nc) d[j] = S[j];
-            }
-            TokIn nxt = cur;
-            if (t + 1 < t_end) nxt = load(t + 1, false);
-            step(cur);
-            cur = nxt;
-        }
+        *abort = 0;
+        mbar_fence_init();
     }
+    __syncthreads();
+    // blocks are visited forward (c = 0 .. nblk-1), then backward (nblk-1 .. 0)
+    auto block_of = [&](int f) { return f < nblk ? f : 2 * nblk - 1 - f; };
 
-    // reverse
-    float dS[CB];
+    if (wp == NWC) {  // ---------------------------------------------- producer
+        const TA *q = (const TA *)a.q, *k = (const TA *)a.k, *v = (const TA *)a.v;
+        const TA *dout = (const TA *)a.dout;
+        for (int f = 0; f < 2 * nblk; ++f) {
+            const int buf = f & 1, use = f >> 1;
+            const bool back = f >= nblk;
+            bool ok = true;
+            if (use >= 1) ok = mbar_wait(bar0 + 16 + 8 * buf, (use - 1) & 1, abort, kWaitLimit);
+            const uint32_t full = bar0 + 8 * buf;
+            if (ok) {
+                float *rb = sm + buf * R_SIZE;
+                TA *rk = (TA *)(rb + R_K), *rq = (TA *)(rb + R_Q);
+                TA *rv = (TA *)(rb + R_V), *rd = (TA *)(rb + R_D);
+                const int tb = t_begin + block_of(f) * BB, nt = min(BB, t_end - tb);
+                if (a.bulk) {  // one bulk copy per token row, counted in bytes on `landed`
+                    const uint32_t landed = bar0 + 32 + 8 * buf;
+                    const int nvc = min(CTC, dv - c0);
+                    const uint32_t es = sizeof(TA);
+                    const uint32_t per_tok =
+                        dk * 4 + dk * es + nvc * es + (back ? dk * es + nvc * es : 0);
+                    fence_async_smem();  // this warp's earlier writes to the slot come first
+                    if (l == 0) mbar_arrive_expect_tx(landed, nt * per_tok);
+                    __syncwarp();
+                    if (l < nt) {
+                        const size_t row = (size_t)(tb + l) * H + h;
+                        bulk_g2s(smem_addr(rb + R_G + l * 128), a.g + row * dk, dk * 4, landed);
+                        bulk_g2s(smem_addr(rk + l * 128), k + row * dk, dk * es, landed);
+                        bulk_g2s(smem_addr(rv + l * CTC), v + row * dv + c0, nvc * es, landed);
+                        if (back) {
+                            bulk_g2s(smem_addr(rq + l * 128), q + row * dk, dk * es, landed);
+                            bulk_g2s(smem_addr(rd + l * CTC), dout + row * dv + c0, nvc * es,
+                                     landed);
+                        }
+                        rb[R_B + l] = a.beta[row];
+                    }
+                    // alpha = e^g in place, once for all consumer warps and visits
+                    if (mbar_wait(landed, use & 1, abort, kWaitLimit)) {
 #pragma unroll
-    for (int j = 0; j < CB; ++j)
-        dS[j] = (row && j < nc && a.dSF) ? a.dSF[((size_t)unit * dk + i) * dv + c0 + j] : 0.f;
-    const int ir = min(i, dk - 1);  // rows past dk read a valid row and discard it
-    for (int c = nblk - 1; c >= 0; --c) {
-        const int tb = t_begin + c * BC, te = min(tb + BC, t_end);
-        {
-            const float *s0 = blk_row(c);
+                        for (int j = 0; j < BB; ++j)
 #pragma unroll
-            for (int j = 0; j < CB; ++j) S[j] = (row && j < nc) ? s0[j] : 0.f;
-        }
-        TokIn cur = load(tb, false);
-        for (int t = tb; t < te; ++t) {  // the block's pre-token states
-            if (row) {
-                float4 *d = tok + ((size_t)(t - tb) * dk + i) * (CB / 4);
+                            for (int rr = 0; rr < RPL; ++rr)
+                                if (j < nt && l + 32 * rr < dk)
+                                    rb[R_G + j * 128 + l + 32 * rr] =
+                                        expf(rb[R_G + j * 128 + l + 32 * rr]);
+                    }
+                } else {  // plain loads, a block's worth in flight
+                    float gv_[BB][RPL], kv_[BB][RPL];
 #pragma unroll
-                for (int j = 0; j < CB / 4; ++j)
-                    d[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-            }
-            TokIn nxt = cur;
-            if (t + 1 < te) nxt = load(t + 1, false);
-            step(cur);
-            cur = nxt;
-        }
-        cur = load(te - 1, true);
-        float Sn[CB];  // the state before the token being processed, a token ahead
-        {
-            const float4 *s = tok + ((size_t)(te - 1 - tb) * dk + ir) * (CB / 4);
+                    for (int j = 0; j < BB; ++j)
 #pragma unroll
-            for (int j = 0; j < CB / 4; ++j) {
-                const float4 f = s[j];
-                Sn[4 * j] = f.x; Sn[4 * j + 1] = f.y; Sn[4 * j + 2] = f.z; Sn[4 * j + 3] = f.w;
-            }
-        }
-        for (int t = te - 1; t >= tb; --t) {
-            const TokIn x = cur;
-            float M[CB];
-            const float alpha = row ? expf(x.g) : 0.f;
+                        for (int rr = 0; rr < RPL; ++rr) {
+                            const int r = l + 32 * rr;
+                            const bool in = j < nt && r < dk;
+                            const size_t ix = ((size_t)(tb + j) * H + h) * dk + r;
+                            gv_[j][rr] = in ? a.g[ix] : 0.f;
+                            kv_[j][rr] = in ? act_ld(k, ix) : 0.f;
+                        }
 #pragma unroll
-            for (int j = 0; j < CB; ++j) M[j] = row ? alpha * Sn[j] : 0.f;
-            if (t > tb) {  // prefetch token t - 1
-                cur = load(t - 1, true);
-                const float4 *s = tok + ((size_t)(t - 1 - tb) * dk + ir) * (CB / 4);
+                    for (int j = 0; j < BB; ++j)
 #pragma unroll
-                for (int j = 0; j < CB / 4; ++j) {
-                    const float4 f = s[j];
-                    Sn[4 * j] = f.x; Sn[4 * j + 1] = f.y; Sn[4 * j + 2] = f.z; Sn[4 * j + 3] = f.w;
+                        for (int rr = 0; rr < RPL; ++rr) gv_[j][rr] = expf(gv_[j][rr]);  // alpha
+                    float vv[BB], bv = 0.f;
+#pragma unroll
+                    for (int j = 0; j < BB; ++j) {
+                        const bool in = j < nt && c0 + l < dv;
+                        vv[j] = in ? act_ld(v, ((size_t)(tb + j) * H + h) * dv + c0 + l) : 0.f;
+                    }
+                    if (l < nt) bv = a.beta[(size_t)(tb + l) * H + h];
+#pragma unroll
+                    for (int j = 0; j < BB; ++j) {
+#pragma unroll
+                        for (int rr = 0; rr < RPL; ++rr) {
+                            rb[R_G + j * 128 + l + 32 * rr] = gv_[j][rr];
+                            act_st(rk, j * 128 + l + 32 * rr, kv_[j][rr]);
+                        }
+                        act_st(rv, j * CTC + l, vv[j]);
+                    }
+                    if (l < BB) rb[R_B + l] = bv;
+                    if (back) {  // the reverse walk also reads q and d_out
+#pragma unroll
+                        for (int j = 0; j < BB; ++j)
+#pragma unroll
+                            for (int rr = 0; rr < RPL; ++rr) {
+                                const int r = l + 32 * rr;
+                                const bool in = j < nt && r < dk;
+                                gv_[j][rr] =
+                                    in ? act_ld(q, ((size_t)(tb + j) * H + h) * dk + r) : 0.f;
+                            }
+#pragma unroll
+                        for (int j = 0; j < BB; ++j) {
+                            const bool in = j < nt && c0 + l < dv;
+                            vv[j] = in ? act_ld(dout, ((size_t)(tb + j) * H + h) * dv + c0 + l)
+                                       : 0.f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < BB; ++j) {
+#pragma unroll
+                            for (int rr = 0; rr < RPL; ++rr)
+                                act_st(rq, j * 128 + l + 32 * rr, gv_[j][rr]);
+                            act_st(rd, j * CTC + l, vv[j]);
+                        }
+                    }
                 }
             }
-            if (i < CB) {
-                vs[i] = x.vj;
-                dos[i] = x.dj;
-            }
-            __syncthreads();  // dos visible
-            float y[CB], z[CB];
-#pragma unroll
-            for (int j = 0; j < CB; ++j) {
-                dS[j] += x.qv * dos[j];  // the read at t
-                y[j] = M[j] * x.kv;
-                z[j] = dS[j] * x.kv;
-            }
-            part[0][wp][lane] = warp_colsum(y);
-            part[1][wp][lane] = warp_colsum(z);
-            __syncthreads();
-            if (i < 2 * CB) {
-                const int jj = i & (CB - 1), r = i >> 5;
-                float s = 0.f;
-#pragma unroll
-                for (int w = 0; w < BT / 32; ++w) s += part[r][w][jj];
-                col[r][jj] = r == 0 ? vs[jj] - s : s;  // u, w = dS^T k
-            }
-            __syncthreads();
-            float dqi = 0.f, dki = 0.f, dgi = 0.f;
-            const float bk = x.b * x.kv;
-#pragma unroll
-            for (int j = 0; j < CB; ++j) {
-                const float u = col[0][j], du = x.b * col[1][j];
-                dqi += (M[j] + bk * u) * dos[j];    // (S_t do)_i
-                dki += x.b * dS[j] * u - M[j] * du;  // (beta dS u - M du)_i
-                const float dM = dS[j] - x.kv * du;
-                dgi += dM * M[j];
-                dS[j] = alpha * dM;  // adjoint of the state before t
-            }
-            const size_t ix = ((size_t)t * H + h) * dk + i;
-            if (row) {
-                atomicAdd(a.gq + ix, dqi);
-                atomicAdd(a.gk + ix, dki);
-                atomicAdd(a.gg + ix, dgi);
-            }
-            if (i < nc) a.gv[((size_t)t * H + h) * dv + c0 + i] = x.b * col[1][i];
-            if (i == CB * 2) {
-                float db = 0.f;
-#pragma unroll
-                for (int j = 0; j < CB; ++j) db += col[1][j] * col[0][j];
-                atomicAdd(a.gbeta + (size_t)t * H + h, db);
-            }
-            __syncthreads();  // part, col, vs, dos are rewritten by the next token
+            mbar_arrive(full);
         }
+        return;
     }
-    if (a.gS0 && row) {
-        float *d = a.gS0 + ((size_t)unit * dk + i) * dv + c0;
+
+    // ------------------------------------------------------------------ consumers
+    const int cw = cb * NWC + wp;  // this warp's WC-column group
+    const int c0w = cw * WC;
+    const bool has_cols = cw < a.ncw;  // a warp past the last column keeps zeros only
+    float S[RPL][WC], dS[RPL][WC];
 #pragma unroll
-        for (int j = 0; j < CB; ++j)
-            if (j < nc) d[j] = dS[j];
+    for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+        for (int j = 0; j < WC; ++j) {
+            const int r = l + 32 * rr, c = c0w + j;
+            S[rr][j] = (a.S0 && r < dk && c < dv) ? a.S0[((size_t)unit * dk + r) * dv + c] : 0.f;
+            dS[rr][j] = (a.dSF && r < dk && c < dv) ? a.dSF[((size_t)unit * dk + r) * dv + c] : 0.f;
+        }
+    float4 *tokw = (float4 *)(sm + SM_TOK + wp * TOK_W);  // [BB][WC/4][128]
+    float *part = sm + SM_PART, *pb = sm + SM_PB;
+    auto blk_ptr = [&](int c, int rr) {
+        return (float4 *)(a.blk_states +
+                          ((((size_t)(blk_base + c) * H + h) * a.ncw + cw) * dk + l + 32 * rr) * WC);
+    };
+    auto put_tok = [&](int j) {
+#pragma unroll
+        for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+            for (int x = 0; x < WC / 4; ++x)
+                tokw[(j * (WC / 4) + x) * 128 + l + 32 * rr] =
+                    make_float4(S[rr][4 * x], S[rr][4 * x + 1], S[rr][4 * x + 2], S[rr][4 * x + 3]);
+    };
+    // one forward token step from ring slot j: S <- M + beta k u^T, M = Diag(alpha) S,
+    // u = v - M^T k
+    auto fstep = [&](const float *rb, int j) {
+        const TA *rk = (const TA *)(rb + R_K);
+        float kr[RPL], al[RPL];
+#pragma unroll
+        for (int rr = 0; rr < RPL; ++rr) {
+            kr[rr] = act_ld(rk, j * 128 + l + 32 * rr);
+            al[rr] = rb[R_G + j * 128 + l + 32 * rr];
+        }
+        // column pairs (jj, jj + 1) as packed fp32x2 operations
+        float p[WC];
+#pragma unroll
+        for (int jj = 0; jj < WC; ++jj) p[jj] = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+            for (int jj = 0; jj < WC; jj += 2) {
+                mul2_inplace(S[rr][jj], S[rr][jj + 1], make_float2(al[rr], al[rr]));
+                fma2_acc(p[jj], p[jj + 1], S[rr][jj], S[rr][jj + 1], kr[rr], kr[rr]);
+            }
+        const float um =
+            act_ld((const TA *)(rb + R_V), j * CTC + WC * wp + (l & (WC - 1))) - colsum(p);
+        const float b = rb[R_B + j];
+        float u[WC];
+#pragma unroll
+        for (int jj = 0; jj < WC; ++jj) u[jj] = b * __shfl_sync(0xffffffffu, um, jj);
+#pragma unroll
+        for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+            for (int jj = 0; jj < WC; jj += 2)
+                fma2_acc(S[rr][jj], S[rr][jj + 1], kr[rr], kr[rr], u[jj], u[jj + 1]);
+    };
+    bool ok = true;
+
+    // forward: the state at every block start
+    for (int f = 0; f < nblk; ++f) {
+        const int buf = f & 1;
+        ok = mbar_wait(bar0 + 8 * buf, (f >> 1) & 1, abort, kWaitLimit) && ok;
+        if (ok) {
+            const float *rb = sm + buf * R_SIZE;
+#pragma unroll
+            for (int rr = 0; rr < RPL; ++rr) {
+                if (!has_cols || l + 32 * rr >= dk) continue;
+                float4 *d = blk_ptr(f, rr);
+#pragma unroll
+                for (int x = 0; x < WC / 4; ++x)
+                    d[x] = make_float4(S[rr][4 * x], S[rr][4 * x + 1], S[rr][4 * x + 2],
+                                       S[rr][4 * x + 3]);
+            }
+            const int nt = min(BB, t_end - (t_begin + f * BB));
+            for (int j = 0; j < nt; ++j) fstep(rb, j);
+        }
+        mbar_arrive(bar0 + 16 + 8 * buf);
+    }
+    auto load_start = [&](int c) {
+#pragma unroll
+        for (int rr = 0; rr < RPL; ++rr) {
+            const bool in = has_cols && l + 32 * rr < dk;  // else the row stays zero
+            const float4 *s = blk_ptr(c, rr);
+#pragma unroll
+            for (int x = 0; x < WC / 4; ++x) {
+                const float4 v4 = in ? s[x] : make_float4(0.f, 0.f, 0.f, 0.f);
+                S[rr][4 * x] = v4.x; S[rr][4 * x + 1] = v4.y;
+                S[rr][4 * x + 2] = v4.z; S[rr][4 * x + 3] = v4.w;
+            }
+        }
+    };
+    if (nblk > 0 && ok) load_start(nblk - 1);
+
+    // reverse
+    for (int f = nblk; f < 2 * nblk; ++f) {
+        const int buf = f & 1, c = 2 * nblk - 1 - f;
+        const int tb = t_begin + c * BB, nt = min(BB, t_end - tb);
+        ok = mbar_wait(bar0 + 8 * buf, (f >> 1) & 1, abort, kWaitLimit) && ok;
+        if (ok) {
+            const float *rb = sm + buf * R_SIZE;
+            for (int j = 0; j < nt; ++j) {  // the block's pre-token states
+                put_tok(j);
+                fstep(rb, j);
+            }
+            if (c > 0) load_start(c - 1);  // lands while this block is walked
+            for (int j = nt - 1; j >= 0; --j) {
+                float kr[RPL], qr[RPL], al[RPL];
+#pragma unroll
+                for (int rr = 0; rr < RPL; ++rr) {
+                    kr[rr] = act_ld((const TA *)(rb + R_K), j * 128 + l + 32 * rr);
+                    qr[rr] = act_ld((const TA *)(rb + R_Q), j * 128 + l + 32 * rr);
+                    al[rr] = rb[R_G + j * 128 + l + 32 * rr];
+                }
+                float dov[WC];
+                loadW((const TA *)(rb + R_D) + j * CTC + WC * wp, dov);
+                float M[RPL][WC];
+#pragma unroll
+                for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+                    for (int x = 0; x < WC / 4; ++x) {
+                        const float4 s4 = tokw[(j * (WC / 4) + x) * 128 + l + 32 * rr];
+                        M[rr][4 * x] = s4.x;
+                        M[rr][4 * x + 1] = s4.y;
+                        M[rr][4 * x + 2] = s4.z;
+                        M[rr][4 * x + 3] = s4.w;
+                    }
+                // column pairs (jj, jj + 1) as packed fp32x2 operations
+                float pu[WC], pw[WC];
+#pragma unroll
+                for (int jj = 0; jj < WC; ++jj) {
+                    pu[jj] = 0.f;
+                    pw[jj] = 0.f;
+                }
+#pragma unroll
+                for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+                    for (int jj = 0; jj < WC; jj += 2) {
+                        mul2_inplace(M[rr][jj], M[rr][jj + 1], make_float2(al[rr], al[rr]));
+                        // the read at t
+                        fma2_acc(dS[rr][jj], dS[rr][jj + 1], qr[rr], qr[rr], dov[jj], dov[jj + 1]);
+                        fma2_acc(pu[jj], pu[jj + 1], M[rr][jj], M[rr][jj + 1], kr[rr], kr[rr]);
+                        fma2_acc(pw[jj], pw[jj + 1], dS[rr][jj], dS[rr][jj + 1], kr[rr], kr[rr]);
+                    }
+                const float um = act_ld((const TA *)(rb + R_V), j * CTC + WC * wp + (l & (WC - 1))) -
+                                 colsum(pu);
+                const float wm = colsum(pw);  // (dS^T k) of column l % WC
+                const float b = rb[R_B + j];
+                const int t = tb + j;
+                if (l < WC && c0w + l < dv) a.gv[((size_t)t * H + h) * dv + c0w + l] = b * wm;
+                float bu[WC], ndu[WC], db = 0.f;  // beta u, -beta w
+#pragma unroll
+                for (int jj = 0; jj < WC; ++jj) {
+                    const float u = __shfl_sync(0xffffffffu, um, jj);
+                    const float w = __shfl_sync(0xffffffffu, wm, jj);
+                    bu[jj] = b * u;
+                    ndu[jj] = -b * w;
+                    db = fmaf(w, u, db);
+                }
+                // per row, even and odd columns summed apart and added at the end
+                float dq[RPL][2], dkr[RPL][2], dg[RPL][2];
+#pragma unroll
+                for (int rr = 0; rr < RPL; ++rr) {
+                    dq[rr][0] = dq[rr][1] = dkr[rr][0] = dkr[rr][1] = dg[rr][0] = dg[rr][1] = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < WC; jj += 2) {
+                        float s0 = M[rr][jj], s1 = M[rr][jj + 1];  // S_t = M + k (beta u)^T
+                        fma2_acc(s0, s1, kr[rr], kr[rr], bu[jj], bu[jj + 1]);
+                        fma2_acc(dq[rr][0], dq[rr][1], s0, s1, dov[jj], dov[jj + 1]);
+                        // dk: beta dS u - M du
+                        fma2_acc(dkr[rr][0], dkr[rr][1], M[rr][jj], M[rr][jj + 1], ndu[jj],
+                                 ndu[jj + 1]);
+                        fma2_acc(dkr[rr][0], dkr[rr][1], dS[rr][jj], dS[rr][jj + 1], bu[jj],
+                                 bu[jj + 1]);
+                        // dM = dS - k du^T, dg += dM o M, dS_prev = Diag(alpha) dM
+                        fma2_acc(dS[rr][jj], dS[rr][jj + 1], kr[rr], kr[rr], ndu[jj], ndu[jj + 1]);
+                        fma2_acc(dg[rr][0], dg[rr][1], dS[rr][jj], dS[rr][jj + 1], M[rr][jj],
+                                 M[rr][jj + 1]);
+                        mul2_inplace(dS[rr][jj], dS[rr][jj + 1], make_float2(al[rr], al[rr]));
+                    }
+                }
+                float *pp = part + (wp * BB + j) * 3 * 128;
+#pragma unroll
+                for (int rr = 0; rr < RPL; ++rr) {
+                    pp[l + 32 * rr] = dq[rr][0] + dq[rr][1];
+                    pp[128 + l + 32 * rr] = dkr[rr][0] + dkr[rr][1];
+                    pp[256 + l + 32 * rr] = dg[rr][0] + dg[rr][1];
+                }
+                if (l == 0) pb[wp * BB + j] = db;
+            }
+        }
+        mbar_arrive(bar0 + 16 + 8 * buf);
+        // the consumer warps' row sums of this block, accumulated over column blocks
+        const bool bad = named_bar_or(1, 32 * NWC, !ok);
+        if (!bad) {
+            const int x = threadIdx.x;  // row (32 * NWC = 128 consumer threads)
+            if (x < dk) {
+                for (int j = 0; j < nt; ++j) {
+                    const size_t ix = ((size_t)(tb + j) * H + h) * dk + x;
+                    float sq = 0.f, sk = 0.f, sg = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NWC; ++w) {
+                        const float *pp = part + (w * BB + j) * 3 * 128;
+                        sq += pp[x];
+                        sk += pp[128 + x];
+                        sg += pp[256 + x];
+                    }
+                    atomicAdd(a.gq + ix, sq);
+                    atomicAdd(a.gk + ix, sk);
+                    atomicAdd(a.gg + ix, sg);
+                }
+            }
+            if (x < nt) {
+                float sb = 0.f;
+#pragma unroll
+                for (int w = 0; w < NWC; ++w) sb += pb[w * BB + x];
+                atomicAdd(a.gbeta + (size_t)(tb + x) * H + h, sb);
+            }
+        }
+        named_bar_sync(1, 32 * NWC);  // the partials are rewritten by the next block
+        ok = ok && !bad;
+    }
+    if (!ok) {
+        dev_fail(a.dev_status, KDA_ERR_TIMEOUT);
+        return;
+    }
+    if (a.gS0) {
+#pragma unroll
+        for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+            for (int j = 0; j < WC; ++j) {
+                const int r = l + 32 * rr, c = c0w + j;
+                if (r < dk && c < dv) a.gS0[((size_t)unit * dk + r) * dv + c] = dS[rr][j];
+            }
     }
 }
 
 }  // namespace
 
 size_t backward_workspace_bytes(int N, int T_tot, int H, int dk, int dv) {
-    const size_t blocks = (size_t)T_tot / BC + N;  // >= sum_n ceil(len_n / 16)
-    const int ncb = (dv + CB - 1) / CB;
-    const size_t a = ((blocks * H * dk * dv * sizeof(float)) + 255) & ~(size_t)255;
-    const size_t b = (size_t)N * H * ncb * BC * dk * CB * sizeof(float);
-    return a + b;
+    const size_t blocks = (size_t)T_tot / BB + N;  // >= sum_n ceil(len_n / 8)
+    const int ncw = (dv + WC - 1) / WC;
+    return blocks * H * ncw * dk * WC * sizeof(float);
 }
 
 cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float *dSF, float *dq,
@@ -287,11 +519,14 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
     a.gq = dq; a.gk = dk; a.gv = dv; a.gg = dg; a.gbeta = dbeta; a.gS0 = dS0;
     a.dev_status = p.dev_status;
     a.N = p.N; a.T_tot = p.T_tot; a.H = p.H; a.dk = p.dk; a.dv = p.dv; a.act = p.act;
-    a.ncb = (p.dv + CB - 1) / CB;
-    const size_t blocks = (size_t)p.T_tot / BC + p.N;
+    a.ncw = (p.dv + WC - 1) / WC;
     a.blk_states = (float *)workspace;
-    a.tok_states = (float *)((uint8_t *)workspace +
-                             (((blocks * p.H * p.dk * p.dv * sizeof(float)) + 255) & ~(size_t)255));
+    {
+        const int es = p.act == KDA_DTYPE_F32 ? 4 : 2;
+        auto al16 = [](const void *x) { return ((uintptr_t)x & 15u) == 0; };
+        a.bulk = al16(p.q) && al16(p.k) && al16(p.v) && al16(dout) && al16(p.g) &&
+                 (p.dk * es) % 16 == 0 && (p.dk * 4) % 16 == 0 && (p.dv * es) % 16 == 0;
+    }
     const size_t Tn = (size_t)p.T_tot * p.H;
     cudaError_t e;
     // the row sums are accumulated by every column block: start from zero
@@ -300,9 +535,17 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
     if ((e = cudaMemsetAsync(dg, 0, Tn * p.dk * sizeof(float), st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dbeta, 0, Tn * sizeof(float), st)) != cudaSuccess) return e;
     if (p.N == 0 || p.H == 0) return cudaSuccess;
-    dim3 grid((unsigned)(p.N * p.H), (unsigned)a.ncb);
-    if (p.act == KDA_DTYPE_F32) backward_kernel<float><<<grid, BT, 0, st>>>(a);
-    else backward_kernel<__nv_bfloat16><<<grid, BT, 0, st>>>(a);
+    dim3 grid((unsigned)(p.N * p.H), (unsigned)((p.dv + CTC - 1) / CTC));
+    if (p.act == KDA_DTYPE_F32) {
+        if ((e = set_max_dynamic_smem((const void *)backward_kernel<float>, (int)BWD_SMEM)) != cudaSuccess)
+            return e;
+        backward_kernel<float><<<grid, BT, BWD_SMEM, st>>>(a);
+    } else {
+        if ((e = set_max_dynamic_smem((const void *)backward_kernel<__nv_bfloat16>, (int)BWD_SMEM)) !=
+            cudaSuccess)
+            return e;
+        backward_kernel<__nv_bfloat16><<<grid, BT, BWD_SMEM, st>>>(a);
+    }
     return cudaGetLastError();
 }
 

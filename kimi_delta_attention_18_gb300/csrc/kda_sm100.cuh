@@ -65,6 +65,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Raise the transaction count the current phase waits for by `bytes` (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- bulk copy
 // Global -> shared bulk copy (the TMA engine's non-tensor form); completion is
 // counted in bytes on `bar`.  dst, src 16-byte aligned, bytes a multiple of 16.
@@ -284,6 +290,15 @@ __device__ __forceinline__ void mul2_inplace(float &x, float &y, float2 d) {
         "mul.rn.f32x2 a, a, b;\n\tmov.b64 {%0, %1}, a;\n\t}"
         : "+f"(x), "+f"(y)
         : "f"(d.x), "f"(d.y));
+}
+// (x, y) += (ax, ay) * (bx, by) as one packed fp32x2 fused multiply-add (the
+// same result as two scalar fmaf).
+__device__ __forceinline__ void fma2_acc(float &x, float &y, float ax, float ay, float bx,
+                                         float by) {
+    asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%0, %1};\n\tfma.rn.f32x2 c, a, b, c;\n\tmov.b64 {%0, %1}, c;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "f"(ax), "f"(ay), "f"(bx), "f"(by));
 }
 // C(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,

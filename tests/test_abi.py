@@ -211,13 +211,9 @@ def test_backward_host_checks():
 
     d = _desc()
     need = L.kda_prefill_backward_workspace_size(ctypes.byref(d))
-    # block-start states [T/16 + N blocks][H][dk][dv] (256-rounded) + one block of
-    # token states [16][dk][32 columns] per (sequence, head, column block)
-    r256 = lambda b: (b + 255) // 256 * 256
-    blocks = d.total_tokens // 16 + d.num_seqs
-    ncb = (d.dv + 31) // 32
-    assert need == r256(blocks * d.num_heads * d.dk * d.dv * 4) + \
-        d.num_seqs * d.num_heads * ncb * 16 * d.dk * 32 * 4
+    # the state at every 8-token block start: [T/8 + N blocks][H][ceil(dv/8)][dk][8] fp32
+    blocks = d.total_tokens // 8 + d.num_seqs
+    assert need == blocks * d.num_heads * ((d.dv + 7) // 8) * d.dk * 8 * 4
     assert L.kda_prefill_backward_workspace_size(ctypes.byref(_desc(chunk=32))) == 0
     assert call(d) == WORKSPACE
     assert call(d, ws=0x40000, ws_len=need - 1) == WORKSPACE
