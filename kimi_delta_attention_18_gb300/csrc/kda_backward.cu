@@ -41,24 +41,27 @@ constexpr int WC = 8;             // state columns per consumer warp
 constexpr int NWC = 4;            // consumer warps (one per SM sub-partition)
 constexpr int CTC = WC * NWC;     // columns per CTA
 constexpr int RPL = 4;            // rows per lane: dk <= 128
+constexpr int NBUF = 3;           // ring slots (blocks staged ahead)
 constexpr int BT = 32 * (NWC + 1);
 constexpr long long kWaitLimit = 4000000000ll;  // ~2 s of SM clocks
 
-// shared memory (floats): ring [2] of {alpha = e^g [BB][128] fp32; k, q [BB][128] and v,
+// shared memory (floats): ring [NBUF] of {alpha = e^g [BB][128] fp32; k, q [BB][128] and v,
 // d_out [BB][CTC] in the activation dtype (regions sized for fp32); beta [BB]};
 // token states [NWC][BB][WC/4][128] float4; each consumer warp's row sums
-// [NWC][BB][3][128] and dbeta [NWC][BB] of the block; then the mbarriers and
-// the abort flag.
+// [NWC][BB][3][128] and dbeta [NWC][BB] of the block; u = v - M^T k of every
+// token of the block [NWC][BB][WC]; then the mbarriers and the abort flag.
 constexpr int R_G = 0, R_K = BB * 128, R_Q = 2 * BB * 128, R_V = 3 * BB * 128,
               R_D = R_V + BB * CTC, R_B = R_D + BB * CTC, R_SIZE = 3600;
-constexpr int SM_TOK = 2 * R_SIZE;
+constexpr int SM_TOK = NBUF * R_SIZE;
 constexpr int TOK_W = BB * 128 * WC;
 constexpr int SM_PART = SM_TOK + NWC * TOK_W;
 constexpr int SM_PB = SM_PART + NWC * BB * 3 * 128;
-constexpr int SM_BAR = SM_PB + NWC * BB;  // 6 mbarriers (12 floats), then the flag
-constexpr size_t BWD_SMEM = (size_t)(SM_BAR + 12 + 4) * sizeof(float);
+constexpr int SM_U = SM_PB + NWC * BB;
+constexpr int SM_BAR = SM_U + NWC * BB * WC;  // 9 mbarriers (18 floats), then the flag
+constexpr size_t BWD_SMEM = (size_t)(SM_BAR + 18 + 4) * sizeof(float);
 static_assert(R_B + BB <= R_SIZE && (R_SIZE % 4) == 0 && (R_D % 4) == 0, "ring layout");
-static_assert((SM_BAR % 2) == 0 && (SM_TOK % 4) == 0, "alignment");
+static_assert((SM_BAR % 2) == 0 && (SM_TOK % 4) == 0 && (SM_U % 4) == 0, "alignment");
+static_assert(BWD_SMEM <= 227 * 1024, "shared memory");
 static_assert(WC % 4 == 0 && 32 % WC == 0, "columns per warp");
 
 struct BwdArgs {
@@ -133,18 +136,22 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
         blk_base += (lm + BB - 1) / BB;
     }
     const int nblk = (t_end - t_begin + BB - 1) / BB;
-    // full[2] (ring slot ready), empty[2] (slot consumed), landed[2] (bulk copies in)
+    // full[NBUF] (ring slot ready), empty[NBUF] (slot consumed), landed[NBUF]
+    // (bulk copies in)
     const uint32_t bar0 = smem_addr(sm + SM_BAR);
-    volatile int *abort = (volatile int *)(sm + SM_BAR + 12);
+    auto bar_full = [&](int b) { return bar0 + 8 * b; };
+    auto bar_empty = [&](int b) { return bar0 + 8 * (NBUF + b); };
+    auto bar_landed = [&](int b) { return bar0 + 8 * (2 * NBUF + b); };
+    volatile int *abort = (volatile int *)(sm + SM_BAR + 18);
     // padded rows (past dk) and columns (past dv) of the ring stay zero: the
     // producer writes only the real ones
-    for (int e = threadIdx.x; e < 2 * R_SIZE; e += BT) sm[e] = 0.f;
+    for (int e = threadIdx.x; e < NBUF * R_SIZE; e += BT) sm[e] = 0.f;
     fence_async_smem();  // before the bulk copies overwrite these bytes
     if (threadIdx.x == 0) {
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar0 + 8 * b, 32);                // producer lanes
-            mbar_init(bar0 + 16 + 8 * b, 32 * NWC);     // consumer threads
-            mbar_init(bar0 + 32 + 8 * b, 1);            // bulk bytes
+        for (int b = 0; b < NBUF; ++b) {
+            mbar_init(bar_full(b), 32);          // producer lanes
+            mbar_init(bar_empty(b), 32 * NWC);   // consumer threads
+            mbar_init(bar_landed(b), 1);         // bulk bytes
         }
         *abort = 0;
         mbar_fence_init();
@@ -156,19 +163,22 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
     if (wp == NWC) {  // ---------------------------------------------- producer
         const TA *q = (const TA *)a.q, *k = (const TA *)a.k, *v = (const TA *)a.v;
         const TA *dout = (const TA *)a.dout;
-        for (int f = 0; f < 2 * nblk; ++f) {
-            const int buf = f & 1, use = f >> 1;
+        // issue(f) stages block visit f into slot f % NBUF (bulk copies in flight,
+        // or plain loads done); finish(f) waits for the copies, turns g into
+        // alpha and releases the slot.  Visit f + 1 is issued before f finishes.
+        bool pok = true;
+        auto issue = [&](int f) {
+            const int buf = f % NBUF, use = f / NBUF;
             const bool back = f >= nblk;
-            bool ok = true;
-            if (use >= 1) ok = mbar_wait(bar0 + 16 + 8 * buf, (use - 1) & 1, abort, kWaitLimit);
-            const uint32_t full = bar0 + 8 * buf;
-            if (ok) {
+            if (use >= 1) pok = mbar_wait(bar_empty(buf), (use - 1) & 1, abort, kWaitLimit) && pok;
+            if (!pok) return;
+            {
                 float *rb = sm + buf * R_SIZE;
                 TA *rk = (TA *)(rb + R_K), *rq = (TA *)(rb + R_Q);
                 TA *rv = (TA *)(rb + R_V), *rd = (TA *)(rb + R_D);
                 const int tb = t_begin + block_of(f) * BB, nt = min(BB, t_end - tb);
                 if (a.bulk) {  // one bulk copy per token row, counted in bytes on `landed`
-                    const uint32_t landed = bar0 + 32 + 8 * buf;
+                    const uint32_t landed = bar_landed(buf);
                     const int nvc = min(CTC, dv - c0);
                     const uint32_t es = sizeof(TA);
                     const uint32_t per_tok =
@@ -187,16 +197,6 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                                      landed);
                         }
                         rb[R_B + l] = a.beta[row];
-                    }
-                    // alpha = e^g in place, once for all consumer warps and visits
-                    if (mbar_wait(landed, use & 1, abort, kWaitLimit)) {
-#pragma unroll
-                        for (int j = 0; j < BB; ++j)
-#pragma unroll
-                            for (int rr = 0; rr < RPL; ++rr)
-                                if (j < nt && l + 32 * rr < dk)
-                                    rb[R_G + j * 128 + l + 32 * rr] =
-                                        expf(rb[R_G + j * 128 + l + 32 * rr]);
                     }
                 } else {  // plain loads, a block's worth in flight
                     float gv_[BB][RPL], kv_[BB][RPL];
@@ -257,7 +257,29 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                     }
                 }
             }
-            mbar_arrive(full);
+        };
+        auto finish = [&](int f) {
+            const int buf = f % NBUF, use = f / NBUF;
+            if (pok && a.bulk) {
+                // alpha = e^g in place, once for all consumer warps and visits
+                pok = mbar_wait(bar_landed(buf), use & 1, abort, kWaitLimit);
+                if (pok) {
+                    float *rb = sm + buf * R_SIZE;
+                    const int tb = t_begin + block_of(f) * BB, nt = min(BB, t_end - tb);
+#pragma unroll
+                    for (int j = 0; j < BB; ++j)
+#pragma unroll
+                        for (int rr = 0; rr < RPL; ++rr)
+                            if (j < nt && l + 32 * rr < dk)
+                                rb[R_G + j * 128 + l + 32 * rr] = expf(rb[R_G + j * 128 + l + 32 * rr]);
+                }
+            }
+            mbar_arrive(bar_full(buf));
+        };
+        if (nblk > 0) issue(0);
+        for (int f = 0; f < 2 * nblk; ++f) {
+            if (f + 1 < 2 * nblk) issue(f + 1);
+            finish(f);
         }
         return;
     }
@@ -277,6 +299,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
         }
     float4 *tokw = (float4 *)(sm + SM_TOK + wp * TOK_W);  // [BB][WC/4][128]
     float *part = sm + SM_PART, *pb = sm + SM_PB;
+    float *us = sm + SM_U + wp * BB * WC;  // [BB][WC]: u of the block's tokens
     auto blk_ptr = [&](int c, int rr) {
         return (float4 *)(a.blk_states +
                           ((((size_t)(blk_base + c) * H + h) * a.ncw + cw) * dk + l + 32 * rr) * WC);
@@ -291,7 +314,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
     };
     // one forward token step from ring slot j: S <- M + beta k u^T, M = Diag(alpha) S,
     // u = v - M^T k
-    auto fstep = [&](const float *rb, int j) {
+    auto fstep = [&](const float *rb, int j, bool keep_u) {
         const TA *rk = (const TA *)(rb + R_K);
         float kr[RPL], al[RPL];
 #pragma unroll
@@ -312,6 +335,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
             }
         const float um =
             act_ld((const TA *)(rb + R_V), j * CTC + WC * wp + (l & (WC - 1))) - colsum(p);
+        if (keep_u && l < WC) us[j * WC + l] = um;
         const float b = rb[R_B + j];
         float u[WC];
 #pragma unroll
@@ -326,8 +350,8 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
 
     // forward: the state at every block start
     for (int f = 0; f < nblk; ++f) {
-        const int buf = f & 1;
-        ok = mbar_wait(bar0 + 8 * buf, (f >> 1) & 1, abort, kWaitLimit) && ok;
+        const int buf = f % NBUF;
+        ok = mbar_wait(bar_full(buf), (f / NBUF) & 1, abort, kWaitLimit) && ok;
         if (ok) {
             const float *rb = sm + buf * R_SIZE;
 #pragma unroll
@@ -340,9 +364,9 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                                        S[rr][4 * x + 3]);
             }
             const int nt = min(BB, t_end - (t_begin + f * BB));
-            for (int j = 0; j < nt; ++j) fstep(rb, j);
+            for (int j = 0; j < nt; ++j) fstep(rb, j, false);
         }
-        mbar_arrive(bar0 + 16 + 8 * buf);
+        mbar_arrive(bar_empty(buf));
     }
     auto load_start = [&](int c) {
 #pragma unroll
@@ -361,15 +385,16 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
 
     // reverse
     for (int f = nblk; f < 2 * nblk; ++f) {
-        const int buf = f & 1, c = 2 * nblk - 1 - f;
+        const int buf = f % NBUF, c = 2 * nblk - 1 - f;
         const int tb = t_begin + c * BB, nt = min(BB, t_end - tb);
-        ok = mbar_wait(bar0 + 8 * buf, (f >> 1) & 1, abort, kWaitLimit) && ok;
+        ok = mbar_wait(bar_full(buf), (f / NBUF) & 1, abort, kWaitLimit) && ok;
         if (ok) {
             const float *rb = sm + buf * R_SIZE;
             for (int j = 0; j < nt; ++j) {  // the block's pre-token states
                 put_tok(j);
-                fstep(rb, j);
+                fstep(rb, j, true);
             }
+            __syncwarp();  // u of lanes 0 .. WC-1 visible to the whole warp
             if (c > 0) load_start(c - 1);  // lands while this block is walked
             for (int j = nt - 1; j >= 0; --j) {
                 float kr[RPL], qr[RPL], al[RPL];
@@ -393,36 +418,31 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                         M[rr][4 * x + 3] = s4.w;
                     }
                 // column pairs (jj, jj + 1) as packed fp32x2 operations
-                float pu[WC], pw[WC];
+                float pw[WC];
 #pragma unroll
-                for (int jj = 0; jj < WC; ++jj) {
-                    pu[jj] = 0.f;
-                    pw[jj] = 0.f;
-                }
+                for (int jj = 0; jj < WC; ++jj) pw[jj] = 0.f;
 #pragma unroll
                 for (int rr = 0; rr < RPL; ++rr)
 #pragma unroll
                     for (int jj = 0; jj < WC; jj += 2) {
-                        mul2_inplace(M[rr][jj], M[rr][jj + 1], make_float2(al[rr], al[rr]));
                         // the read at t
                         fma2_acc(dS[rr][jj], dS[rr][jj + 1], qr[rr], qr[rr], dov[jj], dov[jj + 1]);
-                        fma2_acc(pu[jj], pu[jj + 1], M[rr][jj], M[rr][jj + 1], kr[rr], kr[rr]);
                         fma2_acc(pw[jj], pw[jj + 1], dS[rr][jj], dS[rr][jj + 1], kr[rr], kr[rr]);
+                        mul2_inplace(M[rr][jj], M[rr][jj + 1], make_float2(al[rr], al[rr]));
                     }
-                const float um = act_ld((const TA *)(rb + R_V), j * CTC + WC * wp + (l & (WC - 1))) -
-                                 colsum(pu);
                 const float wm = colsum(pw);  // (dS^T k) of column l % WC
                 const float b = rb[R_B + j];
                 const int t = tb + j;
                 if (l < WC && c0w + l < dv) a.gv[((size_t)t * H + h) * dv + c0w + l] = b * wm;
+                float uj[WC];  // u = v - M^T k, kept by the recompute
+                loadW(us + j * WC, uj);
                 float bu[WC], ndu[WC], db = 0.f;  // beta u, -beta w
 #pragma unroll
                 for (int jj = 0; jj < WC; ++jj) {
-                    const float u = __shfl_sync(0xffffffffu, um, jj);
                     const float w = __shfl_sync(0xffffffffu, wm, jj);
-                    bu[jj] = b * u;
+                    bu[jj] = b * uj[jj];
                     ndu[jj] = -b * w;
-                    db = fmaf(w, u, db);
+                    db = fmaf(w, uj[jj], db);
                 }
                 // per row, even and odd columns summed apart and added at the end
                 float dq[RPL][2], dkr[RPL][2], dg[RPL][2];
@@ -456,7 +476,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                 if (l == 0) pb[wp * BB + j] = db;
             }
         }
-        mbar_arrive(bar0 + 16 + 8 * buf);
+        mbar_arrive(bar_empty(buf));
         // the consumer warps' row sums of this block, accumulated over column blocks
         const bool bad = named_bar_or(1, 32 * NWC, !ok);
         if (!bad) {
