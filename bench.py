@@ -36,6 +36,9 @@ sys.path.insert(0, ROOT)
 PREFILL = "kda_prefill_bf16_h8_t4096_d128"
 DECODE = "kda_decode_b256_h56_d128_x64"
 METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of roofline"
+# fp32 FMA peak of a GB300 at its maximum SM clock (no measured figure exists for
+# CUDA-core fp32): 152 SMs x 128 lanes x 2 flops x 2.07 GHz
+BWD_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_ckpt_h8_t4096",
                  "backward_h8_t1024")
 
@@ -471,9 +474,19 @@ def run_backward(args, kda, x, flush, stream, dev, dist):
         e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dist, dev) / steps
+    # algorithmic work per head-token and state element: the forward step (decay 1,
+    # M^T k 2, rank-1 update 2) and its adjoint (read 2, dS^T k 2, S_t do 2,
+    # dk 4, dM 2, dg 2, decay 1) = 20 flops; fp32 on CUDA cores
+    flops = 20.0 * dk * dv * T * H
+    peak = BWD_FP32_TFLOPS
+    achieved = flops / (ms * 1e-3) / 1e12
     return {"what": "dq, dk, dv, dg, dbeta, dS0 (fp32), token-level SIMT kernel",
             "ms_per_step": round(ms, 4), "tokens_per_s": round(N and T / (ms * 1e-3), 1),
-            "ctas": N * H * ((dv + 31) // 32)}
+            "ctas": N * H * ((dv + 31) // 32),
+            "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "flops_per_head_token": 20 * dk * dv,
+                         "peak_from": "152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz"}}
 
 
 def run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world):
