@@ -55,6 +55,9 @@ def _oracle(x, d_out, d_sf, heads=None):
     ("f32", 16, 16, [64], False),
     ("bf16", 128, 128, [70, 33], True),
     ("bf16", 128, 96, [47, 90], False),
+    # rows that are not whole 16-byte units: the producer's plain-load path
+    ("f32", 30, 20, [45, 19], True),
+    ("bf16", 60, 44, [33, 70], False),
 ])
 def test_backward_matches_oracle(act, dk, dv, lengths, slow):
     H = 2
@@ -106,3 +109,27 @@ def test_backward_bench_size_sampled_heads_and_linearity():
     g2 = _run(x, (d1.float() * 2).to(d1.dtype), s1 * 2)
     for name, a, b in zip(NAMES, got, g2):
         assert rel_err(_np(b), 2 * _np(a)) <= 1e-5, name
+
+
+def test_backward_unaligned_inputs_take_the_plain_path():
+    """Inputs one fp32 element past a 16-byte boundary (the entry point needs 4-byte
+    alignment only): same gradients as the oracle."""
+    lengths = [37, 52]
+    H, d = 2, 32
+    x = make_prefill_inputs(lengths, H, d, d, "f32", s0_std=1.0, seed=39, slow_decay=True)
+    d_out, d_sf = make_backward_adjoints(sum(lengths), 2, H, d, d, "f32", seed=40)
+
+    def shifted(t):  # the same values at a device address 4 bytes past 16-byte alignment
+        buf = torch.empty(t.numel() + 4, dtype=t.dtype, device="cuda")
+        view = buf[1:1 + t.numel()].view(t.shape)
+        view.copy_(t.cuda())
+        assert view.data_ptr() % 16 == 4
+        return view
+
+    got = kda.prefill_backward(shifted(x["q"]), shifted(x["k"]), shifted(x["v"]), shifted(x["g"]),
+                               x["beta"].cuda(), x["S0"].cuda(), x["cu_seqlens"].cuda(),
+                               shifted(d_out), d_sf.cuda())
+    torch.cuda.synchronize()
+    ref = _oracle(x, d_out, d_sf)
+    for name, a, b in zip(NAMES, got, ref):
+        assert rel_err(_np(a), b) <= TOL, name
