@@ -308,10 +308,12 @@ def prefill_backward_workspace_size(desc) -> int:
 
 
 def prefill_backward(q, k, v, g, beta, S0, cu_seqlens, d_out, d_S_final=None, *,
-                     want_dS0=True, workspace=None, dev_status=None, stream=None):
+                     want_dS0=True, num_segments=0, workspace=None, dev_status=None,
+                     stream=None):
     """Gradients of <d_out, o> + <d_S_final, S_final> for the prefill of the same
     inputs (see kda_prefill_backward in kda.h).  d_out ``[T, H, dv]`` in the
-    activation dtype, d_S_final ``[N, H, dk, dv]`` fp32 or None.  Returns fp32
+    activation dtype, d_S_final ``[N, H, dk, dv]`` fp32 or None; num_segments
+    splits each sequence (0: the library's choice).  Returns fp32
     ``(dq, dk, dv, dg, dbeta, dS0)`` (dS0 None unless want_dS0)."""
     dev = q.device
     T, H, dk = q.shape
@@ -340,7 +342,7 @@ def prefill_backward(q, k, v, g, beta, S0, cu_seqlens, d_out, d_S_final=None, *,
     dg = torch.empty((T, H, dk), **f32)
     dbeta = torch.empty((T, H), **f32)
     dS0 = torch.empty((N, H, dk, dv), **f32) if want_dS0 else None
-    desc = _desc(N, T, H, dk, dv, act, 0)
+    desc = _desc(N, T, H, dk, dv, act, num_segments)
     ws_bytes = prefill_backward_workspace_size(desc)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)

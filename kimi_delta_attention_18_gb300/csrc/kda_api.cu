@@ -85,6 +85,23 @@ int choose_segments(const kda_prefill_desc_t *d) {
     return best_s;
 }
 
+// Segments per sequence of the backward pass (desc->num_segments, or the
+// library's choice for 0).  Every (sequence, head, 32 value columns) unit of the
+// backward is a token-sequential chain; with fewer units than SMs the sequences
+// are split (at least ~256 tokens per segment on average, at most 64 segments).
+int backward_segments(const kda_prefill_desc_t *d) {
+    if (d->num_segments > 0) return d->num_segments < 64 ? d->num_segments : 64;
+    const long long units = (long long)d->num_seqs * d->num_heads * ((d->dv + 31) / 32);
+    const int sms = sm_count();
+    if (units <= 0 || units >= sms) return 1;
+    long long sg = sms / units;
+    const long long per_seq = d->num_seqs > 0 ? d->total_tokens / d->num_seqs : 0;
+    const long long cap = per_seq / 256 > 1 ? per_seq / 256 : 1;
+    if (sg > cap) sg = cap;
+    if (sg > 64) sg = 64;
+    return sg < 1 ? 1 : (int)sg;
+}
+
 size_t act_bytes(const kda_prefill_desc_t *d) { return d->act_dtype == KDA_DTYPE_BF16 ? 2 : 4; }
 
 // Split workspace: transfer matrices, zero-initial states and start states for
@@ -302,7 +319,7 @@ kda_status_t kda_prefill_chunked_ckpt(const kda_prefill_desc_t *desc, const void
 size_t kda_prefill_backward_workspace_size(const kda_prefill_desc_t *desc) {
     if (check_desc(desc) != KDA_OK) return 0;
     return backward_workspace_bytes(desc->num_seqs, desc->total_tokens, desc->num_heads, desc->dk,
-                                    desc->dv);
+                                    desc->dv, backward_segments(desc));
 }
 
 kda_status_t kda_prefill_backward(const kda_prefill_desc_t *desc, const void *q, const void *k,
@@ -322,14 +339,15 @@ kda_status_t kda_prefill_backward(const kda_prefill_desc_t *desc, const void *q,
                           dq, dk, dv, dg, dbeta, dS0};
     for (const void *p : ptrs)
         if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
+    const int Sg = backward_segments(desc);
     const size_t need = backward_workspace_bytes(desc->num_seqs, desc->total_tokens,
-                                                 desc->num_heads, desc->dk, desc->dv);
+                                                 desc->num_heads, desc->dk, desc->dv, Sg);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
     PrefillArgs a = base_args(desc);
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0; a.cu = cu_seqlens;
     a.dev_status = dev_status;
-    return from_cuda(launch_backward(a, d_out, d_S_final, dq, dk, dv, dg, dbeta, dS0, workspace,
-                                     (cudaStream_t)stream));
+    return from_cuda(launch_backward(a, d_out, d_S_final, dq, dk, dv, dg, dbeta, dS0, Sg,
+                                     workspace, (cudaStream_t)stream));
 }
 
 kda_status_t kda_prefill_segments(const kda_prefill_desc_t *desc, int32_t seg_begin,

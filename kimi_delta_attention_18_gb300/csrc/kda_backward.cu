@@ -28,6 +28,8 @@
 // memory once per block and added to zeroed fp32 outputs with global atomics
 // (one per column block).  fp32 throughout: a token-level
 // implementation (the chunked tensor-core form of the backward is not built).
+#include <string.h>
+
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -73,7 +75,19 @@ struct BwdArgs {
     int32_t *dev_status;
     int N, T_tot, H, dk, dv, ncw, act;
     int bulk;  // rows and column slices meet the bulk-copy rules (16-byte aligned)
+    // Segments (Sg > 1): the main pass runs segment s from its start state X and
+    // its end adjoint Y ([N][H][Sg][dk][dv] each, from the scan).  The pre-pass
+    // (split = 1) takes roles by column block: the transfer matrix A_s (dk
+    // columns, from the identity, v ignored) -> TA [N][H][Sg][dk][dk], the
+    // zero-start state B_s -> TB, and the zero-end adjoint B^_s (the reverse
+    // chain from dS = 0, which needs no forward state) -> TBh, both
+    // [N][H][Sg][dk][dv].
+    int Sg, split, ncbA, ncbB;
+    float *X, *Y;
+    float *TA, *TB, *TBh;
 };
+
+enum BwdRole { ROLE_MAIN = 0, ROLE_XFER_A = 1, ROLE_XFER_B = 2, ROLE_ADJ = 3 };
 
 // Column sums of a WC-column block spread over the warp's lanes (p[j] of lane
 // l: lane l's part of column j); lane l returns the total of column l % WC.
@@ -119,13 +133,28 @@ __device__ __forceinline__ void loadW(const __nv_bfloat16 *p, float (&o)[WC]) {
 template <typename TA>
 __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
-    const int unit = blockIdx.x, cb = blockIdx.y;
+    const int unit = blockIdx.x, s = blockIdx.z;
     const int n = unit / a.H, h = unit % a.H;
+    int role = ROLE_MAIN, cb = blockIdx.y;  // column block within the role
+    if (a.split) {
+        if (cb < a.ncbA) {
+            role = ROLE_XFER_A;
+        } else if ((cb -= a.ncbA) < a.ncbB) {
+            role = ROLE_XFER_B;
+        } else {
+            cb -= a.ncbB;
+            role = ROLE_ADJ;
+        }
+    }
     const int c0 = cb * CTC;
     const int wp = threadIdx.x >> 5, l = threadIdx.x & 31;
     const int dk = a.dk, dv = a.dv, H = a.H;
+    const int ncol = role == ROLE_XFER_A ? dk : dv;  // columns of this role's matrix
+    // which inputs the role reads: v (forward steps), q and d_out (reverse steps)
+    const bool want_v = role == ROLE_MAIN || role == ROLE_XFER_B;
+    const bool want_qd = role == ROLE_MAIN || role == ROLE_ADJ;
     int t_begin, t_end;
-    if (!segment_range(a.cu, n, a.N, a.T_tot, 0, 1, a.dev_status, t_begin, t_end)) return;
+    if (!segment_range(a.cu, n, a.N, a.T_tot, s, a.Sg, a.dev_status, t_begin, t_end)) return;
     int blk_base = 0;  // this sequence's first stored block
     for (int m = 0; m < n; ++m) {
         const int lm = a.cu[m + 1] - a.cu[m];
@@ -135,7 +164,12 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
         }
         blk_base += (lm + BB - 1) / BB;
     }
+    blk_base += (t_begin - a.cu[n]) / BB;  // segments start on 16-token boundaries
     const int nblk = (t_end - t_begin + BB - 1) / BB;
+    // block visits f: forward (f < nblk) and reverse (f >= nblk); the main pass
+    // makes both, the transfer roles the forward ones, the adjoint role the reverse
+    const int fb = role == ROLE_ADJ ? nblk : 0;
+    const int fe = (role == ROLE_XFER_A || role == ROLE_XFER_B) ? nblk : 2 * nblk;
     // full[NBUF] (ring slot ready), empty[NBUF] (slot consumed), landed[NBUF]
     // (bulk copies in)
     const uint32_t bar0 = smem_addr(sm + SM_BAR);
@@ -168,8 +202,8 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
         // alpha and releases the slot.  Visit f + 1 is issued before f finishes.
         bool pok = true;
         auto issue = [&](int f) {
-            const int buf = f % NBUF, use = f / NBUF;
-            const bool back = f >= nblk;
+            const int buf = (f - fb) % NBUF, use = (f - fb) / NBUF;
+            const bool back = f >= nblk, qd = back && want_qd;
             if (use >= 1) pok = mbar_wait(bar_empty(buf), (use - 1) & 1, abort, kWaitLimit) && pok;
             if (!pok) return;
             {
@@ -181,8 +215,8 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                     const uint32_t landed = bar_landed(buf);
                     const int nvc = min(CTC, dv - c0);
                     const uint32_t es = sizeof(TA);
-                    const uint32_t per_tok =
-                        dk * 4 + dk * es + nvc * es + (back ? dk * es + nvc * es : 0);
+                    const uint32_t per_tok = dk * 4 + dk * es + (want_v ? nvc * es : 0) +
+                                             (qd ? dk * es + nvc * es : 0);
                     fence_async_smem();  // this warp's earlier writes to the slot come first
                     if (l == 0) mbar_arrive_expect_tx(landed, nt * per_tok);
                     __syncwarp();
@@ -190,8 +224,9 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                         const size_t row = (size_t)(tb + l) * H + h;
                         bulk_g2s(smem_addr(rb + R_G + l * 128), a.g + row * dk, dk * 4, landed);
                         bulk_g2s(smem_addr(rk + l * 128), k + row * dk, dk * es, landed);
-                        bulk_g2s(smem_addr(rv + l * CTC), v + row * dv + c0, nvc * es, landed);
-                        if (back) {
+                        if (want_v)
+                            bulk_g2s(smem_addr(rv + l * CTC), v + row * dv + c0, nvc * es, landed);
+                        if (qd) {
                             bulk_g2s(smem_addr(rq + l * 128), q + row * dk, dk * es, landed);
                             bulk_g2s(smem_addr(rd + l * CTC), dout + row * dv + c0, nvc * es,
                                      landed);
@@ -217,7 +252,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                     float vv[BB], bv = 0.f;
 #pragma unroll
                     for (int j = 0; j < BB; ++j) {
-                        const bool in = j < nt && c0 + l < dv;
+                        const bool in = want_v && j < nt && c0 + l < dv;
                         vv[j] = in ? act_ld(v, ((size_t)(tb + j) * H + h) * dv + c0 + l) : 0.f;
                     }
                     if (l < nt) bv = a.beta[(size_t)(tb + l) * H + h];
@@ -231,7 +266,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
                         act_st(rv, j * CTC + l, vv[j]);
                     }
                     if (l < BB) rb[R_B + l] = bv;
-                    if (back) {  // the reverse walk also reads q and d_out
+                    if (qd) {  // the reverse walk also reads q and d_out
 #pragma unroll
                         for (int j = 0; j < BB; ++j)
 #pragma unroll
@@ -259,7 +294,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
             }
         };
         auto finish = [&](int f) {
-            const int buf = f % NBUF, use = f / NBUF;
+            const int buf = (f - fb) % NBUF, use = (f - fb) / NBUF;
             if (pok && a.bulk) {
                 // alpha = e^g in place, once for all consumer warps and visits
                 pok = mbar_wait(bar_landed(buf), use & 1, abort, kWaitLimit);
@@ -276,9 +311,9 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
             }
             mbar_arrive(bar_full(buf));
         };
-        if (nblk > 0) issue(0);
-        for (int f = 0; f < 2 * nblk; ++f) {
-            if (f + 1 < 2 * nblk) issue(f + 1);
+        if (fb < fe) issue(fb);
+        for (int f = fb; f < fe; ++f) {
+            if (f + 1 < fe) issue(f + 1);
             finish(f);
         }
         return;
@@ -287,15 +322,25 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
     // ------------------------------------------------------------------ consumers
     const int cw = cb * NWC + wp;  // this warp's WC-column group
     const int c0w = cw * WC;
-    const bool has_cols = cw < a.ncw;  // a warp past the last column keeps zeros only
+    const bool has_cols = c0w < ncol;  // a warp past the last column keeps zeros only
+    // start state and end adjoint of this segment (main), the identity (A), zeros
+    const size_t seg_mat = ((size_t)unit * a.Sg + s) * dk;  // row 0 of segment s's matrices
+    const float *S_in = role != ROLE_MAIN ? nullptr : a.Sg > 1 ? a.X + seg_mat * dv : a.S0;
+    const float *dS_in = role != ROLE_MAIN ? nullptr : a.Sg > 1 ? a.Y + seg_mat * dv : a.dSF;
+    if (a.Sg == 1) {
+        S_in = S_in ? S_in + (size_t)unit * dk * dv : nullptr;
+        dS_in = dS_in ? dS_in + (size_t)unit * dk * dv : nullptr;
+    }
     float S[RPL][WC], dS[RPL][WC];
 #pragma unroll
     for (int rr = 0; rr < RPL; ++rr)
 #pragma unroll
         for (int j = 0; j < WC; ++j) {
             const int r = l + 32 * rr, c = c0w + j;
-            S[rr][j] = (a.S0 && r < dk && c < dv) ? a.S0[((size_t)unit * dk + r) * dv + c] : 0.f;
-            dS[rr][j] = (a.dSF && r < dk && c < dv) ? a.dSF[((size_t)unit * dk + r) * dv + c] : 0.f;
+            const bool in = r < dk && c < ncol;
+            S[rr][j] = role == ROLE_XFER_A ? (in && r == c ? 1.f : 0.f)
+                                           : (S_in && in) ? S_in[(size_t)r * dv + c] : 0.f;
+            dS[rr][j] = (dS_in && in) ? dS_in[(size_t)r * dv + c] : 0.f;
         }
     float4 *tokw = (float4 *)(sm + SM_TOK + wp * TOK_W);  // [BB][WC/4][128]
     float *part = sm + SM_PART, *pb = sm + SM_PB;
@@ -348,15 +393,15 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
     };
     bool ok = true;
 
-    // forward: the state at every block start
-    for (int f = 0; f < nblk; ++f) {
+    // forward: the state at every block start (main), or the segment's end state
+    for (int f = 0; f < nblk && role != ROLE_ADJ; ++f) {
         const int buf = f % NBUF;
         ok = mbar_wait(bar_full(buf), (f / NBUF) & 1, abort, kWaitLimit) && ok;
         if (ok) {
             const float *rb = sm + buf * R_SIZE;
 #pragma unroll
             for (int rr = 0; rr < RPL; ++rr) {
-                if (!has_cols || l + 32 * rr >= dk) continue;
+                if (role != ROLE_MAIN || !has_cols || l + 32 * rr >= dk) continue;
                 float4 *d = blk_ptr(f, rr);
 #pragma unroll
                 for (int x = 0; x < WC / 4; ++x)
@@ -367,6 +412,22 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
             for (int j = 0; j < nt; ++j) fstep(rb, j, false);
         }
         mbar_arrive(bar_empty(buf));
+    }
+    if (role == ROLE_XFER_A || role == ROLE_XFER_B) {  // A_s or B_s of this segment
+        if (!ok) {
+            dev_fail(a.dev_status, KDA_ERR_TIMEOUT);
+            return;
+        }
+        float *out = role == ROLE_XFER_A ? a.TA + seg_mat * dk : a.TB + seg_mat * dv;
+        const int ld = role == ROLE_XFER_A ? dk : dv;
+#pragma unroll
+        for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+            for (int j = 0; j < WC; ++j) {
+                const int r = l + 32 * rr, c = c0w + j;
+                if (r < dk && c < ncol) out[(size_t)r * ld + c] = S[rr][j];
+            }
+        return;
     }
     auto load_start = [&](int c) {
 #pragma unroll
@@ -381,13 +442,54 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
             }
         }
     };
-    if (nblk > 0 && ok) load_start(nblk - 1);
+    if (role == ROLE_MAIN && nblk > 0 && ok) load_start(nblk - 1);
 
     // reverse
     for (int f = nblk; f < 2 * nblk; ++f) {
-        const int buf = f % NBUF, c = 2 * nblk - 1 - f;
+        const int buf = (f - fb) % NBUF, c = 2 * nblk - 1 - f;
         const int tb = t_begin + c * BB, nt = min(BB, t_end - tb);
-        ok = mbar_wait(bar_full(buf), (f / NBUF) & 1, abort, kWaitLimit) && ok;
+        ok = mbar_wait(bar_full(buf), ((f - fb) / NBUF) & 1, abort, kWaitLimit) && ok;
+        if (role == ROLE_ADJ) {  // the adjoint chain alone: dS <- Diag(alpha)(I - beta k k^T)(dS + q do^T)
+            if (ok) {
+                const float *rb = sm + buf * R_SIZE;
+                for (int j = nt - 1; j >= 0; --j) {
+                    float kr[RPL], qr[RPL], al[RPL], dov[WC], pw[WC];
+#pragma unroll
+                    for (int rr = 0; rr < RPL; ++rr) {
+                        kr[rr] = act_ld((const TA *)(rb + R_K), j * 128 + l + 32 * rr);
+                        qr[rr] = act_ld((const TA *)(rb + R_Q), j * 128 + l + 32 * rr);
+                        al[rr] = rb[R_G + j * 128 + l + 32 * rr];
+                    }
+                    loadW((const TA *)(rb + R_D) + j * CTC + WC * wp, dov);
+#pragma unroll
+                    for (int jj = 0; jj < WC; ++jj) pw[jj] = 0.f;
+#pragma unroll
+                    for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+                        for (int jj = 0; jj < WC; jj += 2) {
+                            fma2_acc(dS[rr][jj], dS[rr][jj + 1], qr[rr], qr[rr], dov[jj],
+                                     dov[jj + 1]);
+                            fma2_acc(pw[jj], pw[jj + 1], dS[rr][jj], dS[rr][jj + 1], kr[rr],
+                                     kr[rr]);
+                        }
+                    const float wm = colsum(pw);
+                    const float nb = -rb[R_B + j];
+                    float ndu[WC];
+#pragma unroll
+                    for (int jj = 0; jj < WC; ++jj) ndu[jj] = nb * __shfl_sync(0xffffffffu, wm, jj);
+#pragma unroll
+                    for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+                        for (int jj = 0; jj < WC; jj += 2) {
+                            fma2_acc(dS[rr][jj], dS[rr][jj + 1], kr[rr], kr[rr], ndu[jj],
+                                     ndu[jj + 1]);
+                            mul2_inplace(dS[rr][jj], dS[rr][jj + 1], make_float2(al[rr], al[rr]));
+                        }
+                }
+            }
+            mbar_arrive(bar_empty(buf));
+            continue;
+        }
         if (ok) {
             const float *rb = sm + buf * R_SIZE;
             for (int j = 0; j < nt; ++j) {  // the block's pre-token states
@@ -511,36 +613,121 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
         dev_fail(a.dev_status, KDA_ERR_TIMEOUT);
         return;
     }
-    if (a.gS0) {
+    // the adjoint at the segment's start: dS0 (main, first segment) or B^_s
+    float *dout_mat = role == ROLE_ADJ ? a.TBh + seg_mat * dv
+                      : (s == 0 && a.gS0) ? a.gS0 + (size_t)unit * dk * dv
+                                          : nullptr;
+    if (dout_mat) {
 #pragma unroll
         for (int rr = 0; rr < RPL; ++rr)
 #pragma unroll
             for (int j = 0; j < WC; ++j) {
                 const int r = l + 32 * rr, c = c0w + j;
-                if (r < dk && c < dv) a.gS0[((size_t)unit * dk + r) * dv + c] = dS[rr][j];
+                if (r < dk && c < dv) dout_mat[(size_t)r * dv + c] = dS[rr][j];
             }
+    }
+}
+
+// The segment scans, fp32: start states X_0 = S0, X_{s+1} = A_s X_s + B_s, and
+// end adjoints Y_{Sg-1} = d_S_final, Y_{s-1} = A_s^T Y_s + B^_s (the adjoint of a
+// segment's linear map is the transpose of its transfer matrix: each token's
+// adjoint step Diag(alpha)(I - beta k k^T) is the transpose of its forward map
+// (I - beta k k^T) Diag(alpha)).  grid (N*H, ceil(dv / 32), 2): z = 0 the forward
+// scan, z = 1 the adjoint scan; thread r keeps row r of a 32-column block.
+constexpr int SC_T = 128;
+__global__ void __launch_bounds__(SC_T) bwd_scan_kernel(const BwdArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const int unit = blockIdx.x, c0 = blockIdx.y * 32, adj = blockIdx.z;
+    const int dk = a.dk, dv = a.dv, Sg = a.Sg, r = threadIdx.x;
+    const int nc = min(32, dv - c0);
+    float *As = sm;                 // [dk][dk + 1]: A_s, padded against bank conflicts
+    float *Z = sm + dk * (dk + 1);  // [dk][32]: the running matrix
+    const size_t base = (size_t)unit * Sg * dk;  // row 0 of segment 0
+    const float *init = adj ? a.dSF : a.S0;
+    float *outm = adj ? a.Y : a.X;
+    float z[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        z[j] = (init && r < dk && j < nc) ? init[((size_t)unit * dk + r) * dv + c0 + j] : 0.f;
+    if (r < dk) {
+        float *o = outm + (base + (size_t)(adj ? Sg - 1 : 0) * dk + r) * dv + c0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < nc) o[j] = z[j];
+    }
+    for (int step = 0; step < Sg - 1; ++step) {
+        const int sa = adj ? Sg - 1 - step : step;  // the segment whose map is applied
+        __syncthreads();  // the previous step's readers are done
+        const float *A = a.TA + (base + (size_t)sa * dk) * dk;
+        for (int e = r; e < dk * dk; e += SC_T) As[(e / dk) * (dk + 1) + e % dk] = A[e];
+        if (r < dk) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) Z[r * 32 + j] = z[j];
+        }
+        __syncthreads();
+        if (r < dk) {
+            const float *Bm = (adj ? a.TBh : a.TB) + (base + (size_t)sa * dk + r) * dv + c0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = j < nc ? Bm[j] : 0.f;
+            for (int kk = 0; kk < dk; ++kk) {
+                const float av = adj ? As[kk * (dk + 1) + r] : As[r * (dk + 1) + kk];
+                const float4 *zr = (const float4 *)(Z + kk * 32);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float4 zz = zr[x];
+                    z[4 * x] = fmaf(av, zz.x, z[4 * x]);
+                    z[4 * x + 1] = fmaf(av, zz.y, z[4 * x + 1]);
+                    z[4 * x + 2] = fmaf(av, zz.z, z[4 * x + 2]);
+                    z[4 * x + 3] = fmaf(av, zz.w, z[4 * x + 3]);
+                }
+            }
+            float *o = outm + (base + (size_t)(adj ? sa - 1 : sa + 1) * dk + r) * dv + c0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < nc) o[j] = z[j];
+        }
     }
 }
 
 }  // namespace
 
-size_t backward_workspace_bytes(int N, int T_tot, int H, int dk, int dv) {
+namespace {
+size_t r256(size_t b) { return (b + 255) & ~(size_t)255; }
+size_t blk_bytes(int N, int T_tot, int H, int dk, int dv) {
     const size_t blocks = (size_t)T_tot / BB + N;  // >= sum_n ceil(len_n / 8)
     const int ncw = (dv + WC - 1) / WC;
     return blocks * H * ncw * dk * WC * sizeof(float);
 }
+}  // namespace
+
+size_t backward_workspace_bytes(int N, int T_tot, int H, int dk, int dv, int Sg) {
+    size_t b = blk_bytes(N, T_tot, H, dk, dv);
+    if (Sg > 1)  // A_s; B_s, B^_s, X_s, Y_s
+        b = r256(b) + (size_t)N * H * Sg * ((size_t)dk * dk + 4 * (size_t)dk * dv) * sizeof(float);
+    return b;
+}
 
 cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float *dSF, float *dq,
-                            float *dk, float *dv, float *dg, float *dbeta, float *dS0,
+                            float *dk, float *dv, float *dg, float *dbeta, float *dS0, int Sg,
                             void *workspace, cudaStream_t st) {
     BwdArgs a;
+    memset(&a, 0, sizeof(a));
     a.q = p.q; a.k = p.k; a.v = p.v; a.dout = dout;
     a.g = p.g; a.beta = p.beta; a.S0 = p.S0; a.dSF = dSF; a.cu = p.cu;
     a.gq = dq; a.gk = dk; a.gv = dv; a.gg = dg; a.gbeta = dbeta; a.gS0 = dS0;
     a.dev_status = p.dev_status;
     a.N = p.N; a.T_tot = p.T_tot; a.H = p.H; a.dk = p.dk; a.dv = p.dv; a.act = p.act;
     a.ncw = (p.dv + WC - 1) / WC;
+    a.Sg = Sg < 1 ? 1 : Sg;
     a.blk_states = (float *)workspace;
+    if (a.Sg > 1) {
+        const size_t nhs = (size_t)p.N * p.H * a.Sg;
+        a.TA = (float *)((uint8_t *)workspace + r256(blk_bytes(p.N, p.T_tot, p.H, p.dk, p.dv)));
+        a.TB = a.TA + nhs * p.dk * p.dk;
+        a.TBh = a.TB + nhs * p.dk * p.dv;
+        a.X = a.TBh + nhs * p.dk * p.dv;
+        a.Y = a.X + nhs * p.dk * p.dv;
+    }
     {
         const int es = p.act == KDA_DTYPE_F32 ? 4 : 2;
         auto al16 = [](const void *x) { return ((uintptr_t)x & 15u) == 0; };
@@ -555,18 +742,33 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
     if ((e = cudaMemsetAsync(dg, 0, Tn * p.dk * sizeof(float), st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dbeta, 0, Tn * sizeof(float), st)) != cudaSuccess) return e;
     if (p.N == 0 || p.H == 0) return cudaSuccess;
-    dim3 grid((unsigned)(p.N * p.H), (unsigned)((p.dv + CTC - 1) / CTC));
-    if (p.act == KDA_DTYPE_F32) {
-        if ((e = set_max_dynamic_smem((const void *)backward_kernel<float>, (int)BWD_SMEM)) != cudaSuccess)
-            return e;
-        backward_kernel<float><<<grid, BT, BWD_SMEM, st>>>(a);
-    } else {
-        if ((e = set_max_dynamic_smem((const void *)backward_kernel<__nv_bfloat16>, (int)BWD_SMEM)) !=
+    const void *kern = p.act == KDA_DTYPE_F32 ? (const void *)backward_kernel<float>
+                                              : (const void *)backward_kernel<__nv_bfloat16>;
+    if ((e = set_max_dynamic_smem(kern, (int)BWD_SMEM)) != cudaSuccess) return e;
+    auto run = [&](dim3 grid) {
+        if (p.act == KDA_DTYPE_F32) backward_kernel<float><<<grid, BT, BWD_SMEM, st>>>(a);
+        else backward_kernel<__nv_bfloat16><<<grid, BT, BWD_SMEM, st>>>(a);
+        return cudaGetLastError();
+    };
+    const int ncb = (p.dv + CTC - 1) / CTC;
+    if (a.Sg > 1) {
+        // pre-pass: A_s, B_s and B^_s of every segment, in parallel
+        a.split = 1;
+        a.ncbA = (p.dk + CTC - 1) / CTC;
+        a.ncbB = ncb;
+        if ((e = run(dim3((unsigned)(p.N * p.H), (unsigned)(a.ncbA + 2 * ncb), (unsigned)a.Sg))) !=
             cudaSuccess)
             return e;
-        backward_kernel<__nv_bfloat16><<<grid, BT, BWD_SMEM, st>>>(a);
+        // scans: every segment's start state and end adjoint
+        const size_t ssm = (size_t)(p.dk * (p.dk + 1) + p.dk * 32) * sizeof(float);
+        if ((e = set_max_dynamic_smem((const void *)bwd_scan_kernel, (int)ssm)) != cudaSuccess)
+            return e;
+        bwd_scan_kernel<<<dim3((unsigned)(p.N * p.H), (unsigned)((p.dv + 31) / 32), 2), SC_T, ssm,
+                          st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        a.split = 0;
     }
-    return cudaGetLastError();
+    return run(dim3((unsigned)(p.N * p.H), (unsigned)ncb, (unsigned)a.Sg));
 }
 
 }  // namespace kda

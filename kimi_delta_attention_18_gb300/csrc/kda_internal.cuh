@@ -147,9 +147,10 @@ cudaError_t launch_ckpt_fixup(const PrefillArgs &a, const float *S0, const float
 
 // Backward pass (kda_backward.cu): workspace bytes, and the launch (zeroes the
 // accumulated outputs on st first).
-size_t backward_workspace_bytes(int N, int T_tot, int H, int dk, int dv);
+// Sg > 1 splits every sequence into Sg segments (pre-pass, scans, main pass).
+size_t backward_workspace_bytes(int N, int T_tot, int H, int dk, int dv, int Sg);
 cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float *dSF, float *dq,
-                            float *dk, float *dv, float *dg, float *dbeta, float *dS0,
+                            float *dk, float *dv, float *dg, float *dbeta, float *dS0, int Sg,
                             void *workspace, cudaStream_t st);
 bool decode_tma_supported(int dk, int dv);
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,

@@ -214,6 +214,11 @@ def test_backward_host_checks():
     # the state at every 8-token block start: [T/8 + N blocks][H][ceil(dv/8)][dk][8] fp32
     blocks = d.total_tokens // 8 + d.num_seqs
     assert need == blocks * d.num_heads * ((d.dv + 7) // 8) * d.dk * 8 * 4
+    # segments: + A_s [dk][dk] and B_s, B^_s, X_s, Y_s [dk][dv] per (sequence, head, segment)
+    d4 = _desc(num_segments=4)
+    r256 = lambda b: (b + 255) // 256 * 256
+    assert L.kda_prefill_backward_workspace_size(ctypes.byref(d4)) == r256(need) + \
+        d4.num_seqs * d4.num_heads * 4 * (d4.dk * d4.dk + 4 * d4.dk * d4.dv) * 4
     assert L.kda_prefill_backward_workspace_size(ctypes.byref(_desc(chunk=32))) == 0
     assert call(d) == WORKSPACE
     assert call(d, ws=0x40000, ws_len=need - 1) == WORKSPACE

@@ -69,6 +69,27 @@ def test_backward_matches_oracle(act, dk, dv, lengths, slow):
         assert rel_err(_np(a), b) <= TOL, (name, rel_err(_np(a), b))
 
 
+@pytest.mark.parametrize("act,d,lengths,nseg", [
+    ("f32", 32, [300, 77, 0, 129], 2),
+    ("f32", 32, [300, 77, 0, 129], 5),
+    ("f32", 48, [200, 31], 3),
+    ("bf16", 128, [250, 90], 4),
+    ("bf16", 128, [250, 90], 0),    # the library's choice
+    ("bf16", 60, [100, 45], 3),     # plain-load producer
+])
+def test_backward_segments_match_oracle(act, d, lengths, nseg):
+    """The segment split (per-segment transfer matrices, zero-start states and
+    zero-end adjoints, fp32 scans, then the gradient pass per segment) against the
+    oracle, with a material initial state and final-state adjoint (slow decay)."""
+    H = 2
+    x = make_prefill_inputs(lengths, H, d, d, act, s0_std=1.0, seed=41, slow_decay=True)
+    d_out, d_sf = make_backward_adjoints(sum(lengths), len(lengths), H, d, d, act, seed=42)
+    got = _run(x, d_out, d_sf, num_segments=nseg)
+    ref = _oracle(x, d_out, d_sf)
+    for name, a, b in zip(NAMES, got, ref):
+        assert rel_err(_np(a), b) <= TOL, (name, rel_err(_np(a), b))
+
+
 def test_backward_without_initial_or_final_state():
     lengths = [29, 0, 50]
     x = make_prefill_inputs(lengths, 2, 32, 32, "f32", seed=33)
