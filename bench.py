@@ -480,9 +480,10 @@ def run_backward(args, kda, x, flush, stream, dev, dist):
     flops = 20.0 * dk * dv * T * H
     peak = BWD_FP32_TFLOPS
     achieved = flops / (ms * 1e-3) / 1e12
-    return {"what": "dq, dk, dv, dg, dbeta, dS0 (fp32), token-level SIMT kernel",
+    return {"what": "dq, dk, dv, dg, dbeta, dS0 (fp32), token-level SIMT kernels, segment split",
             "ms_per_step": round(ms, 4), "tokens_per_s": round(N and T / (ms * 1e-3), 1),
-            "ctas": N * H * ((dv + 31) // 32),
+            "segments": kda.prefill_backward_num_segments(desc),
+            "ctas_per_pass": N * H * ((dv + 31) // 32) * kda.prefill_backward_num_segments(desc),
             "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "flops_per_head_token": 20 * dk * dv,

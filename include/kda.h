@@ -315,6 +315,8 @@ kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_desc_t *desc, const v
  * short workspace, KDA_ERR_UNSUPPORTED as kda_prefill_chunked.
  */
 size_t kda_prefill_backward_workspace_size(const kda_prefill_desc_t *desc);
+/* Segments per sequence the backward pass uses for desc (0 on invalid arguments). */
+int32_t kda_prefill_backward_num_segments(const kda_prefill_desc_t *desc);
 kda_status_t kda_prefill_backward(const kda_prefill_desc_t *desc, const void *q, const void *k,
                                   const void *v, const float *g, const float *beta,
                                   const float *S0, const int32_t *cu_seqlens, const void *d_out,

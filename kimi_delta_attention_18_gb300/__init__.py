@@ -13,6 +13,7 @@ from ._native import (  # noqa: F401
     prefill_combine,
     library_path,
     prefill_backward,
+    prefill_backward_num_segments,
     prefill_backward_workspace_size,
     prefill_chunked,
     prefill_chunked_ckpt,
@@ -29,7 +30,7 @@ from ._native import (  # noqa: F401
 
 __all__ = ["KDAError", "PrefillDesc", "decode_step", "lib", "library_path", "num_checkpoints",
            "prefill_backward",
-           "prefill_backward_workspace_size", "prefill_chunked", "prefill_chunked_ckpt", "prefill_chunked_gated",
+           "prefill_backward_num_segments", "prefill_backward_workspace_size", "prefill_chunked", "prefill_chunked_ckpt", "prefill_chunked_gated",
            "prefill_ckpt_workspace_size", "prefill_combine", "prefill_desc",
            "prefill_num_segments", "prefill_segments", "prefill_workspace_size", "state_compose",
            "state_transfer"]

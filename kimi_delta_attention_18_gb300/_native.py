@@ -63,6 +63,8 @@ def lib():
                 [_I, _P, _P, ctypes.c_size_t, _P, _P]
             L.kda_prefill_backward_workspace_size.restype = ctypes.c_size_t
             L.kda_prefill_backward_workspace_size.argtypes = [ctypes.POINTER(PrefillDesc)]
+            L.kda_prefill_backward_num_segments.restype = _I
+            L.kda_prefill_backward_num_segments.argtypes = [ctypes.POINTER(PrefillDesc)]
             L.kda_prefill_backward.restype = ctypes.c_int
             L.kda_prefill_backward.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 16 + \
                 [ctypes.c_size_t, _P, _P]
@@ -305,6 +307,11 @@ def prefill_chunked_ckpt(q, k, v, g, beta, S0=None, cu_seqlens=None, *, ckpt_int
 def prefill_backward_workspace_size(desc) -> int:
     """Workspace bytes kda_prefill_backward needs for ``desc`` (0 on invalid input)."""
     return int(lib().kda_prefill_backward_workspace_size(ctypes.byref(desc)))
+
+
+def prefill_backward_num_segments(desc) -> int:
+    """Segments per sequence kda_prefill_backward uses for ``desc``."""
+    return int(lib().kda_prefill_backward_num_segments(ctypes.byref(desc)))
 
 
 def prefill_backward(q, k, v, g, beta, S0, cu_seqlens, d_out, d_S_final=None, *,

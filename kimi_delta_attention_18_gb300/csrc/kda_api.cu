@@ -322,6 +322,11 @@ size_t kda_prefill_backward_workspace_size(const kda_prefill_desc_t *desc) {
                                     desc->dv, backward_segments(desc));
 }
 
+int32_t kda_prefill_backward_num_segments(const kda_prefill_desc_t *desc) {
+    if (check_desc(desc) != KDA_OK) return 0;
+    return backward_segments(desc);
+}
+
 kda_status_t kda_prefill_backward(const kda_prefill_desc_t *desc, const void *q, const void *k,
                                   const void *v, const float *g, const float *beta,
                                   const float *S0, const int32_t *cu_seqlens, const void *d_out,

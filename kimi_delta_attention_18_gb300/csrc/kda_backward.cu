@@ -61,6 +61,9 @@ constexpr int SM_PB = SM_PART + NWC * BB * 3 * 128;
 constexpr int SM_U = SM_PB + NWC * BB;
 constexpr int SM_BAR = SM_U + NWC * BB * WC;  // 9 mbarriers (18 floats), then the flag
 constexpr size_t BWD_SMEM = (size_t)(SM_BAR + 18 + 4) * sizeof(float);
+// the pre-pass instantiation keeps only the ring; its barriers follow it
+constexpr int SM_BAR_PRE = NBUF * R_SIZE;
+constexpr size_t BWD_SMEM_PRE = (size_t)(SM_BAR_PRE + 18 + 4) * sizeof(float);
 static_assert(R_B + BB <= R_SIZE && (R_SIZE % 4) == 0 && (R_D % 4) == 0, "ring layout");
 static_assert((SM_BAR % 2) == 0 && (SM_TOK % 4) == 0 && (SM_U % 4) == 0, "alignment");
 static_assert(BWD_SMEM <= 227 * 1024, "shared memory");
@@ -77,12 +80,12 @@ struct BwdArgs {
     int bulk;  // rows and column slices meet the bulk-copy rules (16-byte aligned)
     // Segments (Sg > 1): the main pass runs segment s from its start state X and
     // its end adjoint Y ([N][H][Sg][dk][dv] each, from the scan).  The pre-pass
-    // (split = 1) takes roles by column block: the transfer matrix A_s (dk
+    // (the PRE instantiation) takes roles by column block: the transfer matrix A_s (dk
     // columns, from the identity, v ignored) -> TA [N][H][Sg][dk][dk], the
     // zero-start state B_s -> TB, and the zero-end adjoint B^_s (the reverse
     // chain from dS = 0, which needs no forward state) -> TBh, both
     // [N][H][Sg][dk][dv].
-    int Sg, split, ncbA, ncbB;
+    int Sg, ncbA, ncbB;
     float *X, *Y;
     float *TA, *TB, *TBh;
 };
@@ -130,13 +133,15 @@ __device__ __forceinline__ void loadW(const __nv_bfloat16 *p, float (&o)[WC]) {
     }
 }
 
-template <typename TA>
-__global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
+// PRE: the segment pre-pass (transfer and adjoint roles only, 3 CTAs per SM);
+// otherwise the gradient pass.
+template <typename TA, bool PRE>
+__global__ void __launch_bounds__(BT, PRE ? 3 : 1) backward_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int unit = blockIdx.x, s = blockIdx.z;
     const int n = unit / a.H, h = unit % a.H;
     int role = ROLE_MAIN, cb = blockIdx.y;  // column block within the role
-    if (a.split) {
+    if (PRE) {
         if (cb < a.ncbA) {
             role = ROLE_XFER_A;
         } else if ((cb -= a.ncbA) < a.ncbB) {
@@ -172,11 +177,11 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
     const int fe = (role == ROLE_XFER_A || role == ROLE_XFER_B) ? nblk : 2 * nblk;
     // full[NBUF] (ring slot ready), empty[NBUF] (slot consumed), landed[NBUF]
     // (bulk copies in)
-    const uint32_t bar0 = smem_addr(sm + SM_BAR);
+    const uint32_t bar0 = smem_addr(sm + (PRE ? SM_BAR_PRE : SM_BAR));
     auto bar_full = [&](int b) { return bar0 + 8 * b; };
     auto bar_empty = [&](int b) { return bar0 + 8 * (NBUF + b); };
     auto bar_landed = [&](int b) { return bar0 + 8 * (2 * NBUF + b); };
-    volatile int *abort = (volatile int *)(sm + SM_BAR + 18);
+    volatile int *abort = (volatile int *)(sm + (PRE ? SM_BAR_PRE : SM_BAR) + 18);
     // padded rows (past dk) and columns (past dv) of the ring stay zero: the
     // producer writes only the real ones
     for (int e = threadIdx.x; e < NBUF * R_SIZE; e += BT) sm[e] = 0.f;
@@ -325,8 +330,9 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
     const bool has_cols = c0w < ncol;  // a warp past the last column keeps zeros only
     // start state and end adjoint of this segment (main), the identity (A), zeros
     const size_t seg_mat = ((size_t)unit * a.Sg + s) * dk;  // row 0 of segment s's matrices
-    const float *S_in = role != ROLE_MAIN ? nullptr : a.Sg > 1 ? a.X + seg_mat * dv : a.S0;
-    const float *dS_in = role != ROLE_MAIN ? nullptr : a.Sg > 1 ? a.Y + seg_mat * dv : a.dSF;
+    const bool main_role = !PRE && role == ROLE_MAIN;
+    const float *S_in = !main_role ? nullptr : a.Sg > 1 ? a.X + seg_mat * dv : a.S0;
+    const float *dS_in = !main_role ? nullptr : a.Sg > 1 ? a.Y + seg_mat * dv : a.dSF;
     if (a.Sg == 1) {
         S_in = S_in ? S_in + (size_t)unit * dk * dv : nullptr;
         dS_in = dS_in ? dS_in + (size_t)unit * dk * dv : nullptr;
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
             const float *rb = sm + buf * R_SIZE;
 #pragma unroll
             for (int rr = 0; rr < RPL; ++rr) {
-                if (role != ROLE_MAIN || !has_cols || l + 32 * rr >= dk) continue;
+                if (!main_role || !has_cols || l + 32 * rr >= dk) continue;
                 float4 *d = blk_ptr(f, rr);
 #pragma unroll
                 for (int x = 0; x < WC / 4; ++x)
@@ -442,14 +448,14 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
             }
         }
     };
-    if (role == ROLE_MAIN && nblk > 0 && ok) load_start(nblk - 1);
+    if (main_role && nblk > 0 && ok) load_start(nblk - 1);
 
     // reverse
     for (int f = nblk; f < 2 * nblk; ++f) {
         const int buf = (f - fb) % NBUF, c = 2 * nblk - 1 - f;
         const int tb = t_begin + c * BB, nt = min(BB, t_end - tb);
         ok = mbar_wait(bar_full(buf), ((f - fb) / NBUF) & 1, abort, kWaitLimit) && ok;
-        if (role == ROLE_ADJ) {  // the adjoint chain alone: dS <- Diag(alpha)(I - beta k k^T)(dS + q do^T)
+        if (PRE) {  // ROLE_ADJ: the adjoint chain alone: dS <- Diag(alpha)(I - beta k k^T)(dS + q do^T)
             if (ok) {
                 const float *rb = sm + buf * R_SIZE;
                 for (int j = nt - 1; j >= 0; --j) {
@@ -615,7 +621,7 @@ __global__ void __launch_bounds__(BT, 1) backward_kernel(const BwdArgs a) {
     }
     // the adjoint at the segment's start: dS0 (main, first segment) or B^_s
     float *dout_mat = role == ROLE_ADJ ? a.TBh + seg_mat * dv
-                      : (s == 0 && a.gS0) ? a.gS0 + (size_t)unit * dk * dv
+                      : (main_role && s == 0 && a.gS0) ? a.gS0 + (size_t)unit * dk * dv
                                           : nullptr;
     if (dout_mat) {
 #pragma unroll
@@ -742,22 +748,28 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
     if ((e = cudaMemsetAsync(dg, 0, Tn * p.dk * sizeof(float), st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dbeta, 0, Tn * sizeof(float), st)) != cudaSuccess) return e;
     if (p.N == 0 || p.H == 0) return cudaSuccess;
-    const void *kern = p.act == KDA_DTYPE_F32 ? (const void *)backward_kernel<float>
-                                              : (const void *)backward_kernel<__nv_bfloat16>;
-    if ((e = set_max_dynamic_smem(kern, (int)BWD_SMEM)) != cudaSuccess) return e;
-    auto run = [&](dim3 grid) {
-        if (p.act == KDA_DTYPE_F32) backward_kernel<float><<<grid, BT, BWD_SMEM, st>>>(a);
-        else backward_kernel<__nv_bfloat16><<<grid, BT, BWD_SMEM, st>>>(a);
+    const bool f32 = p.act == KDA_DTYPE_F32;
+    auto run = [&](dim3 grid, bool pre) {
+        const void *kern = pre ? (f32 ? (const void *)backward_kernel<float, true>
+                                      : (const void *)backward_kernel<__nv_bfloat16, true>)
+                               : (f32 ? (const void *)backward_kernel<float, false>
+                                      : (const void *)backward_kernel<__nv_bfloat16, false>);
+        const size_t smem = pre ? BWD_SMEM_PRE : BWD_SMEM;
+        cudaError_t err = set_max_dynamic_smem(kern, (int)smem);
+        if (err != cudaSuccess) return err;
+        if (pre && f32) backward_kernel<float, true><<<grid, BT, smem, st>>>(a);
+        else if (pre) backward_kernel<__nv_bfloat16, true><<<grid, BT, smem, st>>>(a);
+        else if (f32) backward_kernel<float, false><<<grid, BT, smem, st>>>(a);
+        else backward_kernel<__nv_bfloat16, false><<<grid, BT, smem, st>>>(a);
         return cudaGetLastError();
     };
     const int ncb = (p.dv + CTC - 1) / CTC;
     if (a.Sg > 1) {
         // pre-pass: A_s, B_s and B^_s of every segment, in parallel
-        a.split = 1;
         a.ncbA = (p.dk + CTC - 1) / CTC;
         a.ncbB = ncb;
-        if ((e = run(dim3((unsigned)(p.N * p.H), (unsigned)(a.ncbA + 2 * ncb), (unsigned)a.Sg))) !=
-            cudaSuccess)
+        if ((e = run(dim3((unsigned)(p.N * p.H), (unsigned)(a.ncbA + 2 * ncb), (unsigned)a.Sg),
+                      true)) != cudaSuccess)
             return e;
         // scans: every segment's start state and end adjoint
         const size_t ssm = (size_t)(p.dk * (p.dk + 1) + p.dk * 32) * sizeof(float);
@@ -766,9 +778,8 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
         bwd_scan_kernel<<<dim3((unsigned)(p.N * p.H), (unsigned)((p.dv + 31) / 32), 2), SC_T, ssm,
                           st>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        a.split = 0;
     }
-    return run(dim3((unsigned)(p.N * p.H), (unsigned)ncb, (unsigned)a.Sg));
+    return run(dim3((unsigned)(p.N * p.H), (unsigned)ncb, (unsigned)a.Sg), false);
 }
 
 }  // namespace kda

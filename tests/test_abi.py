@@ -220,6 +220,9 @@ def test_backward_host_checks():
     assert L.kda_prefill_backward_workspace_size(ctypes.byref(d4)) == r256(need) + \
         d4.num_seqs * d4.num_heads * 4 * (d4.dk * d4.dk + 4 * d4.dk * d4.dv) * 4
     assert L.kda_prefill_backward_workspace_size(ctypes.byref(_desc(chunk=32))) == 0
+    assert L.kda_prefill_backward_num_segments(ctypes.byref(d4)) == 4
+    assert L.kda_prefill_backward_num_segments(ctypes.byref(_desc(num_segments=500))) == 64
+    assert L.kda_prefill_backward_num_segments(ctypes.byref(_desc(chunk=32))) == 0
     assert call(d) == WORKSPACE
     assert call(d, ws=0x40000, ws_len=need - 1) == WORKSPACE
     assert call(d, ws=0x40008, ws_len=need) == WORKSPACE       # not 16-byte aligned
