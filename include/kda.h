@@ -304,7 +304,7 @@ kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_desc_t *desc, const v
  * are overwritten (dq, dk, dg, dbeta are zeroed on the stream, then accumulated);
  * none may alias an input.  Computed in fp32 at token granularity: one CTA per
  * (sequence, head, 32 value columns) recomputes the states from a checkpoint at
- * every 8-token block start kept in the workspace.  desc->num_segments (0: the
+ * every 4-token block start kept in the workspace.  desc->num_segments (0: the
  * library's choice, at most 64) splits every sequence into segments run in
  * parallel: each segment's transfer matrix A, zero-start state and zero-end
  * adjoint first, then fp32 scans for every segment's start state and end

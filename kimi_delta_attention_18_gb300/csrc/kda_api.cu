@@ -87,14 +87,15 @@ int choose_segments(const kda_prefill_desc_t *d) {
 
 // Segments per sequence of the backward pass (desc->num_segments, or the
 // library's choice for 0).  Every (sequence, head, 32 value columns) unit of the
-// backward is a token-sequential chain; with fewer units than SMs the sequences
-// are split (at least ~256 tokens per segment on average, at most 64 segments).
+// backward is a token-sequential chain and its gradient pass runs two CTAs per
+// SM; with fewer units than that the sequences are split (at least ~256 tokens
+// per segment on average, at most 64 segments).
 int backward_segments(const kda_prefill_desc_t *d) {
     if (d->num_segments > 0) return d->num_segments < 64 ? d->num_segments : 64;
     const long long units = (long long)d->num_seqs * d->num_heads * ((d->dv + 31) / 32);
-    const int sms = sm_count();
-    if (units <= 0 || units >= sms) return 1;
-    long long sg = sms / units;
+    const int slots = 2 * sm_count();
+    if (units <= 0 || units >= slots) return 1;
+    long long sg = slots / units;
     const long long per_seq = d->num_seqs > 0 ? d->total_tokens / d->num_seqs : 0;
     const long long cap = per_seq / 256 > 1 ? per_seq / 256 : 1;
     if (sg > cap) sg = cap;

@@ -19,7 +19,7 @@
 // CTA takes (sequence, head, 32 value columns): four consumer warps own 8
 // columns each and all dk <= 128 rows (4 rows per lane), so the column sums u and
 // w of a token stay inside a warp (shuffles, no block barrier).  A producer warp
-// stages every 8-token block's inputs (g, k, q, v, d_out, beta) into a
+// stages every 4-token block's inputs (g, k, q, v, d_out, beta) into a
 // double-buffered shared-memory ring ahead of use, by bulk copies where the rows
 // allow.  A forward pass keeps the state at every block start in the workspace;
 // the reverse pass recomputes the block's token states into shared memory and
@@ -38,7 +38,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BB = 8;             // tokens per stored block
+constexpr int BB = 4;             // tokens per stored block
 constexpr int WC = 8;             // state columns per consumer warp
 constexpr int NWC = 4;            // consumer warps (one per SM sub-partition)
 constexpr int CTC = WC * NWC;     // columns per CTA
@@ -53,7 +53,7 @@ constexpr long long kWaitLimit = 4000000000ll;  // ~2 s of SM clocks
 // [NWC][BB][3][128] and dbeta [NWC][BB] of the block; u = v - M^T k of every
 // token of the block [NWC][BB][WC]; then the mbarriers and the abort flag.
 constexpr int R_G = 0, R_K = BB * 128, R_Q = 2 * BB * 128, R_V = 3 * BB * 128,
-              R_D = R_V + BB * CTC, R_B = R_D + BB * CTC, R_SIZE = 3600;
+              R_D = R_V + BB * CTC, R_B = R_D + BB * CTC, R_SIZE = (R_B + BB + 3) / 4 * 4;
 constexpr int SM_TOK = NBUF * R_SIZE;
 constexpr int TOK_W = BB * 128 * WC;
 constexpr int SM_PART = SM_TOK + NWC * TOK_W;
@@ -74,7 +74,7 @@ struct BwdArgs {
     const float *g, *beta, *S0, *dSF;
     const int32_t *cu;
     float *gq, *gk, *gv, *gg, *gbeta, *gS0;  // dq, dk, dv, dg, dbeta, dS0
-    float *blk_states;  // [blocks][H][ncw][dk][8]: the state at each 8-token block start
+    float *blk_states;  // [blocks][H][ncw][dk][8]: the state at each BB-token block start
     int32_t *dev_status;
     int N, T_tot, H, dk, dv, ncw, act;
     int bulk;  // rows and column slices meet the bulk-copy rules (16-byte aligned)
@@ -136,7 +136,7 @@ __device__ __forceinline__ void loadW(const __nv_bfloat16 *p, float (&o)[WC]) {
 // PRE: the segment pre-pass (transfer and adjoint roles only, 3 CTAs per SM);
 // otherwise the gradient pass.
 template <typename TA, bool PRE>
-__global__ void __launch_bounds__(BT, PRE ? 3 : 1) backward_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(BT, PRE ? 3 : 2) backward_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int unit = blockIdx.x, s = blockIdx.z;
     const int n = unit / a.H, h = unit % a.H;

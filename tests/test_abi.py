@@ -211,8 +211,8 @@ def test_backward_host_checks():
 
     d = _desc()
     need = L.kda_prefill_backward_workspace_size(ctypes.byref(d))
-    # the state at every 8-token block start: [T/8 + N blocks][H][ceil(dv/8)][dk][8] fp32
-    blocks = d.total_tokens // 8 + d.num_seqs
+    # the state at every 4-token block start: [T/4 + N blocks][H][ceil(dv/8)][dk][8] fp32
+    blocks = d.total_tokens // 4 + d.num_seqs
     assert need == blocks * d.num_heads * ((d.dv + 7) // 8) * d.dk * 8 * 4
     # segments: + A_s [dk][dk] and B_s, B^_s, X_s, Y_s [dk][dv] per (sequence, head, segment)
     d4 = _desc(num_segments=4)
