@@ -639,59 +639,89 @@ __global__ void __launch_bounds__(BT, PRE ? 3 : 2) backward_kernel(const BwdArgs
 // segment's linear map is the transpose of its transfer matrix: each token's
 // adjoint step Diag(alpha)(I - beta k k^T) is the transpose of its forward map
 // (I - beta k k^T) Diag(alpha)).  grid (N*H, ceil(dv / 32), 2): z = 0 the forward
-// scan, z = 1 the adjoint scan; thread r keeps row r of a 32-column block.
-constexpr int SC_T = 128;
+// scan, z = 1 the adjoint scan.  Thread (r, g) keeps row r, columns 8g .. 8g + 7
+// of a 32-column block; the next step's A is loaded into the other shared buffer
+// while the current step's products run (A does not depend on the scan).
+constexpr int SC_T = 512;
+constexpr int SC_PER = 32;  // A elements per thread and step: 128 x 128 / 512
 __global__ void __launch_bounds__(SC_T) bwd_scan_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int unit = blockIdx.x, c0 = blockIdx.y * 32, adj = blockIdx.z;
-    const int dk = a.dk, dv = a.dv, Sg = a.Sg, r = threadIdx.x;
+    const int dk = a.dk, dv = a.dv, Sg = a.Sg;
+    const int r = threadIdx.x & 127, g8 = 8 * (threadIdx.x >> 7);
     const int nc = min(32, dv - c0);
-    float *As = sm;                 // [dk][dk + 1]: A_s, padded against bank conflicts
-    float *Z = sm + dk * (dk + 1);  // [dk][32]: the running matrix
+    const int ald = dk + 1;             // padded rows against bank conflicts
+    auto Abuf = [&](int i) { return sm + i * dk * ald; };  // two A buffers
+    float *Z = sm + 2 * dk * ald;       // [dk][32]: the running matrix
     const size_t base = (size_t)unit * Sg * dk;  // row 0 of segment 0
     const float *init = adj ? a.dSF : a.S0;
     float *outm = adj ? a.Y : a.X;
-    float z[32];
+    const bool row = r < dk;
+    float z[8];
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-        z[j] = (init && r < dk && j < nc) ? init[((size_t)unit * dk + r) * dv + c0 + j] : 0.f;
-    if (r < dk) {
-        float *o = outm + (base + (size_t)(adj ? Sg - 1 : 0) * dk + r) * dv + c0;
+    for (int j = 0; j < 8; ++j) {
+        const int c = g8 + j;
+        z[j] = (init && row && c < nc) ? init[((size_t)unit * dk + r) * dv + c0 + c] : 0.f;
+    }
+    auto store_z = [&](int seg) {
+        if (!row) return;
+        float *o = outm + (base + (size_t)seg * dk + r) * dv + c0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < nc) o[j] = z[j];
+        for (int j = 0; j < 8; ++j)
+            if (g8 + j < nc) o[g8 + j] = z[j];
+    };
+    store_z(adj ? Sg - 1 : 0);
+    auto seg_of = [&](int step) { return adj ? Sg - 1 - step : step; };  // the map applied
+    float pre[SC_PER];
+    auto fetch = [&](int step) {  // this thread's share of A_{seg_of(step)}
+        const float *A = a.TA + (base + (size_t)seg_of(step) * dk) * dk;
+#pragma unroll
+        for (int i = 0; i < SC_PER; ++i) {
+            const int e = threadIdx.x + i * SC_T;
+            pre[i] = e < dk * dk ? A[e] : 0.f;
+        }
+    };
+    auto put = [&](float *As) {
+#pragma unroll
+        for (int i = 0; i < SC_PER; ++i) {
+            const int e = threadIdx.x + i * SC_T;
+            if (e < dk * dk) As[(e / dk) * ald + e % dk] = pre[i];
+        }
+    };
+    if (Sg > 1) {
+        fetch(0);
+        put(Abuf(0));
     }
     for (int step = 0; step < Sg - 1; ++step) {
-        const int sa = adj ? Sg - 1 - step : step;  // the segment whose map is applied
-        __syncthreads();  // the previous step's readers are done
-        const float *A = a.TA + (base + (size_t)sa * dk) * dk;
-        for (int e = r; e < dk * dk; e += SC_T) As[(e / dk) * (dk + 1) + e % dk] = A[e];
-        if (r < dk) {
+        const int sa = seg_of(step);
+        const float *As = Abuf(step & 1);
+        if (row) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) Z[r * 32 + j] = z[j];
+            for (int j = 0; j < 8; ++j) Z[r * 32 + g8 + j] = z[j];
         }
-        __syncthreads();
-        if (r < dk) {
+        __syncthreads();  // A_sa and Z in place
+        if (step + 1 < Sg - 1) fetch(step + 1);
+        if (row) {
             const float *Bm = (adj ? a.TBh : a.TB) + (base + (size_t)sa * dk + r) * dv + c0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = j < nc ? Bm[j] : 0.f;
+            for (int j = 0; j < 8; ++j) z[j] = g8 + j < nc ? Bm[g8 + j] : 0.f;
             for (int kk = 0; kk < dk; ++kk) {
-                const float av = adj ? As[kk * (dk + 1) + r] : As[r * (dk + 1) + kk];
-                const float4 *zr = (const float4 *)(Z + kk * 32);
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const float4 zz = zr[x];
-                    z[4 * x] = fmaf(av, zz.x, z[4 * x]);
-                    z[4 * x + 1] = fmaf(av, zz.y, z[4 * x + 1]);
-                    z[4 * x + 2] = fmaf(av, zz.z, z[4 * x + 2]);
-                    z[4 * x + 3] = fmaf(av, zz.w, z[4 * x + 3]);
-                }
+                const float av = adj ? As[kk * ald + r] : As[r * ald + kk];
+                const float4 z0 = *(const float4 *)(Z + kk * 32 + g8);
+                const float4 z1 = *(const float4 *)(Z + kk * 32 + g8 + 4);
+                z[0] = fmaf(av, z0.x, z[0]);
+                z[1] = fmaf(av, z0.y, z[1]);
+                z[2] = fmaf(av, z0.z, z[2]);
+                z[3] = fmaf(av, z0.w, z[3]);
+                z[4] = fmaf(av, z1.x, z[4]);
+                z[5] = fmaf(av, z1.y, z[5]);
+                z[6] = fmaf(av, z1.z, z[6]);
+                z[7] = fmaf(av, z1.w, z[7]);
             }
-            float *o = outm + (base + (size_t)(adj ? sa - 1 : sa + 1) * dk + r) * dv + c0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (j < nc) o[j] = z[j];
+            store_z(adj ? sa - 1 : sa + 1);
         }
+        __syncthreads();  // Z and this A read by everyone
+        if (step + 1 < Sg - 1) put(Abuf((step + 1) & 1));
     }
 }
 
@@ -772,7 +802,7 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
                       true)) != cudaSuccess)
             return e;
         // scans: every segment's start state and end adjoint
-        const size_t ssm = (size_t)(p.dk * (p.dk + 1) + p.dk * 32) * sizeof(float);
+        const size_t ssm = (size_t)(2 * p.dk * (p.dk + 1) + p.dk * 32) * sizeof(float);
         if ((e = set_max_dynamic_smem((const void *)bwd_scan_kernel, (int)ssm)) != cudaSuccess)
             return e;
         bwd_scan_kernel<<<dim3((unsigned)(p.N * p.H), (unsigned)((p.dv + 31) / 32), 2), SC_T, ssm,
