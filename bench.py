@@ -358,6 +358,7 @@ def run_ours(args):
                                       dist, world, peaks, rank)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(x, N, H)
+        result["backward"]["cpu_baseline"] = cpu_baseline_backward(x, H)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:
@@ -612,6 +613,31 @@ def cpu_baseline(x, N, H, target_s=8.0):
             "kind": "oracle",
             "sample": "%d of %d heads x %d tokens (fp64 token-by-token C oracle, %.2f s)" %
                       (heads, H, T, dt)}
+
+
+def cpu_baseline_backward(x, H, tokens=512):
+    """The oracle's backward (fp64 PyTorch autograd of the token loop, as it
+    stands) on a bounded sample of the backward leg's workload: one head, the
+    first `tokens` tokens."""
+    import numpy as np
+    import torch
+    import oracle
+    from kimi_delta_attention_18_gb300.inputs import make_backward_adjoints
+    f = lambda t: t.detach().float().cpu().double().numpy()
+    T, _, dk = x["q"].shape
+    dv = x["v"].shape[2]
+    n = min(tokens, T)
+    act = "bf16" if x["q"].dtype == torch.bfloat16 else "f32"
+    d_out, d_sf = make_backward_adjoints(T, 1, H, dk, dv, act, seed=7)
+    sl = lambda a: a[:n, :1]
+    t0 = time.perf_counter()
+    oracle.kda_backward(*(sl(f(x[m])) for m in ("q", "k", "v", "g", "beta")), None,
+                        np.array([0, n], dtype=np.int32), sl(f(d_out)), f(d_sf)[:, :1])
+    dt = time.perf_counter() - t0
+    return {"value": round(n / H / dt, 2), "unit": "tokens/s", "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": "1 of %d heads x %d tokens (fp64 autograd of the token loop, %.2f s)" %
+                      (H, n, dt)}
 
 
 # ---------------------------------------------------------------------------
