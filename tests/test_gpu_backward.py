@@ -76,6 +76,8 @@ def test_backward_matches_oracle(act, dk, dv, lengths, slow):
     ("bf16", 128, [250, 90], 4),
     ("bf16", 128, [250, 90], 0),    # the library's choice
     ("bf16", 60, [100, 45], 3),     # plain-load producer
+    ("f32", 16, [40, 5, 0], 8),     # more segments than 16-token chunks: empty segments
+    ("f32", 32, [1500, 260], 64),   # the largest split
 ])
 def test_backward_segments_match_oracle(act, d, lengths, nseg):
     """The segment split (per-segment transfer matrices, zero-start states and
