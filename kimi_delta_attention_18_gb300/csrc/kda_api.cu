@@ -196,7 +196,6 @@ kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, con
     // the fused gate prologue runs in the tensor-core kernels only
     if (gate && !(desc->act_dtype == KDA_DTYPE_BF16 && desc->dk == 128 && desc->dv == 128))
         return KDA_ERR_UNSUPPORTED;
-    if (rc != KDA_OK) return rc;
     if (desc->num_seqs == 0) return KDA_OK;
     if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
     if (desc->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out))
