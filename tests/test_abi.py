@@ -232,3 +232,11 @@ def test_backward_host_checks():
     assert call(d, ws=0x40000, ws_len=need, cu=None) == INVALID
     assert call(_desc(num_seqs=0)) == OK  # nothing to do
     assert call(_desc(dk=256)) == UNSUPPORTED
+
+
+def test_autograd_function_has_no_cpu_fallback():
+    import torch
+    from kimi_delta_attention_18_gb300.autograd import kda_prefill
+    q = torch.zeros(16, 1, 16)
+    with pytest.raises((ValueError, RuntimeError)):
+        kda_prefill(q, q, q, q, torch.zeros(16, 1))

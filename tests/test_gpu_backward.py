@@ -156,3 +156,27 @@ def test_backward_unaligned_inputs_take_the_plain_path():
     ref = _oracle(x, d_out, d_sf)
     for name, a, b in zip(NAMES, got, ref):
         assert rel_err(_np(a), b) <= TOL, name
+
+
+@pytest.mark.parametrize("act,d", [("f32", 32), ("bf16", 128)])
+def test_autograd_function_gradients(act, d):
+    """kda_prefill as a torch.autograd.Function: .grad of every input after
+    loss = <d_out, o> + <d_S_final, S_final> against the oracle (BF16 inputs get
+    BF16 gradients, so their bound is the BF16 one)."""
+    from kimi_delta_attention_18_gb300.autograd import kda_prefill
+    lengths = [90, 41]
+    H = 2
+    x = make_prefill_inputs(lengths, H, d, d, act, s0_std=1.0, seed=43, slow_decay=True)
+    d_out, d_sf = make_backward_adjoints(sum(lengths), 2, H, d, d, act, seed=44)
+    leaves = {n: x[n].cuda().requires_grad_(True) for n in ("q", "k", "v", "g", "beta", "S0")}
+    o, SF = kda_prefill(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"],
+                        leaves["S0"], x["cu_seqlens"].cuda())
+    loss = (o.float() * d_out.cuda().float()).sum() + (SF * d_sf.cuda()).sum()
+    loss.backward()
+    torch.cuda.synchronize()
+    ref = _oracle(x, d_out, d_sf)
+    tol = 1e-4 if act == "f32" else 2e-2
+    for name, leaf, b in zip(NAMES, ("q", "k", "v", "g", "beta", "S0"), ref):
+        got = leaves[leaf].grad
+        assert got.dtype == leaves[leaf].dtype
+        assert rel_err(_np(got), b) <= tol, (name, rel_err(_np(got), b))
