@@ -15,19 +15,28 @@
 //     dS_prev = Diag(alpha) dM
 // and at the sequence start dS0 = dS.
 //
-// Columns of S and dS evolve independently (every step mixes rows only).  One
-// CTA takes (sequence, head, 32 value columns): four consumer warps own 8
-// columns each and all dk <= 128 rows (4 rows per lane), so the column sums u and
-// w of a token stay inside a warp (shuffles, no block barrier).  A producer warp
-// stages every 4-token block's inputs (g, k, q, v, d_out, beta) into a
-// double-buffered shared-memory ring ahead of use, by bulk copies where the rows
-// allow.  A forward pass keeps the state at every block start in the workspace;
-// the reverse pass recomputes the block's token states into shared memory and
-// walks them backwards.  dv and dS0 are column-local and written directly; the
-// row sums dq, dk, dg and dbeta are summed over the consumer warps in shared
-// memory once per block and added to zeroed fp32 outputs with global atomics
-// (one per column block).  fp32 throughout: a token-level
-// implementation (the chunked tensor-core form of the backward is not built).
+// Columns of S and dS evolve independently (every step mixes rows only).  The
+// gradient pass takes (sequence, head, segment, 32 value columns) per CTA: four
+// consumer warps own 8 columns each and all dk <= 128 rows (4 rows per lane), so
+// the column sums u and w of a token stay inside a warp (shuffles, no block
+// barrier).  A producer warp stages every 4-token block's inputs (g, k, q, v,
+// d_out, beta) into a 3-slot shared-memory ring ahead of use, by bulk copies
+// where the rows allow, and forms alpha = e^g there once.  A forward pass keeps
+// the state at every block start in the workspace; the reverse pass recomputes
+// the block's token states into shared memory and walks them backwards.  dv and
+// dS0 are column-local and written directly; the row sums dq, dk, dg and dbeta
+// are summed over the consumer warps in shared memory once per block and added
+// to zeroed fp32 outputs with global atomics.
+//
+// Segments: the adjoint step dS_prev = Diag(alpha)(I - beta k k^T)(dS + q do^T)
+// is linear, and Diag(alpha)(I - beta k k^T) is the transpose of the forward
+// token map (I - beta k k^T) Diag(alpha).  So a segment's adjoint map is A_s^T,
+// A_s its transfer matrix, and its zero-end adjoint needs no forward state.  A
+// pre-pass computes A_s, the zero-start state B_s and the zero-end adjoint of
+// every segment in parallel; bwd_scan_kernel forms every segment's start state
+// and end adjoint in fp32; the gradient pass then runs all segments at once.
+// fp32 throughout: a token-level implementation (the chunked tensor-core form
+// of the backward is not built).
 #include <string.h>
 
 #include "kda_internal.cuh"
