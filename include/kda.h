@@ -310,7 +310,10 @@ kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_desc_t *desc, const v
  * adjoint first, then fp32 scans for every segment's start state and end
  * adjoint (the adjoint map of a segment is A^T), then the gradient pass per
  * segment.  Workspace: kda_prefill_backward_workspace_size(desc) (0 on invalid
- * arguments), 16-byte aligned.  Pointers 4-byte aligned;
+ * arguments), 16-byte aligned: about dk * dv fp32 per head and 4 tokens (16 KB
+ * per head-token at d = 128), so a batch too long for device memory is
+ * differentiated piece by piece, last piece first: each piece from its start
+ * state (S0) with d_S_final = the next piece's dS0.  Pointers 4-byte aligned;
  * KDA_ERR_INVALID_ARG on a missing or misaligned pointer, KDA_ERR_WORKSPACE on a
  * short workspace, KDA_ERR_UNSUPPORTED as kda_prefill_chunked.
  */
