@@ -180,3 +180,29 @@ def test_autograd_function_gradients(act, d):
         got = leaves[leaf].grad
         assert got.dtype == leaves[leaf].dtype
         assert rel_err(_np(got), b) <= tol, (name, rel_err(_np(got), b))
+
+
+def test_backward_piecewise_equals_whole():
+    """A sequence differentiated in two pieces, last piece first, each from its
+    start state with d_S_final = the next piece's dS0 (the documented use for
+    batches whose workspace does not fit), against the oracle on the whole."""
+    L, cut, H, d = 300, 130, 2, 32
+    x = make_prefill_inputs([L], H, d, d, "f32", s0_std=1.0, seed=45, slow_decay=True)
+    d_out, d_sf = make_backward_adjoints(L, 1, H, d, d, "f32", seed=46)
+    c = {n: x[n].cuda() for n in ("q", "k", "v", "g", "beta", "S0")}
+    dO, dSF = d_out.cuda(), d_sf.cuda()
+    one = lambda n: torch.tensor([0, n], dtype=torch.int32, device="cuda")
+    p1 = {n: t[:cut].contiguous() for n, t in c.items() if n != "S0"}
+    p2 = {n: t[cut:].contiguous() for n, t in c.items() if n != "S0"}
+    _, S_mid = kda.prefill_chunked(p1["q"], p1["k"], p1["v"], p1["g"], p1["beta"], c["S0"],
+                                   one(cut))
+    g2 = kda.prefill_backward(p2["q"], p2["k"], p2["v"], p2["g"], p2["beta"], S_mid,
+                              one(L - cut), dO[cut:].contiguous(), dSF)
+    g1 = kda.prefill_backward(p1["q"], p1["k"], p1["v"], p1["g"], p1["beta"], c["S0"], one(cut),
+                              dO[:cut].contiguous(), g2[5])
+    torch.cuda.synchronize()
+    ref = _oracle(x, d_out, d_sf)
+    for i, name in enumerate(NAMES[:5]):
+        got = torch.cat([g1[i], g2[i]], dim=0)
+        assert rel_err(_np(got), ref[i]) <= TOL, name
+    assert rel_err(_np(g1[5]), ref[5]) <= TOL
