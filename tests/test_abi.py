@@ -223,6 +223,17 @@ def test_backward_host_checks():
     assert L.kda_prefill_backward_num_segments(ctypes.byref(d4)) == 4
     assert L.kda_prefill_backward_num_segments(ctypes.byref(_desc(num_segments=500))) == 64
     assert L.kda_prefill_backward_num_segments(ctypes.byref(_desc(chunk=32))) == 0
+    # the library's split for B=1 H=8 T=4096 d=128: 32 (head, 32-column) units and two
+    # gradient-pass CTAs per SM on 148-152 SMs -> 9 segments (at most T / 256 = 16)
+    bench = _desc(num_seqs=1, total_tokens=4096, num_heads=8, dk=128, dv=128, act_dtype=1,
+                  num_segments=0)
+    assert L.kda_prefill_backward_num_segments(ctypes.byref(bench)) == 9
+    short = _desc(num_seqs=1, total_tokens=512, num_heads=8, dk=128, dv=128, act_dtype=1,
+                  num_segments=0)
+    assert L.kda_prefill_backward_num_segments(ctypes.byref(short)) == 2  # 512 / 256
+    many = _desc(num_seqs=64, total_tokens=64 * 512, num_heads=8, dk=128, dv=128,
+                 act_dtype=1, num_segments=0)
+    assert L.kda_prefill_backward_num_segments(ctypes.byref(many)) == 1  # units fill the SMs
     assert call(d) == WORKSPACE
     assert call(d, ws=0x40000, ws_len=need - 1) == WORKSPACE
     assert call(d, ws=0x40008, ws_len=need) == WORKSPACE       # not 16-byte aligned

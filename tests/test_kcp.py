@@ -133,3 +133,25 @@ def test_default_steps_need_the_gpu_library():
     f = {n: x[n].float() for n in ("k", "v", "g", "beta")}
     with pytest.raises((ValueError, RuntimeError, OSError)):
         kcp.local_pairs(f["k"], f["v"], f["g"], f["beta"], x["cu_seqlens"], 2, 0)
+
+
+def test_check_catches_a_wrong_start_state():
+    """A rank that runs its segment from its neighbour's start state (a plausible
+    off-by-one in the scan bookkeeping, planted in the oracle-backed steps) fails
+    the comparison."""
+    x = _inputs()
+    good = oracle_ops()
+
+    def shifted_segment(q, k, v, g, beta, starts, cu, W, r):  # segment r from start r - 1
+        return good.segment(q, k, v, g, beta, torch.roll(starts, 1, dims=2), cu, W, r)
+
+    bad = kcp.KCPOps(good.transfer, good.compose, shifted_segment)
+    W = 3
+    args = (x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"])
+    pairs = [kcp.local_pairs(*args, W, r, bad) for r in range(W)]
+    A_all = torch.stack([p[0] for p in pairs], dim=2)
+    B_all = torch.stack([p[1] for p in pairs], dim=2)
+    res = [kcp.finish(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["cu_seqlens"], W, r,
+                      A_all, B_all, bad) for r in range(W)]
+    with pytest.raises(AssertionError):
+        _check(x, [o for o, _ in res], [f for _, f in res], W)
