@@ -546,9 +546,25 @@ def run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world):
     e1.record(main)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    # the bound: the step's input bytes as one pinned host-to-device copy (the
+    # link, not the kernels, limits this leg)
+    flat_h = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    flat_d = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        flat_d.copy_(flat_h, non_blocking=True)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(main)
+    for _ in range(10):
+        flat_d.copy_(flat_h, non_blocking=True)
+    c1.record(main)
+    torch.cuda.synchronize()
+    link_gbs = h2d * 10 / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    step_ms = ms / args.e2e_steps
     return {"value": round(T * args.e2e_steps * world / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / args.e2e_steps, 4), "streams": nstreams}
+            "ms_per_step": round(step_ms, 4), "streams": nstreams,
+            "h2d_link_gbs": round(link_gbs, 1),
+            "frac_of_link": round(h2d / (step_ms * 1e-3) / 1e9 / link_gbs, 3)}
 
 
 def run_decode(args, kda, make_decode_inputs, w, dev, dist, world, peaks, rank):
