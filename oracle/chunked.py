@@ -1,9 +1,10 @@
 """Chunked (WY / UT-transform) form of the KDA recurrence, fp64 numpy.
 
 TEST INFRASTRUCTURE ONLY: a second, independent way of computing what
-``oracle.kda_forward`` computes, used by the self-checks to pin the algebra that
-a chunked implementation relies on.  It is never the reference the GPU path is
-compared with (that is the token-by-token oracle).
+``oracle.kda_forward`` and ``oracle.kda_backward`` compute, used by the
+self-checks to pin the algebra that a chunked implementation relies on (forward
+and adjoint).  It is never the reference the GPU path is compared with (that is
+the token-by-token oracle).
 
 The chunk size is free (the pages use 16-token blocks so that the in-block
 exponent factors stay inside BF16 range: Kimi K3 technical-report digest,
@@ -74,3 +75,95 @@ def kda_forward_chunked(q, k, v, g, beta, S0=None, cu_seqlens=None, chunk=16):
                 out[t0:t1, h] = O
             SF[n, h] = S
     return out, SF
+
+
+def chunk_step_backward(S, q, k, v, g, beta, dO, dS_next):
+    """Adjoint of ``chunk_step`` for one head and one chunk: given the chunk's start
+    state S and the adjoints dO [C, dv] of its outputs and dS_next [dk, dv] of its
+    end state, returns (dS, dq, dk, dv, dg, dbeta) — the same gradients the
+    token-by-token recurrence gives, through the chunked form's own algebra:
+
+        dU  = Mq^T dO + Kb dS'                   R = V - Kh S,  U = T R
+        dT  = dU R^T,  dR = T^T dU,  dV = dR
+        T = Y Diag(beta), Y = (I + Diag(beta) L)^{-1}:
+            dbeta_j += sum_i dT_ij Y_ij,   dMb = -Y^T (dT Diag(beta)) Y^T,
+            dbeta_i += sum_j dMb_ij L_ij,   dL = Diag(beta) dMb (strictly lower)
+        dMq = lower(dO U^T);  Kh, Kt, Qh, Kb, e^{Gamma_C} -> K, Q, Gamma;
+        dg = reverse cumulative sum of dGamma over the chunk.
+    """
+    C = k.shape[0]
+    Gam = np.cumsum(g, axis=0)
+    Ep, Em = np.exp(Gam), np.exp(-Gam)
+    Eb = np.exp(Gam[-1][None, :] - Gam)
+    eC = np.exp(Gam[-1])
+    Kh, Kt, Qh, Kb = k * Ep, k * Em, q * Ep, k * Eb
+    L = np.tril(Kh @ Kt.T, -1)
+    Mq = np.tril(Qh @ Kt.T, 0)
+    Y = np.linalg.inv(np.eye(C) + beta[:, None] * L)
+    T = Y * beta[None, :]
+    R = v - Kh @ S
+    U = T @ R
+    # O = Qh S + Mq U,  S' = Diag(eC) S + Kb^T U
+    dU = Mq.T @ dO + Kb @ dS_next
+    dS = Qh.T @ dO + eC[:, None] * dS_next
+    dQh = dO @ S.T
+    dMq = np.tril(dO @ U.T, 0)
+    dKb = U @ dS_next.T
+    deC = np.sum(dS_next * S, axis=1)
+    # U = T R, R = V - Kh S
+    dT = dU @ R.T
+    dR = T.T @ dU
+    dv_ = dR
+    dKh = -dR @ S.T
+    dS = dS - Kh.T @ dR
+    # T = Y Diag(beta), Y = (I + Diag(beta) L)^{-1}
+    dbeta = np.sum(dT * Y, axis=0)
+    dMb = -Y.T @ (dT * beta[None, :]) @ Y.T
+    dbeta = dbeta + np.sum(dMb * L, axis=1)
+    dL = np.tril(beta[:, None] * dMb, -1)
+    # L = strict_lower(Kh Kt^T), Mq = lower(Qh Kt^T)
+    dKh = dKh + dL @ Kt
+    dKt = dL.T @ Kh + dMq.T @ Qh
+    dQh = dQh + dMq @ Kt
+    # to K, Q and Gamma
+    dk_ = dKh * Ep + dKt * Em + dKb * Eb
+    dq_ = dQh * Ep
+    dGam = dKh * Kh - dKt * Kt + dQh * Qh - dKb * Kb
+    dGam[-1] += np.sum(dKb * Kb, axis=0) + deC * eC
+    dg_ = np.cumsum(dGam[::-1], axis=0)[::-1]
+    return dS, dq_, dk_, dv_, dg_, dbeta
+
+
+def kda_backward_chunked(q, k, v, g, beta, S0, cu_seqlens, d_out, d_S_final=None, chunk=16):
+    """Same contract as ``oracle.kda_backward`` (fp64), computed chunk by chunk: a
+    forward pass keeping each chunk's start state, then ``chunk_step_backward``
+    from the last chunk to the first."""
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64); g = np.asarray(g, np.float64)
+    beta = np.asarray(beta, np.float64); d_out = np.asarray(d_out, np.float64)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    cu = np.asarray(cu_seqlens, np.int64)
+    N = len(cu) - 1
+    grads = [np.zeros((T, H, dk)), np.zeros((T, H, dk)), np.zeros((T, H, dv)),
+             np.zeros((T, H, dk)), np.zeros((T, H))]
+    dS0 = np.zeros((N, H, dk, dv))
+    for n in range(N):
+        for h in range(H):
+            S = np.zeros((dk, dv)) if S0 is None else np.array(S0[n, h], np.float64)
+            spans, starts = [], []
+            for t0 in range(int(cu[n]), int(cu[n + 1]), chunk):
+                t1 = min(t0 + chunk, int(cu[n + 1]))
+                spans.append((t0, t1))
+                starts.append(S)
+                _, S = chunk_step(S, q[t0:t1, h], k[t0:t1, h], v[t0:t1, h], g[t0:t1, h],
+                                  beta[t0:t1, h])
+            dS = np.zeros((dk, dv)) if d_S_final is None else np.array(d_S_final[n, h])
+            for (t0, t1), Sc in zip(spans[::-1], starts[::-1]):
+                dS, dq_, dk_, dv_, dg_, db_ = chunk_step_backward(
+                    Sc, q[t0:t1, h], k[t0:t1, h], v[t0:t1, h], g[t0:t1, h], beta[t0:t1, h],
+                    d_out[t0:t1, h], dS)
+                for arr, val in zip(grads, (dq_, dk_, dv_, dg_, db_)):
+                    arr[t0:t1, h] = val
+            dS0[n, h] = dS
+    return (*grads, dS0)

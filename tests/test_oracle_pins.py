@@ -404,3 +404,24 @@ def test_backward_forward_matches_and_finite_differences():
             flat[i] = keep
             fd[i] = (up - dn) / (2 * eps)
         assert np.allclose(grad.reshape(-1), fd, rtol=1e-6, atol=1e-7), which
+
+
+@pytest.mark.parametrize("chunk", [1, 5, 16])
+@pytest.mark.parametrize("slow", [False, True])
+def test_chunked_backward_equals_token_backward(chunk, slow):
+    """The chunk-level adjoint (oracle/chunked.py: through the UT transform's
+    inverse, the masked in-chunk products and the cumulative log-decay) gives the
+    autograd gradients of the token recurrence, for any chunk size, ragged
+    sequences included."""
+    from oracle import chunked
+    from kimi_delta_attention_18_gb300.inputs import make_backward_adjoints, make_prefill_inputs
+    lengths = [37, 20, 0, 16]
+    x = make_prefill_inputs(lengths, 2, 6, 5, "f32", seed=61, s0_std=1.0, slow_decay=slow)
+    d_out, d_sf = make_backward_adjoints(sum(lengths), len(lengths), 2, 6, 5, "f32", seed=62)
+    f = lambda t: t.double().numpy()
+    args = [f(x[n]) for n in ("q", "k", "v", "g", "beta", "S0")]
+    cu = x["cu_seqlens"].numpy()
+    ref = oracle.kda_backward(*args, cu, f(d_out), f(d_sf))
+    got = chunked.kda_backward_chunked(*args, cu, f(d_out), f(d_sf), chunk=chunk)
+    for a, b in zip(got, ref):
+        assert np.abs(a - b).max() <= 1e-12 * max(np.abs(b).max(), 1e-300)
