@@ -12,7 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__)
 sys.path.insert(0, ROOT)
 
 import oracle  # noqa: E402
-from kimi_delta_attention_18_gb300.inputs import WORKLOADS, make_prefill_inputs  # noqa: E402
+from kimi_delta_attention_18_gb300.inputs import (WORKLOADS, make_backward_adjoints,  # noqa: E402
+                                                  make_prefill_inputs)
 
 TOKENS = [0, 1, 15, 16, 31, 47, 63]
 
@@ -40,6 +41,44 @@ def main():
             for i in range(16):
                 for j in range(16):
                     fh.write("S %d %d %d %.17g\n" % (h, i, j, S[0, h, i, j]))
+    print("wrote", path)
+    backward(w, x, f)
+
+
+def backward(w, x, f):
+    """Gradients of the same problem for d_out and d_S_final drawn with seed 1."""
+    T, H, d = sum(w["lengths"]), w["H"], w["dk"]
+    d_out, d_sf = make_backward_adjoints(T, 1, H, d, d, w["act"], seed=1)
+    grads = oracle.kda_backward(f(x["q"]), f(x["k"]), f(x["v"]), f(x["g"]), f(x["beta"]),
+                                np.zeros((1, H, d, d)), x["cu_seqlens"].numpy(), f(d_out),
+                                f(d_sf))
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "kda_bwd_f32_h2_t64_d16.txt")
+    names = ("dq", "dk", "dv", "dg", "dbeta")
+    header = [
+        "KDA backward, fp32 inputs, B=1 H=2 T=64 dk=dv=16, S0=0, seed 0; adjoints",
+        "d_out, d_S_final from make_backward_adjoints(seed=1).  Written by",
+        "tests/golden/make_golden.py from the fp64 oracle only: gradients of",
+        "<d_out, o> + <d_S_final, S_final> for the recurrence of 'Kimi K3",
+        "Architecture Explained', section 3.",
+        "lines: 'name t h j value' (dbeta: j = 0) for t in %s, then" % TOKENS,
+        "'dS0 h i j value'.",
+    ]
+    with open(path, "w") as fh:
+        for line in header:
+            fh.write("# " + line + "\n")
+        for name, arr in zip(names, grads[:5]):
+            for t in TOKENS:
+                for h in range(H):
+                    if arr.ndim == 2:
+                        fh.write("%s %d %d 0 %.17g\n" % (name, t, h, arr[t, h]))
+                    else:
+                        for j in range(arr.shape[2]):
+                            fh.write("%s %d %d %d %.17g\n" % (name, t, h, j, arr[t, h, j]))
+        for h in range(H):
+            for i in range(d):
+                for j in range(d):
+                    fh.write("dS0 %d %d %d %.17g\n" % (h, i, j, grads[5][0, h, i, j]))
     print("wrote", path)
 
 
