@@ -124,6 +124,25 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
                                  int32_t *dev_status, void *stream);
 
 /*
+ * kda_prefill_chunked with stage timing, for measurement: identical launches
+ * and results, and in addition records stage_events[0] (cudaEvent_t, created by
+ * the caller) on the stream before the first launch, stage_events[1] after the
+ * transfer pass (or the single output pass when the split is one segment),
+ * stage_events[2] after the segment scan and stage_events[3] after the last
+ * launch (with one segment 1, 2 and 3 follow each other).  Recording an event
+ * between two launches keeps the next kernel from starting while the previous
+ * one drains, so the call can take slightly longer than kda_prefill_chunked.
+ * KDA_ERR_INVALID_ARG if stage_events or one of its four entries is NULL.
+ */
+kda_status_t kda_prefill_chunked_timed(const kda_prefill_desc_t *desc, const void *q,
+                                       const void *k, const void *v, const float *g,
+                                       const float *beta, const float *S0,
+                                       const int32_t *cu_seqlens, void *out, float *S_final,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *const *stage_events,
+                                       void *stream);
+
+/*
  * Fused gate prologue (digest, section 2.1 (1): g = -5 sigmoid(x), so g in
  * (-5, 0)): kda_prefill_chunked from the pre-activations, so the gates and the
  * normalised q, k are never written to memory.  The kernels take
@@ -175,11 +194,14 @@ kda_status_t kda_prefill_chunked_ckpt(const kda_prefill_desc_t *desc, const void
  * with q, k [batch, H, dk], v, out [batch, H, dv] in act_dtype, g [batch, H,
  * dk] and beta [batch, H] fp32.  Streams each state through once.  dv must be
  * a multiple of 4 and S_inout 16-byte aligned (the others 4-byte aligned).
+ * dev_status (device int32 or NULL, 4-byte aligned): KDA_ERR_TIMEOUT if a
+ * bounded device-side wait gave up, in which case some states may not have
+ * been stepped (S_inout is then partly old, partly new).
  */
 kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv,
                              int32_t act_dtype, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, float *S_inout, void *out,
-                             void *stream);
+                             int32_t *dev_status, void *stream);
 
 /*
  * Transfer pass of the context-parallel split (digest, section 2.4 (1)): with
@@ -221,11 +243,15 @@ kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begi
  * [units, segments, 128 * 128] BF16, 16-byte aligned, each start state rounded
  * to BF16 and laid out as the B operand of kda_prefill_combine's tensor-core
  * product (an internal layout: only kda_prefill_combine reads it).
+ *
+ * dev_status (device int32 or NULL, 4-byte aligned): KDA_ERR_TIMEOUT if a
+ * bounded device-side wait of the scan gave up (its outputs are then
+ * incomplete).
  */
 kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int32_t dv,
                                const float *transfer, const float *zero_init_state,
                                const float *S0, float *seg_init_states, float *S_final,
-                               void *start_images, void *stream);
+                               void *start_images, int32_t *dev_status, void *stream);
 
 /*
  * Output correction of the context-parallel split: for every token t of the

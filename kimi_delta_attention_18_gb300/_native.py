@@ -53,6 +53,9 @@ def lib():
             L.kda_prefill_chunked.restype = ctypes.c_int
             L.kda_prefill_chunked.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 10 + \
                 [ctypes.c_size_t, _P, _P]
+            L.kda_prefill_chunked_timed.restype = ctypes.c_int
+            L.kda_prefill_chunked_timed.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 10 + \
+                [ctypes.c_size_t, _P, _P, _P]
             L.kda_prefill_chunked_gated.restype = ctypes.c_int
             L.kda_prefill_chunked_gated.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 10 + \
                 [ctypes.c_size_t, _P, _P]
@@ -73,13 +76,13 @@ def lib():
             L.kda_prefill_chunked_noalloc.restype = ctypes.c_int
             L.kda_prefill_chunked_noalloc.argtypes = [ctypes.POINTER(PrefillDesc)] + [_P] * 11
             L.kda_decode_step.restype = ctypes.c_int
-            L.kda_decode_step.argtypes = [_I] * 5 + [_P] * 8
+            L.kda_decode_step.argtypes = [_I] * 5 + [_P] * 9
             L.kda_state_transfer.restype = ctypes.c_int
             L.kda_state_transfer.argtypes = [ctypes.POINTER(PrefillDesc), _I, _I] + [_P] * 12
             L.kda_prefill_combine.restype = ctypes.c_int
             L.kda_prefill_combine.argtypes = [ctypes.POINTER(PrefillDesc), _I] + [_P] * 7
             L.kda_state_compose.restype = ctypes.c_int
-            L.kda_state_compose.argtypes = [_I] * 4 + [_P] * 7
+            L.kda_state_compose.argtypes = [_I] * 4 + [_P] * 8
             L.kda_selftest_wait_timeout.restype = ctypes.c_int
             L.kda_selftest_wait_timeout.argtypes = [_I, _P, _P]
             L.kda_status_string.restype = ctypes.c_char_p
@@ -144,12 +147,14 @@ def prefill_workspace_size(desc) -> int:
 
 def prefill_chunked(q, k, v, g, beta, S0=None, cu_seqlens=None, *, num_segments=0, out=None,
                     S_final=None, want_final_state=True, workspace=None, dev_status=None,
-                    stream=None):
+                    stream=None, stage_events=None):
     """Chunked KDA prefill over packed sequences (see kda_prefill_chunked in kda.h).
 
     q, k ``[T, H, dk]`` and v ``[T, H, dv]`` (fp32 or bf16, same dtype); g ``[T, H,
     dk]`` and beta ``[T, H]`` fp32; S0 ``[N, H, dk, dv]`` fp32 or None;
     cu_seqlens int32 ``[N+1]`` (None = one sequence).  Returns ``(out, S_final)``.
+    ``stage_events`` (four ``torch.cuda.Event``) calls kda_prefill_chunked_timed
+    instead, which records them around the call's launches (measurement only).
     """
     dev = q.device
     T, H, dk = q.shape
@@ -182,11 +187,26 @@ def prefill_chunked(q, k, v, g, beta, S0=None, cu_seqlens=None, *, num_segments=
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if dev_status is not None:
         _need(dev_status, "dev_status", torch.int32, None, dev)
-    rc = lib().kda_prefill_chunked(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                   _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(out),
-                                   _ptr(S_final), _ptr(workspace), ws_len, _ptr(dev_status),
-                                   _stream(stream, dev))
-    _check("kda_prefill_chunked", rc)
+    if stage_events is None:
+        rc = lib().kda_prefill_chunked(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                       _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(out),
+                                       _ptr(S_final), _ptr(workspace), ws_len, _ptr(dev_status),
+                                       _stream(stream, dev))
+        _check("kda_prefill_chunked", rc)
+        return out, S_final
+    if len(stage_events) != 4:
+        raise ValueError("stage_events must be four torch.cuda.Event")
+    st = torch.cuda.current_stream(dev) if stream is None else stream
+    for e in stage_events:  # torch creates an event's handle at its first record
+        if not e.cuda_event:
+            e.record(st)
+    evs = (ctypes.c_void_p * 4)(*[e.cuda_event for e in stage_events])
+    rc = lib().kda_prefill_chunked_timed(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                         _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(out),
+                                         _ptr(S_final), _ptr(workspace), ws_len,
+                                         _ptr(dev_status), ctypes.cast(evs, ctypes.c_void_p),
+                                         _stream(st, dev))
+    _check("kda_prefill_chunked_timed", rc)
     return out, S_final
 
 
@@ -405,7 +425,7 @@ def prefill_segments(q, k, v, g, beta, seg_init_states, cu_seqlens, num_segments
     return out, S_final
 
 
-def decode_step(q, k, v, g, beta, S, *, out=None, stream=None):
+def decode_step(q, k, v, g, beta, S, *, out=None, dev_status=None, stream=None):
     """One decode token per sequence; updates S ``[B, H, dk, dv]`` in place and
     returns out ``[B, H, dv]`` (see kda_decode_step in kda.h)."""
     dev = S.device
@@ -422,8 +442,10 @@ def decode_step(q, k, v, g, beta, S, *, out=None, stream=None):
     if out is None:
         out = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
     _need(out, "out", q.dtype, (B, H, dv), dev)
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, None, dev)
     rc = lib().kda_decode_step(B, H, dk, dv, act, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                               _ptr(S), _ptr(out), _stream(stream, dev))
+                               _ptr(S), _ptr(out), _ptr(dev_status), _stream(stream, dev))
     _check("kda_decode_step", rc)
     return out
 
@@ -509,7 +531,8 @@ def prefill_combine(out, out_transfer, seg_init_states, cu_seqlens, *, first_seg
 
 
 def state_compose(transfer, zero_init_state, S0=None, *, seg_init_states=None, S_final=None,
-                  want_starts=True, want_final_state=True, start_images=None, stream=None):
+                  want_starts=True, want_final_state=True, start_images=None, dev_status=None,
+                  stream=None):
     """Prefix scan over segments (see kda_state_compose in kda.h): transfer ``[U, S,
     dk, dk]``, zero_init_state ``[U, S, dk, dv]``, S0 ``[U, dk, dv]`` or None.
     Returns ``(seg_init_states [U,S,dk,dv] or None, S_final [U,dk,dv] or None)``;
@@ -529,9 +552,11 @@ def state_compose(transfer, zero_init_state, S0=None, *, seg_init_states=None, S
         S_final = torch.empty((U, dk, dv), dtype=torch.float32, device=dev)
     if start_images is not None:
         _need(start_images, "start_images", torch.bfloat16, (U, Sg, dk * dv), dev)
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, None, dev)
     rc = lib().kda_state_compose(U, Sg, dk, dv, _ptr(transfer), _ptr(zero_init_state), _ptr(S0),
                                  _ptr(seg_init_states), _ptr(S_final), _ptr(start_images),
-                                 _stream(stream, dev))
+                                 _ptr(dev_status), _stream(stream, dev))
     _check("kda_state_compose", rc)
     return seg_init_states, S_final
 

@@ -28,10 +28,14 @@ kda_status_t check_desc(const kda_prefill_desc_t *d) {
     if (d->act_dtype != KDA_DTYPE_F32 && d->act_dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
     if (d->dk > kMaxDim || d->dv > kMaxDim) return KDA_ERR_UNSUPPORTED;
     if (d->num_segments > kMaxSegments) return KDA_ERR_UNSUPPORTED;
-    // Every index the kernels form must fit the int/size_t arithmetic they use.
+    // Every index the kernels form must fit the int/size_t arithmetic they use:
+    // element offsets in 64 bits, and the (sequence, head, segment) unit count
+    // (a grid dimension, formed in int) below 2^31.
     if ((long long)d->total_tokens * d->num_heads * (d->dk > d->dv ? d->dk : d->dv) >
         (1ll << 40))
         return KDA_ERR_UNSUPPORTED;
+    const long long segs = d->num_segments > 0 ? d->num_segments : 64;
+    if ((long long)d->num_seqs * d->num_heads * segs > 0x7fffffffll) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;
 }
 
@@ -190,7 +194,7 @@ kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, con
                               const int32_t *cu_seqlens, void *out, float *S_final,
                               int32_t ckpt_interval, float *ckpt, void *workspace,
                               size_t workspace_bytes, int32_t *dev_status, void *stream,
-                              int gate = 0) {
+                              int gate = 0, const cudaEvent_t *ev = nullptr) {
     kda_status_t rc = check_desc(desc);
     if (rc != KDA_OK) return rc;
     // the fused gate prologue runs in the tensor-core kernels only
@@ -224,11 +228,21 @@ kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, con
     a.ckpt = ckpt_interval > 0 ? ckpt : nullptr;
     a.gate = gate;
 
+    // ev (measurement only): ev[0] before the first launch, ev[1] after the
+    // transfer pass (or the single pass), ev[2] after the scan, ev[3] at the end.
+    auto mark = [&](int i) {
+        return ev ? cudaEventRecord(ev[i], st) : cudaSuccess;
+    };
+    if (mark(0) != cudaSuccess) return KDA_ERR_CUDA;
     if (Sg == 1) {
         a.S0 = S0;
         a.seg_count = 1;
         a.mode = MODE_OUTPUT;
-        return from_cuda(run_prefill_pass(a, st));
+        cudaError_t e = run_prefill_pass(a, st);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+        for (int i = 1; i < 4; ++i)
+            if (mark(i) != cudaSuccess) return KDA_ERR_CUDA;
+        return KDA_OK;
     }
 
     // Context-parallel split: the transfer pass runs every segment twice (from
@@ -259,7 +273,7 @@ kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, con
     if (ckpt_interval > 0)  // partial transfer matrices at the checkpoints
         t.ckpt_a = (float *)((uint8_t *)workspace + workspace_bytes_for(desc, Sg));
     cudaError_t e = run_prefill_pass(t, st);
-    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (e != cudaSuccess || mark(1) != cudaSuccess) return KDA_ERR_CUDA;
     PrefillArgs c = a;
     c.seg_begin = S0 ? 0 : 1;  // from zeros the first segment needs no correction
     c.ckpt_interval = 0;
@@ -269,10 +283,12 @@ kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, con
         combine_uses_images(c, aux, img) && ckpt_interval == 0 ? nullptr : starts;
     e = launch_compose((int)units, Sg, desc->dk, desc->dv, a_img ? nullptr : A, a_img, B, S0,
                        starts_f32, S_final, img, dev_status, st);
-    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (e != cudaSuccess || mark(2) != cudaSuccess) return KDA_ERR_CUDA;
     e = launch_combine(c, starts, aux, img, st);
-    if (e != cudaSuccess || ckpt_interval == 0) return from_cuda(e);
-    return from_cuda(launch_ckpt_fixup(t, S0, starts, max_checkpoints(desc, ckpt_interval), st));
+    if (e == cudaSuccess && ckpt_interval > 0)
+        e = launch_ckpt_fixup(t, S0, starts, max_checkpoints(desc, ckpt_interval), st);
+    if (e != cudaSuccess || mark(3) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
 }
 
 }  // namespace
@@ -286,6 +302,21 @@ kda_status_t kda_prefill_chunked(const kda_prefill_desc_t *desc, const void *q, 
                                  int32_t *dev_status, void *stream) {
     return prefill_one_call(desc, q, k, v, g, beta, S0, cu_seqlens, out, S_final, 0, nullptr,
                             workspace, workspace_bytes, dev_status, stream);
+}
+
+kda_status_t kda_prefill_chunked_timed(const kda_prefill_desc_t *desc, const void *q,
+                                       const void *k, const void *v, const float *g,
+                                       const float *beta, const float *S0,
+                                       const int32_t *cu_seqlens, void *out, float *S_final,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *const *stage_events,
+                                       void *stream) {
+    if (!stage_events) return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+        if (!stage_events[i]) return KDA_ERR_INVALID_ARG;
+    return prefill_one_call(desc, q, k, v, g, beta, S0, cu_seqlens, out, S_final, 0, nullptr,
+                            workspace, workspace_bytes, dev_status, stream, 0,
+                            (const cudaEvent_t *)stage_events);
 }
 
 kda_status_t kda_prefill_chunked_gated(const kda_prefill_desc_t *desc, const void *q,
@@ -416,7 +447,7 @@ kda_status_t kda_prefill_combine(const kda_prefill_desc_t *desc, int32_t first_s
 kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv,
                              int32_t act_dtype, const void *q, const void *k, const void *v,
                              const float *g, const float *beta, float *S_inout, void *out,
-                             void *stream) {
+                             int32_t *dev_status, void *stream) {
     if (batch < 0 || num_heads < 1 || dk < 1 || dv < 1) return KDA_ERR_INVALID_ARG;
     if (act_dtype != KDA_DTYPE_F32 && act_dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
     if (dk > kMaxDim || dv > kMaxDim || (dv & 3) != 0) return KDA_ERR_UNSUPPORTED;
@@ -429,12 +460,13 @@ kda_status_t kda_decode_step(int32_t batch, int32_t num_heads, int32_t dk, int32
         if (!p || ((uintptr_t)p & (act_align - 1u)) != 0) return KDA_ERR_INVALID_ARG;
     if (!g || !beta || !aligned4(g) || !aligned4(beta)) return KDA_ERR_INVALID_ARG;
     if (!S_inout || !aligned16(S_inout)) return KDA_ERR_INVALID_ARG;
+    if (dev_status && !aligned4(dev_status)) return KDA_ERR_INVALID_ARG;
     // dk = dv = 128 with 16-byte aligned rows: the TMA-streamed kernel; otherwise the
     // register-streamed one.
     if (decode_tma_supported(dk, dv) && aligned16(q) && aligned16(k) && aligned16(v) &&
         aligned16(g))
         return from_cuda(launch_decode_tma(batch, num_heads, act_dtype, q, k, v, g, beta,
-                                           S_inout, out, (cudaStream_t)stream));
+                                           S_inout, out, dev_status, (cudaStream_t)stream));
     return from_cuda(launch_decode(batch, num_heads, dk, dv, act_dtype, q, k, v, g, beta,
                                    S_inout, out, (cudaStream_t)stream));
 }
@@ -479,7 +511,7 @@ kda_status_t kda_state_transfer(const kda_prefill_desc_t *desc, int32_t seg_begi
 kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int32_t dv,
                                const float *transfer, const float *zero_init_state,
                                const float *S0, float *seg_init_states, float *S_final,
-                               void *start_images, void *stream) {
+                               void *start_images, int32_t *dev_status, void *stream) {
     if (units < 0 || segments < 1 || dk < 1 || dv < 1) return KDA_ERR_INVALID_ARG;
     if (dk > kMaxDim || dv > kMaxDim) return KDA_ERR_UNSUPPORTED;
     if (start_images && (dk != 128 || dv != 128)) return KDA_ERR_INVALID_ARG;
@@ -488,9 +520,10 @@ kda_status_t kda_state_compose(int32_t units, int32_t segments, int32_t dk, int3
     const void *ptrs[] = {transfer, zero_init_state, S0, seg_init_states, S_final, start_images};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (dev_status && !aligned4(dev_status)) return KDA_ERR_INVALID_ARG;
     return from_cuda(launch_compose(units, segments, dk, dv, transfer, nullptr, zero_init_state,
                                     S0, seg_init_states, S_final, (__nv_bfloat16 *)start_images,
-                                    nullptr, (cudaStream_t)stream));
+                                    dev_status, (cudaStream_t)stream));
 }
 
 const char *kda_status_string(kda_status_t s) {

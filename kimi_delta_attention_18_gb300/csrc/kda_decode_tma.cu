@@ -13,6 +13,12 @@
 // Thread t of the compute warps owns float4 column group (t mod 32) of rows
 // (t div 32) + 8 m, m = 0..15: its 16 float4 stay in registers between the
 // reduction and the update, so shared memory is read once and written once.
+//
+// Every wait is bounded.  A wait that gives up sets the CTA's abort flag; the
+// compute warps decide together whether to stop (a barrier reduction right
+// after each wait), so no warp is left at a named barrier the others never
+// reach, and the CTA records KDA_ERR_TIMEOUT in dev_status before it exits
+// (states it had not reached keep their old value: the step is then incomplete).
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -56,7 +62,8 @@ __device__ __forceinline__ void bulk_wait_all() {
 template <typename TA>
 __global__ void __launch_bounds__(NT, 1) decode_tma_kernel(int units, const TA *q, const TA *k,
                                                            const TA *v, const float *g,
-                                                           const float *beta, float *S, TA *out) {
+                                                           const float *beta, float *S, TA *out,
+                                                           int32_t *dev_status) {
     using L = Layout<TA>;
     extern __shared__ uint8_t smem_raw[];
     // Align by pointer arithmetic on the __shared__ array (not through an integer),
@@ -126,7 +133,9 @@ __global__ void __launch_bounds__(NT, 1) decode_tma_kernel(int units, const TA *
         const int st = i % NSTG;
         int ok = 1;
         if (lane == 0) ok = mbar_wait(full(st), (i / NSTG) & 1, abort, kWaitLimit);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        // one decision for all compute warps: leave together or not at all
+        if (named_bar_or(2, NCW * 32, !ok)) break;
         uint8_t *stg = sm + st * L::STAGE;
         float *Ss = (float *)stg;
         const TA *qs = (const TA *)(stg + L::Q);
@@ -186,6 +195,7 @@ __global__ void __launch_bounds__(NT, 1) decode_tma_kernel(int units, const TA *
     if (t == 0) {
         bulk_wait_all();
         if (prev_st >= 0) mbar_arrive(empty(prev_st));
+        if (*abort) dev_fail(dev_status, KDA_ERR_TIMEOUT);
     }
 }
 
@@ -195,7 +205,7 @@ bool decode_tma_supported(int dk, int dv) { return dk == D && dv == D; }
 
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,
                               const void *v, const float *g, const float *beta, float *S,
-                              void *out, cudaStream_t st) {
+                              void *out, int32_t *dev_status, cudaStream_t st) {
     const int units = batch * H;
     if (units == 0) return cudaSuccess;
     int dev = 0, sms = 148;
@@ -208,14 +218,14 @@ cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const vo
         if (e != cudaSuccess) return e;
         decode_tma_kernel<float><<<grid, NT, bytes, st>>>(units, (const float *)q, (const float *)k,
                                                           (const float *)v, g, beta, S,
-                                                          (float *)out);
+                                                          (float *)out, dev_status);
     } else {
         const int bytes = Layout<__nv_bfloat16>::BYTES;
         cudaError_t e = set_max_dynamic_smem((const void *)decode_tma_kernel<__nv_bfloat16>, bytes);
         if (e != cudaSuccess) return e;
         decode_tma_kernel<__nv_bfloat16><<<grid, NT, bytes, st>>>(
             units, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g,
-            beta, S, (__nv_bfloat16 *)out);
+            beta, S, (__nv_bfloat16 *)out, dev_status);
     }
     return cudaGetLastError();
 }

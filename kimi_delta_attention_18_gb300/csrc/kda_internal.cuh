@@ -153,9 +153,10 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
                             float *dk, float *dv, float *dg, float *dbeta, float *dS0, int Sg,
                             void *workspace, cudaStream_t st);
 bool decode_tma_supported(int dk, int dv);
+// dev_status (nullable) receives KDA_ERR_TIMEOUT if a bounded wait gives up.
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,
                               const void *v, const float *g, const float *beta, float *S,
-                              void *out, cudaStream_t st);
+                              void *out, int32_t *dev_status, cudaStream_t st);
 cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void *aux_out,
                            const __nv_bfloat16 *start_img, cudaStream_t st);
 // True when launch_combine with these arguments reads only the start images (its

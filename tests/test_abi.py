@@ -64,6 +64,8 @@ def _prefill(desc, ptr=0x10000, ws=None, ws_len=0, cu=0x20000):
     (dict(num_heads=0), INVALID),
     (dict(num_segments=-2), INVALID),
     (dict(num_segments=5000), UNSUPPORTED),
+    # (sequence, head, segment) units must fit a grid dimension (below 2^31)
+    (dict(num_seqs=1 << 20, num_heads=64, num_segments=64), UNSUPPORTED),
 ])
 def test_prefill_rejects_bad_descriptor(kw, code):
     assert _prefill(_desc(**kw)) == code
@@ -76,6 +78,16 @@ def test_prefill_rejects_null_and_misaligned_pointers():
     assert _prefill(_desc(), ptr=0x10004) == INVALID    # not 16-byte aligned
     assert _prefill(_desc(), cu=0) == INVALID           # cu_seqlens missing
     assert _prefill(_desc(num_seqs=0)) == OK            # nothing to do, nothing launched
+
+
+def test_timed_prefill_needs_its_four_events():
+    L = kda.lib()
+    p = ctypes.c_void_p(0x10000)
+    args = [ctypes.byref(_desc()), p, p, p, p, p, None, ctypes.c_void_p(0x20000), p, None, None, 0,
+            None]
+    assert L.kda_prefill_chunked_timed(*args, None, None) == INVALID
+    evs = (ctypes.c_void_p * 4)(0x1, 0x2, None, 0x4)
+    assert L.kda_prefill_chunked_timed(*args, ctypes.cast(evs, ctypes.c_void_p), None) == INVALID
 
 
 def test_prefill_split_requires_workspace():
@@ -114,22 +126,27 @@ def test_segment_choice():
 def test_decode_and_compose_host_checks():
     L = kda.lib()
     p = ctypes.c_void_p(0x10000)
-    assert L.kda_decode_step(4, 2, 16, 18, 1, p, p, p, p, p, p, p, None) == UNSUPPORTED  # dv % 4
-    assert L.kda_decode_step(4, 2, 256, 16, 1, p, p, p, p, p, p, p, None) == UNSUPPORTED
-    assert L.kda_decode_step(4, 2, 16, 16, 3, p, p, p, p, p, p, p, None) == UNSUPPORTED
-    assert L.kda_decode_step(4, 0, 16, 16, 1, p, p, p, p, p, p, p, None) == INVALID
-    assert L.kda_decode_step(4, 2, 16, 16, 1, p, p, p, p, None, p, p, None) == INVALID
+    assert L.kda_decode_step(4, 2, 16, 18, 1, p, p, p, p, p, p, p, None, None) == UNSUPPORTED  # dv % 4
+    assert L.kda_decode_step(4, 2, 256, 16, 1, p, p, p, p, p, p, p, None, None) == UNSUPPORTED
+    assert L.kda_decode_step(4, 2, 16, 16, 3, p, p, p, p, p, p, p, None, None) == UNSUPPORTED
+    assert L.kda_decode_step(4, 0, 16, 16, 1, p, p, p, p, p, p, p, None, None) == INVALID
+    assert L.kda_decode_step(4, 2, 16, 16, 1, p, p, p, p, None, p, p, None, None) == INVALID
     assert L.kda_decode_step(4, 2, 16, 16, 1, p, p, p, p, ctypes.c_void_p(0x10002), p, p,
+                             None, None) == INVALID
+    # a misaligned status word is refused before anything is launched
+    assert L.kda_decode_step(4, 2, 16, 16, 1, p, p, p, p, p, p, p, ctypes.c_void_p(0x10002),
                              None) == INVALID
-    assert L.kda_decode_step(0, 2, 16, 16, 1, p, p, p, p, p, p, p, None) == OK
-    assert L.kda_state_compose(2, 0, 16, 16, p, p, None, None, None, None, None) == INVALID
-    assert L.kda_state_compose(2, 3, 16, 200, p, p, None, None, None, None, None) == UNSUPPORTED
-    assert L.kda_state_compose(2, 3, 16, 16, None, p, None, None, None, None, None) == INVALID
-    assert L.kda_state_compose(0, 3, 16, 16, None, None, None, None, None, None, None) == OK
+    assert L.kda_decode_step(0, 2, 16, 16, 1, p, p, p, p, p, p, p, None, None) == OK
+    assert L.kda_state_compose(2, 0, 16, 16, p, p, None, None, None, None, None, None) == INVALID
+    assert L.kda_state_compose(2, 3, 16, 200, p, p, None, None, None, None, None, None) == UNSUPPORTED
+    assert L.kda_state_compose(2, 3, 16, 16, None, p, None, None, None, None, None, None) == INVALID
+    assert L.kda_state_compose(0, 3, 16, 16, None, None, None, None, None, None, None, None) == OK
     # start images exist only for dk = dv = 128 and must be 16-byte aligned
-    assert L.kda_state_compose(2, 3, 16, 16, p, p, None, None, None, p, None) == INVALID
+    assert L.kda_state_compose(2, 3, 16, 16, p, p, None, None, None, p, None, None) == INVALID
     assert L.kda_state_compose(2, 3, 128, 128, p, p, None, None, None,
-                               ctypes.c_void_p(0x10008), None) == INVALID
+                               ctypes.c_void_p(0x10008), None, None) == INVALID
+    assert L.kda_state_compose(2, 3, 16, 16, p, p, None, None, None, None,
+                               ctypes.c_void_p(0x10002), None) == INVALID
     d = _desc(num_segments=0)
     assert L.kda_state_transfer(ctypes.byref(d), 0, 1, None, p, p, p, p, p, p, p, None, None, None,
                                 None) == INVALID
