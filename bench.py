@@ -1,19 +1,23 @@
 #!/usr/bin/env python
-"""KDA on GB300: prefill tokens/s (chunked, BF16, B=1 H=8 T=4096 d=128) and
-decode tokens/s (256 sequences x 56 heads, 64 single-token steps), with the
-roofline fraction of the dominant kernel.
+"""KDA on GB300: prefill tokens/s and decode tokens/s, with the roofline fraction
+of the dominant kernel.
 
-One step = one whole prefill of the workload through the one-call entry point
-kda_prefill_chunked, bracketed by CUDA events on the launching stream: the
-transfer pass over all S segments with outputs, the segment scan and the output
-combine launched back to back (a single output pass when the library picks
-S = 1).  A separate pass through the three stage entry points, with events
-between them, gives the per-stage times behind the roofline.  Inputs are
-resident in HBM; the 50 MB working set is smaller than L2, so a 512 MB buffer is
-rewritten between timed steps (outside the events).  ``e2e`` times the same
-call with every step's inputs copied in from pinned host memory and its outputs
-copied back, steps alternating between two streams (one step's input copies
-overlap the previous step's compute and output copies).
+Headline (``value``): the long-context prefill, B=1 H=56 T=1,048,576 d=128 BF16,
+every sequence split into 64 segments joined by the transfer-matrix scan, through
+the one-call entry point kda_prefill_chunked (one step = one whole prefill: the
+transfer pass with outputs, the segment scan and the output combine launched
+back to back), bracketed by CUDA events on the launching stream.  Its inputs
+(~75 GB per step) are far larger than the 129 MB L2, so nothing is flushed
+between steps.  The dominant kernel is timed inside the same call path:
+kda_prefill_chunked_timed records events between its launches.
+
+Beside it: the variable-length prefill (4 sequences of 8K/16K/24K/32K tokens,
+H=56, S0 ~ N(0, 0.02^2)), the short prefill (B=1 H=8 T=4096, a latency-bound
+case, L2 flushed between steps), the decode step (256 sequences x 56 heads, 64
+single-token steps), the fused gate prologue and the state checkpoints on the
+headline workload, the backward pass on the short workload, the e2e leg (the
+headline call with its inputs copied in from pinned host memory and its outputs
+copied back inside the timed region) and the oracle on the host cores.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own batch (weak scaling, no collective on
@@ -22,8 +26,10 @@ the data path); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -33,25 +39,38 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-PREFILL = "kda_prefill_bf16_h8_t4096_d128"
+HEADLINE = "kda_prefill_kcp64_h56_t1m_d128"
+VARLEN = "kda_prefill_varlen4_h56_t81920_d128_s0"
+SHORT = "kda_prefill_bf16_h8_t4096_d128"
 DECODE = "kda_decode_b256_h56_d128_x64"
 METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of roofline"
-# fp32 FMA peak of a GB300 at its maximum SM clock (no measured figure exists for
-# CUDA-core fp32): 152 SMs x 128 lanes x 2 flops x 2.07 GHz
-BWD_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_ckpt_h8_t4096",
-                 "backward_h8_t1024")
+# per head-token at dk = dv = 128, BF16 activations (the method's algorithmic bytes):
+# one pass reads q, k, v (BF16), g (fp32), beta (fp32) and writes o (BF16)
+ONE_PASS_B = 4 * 256 + 512 + 4
+# the context-parallel split as the method runs it: a transfer pass over k, v, g,
+# beta, then an output pass over everything
+KCP_B = (2 * 256 + 512 + 4) + ONE_PASS_B
+CKPT_INTERVAL = 4096
+PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_kcp_h56_t64k",
+                 "prefill_ckpt_h8_t4096", "backward_h8_t1024")
+# the ncu summary that gives the transfer pass's DRAM traffic per launch, and the
+# kernel source it was taken on
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "prefill_tc_kernel_kcp_h56_t64k_d128.md")
+TRANSFER_KERNEL_SRC = os.path.join(ROOT, "kimi_delta_attention_18_gb300", "csrc",
+                                   "kda_prefill_tc.cu")
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-extras", action="store_true",
+                   help="headline and decode only (no gated, checkpoint, backward legs)")
+    p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--profile", choices=sorted(PROFILE_CASES), default=None,
                    help="run one small case twice for an ncu capture (no timing, no JSON)")
     return p.parse_args()
@@ -160,58 +179,137 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-# ---------------------------------------------------------------------------
-# algorithmic bytes (what the method must move, per launch)
-# ---------------------------------------------------------------------------
-def prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes):
-    """Bytes each stage must read and write at minimum.
-
-    one pass (S = 1): q, k, v, out (activation dtype) + g, beta (fp32) per
-                      head-token, plus the final states.
-    transfer pass   : q, k, v, g, beta read once per head-token; the zero-start
-                      outputs and A_t^T q_t written (activation dtype); A and B
-                      written per (sequence, head, segment).
-    scan            : A, B read, start states and final states written (and, for
-                      BF16 at d = 128, each start state's BF16 operand image).
-    combine         : A_t^T q_t and the zero-start outputs read, outputs written,
-                      start states read (their BF16 images for BF16 at d = 128).
-    """
-    if Sg == 1:
-        return {"output_pass": T * H * ((2 * dk + 2 * dv) * act_bytes + 4 * dk + 4) +
-                N * H * dk * dv * 4}
-    states = N * H * Sg * (dk * dk + dk * dv) * 4
-    start_bytes = 2 if (act_bytes == 2 and dk == 128 and dv == 128) else 4
-    transfer = T * H * ((2 * dk + dv) * act_bytes + 4 * dk + 4) + \
-        T * H * (dv + dk) * act_bytes + states
-    scan = states + N * H * Sg * dk * dv * 4 + N * H * dk * dv * 4
-    if start_bytes == 2:
-        scan += N * H * Sg * dk * dv * 2
-    combine = T * H * (dk + 2 * dv) * act_bytes + N * H * Sg * dk * dv * start_bytes
-    return {"transfer_pass": transfer, "segment_scan": scan, "combine": combine}
-
-
-def method_roofline(head_tokens, ms, dk, dv, act_bytes, peaks):
-    """The whole step against the method's own algorithmic counts per head-token:
-    flops = 6 dk dv + C (3 dk + 2 dv) (C = 16, triangle-aware) and bytes = q, k, v,
-    out in the activation dtype + g fp32 + beta fp32; the attainable ceiling is
-    min(P_bf16, I * BW) with I = flops / bytes (I * BW is below P here: HBM-bound)."""
-    C = 16
-    flops = 6 * dk * dv + C * (3 * dk + 2 * dv)
-    nbytes = (2 * dk + 2 * dv) * act_bytes + 4 * dk + 4
-    sec = ms / 1e3
-    tflops = head_tokens * flops / sec / 1e12
-    gbs = head_tokens * nbytes / sec / 1e9
-    attain = min(peaks["bf16_tflops"], flops / nbytes * peaks["hbm_gbs"] / 1e3)
-    return {"flops_per_head_token": flops, "bytes_per_head_token": nbytes,
-            "tflops": round(tflops, 2), "tflops_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
-            "attainable_tflops": round(attain, 1), "attainable_frac": round(tflops / attain, 4),
-            "gbs": round(gbs, 1), "gbs_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
-            "peak_source": peaks["source"]}
+def transfer_traffic(T, H, N, Sg, dk, dv):
+    """DRAM bytes per launch of the transfer pass for this workload, scaled from the
+    committed ncu summary (a scaled-down case of the same kernel); None when the
+    kernel source has changed since those counters were taken."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+        src = open(TRANSFER_KERNEL_SRC, "rb").read()
+    except OSError:
+        return None, "no profile"
+    got = {k_: v_ for k_, v_ in re.findall(r"^- (\w+): (\S+)$", text, flags=re.M)}
+    try:
+        if got["kernel_sha256_16"] != hashlib.sha256(src).hexdigest()[:16]:
+            return None, "kernel changed since the capture"
+        per_ht = float(got["token_bytes_per_head_token"])
+        per_unit = float(got["state_bytes_per_segment"])
+    except (KeyError, ValueError):
+        return None, "profile lacks the traffic lines"
+    return int(per_ht * T * H + per_unit * N * H * Sg), "scaled from " + \
+        os.path.basename(TRAFFIC_PROFILE)
 
 
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def ev_pair():
+    import torch
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def time_calls(call, steps, warmup, flush=None):
+    """Mean device ms of `call` over `steps` calls after `warmup`, each bracketed by
+    CUDA events on the current stream (an L2 flush before each when given)."""
+    import torch
+    for _ in range(warmup):
+        if flush is not None:
+            flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    evs = [ev_pair() for _ in range(steps)]
+    for e0, e1 in evs:
+        if flush is not None:
+            flush.zero_()
+        e0.record()
+        call()
+        e1.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def stage_times(kda, x, Sg, out, SF, ws, reps, flush=None):
+    """Per-launch device times inside kda_prefill_chunked (its timed variant):
+    transfer pass, segment scan, combine (or the single pass for S = 1)."""
+    import torch
+    res = {"transfer_pass": [], "segment_scan": [], "combine": []}
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["cu_seqlens"],
+                            num_segments=Sg, out=out, S_final=SF, workspace=ws,
+                            stage_events=evs)
+        torch.cuda.synchronize()
+        res["transfer_pass"].append(evs[0].elapsed_time(evs[1]))
+        res["segment_scan"].append(evs[1].elapsed_time(evs[2]))
+        res["combine"].append(evs[2].elapsed_time(evs[3]))
+    if Sg == 1:
+        return {"output_pass": statistics.mean(res["transfer_pass"])}
+    return {k_: statistics.mean(v_) for k_, v_ in res.items()}
+
+
+def prefill_leg(kda, name, w, x, Sg, steps, warmup, peaks, dev, dist, world, flush=None):
+    """One prefill workload through kda_prefill_chunked: tokens/s, the per-launch
+    times inside the call, and the whole step against the method's bytes."""
+    import torch
+    T, H, dk = x["q"].shape
+    dv = x["v"].shape[2]
+    N = len(x["lengths"])
+    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"], Sg)
+    Sg = kda.prefill_num_segments(desc)
+    out = torch.empty_like(x["v"])
+    SF = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(kda.prefill_workspace_size(desc), 16), dtype=torch.uint8, device=dev)
+
+    def call():
+        kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], x["cu_seqlens"],
+                            num_segments=Sg, out=out, S_final=SF, workspace=ws)
+
+    per = time_calls(call, steps, warmup, flush)
+    ms = max_over_ranks(sum(per), dist, dev) / steps
+    stages = stage_times(kda, x, Sg, out, SF, ws, max(3, min(steps, 5)), flush)
+    states = N * H * dk * dv * 4 * (2 if x["S0"] is not None else 1)  # S0 in, S_final out
+    step_b = (KCP_B if Sg > 1 else ONE_PASS_B) * T * H + states
+    sec = ms / 1e3
+    res = {"workload": name, "tokens_per_s": round(T * world / sec, 1),
+           "ms_per_step": round(ms, 4), "segments": Sg, "steps": steps,
+           "launches_per_step": 3 if Sg > 1 else 1,
+           "stage_ms": {k_: round(v_, 4) for k_, v_ in stages.items()},
+           "method_bytes_per_step": step_b,
+           "method_gbs": round(step_b / sec / 1e9, 1),
+           "method_frac_of_hbm": round(step_b / sec / 1e9 / peaks["hbm_gbs"], 4),
+           "bytes_per_head_token": KCP_B if Sg > 1 else ONE_PASS_B,
+           "hbm_bound_ms": round(step_b / (peaks["hbm_gbs"] * 1e9) * 1e3, 4)}
+    return res, (out, SF, ws, Sg, stages)
+
+
+def roofline_of(stages, T, H, N, Sg, dk, dv, peaks, traffic):
+    """Roofline of the dominant launch of the call from its algorithmic bytes.
+
+    transfer pass: q, k, v, g, beta read once and o written once per head-token
+    (the bytes of one pass; the A_t^T q_t intermediate it also writes is this
+    implementation's traffic, not the method's) plus the (A, B) pair of every
+    segment; single pass: the same per head-token plus the states."""
+    dom = max(stages, key=stages.get)
+    if dom == "transfer_pass":
+        nbytes = ONE_PASS_B * T * H + N * H * Sg * (dk * dk + dk * dv) * 4
+    elif dom == "output_pass":
+        nbytes = ONE_PASS_B * T * H + N * H * dk * dv * 4
+    elif dom == "combine":  # the output correction: A_t^T q_t and out read, out written
+        nbytes = 3 * 256 * T * H
+    else:  # the scan: A, B read, start states written
+        nbytes = N * H * Sg * (dk * dk + 2 * dk * dv) * 4
+    achieved = nbytes / (stages[dom] / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic[0] if dom == "transfer_pass" else None,
+            "traffic_note": traffic[1] if dom == "transfer_pass" else "not captured",
+            "algorithmic_bytes_per_launch": nbytes,
+            "peak_source": peaks["source"] + " (burst copy)"}
+
+
 def run_ours(args):
     import torch
     import kimi_delta_attention_18_gb300 as kda
@@ -223,229 +321,166 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     dist = dist_init(world, "nccl")
     kda.lib()  # fail loudly now if the library is missing
+    peaks = measured_peaks()
 
-    w = WORKLOADS[PREFILL]
+    # ---- headline: 1M tokens x 56 heads, 64 segments
+    w = WORKLOADS[HEADLINE]
     x = make_prefill_inputs(w["lengths"], w["H"], w["dk"], w["dv"], w["act"], seed=rank,
-                            device=dev)
+                            s0_std=w["s0_std"], device=dev)
     T, H, dk = x["q"].shape
     dv = x["v"].shape[2]
     N = len(w["lengths"])
-    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"])
-    Sg = kda.prefill_num_segments(desc)
-    act_bytes = x["q"].element_size()
+    Sg = w["num_segments"]
+    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"], Sg)
     out = torch.empty_like(x["v"])
-    S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
-    A = torch.empty((N, H, Sg, dk, dk), dtype=torch.float32, device=dev)
-    B = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
-    starts = torch.empty((N, H, Sg, dk, dv), dtype=torch.float32, device=dev)
-    # L2 flush between timed steps: a 512 MB fill (torch's fill kernel) evicts the
-    # 129 MB L2 before every step
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    SF = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(kda.prefill_workspace_size(desc), 16), dtype=torch.uint8, device=dev)
 
-    aux = torch.empty((T, H, dk), dtype=x["q"].dtype, device=dev)
-    # the start states' BF16 operand images (BF16 at d = 128), as the one-call path uses
-    imgs = (torch.empty((N * H, Sg, dk * dv), dtype=torch.bfloat16, device=dev)
-            if x["q"].dtype == torch.bfloat16 and dk == 128 and dv == 128 else None)
-
-    ws_bytes = kda.prefill_workspace_size(desc)
-    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-
-    def step(ev):
-        # the call a user makes: kda_prefill_chunked launches the transfer pass,
-        # the segment scan and the output combine back to back (or one output
-        # pass when the split is a single segment)
-        ev[0].record(stream)
+    def step():
         kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["cu_seqlens"],
-                            out=out, S_final=S_final, workspace=workspace)
-        ev[1].record(stream)
+                            num_segments=Sg, out=out, S_final=SF, workspace=ws)
 
-    def staged(ev):
-        # exactly the launches kda_prefill_chunked makes, with events between them
-        ev[0].record(stream)
-        if Sg > 1:
-            kda.state_transfer(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], Sg,
-                               transfer=A, zero_init_state=B, q=x["q"], out_zero=out,
-                               out_transfer=aux)
-        ev[1].record(stream)
-        if Sg > 1:
-            kda.state_compose(A.view(N * H, Sg, dk, dk), B.view(N * H, Sg, dk, dv), None,
-                              seg_init_states=starts.view(N * H, Sg, dk, dv),
-                              S_final=S_final.view(N * H, dk, dv), start_images=imgs)
-        ev[2].record(stream)
-        if Sg > 1:
-            kda.prefill_combine(out, aux, starts, x["cu_seqlens"], first_segment=1,
-                                start_images=imgs)
-        else:
-            kda.prefill_segments(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
-                                 x["cu_seqlens"], 1, out=out, S_final=S_final)
-        ev[3].record(stream)
-
-    mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     for _ in range(args.warmup):
-        flush.zero_()
-        step(mk(2))
+        step()
     torch.cuda.synchronize()
-    events = [mk(2) for _ in range(args.steps)]
+    events = [ev_pair() for _ in range(args.steps)]
     clocks = Clocks(local)
     barrier(dist)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        step(events[i])
+    for e0, e1 in events:
+        e0.record()
+        step()
+        e1.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(dist)
     clk = clocks.stop()
-    total_ms = [ev[0].elapsed_time(ev[1]) for ev in events]
-    dev_ms = sum(total_ms)
+    dev_ms = sum(a.elapsed_time(b) for a, b in events)
     dev_ms_max = max_over_ranks(dev_ms, dist, dev)
-    tokens = T * args.steps * world
-    value = tokens / (dev_ms_max / 1e3)
+    step_ms = dev_ms_max / args.steps
+    value = T * args.steps * world / (dev_ms_max / 1e3)
 
-    # per-stage device times (a separate pass through the stage entry points; the
-    # host has time to queue each step's launches behind the L2 flush)
-    stage_ms = {"transfer_pass": [], "segment_scan": [], "combine": [], "output_pass": []}
-    for _ in range(max(3, min(args.steps, 10))):
-        ev = mk(4)
-        flush.zero_()
-        staged(ev)
-        torch.cuda.synchronize()
-        stage_ms["transfer_pass"].append(ev[0].elapsed_time(ev[1]))
-        stage_ms["segment_scan"].append(ev[1].elapsed_time(ev[2]))
-        stage_ms["combine" if Sg > 1 else "output_pass"].append(ev[2].elapsed_time(ev[3]))
-
-    # roofline of the dominant kernel (HBM-bound: see the design notes)
-    peaks = measured_peaks()
-    sbytes = prefill_stage_bytes(T, H, dk, dv, N, Sg, act_bytes)
-    means = {k_: statistics.mean(v_) for k_, v_ in stage_ms.items() if k_ in sbytes}
-    dom = max(means, key=means.get)
-    achieved = sbytes[dom] / (means[dom] / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": None, "peak_source": peaks["source"] + " (burst copy)",
-                "stage_ms": {k_: round(v_, 4) for k_, v_ in means.items()},
-                "stage_bytes": sbytes}
-    launches_per_step = 3 if Sg > 1 else 1
-
+    stages = stage_times(kda, {**x, "S0": None}, Sg, out, SF, ws, 3)
+    roofline = roofline_of(stages, T, H, N, Sg, dk, dv, peaks,
+                           transfer_traffic(T, H, N, Sg, dk, dv))
+    roofline["stage_ms"] = {k_: round(v_, 4) for k_, v_ in stages.items()}
+    method_b = KCP_B * T * H + N * H * dk * dv * 4
     result = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
               "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-              "ms_per_step": round(dev_ms_max / args.steps, 5), "higher_is_better": True,
+              "ms_per_step": round(step_ms, 4), "higher_is_better": True,
               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-              "config": {"workload": PREFILL, "batch": N, "seq_len": T, "heads": H, "dk": dk,
+              "config": {"workload": HEADLINE, "batch": N, "seq_len": T, "heads": H, "dk": dk,
                          "dv": dv, "chunk": 16, "segments": Sg, "state": "fp32",
-                         "l2": "512 MB buffer zero-filled between timed steps (working set 50 MB)",
+                         "l2": "no flush: every step reads ~75 GB of inputs, far more than "
+                               "the 129 MB L2",
                          "parallelism": "dp%d (one batch per GPU)" % world},
               "wall_s_timed_loop": round(wall, 4), "clocks": clk, "roofline": roofline,
-              "method": method_roofline(T * H * world, dev_ms_max / args.steps, dk, dv,
-                                        act_bytes, peaks),
-              "gpu_launches": launches_per_step * args.steps}
+              "method": {"bytes_per_head_token": KCP_B, "step_bytes": method_b,
+                         "gbs": round(method_b / (step_ms / 1e3) / 1e9, 1),
+                         "frac_of_hbm": round(method_b / (step_ms / 1e3) / 1e9 /
+                                              peaks["hbm_gbs"], 4),
+                         "hbm_bound_ms": round(method_b / (peaks["hbm_gbs"] * 1e9) * 1e3, 3),
+                         "one_pass_bound_ms": round(ONE_PASS_B * T * H /
+                                                    (peaks["hbm_gbs"] * 1e9) * 1e3, 3),
+                         "what": "the transfer-matrix split as the method runs it: k, v, g, "
+                                 "beta read for the transfer pass, then q, k, v, g, beta read "
+                                 "and o written (2568 B per head-token)"},
+              "gpu_launches": 3 * args.steps}
 
-    # the same step from the pre-activations (fused gate prologue)
-    result["gated"] = run_gated(args, kda, x, flush, stream, dev, dist, dev_ms_max / args.steps)
-    # the same step with a state checkpoint every 512 tokens of each sequence
-    result["checkpoints"] = run_ckpt(args, kda, x, flush, stream, dev, dist,
-                                     dev_ms_max / args.steps)
-    result["backward"] = run_backward(args, kda, x, flush, stream, dev, dist)
-    # e2e: one-call C entry point with pinned host buffers, copies included
-    result["e2e"] = run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world)
+    if not args.no_extras:
+        result["gated"] = run_gated(kda, x, Sg, out, ws, dev, dist, step_ms)
+        result["checkpoints"] = run_ckpt(kda, x, Sg, out, dev, dist, step_ms)
+    result["e2e"] = run_e2e(args, kda, x, Sg, out, SF, ws, dev, dist, world)
+    del x, out, ws
+    torch.cuda.empty_cache()
+
+    # ---- variable-length prefill from cached prefixes (S0 != 0)
+    w2 = WORKLOADS[VARLEN]
+    x2 = make_prefill_inputs(w2["lengths"], w2["H"], w2["dk"], w2["dv"], w2["act"], seed=rank,
+                             s0_std=w2["s0_std"], device=dev)
+    res2, _ = prefill_leg(kda, VARLEN, w2, x2, 0, max(5, args.steps), args.warmup, peaks, dev,
+                          dist, world)
+    result["varlen"] = res2
+    del x2
+
+    # ---- short prefill (latency-bound); its 50 MB working set fits in L2, so a 512 MB
+    # buffer is rewritten before every step (outside the events)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    w1 = WORKLOADS[SHORT]
+    x1 = make_prefill_inputs(w1["lengths"], w1["H"], w1["dk"], w1["dv"], w1["act"], seed=rank,
+                             device=dev)
+    res1, (o1, _, _, Sg1, st1) = prefill_leg(kda, SHORT, w1, x1, 0, max(20, args.steps),
+                                             args.warmup, peaks, dev, dist, world, flush)
+    res1["roofline"] = roofline_of(st1, 4096, 8, 1, Sg1, 128, 128, peaks, (None, "not captured"))
+    res1["l2"] = "512 MB buffer zero-filled between timed steps (working set 50 MB)"
+    result["short"] = res1
+    if not args.no_extras:
+        result["backward"] = run_backward(kda, x1, flush, dev, dist)
     if not args.no_decode:
-        result["decode"] = run_decode(args, kda, make_decode_inputs, WORKLOADS[DECODE], dev,
-                                      dist, world, peaks, rank)
+        result["decode"] = run_decode(kda, make_decode_inputs, WORKLOADS[DECODE], dev, dist,
+                                      world, peaks, rank)
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(x, N, H)
-        result["backward"]["cpu_baseline"] = cpu_baseline_backward(x, H)
+        result["cpu_baseline"] = cpu_baseline(rank)
+        if "backward" in result:
+            result["backward"]["cpu_baseline"] = cpu_baseline_backward(x1, 8)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 
 
-def run_gated(args, kda, x, flush, stream, dev, dist, plain_ms):
-    """kda_prefill_chunked_gated on the timed workload (raw q, k; x_g in BF16 and
-    x_beta fp32; the kernels form g, beta and the normalised q, k), timed like the
-    plain step."""
+def run_gated(kda, x, Sg, out, ws, dev, dist, plain_ms):
+    """kda_prefill_chunked_gated on the headline workload (raw q, k; x_g in BF16
+    and x_beta fp32; the kernels form g, beta and the normalised q, k), timed like
+    the plain step."""
     import torch
     T, H, dk = x["q"].shape
     dv = x["v"].shape[2]
-    if x["q"].dtype != torch.bfloat16 or dk != 128 or dv != 128:
-        return None
-    out = torch.empty_like(x["v"])
     SF = torch.empty((len(x["lengths"]), H, dk, dv), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(kda.prefill_workspace_size(kda.prefill_desc(x["q"], x["v"],
-                                                                     x["cu_seqlens"])), 1),
-                     dtype=torch.uint8, device=dev)
 
     def call():
         kda.prefill_chunked_gated(x["q_raw"], x["k_raw"], x["v"], x["x_g"], x["x_beta"], None,
-                                  x["cu_seqlens"], out=out, S_final=SF, workspace=ws)
+                                  x["cu_seqlens"], num_segments=Sg, out=out, S_final=SF,
+                                  workspace=ws)
 
-    for _ in range(3):
-        flush.zero_()
-        call()
-    steps = max(5, min(args.steps, 20))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    torch.cuda.synchronize()
-    for e0, e1 in evs:
-        flush.zero_()
-        e0.record(stream)
-        call()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dist, dev) / steps
-    nbytes = T * H * ((2 * dk + 2 * dv) * 2 + 2 * dk + 4)  # q, k, v, out, x_g BF16, x_beta
-    return {"ms_per_step": round(ms, 5), "tokens_per_s": round(T / (ms / 1e3), 1),
-            "bytes_per_head_token": nbytes // (T * H), "vs_plain": round(ms / plain_ms - 1.0, 4)}
+    per = time_calls(call, 3, 2)
+    ms = max_over_ranks(sum(per), dist, dev) / len(per)
+    nbytes = (2 * dk + 2 * dv) * 2 + 2 * dk + 4  # q, k, v, out, x_g BF16, x_beta
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1),
+            "bytes_per_head_token_one_pass": nbytes, "vs_plain": round(ms / plain_ms - 1.0, 4)}
 
 
-def run_ckpt(args, kda, x, flush, stream, dev, dist, plain_ms, interval=512):
-    """kda_prefill_chunked_ckpt on the timed workload: the step with a state
-    checkpoint after every `interval` tokens, timed like the plain step (L2
-    flushed before each call, CUDA events around it)."""
+def run_ckpt(kda, x, Sg, out, dev, dist, plain_ms, interval=CKPT_INTERVAL):
+    """kda_prefill_chunked_ckpt on the headline workload: the step with a state
+    checkpoint after every `interval` tokens, timed like the plain step."""
     import torch
     T, H, dk = x["q"].shape
     dv = x["v"].shape[2]
     K = kda.num_checkpoints(x["cu_seqlens"], interval)
     ck = torch.empty((max(K, 1), H, dk, dv), dtype=torch.float32, device=dev)
-    out = torch.empty_like(x["v"])
     SF = torch.empty((len(x["lengths"]), H, dk, dv), dtype=torch.float32, device=dev)
-    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"])
-    ws_bytes = kda.prefill_ckpt_workspace_size(desc, interval)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"], Sg)
+    ws = torch.empty(max(kda.prefill_ckpt_workspace_size(desc, interval), 16), dtype=torch.uint8,
+                     device=dev)
 
     def call():
         kda.prefill_chunked_ckpt(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                  x["cu_seqlens"], ckpt_interval=interval, ckpt_states=ck,
-                                 out=out, S_final=SF, workspace=ws)
+                                 num_segments=Sg, out=out, S_final=SF, workspace=ws)
 
-    for _ in range(3):
-        flush.zero_()
-        call()
-    steps = max(5, min(args.steps, 20))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    torch.cuda.synchronize()
-    for e0, e1 in evs:
-        flush.zero_()
-        e0.record(stream)
-        call()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dist, dev) / steps
+    per = time_calls(call, 3, 2)
+    ms = max_over_ranks(sum(per), dist, dev) / len(per)
     return {"interval": interval, "checkpoints_per_step": K * H,
-            "bytes_per_step": K * H * dk * dv * 4, "ms_per_step": round(ms, 5),
+            "bytes_per_step": K * H * dk * dv * 4, "ms_per_step": round(ms, 4),
             "overhead_vs_plain": round(ms / plain_ms - 1.0, 4)}
 
 
-def run_backward(args, kda, x, flush, stream, dev, dist):
-    """kda_prefill_backward on the timed workload (d_out ~ N(0, 1), d_S_final ~
-    N(0, 1)): dq, dk, dv, dg, dbeta, dS0 in fp32; L2 flushed before each call,
-    CUDA events around it."""
+def run_backward(kda, x, flush, dev, dist):
+    """kda_prefill_backward on the short workload (d_out ~ N(0, 1), d_S_final ~
+    N(0, 1)): dq, dk, dv, dg, dbeta, dS0 in fp32; L2 flushed before each call."""
     import torch
     from kimi_delta_attention_18_gb300.inputs import make_backward_adjoints
     T, H, dk = x["q"].shape
@@ -461,121 +496,92 @@ def run_backward(args, kda, x, flush, stream, dev, dist):
         kda.prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["cu_seqlens"],
                              d_out, d_sf, workspace=ws)
 
-    for _ in range(3):
-        flush.zero_()
-        call()
-    steps = 5
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    torch.cuda.synchronize()
-    for e0, e1 in evs:
-        flush.zero_()
-        e0.record(stream)
-        call()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dist, dev) / steps
+    per = time_calls(call, 5, 3, flush)
+    ms = max_over_ranks(sum(per), dist, dev) / len(per)
     # algorithmic work per head-token and state element: the forward step (decay 1,
     # M^T k 2, rank-1 update 2) and its adjoint (read 2, dS^T k 2, S_t do 2,
     # dk 4, dM 2, dg 2, decay 1) = 20 flops; fp32 on CUDA cores
     flops = 20.0 * dk * dv * T * H
-    peak = BWD_FP32_TFLOPS
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    peak = sms * 128 * 2 * 2.07e9 / 1e12
     achieved = flops / (ms * 1e-3) / 1e12
-    return {"what": "dq, dk, dv, dg, dbeta, dS0 (fp32), token-level SIMT kernels, segment split",
-            "ms_per_step": round(ms, 4), "tokens_per_s": round(N and T / (ms * 1e-3), 1),
+    return {"workload": SHORT,
+            "what": "dq, dk, dv, dg, dbeta, dS0 (fp32), token-level SIMT kernels, segment split",
+            "ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
             "segments": kda.prefill_backward_num_segments(desc),
-            "ctas_per_pass": N * H * ((dv + 31) // 32) * kda.prefill_backward_num_segments(desc),
-            "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": peak,
+            "workspace_bytes": int(ws.numel()),
+            "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 2),
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "flops_per_head_token": 20 * dk * dv,
-                         "peak_from": "152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz"}}
+                         "peak_from": "%d SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (maximum "
+                                      "SM clock)" % sms}}
 
 
-def run_e2e(args, kda, x, N, T, H, dk, dv, dev, dist, world):
-    """One-call prefill with its inputs copied in from pinned host memory and its
-    outputs (out, S_final) copied back, every step.  Steps alternate between two
-    streams with their own device buffers, as a caller streaming prefills would
-    run them: one step's input copies overlap the previous step's compute and
-    output copies."""
+def run_e2e(args, kda, x, Sg, out, SF, ws, dev, dist, world):
+    """The headline call end to end: every step copies q, k, v, g, beta in from
+    pinned host memory, runs kda_prefill_chunked and copies out and S_final back,
+    all inside the timed region (one stream; the device buffers are the headline
+    leg's own, rewritten with the same values)."""
     import torch
-    host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
-    desc = kda.prefill_desc(x["q"], x["v"], x["cu_seqlens"])
-    nstreams = 2
-    streams = [torch.cuda.Stream(dev) for _ in range(nstreams)]
-    sets = []
-    for _ in range(nstreams):
-        sets.append({
-            "in": {n: torch.empty_like(x[n]) for n in host},
-            "out_d": torch.empty_like(x["v"]),
-            "sf_d": torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev),
-            "ws": torch.empty(max(1, kda.prefill_workspace_size(desc)), dtype=torch.uint8,
-                              device=dev),
-            "out_h": torch.empty((T, H, dv), dtype=x["q"].dtype).pin_memory(),
-            "sf_h": torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory(),
-        })
+    names = ("q", "k", "v", "g", "beta")
+    try:
+        host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        sf_h = torch.empty(SF.shape, dtype=SF.dtype, pin_memory=True)
+    except RuntimeError as e:  # not enough pinnable host memory on this machine
+        return {"value": None, "unavailable": "pinned host buffers: %s" % str(e)[:120]}
+    for n in names:
+        host[n].copy_(x[n])
+    T = x["q"].shape[0]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sets[0]["out_h"].numel() * sets[0]["out_h"].element_size() + \
-        sets[0]["sf_h"].numel() * sets[0]["sf_h"].element_size()
+    d2h = out_h.numel() * out_h.element_size() + sf_h.numel() * sf_h.element_size()
 
-    def one(i):
-        b, st = sets[i % nstreams], streams[i % nstreams]
-        with torch.cuda.stream(st):
-            for n in host:
-                b["in"][n].copy_(host[n], non_blocking=True)
-            kda.prefill_chunked(b["in"]["q"], b["in"]["k"], b["in"]["v"], b["in"]["g"],
-                                b["in"]["beta"], None, x["cu_seqlens"], out=b["out_d"],
-                                S_final=b["sf_d"], workspace=b["ws"])
-            b["out_h"].copy_(b["out_d"], non_blocking=True)
-            b["sf_h"].copy_(b["sf_d"], non_blocking=True)
+    def one():
+        for n in names:
+            x[n].copy_(host[n], non_blocking=True)
+        kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["cu_seqlens"],
+                            num_segments=Sg, out=out, S_final=SF, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        sf_h.copy_(SF, non_blocking=True)
 
-    main = torch.cuda.current_stream(dev)
-    for st in streams:
-        st.wait_stream(main)  # inputs and cu_seqlens are ready
-    for i in range(3):
-        one(i)
+    one()
     torch.cuda.synchronize()
     barrier(dist)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(main)
-    for st in streams:
-        st.wait_event(e0)
-    for i in range(args.e2e_steps):
-        one(i)
-    for st in streams:
-        main.wait_stream(st)
-    e1.record(main)
+    e0, e1 = ev_pair()
+    e0.record()
+    for _ in range(args.e2e_steps):
+        one()
+    e1.record()
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
-    # the bound: the step's input bytes as one pinned host-to-device copy (the
-    # link, not the kernels, limits this leg)
-    flat_h = torch.empty(h2d, dtype=torch.uint8).pin_memory()
-    flat_d = torch.empty(h2d, dtype=torch.uint8, device=dev)
-    for _ in range(3):
-        flat_d.copy_(flat_h, non_blocking=True)
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    c0.record(main)
-    for _ in range(10):
-        flat_d.copy_(flat_h, non_blocking=True)
-    c1.record(main)
-    torch.cuda.synchronize()
-    link_gbs = h2d * 10 / (c0.elapsed_time(c1) * 1e-3) / 1e9
     step_ms = ms / args.e2e_steps
+    # the bound: the step's input bytes over the host-to-device link (one pinned copy
+    # of q, timed alone, gives the link's rate)
+    c0, c1 = ev_pair()
+    c0.record()
+    x["q"].copy_(host["q"], non_blocking=True)
+    c1.record()
+    torch.cuda.synchronize()
+    link = host["q"].numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
     return {"value": round(T * args.e2e_steps * world / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(step_ms, 4), "streams": nstreams,
-            "h2d_link_gbs": round(link_gbs, 1),
-            "frac_of_link": round(h2d / (step_ms * 1e-3) / 1e9 / link_gbs, 3)}
+            "ms_per_step": round(step_ms, 3), "streams": 1,
+            "h2d_link_gbs": round(link, 1),
+            "link_bound_ms": round((h2d + d2h) / (link * 1e9) * 1e3, 3)}
 
 
-def run_decode(args, kda, make_decode_inputs, w, dev, dist, world, peaks, rank):
+def run_decode(kda, make_decode_inputs, w, dev, dist, world, peaks, rank):
     import torch
     steps = w["steps"]
     x = make_decode_inputs(w["batch"], w["H"], w["dk"], w["dv"], steps, w["act"],
                            s0_std=w["s0_std"], seed=rank, device=dev)
     S = x["S0"].clone()
     out = torch.empty((w["batch"], w["H"], w["dv"]), dtype=x["q"].dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     for t in range(3):
-        kda.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], S, out=out)
+        kda.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], S, out=out,
+                        dev_status=status)
     S.copy_(x["S0"])
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
@@ -585,10 +591,13 @@ def run_decode(args, kda, make_decode_inputs, w, dev, dist, world, peaks, rank):
     time.sleep(0.3)
     ev[0].record()
     for t in range(steps):
-        kda.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], S, out=out)
+        kda.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], S, out=out,
+                        dev_status=status)
         ev[t + 1].record()
     torch.cuda.synchronize()
     clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError("decode reported device status %d" % int(status.item()))
     per = [ev[t].elapsed_time(ev[t + 1]) for t in range(steps)]
     total = max_over_ranks(sum(per), dist, dev)
     units = w["batch"] * w["H"]
@@ -597,7 +606,7 @@ def run_decode(args, kda, make_decode_inputs, w, dev, dist, world, peaks, rank):
                                 4 * w["dk"] + 4)
     achieved = bytes_per_launch / (statistics.mean(per) / 1e3) / 1e9
     return {"value": round(w["batch"] * steps * world / (total / 1e3), 1), "unit": "tokens/s",
-            "workload": "kda_decode_b256_h56_d128_x64", "steps": steps,
+            "workload": DECODE, "steps": steps,
             "ms_per_step": round(total / steps, 5), "gpu_launches": steps,
             "clocks": clk,
             "roofline": {"bound": "hbm", "kernel": "decode_step", "achieved": round(achieved, 1),
@@ -607,28 +616,43 @@ def run_decode(args, kda, make_decode_inputs, w, dev, dist, world, peaks, rank):
                          "peak_source": peaks["source"] + " (burst copy)"}}
 
 
-def cpu_baseline(x, N, H, target_s=8.0):
+def _oracle_prefix(x, tokens, head=0):
+    """A token prefix of one head of a prefill workload, as fp64 host arrays."""
+    import numpy as np
+    f = lambda t: np.ascontiguousarray(t[:tokens, head:head + 1].detach().float().cpu().double()
+                                       .numpy())
+    return [f(x[n]) for n in ("q", "k", "v", "g", "beta")]
+
+
+def _headline_host_inputs(seed, tokens):
+    """A bounded sample of the headline workload for the oracle: `tokens` tokens of
+    one head at d = 128 in BF16, drawn on the host with the headline's recipe
+    (q, k unit rows, v ~ N(0, 1), g = -5 sigmoid(N(0, 1)), beta = sigmoid(N(0, 1)))."""
+    from kimi_delta_attention_18_gb300.inputs import WORKLOADS, make_prefill_inputs
+    w = WORKLOADS[HEADLINE]
+    x = make_prefill_inputs([tokens], 1, w["dk"], w["dv"], w["act"], seed=seed)
+    return _oracle_prefix(x, tokens)
+
+
+def cpu_baseline(seed, target_s=10.0):
     """The fp64 oracle as it stands, on the host cores, over a bounded sample of the
-    same workload (the first heads of the batch, whole sequence)."""
+    headline workload: a token prefix of one head, sized to ~target_s seconds."""
     import oracle
-    f = lambda t: t.detach().float().cpu().double().numpy()
-    q, k, v, g, b = (f(x[n]) for n in ("q", "k", "v", "g", "beta"))
-    cu = x["cu_seqlens"].cpu().numpy()
     threads = oracle.host_threads()
+    xs = _headline_host_inputs(seed, 1 << 17)
     t0 = time.perf_counter()
-    oracle.kda_forward(q[:, :1], k[:, :1], v[:, :1], g[:, :1], b[:, :1], None, cu,
-                       threads=threads)
-    one = time.perf_counter() - t0
-    heads = max(1, min(H, int(target_s / max(one, 1e-3))))
+    oracle.kda_forward(*(a[:4096] for a in xs), threads=threads)
+    per_tok = (time.perf_counter() - t0) / 4096
+    n = int(max(4096, min(xs[0].shape[0], target_s / max(per_tok, 1e-9))))
     t0 = time.perf_counter()
-    oracle.kda_forward(q[:, :heads], k[:, :heads], v[:, :heads], g[:, :heads], b[:, :heads],
-                       None, cu, threads=threads)
+    oracle.kda_forward(*(a[:n] for a in xs), threads=threads)
     dt = time.perf_counter() - t0
-    T = q.shape[0]
-    return {"value": round(T * heads / H / dt, 2), "unit": "tokens/s", "cores": threads,
+    H = 56
+    return {"value": round(n / H / dt, 2), "unit": "tokens/s", "cores": threads,
             "kind": "oracle",
-            "sample": "%d of %d heads x %d tokens (fp64 token-by-token C oracle, %.2f s)" %
-                      (heads, H, T, dt)}
+            "sample": "1 of %d heads x %d of 1048576 tokens of the headline workload's recipe, "
+                      "drawn on the host (fp64 token-by-token C oracle, %.2f s); tokens/s "
+                      "counts all 56 heads of a token" % (H, n, dt)}
 
 
 def cpu_baseline_backward(x, H, tokens=512):
@@ -663,41 +687,37 @@ def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
         return
-    import numpy as np
     import oracle
-    from kimi_delta_attention_18_gb300.inputs import WORKLOADS, make_prefill_inputs
-    w = WORKLOADS[PREFILL]
-    x = make_prefill_inputs(w["lengths"], w["H"], w["dk"], w["dv"], w["act"], seed=0)
-    f = lambda t: t.detach().float().double().numpy()
-    q, k, v, g, b = (f(x[n]) for n in ("q", "k", "v", "g", "beta"))
-    T, H = q.shape[:2]
     threads = oracle.host_threads()
+    xs = _headline_host_inputs(0, 1 << 16)
     # size each step (a token prefix of one head) so the whole run stays within ~2 min
     t0 = time.perf_counter()
-    oracle.kda_forward(q[:512, :1], k[:512, :1], v[:512, :1], g[:512, :1], b[:512, :1],
-                       threads=threads)
-    per_tok = (time.perf_counter() - t0) / 512
+    oracle.kda_forward(*(a[:1024] for a in xs), threads=threads)
+    per_tok = (time.perf_counter() - t0) / 1024
     budget = 100.0 / max(1, args.steps + args.warmup)
-    Ts = int(max(64, min(T, budget / max(per_tok, 1e-9))))
-    sl = lambda a: np.ascontiguousarray(a[:Ts, :1])
-    qs, ks, vs, gs, bs = map(sl, (q, k, v, g, b))
+    Ts = int(max(256, min(xs[0].shape[0], budget / max(per_tok, 1e-9))))
+    xs = [a[:Ts].copy() for a in xs]
     for _ in range(args.warmup):
-        oracle.kda_forward(qs, ks, vs, gs, bs, threads=threads)
+        oracle.kda_forward(*xs, threads=threads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.kda_forward(qs, ks, vs, gs, bs, threads=threads)
+        oracle.kda_forward(*xs, threads=threads)
     dt = time.perf_counter() - t0
+    H = 56
     value = Ts * args.steps / H / dt
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL, "batch": 1, "seq_len": T, "heads": H, "dk": 128,
-                   "dv": 128, "chunk": 16},
+        "config": {"workload": HEADLINE, "batch": 1, "seq_len": 1048576, "heads": H, "dk": 128,
+                   "dv": 128, "chunk": 16, "segments": 64, "state": "fp64",
+                   "parallelism": "host threads"},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle",
-                         "sample": "1 of %d heads x %d tokens per step (fp64 C oracle)" % (H, Ts)},
+                         "sample": "1 of %d heads x %d tokens per step of the headline "
+                                   "workload's recipe, drawn on the host (fp64 C oracle); "
+                                   "tokens/s counts all 56 heads of a token" % (H, Ts)},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}), flush=True)
 
@@ -719,20 +739,24 @@ def run_profile_case(name):
         for _ in range(2):
             kda.prefill_segments(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                  x["cu_seqlens"], 1)
+    elif name == "prefill_kcp_h56_t64k":
+        # the headline's kernels at 1/16 of its length: 56 heads x 65,536 tokens in 4
+        # segments of 16,384 tokens (the headline's segment length); 5.6 GB of inputs
+        x = make_prefill_inputs([65536], 56, 128, 128, "bf16", device=dev)
+        for _ in range(2):
+            kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                x["cu_seqlens"], num_segments=4)
     elif name == "prefill_h8_t4096":
-        # the benchmark's own workload: transfer pass, scan and combine per call
         x = make_prefill_inputs([4096], 8, 128, 128, "bf16", device=dev)
         for _ in range(2):
             kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                 x["cu_seqlens"])
     elif name == "prefill_ckpt_h8_t4096":
-        # the benchmark's workload with a state checkpoint every 512 tokens
         x = make_prefill_inputs([4096], 8, 128, 128, "bf16", device=dev)
         for _ in range(2):
             kda.prefill_chunked_ckpt(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                      x["cu_seqlens"], ckpt_interval=512)
     elif name == "backward_h8_t1024":
-        # the backward kernel on the benchmark's shape at a quarter of its length
         from kimi_delta_attention_18_gb300.inputs import make_backward_adjoints
         x = make_prefill_inputs([1024], 8, 128, 128, "bf16", device=dev)
         d_out, d_sf = make_backward_adjoints(1024, 1, 8, 128, 128, "bf16", seed=7, device=dev)

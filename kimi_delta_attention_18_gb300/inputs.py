@@ -51,14 +51,20 @@ def make_prefill_inputs(lengths, H, dk, dv, act="bf16", *, seed=0, s0_std=None,
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     dt = DTYPES[act]
-    q_raw = _normal((T, H, dk), gen, device)
-    k_raw = _normal((T, H, dk), gen, device)
-    q = _unit_rows(q_raw).to(dt)
-    k = _unit_rows(k_raw).to(dt)
+    # each fp32 draw is turned into what is kept before the next one is made, so
+    # at most two fp32 copies of one array exist at a time (a 1M-token x 56-head
+    # workload stays well inside device memory)
+    x = _normal((T, H, dk), gen, device)
+    q, q_raw = _unit_rows(x).to(dt), x.to(dt)
+    x = _normal((T, H, dk), gen, device)
+    k, k_raw = _unit_rows(x).to(dt), x.to(dt)
+    del x
     v = _normal((T, H, dv), gen, device).to(dt)
     xg = _normal((T, H, dk), gen, device, mean=-10.0 if slow_decay else 0.0)
+    x_g = xg.to(dt).contiguous()
+    g = torch.sigmoid(xg).mul_(-5.0)
+    del xg
     xb = _normal((T, H), gen, device, mean=-6.0 if slow_decay else 0.0)
-    g = -5.0 * torch.sigmoid(xg)
     beta = torch.sigmoid(xb)
     S0 = None
     if s0_std is not None:
@@ -69,8 +75,7 @@ def make_prefill_inputs(lengths, H, dk, dv, act="bf16", *, seed=0, s0_std=None,
     cu_seqlens = torch.tensor(cu, dtype=torch.int32, device=device)
     return {"q": q, "k": k, "v": v, "g": g.contiguous(), "beta": beta.contiguous(),
             "S0": S0, "cu_seqlens": cu_seqlens, "lengths": lengths,
-            "q_raw": q_raw.to(dt), "k_raw": k_raw.to(dt), "x_g": xg.to(dt).contiguous(),
-            "x_beta": xb.contiguous()}
+            "q_raw": q_raw, "k_raw": k_raw, "x_g": x_g, "x_beta": xb.contiguous()}
 
 
 def make_backward_adjoints(T, N, H, dk, dv, act="bf16", *, seed=0, device="cpu",

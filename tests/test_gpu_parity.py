@@ -100,6 +100,41 @@ def test_bf16_slow_decay_initial_state_and_split(nseg):
     assert rel_err(_np(SF0), S_ref) > 0.1
 
 
+@pytest.mark.parametrize("nseg", [0, 1])
+def test_config1_shape_slow_decay_with_initial_state(nseg):
+    """The short-prefill shape (H = 8, T = 4096) with slow forgetting and S0 ~
+    N(0, 1): S0 and every segment's transfer matrix stay material over the whole
+    sequence, so the chosen split (nseg = 0) and the single pass are both held to
+    the oracle on every head, and dropping S0 must break parity."""
+    x = _gpu_inputs([4096], 8, 128, 128, "bf16", s0_std=1.0, seed=21, slow_decay=True,
+                    device="cuda")
+    o_ref, S_ref = _oracle_prefill(x)
+    out, SF = _run(x, nseg)
+    assert rel_err(_np(out), o_ref) <= 2e-2
+    assert rel_err(_np(SF), S_ref) <= 2e-2
+    _, SF0 = _run(x, nseg, S0=None)
+    assert rel_err(_np(SF0), S_ref) > 0.1
+
+
+def test_config4_shape_slow_decay_64_segments_sampled_heads():
+    """The long-context shape (H = 56, 64 segments) at a reduced length (64 x 256
+    tokens) with slow forgetting and S0 ~ N(0, 1): every segment's start state is
+    the composition of all the segments before it, so a wrong transfer matrix or a
+    wrong scan step shows.  Sampled heads against the oracle; dropping S0 must
+    break parity."""
+    T, H, nseg = 64 * 256, 56, 64
+    x = _gpu_inputs([T], H, 128, 128, "bf16", s0_std=1.0, seed=22, slow_decay=True,
+                    device="cuda")
+    out, SF = _run(x, nseg)
+    heads = [3, 40]
+    o_ref, S_ref = _oracle_prefill(x, heads=heads)
+    assert rel_err(_np(out[:, heads]), o_ref) <= 2e-2
+    assert rel_err(_np(SF[:, heads]), S_ref) <= 2e-2
+    assert torch.isfinite(out.float()).all() and torch.isfinite(SF).all()
+    _, SF0 = _run(x, nseg, S0=None)
+    assert rel_err(_np(SF0[:, heads]), S_ref) > 0.1
+
+
 def test_config2_varlen_full_size_sampled_heads():
     w = WORKLOADS["kda_prefill_varlen4_h56_t81920_d128_s0"]
     x = _gpu_inputs(w["lengths"], w["H"], w["dk"], w["dv"], w["act"], s0_std=w["s0_std"],
