@@ -117,12 +117,14 @@ def test_config1_shape_slow_decay_with_initial_state(nseg):
 
 
 def test_config4_shape_slow_decay_64_segments_sampled_heads():
-    """The long-context shape (H = 56, 64 segments) at a reduced length (64 x 256
+    """The long-context shape (H = 56, 64 segments) at a reduced length (64 x 128
     tokens) with slow forgetting and S0 ~ N(0, 1): every segment's start state is
     the composition of all the segments before it, so a wrong transfer matrix or a
     wrong scan step shows.  Sampled heads against the oracle; dropping S0 must
-    break parity."""
-    T, H, nseg = 64 * 256, 56, 64
+    break parity.  (The stress mix has E[g] of about -3.7e-4 per token, so S0
+    still carries about e^-3 of its weight after 8192 tokens, far above the written
+    part's share; at 16K tokens it would be e^-6.)"""
+    T, H, nseg = 64 * 128, 56, 64
     x = _gpu_inputs([T], H, 128, 128, "bf16", s0_std=1.0, seed=22, slow_decay=True,
                     device="cuda")
     out, SF = _run(x, nseg)

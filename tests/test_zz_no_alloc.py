@@ -1,6 +1,7 @@
 """The allocation-free prefill entry point (for callers that may not call
 cudaMalloc, e.g. an engine plugin enqueueing work into memory it was handed up
-front) must give what the ordinary one-call prefill gives.
+front) must give what the ordinary one-call prefill gives, and what the fp64
+oracle gives.
 
 Called through the C ABI twice in a row, on different inputs, so that whatever
 the first call leaves in the library's shared scratch cannot leak into the
@@ -11,6 +12,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import kimi_delta_attention_18_gb300 as kda
 from kimi_delta_attention_18_gb300.inputs import make_prefill_inputs
 from tests.conftest import rel_err
@@ -52,6 +54,12 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row():
         assert int(status.item()) == 0
         assert rel_err(out.float().cpu().numpy(), ref_out.float().cpu().numpy()) <= TOL
         assert rel_err(SF.cpu().numpy(), ref_SF.cpu().numpy()) <= TOL
+        # and directly against the oracle on the same inputs
+        f = lambda t: None if t is None else t.detach().float().cpu().double().numpy()
+        o_ref, S_ref = oracle.kda_forward(*(f(x[n]) for n in ("q", "k", "v", "g", "beta")),
+                                          f(x["S0"]), x["cu_seqlens"].cpu().numpy())
+        assert rel_err(out.float().cpu().numpy(), o_ref) <= TOL
+        assert rel_err(SF.cpu().numpy(), S_ref) <= TOL
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
