@@ -137,6 +137,41 @@ def test_config4_shape_slow_decay_64_segments_sampled_heads():
     assert rel_err(_np(SF0[:, heads]), S_ref) > 0.1
 
 
+@pytest.mark.parametrize("gated", [False, True])
+def test_two_chain_transfer_pass_ragged(gated):
+    """Enough segments (N x H x S = 3 x 16 x 4 = 192, at least one per SM) that the
+    transfer pass runs a segment's identity-start and zero-start chains in one CTA
+    from one prep; ragged lengths with partial last blocks, slow forgetting and
+    S0 ~ N(0, 1), plain and from the gate pre-activations, against the oracle."""
+    lengths = [300, 45, 130]
+    H, nseg = 16, 4
+    x = _gpu_inputs(lengths, H, 128, 128, "bf16", s0_std=1.0, seed=17, slow_decay=True,
+                    device="cuda")
+    assert len(lengths) * H * nseg >= torch.cuda.get_device_properties(0).multi_processor_count
+    if gated:
+        out, SF = kda.prefill_chunked_gated(x["q_raw"], x["k_raw"], x["v"], x["x_g"],
+                                            x["x_beta"], x["S0"], x["cu_seqlens"],
+                                            num_segments=nseg)
+        torch.cuda.synchronize()
+        qn, kn, g, beta = oracle.gate_prologue(_np(x["q_raw"]), _np(x["k_raw"]), _np(x["x_g"]),
+                                               _np(x["x_beta"]))
+        o_ref, S_ref = oracle.kda_forward(qn, kn, _np(x["v"]), g, beta, _np(x["S0"]),
+                                          x["cu_seqlens"].cpu().numpy())
+    else:
+        out, SF = _run(x, nseg)
+        o_ref, S_ref = _oracle_prefill(x)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(SF).all()
+    assert rel_err(_np(out), o_ref) <= 2e-2
+    assert rel_err(_np(SF), S_ref) <= 2e-2
+    if not gated:  # the stage entry point in the same regime: A, B against the oracle
+        A, B = kda.state_transfer(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], nseg)
+        torch.cuda.synchronize()
+        A_ref, B_ref = oracle.kda_state_transfer(_np(x["k"]), _np(x["v"]), _np(x["g"]),
+                                                 _np(x["beta"]), x["cu_seqlens"].cpu().numpy(),
+                                                 nseg)
+        assert rel_err(_np(A), A_ref) <= 2e-2 and rel_err(_np(B), B_ref) <= 2e-2
+
+
 def test_config2_varlen_full_size_sampled_heads():
     w = WORKLOADS["kda_prefill_varlen4_h56_t81920_d128_s0"]
     x = _gpu_inputs(w["lengths"], w["H"], w["dk"], w["dv"], w["act"], s0_std=w["s0_std"],
