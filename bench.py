@@ -52,7 +52,7 @@ ONE_PASS_B = 4 * 256 + 512 + 4
 KCP_B = (2 * 256 + 512 + 4) + ONE_PASS_B
 CKPT_INTERVAL = 4096
 PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_kcp_h56_t64k",
-                 "prefill_ckpt_h8_t4096", "backward_h8_t1024")
+                 "prefill_ckpt_h8_t4096", "backward_h8_t1024", "backward_h8_t4096")
 # the ncu summary that gives the transfer pass's DRAM traffic per launch, and the
 # kernel source it was taken on
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "prefill_tc_kernel_kcp_h56_t64k_d128.md")
@@ -756,10 +756,11 @@ def run_profile_case(name):
         for _ in range(2):
             kda.prefill_chunked_ckpt(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                      x["cu_seqlens"], ckpt_interval=512)
-    elif name == "backward_h8_t1024":
+    elif name in ("backward_h8_t1024", "backward_h8_t4096"):
         from kimi_delta_attention_18_gb300.inputs import make_backward_adjoints
-        x = make_prefill_inputs([1024], 8, 128, 128, "bf16", device=dev)
-        d_out, d_sf = make_backward_adjoints(1024, 1, 8, 128, 128, "bf16", seed=7, device=dev)
+        T = 1024 if name.endswith("1024") else 4096
+        x = make_prefill_inputs([T], 8, 128, 128, "bf16", device=dev)
+        d_out, d_sf = make_backward_adjoints(T, 1, 8, 128, 128, "bf16", seed=7, device=dev)
         for _ in range(2):
             kda.prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                  x["cu_seqlens"], d_out, d_sf)

@@ -107,6 +107,28 @@ int backward_segments(const kda_prefill_desc_t *d) {
     return sg < 1 ? 1 : (int)sg;
 }
 
+// BF16 at dk = dv = 128: the chunked tensor-core backward (16-byte aligned rows);
+// otherwise the token-level fp32 one.
+bool backward_chunked(const kda_prefill_desc_t *d) {
+    return d->act_dtype == KDA_DTYPE_BF16 && d->dk == 128 && d->dv == 128;
+}
+// Segments per sequence of the chunked backward.  It runs four sequential passes
+// (transfer pass, zero-end adjoint pass, forward and adjoint passes from the
+// scanned states) around two cheap tensor-core scans, so it splits further than
+// the forward: the fewest segments that give every SM a one-chain CTA, with at
+// least 4 blocks of 16 tokens per segment (mean length) and at most 64.
+int backward_chunked_segments(const kda_prefill_desc_t *d) {
+    if (d->num_segments > 0) return d->num_segments;
+    const long long chains = (long long)d->num_seqs * d->num_heads;
+    const long long sms = sm_count();
+    if (chains == 0 || chains >= sms) return 1;
+    long long S = (sms + chains - 1) / chains;
+    const long long blocks = ((long long)d->total_tokens / d->num_seqs + 15) / 16;
+    if (S > blocks / 4) S = blocks / 4;
+    if (S > 64) S = 64;
+    return S < 1 ? 1 : (int)S;
+}
+
 size_t act_bytes(const kda_prefill_desc_t *d) { return d->act_dtype == KDA_DTYPE_BF16 ? 2 : 4; }
 
 // Split workspace: transfer matrices, zero-initial states and start states for
@@ -349,13 +371,16 @@ kda_status_t kda_prefill_chunked_ckpt(const kda_prefill_desc_t *desc, const void
 
 size_t kda_prefill_backward_workspace_size(const kda_prefill_desc_t *desc) {
     if (check_desc(desc) != KDA_OK) return 0;
+    if (backward_chunked(desc))
+        return backward_chunked_workspace_bytes(desc->num_seqs, desc->total_tokens,
+                                                desc->num_heads, backward_chunked_segments(desc));
     return backward_workspace_bytes(desc->num_seqs, desc->total_tokens, desc->num_heads, desc->dk,
                                     desc->dv, backward_segments(desc));
 }
 
 int32_t kda_prefill_backward_num_segments(const kda_prefill_desc_t *desc) {
     if (check_desc(desc) != KDA_OK) return 0;
-    return backward_segments(desc);
+    return backward_chunked(desc) ? backward_chunked_segments(desc) : backward_segments(desc);
 }
 
 kda_status_t kda_prefill_backward(const kda_prefill_desc_t *desc, const void *q, const void *k,
@@ -375,6 +400,21 @@ kda_status_t kda_prefill_backward(const kda_prefill_desc_t *desc, const void *q,
                           dq, dk, dv, dg, dbeta, dS0};
     for (const void *p : ptrs)
         if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
+    if (backward_chunked(desc)) {
+        // rows move as 16-byte pieces and tensor-map boxes
+        const void *rows[] = {q, k, v, g, d_out};
+        for (const void *p : rows)
+            if (desc->total_tokens > 0 && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+        const int Sg = backward_chunked_segments(desc);
+        const size_t need = backward_chunked_workspace_bytes(desc->num_seqs, desc->total_tokens,
+                                                             desc->num_heads, Sg);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+        PrefillArgs a = base_args(desc);
+        a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0; a.cu = cu_seqlens;
+        a.dev_status = dev_status;
+        return from_cuda(launch_backward_chunked(a, d_out, d_S_final, dq, dk, dv, dg, dbeta, dS0,
+                                                 Sg, workspace, (cudaStream_t)stream));
+    }
     const int Sg = backward_segments(desc);
     const size_t need = backward_workspace_bytes(desc->num_seqs, desc->total_tokens,
                                                  desc->num_heads, desc->dk, desc->dv, Sg);

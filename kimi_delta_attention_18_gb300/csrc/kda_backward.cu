@@ -821,4 +821,92 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
     return run(dim3((unsigned)(p.N * p.H), (unsigned)ncb, (unsigned)a.Sg), false);
 }
 
+// ---------------------------------------------------------------------------
+// Chunked backward for BF16 activations at dk = dv = 128.
+//
+// The state at every 16-token block end and the adjoint at every block end are
+// produced by the prefill kernels (forward chain with chunk states; adjoint
+// chain run from the last block to the first), then every block's gradients
+// come from kda_bwd_chunk.cu in parallel.  With Sg > 1 segments per sequence the
+// two chains start from scanned segment states: the transfer pass gives A_s (as
+// the BF16 hi/lo images of A_s for the forward scan and of A_s^T, segments
+// reversed, for the adjoint scan) and B_s, the adjoint chain from a zero end
+// adjoint gives B^_s (segments reversed), and the tensor-core scan runs twice:
+// X_s = A_{s-1} X_{s-1} + B_{s-1} (start states) and, over the reversed segments,
+// Y_s = A_{s+1}^T Y_{s+1} + B^_{s+1} (end adjoints).
+// Workspace (each piece 256-byte aligned): forward states [T_tot / 16][H][128][128]
+// BF16, adjoints [ceil(T_tot / 16) + N][H][128][128] BF16, and with Sg > 1 the
+// images of A and A^T (2 x 2 x 128 x 128 BF16) and B, B^, X, Y (fp32) per
+// (sequence, head, segment).
+size_t backward_chunked_workspace_bytes(int N, int T_tot, int H, int Sg) {
+    const size_t img = (size_t)128 * 128 * 2;
+    const size_t fwd = r256((size_t)(T_tot / 16) * H * img);
+    const size_t adj = r256((size_t)((T_tot + 15) / 16 + N) * H * img);
+    const size_t seg = Sg > 1 ? 6 * r256((size_t)N * H * Sg * 128 * 128 * 4) : 0;
+    return fwd + adj + seg;
+}
+
+cudaError_t launch_backward_chunked(const PrefillArgs &p, const void *dout, const float *dSF,
+                                    float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                                    float *dS0, int Sg, void *workspace, cudaStream_t st) {
+    if (p.N == 0 || p.H == 0) return cudaSuccess;
+    const size_t img = (size_t)128 * 128 * 2;
+    uint8_t *ws = (uint8_t *)workspace;
+    __nv_bfloat16 *fwd_states = (__nv_bfloat16 *)ws;
+    ws += r256((size_t)(p.T_tot / 16) * p.H * img);
+    __nv_bfloat16 *adj_states = (__nv_bfloat16 *)ws;
+    ws += r256((size_t)((p.T_tot + 15) / 16 + p.N) * p.H * img);
+    PrefillArgs base = p;
+    base.Sg = Sg;
+    base.seg_begin = 0;
+    base.seg_count = Sg;
+    base.out = nullptr;
+    base.S_final = nullptr;
+    base.aux_out = nullptr;
+    base.emit_out = 0;
+    base.ckpt_interval = 0;
+    base.gate = 0;
+    PrefillArgs fwd = base, adj = base;
+    fwd.mode = adj.mode = MODE_OUTPUT;
+    fwd.chunk_states = fwd_states;
+    adj.chunk_states = adj_states;
+    adj.rev = 1;
+    adj.v = dout;           // the adjoint chain reads d_out where the forward reads v
+    adj.S_final = dS0;      // the adjoint at the start of segment 0
+    cudaError_t e;
+    if (Sg > 1) {
+        const int units = p.N * p.H;
+        const size_t seg = r256((size_t)units * Sg * 128 * 128 * 4);
+        __nv_bfloat16 *a_img = (__nv_bfloat16 *)ws, *a_img_t = (__nv_bfloat16 *)(ws + seg);
+        float *TB = (float *)(ws + 2 * seg), *TBh = (float *)(ws + 3 * seg);
+        float *X = (float *)(ws + 4 * seg), *Yr = (float *)(ws + 5 * seg);
+        PrefillArgs t = base;  // A_s (both images) and B_s
+        t.mode = MODE_TRANSFER;
+        t.transfer = nullptr;
+        t.transfer_img = a_img;
+        t.transfer_img_t = a_img_t;
+        t.zero_state = TB;
+        if ((e = launch_prefill_tc(t, st)) != cudaSuccess) return e;
+        PrefillArgs tz = base;  // B^_s: the adjoint chain from a zero end adjoint
+        tz.mode = MODE_TRANSFER;
+        tz.rev = 1;
+        tz.v = dout;
+        tz.zero_state = TBh;
+        if ((e = launch_prefill_tc(tz, st)) != cudaSuccess) return e;
+        if ((e = launch_compose(units, Sg, 128, 128, nullptr, a_img, TB, p.S0, X, nullptr, nullptr,
+                                p.dev_status, st)) != cudaSuccess)
+            return e;
+        if ((e = launch_compose(units, Sg, 128, 128, nullptr, a_img_t, TBh, dSF, Yr, nullptr,
+                                nullptr, p.dev_status, st)) != cudaSuccess)
+            return e;
+        fwd.seg_init = X;
+        adj.seg_init = Yr;  // read at the reversed segment index
+    } else {
+        adj.S0 = dSF;  // the adjoint chain starts from d_S_final (NULL: zero)
+    }
+    if ((e = launch_prefill_tc(fwd, st)) != cudaSuccess) return e;
+    if ((e = launch_prefill_tc(adj, st)) != cudaSuccess) return e;
+    return launch_bwd_chunk(p, dout, fwd_states, adj_states, dq, dk, dv, dg, dbeta, st);
+}
+
 }  // namespace kda

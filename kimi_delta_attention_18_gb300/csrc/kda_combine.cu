@@ -141,129 +141,261 @@ __global__ void __launch_bounds__(BF_WARPS * 32) combine_bf16_kernel(
     }
 }
 
-// ---- tcgen05 path: D[t][j] = sum_i aux[t][i] start_s[i][j] over a 128-token tile
+// ---- tcgen05 path: D[t][j] = sum_i aux[t][i] start_s[i][j] over 128-token tiles.
+// A persistent CTA per SM walks a contiguous range of the (sequence, head,
+// segment, tile) list, so consecutive tiles share a segment and its start image
+// is loaded once per segment.  Warp roles:
+//   warp 0   producer: per tile, the A_t^T q_t rows and the out rows as two TMA
+//            boxes each (64 columns x 128 tokens, 128-byte swizzle) into one of
+//            three stages; per segment, the start image (K-major core matrices
+//            without swizzle) by one bulk copy.
+//   warp 1   one thread issues eight tcgen05.mma (M = N = 128, K = 16) per tile
+//            into one of two TMEM accumulators and commits.
+//   warps 2-9 epilogue: thread = (token row = TMEM lane, 64-column half): reads
+//            its 64 products with one tcgen05.ld, adds its zero-start out values
+//            from the stage in fp32 and puts the results back in place; then one
+//            thread stores the tile with one TMA store per 64-column box (a tile
+//            that ends inside the segment is written row by row instead, only its
+//            live rows).
+// A stage is free once its products are done (commit) and its tile has been
+// stored (the bulk store has read the stage); an accumulator once the epilogue
+// has loaded it; the image once the last products of its segment are done.  Every wait is
+// bounded; on an abort the roles stop, copies and products in flight complete
+// before the CTA frees its TMEM, and dev_status records KDA_ERR_TIMEOUT.
 constexpr int TC_TILE = 128;
-constexpr int TC_A = 0;         // aux tile: 2 TMA boxes of 64 channels x 128 rows, 128-byte swizzle
-constexpr int TC_B = 32768;     // start image: K-major core matrices without swizzle (rows j)
-constexpr int TC_O = 65536;     // out tile: 2 TMA boxes of 64 columns x 128 rows, 128-byte swizzle
-constexpr int TC_BAR = 98304;   // [0] operands landed, [8] products done, [16] abort, [24] TMEM base
-constexpr int TC_SMEM = TC_BAR + 32 + 1024;  // + slack for the 1024-byte alignment of the base
-constexpr uint32_t TC_COLS = 128;
-constexpr long long kTcWaitLimit = 4000000000ll;  // ~2 s of SM clocks
+constexpr int TC_NST = 3;
+constexpr int TC_STAGE = 65536;                     // aux (2 x 16 KB) then out (2 x 16 KB)
+constexpr int TC_IMG = TC_NST * TC_STAGE;           // start image, 32 KB
+constexpr int TC_BAR = TC_IMG + 32768;
+enum { PB_FULL = 0, PB_EMPTY = PB_FULL + TC_NST, PB_ACCF = PB_EMPTY + TC_NST, PB_ACCE = PB_ACCF + 2,
+       PB_IMGF = PB_ACCE + 2, PB_IMGE = PB_IMGF + 1, PB_FIN = PB_IMGE + 1, PB_N = PB_FIN + 1 };
+constexpr int TC_MISC = TC_BAR + PB_N * 8;          // [0] abort, [4] TMEM base
+constexpr int TC_SMEM = TC_MISC + 16 + 1024;        // + slack for the 1024-byte alignment
+constexpr uint32_t TC_COLS = 256;                   // two 128-column accumulators
+constexpr long long kTcWaitLimit = 4000000000ll;    // ~2 s of SM clocks
+static_assert(TC_SMEM <= 227 * 1024, "shared memory budget");
 
-// A (the tile's A_t^T q_t rows) and the tile's out rows arrive as two 64-column
-// TMA boxes each with 128-byte swizzle, so every copy moves whole 128-byte row
-// pieces; B, the start image, is K-major without swizzle (core matrices 8 rows x
-// 16 bytes, adjacent along K 2048 bytes apart, 8-row groups 128 bytes apart).
-// The accumulator row m is TMEM lane m, so warp w reads the products of tokens
-// 32w..32w+31 and corrects their out rows in fp32 (each thread reads its row's
-// swizzled chunks: conflict-free).  All waits are bounded; a CTA that gives up
-// records KDA_ERR_TIMEOUT, lets its copies land and frees its TMEM.
-__global__ void __launch_bounds__(128) combine_tc_kernel(const __grid_constant__ PrefillArgs p,
-                                                         const __grid_constant__ CUtensorMap tm_aux,
-                                                         const __grid_constant__ CUtensorMap tm_out,
-                                                         const __nv_bfloat16 *img, int tile_base) {
+struct TileRef {
+    int us;       // (sequence, head, segment) index: (n H + h) Sg + s
+    int h, t0, nt;
+    bool ok;      // the tile has tokens
+};
+
+// Tile f of the list (segments from seg_begin on, ntile tiles reserved per segment).
+__device__ __forceinline__ TileRef tile_ref(const PrefillArgs &p, long long f, int ntile) {
+    TileRef r;
+    const int sact = p.Sg - p.seg_begin;
+    const long long us_act = f / ntile;
+    const int tile = (int)(f % ntile);
+    const int unit = (int)(us_act / sact), s = p.seg_begin + (int)(us_act % sact);
+    const int n = unit / p.H;
+    r.h = unit % p.H;
+    r.us = unit * p.Sg + s;
+    int a, b;
+    r.ok = segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b);
+    r.t0 = a + tile * TC_TILE;
+    r.nt = min(TC_TILE, b - r.t0);
+    r.ok = r.ok && r.t0 < b;
+    return r;
+}
+
+constexpr int TC_EPI = 8;  // epilogue warps
+__global__ void __launch_bounds__(32 * (2 + TC_EPI), 1) combine_tc_kernel(const __grid_constant__ PrefillArgs p,
+                                                            const __grid_constant__ CUtensorMap tm_aux,
+                                                            const __grid_constant__ CUtensorMap tm_out,
+                                                            const __nv_bfloat16 *img, int ntile,
+                                                            long long total) {
     extern __shared__ uint8_t smem_raw[];
     griddep_wait();  // out, A_t^T q_t and the start images come from earlier kernels
     griddep_launch_dependents();
     uint8_t *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(sm);
-    const uint32_t full = sb + TC_BAR, mmad = sb + TC_BAR + 8;
-    volatile int *abort = (volatile int *)(sm + TC_BAR + 16);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int u = blockIdx.x;
-    const int n = u / (p.H * p.Sg), h = (u / p.Sg) % p.H, s = u % p.Sg;
-    if (s < p.seg_begin) return;  // segments before seg_begin start from zeros
-    int a, b;
-    if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b)) return;
-    const int t0 = a + (tile_base + blockIdx.y) * TC_TILE;
-    if (t0 >= b) return;
-    const int nt = min(TC_TILE, b - t0);
-    const size_t unit = (size_t)(u / p.Sg);  // (n, h)
+    auto bar = [&](int i) { return sb + TC_BAR + 8 * i; };
+    volatile int *abort = (volatile int *)(sm + TC_MISC);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long f0 = (long long)blockIdx.x * total / gridDim.x;
+    const long long f1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
 
-    const int row = 32 * warp + lane;  // this thread's token in the tile
-    const bool live = row < nt;
-    uint4 *orow = (uint4 *)((__nv_bfloat16 *)p.out + ((size_t)(t0 + row) * p.H + h) * 128);
-
-    if (tid == 0) {
-        mbar_init(full, 1);
-        mbar_init(mmad, 1);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < TC_NST; ++i) {
+            mbar_init(bar(PB_FULL + i), 1);
+            mbar_init(bar(PB_EMPTY + i), 1 + 1);  // products done + tile stored
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(PB_ACCF + i), 1);
+            mbar_init(bar(PB_ACCE + i), TC_EPI);
+        }
+        mbar_init(bar(PB_IMGF), 1);
+        mbar_init(bar(PB_IMGE), 1);
+        mbar_init(bar(PB_FIN), 1);
         *abort = 0;
         mbar_fence_init();
     }
     if (warp == 0) {
-        tmem_alloc(sb + TC_BAR + 24, TC_COLS);
+        tmem_alloc(sb + TC_MISC + 4, TC_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *(volatile uint32_t *)(sm + TC_BAR + 24);
+    const uint32_t tmem = *(volatile uint32_t *)(sm + TC_MISC + 4);
 
-    bool landed = false;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(full, 3 * 32768);
-        const uint64_t ta = reinterpret_cast<uint64_t>(&tm_aux);
-        const uint64_t to = reinterpret_cast<uint64_t>(&tm_out);
-        // rows past the segment's end come along (the next segment's, or zero fill
-        // past the array); they are never used
+    if (warp == 0) {
+        // ---- producer
+        if (lane == 0) {
+            const uint64_t ta = reinterpret_cast<uint64_t>(&tm_aux);
+            const uint64_t to = reinterpret_cast<uint64_t>(&tm_out);
+            int i = 0, nimg = 0, cur = -1, pending = 0;
+            for (long long f = f0; f < f1; ++f) {
+                const TileRef t = tile_ref(p, f, ntile);
+                if (!t.ok) continue;
+                if (t.us != cur) {  // a new segment: its start image, once the old one is free
+                    if (nimg > 0 && !mbar_wait(bar(PB_IMGE), (nimg - 1) & 1, abort, kTcWaitLimit))
+                        break;
+                    mbar_arrive_expect_tx(bar(PB_IMGF), 32768);
+                    bulk_g2s(sb + TC_IMG, img + (size_t)t.us * kStartImgElems, 32768, bar(PB_IMGF));
+                    cur = t.us;
+                    ++nimg;
+                }
+                const int stg = i % TC_NST;
+                if (!mbar_wait(bar(PB_EMPTY + stg), ((i / TC_NST) & 1) ^ 1, abort, kTcWaitLimit))
+                    break;
+                const uint32_t st = sb + stg * TC_STAGE;
+                mbar_arrive_expect_tx(bar(PB_FULL + stg), 4 * 16384);
+                // rows past the segment's end come along (the next segment's, or zero
+                // fill past the array); they are never used
 #pragma unroll
-        for (int bx = 0; bx < 2; ++bx) {
-            tma_load_2d(sb + TC_A + bx * 16384, ta, h * 128 + 64 * bx, t0, full);
-            tma_load_2d(sb + TC_O + bx * 16384, to, h * 128 + 64 * bx, t0, full);
+                for (int bx = 0; bx < 2; ++bx) {
+                    tma_load_2d(st + bx * 16384, ta, t.h * 128 + 64 * bx, t.t0, bar(PB_FULL + stg));
+                    tma_load_2d(st + 32768 + bx * 16384, to, t.h * 128 + 64 * bx, t.t0,
+                                bar(PB_FULL + stg));
+                }
+                ++i;
+                pending = i;
+            }
+            // on an abort, let the copies in flight land before the CTA exits
+            if (*abort) {
+                volatile int never = 0;
+                for (int k = pending - TC_NST > 0 ? pending - TC_NST : 0; k < pending; ++k)
+                    mbar_wait(bar(PB_FULL + k % TC_NST), (k / TC_NST) & 1, &never, kTcWaitLimit);
+                if (nimg > 0) mbar_wait(bar(PB_IMGF), (nimg - 1) & 1, &never, kTcWaitLimit);
+            }
         }
-        bulk_g2s(sb + TC_B, img + (unit * p.Sg + s) * (size_t)kStartImgElems, 32768, full);
-        landed = mbar_wait(full, 0, abort, kTcWaitLimit);
-        if (landed) {
-            tc_fence_after();
+    } else if (warp == 1) {
+        // ---- products
+        if (lane == 0) {
             const uint32_t idesc = umma_idesc_bf16(128, 128);
+            int i = 0, nimg = 0, cur = -1;
+            for (long long f = f0; f < f1; ++f) {
+                const TileRef t = tile_ref(p, f, ntile);
+                if (!t.ok) continue;
+                if (t.us != cur) {
+                    if (!mbar_wait(bar(PB_IMGF), nimg & 1, abort, kTcWaitLimit)) break;
+                    cur = t.us;
+                    ++nimg;
+                }
+                const int stg = i % TC_NST, acc = i & 1;
+                if (!mbar_wait(bar(PB_FULL + stg), (i / TC_NST) & 1, abort, kTcWaitLimit)) break;
+                if (!mbar_wait(bar(PB_ACCE + acc), ((i >> 1) & 1) ^ 1, abort, kTcWaitLimit)) break;
+                tc_fence_after();
+                const uint32_t st = sb + stg * TC_STAGE;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                umma_bf16(tmem, umma_desc_sw128(sb + TC_A + (kk >> 2) * 16384 + (kk & 3) * 32, 1024),
-                          umma_desc(sb + TC_B + kk * 4096, 2048, 128), idesc, kk > 0);
-            umma_commit(mmad);
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16(tmem + 128 * acc,
+                              umma_desc_sw128(st + (kk >> 2) * 16384 + (kk & 3) * 32, 1024),
+                              umma_desc(sb + TC_IMG + kk * 4096, 2048, 128), idesc, kk > 0);
+                umma_commit(bar(PB_ACCF + acc));
+                umma_commit(bar(PB_EMPTY + stg));
+                // the last tile of this segment in the range frees the image
+                bool last = true;
+                for (long long g = f + 1; g < f1; ++g) {
+                    const TileRef u = tile_ref(p, g, ntile);
+                    if (u.ok) {
+                        last = u.us != cur;
+                        break;
+                    }
+                }
+                if (last) umma_commit(bar(PB_IMGE));
+                ++i;
+            }
+            if (*abort) {  // products in flight complete before TMEM is freed
+                umma_commit(bar(PB_FIN));
+                volatile int never = 0;
+                mbar_wait(bar(PB_FIN), 0, &never, kTcWaitLimit);
+            }
         }
-    }
-    // products done; the operand barrier (long complete) orders the out tile's
-    // landing before this thread's reads of it
-    const bool done = mbar_wait(mmad, 0, abort, kTcWaitLimit) && mbar_wait(full, 0, abort, kTcWaitLimit);
-    if (__all_sync(0xffffffffu, done)) {
-        tc_fence_after();
-        uint4 ov[16];  // this thread's out row from the swizzled tile
+    } else {
+        // ---- epilogue: thread = (token row = TMEM lane 32 (warp % 4) + lane, columns
+        // 64 half .. 64 half + 63 = TMA box `half` of the out tile)
+        const int row = 32 * (warp & 3) + lane, half = (warp - 2) >> 2;
+        const bool leader = warp == 2 && lane == 0;
+        const uint64_t to = reinterpret_cast<uint64_t>(&tm_out);
+        int i = 0, pending = -1;  // stage whose bulk store may still read shared memory
+        for (long long f = f0; f < f1; ++f) {
+            const TileRef t = tile_ref(p, f, ntile);
+            if (!t.ok) continue;
+            const int stg = i % TC_NST, acc = i & 1;
+            bool ok = mbar_wait(bar(PB_ACCF + acc), (i >> 1) & 1, abort, kTcWaitLimit) &&
+                      mbar_wait(bar(PB_FULL + stg), (i / TC_NST) & 1, abort, kTcWaitLimit);
+            // one decision for the eight warps (they meet at a named barrier below)
+            if (named_bar_or(1, 32 * TC_EPI, !ok)) break;
+            tc_fence_after();
+            float d[64];
+            tmem_ld64(tmem + 128 * acc + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * half, d);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(PB_ACCE + acc));  // the accumulator is in registers
+            uint8_t *obox = sm + stg * TC_STAGE + 32768 + half * 16384 + row * 128;
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            ov[q] = *(const uint4 *)(sm + TC_O + (q >> 3) * 16384 + row * 128 +
-                                     (((q & 7) ^ (row & 7)) << 4));
+            for (int q = 0; q < 8; ++q) {  // 16-byte chunk q of this row's box, swizzled
+                uint4 *ptr = (uint4 *)(obox + ((q ^ (row & 7)) << 4));
+                const uint4 ov = *ptr;
+                const __nv_bfloat162 *o2 = (const __nv_bfloat162 *)&ov;
+                const float *dd = d + 8 * q;
+                const float2 a0 = __bfloat1622float2(o2[0]), a1 = __bfloat1622float2(o2[1]);
+                const float2 a2 = __bfloat1622float2(o2[2]), a3 = __bfloat1622float2(o2[3]);
+                *ptr = make_uint4(pack_bf16x2(a0.x + dd[0], a0.y + dd[1]),
+                                  pack_bf16x2(a1.x + dd[2], a1.y + dd[3]),
+                                  pack_bf16x2(a2.x + dd[4], a2.y + dd[5]),
+                                  pack_bf16x2(a3.x + dd[6], a3.y + dd[7]));
+            }
+            const bool full_tile = t.nt == TC_TILE;
+            if (full_tile) fence_async_smem();  // the tile goes out through the TMA engine
+            named_bar_sync(1, 32 * TC_EPI);
+            if (!full_tile && row < t.nt) {  // a partial tile: its live rows, row by row
+                uint4 *orow = (uint4 *)((__nv_bfloat16 *)p.out +
+                                        ((size_t)(t.t0 + row) * p.H + t.h) * 128 + 64 * half);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {  // 32 columns j at a time
-            float d[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * c, d);
-            if (live) {
+                for (int q = 0; q < 8; ++q) orow[q] = *(const uint4 *)(obox + ((q ^ (row & 7)) << 4));
+            }
+            if (!full_tile) named_bar_sync(1, 32 * TC_EPI);  // the stage has been read
+            if (leader) {
+                if (full_tile) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const __nv_bfloat162 *o2 = (const __nv_bfloat162 *)&ov[4 * c + q4];
-                    const float *dd = d + 8 * q4;
-                    uint4 w;
-                    const float2 f0 = __bfloat1622float2(o2[0]), f1 = __bfloat1622float2(o2[1]);
-                    const float2 f2 = __bfloat1622float2(o2[2]), f3 = __bfloat1622float2(o2[3]);
-                    w.x = pack_bf16x2(f0.x + dd[0], f0.y + dd[1]);
-                    w.y = pack_bf16x2(f1.x + dd[2], f1.y + dd[3]);
-                    w.z = pack_bf16x2(f2.x + dd[4], f2.y + dd[5]);
-                    w.w = pack_bf16x2(f3.x + dd[6], f3.y + dd[7]);
-                    orow[4 * c + q4] = w;
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_store_2d(to, sb + stg * TC_STAGE + 32768 + bx * 16384,
+                                     t.h * 128 + 64 * bx, t.t0);
+                    cp_bulk_commit();
+                    cp_bulk_wait_read<1>();  // the previous tile's store has read its stage
+                    if (pending >= 0) mbar_arrive(bar(PB_EMPTY + pending));
+                    pending = stg;
+                } else {
+                    cp_bulk_wait_read<0>();
+                    if (pending >= 0) mbar_arrive(bar(PB_EMPTY + pending));
+                    pending = -1;
+                    mbar_arrive(bar(PB_EMPTY + stg));
                 }
             }
+            ++i;
+        }
+        if (leader) {  // every store has completed before the CTA ends
+            cp_bulk_wait<0>();
+            if (pending >= 0) mbar_arrive(bar(PB_EMPTY + pending));
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && *abort) {
-        dev_fail(p.dev_status, KDA_ERR_TIMEOUT);
-        if (!landed) {  // let the copies in flight land before the CTA exits
-            volatile int never = 0;
-            mbar_wait(full, 0, &never, kTcWaitLimit);
-        }
-    }
+    if (threadIdx.x == 0 && *abort) dev_fail(p.dev_status, KDA_ERR_TIMEOUT);
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, TC_COLS);
@@ -336,14 +468,16 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
             return cudaErrorInvalidValue;
         cudaError_t e = set_max_dynamic_smem((const void *)combine_tc_kernel, TC_SMEM);
         if (e != cudaSuccess) return e;
-        const long long tc_tiles = (seg_tokens + TC_TILE - 1) / TC_TILE;
-        for (long long base = 0; base < tc_tiles; base += 65535) {
-            const unsigned ny = (unsigned)(tc_tiles - base < 65535 ? tc_tiles - base : 65535);
-            e = launch_dependent(combine_tc_kernel, dim3((unsigned)units, ny), dim3(128), TC_SMEM, st,
-                                 a, tm, tmo, start_img, (int)base);
-            if (e != cudaSuccess) return e;
-        }
-        return cudaSuccess;
+        // (sequence, head, segment) x tiles from seg_begin on; one persistent CTA per SM
+        const long long ntile = (seg_tokens + TC_TILE - 1) / TC_TILE;
+        const long long total = (long long)a.N * a.H * (a.Sg - a.seg_begin) * ntile;
+        if (total <= 0) return cudaSuccess;
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess)
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const unsigned grid = (unsigned)(total < sms ? total : sms);
+        return launch_dependent(combine_tc_kernel, dim3(grid), dim3(32 * (2 + TC_EPI)), TC_SMEM, st,
+                                a, tm, tmo, start_img, (int)ntile, total);
     }
     if (a.act == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128) {
         // Tiles per CTA: about one CTA per SM, each reusing its converted start

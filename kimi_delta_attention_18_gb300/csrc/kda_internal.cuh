@@ -87,6 +87,28 @@ struct PrefillArgs {
     // g = -5 sigmoid(x_g), beta = sigmoid(x_beta) and q, k divided by their L2 norm
     // per (token, head) (a zero row stays zero).
     int gate;
+    // Backward (BF16, dk = dv = 128).  rev: the kernel runs the adjoint chain
+    // instead (blocks last to first, v is d_out; the state is the adjoint dS of
+    // the state, stepping dS <- Diag(e^{Gamma_C}) dS' + Qh^T dO - Kh^T dR with
+    // dR = T^T (Mq^T dO + Kb dS')); in MODE_TRANSFER it runs only the chain from a
+    // zero end adjoint (written to zero_state), in MODE_OUTPUT from seg_init (or
+    // S0) and S_final receives the adjoint at the start of segment 0.
+    // chunk_states (if set): [slots][H][dv][dk] BF16, the state transposed (row j
+    // = value column, key channels contiguous): the forward chain writes the state
+    // after every full 16-token block of a sequence to slot
+    // ckpt_base(n, 16) + done / 16 - 1; the adjoint chain writes the adjoint at the
+    // end of every block, before stepping through it, to slot cbase(n) + block
+    // (cbase(n) = sum over m < n of ceil(len_m / 16)).
+    // In rev mode the segments' arrays run in reverse order: seg_init is read and
+    // zero_state written at segment index Sg - 1 - s, so that the adjoint scan
+    // Y_{s-1} = A_s^T Y_s + B^_s is the ordinary forward scan over reversed
+    // segments.  transfer_img_t (MODE_TRANSFER, dk = dv = 128): the identity-start
+    // chain also writes the hi/lo BF16 images of A^T in the layout transfer_img
+    // uses for A ([N,H,Sg][2][128][128], i.e. A row-major), at segment index
+    // Sg - 1 - s, for that reversed scan.
+    int rev;
+    __nv_bfloat16 *chunk_states;
+    __nv_bfloat16 *transfer_img_t;
     int N, T_tot, H, dk, dv;
     int Sg;                 // segments per sequence (layout and bounds)
     int seg_begin;          // segments seg_begin .. seg_begin+seg_count-1 are
@@ -120,6 +142,14 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 // runtime call.  Thread-safe.
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
 
+// First 16-token block of sequence n when every sequence's blocks are numbered
+// one after another (ceil(len / 16) of them per sequence).
+__device__ __forceinline__ int block_base(const int32_t *cu, int n) {
+    int b = 0;
+    for (int m = 0; m < n; ++m) b += (cu[m + 1] - cu[m] + 15) / 16;
+    return b;
+}
+
 // Slot of sequence n's first checkpoint: checkpoints of earlier sequences come
 // first, floor(len / interval) of them per sequence.
 __device__ __forceinline__ int ckpt_base(const int32_t *cu, int n, int interval) {
@@ -152,6 +182,17 @@ size_t backward_workspace_bytes(int N, int T_tot, int H, int dk, int dv, int Sg)
 cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float *dSF, float *dq,
                             float *dk, float *dv, float *dg, float *dbeta, float *dS0, int Sg,
                             void *workspace, cudaStream_t st);
+// Chunked backward for BF16 activations at dk = dv = 128 (16-byte aligned rows):
+// its workspace, the whole backward, and its last kernel (the per-block
+// gradients from the forward states and adjoints at every block end).
+size_t backward_chunked_workspace_bytes(int N, int T_tot, int H, int Sg);
+cudaError_t launch_backward_chunked(const PrefillArgs &p, const void *dout, const float *dSF,
+                                    float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                                    float *dS0, int Sg, void *workspace, cudaStream_t st);
+cudaError_t launch_bwd_chunk(const PrefillArgs &p, const void *dout,
+                             const __nv_bfloat16 *fwd_states, const __nv_bfloat16 *adj_states,
+                             float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                             cudaStream_t st);
 bool decode_tma_supported(int dk, int dv);
 // dev_status (nullable) receives KDA_ERR_TIMEOUT if a bounded wait gives up.
 cudaError_t launch_decode_tma(int batch, int H, int act, const void *q, const void *k,

@@ -151,10 +151,28 @@ struct Ctx {
     volatile int *abort;
     int n, h, s;
     int seq0, ckpt_base;  // the sequence's first token; its first checkpoint slot
+    int cs_base;          // first chunk-state slot of the sequence (chunk_states)
     int t_begin, t_end, nchunks;
     bool transfer, partA, want_q, want_v;
     __device__ uint32_t bar(int i) const { return sbase + BAR_OFF + 8 * i; }
 };
+
+// Index of the sequence with the r-th longest length (ties: lower index first),
+// for N <= 32; every lane of the warp takes part.  CTAs are handed out in
+// launch order, so giving the first CTAs the longest sequences' chains starts
+// the critical path first (longest processing time first): with more chains
+// than SMs a long sequence would otherwise wait for a wave of short ones.
+__device__ __forceinline__ int longest_first(const PrefillArgs &p, int r) {
+    const int lane = threadIdx.x & 31;
+    const int len = lane < p.N ? p.cu[lane + 1] - p.cu[lane] : -1;
+    int rank = 0;
+    for (int m = 0; m < p.N; ++m) {
+        const int lm = __shfl_sync(0xffffffffu, len, m);
+        rank += (lm > len) || (lm == len && m < lane);
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < p.N && rank == r);
+    return hit ? __ffs(hit) - 1 : r;
+}
 
 // Every lane polls the barrier (each with acquire semantics), so the warp does
 // not split around the wait: a lane-0 wait with the other lanes parked at a
@@ -263,7 +281,7 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
 // One warp prepares one whole block: elementwise factors, L and Mq and the
 // solve for T, written with V into a record slot.  Prep warp p takes
 // blocks p, p + 4, p + 8, ...; it frees the input stage as soon as it has read it.
-template <bool WANT_Q, bool GATE>
+template <bool WANT_Q, bool GATE, bool REV>
 __device__ __forceinline__ void prep_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int pw = (threadIdx.x >> 5) - W_PREP0;
@@ -279,12 +297,15 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
     // The warp loads its own blocks: one 2D tensor-map TMA copy per array (whole
     // 16-row boxes; rows past the block's end hold the next sequence's tokens,
     // masked below, or past the array zero fill).
+    // the c-th block prepared is block c of the segment, or with REV block
+    // nchunks - 1 - c (the adjoint chain runs from the last block to the first)
+    auto first_token = [&](int c) { return x.t_begin + C * (REV ? x.nchunks - 1 - c : c); };
     auto issue = [&](int c) {
         if (lane == 0) {
             const uint32_t bytes =
                 (WANT_Q ? 4096u : 0u) + 4096u + (x.want_v ? 4096u : 0u) + (GATE ? 4096u : 8192u);
             mbar_arrive_expect_tx(full, bytes);
-            const int xc = x.h * D, t0 = x.t_begin + C * c;
+            const int xc = x.h * D, t0 = first_token(c);
             if (WANT_Q) tma_load_2d(in_s + IN_Q, x.tm_q, xc, t0, full);
             tma_load_2d(in_s + IN_K, x.tm_k, xc, t0, full);
             if (x.want_v) tma_load_2d(in_s + IN_V, x.tm_v, xc, t0, full);
@@ -294,7 +315,7 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
     // beta of rows g8 and g8 + 8 (for L) and of column lane (for T), zero past the
     // block's end; loaded one block ahead
     auto load_beta = [&](int c, float &lo, float &hi, float &col) {
-        const int t0 = x.t_begin + C * c, nt = min(C, x.t_end - t0);
+        const int t0 = first_token(c), nt = min(C, x.t_end - t0);
         const float *bp = p.beta + (size_t)t0 * p.H + x.h;
         auto b = [&](int r) {  // beta, or sigmoid(x_beta) with the fused prologue
             const float v = bp[(size_t)r * p.H];
@@ -321,7 +342,7 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
         if (!warp_wait(x, B_IN_FULL + st, uses & 1)) break;
         uint8_t *rec = x.smem + REC_OFF + slot * R_SIZE;
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
-        const int nt = min(C, x.t_end - (x.t_begin + C * c));
+        const int nt = min(C, x.t_end - first_token(c));
 
         // ---- fused prologue: inverse L2 norms of this block's k and q rows (a zero
         // row keeps scale 0), over the 128 channels = 4 per lane, then the warp
@@ -463,14 +484,14 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
 // share every B fragment the warp loads from the record.
 constexpr int MT = 2;  // m-tiles per chain warp
 
-template <bool WANT_Q, int NCH>
+template <bool WANT_Q, int NCH, bool REV, bool CKS>
 __device__ __forceinline__ void chain_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int chain = ((threadIdx.x >> 5) - W_CHAIN0) / N_CHAIN;  // 0 unless NCH = 2
     const int cw = ((threadIdx.x >> 5) - W_CHAIN0) % N_CHAIN;
     // with two chains per CTA, chain 0 starts from the identity (transfer matrix)
     // and chain 1 from zeros with the values (zero-initial state)
-    const bool partA = NCH == 2 ? chain == 0 : x.partA;
+    const bool partA = !REV && (NCH == 2 ? chain == 0 : x.partA);
     const bool want_v = !partA;
     const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
     const int j0 = 16 * MT * cw;
@@ -480,8 +501,9 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
     float S[MT][16][4];
     {
         const float *src = nullptr;
+        const int sidx = REV ? p.Sg - 1 - x.s : x.s;  // the adjoint's arrays run reversed
         if (!x.transfer)
-            src = p.seg_init ? p.seg_init + (unit * p.Sg + x.s) * (size_t)D * D
+            src = p.seg_init ? p.seg_init + (unit * p.Sg + sidx) * (size_t)D * D
                              : (p.S0 ? p.S0 + unit * (size_t)D * D : nullptr);
 #pragma unroll
         for (int m = 0; m < MT; ++m)
@@ -500,11 +522,118 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
     __nv_bfloat16 *out = (__nv_bfloat16 *)(partA ? p.aux_out : p.out);
     const uint32_t ost_s = x.sbase + OST_OFF + (chain * N_CHAIN + cw) * OST_SIZE;
     const uint8_t *ost = x.smem + OST_OFF + (chain * N_CHAIN + cw) * OST_SIZE;
+    // The state, transposed and in BF16, into chunk-state slot `slot` ([dv][dk]:
+    // the two channels a lane holds per row are adjacent, one 4-byte store each).
+    auto store_chunk_state = [&](int cslot) {
+        __nv_bfloat16 *d = p.chunk_states + ((size_t)cslot * p.H + x.h) * D * D;
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi)
+                    *(uint32_t *)(d + (size_t)(j0 + 16 * m + g8 + 8 * hi) * D + 8 * n + 2 * t4) =
+                        pack_bf16x2(S[m][n][2 * hi], S[m][n][2 * hi + 1]);
+    };
     for (int c = 0; c < x.nchunks; ++c) {
         const int slot = c % NR;
         if (!warp_wait(x, B_REC_FULL + slot, (c / NR) & 1)) break;
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
         const float *decay = (const float *)(x.smem + REC_OFF + slot * R_SIZE + R_DECAY);
+        if constexpr (REV) {
+            // ---- adjoint chain, block nchunks - 1 - c: the state is dS', the
+            // adjoint of the state after the block (written out first)
+            if (p.chunk_states)
+                store_chunk_state(x.cs_base + (x.t_begin - x.seq0) / C + x.nchunks - 1 - c);
+            // dU^T = dO^T Mq + dS'^T Kb^T (j x r): seeded with dO^T Mq
+            float E[MT][2][4] = {};
+            uint32_t doa[MT][4];  // dO^T as A fragments (rows j, k = r)
+            {
+                uint32_t mqt[4];
+                ldsm_x4_t(rec_s + R_MQ + ((lane & 7) + 8 * ((lane >> 3) & 1)) * (TL * 2) +
+                              16 * (lane >> 4),
+                          mqt);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    ldsm_x4_t(rec_s + R_V + (8 * (lane >> 4) + (lane & 7)) * VROWB +
+                                  (j0 + 16 * m + 8 * ((lane >> 3) & 1)) * 2,
+                              doa[m]);
+                    mma_bf16_16816(E[m][0], doa[m], mqt[0], mqt[1]);
+                    mma_bf16_16816(E[m][1], doa[m], mqt[2], mqt[3]);
+                }
+            }
+            {
+                uint32_t bk[2][4];
+                auto load_b = [&](int kk, uint32_t (&w)[4]) {
+                    ldsm_x4_t(rec_s + (16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1)) * RLB +
+                                  16 * (lane >> 4) + RC_K * 2,
+                              w);
+                };
+                load_b(0, bk[0]);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    if (kk + 1 < 8) load_b(kk + 1, bk[(kk + 1) & 1]);
+                    const uint32_t(&w)[4] = bk[kk & 1];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const uint32_t a[4] = {
+                            pack_bf16x2(S[m][2 * kk][0], S[m][2 * kk][1]),
+                            pack_bf16x2(S[m][2 * kk][2], S[m][2 * kk][3]),
+                            pack_bf16x2(S[m][2 * kk + 1][0], S[m][2 * kk + 1][1]),
+                            pack_bf16x2(S[m][2 * kk + 1][2], S[m][2 * kk + 1][3])};
+                        mma_bf16_16816(E[m][0], a, w[0], w[1]);
+                        mma_bf16_16816(E[m][1], a, w[2], w[3]);
+                    }
+                }
+            }
+            // dR^T = dU^T T (j x r), kept negated as A fragments
+            uint32_t ndra[MT][4];
+            {
+                uint32_t tt[4];
+                ldsm_x4_t(rec_s + R_T + ((lane & 7) + 8 * ((lane >> 3) & 1)) * (TL * 2) +
+                              16 * (lane >> 4),
+                          tt);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint32_t dua[4] = {pack_bf16x2(E[m][0][0], E[m][0][1]),
+                                             pack_bf16x2(E[m][0][2], E[m][0][3]),
+                                             pack_bf16x2(E[m][1][0], E[m][1][1]),
+                                             pack_bf16x2(E[m][1][2], E[m][1][3])};
+                    float R[2][4] = {};
+                    mma_bf16_16816(R[0], dua, tt[0], tt[1]);
+                    mma_bf16_16816(R[1], dua, tt[2], tt[3]);
+                    ndra[m][0] = pack_bf16x2(-R[0][0], -R[0][1]);
+                    ndra[m][1] = pack_bf16x2(-R[0][2], -R[0][3]);
+                    ndra[m][2] = pack_bf16x2(-R[1][0], -R[1][1]);
+                    ndra[m][3] = pack_bf16x2(-R[1][2], -R[1][3]);
+                }
+            }
+            // dS^T <- dS'^T Diag(e^{Gamma_C}) + dO^T Qh - dR^T Kh
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                uint32_t fq[4], fk[4];
+                const uint32_t row = rec_s + (16 * np + (lane & 7) + 8 * (lane >> 4)) * RLB +
+                                     16 * ((lane >> 3) & 1);
+                ldsm_x4(row + RC_Q * 2, fq);
+                ldsm_x4(row + RC_KH * 2, fk);
+                const float2 d0 = *(const float2 *)(decay + 16 * np + 2 * t4);
+                const float2 d1 = *(const float2 *)(decay + 16 * np + 8 + 2 * t4);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    mul2_inplace(S[m][2 * np][0], S[m][2 * np][1], d0);
+                    mul2_inplace(S[m][2 * np][2], S[m][2 * np][3], d0);
+                    mul2_inplace(S[m][2 * np + 1][0], S[m][2 * np + 1][1], d1);
+                    mul2_inplace(S[m][2 * np + 1][2], S[m][2 * np + 1][3], d1);
+                    mma_bf16_16816(S[m][2 * np], doa[m], fq[0], fq[1]);
+                    mma_bf16_16816(S[m][2 * np], ndra[m], fk[0], fk[1]);
+                    mma_bf16_16816(S[m][2 * np + 1], doa[m], fq[2], fq[3]);
+                    mma_bf16_16816(S[m][2 * np + 1], ndra[m], fk[2], fk[3]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x.bar(B_REC_EMPTY + slot));
+            continue;
+        }
 
         // E^T = S^T Kh^T - V^T (j x r) = -(V - Kh S)^T in fp32.  V^T is loaded as
         // an A fragment, whose element positions are those of the 16 x 16
@@ -635,6 +764,10 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(x.bar(B_REC_EMPTY + slot));
+        if (CKS) {  // the state after every full block, BF16 transposed
+            const int done = min(x.t_begin + C * (c + 1), x.t_end) - x.seq0;
+            if (done % C == 0) store_chunk_state(x.cs_base + done / C - 1);
+        }
         if (p.ckpt_interval > 0) {  // state checkpoint after this block
             const int done = min(x.t_begin + C * (c + 1), x.t_end) - x.seq0;
             float *d = partA ? p.ckpt_a : p.ckpt;
@@ -662,10 +795,12 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
 
     float *dst = nullptr;
     if (!x.transfer) {
-        if (x.s == p.Sg - 1 && p.S_final) dst = p.S_final + unit * (size_t)D * D;
+        // the adjoint chain ends at the segment's start: segment 0 gives dS0
+        if (x.s == (REV ? 0 : p.Sg - 1) && p.S_final) dst = p.S_final + unit * (size_t)D * D;
     } else {
         float *base = partA ? p.transfer : p.zero_state;
-        if (base) dst = base + (unit * p.Sg + x.s) * (size_t)D * D;
+        const int sidx = REV ? p.Sg - 1 - x.s : x.s;
+        if (base) dst = base + (unit * p.Sg + sidx) * (size_t)D * D;
     }
     // Final writes go through shared memory so that every global store is a fully
     // used 16-byte piece of a contiguous run.  Every record has been consumed, so
@@ -707,7 +842,41 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
                 *(uint4 *)(hi + (size_t)img * D * D + (size_t)(j0 + row) * D + 8 * c16) =
                     *(const uint4 *)(fw + img * 32 * FW_IROW + row * FW_IROW + 16 * c16);
             }
-    } else if (dst) {
+    }
+    if (partA && p.transfer_img_t) {
+        // A[i][j] row-major as hi/lo BF16 images (the images of A^T in the layout
+        // above) at the reversed segment index: stage fp32 [128 i][FW_JROW] as for
+        // the states below, then each row's 32 columns as 64-byte pieces
+        if (p.transfer_img) __syncwarp();  // the staging above has been read
+        float *f = (float *)fw;
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    f[(8 * n + 2 * t4 + (e & 1)) * FW_JROW + 16 * m + g8 + 8 * (e >> 1)] = S[m][n][e];
+        __syncwarp();
+        __nv_bfloat16 *hi = p.transfer_img_t + (unit * p.Sg + p.Sg - 1 - x.s) * (size_t)2 * D * D;
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {  // 128 rows x 4 pieces of 8 columns
+            const int idx = 32 * it + lane, i = idx >> 2, c = idx & 3;
+            const float4 v0 = *(const float4 *)(f + i * FW_JROW + 8 * c);
+            const float4 v1 = *(const float4 *)(f + i * FW_JROW + 8 * c + 4);
+            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint32_t wh[4], wl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                const float2 hf = __bfloat1622float2(h2);
+                wh[e] = *(const uint32_t *)&h2;
+                wl[e] = pack_bf16x2(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+            }
+            const size_t o = (size_t)i * D + j0 + 8 * c;
+            *(uint4 *)(hi + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *(uint4 *)(hi + (size_t)D * D + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
+    } else if (dst && !(partA && p.transfer_img)) {
         // S[i][j] (j contiguous) is the transpose of the accumulator layout: stage
         // this warp's columns as [128 i][FW_JROW floats] (conflict-free scalar
         // stores), then write 128-byte row segments.
@@ -742,21 +911,29 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
 // parameter: the identity-start and zero-start CTAs of the transfer pass then
 // run the same instructions, so the code that the first of them fetches into the
 // instruction caches serves the other, and the kernel's code footprint halves.
-template <bool WANT_Q, bool GATE, int NCH>
+// REV: the adjoint chain; CKS: the forward chain also writes chunk states (the
+// backward's forward pass).  Both are separate instantiations, so the prefill's
+// own kernels carry none of their code.
+template <bool WANT_Q, bool GATE, int NCH, bool REV = false, bool CKS = false>
 __device__ __forceinline__ void run_role(const Ctx &x, int warp) {
     if (warp < W_CHAIN0) {
         if (NCH == 2) regs_dealloc<PREP_REGS>();
-        prep_role<WANT_Q, GATE>(x);
+        prep_role<WANT_Q, GATE, REV>(x);
     } else {
         if (NCH == 2) regs_alloc<CHAIN_REGS>();
-        chain_role<WANT_Q, NCH>(x);
+        chain_role<WANT_Q, NCH, REV, CKS>(x);
     }
 }
 
 // GATE (the fused prologue) is a separate kernel: the plain kernel's code is then
 // only its own, which matters because the kernel starts with cold instruction
 // caches after the scan and the combine of the previous call.
-template <bool GATE, int NCH>
+// VAR: 0 the prefill, 1 the adjoint chain of the backward, 2 the backward's
+// forward chain with chunk states.  Separate kernels, so that each one's code is
+// only its own (the prefill starts with cold instruction caches after the scan
+// and the combine of the previous call).
+enum { VAR_PREFILL = 0, VAR_ADJOINT = 1, VAR_CHUNK_STATES = 2 };
+template <bool GATE, int NCH, int VAR = VAR_PREFILL>
 __global__ void __launch_bounds__(cta_threads(NCH), 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -779,17 +956,21 @@ __global__ void __launch_bounds__(cta_threads(NCH), 1)
     x.abort = (volatile int *)(smem + MISC_OFF);
     const int u = blockIdx.x;
     x.n = u / (p.H * p.seg_count);
+    if (p.N <= 32) x.n = longest_first(p, x.n);
     x.h = (u / p.seg_count) % p.H;
     x.s = p.seg_begin + u % p.seg_count;
     x.transfer = p.mode == MODE_TRANSFER;
-    x.partA = NCH == 1 && x.transfer && blockIdx.y == 0;
-    x.want_q = !x.transfer || p.emit_out;
+    x.partA = NCH == 1 && x.transfer && blockIdx.y == 0 && !p.rev;
+    // outputs (and q) only where they are written: the prefill's out, or the
+    // transfer pass's outputs; the adjoint chain always needs q
+    x.want_q = (!x.transfer && p.out) || p.emit_out || p.rev;
     x.want_v = !x.partA;  // the prep loads V whenever a chain of the CTA uses it
     if (!segment_range(p.cu, x.n, p.N, p.T_tot, x.s, p.Sg, p.dev_status, x.t_begin, x.t_end))
         return;
     x.nchunks = (x.t_end - x.t_begin + C - 1) / C;
     x.seq0 = p.cu[x.n];
     x.ckpt_base = p.ckpt_interval > 0 ? ckpt_base(p.cu, x.n, p.ckpt_interval) : 0;
+    x.cs_base = !p.chunk_states ? 0 : (p.rev ? block_base(p.cu, x.n) : ckpt_base(p.cu, x.n, C));
 
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
@@ -803,7 +984,9 @@ __global__ void __launch_bounds__(cta_threads(NCH), 1)
     }
     __syncthreads();
 
-    if (GATE) run_role<true, true, NCH>(x, warp);  // (the fused prologue always has q)
+    if (VAR == VAR_ADJOINT) run_role<true, false, 1, true>(x, warp);
+    else if (VAR == VAR_CHUNK_STATES) run_role<false, false, 1, false, true>(x, warp);
+    else if (GATE) run_role<true, true, NCH>(x, warp);  // (the fused prologue always has q)
     else if (x.want_q) run_role<true, false, NCH>(x, warp);
     else run_role<false, false, NCH>(x, warp);
 
@@ -857,8 +1040,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     int sms = 148, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool two = a.mode == MODE_TRANSFER && units >= sms;
-    const dim3 grid(units, a.mode == MODE_TRANSFER && !two ? 2 : 1);
+    const bool two = a.mode == MODE_TRANSFER && units >= sms && !a.rev;
+    const dim3 grid(units, a.mode == MODE_TRANSFER && !two && !a.rev ? 2 : 1);
     auto go = [&](auto kernel, int threads) -> cudaError_t {
         cudaError_t e = set_max_dynamic_smem((const void *)kernel, SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -867,6 +1050,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     if (a.gate)
         return two ? go(prefill_tc_kernel<true, 2>, cta_threads(2))
                    : go(prefill_tc_kernel<true, 1>, cta_threads(1));
+    if (a.rev) return go(prefill_tc_kernel<false, 1, VAR_ADJOINT>, cta_threads(1));
+    if (a.chunk_states) return go(prefill_tc_kernel<false, 1, VAR_CHUNK_STATES>, cta_threads(1));
     return two ? go(prefill_tc_kernel<false, 2>, cta_threads(2))
                : go(prefill_tc_kernel<false, 1>, cta_threads(1));
 }

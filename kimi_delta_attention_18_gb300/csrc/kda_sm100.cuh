@@ -95,6 +95,38 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, uint64_t tmap, int x, 
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (zero fill when !pred: no bytes are
+// read, src must still be a valid address); complete with cp_async_wait_all().
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(pred ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// 2D tiled tensor copy shared -> global (box size and swizzle fixed by the tensor
+// map), as one bulk-async group: cp_bulk_commit() closes the group,
+// cp_bulk_wait_read<N>() waits until at most N groups still read shared memory.
+__device__ __forceinline__ void tma_store_2d(uint64_t tmap, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     tmap),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -240,17 +240,32 @@ def test_backward_host_checks():
     assert L.kda_prefill_backward_num_segments(ctypes.byref(d4)) == 4
     assert L.kda_prefill_backward_num_segments(ctypes.byref(_desc(num_segments=500))) == 64
     assert L.kda_prefill_backward_num_segments(ctypes.byref(_desc(chunk=32))) == 0
-    # the library's split for B=1 H=8 T=4096 d=128: 32 (head, 32-column) units and two
-    # gradient-pass CTAs per SM on 148-152 SMs -> 9 segments (at most T / 256 = 16)
-    bench = _desc(num_seqs=1, total_tokens=4096, num_heads=8, dk=128, dv=128, act_dtype=1,
+    # BF16 at dk = dv = 128 takes the chunked backward, which splits sequences until
+    # every SM has a one-chain CTA (at least 4 blocks per segment, at most 64) and keeps
+    # BF16 states per 16-token block:
+    # [T/16][H] forward states and [ceil(T/16) + N][H] adjoints of 128 x 128 BF16, plus
+    # with S > 1 the BF16 images of A and A^T and the fp32 B, B^, X, Y per (sequence,
+    # head, segment)
+    for T, H, N in ((4096, 8, 1), (512, 8, 1), (64 * 512, 8, 64)):
+        c = _desc(num_seqs=N, total_tokens=T, num_heads=H, dk=128, dv=128, act_dtype=1,
                   num_segments=0)
-    assert L.kda_prefill_backward_num_segments(ctypes.byref(bench)) == 9
-    short = _desc(num_seqs=1, total_tokens=512, num_heads=8, dk=128, dv=128, act_dtype=1,
-                  num_segments=0)
-    assert L.kda_prefill_backward_num_segments(ctypes.byref(short)) == 2  # 512 / 256
-    many = _desc(num_seqs=64, total_tokens=64 * 512, num_heads=8, dk=128, dv=128,
-                 act_dtype=1, num_segments=0)
-    assert L.kda_prefill_backward_num_segments(ctypes.byref(many)) == 1  # units fill the SMs
+        S = L.kda_prefill_backward_num_segments(ctypes.byref(c))
+        import torch  # the library counts the device's SMs, or assumes 148 without one
+        sms = (torch.cuda.get_device_properties(0).multi_processor_count
+               if torch.cuda.is_available() else 148)
+        chains = N * H
+        want_s = 1 if chains >= sms else max(1, min(-(-sms // chains), T // N // 16 // 4, 64))
+        assert S == want_s, (T, H, N, S)
+        img = 128 * 128 * 2
+        want = r256(T // 16 * H * img) + r256(((T + 15) // 16 + N) * H * img)
+        if S > 1:
+            want += 6 * r256(N * H * S * 128 * 128 * 4)
+        assert L.kda_prefill_backward_workspace_size(ctypes.byref(c)) == want
+    # the chunked path moves rows as 16-byte pieces: unaligned rows are refused
+    c = _desc(num_seqs=1, total_tokens=64, num_heads=2, dk=128, dv=128, act_dtype=1,
+              num_segments=1)
+    cneed = L.kda_prefill_backward_workspace_size(ctypes.byref(c))
+    assert call(c, ws=0x40000, ws_len=cneed, g=ctypes.c_void_p(0x10004)) == INVALID
     assert call(d) == WORKSPACE
     assert call(d, ws=0x40000, ws_len=need - 1) == WORKSPACE
     assert call(d, ws=0x40008, ws_len=need) == WORKSPACE       # not 16-byte aligned

@@ -15,10 +15,16 @@ from tests.conftest import rel_err
 
 pytestmark = pytest.mark.gpu
 
-# fp32 arithmetic on both activation dtypes: the oracle sees the same (BF16-exact)
-# inputs, so the fp32 bound applies to both.
+# The token-level path (fp32 activations, and BF16 at other widths) computes in
+# fp32: the oracle sees the same (BF16-exact) inputs, so the fp32 bound applies.
+# BF16 at dk = dv = 128 takes the chunked tensor-core path (BF16 operands, fp32
+# accumulation and state), held to the BF16 bound of the forward.
 TOL = 1e-4
 NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dS0")
+
+
+def _tol(act, dk, dv):
+    return 2e-2 if act == "bf16" and dk == 128 and dv == 128 else TOL
 
 
 def _np(t):
@@ -66,7 +72,7 @@ def test_backward_matches_oracle(act, dk, dv, lengths, slow):
     got = _run(x, d_out, d_sf)
     ref = _oracle(x, d_out, d_sf)
     for name, a, b in zip(NAMES, got, ref):
-        assert rel_err(_np(a), b) <= TOL, (name, rel_err(_np(a), b))
+        assert rel_err(_np(a), b) <= _tol(act, dk, dv), (name, rel_err(_np(a), b))
 
 
 @pytest.mark.parametrize("act,d,lengths,nseg", [
@@ -75,6 +81,8 @@ def test_backward_matches_oracle(act, dk, dv, lengths, slow):
     ("f32", 48, [200, 31], 3),
     ("bf16", 128, [250, 90], 4),
     ("bf16", 128, [250, 90], 0),    # the library's choice
+    ("bf16", 128, [700, 0, 333, 45], 16),  # chunked: empty sequence, more segments
+    ("bf16", 128, [40, 5, 0], 8),   # chunked: segments without a block
     ("bf16", 60, [100, 45], 3),     # plain-load producer
     ("f32", 16, [40, 5, 0], 8),     # more segments than 16-token chunks: empty segments
     ("f32", 32, [1500, 260], 64),   # the largest split
@@ -89,17 +97,18 @@ def test_backward_segments_match_oracle(act, d, lengths, nseg):
     got = _run(x, d_out, d_sf, num_segments=nseg)
     ref = _oracle(x, d_out, d_sf)
     for name, a, b in zip(NAMES, got, ref):
-        assert rel_err(_np(a), b) <= TOL, (name, rel_err(_np(a), b))
+        assert rel_err(_np(a), b) <= _tol(act, d, d), (name, rel_err(_np(a), b))
 
 
-def test_backward_without_initial_or_final_state():
+@pytest.mark.parametrize("act,d", [("f32", 32), ("bf16", 128)])
+def test_backward_without_initial_or_final_state(act, d):
     lengths = [29, 0, 50]
-    x = make_prefill_inputs(lengths, 2, 32, 32, "f32", seed=33)
-    d_out, _ = make_backward_adjoints(sum(lengths), 3, 2, 32, 32, "f32", seed=34, final=False)
+    x = make_prefill_inputs(lengths, 2, d, d, act, seed=33)
+    d_out, _ = make_backward_adjoints(sum(lengths), 3, 2, d, d, act, seed=34, final=False)
     got = _run(x, d_out, None)
     ref = _oracle(x, d_out, None)  # zero S0: its gradient is still defined
     for name, a, b in zip(NAMES, got, ref):
-        assert rel_err(_np(a), b) <= TOL, name
+        assert rel_err(_np(a), b) <= _tol(act, d, d), name
     # an empty sequence's dS0 is its (zero) final-state adjoint
     assert torch.count_nonzero(got[5][1]) == 0
 
@@ -126,9 +135,9 @@ def test_backward_bench_size_sampled_heads_and_linearity():
         ref = _oracle(x, d1, s1, heads=[h])
         for name, a, b in zip(NAMES, got, ref):
             a = _np(a)[:, [h]]
-            assert rel_err(a, b) <= TOL, (h, name)
+            assert rel_err(a, b) <= _tol("bf16", d, d), (h, name, rel_err(a, b))
     # linearity: backward(2 d_out, 2 d_S_final) = 2 backward(d_out, d_S_final),
-    # exact in binary floating point up to the atomics' summation order
+    # exact in binary floating point (scaling by 2 commutes with every rounding)
     g2 = _run(x, (d1.float() * 2).to(d1.dtype), s1 * 2)
     for name, a, b in zip(NAMES, got, g2):
         assert rel_err(_np(b), 2 * _np(a)) <= 1e-5, name
