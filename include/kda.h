@@ -327,21 +327,36 @@ kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_desc_t *desc, const v
  *     dq, dk, dg  [T_tot, H, dk] fp32,   dv [T_tot, H, dv] fp32,
  *     dbeta [T_tot, H] fp32,             dS0 [N, H, dk, dv] fp32 (NULL: skipped).
  * dg is the gradient with respect to the log-decay g (alpha = e^g).  All outputs
- * are overwritten (dq, dk, dg, dbeta are zeroed on the stream, then accumulated);
- * none may alias an input.  Computed in fp32 at token granularity: one CTA per
- * (sequence, head, 32 value columns) recomputes the states from a checkpoint at
- * every 4-token block start kept in the workspace.  desc->num_segments (0: the
- * library's choice, at most 64) splits every sequence into segments run in
- * parallel: each segment's transfer matrix A, zero-start state and zero-end
- * adjoint first, then fp32 scans for every segment's start state and end
- * adjoint (the adjoint map of a segment is A^T), then the gradient pass per
- * segment.  Workspace: kda_prefill_backward_workspace_size(desc) (0 on invalid
- * arguments), 16-byte aligned: about dk * dv fp32 per head and 4 tokens (16 KB
- * per head-token at d = 128), so a batch too long for device memory is
- * differentiated piece by piece, last piece first: each piece from its start
- * state (S0) with d_S_final = the next piece's dS0.  Pointers 4-byte aligned;
- * KDA_ERR_INVALID_ARG on a missing or misaligned pointer, KDA_ERR_WORKSPACE on a
- * short workspace, KDA_ERR_UNSUPPORTED as kda_prefill_chunked.
+ * are overwritten; none may alias an input.
+ *
+ * BF16 activations at dk = dv = 128 take the chunked form on tensor cores (the
+ * 16-token blocks of the prefill): the forward chain stores the state after
+ * every full block (BF16), an adjoint chain runs every segment from its last
+ * block to its first and stores the adjoint at every block end (BF16), and one
+ * CTA per (block, head) then forms that block's gradients from its start state
+ * and end adjoint, all blocks in parallel, with no atomics.  q, k, v, g and d_out
+ * must then be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).  Its results
+ * follow BF16 rounding of the chain's operands and of the stored states (the BF16
+ * tolerance of the prefill applies).  Workspace: 32 KB per head and 16 tokens
+ * for the states plus the same, plus one block per sequence, for the adjoints
+ * (4 KB per head-token), plus 384 KB per (sequence, head, segment) when
+ * segments are used.  Other dtypes and shapes take the token-level form in fp32:
+ * one CTA per (sequence, head, 32 value columns) recomputes the states from a
+ * checkpoint at every 4-token block start (16 KB of workspace per head-token at
+ * d = 128); dq, dk, dg and dbeta are zeroed on the stream, then accumulated.
+ *
+ * desc->num_segments (0: the library's choice, at most 64) splits every sequence
+ * into segments run in parallel: each segment's transfer matrix A, zero-start
+ * state and zero-end adjoint first, then scans for every segment's start state
+ * and end adjoint (the adjoint map of a segment is A^T), then the chains per
+ * segment.  The library's choice gives every SM one chain (chunked form: at least
+ * 4 blocks per segment) or two (token-level form).  Workspace:
+ * kda_prefill_backward_workspace_size(desc) (0 on invalid arguments).  A batch
+ * too long for device memory is differentiated piece by piece, last piece first:
+ * each piece from its start state (S0) with d_S_final = the next piece's dS0.
+ * Pointers at least 4-byte aligned; KDA_ERR_INVALID_ARG on a missing or
+ * misaligned pointer, KDA_ERR_WORKSPACE on a short workspace,
+ * KDA_ERR_UNSUPPORTED as kda_prefill_chunked.
  */
 size_t kda_prefill_backward_workspace_size(const kda_prefill_desc_t *desc);
 /* Segments per sequence the backward pass uses for desc (0 on invalid arguments). */

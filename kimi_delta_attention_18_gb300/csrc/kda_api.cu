@@ -211,6 +211,23 @@ namespace {
 
 // The one-call prefill, optionally with sparse state checkpoints (interval 0:
 // none).
+// Lead segment of the one-call split (see PrefillArgs::lead): with fewer chains
+// (sequence, head) than SMs, every chain's first segment, whose start state S0 is
+// known, runs as an output pass on an SM of its own while the remaining SMs run
+// the transfer pass of the other segments, each of which costs both chains and
+// a share of the combine.  The lead fraction f balances the two: f c1 = (1 - f)
+// u c2 / (P - u) for u chains on P SMs, c1 the time of a 16-token block of one
+// chain and c2 that of a block of the transfer pass's two chains together
+// (measured on GB300, H = 38 heads x 256K tokens: c2 / c1 = 1.59 / 1.00 us).
+// Only the tensor-core two-chain transfer pass supports it; 0 elsewhere.
+int lead_fraction(const PrefillArgs &t) {
+    if (t.Sg < 2 || !prefill_tc_supported(t) || !prefill_tc_two_chain(t)) return 0;
+    const double u = (double)t.N * t.H, P = (double)sm_count(), r = 1.6;
+    if (u >= P) return 0;
+    const double f = u * r / ((P - u) + u * r);
+    return (int)(f * 65536.0);
+}
+
 kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, const void *k,
                               const void *v, const float *g, const float *beta, const float *S0,
                               const int32_t *cu_seqlens, void *out, float *S_final,
@@ -292,12 +309,16 @@ kda_status_t prefill_one_call(const kda_prefill_desc_t *desc, const void *q, con
     t.emit_out = 1;
     t.aux_out = aux;
     t.S_final = nullptr;
+    t.lead = lead_fraction(t);
+    if (t.lead) t.S0 = S0;  // the lead segment's zero-start chain starts from S0
     if (ckpt_interval > 0)  // partial transfer matrices at the checkpoints
         t.ckpt_a = (float *)((uint8_t *)workspace + workspace_bytes_for(desc, Sg));
     cudaError_t e = run_prefill_pass(t, st);
     if (e != cudaSuccess || mark(1) != cudaSuccess) return KDA_ERR_CUDA;
     PrefillArgs c = a;
-    c.seg_begin = S0 ? 0 : 1;  // from zeros the first segment needs no correction
+    // from zeros (or run from S0 as the lead) the first segment needs no correction
+    c.seg_begin = S0 && !t.lead ? 0 : 1;
+    c.lead = t.lead;
     c.ckpt_interval = 0;
     // the tcgen05 combine reads the start states' BF16 images only: the scan then
     // skips the fp32 copies (unless checkpoints need them)

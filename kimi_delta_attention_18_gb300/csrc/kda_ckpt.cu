@@ -45,11 +45,16 @@ __global__ void __launch_bounds__(FX_T) ckpt_fixup_kernel(const PrefillArgs p, c
     if (n < 0) return;  // fewer checkpoints than the bound
     const int len = p.cu[n + 1] - p.cu[n];
     const int done = (kg - base + 1) * iv;  // tokens of the sequence before the checkpoint
-    // its segment: the one whose blocks [floor(s c / Sg), floor((s + 1) c / Sg)) hold
-    // block done / 16 - 1 (the same split as every kernel of the split path)
+    // its segment: the one whose blocks hold block done / 16 - 1 (the same split
+    // as every kernel of the split path)
     const long long c = (len + 15) / 16, blk = done / 16 - 1;
     int s = 0;
-    while (s < p.Sg - 1 && blk >= (long long)(s + 1) * c / p.Sg) ++s;
+    for (; s < p.Sg - 1; ++s) {
+        long long c0, c1;
+        segment_blocks(c, s, p.Sg, p.lead, c0, c1);
+        if (blk < c1) break;
+    }
+    if (p.lead > 0 && s == 0) return;  // the lead segment ran from S0: already the state
     const size_t unit = (size_t)n * H + h;
     const float *start = s == 0 ? (S0 ? S0 + unit * dk * dv : nullptr)
                                 : starts + (unit * p.Sg + s) * (size_t)dk * dv;

@@ -35,7 +35,7 @@ __device__ __forceinline__ bool tile_range(const PrefillArgs &p, int u, int tile
     s = u % p.Sg;
     if (s < p.seg_begin) return false;  // segments before seg_begin start from zeros
     int a, b;
-    if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b)) return false;
+    if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b, p.lead)) return false;
     t0 = a + tile * TILE;
     t1 = min(b, t0 + TILE);
     return t0 < t1;
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(BF_WARPS * 32) combine_bf16_kernel(
     const int n = u / (p.H * p.Sg), h = (u / p.Sg) % p.H, s = u % p.Sg;
     if (s < p.seg_begin) return;  // segments before seg_begin start from zeros
     int a, b;
-    if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b)) return;
+    if (!segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b, p.lead)) return;
     const int t0 = a + (group_base + blockIdx.y) * gtiles * TILE;
     const int t1 = min(b, t0 + gtiles * TILE);
     if (t0 >= t1) return;
@@ -192,7 +192,7 @@ __device__ __forceinline__ TileRef tile_ref(const PrefillArgs &p, long long f, i
     r.h = unit % p.H;
     r.us = unit * p.Sg + s;
     int a, b;
-    r.ok = segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b);
+    r.ok = segment_range(p.cu, n, p.N, p.T_tot, s, p.Sg, p.dev_status, a, b, p.lead);
     r.t0 = a + tile * TC_TILE;
     r.nt = min(TC_TILE, b - r.t0);
     r.ok = r.ok && r.t0 < b;
@@ -444,9 +444,16 @@ cudaError_t launch_combine(const PrefillArgs &a, const float *starts, const void
                            const __nv_bfloat16 *start_img, cudaStream_t st) {
     const long long units = (long long)a.N * a.H * a.Sg;
     if (units == 0 || a.T_tot == 0) return cudaSuccess;
-    // tokens of one segment: at most ceil(ceil(T_tot / 16) / Sg) blocks of 16
+    // tokens of one segment: at most ceil(ceil(T_tot / 16) / Sg) blocks of 16; with a
+    // lead segment (skipped here) the others split what the lead leaves of the
+    // longest possible sequence
     const long long blocks = ((long long)a.T_tot + 15) / 16;
-    const long long seg_tokens = 16 * ((blocks + a.Sg - 1) / a.Sg);
+    long long seg_blocks = (blocks + a.Sg - 1) / a.Sg;
+    if (a.lead > 0 && a.Sg >= 2 && a.seg_begin >= 1) {
+        const long long rest = blocks - (blocks * a.lead >> 16);
+        seg_blocks = (rest + a.Sg - 2) / (a.Sg - 1);
+    }
+    const long long seg_tokens = 16 * seg_blocks;
     const long long tiles = (seg_tokens + TILE - 1) / TILE;
     PFN_cuTensorMapEncodeTiled_v12000 enc = sm100::tensor_map_encoder();
     if (combine_uses_images(a, aux_out, start_img)) {

@@ -26,21 +26,37 @@ __device__ __forceinline__ void dev_fail(int32_t *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
-// Token range [t_begin, t_end) of segment s (of Sg) of sequence n.  The
-// sequence's chunks are split evenly: segment s takes chunks
-// [floor(s c / Sg), floor((s+1) c / Sg)) with c = ceil(len / 16).
-// Returns false (and records KDA_ERR_INVALID_ARG) if cu_seqlens is malformed.
+// Blocks [c0, c1) of segment s (of Sg) of a sequence of c 16-token blocks.
+// lead = 0: the blocks are split evenly, segment s takes [floor(s c / Sg),
+// floor((s+1) c / Sg)).  lead > 0 (a fraction of 2^16; used with Sg >= 2):
+// segment 0 takes the first floor(c lead / 2^16) blocks and segments 1 .. Sg-1
+// split the rest evenly.
+__host__ __device__ __forceinline__ void segment_blocks(long long c, int s, int Sg, int lead,
+                                                        long long &c0, long long &c1) {
+    if (lead <= 0 || Sg < 2) {
+        c0 = (long long)s * c / Sg;
+        c1 = (long long)(s + 1) * c / Sg;
+        return;
+    }
+    const long long cl = c * lead >> 16, rest = c - cl;
+    c0 = s == 0 ? 0 : cl + (long long)(s - 1) * rest / (Sg - 1);
+    c1 = cl + (long long)s * rest / (Sg - 1);
+}
+
+// Token range [t_begin, t_end) of segment s (of Sg) of sequence n, from the
+// block split above (c = ceil(len / 16) blocks).  Returns false (and records
+// KDA_ERR_INVALID_ARG) if cu_seqlens is malformed.
 __device__ __forceinline__ bool segment_range(const int32_t *cu, int n, int N, int T_tot,
                                               int s, int Sg, int32_t *status, int &t_begin,
-                                              int &t_end) {
+                                              int &t_end, int lead = 0) {
     const int a = cu[n], b = cu[n + 1];
     if (a < 0 || b < a || b > T_tot || cu[0] != 0 || cu[N] != T_tot) {
         dev_fail(status, KDA_ERR_INVALID_ARG);
         return false;
     }
     const long long len = b - a;
-    const long long c = (len + 15) / 16;
-    const long long c0 = (long long)s * c / Sg, c1 = (long long)(s + 1) * c / Sg;
+    long long c0, c1;
+    segment_blocks((len + 15) / 16, s, Sg, lead, c0, c1);
     t_begin = a + (int)min(len, c0 * 16);
     t_end = a + (int)min(len, c1 * 16);
     return true;
@@ -109,6 +125,14 @@ struct PrefillArgs {
     int rev;
     __nv_bfloat16 *chunk_states;
     __nv_bfloat16 *transfer_img_t;
+    // Lead segment (one-call split prefill, tensor-core path only): segment 0 takes
+    // the first lead / 2^16 of every sequence's blocks (segment_blocks) and runs
+    // from S0 as an output pass inside the transfer pass: its zero-start chain
+    // starts from S0 and writes the final outputs, its end state goes to
+    // zero_state and zero images to transfer_img, so the scan carries the end
+    // state on unchanged and the combine skips the segment.  The lead CTAs come
+    // first in the grid.  0: segments of equal length.
+    int lead;
     int N, T_tot, H, dk, dv;
     int Sg;                 // segments per sequence (layout and bounds)
     int seg_begin;          // segments seg_begin .. seg_begin+seg_count-1 are
@@ -161,6 +185,8 @@ __device__ __forceinline__ int ckpt_base(const int32_t *cu, int n, int interval)
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t st);
 bool prefill_tc_supported(const PrefillArgs &a);
+// Whether the tensor-core transfer pass runs both chains of a segment in one CTA.
+bool prefill_tc_two_chain(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st);
 // A (fp32) or, for BF16 at dk = dv = 128, a_img (the transfer pass's hi/lo
 // images) gives the transfer matrices; exactly one of them is non-null.

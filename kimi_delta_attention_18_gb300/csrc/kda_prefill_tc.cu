@@ -154,6 +154,7 @@ struct Ctx {
     int cs_base;          // first chunk-state slot of the sequence (chunk_states)
     int t_begin, t_end, nchunks;
     bool transfer, partA, want_q, want_v;
+    bool lead;  // a lead CTA: segment 0 run from S0 by the zero-start chain only
     __device__ uint32_t bar(int i) const { return sbase + BAR_OFF + 8 * i; }
 };
 
@@ -493,6 +494,10 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
     // and chain 1 from zeros with the values (zero-initial state)
     const bool partA = !REV && (NCH == 2 ? chain == 0 : x.partA);
     const bool want_v = !partA;
+    // In a lead CTA the identity-start chain has nothing to do: its transfer
+    // matrix is written as zeros (the scan then passes the lead segment's end
+    // state on as the next start state), and the zero-start chain starts from S0.
+    const bool idle = NCH == 2 && x.lead && partA;
     const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
     const int j0 = 16 * MT * cw;
     const size_t unit = (size_t)x.n * p.H + x.h;
@@ -505,6 +510,8 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         if (!x.transfer)
             src = p.seg_init ? p.seg_init + (unit * p.Sg + sidx) * (size_t)D * D
                              : (p.S0 ? p.S0 + unit * (size_t)D * D : nullptr);
+        else if (NCH == 2 && x.lead && !partA && p.S0)
+            src = p.S0 + unit * (size_t)D * D;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -512,7 +519,7 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 8 * n + 2 * t4 + (e & 1), j = j0 + 16 * m + g8 + 8 * (e >> 1);
-                    S[m][n][e] = partA ? (i == j ? 1.f : 0.f)
+                    S[m][n][e] = partA ? (i == j && !idle ? 1.f : 0.f)
                                          : (src ? src[(size_t)i * D + j] : 0.f);
                 }
     }
@@ -535,7 +542,8 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
                     *(uint32_t *)(d + (size_t)(j0 + 16 * m + g8 + 8 * hi) * D + 8 * n + 2 * t4) =
                         pack_bf16x2(S[m][n][2 * hi], S[m][n][2 * hi + 1]);
     };
-    for (int c = 0; c < x.nchunks; ++c) {
+    const int nck = idle ? 0 : x.nchunks;
+    for (int c = 0; c < nck; ++c) {
         const int slot = c % NR;
         if (!warp_wait(x, B_REC_FULL + slot, (c / NR) & 1)) break;
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
@@ -955,17 +963,35 @@ __global__ void __launch_bounds__(cta_threads(NCH), 1)
     x.sbase = smem_addr(smem);
     x.abort = (volatile int *)(smem + MISC_OFF);
     const int u = blockIdx.x;
-    x.n = u / (p.H * p.seg_count);
-    if (p.N <= 32) x.n = longest_first(p, x.n);
-    x.h = (u / p.seg_count) % p.H;
-    x.s = p.seg_begin + u % p.seg_count;
     x.transfer = p.mode == MODE_TRANSFER;
+    if (NCH == 2 && p.lead && x.transfer) {
+        // the lead units (segment 0 of every chain, the longest) first, then
+        // segments 1 .. Sg-1 of every chain
+        const int nh = p.N * p.H, sc = p.Sg - 1;
+        if (u < nh) {
+            x.n = u / p.H;
+            x.h = u % p.H;
+            x.s = 0;
+        } else {
+            const int v = u - nh;
+            x.n = v / (p.H * sc);
+            x.h = (v / sc) % p.H;
+            x.s = 1 + v % sc;
+        }
+    } else {
+        x.n = u / (p.H * p.seg_count);
+        x.h = (u / p.seg_count) % p.H;
+        x.s = p.seg_begin + u % p.seg_count;
+    }
+    if (p.N <= 32) x.n = longest_first(p, x.n);
+    x.lead = NCH == 2 && p.lead && x.transfer && x.s == 0;
     x.partA = NCH == 1 && x.transfer && blockIdx.y == 0 && !p.rev;
     // outputs (and q) only where they are written: the prefill's out, or the
     // transfer pass's outputs; the adjoint chain always needs q
     x.want_q = (!x.transfer && p.out) || p.emit_out || p.rev;
     x.want_v = !x.partA;  // the prep loads V whenever a chain of the CTA uses it
-    if (!segment_range(p.cu, x.n, p.N, p.T_tot, x.s, p.Sg, p.dev_status, x.t_begin, x.t_end))
+    if (!segment_range(p.cu, x.n, p.N, p.T_tot, x.s, p.Sg, p.dev_status, x.t_begin, x.t_end,
+                       NCH == 2 ? p.lead : 0))
         return;
     x.nchunks = (x.t_end - x.t_begin + C - 1) / C;
     x.seq0 = p.cu[x.n];
@@ -977,7 +1003,7 @@ __global__ void __launch_bounds__(cta_threads(NCH), 1)
         for (int i = 0; i < NS; ++i) mbar_init(x.bar(B_IN_FULL + i), 1);
         for (int i = 0; i < NR; ++i) {
             mbar_init(x.bar(B_REC_FULL + i), 1);
-            mbar_init(x.bar(B_REC_EMPTY + i), N_CHAIN * NCH);
+            mbar_init(x.bar(B_REC_EMPTY + i), N_CHAIN * (x.lead ? 1 : NCH));
         }
         *x.abort = 0;
         mbar_fence_init();
@@ -995,6 +1021,16 @@ __global__ void __launch_bounds__(cta_threads(NCH), 1)
 }
 
 }  // namespace
+
+// The transfer pass runs both chains of a segment in one CTA once there are at
+// least as many segments as SMs (the throughput regime: inputs read and prepared
+// once); with fewer, each chain gets its own CTA and SM.
+bool prefill_tc_two_chain(const PrefillArgs &a) {
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return a.mode == MODE_TRANSFER && (long long)a.N * a.H * a.seg_count >= sms && !a.rev;
+}
 
 bool prefill_tc_supported(const PrefillArgs &a) {
     if (a.gate && !(a.q && (a.mode == MODE_OUTPUT || a.emit_out))) return false;
@@ -1034,13 +1070,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
             !encode_rows(enc, &tg, a.g, a.T_tot, a.H, !a.gate))
             return cudaErrorInvalidValue;
     }
-    // The transfer pass runs both chains of a segment in one CTA once there are
-    // at least as many segments as SMs (the throughput regime: inputs read and
-    // prepared once); with fewer, each chain gets its own CTA and SM.
-    int sms = 148, dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool two = a.mode == MODE_TRANSFER && units >= sms && !a.rev;
+    const bool two = prefill_tc_two_chain(a);
+    if (a.lead && !(two && a.seg_begin == 0 && a.seg_count == a.Sg && a.Sg >= 2))
+        return cudaErrorInvalidValue;  // lead segments exist only in the full two-chain pass
     const dim3 grid(units, a.mode == MODE_TRANSFER && !two && !a.rev ? 2 : 1);
     auto go = [&](auto kernel, int threads) -> cudaError_t {
         cudaError_t e = set_max_dynamic_smem((const void *)kernel, SMEM_BYTES);

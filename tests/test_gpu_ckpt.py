@@ -23,6 +23,9 @@ def _np(t):
 
 @pytest.mark.parametrize("act,d,interval,nseg", [
     ("bf16", 128, 256, 1), ("bf16", 128, 256, 4), ("bf16", 128, 112, 8), ("bf16", 128, 64, 0),
+    # 8 chains x 20 segments fill the SMs: two-chain transfer pass with a lead segment
+    # (the first blocks of the 700-token sequence, run from S0, hold a checkpoint)
+    ("bf16", 128, 32, 20),
     ("f32", 32, 64, 1), ("f32", 32, 48, 3),
 ])
 def test_checkpoints_match_oracle_prefix_states(act, d, interval, nseg):

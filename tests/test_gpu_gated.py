@@ -18,7 +18,7 @@ def _np(t):
     return t.detach().float().cpu().double().numpy()
 
 
-@pytest.mark.parametrize("nseg,slow", [(1, False), (1, True), (4, True), (8, False)])
+@pytest.mark.parametrize("nseg,slow", [(1, False), (1, True), (4, True), (8, False), (20, True)])
 def test_gated_prefill_matches_oracle(nseg, slow):
     lengths = [700, 333, 45, 256]
     H = 2
