@@ -216,13 +216,13 @@ namespace {
 // known, runs as an output pass on an SM of its own while the remaining SMs run
 // the transfer pass of the other segments, each of which costs both chains and
 // a share of the combine.  The lead fraction f balances the two: f c1 = (1 - f)
-// u c2 / (P - u) for u chains on P SMs, c1 the time of a 16-token block of one
+// u c2 / (P - u) for u chains on P SMs, c1 the time of a 16-token block of a lead
 // chain and c2 that of a block of the transfer pass's two chains together
-// (measured on GB300, H = 38 heads x 256K tokens: c2 / c1 = 1.59 / 1.00 us).
+// (measured on GB300, 56 heads x 256K tokens: c1 = 1.12 us, c2 = 1.57 us).
 // Only the tensor-core two-chain transfer pass supports it; 0 elsewhere.
 int lead_fraction(const PrefillArgs &t) {
     if (t.Sg < 2 || !prefill_tc_supported(t) || !prefill_tc_two_chain(t)) return 0;
-    const double u = (double)t.N * t.H, P = (double)sm_count(), r = 1.6;
+    const double u = (double)t.N * t.H, P = (double)sm_count(), r = 1.41;
     if (u >= P) return 0;
     const double f = u * r / ((P - u) + u * r);
     return (int)(f * 65536.0);

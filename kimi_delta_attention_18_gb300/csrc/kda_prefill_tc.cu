@@ -81,8 +81,11 @@ constexpr int W_PREP0 = 0, W_CHAIN0 = W_PREP0 + N_PREP, N_CHAIN = 4;
 // threads of a CTA with nch chains (four chain warps each)
 __host__ __device__ constexpr int cta_threads(int nch) { return (W_CHAIN0 + N_CHAIN * nch) * 32; }
 // Register split of the two-chain CTA: 384 threads launch with 168 registers each;
-// the prep warpgroup gives back what the two chain warpgroups take.
-constexpr int PREP_REGS = 136, CHAIN_REGS = 184;
+// the prep warpgroup gives back what the two chain warpgroups take.  Measured on
+// GB300 (16-token block of the two-chain transfer pass / of a lead chain):
+// 136 / 184: 1.65 / 1.20 us; 120 / 192: 1.57 / 1.12 us (a few spilled prep
+// registers); 104 / 200: 1.60 / 1.08 us.
+constexpr int PREP_REGS = 120, CHAIN_REGS = 192;
 static_assert(128 * PREP_REGS + 256 * CHAIN_REGS <= 384 * 168, "register split");
 constexpr long long kWaitLimit = 4000000000ll;  // ~2 s of SM clocks
 
@@ -251,20 +254,11 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
                 mul2_inplace(o[2 * e], o[2 * e + 1], make_float2(y[2 * e], y[2 * e + 1]));
             }
         };
+        // the products with e^{Gamma} first (Kh, Qh), so that fwd is dead before the
+        // reverse factors are used: fewer arrays live at once
         float tmp[C];
         vmul(tmp, kv, fwd);
         put_row(rec + ch * RLB + RC_KH * 2, tmp);
-        float inv[C];  // e^{-Gamma_r} = e^{Gamma_C - Gamma_r} / e^{Gamma_C}
-#pragma unroll
-        for (int e = 0; e < C / 2; ++e) {
-            inv[2 * e] = rev[2 * e];
-            inv[2 * e + 1] = rev[2 * e + 1];
-            mul2_inplace(inv[2 * e], inv[2 * e + 1], make_float2(einv, einv));
-        }
-        vmul(tmp, kv, inv);
-        put_row(scr + X_KT + ch * TROW, tmp);
-        vmul(tmp, kv, rev);
-        put_row(rec + ch * RLB + RC_K * 2, tmp);
         if (WANT_Q) {
             float qv[C];
 #pragma unroll
@@ -275,6 +269,12 @@ __device__ __forceinline__ void elementwise(const uint8_t *in, uint8_t *scr, uin
             vmul(tmp, qv, fwd);
             put_row(rec + ch * RLB + RC_Q * 2, tmp);
         }
+        vmul(tmp, kv, rev);
+        put_row(rec + ch * RLB + RC_K * 2, tmp);
+        // Kt = K e^{-Gamma_r} = Kb / e^{Gamma_C}, in place
+#pragma unroll
+        for (int e = 0; e < C / 2; ++e) mul2_inplace(tmp[2 * e], tmp[2 * e + 1], make_float2(einv, einv));
+        put_row(scr + X_KT + ch * TROW, tmp);
         ((float *)(rec + R_DECAY))[ch] = eGC;
     }
 }
