@@ -418,7 +418,10 @@ def run_ours(args):
     res1["l2"] = "512 MB buffer zero-filled between timed steps (working set 50 MB)"
     result["short"] = res1
     if not args.no_extras:
-        result["backward"] = run_backward(kda, x1, flush, dev, dist)
+        result["backward"] = run_backward(kda, x1, flush, dev, dist, peaks)
+        # the same workload's one-call forward step, timed just above
+        result["backward"]["vs_forward"] = round(result["backward"]["ms_per_step"] /
+                                                 res1["ms_per_step"], 3)
     if not args.no_decode:
         result["decode"] = run_decode(kda, make_decode_inputs, WORKLOADS[DECODE], dev, dist,
                                       world, peaks, rank)
@@ -478,7 +481,7 @@ def run_ckpt(kda, x, Sg, out, dev, dist, plain_ms, interval=CKPT_INTERVAL):
             "overhead_vs_plain": round(ms / plain_ms - 1.0, 4)}
 
 
-def run_backward(kda, x, flush, dev, dist):
+def run_backward(kda, x, flush, dev, dist, peaks):
     """kda_prefill_backward on the short workload (d_out ~ N(0, 1), d_S_final ~
     N(0, 1)): dq, dk, dv, dg, dbeta, dS0 in fp32; L2 flushed before each call."""
     import torch
@@ -498,24 +501,44 @@ def run_backward(kda, x, flush, dev, dist):
 
     per = time_calls(call, 5, 3, flush)
     ms = max_over_ranks(sum(per), dist, dev) / len(per)
-    # algorithmic work per head-token and state element: the forward step (decay 1,
-    # M^T k 2, rank-1 update 2) and its adjoint (read 2, dS^T k 2, S_t do 2,
-    # dk 4, dM 2, dg 2, decay 1) = 20 flops; fp32 on CUDA cores
-    flops = 20.0 * dk * dv * T * H
-    props = torch.cuda.get_device_properties(dev)
-    sms = props.multi_processor_count
-    peak = sms * 128 * 2 * 2.07e9 / 1e12
-    achieved = flops / (ms * 1e-3) / 1e12
-    return {"workload": SHORT,
-            "what": "dq, dk, dv, dg, dbeta, dS0 (fp32), token-level SIMT kernels, segment split",
-            "ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    base = {"workload": SHORT, "ms_per_step": round(ms, 4),
+            "tokens_per_s": round(T / (ms * 1e-3), 1),
             "segments": kda.prefill_backward_num_segments(desc),
             "workspace_bytes": int(ws.numel()),
-            "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 2),
-                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                         "flops_per_head_token": 20 * dk * dv,
-                         "peak_from": "%d SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (maximum "
-                                      "SM clock)" % sms}}
+            "vs_forward": None}
+    if act == "bf16" and dk == 128 and dv == 128:
+        # chunked form: per 16-token block, products of 16 x 128 x 128 (B = 2 * 16 *
+        # 128 * 128 flops) and 16 x 16 x 128 (S = 2 * 16 * 16 * 128): the forward
+        # chain 2B + S and its L, Mq 2S; the adjoint chain 3B + 2S and its L, Mq 2S;
+        # the gradients 5B + 11S (R, K_b dS', dO S^T, dR S^T, U dS'^T; L, Mq, Mq^T dO,
+        # T R, T^T dU, dU R^T, dO U^T, and four more for dKt, dQh, dKh)
+        B, S = 2 * 16 * 128 * 128, 2 * 16 * 16 * 128
+        fpt = (10 * B + 18 * S) // 16
+        achieved = fpt * T * H / (ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        base["what"] = ("dq, dk, dv, dg, dbeta, dS0 (fp32) in the chunked form: forward and "
+                        "adjoint chains and per-block gradients on mma.sync, segment split")
+        base["roofline"] = {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                            "flops_per_head_token": fpt,
+                            "peak_from": "measured BF16 dense GEMM (%s); the products run on "
+                                         "mma.sync, whose issue rate caps them near 629 "
+                                         "TFLOP/s" % peaks["source"]}
+        return base
+    # token level (fp32 on CUDA cores): per head-token and state element the forward
+    # step (decay 1, M^T k 2, rank-1 update 2) and its adjoint (read 2, dS^T k 2,
+    # S_t do 2, dk 4, dM 2, dg 2, decay 1) = 20 flops
+    flops = 20.0 * dk * dv * T * H
+    peak = sms * 128 * 2 * 2.07e9 / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
+    base["what"] = "dq, dk, dv, dg, dbeta, dS0 (fp32), token-level kernels, segment split"
+    base["roofline"] = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 2),
+                        "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                        "flops_per_head_token": 20 * dk * dv,
+                        "peak_from": "%d SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (maximum "
+                                     "SM clock)" % sms}
+    return base
 
 
 def run_e2e(args, kda, x, Sg, out, SF, ws, dev, dist, world):

@@ -102,8 +102,10 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
     const int nt = min(C, a.cu[n + 1] - t0);
     const size_t row_stride = (size_t)a.H * D;  // elements between tokens
 
-    // ---- loads (asynchronous copies, all in flight at once): inputs (rows past
-    // the block's end are zero-filled), dS'^T, and S^T
+    // ---- loads (asynchronous copies, all in flight at once) in two groups: the
+    // block's inputs (rows past the block's end are zero-filled), then dS'^T and
+    // S^T (64 KB), which the elementwise factors, L, Mq and Y do not need, so they
+    // land while those run
     {
         const size_t base = ((size_t)t0 * a.H + h) * D;
         for (int e = tid; e < 4 * C * 16; e += GT) {  // q, k, v, dO: 16 rows x 16 chunks
@@ -119,6 +121,11 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             cp_async16(sb + F_G + r * 512 + 16 * c4, a.g + base + (r < nt ? r : 0) * row_stride + 4 * c4,
                        r < nt);
         }
+        if (tid < C) {
+            float *bt = (float *)(sm + F_VEC);
+            bt[tid] = tid < nt ? a.beta[(size_t)(t0 + tid) * a.H + h] : 0.f;
+        }
+        cp_async_commit();
         const __nv_bfloat16 *dsrc = a.dSck + ((size_t)(cbase + c) * a.H + h) * D * D;
         for (int e = tid; e < D * 16; e += GT) {  // the adjoint at this block's end
             const int j = e >> 4, cc = e & 15;
@@ -131,10 +138,6 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
                 cp_async16(sb + T_ST + sw(j, cc), ssrc + (size_t)j * D + 8 * cc, true);
             }
         }
-        if (tid < C) {
-            float *bt = (float *)(sm + F_VEC);
-            bt[tid] = tid < nt ? a.beta[(size_t)(t0 + tid) * a.H + h] : 0.f;
-        }
         if (c == 0) {  // the sequence's initial state (fp32 [i][j]) or zeros
             const float *s0 = a.S0 ? a.S0 + ((size_t)n * a.H + h) * D * D : nullptr;
             for (int e = tid; e < D * D / 2; e += GT) {
@@ -144,7 +147,8 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
                 *(uint32_t *)(sm + T_ST + sw(j, i2 >> 2) + 4 * (i2 & 3)) = pack_bf16x2(x0, x1);
             }
         }
-        cp_async_wait_all();
+        cp_async_commit();
+        cp_async_wait_group<1>();  // the inputs
     }
     __syncthreads();
 
@@ -153,36 +157,47 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
     auto small = [&](int which) { return (float *)(sm + F_SMALL) + which * 16 * SQ; };
     auto sbf = [&](int which) { return (__nv_bfloat16 *)(sm + B_SMALL) + which * 16 * TS; };
 
-    // ---- elementwise factors, one thread per key channel (threads 0-127):
-    // e^{Gamma_r} by the running product of alpha = e^g, e^{Gamma_C - Gamma_r} by the
-    // reverse one, e^{-Gamma_r} = e^{Gamma_C - Gamma_r} / e^{Gamma_C}
-    if (tid < D) {
-        const int i = tid;
-        float al[C], fwd[C], rev[C];
+    // ---- elementwise factors, two threads per key channel: threads 0-127 take the
+    // running product of alpha = e^g (e^{Gamma_r}: Kh, Qh), threads 128-255 the
+    // reverse one (e^{Gamma_C - Gamma_r}: Kb; e^{-Gamma_r} = e^{Gamma_C - Gamma_r} /
+    // e^{Gamma_C}: Kt; e^{Gamma_C} itself)
+    {
+        const int i = tid & (D - 1);
+        const bool fwd_half = tid < D;
+        float al[C];
 #pragma unroll
         for (int r = 0; r < C; ++r) al[r] = __expf(fG[r * D + i]);
-        float run = 1.f;
-#pragma unroll
-        for (int r = 0; r < C; ++r) { run *= al[r]; fwd[r] = run; }
-        float b = 1.f;
-#pragma unroll
-        for (int r = C - 1; r >= 0; --r) { rev[r] = b; b *= al[r]; }
-        const float ec = fwd[C - 1], einv = 1.f / ec;
-        eC[i] = ec;
-        const __nv_bfloat16 *qr = (const __nv_bfloat16 *)(sm + T_Q);
         const __nv_bfloat16 *kr = (const __nv_bfloat16 *)(sm + T_K);
+        const __nv_bfloat16 *qr = (const __nv_bfloat16 *)(sm + T_Q);
+        __syncthreads();  // every thread has read g before fG is overwritten
+        if (fwd_half) {
+            float run = 1.f;
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            const float kv = __bfloat162float(kr[r * D + i]), qv = __bfloat162float(qr[r * D + i]);
-            const float em = rev[r] * einv;
-            fG[r * D + i] = fwd[r];  // g is no longer needed: keep e^{Gamma}
-            fEm[r * D + i] = em;
-            fEb[r * D + i] = rev[r];
-            const uint32_t off = sw(r, i >> 3) + 2 * (i & 7);
-            *(__nv_bfloat16 *)(sm + T_KH + off) = __float2bfloat16_rn(kv * fwd[r]);
-            *(__nv_bfloat16 *)(sm + T_KT + off) = __float2bfloat16_rn(kv * em);
-            *(__nv_bfloat16 *)(sm + T_QH + off) = __float2bfloat16_rn(qv * fwd[r]);
-            *(__nv_bfloat16 *)(sm + T_KB + off) = __float2bfloat16_rn(kv * rev[r]);
+            for (int r = 0; r < C; ++r) {
+                run *= al[r];
+                const float kv = __bfloat162float(kr[r * D + i]), qv = __bfloat162float(qr[r * D + i]);
+                fG[r * D + i] = run;  // g is no longer needed: keep e^{Gamma}
+                const uint32_t off = sw(r, i >> 3) + 2 * (i & 7);
+                *(__nv_bfloat16 *)(sm + T_KH + off) = __float2bfloat16_rn(kv * run);
+                *(__nv_bfloat16 *)(sm + T_QH + off) = __float2bfloat16_rn(qv * run);
+            }
+        } else {
+            float rev[C];
+            float b = 1.f;
+#pragma unroll
+            for (int r = C - 1; r >= 0; --r) { rev[r] = b; b *= al[r]; }
+            const float einv = 1.f / b;  // b = e^{Gamma_C}
+            eC[i] = b;
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                const float kv = __bfloat162float(kr[r * D + i]);
+                const float em = rev[r] * einv;
+                fEm[r * D + i] = em;
+                fEb[r * D + i] = rev[r];
+                const uint32_t off = sw(r, i >> 3) + 2 * (i & 7);
+                *(__nv_bfloat16 *)(sm + T_KT + off) = __float2bfloat16_rn(kv * em);
+                *(__nv_bfloat16 *)(sm + T_KB + off) = __float2bfloat16_rn(kv * rev[r]);
+            }
         }
     }
     __syncthreads();
@@ -272,6 +287,7 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             sbf(SB_T)[r * TS + j] = __float2bfloat16_rn(y[r] * beta[j]);  // T = Y Diag(beta)
         }
     }
+    cp_async_wait_group<0>();  // dS'^T and S^T
     __syncthreads();
 
     const int j0 = 16 * warp;  // this warp's 16 value columns (then key channels)

@@ -346,30 +346,44 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
         const int nt = min(C, x.t_end - first_token(c));
 
         // ---- fused prologue: inverse L2 norms of this block's k and q rows (a zero
-        // row keeps scale 0), over the 128 channels = 4 per lane, then the warp
+        // row keeps scale 0).  |k_r|^2 is the diagonal of K K^T, a 16 x 16 x 128
+        // product on the tensor cores (BF16 products are exact in fp32, fp32
+        // accumulation).  One ldmatrix per 16-channel step gives both operands: the
+        // A fragment of rows r is also the B fragment of columns r.  Each row reads its
+        // channels in its own rotated order (chunk + r), which leaves the diagonal
+        // unchanged and puts the eight rows of every 8 x 8 matrix on different banks
+        // of the dense 256-byte rows; the off-diagonal entries are not used.
         float rk[C], rq[C];
         if (GATE) {
-            const __nv_bfloat16 *kin = (const __nv_bfloat16 *)(in + IN_K);
-            const __nv_bfloat16 *qin = (const __nv_bfloat16 *)(in + IN_Q);
+            float accK[2][4] = {}, accQ[2][4] = {};
+            const int mi = lane >> 3, row = (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = row * IN_ROWB + 16 * ((2 * kk + (mi >> 1) + row) & 15);
+                uint32_t f[4];
+                ldsm_x4(in_s + IN_K + off, f);
+                mma_bf16_16816(accK[0], f, f[0], f[2]);
+                mma_bf16_16816(accK[1], f, f[1], f[3]);
+                if (WANT_Q) {
+                    uint32_t fq[4];
+                    ldsm_x4(in_s + IN_Q + off, fq);
+                    mma_bf16_16816(accQ[0], fq, fq[0], fq[2]);
+                    mma_bf16_16816(accQ[1], fq, fq[1], fq[3]);
+                }
+            }
+            // diagonal entry (r, r) sits in lane 4 (r % 8) + (r % 8) / 2: element r % 2
+            // of the first column tile for r < 8, element 2 + r % 2 of the second
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                float sk = 0.f, sq = 0.f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float kv = __bfloat162float(kin[r * D + lane + 32 * m]);
-                    sk += kv * kv;
-                    if (WANT_Q) {
-                        const float qv = __bfloat162float(qin[r * D + lane + 32 * m]);
-                        sq += qv * qv;
-                    }
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
-                    if (WANT_Q) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                }
+                const int src = 4 * (r & 7) + ((r & 7) >> 1);
+                const float sk = __shfl_sync(0xffffffffu, r < 8 ? accK[0][r & 1] : accK[1][2 + (r & 1)], src);
                 rk[r] = sk > 0.f ? rsqrtf(sk) : 0.f;
-                rq[r] = sq > 0.f ? rsqrtf(sq) : 0.f;
+                if (WANT_Q) {
+                    const float sq = __shfl_sync(0xffffffffu, r < 8 ? accQ[0][r & 1] : accQ[1][2 + (r & 1)], src);
+                    rq[r] = sq > 0.f ? rsqrtf(sq) : 0.f;
+                } else {
+                    rq[r] = 0.f;
+                }
             }
         }
 

@@ -105,6 +105,15 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool p
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// Close the group of this thread's copies issued so far; wait until at most N of
+// its groups are still in flight.
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // 2D tiled tensor copy shared -> global (box size and swizzle fixed by the tensor
 // map), as one bulk-async group: cp_bulk_commit() closes the group,
