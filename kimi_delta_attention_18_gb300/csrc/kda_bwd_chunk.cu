@@ -45,16 +45,17 @@ constexpr int T_KH = T_DS + 32768;        // [16 r][128 i]
 constexpr int T_KT = T_KH + 4096;
 constexpr int T_QH = T_KT + 4096;
 constexpr int T_KB = T_QH + 4096;
-constexpr int T_DO = T_KB + 4096;         // [16 r][128 j]
-constexpr int T_R = T_DO + 4096;
+constexpr int T_R = T_KB + 4096;          // [16 r][128 j]
 constexpr int T_U = T_R + 4096;
 constexpr int T_DU = T_U + 4096;
 constexpr int T_NDR = T_DU + 4096;        // -dR
-constexpr int T_Q = T_NDR + 4096;         // raw q, k, v rows [16][128] BF16 (dense)
-constexpr int T_K = T_Q + 4096;
-constexpr int T_V = T_K + 4096;
-constexpr int F_G = T_V + 4096;           // g [16][128] fp32, then e^{Gamma}
-constexpr int F_EM = F_G + 8192;          // e^{-Gamma}
+// Input buffers, two, alternating between consecutive blocks of a CTA: raw q, k, v
+// rows [16][128] BF16 (dense), dO [16][128 j] BF16 (swizzled), g [16][128] fp32
+// (then e^{Gamma}), beta [16]
+constexpr int IB_Q = 0, IB_K = 4096, IB_V = 8192, IB_DO = 12288, IB_G = 16384, IB_BETA = 24576;
+constexpr int IB_SIZE = IB_BETA + 128;
+constexpr int IB0 = T_NDR + 4096;
+constexpr int F_EM = IB0 + 2 * IB_SIZE;   // e^{-Gamma}
 constexpr int F_EB = F_EM + 8192;         // e^{Gamma_C - Gamma}
 constexpr int F_DGAM = F_EB + 8192;       // dGamma [16][128] fp32
 constexpr int F_PART = F_DGAM + 8192;     // partial 16 x 16 products [GW][2][16][16] fp32
@@ -64,8 +65,9 @@ enum { SM_L = 0, SM_MQ, SM_Y, SM_DT, SM_DMQ, SM_P, SM_DMB, NSMALL };
 constexpr int TS = 24;                    // BF16 16 x 16 rows: 16 + pad (48 bytes)
 constexpr int B_SMALL = F_SMALL + NSMALL * 16 * SQ * 4;  // BF16: T, Mq, dMq, dL
 enum { SB_T = 0, SB_MQ, SB_DMQ, SB_DL, NSB };
-constexpr int F_VEC = B_SMALL + NSB * 16 * TS * 2;       // beta [16], eC [128], deC [128]
-constexpr int SMEM_BYTES = F_VEC + (16 + 128 + 128) * 4;
+constexpr int F_VEC = B_SMALL + NSB * 16 * TS * 2;       // eC [128], deC [128]
+constexpr int SMEM_BYTES = F_VEC + (128 + 128) * 4;
+static_assert(IB_SIZE % 128 == 0 && IB0 % 128 == 0, "input buffer alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 struct GradArgs {
@@ -86,60 +88,80 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
     extern __shared__ __align__(128) uint8_t sm[];
     const uint32_t sb = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, t4 = lane & 3;
-    const int h = blockIdx.y;
-    // ---- which block of which sequence
-    int n = 0, c = blockIdx.x, cbase = 0, sbase = 0;
-    for (;; ++n) {
-        if (n >= a.N) return;  // past the last block
-        const int len = a.cu[n + 1] - a.cu[n];
-        const int nb = (len + C - 1) / C;
-        if (c < nb) break;
-        c -= nb;
-        cbase += nb;
-        sbase += len / C;
-    }
-    const int t0 = a.cu[n] + C * c;
-    const int nt = min(C, a.cu[n + 1] - t0);
+    // The work: every (16-token block, head), blocks counted over all sequences.
+    // CTA x takes items x, x + gridDim.x, ...; while one is computed, the next one's
+    // inputs are in flight into the other input buffer, and its 64 KB of S^T and
+    // dS'^T tiles are requested as soon as this one's last products have read them.
+    int nblk = 0;
+    for (int m = 0; m < a.N; ++m) nblk += (a.cu[m + 1] - a.cu[m] + C - 1) / C;
+    const long long items = (long long)nblk * a.H;
     const size_t row_stride = (size_t)a.H * D;  // elements between tokens
-
-    // ---- loads (asynchronous copies, all in flight at once) in two groups: the
-    // block's inputs (rows past the block's end are zero-filled), then dS'^T and
-    // S^T (64 KB), which the elementwise factors, L, Mq and Y do not need, so they
-    // land while those run
-    {
-        const size_t base = ((size_t)t0 * a.H + h) * D;
+    struct Item {
+        bool ok;
+        int n, c, h, t0, nt, cbase, sbase;
+    };
+    auto item = [&](long long it) {
+        Item w{};
+        w.ok = it < items;
+        if (!w.ok) return w;
+        w.h = (int)(it / nblk);
+        int c = (int)(it % nblk), n = 0, cb = 0, sbs = 0;
+        for (;; ++n) {
+            if (n >= a.N) {  // (only with inconsistent lengths)
+                w.ok = false;
+                return w;
+            }
+            const int len = a.cu[n + 1] - a.cu[n];
+            const int nb = (len + C - 1) / C;
+            if (c < nb) break;
+            c -= nb;
+            cb += nb;
+            sbs += len / C;
+        }
+        w.n = n;
+        w.c = c;
+        w.cbase = cb;
+        w.sbase = sbs;
+        w.t0 = a.cu[n] + C * c;
+        w.nt = min(C, a.cu[n + 1] - w.t0);
+        return w;
+    };
+    // the block's inputs, rows past its end zero-filled
+    auto issue_inputs = [&](const Item &w, int ibo) {
+        const size_t base = ((size_t)w.t0 * a.H + w.h) * D;
         for (int e = tid; e < 4 * C * 16; e += GT) {  // q, k, v, dO: 16 rows x 16 chunks
             const int arr = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const __nv_bfloat16 *src = arr == 0 ? a.q : arr == 1 ? a.k : arr == 2 ? a.v : a.dout;
-            const uint32_t dst = arr == 3 ? sb + T_DO + sw(r, cc)
-                                          : sb + (arr == 0 ? T_Q : arr == 1 ? T_K : T_V) +
+            const uint32_t dst = arr == 3 ? sb + ibo + IB_DO + sw(r, cc)
+                                          : sb + ibo + (arr == 0 ? IB_Q : arr == 1 ? IB_K : IB_V) +
                                                 r * 256 + 16 * cc;
-            cp_async16(dst, src + base + (r < nt ? r : 0) * row_stride + 8 * cc, r < nt);
+            cp_async16(dst, src + base + (r < w.nt ? r : 0) * row_stride + 8 * cc, r < w.nt);
         }
         for (int e = tid; e < C * 32; e += GT) {  // g: 16 rows x 32 float4
             const int r = e >> 5, c4 = e & 31;
-            cp_async16(sb + F_G + r * 512 + 16 * c4, a.g + base + (r < nt ? r : 0) * row_stride + 4 * c4,
-                       r < nt);
+            cp_async16(sb + ibo + IB_G + r * 512 + 16 * c4,
+                       a.g + base + (r < w.nt ? r : 0) * row_stride + 4 * c4, r < w.nt);
         }
-        if (tid < C) {
-            float *bt = (float *)(sm + F_VEC);
-            bt[tid] = tid < nt ? a.beta[(size_t)(t0 + tid) * a.H + h] : 0.f;
-        }
-        cp_async_commit();
-        const __nv_bfloat16 *dsrc = a.dSck + ((size_t)(cbase + c) * a.H + h) * D * D;
-        for (int e = tid; e < D * 16; e += GT) {  // the adjoint at this block's end
+        if (tid < C)
+            cp_async4(sb + ibo + IB_BETA + 4 * tid,
+                      a.beta + (size_t)(w.t0 + (tid < w.nt ? tid : 0)) * a.H + w.h, tid < w.nt);
+    };
+    // dS'^T (the adjoint at the block's end) and S^T (the forward state after the
+    // previous block, or the sequence's initial state)
+    auto issue_tiles = [&](const Item &w) {
+        const __nv_bfloat16 *dsrc = a.dSck + ((size_t)(w.cbase + w.c) * a.H + w.h) * D * D;
+        for (int e = tid; e < D * 16; e += GT) {
             const int j = e >> 4, cc = e & 15;
             cp_async16(sb + T_DS + sw(j, cc), dsrc + (size_t)j * D + 8 * cc, true);
         }
-        if (c > 0) {  // S^T: the forward state after the previous block
-            const __nv_bfloat16 *ssrc = a.Sck + ((size_t)(sbase + c - 1) * a.H + h) * D * D;
+        if (w.c > 0) {
+            const __nv_bfloat16 *ssrc = a.Sck + ((size_t)(w.sbase + w.c - 1) * a.H + w.h) * D * D;
             for (int e = tid; e < D * 16; e += GT) {
                 const int j = e >> 4, cc = e & 15;
                 cp_async16(sb + T_ST + sw(j, cc), ssrc + (size_t)j * D + 8 * cc, true);
             }
-        }
-        if (c == 0) {  // the sequence's initial state (fp32 [i][j]) or zeros
-            const float *s0 = a.S0 ? a.S0 + ((size_t)n * a.H + h) * D * D : nullptr;
+        } else {  // fp32 [i][j] or zeros, converted here
+            const float *s0 = a.S0 ? a.S0 + ((size_t)w.n * a.H + w.h) * D * D : nullptr;
             for (int e = tid; e < D * D / 2; e += GT) {
                 const int j = e & 127, i2 = e >> 7;  // channels 2 i2, 2 i2 + 1 of column j
                 const float x0 = s0 ? s0[(size_t)(2 * i2) * D + j] : 0.f;
@@ -147,13 +169,27 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
                 *(uint32_t *)(sm + T_ST + sw(j, i2 >> 2) + 4 * (i2 & 3)) = pack_bf16x2(x0, x1);
             }
         }
-        cp_async_commit();
-        cp_async_wait_group<1>();  // the inputs
-    }
+    };
+
+    const long long G = gridDim.x;
+    long long it = blockIdx.x;
+    Item cur = item(it), nxt = item(it + G);
+    if (!cur.ok) return;
+    // copy groups in flight, oldest first: inputs(k), tiles(k), inputs(k + 1)
+    issue_inputs(cur, IB0);
+    cp_async_commit();
+    issue_tiles(cur);
+    cp_async_commit();
+    if (nxt.ok) issue_inputs(nxt, IB0 + IB_SIZE);
+    cp_async_commit();
+    for (int k = 0;; ++k) {
+    const int ibo = IB0 + (k & 1) * IB_SIZE;
+    const int h = cur.h, t0 = cur.t0, nt = cur.nt;
+    cp_async_wait_group<2>();  // this block's inputs
     __syncthreads();
 
-    float *fG = (float *)(sm + F_G), *fEm = (float *)(sm + F_EM), *fEb = (float *)(sm + F_EB);
-    float *beta = (float *)(sm + F_VEC), *eC = beta + 16, *deC = eC + 128;
+    float *fG = (float *)(sm + ibo + IB_G), *fEm = (float *)(sm + F_EM), *fEb = (float *)(sm + F_EB);
+    float *beta = (float *)(sm + ibo + IB_BETA), *eC = (float *)(sm + F_VEC), *deC = eC + 128;
     auto small = [&](int which) { return (float *)(sm + F_SMALL) + which * 16 * SQ; };
     auto sbf = [&](int which) { return (__nv_bfloat16 *)(sm + B_SMALL) + which * 16 * TS; };
 
@@ -167,8 +203,8 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
         float al[C];
 #pragma unroll
         for (int r = 0; r < C; ++r) al[r] = __expf(fG[r * D + i]);
-        const __nv_bfloat16 *kr = (const __nv_bfloat16 *)(sm + T_K);
-        const __nv_bfloat16 *qr = (const __nv_bfloat16 *)(sm + T_Q);
+        const __nv_bfloat16 *kr = (const __nv_bfloat16 *)(sm + ibo + IB_K);
+        const __nv_bfloat16 *qr = (const __nv_bfloat16 *)(sm + ibo + IB_Q);
         __syncthreads();  // every thread has read g before fG is overwritten
         if (fwd_half) {
             float run = 1.f;
@@ -287,7 +323,7 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             sbf(SB_T)[r * TS + j] = __float2bfloat16_rn(y[r] * beta[j]);  // T = Y Diag(beta)
         }
     }
-    cp_async_wait_group<0>();  // dS'^T and S^T
+    cp_async_wait_group<1>();  // this block's S^T and dS'^T
     __syncthreads();
 
     const int j0 = 16 * warp;  // this warp's 16 value columns (then key channels)
@@ -308,12 +344,12 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
     {
         uint32_t am[4], bd[4];
         lda_small(sbf(SB_MQ), true, am);  // Mq^T
-        ldb_t(T_DO, 0, j0, bd);           // B[k = r'][n = j] = dO[r'][j]
+        ldb_t(ibo + IB_DO, 0, j0, bd);    // B[k = r'][n = j] = dO[r'][j]
         mma_bf16_16816(dUf[0], am, bd[0], bd[1]);
         mma_bf16_16816(dUf[1], am, bd[2], bd[3]);
     }
     // R = V - Kh S (V from the raw rows), both to shared memory as BF16
-    const __nv_bfloat16 *vr = (const __nv_bfloat16 *)(sm + T_V);
+    const __nv_bfloat16 *vr = (const __nv_bfloat16 *)(sm + ibo + IB_V);
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
@@ -358,7 +394,7 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
         float accT[2][4] = {}, accM[2][4] = {};
         uint32_t adu[4], ado[4], br[4], bu[4];
         lda(T_DU, warp, adu);
-        lda(T_DO, warp, ado);
+        lda(ibo + IB_DO, warp, ado);
         ldb_nt(T_R, 0, 2 * warp, br);  // B[k = j][n = r'] = R[r'][j]
         ldb_nt(T_U, 0, 2 * warp, bu);
         mma_bf16_16816(accT[0], adu, br[0], br[1]);
@@ -445,7 +481,7 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         uint32_t ad[4], an[4], au[4], bs[4], bd[4];
-        lda(T_DO, kk, ad);
+        lda(ibo + IB_DO, kk, ad);
         lda(T_NDR, kk, an);
         lda(T_U, kk, au);
         ldb_t(T_ST, 16 * kk, i0, bs);  // B[k = j][n = i] = S^T[j][i]
@@ -478,8 +514,8 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
     // ---- elementwise: dk, dq and dGamma (fp32 factors), then dg per channel
     float *dgam = (float *)(sm + F_DGAM);
     float *kbk = (float *)(sm + F_PART);  // dKb o Kb [16][128] (the partials are consumed)
-    const __nv_bfloat16 *kraw = (const __nv_bfloat16 *)(sm + T_K);
-    const __nv_bfloat16 *qraw = (const __nv_bfloat16 *)(sm + T_Q);
+    const __nv_bfloat16 *kraw = (const __nv_bfloat16 *)(sm + ibo + IB_K);
+    const __nv_bfloat16 *qraw = (const __nv_bfloat16 *)(sm + ibo + IB_Q);
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
@@ -505,7 +541,10 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
                 *(float2 *)(a.dq + o) = make_float2(dq2[0], dq2[1]);
             }
         }
-    __syncthreads();
+    __syncthreads();  // every read of S^T and dS'^T is done: the next block's tiles
+    const Item nx2 = item(it + 2 * G);
+    if (nxt.ok) issue_tiles(nxt);
+    cp_async_commit();
     // dg[r] = sum over r' >= r of dGamma[r'], the last row taking sum_r (dKb o Kb)_r
     // (Gamma_C enters Kb of every row) and deC o e^{Gamma_C}
     if (tid < D) {
@@ -522,6 +561,14 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
 #pragma unroll
         for (int r = 0; r < C; ++r)
             if (r < nt) a.dg[((size_t)(t0 + r) * a.H + h) * D + i] = out[r];
+    }
+    __syncthreads();  // this input buffer is free: the block after next goes into it
+    if (nx2.ok) issue_inputs(nx2, ibo);
+    cp_async_commit();
+    if (!nxt.ok) break;
+    cur = nxt;
+    nxt = nx2;
+    it += G;
     }
 }
 
@@ -541,9 +588,14 @@ cudaError_t launch_bwd_chunk(const PrefillArgs &p, const void *dout,
     a.N = p.N; a.T_tot = p.T_tot; a.H = p.H;
     cudaError_t e = set_max_dynamic_smem((const void *)bwd_chunk_kernel, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    // at most T_tot / 16 + N blocks over all sequences; CTAs past the last one return
-    const unsigned blocks = (unsigned)((p.T_tot + C - 1) / C + p.N);
-    bwd_chunk_kernel<<<dim3(blocks, (unsigned)p.H), GT, SMEM_BYTES, st>>>(a);
+    // one CTA per SM walks the (block, head) list; at most T_tot / 16 + N blocks over
+    // all sequences
+    const long long bound = ((long long)(p.T_tot + C - 1) / C + p.N) * p.H;
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const unsigned grid = (unsigned)(bound < sms ? bound : sms);
+    bwd_chunk_kernel<<<grid, GT, SMEM_BYTES, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -105,6 +105,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool p
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// 4-byte asynchronous copy global -> shared through L1 (zero fill when !pred).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool pred) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(pred ? 4 : 0)
+                 : "memory");
+}
 // Close the group of this thread's copies issued so far; wait until at most N of
 // its groups are still in flight.
 __device__ __forceinline__ void cp_async_commit() {
