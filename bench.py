@@ -52,7 +52,8 @@ ONE_PASS_B = 4 * 256 + 512 + 4
 KCP_B = (2 * 256 + 512 + 4) + ONE_PASS_B
 CKPT_INTERVAL = 4096
 PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_kcp_h56_t64k",
-                 "prefill_ckpt_h8_t4096", "backward_h8_t1024", "backward_h8_t4096")
+                 "prefill_kcp_h56_t16k", "prefill_ckpt_h8_t4096", "backward_h8_t1024",
+                 "backward_h8_t4096")
 # the ncu summary that gives the transfer pass's DRAM traffic per launch, and the
 # kernel source it was taken on
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "prefill_tc_kernel_kcp_h56_t64k_d128.md")
@@ -766,6 +767,14 @@ def run_profile_case(name):
         # the headline's kernels at 1/16 of its length: 56 heads x 65,536 tokens in 4
         # segments of 16,384 tokens (the headline's segment length); 5.6 GB of inputs
         x = make_prefill_inputs([65536], 56, 128, 128, "bf16", device=dev)
+        for _ in range(2):
+            kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                x["cu_seqlens"], num_segments=4)
+    elif name == "prefill_kcp_h56_t16k":
+        # the same kernels on a case small enough for a many-pass capture: 56 heads x
+        # 16,384 tokens in 4 segments (224 units: two-chain transfer pass with a lead
+        # segment), 1.4 GB of inputs
+        x = make_prefill_inputs([16384], 56, 128, 128, "bf16", device=dev)
         for _ in range(2):
             kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                 x["cu_seqlens"], num_segments=4)

@@ -35,8 +35,9 @@
 // pre-pass computes A_s, the zero-start state B_s and the zero-end adjoint of
 // every segment in parallel; bwd_scan_kernel forms every segment's start state
 // and end adjoint in fp32; the gradient pass then runs all segments at once.
-// fp32 throughout: a token-level implementation (the chunked tensor-core form
-// of the backward is not built).
+// fp32 throughout: this token-level form serves fp32 activations and shapes
+// other than dk = dv = 128.  BF16 activations at dk = dv = 128 take the chunked
+// form on tensor cores (launch_backward_chunked at the end of this file).
 #include <string.h>
 
 #include "kda_internal.cuh"

@@ -35,15 +35,24 @@
 // one CTA (NCH = 2): a second group of four chain warps (warps 8-11) consumes the
 // same records, so each block is loaded and prepared once for the identity-start
 // and the zero-start chain.  The warpgroups then run with different register
-// budgets (setmaxnreg): the prep warps give registers to the chain warps.
+// budgets (setmaxnreg): the prep warps give registers to the chain warps.  There
+// the one-call split may also have a lead segment (PrefillArgs::lead): segment 0
+// of every chain, whose start state S0 is known, runs in a lead CTA as an output
+// pass (the zero-start chain from S0, the identity-start warps idle and writing a
+// zero transfer matrix), and the lead CTAs come first in the grid.
+//
+// Two more instantiations serve the chunked backward: the forward chain writing
+// its BF16 state after every full block (chunk states), and the adjoint chain,
+// which takes the blocks from the last to the first with d_out in place of v.
 //
 // The chain is a strict sequence of small products (16 x 128 x 128 per block).
 // Kept in registers, one step costs a handful of dependent mma.sync issues and
 // no round trip through shared or tensor memory, no commit and no cross-warp
 // barrier; the fp32 master state never leaves registers and only its BF16
 // rounding feeds the products, so the decay term e^{Gamma_C} S stays exact in
-// fp32.  In the transfer pass two CTAs per unit run the same recurrence from the
-// identity with zero values (transfer matrix) and from zeros (zero-initial state).
+// fp32.  In the transfer pass the same recurrence runs from the identity with zero
+// values (transfer matrix) and from zeros (zero-initial state): in one CTA (NCH =
+// 2) or, below the throughput regime, in two CTAs per unit.
 //
 // mma.sync m16n8k16 fragments (g8 = lane / 4, t4 = lane % 4):
 //   A (16x16): a0 = A[g8][2t4..+1], a1 = A[g8+8][2t4..+1], a2 = A[g8][2t4+8..+9],
