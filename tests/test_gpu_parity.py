@@ -172,6 +172,31 @@ def test_two_chain_transfer_pass_ragged(gated):
         assert rel_err(_np(A), A_ref) <= 2e-2 and rel_err(_np(B), B_ref) <= 2e-2
 
 
+def test_lead_segment_with_empty_and_short_sequences():
+    """The lead regime (120 chains, fewer than the SMs; 4 segments, so at least one
+    unit per SM): the first segment of every chain is longer and runs from S0 beside
+    the transfer pass.  Empty sequences (every segment empty: the final state is S0
+    itself), a sequence shorter than one block and ragged ones, with slow forgetting
+    and S0 ~ N(0, 1), against the oracle; dropping S0 must break parity."""
+    lengths = [0, 200, 0, 7, 61]
+    H, nseg = 24, 4
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert len(lengths) * H < sms <= len(lengths) * H * nseg
+    x = _gpu_inputs(lengths, H, 128, 128, "bf16", s0_std=1.0, seed=23, slow_decay=True,
+                    device="cuda")
+    out, SF = _run(x, nseg)
+    o_ref, S_ref = _oracle_prefill(x)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(SF).all()
+    assert rel_err(_np(out), o_ref) <= 2e-2
+    assert rel_err(_np(SF), S_ref) <= 2e-2
+    # an empty sequence hands its initial state through unchanged, up to the scan's
+    # hi/lo BF16 split of each state (about 2^-16 of it per segment step)
+    for n in (0, 2):
+        assert rel_err(_np(SF[n]), _np(x["S0"][n])) <= 1e-4
+    _, SF0 = _run(x, nseg, S0=None)
+    assert rel_err(_np(SF0), S_ref) > 0.1
+
+
 def test_config2_varlen_full_size_sampled_heads():
     w = WORKLOADS["kda_prefill_varlen4_h56_t81920_d128_s0"]
     x = _gpu_inputs(w["lengths"], w["H"], w["dk"], w["dv"], w["act"], s0_std=w["s0_std"],
