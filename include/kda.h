@@ -330,20 +330,22 @@ kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_desc_t *desc, const v
  * are overwritten; none may alias an input.
  *
  * BF16 activations at dk = dv = 128 take the chunked form on tensor cores (the
- * 16-token blocks of the prefill): the forward chain stores the state after
- * every full block (BF16), an adjoint chain runs every segment from its last
- * block to its first and stores the adjoint at every block end (BF16), and one
- * CTA per (block, head) then forms that block's gradients from its start state
- * and end adjoint, all blocks in parallel, with no atomics.  q, k, v, g and d_out
- * must then be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).  Its results
- * follow BF16 rounding of the chain's operands and of the stored states (the BF16
- * tolerance of the prefill applies).  Workspace: 32 KB per head and 16 tokens
- * for the states plus the same, plus one block per sequence, for the adjoints
- * (4 KB per head-token), plus 384 KB per (sequence, head, segment) when
- * segments are used.  Other dtypes and shapes take the token-level form in fp32:
- * one CTA per (sequence, head, 32 value columns) recomputes the states from a
- * checkpoint at every 4-token block start (16 KB of workspace per head-token at
- * d = 128); dq, dk, dg and dbeta are zeroed on the stream, then accumulated.
+ * 16-token blocks of the prefill): the forward chain stores the BF16 state after
+ * every 32 tokens, an adjoint chain runs every segment from its last block to its
+ * first and stores the adjoint at every block end (BF16), and one CTA per SM then
+ * walks the (block pair, head) items, forming every block's gradients from its
+ * start state (stored, or one small product away inside the pair) and its end
+ * adjoint, with no atomics.  q, k, v, g and d_out must then be 16-byte aligned
+ * (KDA_ERR_INVALID_ARG otherwise).  Its results follow BF16 rounding of the
+ * chain's operands and of the stored states (the BF16 tolerance of the prefill
+ * applies).  Workspace: 32 KB per head and 32 tokens for the states and 32 KB per
+ * head and 16 tokens (plus one block per sequence) for the adjoints, about 3 KB per
+ * head-token, plus 256 KB per (sequence, head, segment) when segments are used,
+ * part of it shared with the states.  Other dtypes and shapes take the token-level
+ * form in fp32: one CTA per (sequence, head, 32 value columns) recomputes the
+ * states from a checkpoint at every 4-token block start (16 KB of workspace per
+ * head-token at d = 128); dq, dk, dg and dbeta are zeroed on the stream, then
+ * accumulated.
  *
  * desc->num_segments (0: the library's choice, at most 64) splits every sequence
  * into segments run in parallel: each segment's transfer matrix A, zero-start

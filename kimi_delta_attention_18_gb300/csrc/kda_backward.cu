@@ -835,28 +835,40 @@ cudaError_t launch_backward(const PrefillArgs &p, const void *dout, const float 
 // adjoint gives B^_s (segments reversed), and the tensor-core scan runs twice:
 // X_s = A_{s-1} X_{s-1} + B_{s-1} (start states) and, over the reversed segments,
 // Y_s = A_{s+1}^T Y_{s+1} + B^_{s+1} (end adjoints).
-// Workspace (each piece 256-byte aligned): forward states [T_tot / 16][H][128][128]
-// BF16, adjoints [ceil(T_tot / 16) + N][H][128][128] BF16, and with Sg > 1 the
-// images of A and A^T (2 x 2 x 128 x 128 BF16) and B, B^, X, Y (fp32) per
-// (sequence, head, segment).
+// Workspace (each piece 256-byte aligned), in the order of the launches:
+//   region A: with Sg > 1 first two of the four segment buffers (below), then,
+//             once the scans have read them, the forward states [T_tot / 32][H]
+//             [128][128] BF16 (the state after every 32 tokens of a sequence; the
+//             gradient kernel forms the state after the 16 tokens in between);
+//   with Sg > 1 the other two segment buffers;
+//   the adjoints [ceil(T_tot / 16) + N][H][128][128] BF16.
+// The four segment buffers are 128 x 128 fp32 per (sequence, head, segment):
+// buf0 the images of A (hi, lo), then B^; buf2 the images of A^T; buf1 B, then Y;
+// buf3 X.
+static size_t seg_buffer_bytes(int N, int H, int Sg) {
+    return r256((size_t)N * H * Sg * 128 * 128 * 4);
+}
+static size_t fwd_state_bytes(int T_tot, int H) {
+    return r256((size_t)(T_tot / 32) * H * 128 * 128 * 2);
+}
+static size_t region_a_bytes(int N, int T_tot, int H, int Sg) {
+    const size_t fwd = fwd_state_bytes(T_tot, H), two = 2 * seg_buffer_bytes(N, H, Sg);
+    return Sg > 1 && two > fwd ? two : fwd;
+}
 size_t backward_chunked_workspace_bytes(int N, int T_tot, int H, int Sg) {
-    const size_t img = (size_t)128 * 128 * 2;
-    const size_t fwd = r256((size_t)(T_tot / 16) * H * img);
-    const size_t adj = r256((size_t)((T_tot + 15) / 16 + N) * H * img);
-    const size_t seg = Sg > 1 ? 6 * r256((size_t)N * H * Sg * 128 * 128 * 4) : 0;
-    return fwd + adj + seg;
+    const size_t adj = r256((size_t)((T_tot + 15) / 16 + N) * H * 128 * 128 * 2);
+    return region_a_bytes(N, T_tot, H, Sg) + (Sg > 1 ? 2 * seg_buffer_bytes(N, H, Sg) : 0) + adj;
 }
 
 cudaError_t launch_backward_chunked(const PrefillArgs &p, const void *dout, const float *dSF,
                                     float *dq, float *dk, float *dv, float *dg, float *dbeta,
                                     float *dS0, int Sg, void *workspace, cudaStream_t st) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
-    const size_t img = (size_t)128 * 128 * 2;
     uint8_t *ws = (uint8_t *)workspace;
-    __nv_bfloat16 *fwd_states = (__nv_bfloat16 *)ws;
-    ws += r256((size_t)(p.T_tot / 16) * p.H * img);
-    __nv_bfloat16 *adj_states = (__nv_bfloat16 *)ws;
-    ws += r256((size_t)((p.T_tot + 15) / 16 + p.N) * p.H * img);
+    const size_t ra = region_a_bytes(p.N, p.T_tot, p.H, Sg);
+    const size_t seg = Sg > 1 ? seg_buffer_bytes(p.N, p.H, Sg) : 0;
+    __nv_bfloat16 *fwd_states = (__nv_bfloat16 *)ws;  // written after the scans
+    __nv_bfloat16 *adj_states = (__nv_bfloat16 *)(ws + ra + 2 * seg);
     PrefillArgs base = p;
     base.Sg = Sg;
     base.seg_begin = 0;
@@ -876,11 +888,16 @@ cudaError_t launch_backward_chunked(const PrefillArgs &p, const void *dout, cons
     adj.S_final = dS0;      // the adjoint at the start of segment 0
     cudaError_t e;
     if (Sg > 1) {
+        // The launch order lets four buffers serve six arrays: the forward scan
+        // reads A's images and B, after which the zero-end adjoint chain writes B^
+        // over A's images and the adjoint scan writes Y over B.  buf0 and buf2 are
+        // dead once the adjoint scan has run, and the forward states take their
+        // place.
         const int units = p.N * p.H;
-        const size_t seg = r256((size_t)units * Sg * 128 * 128 * 4);
-        __nv_bfloat16 *a_img = (__nv_bfloat16 *)ws, *a_img_t = (__nv_bfloat16 *)(ws + seg);
-        float *TB = (float *)(ws + 2 * seg), *TBh = (float *)(ws + 3 * seg);
-        float *X = (float *)(ws + 4 * seg), *Yr = (float *)(ws + 5 * seg);
+        uint8_t *buf0 = ws, *buf2 = ws + seg, *buf1 = ws + ra, *buf3 = ws + ra + seg;
+        __nv_bfloat16 *a_img = (__nv_bfloat16 *)buf0, *a_img_t = (__nv_bfloat16 *)buf2;
+        float *TB = (float *)buf1, *X = (float *)buf3;
+        float *TBh = (float *)buf0, *Yr = (float *)buf1;
         PrefillArgs t = base;  // A_s (both images) and B_s
         t.mode = MODE_TRANSFER;
         t.transfer = nullptr;
@@ -888,15 +905,15 @@ cudaError_t launch_backward_chunked(const PrefillArgs &p, const void *dout, cons
         t.transfer_img_t = a_img_t;
         t.zero_state = TB;
         if ((e = launch_prefill_tc(t, st)) != cudaSuccess) return e;
+        if ((e = launch_compose(units, Sg, 128, 128, nullptr, a_img, TB, p.S0, X, nullptr, nullptr,
+                                p.dev_status, st)) != cudaSuccess)
+            return e;
         PrefillArgs tz = base;  // B^_s: the adjoint chain from a zero end adjoint
         tz.mode = MODE_TRANSFER;
         tz.rev = 1;
         tz.v = dout;
         tz.zero_state = TBh;
         if ((e = launch_prefill_tc(tz, st)) != cudaSuccess) return e;
-        if ((e = launch_compose(units, Sg, 128, 128, nullptr, a_img, TB, p.S0, X, nullptr, nullptr,
-                                p.dev_status, st)) != cudaSuccess)
-            return e;
         if ((e = launch_compose(units, Sg, 128, 128, nullptr, a_img_t, TBh, dSF, Yr, nullptr,
                                 nullptr, p.dev_status, st)) != cudaSuccess)
             return e;

@@ -74,7 +74,7 @@ struct GradArgs {
     const __nv_bfloat16 *q, *k, *v, *dout;
     const float *g, *beta, *S0;
     const int32_t *cu;
-    const __nv_bfloat16 *Sck;   // forward states after every full block: slot ckpt_base(n, 16) + c
+    const __nv_bfloat16 *Sck;   // forward states after every 32 tokens: slot ckpt_base(n, 32) + m
     const __nv_bfloat16 *dSck;  // adjoints at every block end: slot block_base(n) + c
     float *dq, *dk, *dv, *dg, *dbeta;
     int N, T_tot, H;
@@ -88,24 +88,35 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
     extern __shared__ __align__(128) uint8_t sm[];
     const uint32_t sb = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, t4 = lane & 3;
-    // The work: every (16-token block, head), blocks counted over all sequences.
-    // CTA x takes items x, x + gridDim.x, ...; while one is computed, the next one's
-    // inputs are in flight into the other input buffer, and its 64 KB of S^T and
-    // dS'^T tiles are requested as soon as this one's last products have read them.
-    int nblk = 0;
-    for (int m = 0; m < a.N; ++m) nblk += (a.cu[m + 1] - a.cu[m] + C - 1) / C;
-    const long long items = (long long)nblk * a.H;
+    // The work: pairs of 16-token blocks (2p, 2p + 1) of a sequence, for every head,
+    // pairs counted over all sequences.  CTA x takes pair items x, x + gridDim.x,
+    // ..., and of each the even block, then the odd one.  The forward chain stored
+    // the state after every 32 tokens, i.e. at the start of every even block; the
+    // start state of an odd block is formed here from the even block's S, U and
+    // Kb.  While one block is computed, the next one's inputs are in flight into
+    // the other input buffer, and its tiles are requested as soon as this one's
+    // last products have read them.
+    int npair = 0;
+    for (int m = 0; m < a.N; ++m) npair += ((a.cu[m + 1] - a.cu[m] + C - 1) / C + 1) / 2;
+    const long long items = (long long)npair * a.H;
+    const long long G = gridDim.x;
     const size_t row_stride = (size_t)a.H * D;  // elements between tokens
     struct Item {
-        bool ok;
+        bool ok, odd;
+        long long it;
         int n, c, h, t0, nt, cbase, sbase;
     };
-    auto item = [&](long long it) {
+    auto fill = [&](Item &w) {
+        w.t0 = a.cu[w.n] + C * w.c;
+        w.nt = min(C, a.cu[w.n + 1] - w.t0);
+    };
+    auto pair_item = [&](long long it) {  // the even block of pair item it
         Item w{};
+        w.it = it;
         w.ok = it < items;
         if (!w.ok) return w;
-        w.h = (int)(it / nblk);
-        int c = (int)(it % nblk), n = 0, cb = 0, sbs = 0;
+        w.h = (int)(it / npair);
+        int q = (int)(it % npair), n = 0, cb = 0, sbs = 0;
         for (;; ++n) {
             if (n >= a.N) {  // (only with inconsistent lengths)
                 w.ok = false;
@@ -113,18 +124,28 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             }
             const int len = a.cu[n + 1] - a.cu[n];
             const int nb = (len + C - 1) / C;
-            if (c < nb) break;
-            c -= nb;
+            if (q < (nb + 1) / 2) break;
+            q -= (nb + 1) / 2;
             cb += nb;
-            sbs += len / C;
+            sbs += len / (2 * C);
         }
         w.n = n;
-        w.c = c;
+        w.c = 2 * q;
         w.cbase = cb;
         w.sbase = sbs;
-        w.t0 = a.cu[n] + C * c;
-        w.nt = min(C, a.cu[n + 1] - w.t0);
+        fill(w);
         return w;
+    };
+    auto next_of = [&](const Item &w) {
+        if (!w.ok) return w;
+        if (!w.odd && w.t0 + C < a.cu[w.n + 1]) {  // the odd block of the same pair
+            Item v = w;
+            v.odd = true;
+            v.c = w.c + 1;
+            fill(v);
+            return v;
+        }
+        return pair_item(w.it + G);
     };
     // the block's inputs, rows past its end zero-filled
     auto issue_inputs = [&](const Item &w, int ibo) {
@@ -146,16 +167,18 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             cp_async4(sb + ibo + IB_BETA + 4 * tid,
                       a.beta + (size_t)(w.t0 + (tid < w.nt ? tid : 0)) * a.H + w.h, tid < w.nt);
     };
-    // dS'^T (the adjoint at the block's end) and S^T (the forward state after the
-    // previous block, or the sequence's initial state)
+    // dS'^T (the adjoint at the block's end) and, for an even block, S^T (the forward
+    // state after the previous block, or the sequence's initial state)
     auto issue_tiles = [&](const Item &w) {
         const __nv_bfloat16 *dsrc = a.dSck + ((size_t)(w.cbase + w.c) * a.H + w.h) * D * D;
         for (int e = tid; e < D * 16; e += GT) {
             const int j = e >> 4, cc = e & 15;
             cp_async16(sb + T_DS + sw(j, cc), dsrc + (size_t)j * D + 8 * cc, true);
         }
-        if (w.c > 0) {
-            const __nv_bfloat16 *ssrc = a.Sck + ((size_t)(w.sbase + w.c - 1) * a.H + w.h) * D * D;
+        if (w.odd) {
+            // formed from the even block's data (next_state)
+        } else if (w.c > 0) {
+            const __nv_bfloat16 *ssrc = a.Sck + ((size_t)(w.sbase + w.c / 2 - 1) * a.H + w.h) * D * D;
             for (int e = tid; e < D * 16; e += GT) {
                 const int j = e >> 4, cc = e & 15;
                 cp_async16(sb + T_ST + sw(j, cc), ssrc + (size_t)j * D + 8 * cc, true);
@@ -171,9 +194,7 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
         }
     };
 
-    const long long G = gridDim.x;
-    long long it = blockIdx.x;
-    Item cur = item(it), nxt = item(it + G);
+    Item cur = pair_item(blockIdx.x), nxt = next_of(cur);
     if (!cur.ok) return;
     // copy groups in flight, oldest first: inputs(k), tiles(k), inputs(k + 1)
     issue_inputs(cur, IB0);
@@ -542,9 +563,46 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             }
         }
     __syncthreads();  // every read of S^T and dS'^T is done: the next block's tiles
-    const Item nx2 = item(it + 2 * G);
+    const Item nx2 = next_of(nxt);
     if (nxt.ok) issue_tiles(nxt);
     cp_async_commit();
+    if (nxt.ok && nxt.odd) {
+        // S^T of the odd block: S^T Diag(e^{Gamma_C}) + U^T Kb of this one, this
+        // warp's rows j of the S^T tile in place (every element is read and
+        // written by the lane that holds it in the fragments)
+        const int jw = 16 * warp;
+        uint32_t au[4];  // A = U^T (rows j, k = r) from the [16 r][128 j] U tile
+        {
+            const int mi = lane >> 3, row = (lane & 7) + 8 * (mi >> 1);
+            ldsm_x4_t(sb + T_U + sw(row, (jw >> 3) + (mi & 1)), au);
+        }
+        float acc[16][4];
+#pragma unroll
+        for (int nt8 = 0; nt8 < 16; ++nt8)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int j = jw + g8 + 8 * hh, i = 8 * nt8 + 2 * t4;
+                const float2 sv = __bfloat1622float2(
+                    *(const __nv_bfloat162 *)(sm + T_ST + sw(j, i >> 3) + 2 * (i & 7)));
+                acc[nt8][2 * hh] = sv.x * eC[i];
+                acc[nt8][2 * hh + 1] = sv.y * eC[i + 1];
+            }
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t bk[4];
+            ldb_t(T_KB, 0, 16 * np, bk);  // B[k = r][n = i] = Kb[r][i]
+            mma_bf16_16816(acc[2 * np], au, bk[0], bk[1]);
+            mma_bf16_16816(acc[2 * np + 1], au, bk[2], bk[3]);
+        }
+#pragma unroll
+        for (int nt8 = 0; nt8 < 16; ++nt8)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int j = jw + g8 + 8 * hh, i = 8 * nt8 + 2 * t4;
+                *(uint32_t *)(sm + T_ST + sw(j, i >> 3) + 2 * (i & 7)) =
+                    pack_bf16x2(acc[nt8][2 * hh], acc[nt8][2 * hh + 1]);
+            }
+    }
     // dg[r] = sum over r' >= r of dGamma[r'], the last row taking sum_r (dKb o Kb)_r
     // (Gamma_C enters Kb of every row) and deC o e^{Gamma_C}
     if (tid < D) {
@@ -568,7 +626,6 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
     if (!nxt.ok) break;
     cur = nxt;
     nxt = nx2;
-    it += G;
     }
 }
 

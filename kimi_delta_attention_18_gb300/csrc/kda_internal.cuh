@@ -111,8 +111,8 @@ struct PrefillArgs {
     // S0) and S_final receives the adjoint at the start of segment 0.
     // chunk_states (if set): [slots][H][dv][dk] BF16, the state transposed (row j
     // = value column, key channels contiguous): the forward chain writes the state
-    // after every full 16-token block of a sequence to slot
-    // ckpt_base(n, 16) + done / 16 - 1; the adjoint chain writes the adjoint at the
+    // after every 32 tokens of a sequence (every second 16-token block) to slot
+    // ckpt_base(n, 32) + done / 32 - 1; the adjoint chain writes the adjoint at the
     // end of every block, before stepping through it, to slot cbase(n) + block
     // (cbase(n) = sum over m < n of ceil(len_m / 16)).
     // In rev mode the segments' arrays run in reverse order: seg_init is read and

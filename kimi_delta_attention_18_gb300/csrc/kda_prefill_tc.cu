@@ -42,7 +42,7 @@
 // zero transfer matrix), and the lead CTAs come first in the grid.
 //
 // Two more instantiations serve the chunked backward: the forward chain writing
-// its BF16 state after every full block (chunk states), and the adjoint chain,
+// its BF16 state after every 32 tokens (chunk states), and the adjoint chain,
 // which takes the blocks from the last to the first with d_out in place of v.
 //
 // The chain is a strict sequence of small products (16 x 128 x 128 per block).
@@ -795,9 +795,9 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(x.bar(B_REC_EMPTY + slot));
-        if (CKS) {  // the state after every full block, BF16 transposed
+        if (CKS) {  // the state after every 32 tokens, BF16 transposed
             const int done = min(x.t_begin + C * (c + 1), x.t_end) - x.seq0;
-            if (done % C == 0) store_chunk_state(x.cs_base + done / C - 1);
+            if (done % (2 * C) == 0) store_chunk_state(x.cs_base + done / (2 * C) - 1);
         }
         if (p.ckpt_interval > 0) {  // state checkpoint after this block
             const int done = min(x.t_begin + C * (c + 1), x.t_end) - x.seq0;
@@ -1019,7 +1019,7 @@ __global__ void __launch_bounds__(cta_threads(NCH), 1)
     x.nchunks = (x.t_end - x.t_begin + C - 1) / C;
     x.seq0 = p.cu[x.n];
     x.ckpt_base = p.ckpt_interval > 0 ? ckpt_base(p.cu, x.n, p.ckpt_interval) : 0;
-    x.cs_base = !p.chunk_states ? 0 : (p.rev ? block_base(p.cu, x.n) : ckpt_base(p.cu, x.n, C));
+    x.cs_base = !p.chunk_states ? 0 : (p.rev ? block_base(p.cu, x.n) : ckpt_base(p.cu, x.n, 2 * C));
 
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {

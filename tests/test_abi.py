@@ -242,10 +242,10 @@ def test_backward_host_checks():
     assert L.kda_prefill_backward_num_segments(ctypes.byref(_desc(chunk=32))) == 0
     # BF16 at dk = dv = 128 takes the chunked backward, which splits sequences until
     # every SM has a one-chain CTA (at least 4 blocks per segment, at most 64) and keeps
-    # BF16 states per 16-token block:
-    # [T/16][H] forward states and [ceil(T/16) + N][H] adjoints of 128 x 128 BF16, plus
-    # with S > 1 the BF16 images of A and A^T and the fp32 B, B^, X, Y per (sequence,
-    # head, segment)
+    # BF16 states: [T/32][H] forward states (every 32 tokens) and [ceil(T/16) + N][H]
+    # adjoints (every 16-token block) of 128 x 128 BF16, plus with S > 1 four 128 x 128
+    # fp32 buffers per (sequence, head, segment), reused between the launches: the
+    # forward states share their bytes with two of them
     for T, H, N in ((4096, 8, 1), (512, 8, 1), (64 * 512, 8, 64)):
         c = _desc(num_seqs=N, total_tokens=T, num_heads=H, dk=128, dv=128, act_dtype=1,
                   num_segments=0)
@@ -257,9 +257,9 @@ def test_backward_host_checks():
         want_s = 1 if chains >= sms else max(1, min(-(-sms // chains), T // N // 16 // 4, 64))
         assert S == want_s, (T, H, N, S)
         img = 128 * 128 * 2
-        want = r256(T // 16 * H * img) + r256(((T + 15) // 16 + N) * H * img)
-        if S > 1:
-            want += 6 * r256(N * H * S * 128 * 128 * 4)
+        fwd, seg = r256(T // 32 * H * img), r256(N * H * S * 128 * 128 * 4)
+        want = r256(((T + 15) // 16 + N) * H * img)
+        want += max(fwd, 2 * seg) + 2 * seg if S > 1 else fwd
         assert L.kda_prefill_backward_workspace_size(ctypes.byref(c)) == want
     # the chunked path moves rows as 16-byte pieces: unaligned rows are refused
     c = _desc(num_seqs=1, total_tokens=64, num_heads=2, dk=128, dv=128, act_dtype=1,
