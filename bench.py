@@ -545,8 +545,11 @@ def run_backward(kda, x, flush, dev, dist, peaks):
 def run_e2e(args, kda, x, Sg, out, SF, ws, dev, dist, world):
     """The headline call end to end: every step copies q, k, v, g, beta in from
     pinned host memory, runs kda_prefill_chunked and copies out and S_final back,
-    all inside the timed region (one stream; the device buffers are the headline
-    leg's own, rewritten with the same values)."""
+    all inside the timed region.  The device-to-host copy of step i runs on a
+    second stream, into two alternating device result buffers, so that it overlaps
+    the host-to-device copy of step i + 1 (the link carries both directions at
+    once); the inputs are the headline leg's own device buffers, rewritten with
+    the same values every step."""
     import torch
     names = ("q", "k", "v", "g", "beta")
     try:
@@ -560,27 +563,44 @@ def run_e2e(args, kda, x, Sg, out, SF, ws, dev, dist, world):
     T = x["q"].shape[0]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size() + sf_h.numel() * sf_h.element_size()
+    outs, sfs = [out, torch.empty_like(out)], [SF, torch.empty_like(SF)]
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    computed = [torch.cuda.Event(), torch.cuda.Event()]
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    for ev in copied:
+        ev.record(main)
 
-    def one():
+    def step(i):
+        b = i % 2
         for n in names:
             x[n].copy_(host[n], non_blocking=True)
+        main.wait_event(copied[b])  # the result buffer has been copied out
         kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["cu_seqlens"],
-                            num_segments=Sg, out=out, S_final=SF, workspace=ws)
-        out_h.copy_(out, non_blocking=True)
-        sf_h.copy_(SF, non_blocking=True)
+                            num_segments=Sg, out=outs[b], S_final=sfs[b], workspace=ws)
+        computed[b].record(main)
+        side.wait_event(computed[b])
+        with torch.cuda.stream(side):
+            out_h.copy_(outs[b], non_blocking=True)
+            sf_h.copy_(sfs[b], non_blocking=True)
+        copied[b].record(side)
 
-    one()
+    step(0)
+    main.wait_stream(side)
     torch.cuda.synchronize()
     barrier(dist)
     e0, e1 = ev_pair()
     e0.record()
-    for _ in range(args.e2e_steps):
-        one()
+    for i in range(args.e2e_steps):
+        step(i)
+    main.wait_stream(side)
     e1.record()
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     step_ms = ms / args.e2e_steps
-    # the step's two copies timed alone (best of two): their sum bounds the step
+
+    # the step's two copies timed alone (best of two); with the overlap the step is
+    # bounded by the host-to-device copy plus the call
     def timed(fn):
         c0, c1 = ev_pair()
         c0.record()
@@ -601,10 +621,12 @@ def run_e2e(args, kda, x, Sg, out, SF, ws, dev, dist, world):
     out_ms = min(timed(copy_out) for _ in range(2))
     return {"value": round(T * args.e2e_steps * world / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(step_ms, 3), "streams": 1,
+            "ms_per_step": round(step_ms, 3), "streams": 2,
+            "overlap": "the device-to-host copy of step i overlaps the host-to-device "
+                       "copy of step i + 1",
             "h2d_ms": round(in_ms, 3), "h2d_gbs": round(h2d / (in_ms * 1e-3) / 1e9, 1),
             "d2h_ms": round(out_ms, 3), "d2h_gbs": round(d2h / (out_ms * 1e-3) / 1e9, 1),
-            "copy_bound_ms": round(in_ms + out_ms, 3)}
+            "bound_ms": round(in_ms, 3)}
 
 
 def run_decode(kda, make_decode_inputs, w, dev, dist, world, peaks, rank):
