@@ -96,6 +96,12 @@ __host__ __device__ constexpr int cta_threads(int nch) { return (W_CHAIN0 + N_CH
 // registers); 104 / 200: 1.60 / 1.08 us.
 constexpr int PREP_REGS = 120, CHAIN_REGS = 192;
 static_assert(128 * PREP_REGS + 256 * CHAIN_REGS <= 384 * 168, "register split");
+// In a lead CTA only the zero-start chain runs: the identity-start warpgroup keeps
+// just what writing a zero transfer matrix takes, and the running chain gets the
+// rest (a separate instantiation, compiled for that budget).
+constexpr int LEAD_IDLE_REGS = 40, LEAD_CHAIN_REGS = 232;
+static_assert(128 * (PREP_REGS + LEAD_IDLE_REGS + LEAD_CHAIN_REGS) <= 384 * 168,
+              "lead register split");
 constexpr long long kWaitLimit = 4000000000ll;  // ~2 s of SM clocks
 
 // ---- shared memory: [NS input stages | NR records | N_PREP prep scratches | O staging]
@@ -508,19 +514,16 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
 // share every B fragment the warp loads from the record.
 constexpr int MT = 2;  // m-tiles per chain warp
 
-template <bool WANT_Q, int NCH, bool REV, bool CKS>
+template <bool WANT_Q, int NCH, bool REV, bool CKS, bool LEAD = false>
 __device__ __forceinline__ void chain_role(const Ctx &x) {
     const PrefillArgs &p = *x.p;
     const int chain = ((threadIdx.x >> 5) - W_CHAIN0) / N_CHAIN;  // 0 unless NCH = 2
     const int cw = ((threadIdx.x >> 5) - W_CHAIN0) % N_CHAIN;
     // with two chains per CTA, chain 0 starts from the identity (transfer matrix)
     // and chain 1 from zeros with the values (zero-initial state)
-    const bool partA = !REV && (NCH == 2 ? chain == 0 : x.partA);
+    // (LEAD: the zero-start chain of a lead CTA, which starts from S0)
+    const bool partA = !REV && !LEAD && (NCH == 2 ? chain == 0 : x.partA);
     const bool want_v = !partA;
-    // In a lead CTA the identity-start chain has nothing to do: its transfer
-    // matrix is written as zeros (the scan then passes the lead segment's end
-    // state on as the next start state), and the zero-start chain starts from S0.
-    const bool idle = NCH == 2 && x.lead && partA;
     const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
     const int j0 = 16 * MT * cw;
     const size_t unit = (size_t)x.n * p.H + x.h;
@@ -533,7 +536,7 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
         if (!x.transfer)
             src = p.seg_init ? p.seg_init + (unit * p.Sg + sidx) * (size_t)D * D
                              : (p.S0 ? p.S0 + unit * (size_t)D * D : nullptr);
-        else if (NCH == 2 && x.lead && !partA && p.S0)
+        else if (LEAD && p.S0)
             src = p.S0 + unit * (size_t)D * D;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
@@ -542,7 +545,7 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 8 * n + 2 * t4 + (e & 1), j = j0 + 16 * m + g8 + 8 * (e >> 1);
-                    S[m][n][e] = partA ? (i == j && !idle ? 1.f : 0.f)
+                    S[m][n][e] = partA ? (i == j ? 1.f : 0.f)
                                          : (src ? src[(size_t)i * D + j] : 0.f);
                 }
     }
@@ -565,8 +568,7 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
                     *(uint32_t *)(d + (size_t)(j0 + 16 * m + g8 + 8 * hi) * D + 8 * n + 2 * t4) =
                         pack_bf16x2(S[m][n][2 * hi], S[m][n][2 * hi + 1]);
     };
-    const int nck = idle ? 0 : x.nchunks;
-    for (int c = 0; c < nck; ++c) {
+    for (int c = 0; c < x.nchunks; ++c) {
         const int slot = c % NR;
         if (!warp_wait(x, B_REC_FULL + slot, (c / NR) & 1)) break;
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
@@ -945,11 +947,48 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
 // REV: the adjoint chain; CKS: the forward chain also writes chunk states (the
 // backward's forward pass).  Both are separate instantiations, so the prefill's
 // own kernels carry none of their code.
+// The identity-start warpgroup of a lead CTA: the lead segment runs from S0, so its
+// transfer matrix is zero (the scan then passes the segment's end state on as the
+// next start state).  Each warp zeroes its 32 rows of both images (or its 32
+// columns of the fp32 matrix) and meets the running chain at its final barrier.
+__device__ __forceinline__ void lead_idle_role(const Ctx &x) {
+    const PrefillArgs &p = *x.p;
+    const int cw = ((threadIdx.x >> 5) - W_CHAIN0) % N_CHAIN, lane = threadIdx.x & 31;
+    const int j0 = 32 * cw;
+    const size_t unit = (size_t)x.n * p.H + x.h;
+    if (p.transfer_img) {
+        __nv_bfloat16 *img = p.transfer_img + (unit * p.Sg + x.s) * (size_t)2 * D * D;
+#pragma unroll 4
+        for (int it = 0; it < 32; ++it) {  // 2 images x 32 rows x 16 pieces of 16 bytes
+            const int idx = 32 * it + lane, im = idx >> 9, row = (idx >> 4) & 31, c16 = idx & 15;
+            *(uint4 *)(img + (size_t)im * D * D + (size_t)(j0 + row) * D + 8 * c16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+    } else if (p.transfer) {
+        float *t = p.transfer + (unit * p.Sg + x.s) * (size_t)D * D;  // [i][j]
+#pragma unroll 4
+        for (int it = 0; it < 32; ++it) {  // 128 rows x 32 columns
+            const int idx = 32 * it + lane, i = idx >> 3, c = idx & 7;
+            float *d = t + (size_t)i * D + j0 + 4 * c;
+            d[0] = d[1] = d[2] = d[3] = 0.f;
+        }
+    }
+    named_bar_or(1, N_CHAIN * 64, *x.abort != 0);
+}
+
 template <bool WANT_Q, bool GATE, int NCH, bool REV = false, bool CKS = false>
 __device__ __forceinline__ void run_role(const Ctx &x, int warp) {
     if (warp < W_CHAIN0) {
         if (NCH == 2) regs_dealloc<PREP_REGS>();
         prep_role<WANT_Q, GATE, REV>(x);
+    } else if (NCH == 2 && !REV && !CKS && x.lead) {
+        if ((warp - W_CHAIN0) / N_CHAIN == 0) {
+            regs_dealloc<LEAD_IDLE_REGS>();
+            lead_idle_role(x);
+        } else {
+            regs_alloc<LEAD_CHAIN_REGS>();
+            chain_role<WANT_Q, NCH, REV, CKS, true>(x);
+        }
     } else {
         if (NCH == 2) regs_alloc<CHAIN_REGS>();
         chain_role<WANT_Q, NCH, REV, CKS>(x);
