@@ -218,11 +218,13 @@ namespace {
 // a share of the combine.  The lead fraction f balances the two: f c1 = (1 - f)
 // u c2 / (P - u) for u chains on P SMs, c1 the time of a 16-token block of a lead
 // chain and c2 that of a block of the transfer pass's two chains together
-// (measured on GB300, 56 heads x 256K tokens: c1 = 1.00 us, c2 = 1.57 us).
-// Only the tensor-core two-chain transfer pass supports it; 0 elsewhere.
+// (measured on GB300, 56 heads x 256K tokens: c1 = 1.00 us, c2 = 1.57 us; with the
+// fused gate prologue, whose heavier prep bounds the lead chain, c1 = 1.37 us,
+// c2 = 1.89 us).  Only the tensor-core two-chain transfer pass supports it; 0
+// elsewhere.
 int lead_fraction(const PrefillArgs &t) {
     if (t.Sg < 2 || !prefill_tc_supported(t) || !prefill_tc_two_chain(t)) return 0;
-    const double u = (double)t.N * t.H, P = (double)sm_count(), r = 1.57;
+    const double u = (double)t.N * t.H, P = (double)sm_count(), r = t.gate ? 1.38 : 1.57;
     if (u >= P) return 0;
     const double f = u * r / ((P - u) + u * r);
     return (int)(f * 65536.0);
