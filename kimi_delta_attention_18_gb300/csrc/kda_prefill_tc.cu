@@ -568,6 +568,13 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
                     *(uint32_t *)(d + (size_t)(j0 + 16 * m + g8 + 8 * hi) * D + 8 * n + 2 * t4) =
                         pack_bf16x2(S[m][n][2 * hi], S[m][n][2 * hi + 1]);
     };
+    // Checkpoints fall on the blocks whose end is a multiple of ckpt_interval tokens
+    // into the sequence (a multiple of 16; segments start on block boundaries):
+    // every ck_step-th block from ck_c on, the k-th of the sequence being ck_k.
+    const int ck_step = p.ckpt_interval > 0 ? p.ckpt_interval / C : 0;
+    const int blk0 = (x.t_begin - x.seq0) / C;
+    int ck_c = ck_step > 0 ? ck_step - 1 - blk0 % ck_step : -1;
+    int ck_k = ck_step > 0 ? (blk0 + ck_c + 1) / ck_step : 0;
     for (int c = 0; c < x.nchunks; ++c) {
         const int slot = c % NR;
         if (!warp_wait(x, B_REC_FULL + slot, (c / NR) & 1)) break;
@@ -801,11 +808,10 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
             const int done = min(x.t_begin + C * (c + 1), x.t_end) - x.seq0;
             if (done % (2 * C) == 0) store_chunk_state(x.cs_base + done / (2 * C) - 1);
         }
-        if (p.ckpt_interval > 0) {  // state checkpoint after this block
-            const int done = min(x.t_begin + C * (c + 1), x.t_end) - x.seq0;
+        if (c == ck_c) {  // state checkpoint after this block
             float *d = partA ? p.ckpt_a : p.ckpt;
-            if (done % p.ckpt_interval == 0 && d) {
-                d += ((size_t)(x.ckpt_base + done / p.ckpt_interval - 1) * p.H + x.h) * D * D;
+            if (x.t_begin + C * (c + 1) <= x.t_end && d) {
+                d += ((size_t)(x.ckpt_base + ck_k - 1) * p.H + x.h) * D * D;
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -815,6 +821,8 @@ __device__ __forceinline__ void chain_role(const Ctx &x) {
                             d[(size_t)(8 * n + 2 * t4 + (e & 1)) * D + j0 + 16 * m + g8 + 8 * (e >> 1)] =
                                 S[m][n][e];
             }
+            ck_c += ck_step;
+            ++ck_k;
         }
     }
     // Both chains of a two-chain CTA have consumed every record before either
