@@ -328,18 +328,21 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
             tma_load_2d(in_s + IN_G, x.tm_g, xc, t0, full);
         }
     };
-    // beta of rows g8 and g8 + 8 (for L) and of column lane (for T), zero past the
-    // block's end; loaded one block ahead
+    // beta (or with the fused prologue its pre-activation) of rows g8 and g8 + 8
+    // (for L) and of column lane (for T), loaded one block ahead; rows past the
+    // block's end read nothing
     auto load_beta = [&](int c, float &lo, float &hi, float &col) {
         const int t0 = first_token(c), nt = min(C, x.t_end - t0);
         const float *bp = p.beta + (size_t)t0 * p.H + x.h;
-        auto b = [&](int r) {  // beta, or sigmoid(x_beta) with the fused prologue
-            const float v = bp[(size_t)r * p.H];
-            return GATE ? __fdividef(1.f, 1.f + __expf(-v)) : v;
-        };
-        lo = g8 < nt ? b(g8) : 0.f;
-        hi = g8 + 8 < nt ? b(g8 + 8) : 0.f;
-        col = (lane & 15) < nt ? b(lane & 15) : 0.f;
+        lo = g8 < nt ? bp[(size_t)g8 * p.H] : 0.f;
+        hi = g8 + 8 < nt ? bp[(size_t)(g8 + 8) * p.H] : 0.f;
+        col = (lane & 15) < nt ? bp[(size_t)(lane & 15) * p.H] : 0.f;
+    };
+    // The sigmoid of the fused prologue is taken a block after the load, when the
+    // value is used, so that no instruction waits on the load in flight; rows past
+    // the block's end get beta = 0.
+    auto act = [&](float v, int r, int nt) {
+        return r < nt ? (GATE ? __fdividef(1.f, 1.f + __expf(-v)) : v) : 0.f;
     };
     int issued = 0;  // blocks whose copies were issued (for an orderly abort)
     float b_lo = 0.f, b_hi = 0.f, b_col = 0.f;
@@ -352,53 +355,67 @@ __device__ __forceinline__ void prep_role(const Ctx &x) {
     int uses = 0;  // completed uses of the input stage
     for (int c = pw; c < x.nchunks; c += N_PREP, ++uses) {
         const int slot = c % NR;
-        const float beta_lo = b_lo, beta_hi = b_hi, beta_col = b_col;
+        const int nt = min(C, x.t_end - first_token(c));
+        const float beta_lo = act(b_lo, g8, nt), beta_hi = act(b_hi, g8 + 8, nt),
+                    beta_col = act(b_col, lane & 15, nt);
         if (c + N_PREP < x.nchunks) load_beta(c + N_PREP, b_lo, b_hi, b_col);
         if (!warp_wait(x, B_REC_EMPTY + slot, ((c / NR) & 1) ^ 1)) break;
         if (!warp_wait(x, B_IN_FULL + st, uses & 1)) break;
         uint8_t *rec = x.smem + REC_OFF + slot * R_SIZE;
         const uint32_t rec_s = x.sbase + REC_OFF + slot * R_SIZE;
-        const int nt = min(C, x.t_end - first_token(c));
 
         // ---- fused prologue: inverse L2 norms of this block's k and q rows (a zero
-        // row keeps scale 0).  |k_r|^2 is the diagonal of K K^T, a 16 x 16 x 128
-        // product on the tensor cores (BF16 products are exact in fp32, fp32
-        // accumulation).  One ldmatrix per 16-channel step gives both operands: the
-        // A fragment of rows r is also the B fragment of columns r.  Each row reads its
-        // channels in its own rotated order (chunk + r), which leaves the diagonal
-        // unchanged and puts the eight rows of every 8 x 8 matrix on different banks
-        // of the dense 256-byte rows; the off-diagonal entries are not used.
+        // row keeps scale 0), in fp32 FMAs: lane (r, half) sums the squares of 64
+        // channels of row r = lane / 2, reading its 16-byte chunks in a rotated order
+        // so that the eight lanes of each quarter-warp hit eight different banks,
+        // then adds its partner's half.  The row scales reach every lane through the
+        // L scratch, which is free until L is formed below.  (The diagonal of K K^T
+        // on the tensor cores took several times longer per block: its 32 small
+        // products waited behind the chain warps' products on the same pipe.)
         float rk[C], rq[C];
         if (GATE) {
-            float accK[2][4] = {}, accQ[2][4] = {};
-            const int mi = lane >> 3, row = (lane & 7) + 8 * (mi & 1);
+            const int rr = lane >> 1, hf = lane & 1;
+            float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = row * IN_ROWB + 16 * ((2 * kk + (mi >> 1) + row) & 15);
-                uint32_t f[4];
-                ldsm_x4(in_s + IN_K + off, f);
-                mma_bf16_16816(accK[0], f, f[0], f[2]);
-                mma_bf16_16816(accK[1], f, f[1], f[3]);
+            for (int v = 0; v < 8; ++v) {
+                const int off = rr * IN_ROWB + hf * 128 + 16 * ((v + lane) & 7);
+                const uint4 wk = *(const uint4 *)(in + IN_K + off);
+                const uint32_t k4[4] = {wk.x, wk.y, wk.z, wk.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&k4[e]));
+                    fma2_acc(ak.x, ak.y, f.x, f.y, f.x, f.y);
+                }
                 if (WANT_Q) {
-                    uint32_t fq[4];
-                    ldsm_x4(in_s + IN_Q + off, fq);
-                    mma_bf16_16816(accQ[0], fq, fq[0], fq[2]);
-                    mma_bf16_16816(accQ[1], fq, fq[1], fq[3]);
+                    const uint4 wq = *(const uint4 *)(in + IN_Q + off);
+                    const uint32_t q4[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q4[e]));
+                        fma2_acc(aq.x, aq.y, f.x, f.y, f.x, f.y);
+                    }
                 }
             }
-            // diagonal entry (r, r) sits in lane 4 (r % 8) + (r % 8) / 2: element r % 2
-            // of the first column tile for r < 8, element 2 + r % 2 of the second
+            float sk = ak.x + ak.y, sq = aq.x + aq.y;
+            sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+            if (hf == 0) {
+                Lf[rr] = sk > 0.f ? rsqrtf(sk) : 0.f;
+                Lf[C + rr] = sq > 0.f ? rsqrtf(sq) : 0.f;
+            }
+            __syncwarp();
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                const int src = 4 * (r & 7) + ((r & 7) >> 1);
-                const float sk = __shfl_sync(0xffffffffu, r < 8 ? accK[0][r & 1] : accK[1][2 + (r & 1)], src);
-                rk[r] = sk > 0.f ? rsqrtf(sk) : 0.f;
-                if (WANT_Q) {
-                    const float sq = __shfl_sync(0xffffffffu, r < 8 ? accQ[0][r & 1] : accQ[1][2 + (r & 1)], src);
-                    rq[r] = sq > 0.f ? rsqrtf(sq) : 0.f;
-                } else {
-                    rq[r] = 0.f;
-                }
+            for (int r4 = 0; r4 < C / 4; ++r4) {
+                const float4 a4 = *(const float4 *)(Lf + 4 * r4);
+                const float4 b4 = *(const float4 *)(Lf + C + 4 * r4);
+                rk[4 * r4] = a4.x;
+                rk[4 * r4 + 1] = a4.y;
+                rk[4 * r4 + 2] = a4.z;
+                rk[4 * r4 + 3] = a4.w;
+                rq[4 * r4] = WANT_Q ? b4.x : 0.f;
+                rq[4 * r4 + 1] = WANT_Q ? b4.y : 0.f;
+                rq[4 * r4 + 2] = WANT_Q ? b4.z : 0.f;
+                rq[4 * r4 + 3] = WANT_Q ? b4.w : 0.f;
             }
         }
 
