@@ -49,16 +49,23 @@ constexpr int T_R = T_KB + 4096;          // [16 r][128 j]
 constexpr int T_U = T_R + 4096;
 constexpr int T_DU = T_U + 4096;
 constexpr int T_NDR = T_DU + 4096;        // -dR
+// Row strides of the token-by-channel arrays that are read element-wise: BS BF16
+// elements (272-byte rows) and FS floats (544-byte rows).  Lanes of a fragment read
+// 8 rows at once; with dense rows those share banks (8-way conflicts), with 68- or
+// 136-word rows their 4- and 8-byte reads fall on distinct banks.
+constexpr int BS = 136, FS = 136;
 // Input buffers, two, alternating between consecutive blocks of a CTA: raw q, k, v
-// rows [16][128] BF16 (dense), dO [16][128 j] BF16 (swizzled), g [16][128] fp32
-// (then e^{Gamma}), beta [16]
-constexpr int IB_Q = 0, IB_K = 4096, IB_V = 8192, IB_DO = 12288, IB_G = 16384, IB_BETA = 24576;
+// rows [16][BS] BF16, dO [16][128 j] BF16 (swizzled), g [16][FS] fp32 (then
+// e^{Gamma}), beta [16]
+constexpr int IB_Q = 0, IB_K = IB_Q + C * BS * 2, IB_V = IB_K + C * BS * 2;
+constexpr int IB_DO = IB_V + C * BS * 2, IB_G = IB_DO + 4096, IB_BETA = IB_G + C * FS * 4;
 constexpr int IB_SIZE = IB_BETA + 128;
+static_assert(IB_DO % 128 == 0 && IB_G % 128 == 0 && IB_SIZE % 128 == 0, "input buffer alignment");
 constexpr int IB0 = T_NDR + 4096;
-constexpr int F_EM = IB0 + 2 * IB_SIZE;   // e^{-Gamma}
-constexpr int F_EB = F_EM + 8192;         // e^{Gamma_C - Gamma}
-constexpr int F_DGAM = F_EB + 8192;       // dGamma [16][128] fp32
-constexpr int F_PART = F_DGAM + 8192;     // partial 16 x 16 products [GW][2][16][16] fp32
+constexpr int F_EM = IB0 + 2 * IB_SIZE;   // e^{-Gamma} [16][FS]
+constexpr int F_EB = F_EM + C * FS * 4;   // e^{Gamma_C - Gamma} [16][FS]
+constexpr int F_DGAM = F_EB + C * FS * 4; // dGamma [16][FS] fp32
+constexpr int F_PART = F_DGAM + C * FS * 4;  // partial 16 x 16 products [GW][2][16][16] fp32
 constexpr int SQ = 17;                    // fp32 16 x 16 row stride
 constexpr int F_SMALL = F_PART + GW * 2 * 256 * 4;   // fp32 16 x 16: L, Mq, Y, dT, dMq, P
 enum { SM_L = 0, SM_MQ, SM_Y, SM_DT, SM_DMQ, SM_P, SM_DMB, NSMALL };
@@ -155,12 +162,12 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             const __nv_bfloat16 *src = arr == 0 ? a.q : arr == 1 ? a.k : arr == 2 ? a.v : a.dout;
             const uint32_t dst = arr == 3 ? sb + ibo + IB_DO + sw(r, cc)
                                           : sb + ibo + (arr == 0 ? IB_Q : arr == 1 ? IB_K : IB_V) +
-                                                r * 256 + 16 * cc;
+                                                r * (BS * 2) + 16 * cc;
             cp_async16(dst, src + base + (r < w.nt ? r : 0) * row_stride + 8 * cc, r < w.nt);
         }
         for (int e = tid; e < C * 32; e += GT) {  // g: 16 rows x 32 float4
             const int r = e >> 5, c4 = e & 31;
-            cp_async16(sb + ibo + IB_G + r * 512 + 16 * c4,
+            cp_async16(sb + ibo + IB_G + r * (FS * 4) + 16 * c4,
                        a.g + base + (r < w.nt ? r : 0) * row_stride + 4 * c4, r < w.nt);
         }
         if (tid < C)
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
         const bool fwd_half = tid < D;
         float al[C];
 #pragma unroll
-        for (int r = 0; r < C; ++r) al[r] = __expf(fG[r * D + i]);
+        for (int r = 0; r < C; ++r) al[r] = __expf(fG[r * FS + i]);
         const __nv_bfloat16 *kr = (const __nv_bfloat16 *)(sm + ibo + IB_K);
         const __nv_bfloat16 *qr = (const __nv_bfloat16 *)(sm + ibo + IB_Q);
         __syncthreads();  // every thread has read g before fG is overwritten
@@ -232,8 +239,8 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
 #pragma unroll
             for (int r = 0; r < C; ++r) {
                 run *= al[r];
-                const float kv = __bfloat162float(kr[r * D + i]), qv = __bfloat162float(qr[r * D + i]);
-                fG[r * D + i] = run;  // g is no longer needed: keep e^{Gamma}
+                const float kv = __bfloat162float(kr[r * BS + i]), qv = __bfloat162float(qr[r * BS + i]);
+                fG[r * FS + i] = run;  // g is no longer needed: keep e^{Gamma}
                 const uint32_t off = sw(r, i >> 3) + 2 * (i & 7);
                 *(__nv_bfloat16 *)(sm + T_KH + off) = __float2bfloat16_rn(kv * run);
                 *(__nv_bfloat16 *)(sm + T_QH + off) = __float2bfloat16_rn(qv * run);
@@ -247,10 +254,10 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             eC[i] = b;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float kv = __bfloat162float(kr[r * D + i]);
+                const float kv = __bfloat162float(kr[r * BS + i]);
                 const float em = rev[r] * einv;
-                fEm[r * D + i] = em;
-                fEb[r * D + i] = rev[r];
+                fEm[r * FS + i] = em;
+                fEb[r * FS + i] = rev[r];
                 const uint32_t off = sw(r, i >> 3) + 2 * (i & 7);
                 *(__nv_bfloat16 *)(sm + T_KT + off) = __float2bfloat16_rn(kv * em);
                 *(__nv_bfloat16 *)(sm + T_KB + off) = __float2bfloat16_rn(kv * rev[r]);
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int r = g8 + 8 * hh, j = j0 + 8 * nb + 2 * t4;
-            const float2 v2 = __bfloat1622float2(*(const __nv_bfloat162 *)(vr + r * D + j));
+            const float2 v2 = __bfloat1622float2(*(const __nv_bfloat162 *)(vr + r * BS + j));
             Rf[nb][2 * hh] = v2.x - Rf[nb][2 * hh];
             Rf[nb][2 * hh + 1] = v2.y - Rf[nb][2 * hh + 1];
             const uint32_t off = sw(r, j >> 3) + 2 * (j & 7);
@@ -542,20 +549,27 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int r = g8 + 8 * hh, i = i0 + 8 * nb + 2 * t4;
-            float dk2[2], dq2[2];
+            // channels i, i + 1 of row r: one 8-byte read per fp32 array, one 4-byte
+            // read per BF16 row
+            const float2 ep2 = *(const float2 *)(fG + r * FS + i);
+            const float2 em2 = *(const float2 *)(fEm + r * FS + i);
+            const float2 eb2 = *(const float2 *)(fEb + r * FS + i);
+            const float2 kv2 = __bfloat1622float2(*(const __nv_bfloat162 *)(kraw + r * BS + i));
+            const float2 qv2 = __bfloat1622float2(*(const __nv_bfloat162 *)(qraw + r * BS + i));
+            float dk2[2], dq2[2], dg2[2], kb2[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int q4 = 2 * hh + e, ii = i + e;
-                const float ep = fG[r * D + ii], em = fEm[r * D + ii], eb = fEb[r * D + ii];
-                const float kv = __bfloat162float(kraw[r * D + ii]);
-                const float qv = __bfloat162float(qraw[r * D + ii]);
+                const int q4 = 2 * hh + e;
+                const float ep = e ? ep2.y : ep2.x, em = e ? em2.y : em2.x, eb = e ? eb2.y : eb2.x;
+                const float kv = e ? kv2.y : kv2.x, qv = e ? qv2.y : qv2.x;
                 dk2[e] = dKh[nb][q4] * ep + dKt[nb][q4] * em + dKb[nb][q4] * eb;
                 dq2[e] = dQh[nb][q4] * ep;
-                const float kbt = dKb[nb][q4] * kv * eb;
-                dgam[r * D + ii] = dKh[nb][q4] * kv * ep - dKt[nb][q4] * kv * em +
-                                   dQh[nb][q4] * qv * ep - kbt;
-                kbk[r * D + ii] = kbt;
+                kb2[e] = dKb[nb][q4] * kv * eb;
+                dg2[e] = dKh[nb][q4] * kv * ep - dKt[nb][q4] * kv * em + dQh[nb][q4] * qv * ep -
+                         kb2[e];
             }
+            *(float2 *)(dgam + r * FS + i) = make_float2(dg2[0], dg2[1]);
+            *(float2 *)(kbk + r * FS + i) = make_float2(kb2[0], kb2[1]);
             if (r < nt) {
                 const size_t o = ((size_t)(t0 + r) * a.H + h) * D + i;
                 *(float2 *)(a.dk + o) = make_float2(dk2[0], dk2[1]);
@@ -609,11 +623,11 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
         const int i = tid;
         float acc = deC[i] * eC[i];
 #pragma unroll
-        for (int r = 0; r < C; ++r) acc += kbk[r * D + i];
+        for (int r = 0; r < C; ++r) acc += kbk[r * FS + i];
         float out[C];
 #pragma unroll
         for (int r = C - 1; r >= 0; --r) {
-            acc += dgam[r * D + i];
+            acc += dgam[r * FS + i];
             out[r] = acc;
         }
 #pragma unroll

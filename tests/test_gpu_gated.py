@@ -59,3 +59,24 @@ def test_gated_zero_rows_stay_finite():
     o_ref, S_ref = oracle.kda_forward(qn, kn, _np(x["v"]), g, beta, None,
                                       x["cu_seqlens"].cpu().numpy())
     assert rel_err(_np(out), o_ref) <= 2e-2 and rel_err(_np(SF), S_ref) <= 2e-2
+
+
+def test_gated_lead_path_with_zero_rows():
+    # 8 chains x 20 segments: the two-chain transfer pass with a lead segment, whose
+    # CTAs take the norms and the gate from their helper warps; zero rows inside
+    # and outside the lead, and a ragged tail
+    x = make_prefill_inputs([1000, 37], 4, 128, 128, "bf16", s0_std=1.0, seed=33, slow_decay=True)
+    x = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    q = x["q_raw"].clone()
+    k = x["k_raw"].clone()
+    q[5].zero_()
+    k[9].zero_()
+    k[700, 2].zero_()
+    out, SF = kda.prefill_chunked_gated(q, k, x["v"], x["x_g"], x["x_beta"], x["S0"],
+                                        x["cu_seqlens"], num_segments=20)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(SF).all()
+    qn, kn, g, beta = oracle.gate_prologue(_np(q), _np(k), _np(x["x_g"]), _np(x["x_beta"]))
+    o_ref, S_ref = oracle.kda_forward(qn, kn, _np(x["v"]), g, beta, _np(x["S0"]),
+                                      x["cu_seqlens"].cpu().numpy())
+    assert rel_err(_np(out), o_ref) <= 2e-2 and rel_err(_np(SF), S_ref) <= 2e-2
