@@ -55,14 +55,14 @@ constexpr int T_NDR = T_DU + 4096;        // -dR
 // 136-word rows their 4- and 8-byte reads fall on distinct banks.
 constexpr int BS = 136, FS = 136;
 // Input buffers, two, alternating between consecutive blocks of a CTA: raw q, k, v
-// rows [16][BS] BF16, dO [16][128 j] BF16 (swizzled), g [16][FS] fp32 (then
-// e^{Gamma}), beta [16]
+// rows [16][BS] BF16, dO [16][128 j] BF16 (swizzled), g [16][FS] fp32, beta [16]
 constexpr int IB_Q = 0, IB_K = IB_Q + C * BS * 2, IB_V = IB_K + C * BS * 2;
 constexpr int IB_DO = IB_V + C * BS * 2, IB_G = IB_DO + 4096, IB_BETA = IB_G + C * FS * 4;
 constexpr int IB_SIZE = IB_BETA + 128;
 static_assert(IB_DO % 128 == 0 && IB_G % 128 == 0 && IB_SIZE % 128 == 0, "input buffer alignment");
 constexpr int IB0 = T_NDR + 4096;
-constexpr int F_EM = IB0 + 2 * IB_SIZE;   // e^{-Gamma} [16][FS]
+constexpr int F_EP = IB0 + 2 * IB_SIZE;   // e^{Gamma} [16][FS]
+constexpr int F_EM = F_EP + C * FS * 4;   // e^{-Gamma} [16][FS]
 constexpr int F_EB = F_EM + C * FS * 4;   // e^{Gamma_C - Gamma} [16][FS]
 constexpr int F_DGAM = F_EB + C * FS * 4; // dGamma [16][FS] fp32
 constexpr int F_PART = F_DGAM + C * FS * 4;  // partial 16 x 16 products [GW][2][16][16] fp32
@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
     cp_async_wait_group<2>();  // this block's inputs
     __syncthreads();
 
-    float *fG = (float *)(sm + ibo + IB_G), *fEm = (float *)(sm + F_EM), *fEb = (float *)(sm + F_EB);
+    const float *fG = (const float *)(sm + ibo + IB_G);
+    float *fEp = (float *)(sm + F_EP), *fEm = (float *)(sm + F_EM), *fEb = (float *)(sm + F_EB);
     float *beta = (float *)(sm + ibo + IB_BETA), *eC = (float *)(sm + F_VEC), *deC = eC + 128;
     auto small = [&](int which) { return (float *)(sm + F_SMALL) + which * 16 * SQ; };
     auto sbf = [&](int which) { return (__nv_bfloat16 *)(sm + B_SMALL) + which * 16 * TS; };
@@ -233,14 +234,13 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
         for (int r = 0; r < C; ++r) al[r] = __expf(fG[r * FS + i]);
         const __nv_bfloat16 *kr = (const __nv_bfloat16 *)(sm + ibo + IB_K);
         const __nv_bfloat16 *qr = (const __nv_bfloat16 *)(sm + ibo + IB_Q);
-        __syncthreads();  // every thread has read g before fG is overwritten
         if (fwd_half) {
             float run = 1.f;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
                 run *= al[r];
                 const float kv = __bfloat162float(kr[r * BS + i]), qv = __bfloat162float(qr[r * BS + i]);
-                fG[r * FS + i] = run;  // g is no longer needed: keep e^{Gamma}
+                fEp[r * FS + i] = run;
                 const uint32_t off = sw(r, i >> 3) + 2 * (i & 7);
                 *(__nv_bfloat16 *)(sm + T_KH + off) = __float2bfloat16_rn(kv * run);
                 *(__nv_bfloat16 *)(sm + T_QH + off) = __float2bfloat16_rn(qv * run);
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
             const int r = g8 + 8 * hh, i = i0 + 8 * nb + 2 * t4;
             // channels i, i + 1 of row r: one 8-byte read per fp32 array, one 4-byte
             // read per BF16 row
-            const float2 ep2 = *(const float2 *)(fG + r * FS + i);
+            const float2 ep2 = *(const float2 *)(fEp + r * FS + i);
             const float2 em2 = *(const float2 *)(fEm + r * FS + i);
             const float2 eb2 = *(const float2 *)(fEb + r * FS + i);
             const float2 kv2 = __bfloat1622float2(*(const __nv_bfloat162 *)(kraw + r * BS + i));
