@@ -309,46 +309,50 @@ __global__ void __launch_bounds__(GT, 1) bwd_chunk_kernel(const __grid_constant_
         return s;
     };
 
-    // ---- L = strict_lower(Kh Kt^T), Mq = lower(Qh Kt^T): warp w takes channels 16 w..
-    {
+    // ---- L = strict_lower(Kh Kt^T), Mq = lower(Qh Kt^T) (16 x 16 x 128) and Y = (I +
+    // Diag(beta) L)^{-1}, all in warp 0: the full products take it a few hundred
+    // cycles, less than partial products summed across the warps behind a barrier
+    if (warp == 0) {
         float accL[2][4] = {}, accM[2][4] = {};
-        uint32_t af[4], aq[4], bf[4];
-        lda(T_KH, warp, af);
-        lda(T_QH, warp, aq);
-        ldb_nt(T_KT, 0, 2 * warp, bf);  // B[k = i][n = r'] = Kt[r'][i]
-        mma_bf16_16816(accL[0], af, bf[0], bf[1]);
-        mma_bf16_16816(accL[1], af, bf[2], bf[3]);
-        mma_bf16_16816(accM[0], aq, bf[0], bf[1]);
-        mma_bf16_16816(accM[1], aq, bf[2], bf[3]);
-        put_part(0, accL);
-        put_part(1, accM);
-    }
-    __syncthreads();
-    {
-        const int r = tid >> 4, cc = tid & 15;  // 256 threads = 16 x 16 entries
-        const float l = cc < r ? sum_parts(0, r, cc) : 0.f;
-        const float mq = cc <= r ? sum_parts(1, r, cc) : 0.f;
-        small(SM_L)[r * SQ + cc] = l;
-        small(SM_MQ)[r * SQ + cc] = mq;
-        sbf(SB_MQ)[r * TS + cc] = __float2bfloat16_rn(mq);
-    }
-    __syncthreads();
-    // ---- Y = (I + Diag(beta) L)^{-1}: forward substitution, thread = column (fp32)
-    if (tid < C) {
-        const int j = tid;
-        const float *L = small(SM_L);
-        float y[C];
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            float s = r == j ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < r; ++m) s -= beta[r] * L[r * SQ + m] * y[m];
-            y[r] = r < j ? 0.f : s;
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t af[4], aq[4], bf[4];
+            lda(T_KH, kk, af);
+            lda(T_QH, kk, aq);
+            ldb_nt(T_KT, 0, 2 * kk, bf);  // B[k = i][n = r'] = Kt[r'][i]
+            mma_bf16_16816(accL[0], af, bf[0], bf[1]);
+            mma_bf16_16816(accL[1], af, bf[2], bf[3]);
+            mma_bf16_16816(accM[0], aq, bf[0], bf[1]);
+            mma_bf16_16816(accM[1], aq, bf[2], bf[3]);
         }
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            small(SM_Y)[r * SQ + j] = y[r];
-            sbf(SB_T)[r * TS + j] = __float2bfloat16_rn(y[r] * beta[j]);  // T = Y Diag(beta)
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = g8 + 8 * (e >> 1), cc = nb * 8 + 2 * t4 + (e & 1);
+                const float mq = cc <= r ? accM[nb][e] : 0.f;
+                small(SM_L)[r * SQ + cc] = cc < r ? accL[nb][e] : 0.f;
+                small(SM_MQ)[r * SQ + cc] = mq;
+                sbf(SB_MQ)[r * TS + cc] = __float2bfloat16_rn(mq);
+            }
+        __syncwarp();
+        // forward substitution, lane = column (fp32)
+        if (lane < C) {
+            const int j = lane;
+            const float *L = small(SM_L);
+            float y[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                float s = r == j ? 1.f : 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) s -= beta[r] * L[r * SQ + m] * y[m];
+                y[r] = r < j ? 0.f : s;
+            }
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                small(SM_Y)[r * SQ + j] = y[r];
+                sbf(SB_T)[r * TS + j] = __float2bfloat16_rn(y[r] * beta[j]);  // T = Y Diag(beta)
+            }
         }
     }
     cp_async_wait_group<1>();  // this block's S^T and dS'^T
