@@ -52,8 +52,8 @@ ONE_PASS_B = 4 * 256 + 512 + 4
 KCP_B = (2 * 256 + 512 + 4) + ONE_PASS_B
 CKPT_INTERVAL = 4096
 PROFILE_CASES = ("decode", "prefill_output_pass", "prefill_h8_t4096", "prefill_kcp_h56_t64k",
-                 "prefill_kcp_h56_t16k", "prefill_ckpt_h8_t4096", "backward_h8_t1024",
-                 "backward_h8_t4096")
+                 "prefill_kcp_h56_t16k", "prefill_gated_kcp_h56_t16k", "prefill_ckpt_h8_t4096",
+                 "backward_h8_t1024", "backward_h8_t4096")
 # the ncu summary that gives the transfer pass's DRAM traffic per launch, and the
 # kernel source it was taken on
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "prefill_tc_kernel_kcp_h56_t64k_d128.md")
@@ -837,6 +837,12 @@ def run_profile_case(name):
         for _ in range(2):
             kda.prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
                                 x["cu_seqlens"], num_segments=4)
+    elif name == "prefill_gated_kcp_h56_t16k":
+        # the same workload from the gate pre-activations (the fused prologue)
+        x = make_prefill_inputs([16384], 56, 128, 128, "bf16", device=dev)
+        for _ in range(2):
+            kda.prefill_chunked_gated(x["q_raw"], x["k_raw"], x["v"], x["x_g"], x["x_beta"],
+                                      None, x["cu_seqlens"], num_segments=4)
     elif name == "prefill_h8_t4096":
         x = make_prefill_inputs([4096], 8, 128, 128, "bf16", device=dev)
         for _ in range(2):
