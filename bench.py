@@ -110,6 +110,18 @@ def barrier(dist):
         dist.barrier()
 
 
+def host_available_bytes():
+    """MemAvailable of this machine (Linux /proc/meminfo), or None if unknown."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        return None
+    return None
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
@@ -555,12 +567,26 @@ def run_e2e(args, kda, x, Sg, out, SF, ws, dev, dist, world):
     call."""
     import torch
     names = ("q", "k", "v", "g", "beta")
+    # Every rank on this node pins its inputs and outputs; all ranks take the leg or
+    # none does (a rank that left it early would leave the others at its barrier).
+    need = sum(x[n].numel() * x[n].element_size() for n in names) + \
+        out.numel() * out.element_size() + SF.numel() * SF.element_size()
+    local = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    avail = host_available_bytes()
+    fits = avail is None or need * local <= 0.8 * avail
+    if max_over_ranks(0.0 if fits else 1.0, dist, dev) > 0:
+        return {"value": None, "unavailable": "host memory: %d ranks x %.1f GB pinned against "
+                "%.1f GB available" % (local, need / 1e9, (avail or 0) / 1e9)}
     try:
         host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
         out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         sf_h = torch.empty(SF.shape, dtype=SF.dtype, pin_memory=True)
+        pinned = True
     except RuntimeError as e:  # not enough pinnable host memory on this machine
-        return {"value": None, "unavailable": "pinned host buffers: %s" % str(e)[:120]}
+        pinned, why = False, str(e)[:120]
+    if max_over_ranks(0.0 if pinned else 1.0, dist, dev) > 0:
+        return {"value": None, "unavailable": "pinned host buffers: %s" % (
+            why if not pinned else "another rank could not pin its buffers")}
     for n in names:
         host[n].copy_(x[n])
     T = x["q"].shape[0]
